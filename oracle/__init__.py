@@ -1,0 +1,303 @@
+"""CPU oracle of the Lynx split-stream KV codec and of decode attention.
+
+TEST INFRASTRUCTURE ONLY.  The product library (``split_stream_kv_gb300``)
+never imports this package; only ``tests/``, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline leg do.  The arithmetic lives in the plain C file
+``lynx_oracle.c`` (compiled with ``-ffp-contract=off -fno-fast-math``); this
+module builds it, loads it with ctypes and wraps it for numpy arrays.  A few
+closed-form size formulas from the pages are written here in Python.
+
+Sources, cited by page title and section:
+  [Review] "Lynx: Progressive Speculative KV Cache Transfer for Disaggregated
+           LLM Inference" (technical review of the paper).
+  [Digest] "Lynx: Progressive Speculative Quantization for accelerating KV
+           Transfer in Long-Context Inference" (paper digest).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lynx_oracle.c")
+_LIB = os.path.join(_HERE, "liblynx_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+EPS = 1e-6  # the pages leave eps open; float32 1e-6 on both sides
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-Wall", "-Wextra", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        lib.oracle_compand_y.argtypes = [F, F]
+        lib.oracle_compand_y.restype = ctypes.c_double
+        lib.oracle_round_code.argtypes = [F, F]
+        lib.oracle_round_code.restype = I
+        lib.oracle_expand.argtypes = [I, F]
+        lib.oracle_expand.restype = F
+        lib.oracle_stage4_literal.argtypes = [I, I, P]
+        lib.oracle_stage4_literal.restype = None
+        lib.oracle_code8.argtypes = [I, I]
+        lib.oracle_code8.restype = I
+        lib.oracle_anchor_nibble.argtypes = [I]
+        lib.oracle_anchor_nibble.restype = I
+        lib.oracle_residual_nibble.argtypes = [I]
+        lib.oracle_residual_nibble.restype = I
+        lib.oracle_f32_to_bf16.argtypes = [F]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_encode_block.argtypes = [P, I64, I, I, I, F, P, P, P]
+        lib.oracle_encode_block.restype = I
+        lib.oracle_encode_range.argtypes = [P, I64, I64, I, I, I, I, F, P, P, P,
+                                            I64, I64]
+        lib.oracle_encode_range.restype = I
+        lib.oracle_decode_block.argtypes = [P, P, P, I, I, I, F, P, I64]
+        lib.oracle_decode_block.restype = I
+        lib.oracle_decode_range.argtypes = [P, P, P, I64, I64, I, I, I, I, F, P,
+                                            I64, I64]
+        lib.oracle_decode_range.restype = I
+        lib.oracle_attention_row.argtypes = [P, P, P, I64, I, I64, P]
+        lib.oracle_attention_row.restype = None
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+# ------------------------------------------------------------ scalar pieces
+
+def compand_y(a: float, alpha: float) -> float:
+    """Eq. 7 value Y in float64 from float32 |X_final| [Review, Stage 3]."""
+    return _load().oracle_compand_y(a, alpha)
+
+
+def round_code(a: float, alpha: float) -> int:
+    """I = Round(Y) in 0..127 [Review, Stage 3]."""
+    return _load().oracle_round_code(a, alpha)
+
+
+def expand(I: int, alpha: float) -> float:
+    """float32(((1+alpha)^(I/127) - 1)/alpha) [Review, Eq. 14/15]."""
+    return _load().oracle_expand(I, alpha)
+
+
+def expand_table(alpha: float) -> np.ndarray:
+    return np.array([expand(i, alpha) for i in range(128)], dtype=np.float32)
+
+
+def stage4_literal(I: int, S: int) -> dict:
+    """Stage 4 exactly as printed: I_bias, V_mag, V_recon, V_res, Q_anc
+    [Review, Stage 4, Eq. 9]."""
+    out = (ctypes.c_int * 5)()
+    _load().oracle_stage4_literal(I, S, ctypes.cast(out, ctypes.c_void_p))
+    return dict(I_bias=out[0], V_mag=out[1], V_recon=out[2], V_res=out[3],
+                Q_anc=out[4])
+
+
+def code8(I: int, S: int) -> int:
+    """Eq. 9 on the full magnitude, as an 8-bit two's-complement pattern."""
+    return _load().oracle_code8(I, S)
+
+
+def anchor_nibble(c8: int) -> int:
+    return _load().oracle_anchor_nibble(c8)
+
+
+def residual_nibble(c8: int) -> int:
+    return _load().oracle_residual_nibble(c8)
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even float32 -> bf16 bit patterns (uint16)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(h, dtype=np.uint16).astype(np.uint32)
+            << 16).view(np.float32)
+
+
+# ------------------------------------------------------------ codec
+
+def meta_rows(P: int, C: int) -> int:
+    """2 + 2P/C float32 rows of D per page block [Review, Stage 1 and 2]."""
+    return 2 + 2 * (P // C)
+
+
+def encode_block(x_bits: np.ndarray, C: int, alpha: float):
+    """Algorithm 1 on one block x_bits[P][D] (uint16 BF16 bits)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    P, D = x.shape
+    anc = np.zeros((P, D // 2), np.uint8)
+    res = np.zeros((P, D // 2), np.uint8)
+    meta = np.zeros((meta_rows(P, C), D), np.float32)
+    rc = _load().oracle_encode_block(_ptr(x), D, P, D, C, alpha, _ptr(anc),
+                                     _ptr(res), _ptr(meta))
+    if rc:
+        raise ValueError("oracle_encode_block: bad arguments")
+    return anc, res, meta
+
+
+def _split(n: int, parts: int):
+    parts = max(1, min(parts, n))
+    step = (n + parts - 1) // parts
+    return [(i, min(n, i + step)) for i in range(0, n, step)]
+
+
+def encode(kv_bits: np.ndarray, P: int, C: int, alpha: float,
+           threads: int = 1, block_range=None):
+    """Encode kv_bits[B][L][H][D] (uint16 BF16 bits).  Returns
+    (anchor[B][NB][H][P][D/2], residual, meta[B][NB][H][2+2P/C][D])."""
+    kv = np.ascontiguousarray(kv_bits, dtype=np.uint16)
+    B, L, H, D = kv.shape
+    NB = L // P
+    anc = np.zeros((B, NB, H, P, D // 2), np.uint8)
+    res = np.zeros_like(anc)
+    meta = np.zeros((B, NB, H, meta_rows(P, C), D), np.float32)
+    lo, hi = block_range if block_range is not None else (0, B * NB * H)
+    lib = _load()
+
+    def run(rng):
+        rc = lib.oracle_encode_range(_ptr(kv), B, L, H, D, P, C, alpha,
+                                     _ptr(anc), _ptr(res), _ptr(meta),
+                                     rng[0], rng[1])
+        if rc:
+            raise ValueError("oracle_encode_range: bad arguments")
+
+    chunks = [(a + lo, b + lo) for a, b in _split(hi - lo, threads)]
+    if threads <= 1 or len(chunks) == 1:
+        for c in chunks:
+            run(c)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, chunks))
+    return anc, res, meta
+
+
+def decode_block(anc: np.ndarray, res, meta: np.ndarray, C: int,
+                 alpha: float) -> np.ndarray:
+    """Decode one block; res=None gives the Anchor-only reconstruction."""
+    anc = np.ascontiguousarray(anc, dtype=np.uint8)
+    P = anc.shape[0]
+    D = anc.shape[1] * 2
+    meta = np.ascontiguousarray(meta, dtype=np.float32)
+    out = np.zeros((P, D), np.float32)
+    rp = None
+    if res is not None:
+        res = np.ascontiguousarray(res, dtype=np.uint8)
+        rp = _ptr(res)
+    rc = _load().oracle_decode_block(_ptr(anc), rp, _ptr(meta), P, D, C, alpha,
+                                     _ptr(out), D)
+    if rc:
+        raise ValueError("oracle_decode_block: bad arguments")
+    return out
+
+
+def decode(anc: np.ndarray, res, meta: np.ndarray, L: int, P: int, C: int,
+           alpha: float, threads: int = 1, block_range=None) -> np.ndarray:
+    """Decode streams laid out as encode() returns them to float32
+    [B][L][H][D]; res=None gives the Anchor-only reconstruction."""
+    anc = np.ascontiguousarray(anc, dtype=np.uint8)
+    B, NB, H, _, half = anc.shape
+    D = half * 2
+    meta = np.ascontiguousarray(meta, dtype=np.float32)
+    out = np.zeros((B, L, H, D), np.float32)
+    rp = None
+    if res is not None:
+        res = np.ascontiguousarray(res, dtype=np.uint8)
+        rp = _ptr(res)
+    lib = _load()
+    lo, hi = block_range if block_range is not None else (0, B * NB * H)
+
+    def run(rng):
+        rc = lib.oracle_decode_range(_ptr(anc), rp, _ptr(meta), B, L, H, D, P,
+                                     C, alpha, _ptr(out), rng[0], rng[1])
+        if rc:
+            raise ValueError("oracle_decode_range: bad arguments")
+
+    chunks = [(a + lo, b + lo) for a, b in _split(hi - lo, threads)]
+    if threads <= 1 or len(chunks) == 1:
+        for c in chunks:
+            run(c)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, chunks))
+    return out
+
+
+# ------------------------------------------------------------ attention
+
+def attention_row(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """float64 softmax(q K^T / sqrt(D)) V for one query row [Review, Eq. 1].
+    q[D], K[L][D], V[L][D] as float32 (the values the attention sees)."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    L, D = K.shape
+    out = np.zeros(D, np.float64)
+    _load().oracle_attention_row(_ptr(q), _ptr(K), _ptr(V), L, D, D, _ptr(out))
+    return out
+
+
+# ------------------------------------------------------------ size formulas
+
+def kv_size_bytes(k_factor: int, L: int, D: int, n_layers: int,
+                  precision_bytes: int) -> int:
+    """Size_KV = K_factor * L * D * N_layers * Precision, D = H_heads*D_head
+    [Review, Prerequisites, Eq. 2]."""
+    return k_factor * L * D * n_layers * precision_bytes
+
+
+def metadata_scalars(H: int, P: int, C: int) -> int:
+    """H * (2 + 2P/C) scalars per page block [Review, "Why Not Global Grouped
+    Quantization?"]."""
+    return H * (2 + 2 * (P // C))
+
+
+def effective_bins(B: int, ratio_local_to_global: float) -> float:
+    """Bins_eff ~ 2^B * m_i / m [Review, Prerequisites, Eq. 5]."""
+    return (2 ** B) * ratio_local_to_global
+
+
+def anchor_ratio(alpha: float) -> float:
+    """Ratio of consecutive Anchor buckets (1+alpha)^(16/127): the geometric
+    interval of the Anchor ("effective exponentiation (1+alpha)^q_anc",
+    [Digest, Method])."""
+    return (1.0 + alpha) ** (16.0 / 127.0)
+
+
+__all__ = [
+    "EPS", "build", "compand_y", "round_code", "expand", "expand_table",
+    "stage4_literal", "code8", "anchor_nibble", "residual_nibble",
+    "f32_to_bf16_bits", "bf16_bits_to_f32", "meta_rows", "encode_block",
+    "encode", "decode_block", "decode", "attention_row", "kv_size_bytes",
+    "metadata_scalars", "effective_bins", "anchor_ratio",
+]

@@ -1,0 +1,372 @@
+/*
+ * lynx_oracle.c -- plain, slow CPU oracle of the Lynx split-stream KV codec
+ * and of decode attention over the reconstructed KV.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, calls or
+ * includes this file; only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg load it.  It shares no source, header, table or constant
+ * generator with the CUDA library.
+ *
+ * Sources (web pages about one paper; cited by title and section):
+ *   [Review] "Lynx: Progressive Speculative KV Cache Transfer for
+ *            Disaggregated LLM Inference" (technical review of the paper),
+ *            sections "Mechanism 1: Hierarchical Non-Linear Quantization
+ *            (Algorithm 1)" Stages 1-4 with Eq. 7-9, "Mechanism 2" (decode
+ *            side, Anchor and Residual phases), "Worked Example" Eq. 12-15,
+ *            "Implementation Notes", "Appendix A.1", and "Prerequisites" Eq. 1.
+ *   [Digest] "Lynx: Progressive Speculative Quantization for accelerating KV
+ *            Transfer in Long-Context Inference" (paper digest), "Method".
+ *
+ * Arithmetic conventions (compiled with -ffp-contract=off -fno-fast-math):
+ *   - Stage 1 and 2 statistics are IEEE binary32, one rounding per operation,
+ *     in the order written below.  The pages store the metadata as float32
+ *     ([Review], "Why Not Global Grouped Quantization?": "9 KB metadata per
+ *     page in float32"), and a code is an integer decided from these values,
+ *     so both this oracle and the GPU take that decision from the same
+ *     float32 statistics.
+ *   - The alpha-law value Y (Eq. 7) is evaluated in float64 from the float32
+ *     magnitude, then rounded to the nearest integer.
+ *   - Reconstruction tables and attention are float64.
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   eps = 1e-6 in both divisions; a division by (s + eps) is a multiplication
+ *   by the correctly rounded float32 reciprocal; the chunk mean sums its C
+ *   values by a pairwise-halving tree (v[i] += v[i+h], h = C/2 ... 1), C a
+ *   power of two; the sign S is the sign of the centred value (d >= 0 -> +1);
+ *   Stage 4 applies Eq. 9 to the full 7-bit magnitude, giving one signed
+ *   8-bit code whose arithmetic high nibble is the Anchor (Eq. 9 applied to
+ *   V = I >> 4) and whose low nibble is the Residual (the extraction of
+ *   [Review] Appendix A.1); Anchor-only reconstruction uses the bucket point
+ *   16*V + 7 (the "+7 = 2^3 - 1" round-half-down bias of Stage 4).
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_EPS 1e-6f
+
+/* ---------------------------------------------------------------- helpers */
+
+static float bf16_bits_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round-to-nearest-even float32 -> bfloat16 bit pattern (finite inputs). */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+float oracle_bf16_to_f32(uint16_t h) { return bf16_bits_to_f32(h); }
+
+/* ------------------------------------------------------ Stage 3 (Eq. 7) */
+
+/* Y = ln(1 + alpha |x|) / ln(1 + alpha) * (2^7 - 1)   [Review, Stage 3, Eq. 7]
+ * evaluated in float64 from the float32 magnitude a = |X_final|. */
+double oracle_compand_y(float a, float alpha)
+{
+    double al = (double)alpha;
+    return 127.0 * log1p(al * (double)a) / log1p(al);
+}
+
+/* I = Round(Y) in {0..127}                      [Review, Stage 3, after Eq. 7]
+ * Round to nearest; Y >= 0 so floor(Y + 1/2) is nearest with ties upward. */
+int oracle_round_code(float a, float alpha)
+{
+    double y = oracle_compand_y(a, alpha);
+    double r = floor(y + 0.5);
+    if (r < 0.0) r = 0.0;
+    if (r > 127.0) r = 127.0;
+    return (int)r;
+}
+
+/* Inverse compander |x^| = ((1 + alpha)^(I/127) - 1) / alpha, float64, then
+ * rounded once to float32.            [Review, Worked Example, Eq. 14 and 15] */
+float oracle_expand(int I, float alpha)
+{
+    double al = (double)alpha;
+    return (float)((pow(1.0 + al, (double)I / 127.0) - 1.0) / al);
+}
+
+/* ------------------------------------------------------ Stage 4 (Eq. 9) */
+
+/* Stage 4 exactly as the review prints it, for one element:
+ *   I_bias = I + 7; V_mag = I_bias >> 4; V_recon = V_mag << 4;
+ *   V_res = V_recon - I; Q_anc = V_mag * S + min(S, 0).
+ * out[0..4] = I_bias, V_mag, V_recon, V_res, Q_anc.   [Review, Stage 4, Eq. 9]
+ * Used only to check the worked example and to count the V_mag = 8 cases
+ * that do not fit a 4-bit Anchor; the codec below uses the 8-bit reading. */
+void oracle_stage4_literal(int I, int S, int *out)
+{
+    int I_bias = I + 7;
+    int V_mag = I_bias >> 4;
+    int V_recon = V_mag << 4;
+    int V_res = V_recon - I;
+    int Q_anc = V_mag * S + (S < 0 ? S : 0);
+    out[0] = I_bias;
+    out[1] = V_mag;
+    out[2] = V_recon;
+    out[3] = V_res;
+    out[4] = Q_anc;
+}
+
+/* Eq. 9 applied to the full magnitude: Q8 = I*S + min(S, 0) in [-128, 127],
+ * stored as its 8-bit two's-complement pattern.        [Review, Stage 4, Eq. 9] */
+int oracle_code8(int I, int S)
+{
+    int q8 = I * S + (S < 0 ? S : 0);
+    return q8 & 0xff;
+}
+
+/* Split of the signed 8-bit code: Anchor = Q8 >> 4 (arithmetic, a signed
+ * 4-bit value = Eq. 9 applied to V = I >> 4), Residual = Q8 & 0xF.
+ *                              [Review, Stage 4; Review, Appendix A.1] */
+int oracle_anchor_nibble(int code8) { return (code8 >> 4) & 0xf; }
+int oracle_residual_nibble(int code8) { return code8 & 0xf; }
+
+/* --------------------------------------------------------------- encode */
+
+/*
+ * Algorithm 1 on one page block: P tokens x D channels of one KV head.
+ *   x          BF16 bits, element (t, d) at x[t * row_stride + d]
+ *   anchor     P x D/2 bytes, token-major; channel 2j -> low nibble of byte j,
+ *              channel 2j+1 -> high nibble ([Review, Implementation Notes]:
+ *              two 4-bit values packed per uint8)
+ *   residual   same layout
+ *   meta       (2 + 2 P/C) x D floats: gamma_min[D], gamma_scale[D],
+ *              mu[P/C][D], sigma[P/C][D]
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_encode_block(const uint16_t *x, int64_t row_stride, int P, int D,
+                        int C, float alpha, uint8_t *anchor, uint8_t *residual,
+                        float *meta)
+{
+    if (P <= 0 || D <= 0 || (D & 1) || C <= 0 || (C & (C - 1)) || P % C)
+        return -1;
+    const int NC = P / C;
+    float *g_min = meta;
+    float *g_scale = meta + D;
+    float *mu_rows = meta + 2 * D;
+    float *sg_rows = meta + (size_t)(2 + NC) * D;
+    float *n = (float *)malloc(sizeof(float) * (size_t)P);
+    float *v = (float *)malloc(sizeof(float) * (size_t)C);
+    if (!n || !v) {
+        free(n);
+        free(v);
+        return -1;
+    }
+    memset(anchor, 0, (size_t)P * (size_t)(D / 2));
+    memset(residual, 0, (size_t)P * (size_t)(D / 2));
+
+    for (int d = 0; d < D; ++d) {
+        /* Stage 1: gamma_min = min over the page, gamma_scale = max - min,
+         * X <- (X - gamma_min) / (gamma_scale + eps)      [Review, Stage 1] */
+        float lo = FLT_MAX, hi = -FLT_MAX;
+        for (int t = 0; t < P; ++t) {
+            float xv = bf16_bits_to_f32(x[(int64_t)t * row_stride + d]);
+            if (xv < lo) lo = xv;
+            if (xv > hi) hi = xv;
+        }
+        float gs = hi - lo;
+        float rg = 1.0f / (gs + ORACLE_EPS);
+        for (int t = 0; t < P; ++t) {
+            float xv = bf16_bits_to_f32(x[(int64_t)t * row_stride + d]);
+            n[t] = (xv - lo) * rg;
+        }
+        g_min[d] = lo;
+        g_scale[d] = gs;
+
+        for (int c = 0; c < NC; ++c) {
+            const float *nc = n + (size_t)c * C;
+            /* Stage 2: mu = Mean over the C tokens of the chunk,
+             * sigma = max |X - mu|, X_final = (X - mu) / (sigma + eps)
+             *                                           [Review, Stage 2] */
+            for (int i = 0; i < C; ++i) v[i] = nc[i];
+            for (int h = C / 2; h >= 1; h /= 2)
+                for (int i = 0; i < h; ++i) v[i] = v[i] + v[i + h];
+            float mu = v[0] * (1.0f / (float)C);
+            float sg = 0.0f;
+            for (int i = 0; i < C; ++i) {
+                float dd = nc[i] - mu;
+                float ad = fabsf(dd);
+                if (ad > sg) sg = ad;
+            }
+            float rs = 1.0f / (sg + ORACLE_EPS);
+            mu_rows[(size_t)c * D + d] = mu;
+            sg_rows[(size_t)c * D + d] = sg;
+
+            for (int i = 0; i < C; ++i) {
+                float dd = nc[i] - mu;
+                int S = dd >= 0.0f ? 1 : -1;
+                float xf = dd * rs;
+                /* Stage 3: I = Round(Y(|X_final|))  [Review, Stage 3, Eq. 7] */
+                int I = oracle_round_code(fabsf(xf), alpha);
+                /* Stage 4: signed 8-bit code, split into two nibbles. */
+                int code8 = oracle_code8(I, S);
+                int t = c * C + i;
+                size_t byte = (size_t)t * (size_t)(D / 2) + (size_t)(d >> 1);
+                int sh = (d & 1) ? 4 : 0;
+                anchor[byte] |= (uint8_t)(oracle_anchor_nibble(code8) << sh);
+                residual[byte] |= (uint8_t)(oracle_residual_nibble(code8) << sh);
+            }
+        }
+    }
+    free(n);
+    free(v);
+    return 0;
+}
+
+/*
+ * Whole tensor kv[B][L][H][D] (BF16 bits), page blocks in the order
+ * (b, page, h), for the blocks [blk_begin, blk_end) of that order.
+ * Outputs are the full-size streams: anchor/residual [B][L/P][H][P][D/2],
+ * meta [B][L/P][H][2 + 2P/C][D]; only the selected blocks are written.
+ */
+int oracle_encode_range(const uint16_t *kv, int64_t B, int64_t L, int H, int D,
+                        int P, int C, float alpha, uint8_t *anchor,
+                        uint8_t *residual, float *meta, int64_t blk_begin,
+                        int64_t blk_end)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || P <= 0 || L % P) return -1;
+    const int64_t NB = L / P;
+    const int NC = P / C;
+    const size_t code_blk = (size_t)P * (size_t)(D / 2);
+    const size_t meta_blk = (size_t)(2 + 2 * NC) * (size_t)D;
+    for (int64_t blk = blk_begin; blk < blk_end; ++blk) {
+        int64_t h = blk % H;
+        int64_t p = (blk / H) % NB;
+        int64_t b = blk / (H * NB);
+        const uint16_t *x = kv + ((b * L + p * P) * H + h) * D;
+        int rc = oracle_encode_block(x, (int64_t)H * D, P, D, C, alpha,
+                                     anchor + blk * code_blk,
+                                     residual + blk * code_blk,
+                                     meta + blk * meta_blk);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+/* --------------------------------------------------------------- decode */
+
+/*
+ * Decode one page block back to float32 values out[t * out_stride + d].
+ * residual == NULL: Anchor-only reconstruction ("Q_approx = dequant(Q_anc,
+ *   gamma, mu, sigma)" [Review, Mechanism 2, Anchor Phase]): the signed
+ *   Anchor a gives S and V (a >= 0: S = +1, V = a; a < 0: S = -1,
+ *   V = -a - 1) and the bucket point I = 16 V + 7.
+ * residual != NULL: full reconstruction ("Q_full = dequant(Q_anc + Q_res)"
+ *   [Review, Mechanism 2, Residual Phase]): Q8 = Anchor * 16 + Residual as a
+ *   signed 8-bit value, S = sign, I = Q8 (S = +1) or -Q8 - 1 (S = -1).
+ * Then |x_final| = ((1+alpha)^(I/127) - 1)/alpha (Eq. 14/15) with sign S, and
+ * the two affine steps of Stages 2 and 1 are undone with fused multiply-adds:
+ *   n = fma(x_final, sigma + eps, mu); x = fma(n, gamma_scale + eps, gamma_min).
+ */
+int oracle_decode_block(const uint8_t *anchor, const uint8_t *residual,
+                        const float *meta, int P, int D, int C, float alpha,
+                        float *out, int64_t out_stride)
+{
+    if (P <= 0 || D <= 0 || (D & 1) || C <= 0 || P % C) return -1;
+    const int NC = P / C;
+    const float *g_min = meta;
+    const float *g_scale = meta + D;
+    const float *mu_rows = meta + 2 * D;
+    const float *sg_rows = meta + (size_t)(2 + NC) * D;
+    float table[128];
+    for (int I = 0; I < 128; ++I) table[I] = oracle_expand(I, alpha);
+
+    for (int t = 0; t < P; ++t) {
+        int c = t / C;
+        for (int d = 0; d < D; ++d) {
+            size_t byte = (size_t)t * (size_t)(D / 2) + (size_t)(d >> 1);
+            int sh = (d & 1) ? 4 : 0;
+            int a = (anchor[byte] >> sh) & 0xf;
+            int S, I;
+            if (residual) {
+                int r = (residual[byte] >> sh) & 0xf;
+                int q8 = (a << 4) | r;
+                if (q8 >= 128) q8 -= 256;
+                S = q8 >= 0 ? 1 : -1;
+                I = S > 0 ? q8 : -q8 - 1;
+            } else {
+                int qa = a >= 8 ? a - 16 : a;
+                S = qa >= 0 ? 1 : -1;
+                int V = S > 0 ? qa : -qa - 1;
+                I = 16 * V + 7;
+            }
+            float xf = S > 0 ? table[I] : -table[I];
+            float sg = sg_rows[(size_t)c * D + d];
+            float mu = mu_rows[(size_t)c * D + d];
+            float nv = fmaf(xf, sg + ORACLE_EPS, mu);
+            float xv = fmaf(nv, g_scale[d] + ORACLE_EPS, g_min[d]);
+            out[(int64_t)t * out_stride + d] = xv;
+        }
+    }
+    return 0;
+}
+
+/* Whole-tensor decode into out[B][L][H][D] float32 for blocks
+ * [blk_begin, blk_end) of the (b, page, h) order. */
+int oracle_decode_range(const uint8_t *anchor, const uint8_t *residual,
+                        const float *meta, int64_t B, int64_t L, int H, int D,
+                        int P, int C, float alpha, float *out,
+                        int64_t blk_begin, int64_t blk_end)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || P <= 0 || L % P) return -1;
+    const int64_t NB = L / P;
+    const int NC = P / C;
+    const size_t code_blk = (size_t)P * (size_t)(D / 2);
+    const size_t meta_blk = (size_t)(2 + 2 * NC) * (size_t)D;
+    for (int64_t blk = blk_begin; blk < blk_end; ++blk) {
+        int64_t h = blk % H;
+        int64_t p = (blk / H) % NB;
+        int64_t b = blk / (H * NB);
+        float *o = out + ((b * L + p * P) * H + h) * D;
+        int rc = oracle_decode_block(anchor + blk * code_blk,
+                                     residual ? residual + blk * code_blk : NULL,
+                                     meta + blk * meta_blk, P, D, C, alpha, o,
+                                     (int64_t)H * D);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------ attention */
+
+/*
+ * One query row of O = softmax(q K^T / sqrt(d_k)) V   [Review, Eq. 1]
+ * in float64 over L cached tokens: K[t * kv_stride + d], V likewise.
+ * out[D] receives the float64 result.
+ */
+void oracle_attention_row(const float *q, const float *K, const float *V,
+                          int64_t L, int D, int64_t kv_stride, double *out)
+{
+    double scale = 1.0 / sqrt((double)D);
+    double *s = (double *)malloc(sizeof(double) * (size_t)L);
+    double m = -HUGE_VAL;
+    for (int64_t t = 0; t < L; ++t) {
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += (double)q[d] * (double)K[t * kv_stride + d];
+        s[t] = acc * scale;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t t = 0; t < L; ++t) {
+        double w = exp(s[t] - m);
+        l += w;
+        for (int d = 0; d < D; ++d) out[d] += w * (double)V[t * kv_stride + d];
+    }
+    for (int d = 0; d < D; ++d) out[d] /= l;
+    free(s);
+}

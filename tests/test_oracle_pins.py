@@ -1,0 +1,436 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Every check here is independent of the oracle's own code path: values printed
+on the pages (tests/golden/), closed forms, hand-derived tiny cases,
+invariants and error bounds.  Sources: "Lynx: Progressive Speculative KV Cache
+Transfer for Disaggregated LLM Inference" (technical review, cited as Review)
+and the paper digest page (cited as Digest).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+ALPHA = 255.0
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def f32(x):
+    return float(np.float32(x))
+
+
+# ----------------------------------------------------------- worked example
+
+def test_worked_example_stage3(oracle_mod):
+    """Review, Worked Example, Eq. 12-13: x_final = 0.37/0.55, alpha = 255,
+    Y ~ 117.9, I = 118."""
+    g = golden("worked_example.json")
+    xf = f32((g["x_view"] - g["mu"]) / g["sigma"])
+    assert abs(xf - g["x_final_printed"]) < 5e-4
+    y = oracle_mod.compand_y(xf, g["alpha"])
+    # printed 117.9 comes from 4-digit intermediates (5.151/5.545*127 = 117.97)
+    assert abs(y - g["Y_printed"]) < 0.1
+    assert abs(math.log1p(g["alpha"] * xf) - g["ln_1_plus_alpha_x_printed"]) < 2e-3
+    assert oracle_mod.round_code(xf, g["alpha"]) == g["I"]
+
+
+def test_worked_example_stage4_literal(oracle_mod):
+    """Review, Worked Example, Stage 4 trace: 125, 7, 112, -6, Q_anc = 7."""
+    g = golden("worked_example.json")
+    r = oracle_mod.stage4_literal(g["I"], g["S"])
+    assert r == dict(I_bias=g["I_bias"], V_mag=g["V_mag"], V_recon=g["V_recon"],
+                     V_res=g["V_res"], Q_anc=g["Q_anc"])
+    # decode side of the trace: I = V_recon - V_res recovers 118
+    assert r["V_recon"] - r["V_res"] == g["I_full_recovered"]
+
+
+def test_worked_example_reconstructions(oracle_mod):
+    """Review, Eq. 14-15: the closed forms of the printed expressions, and the
+    page's claim that the full reconstruction is within 1%."""
+    g = golden("worked_example.json")
+    xf = f32((g["x_view"] - g["mu"]) / g["sigma"])
+    full = oracle_mod.expand(g["I"], g["alpha"])
+    assert abs(full - g["full_closed_form_I118"]) < 1e-4
+    assert abs(full - xf) / xf < 0.01                       # "< 1%"
+    assert abs(full - g["full_reconstruction_printed"]) / full < 0.01
+    # Eq. 14's printed expression ((1+a)^(112/127) - 1)/a evaluated exactly
+    anc = oracle_mod.expand(g["anchor_only_I_printed"], g["alpha"])
+    assert abs(anc - g["anchor_only_closed_form_I112"]) < 1e-4
+    assert abs(anc - g["anchor_only_printed"]) > 0.1        # the page's slip
+    # 256^(112/127) = 132.98, not the printed 187
+    assert abs((1 + g["alpha"]) ** (112 / 127) - 132.98) < 0.01
+
+
+# ----------------------------------------------------------- Stage 4 / Eq. 9
+
+def test_stage4_split_is_a_bijection(oracle_mod):
+    """Review, Stage 4 and Eq. 9: the (sign, magnitude) code splits into an
+    Anchor nibble and a Residual nibble with Anchor<<4 | Residual == code,
+    every one of the 256 pairs used once; the Anchor is Eq. 9 applied to the
+    top magnitude bits V = I >> 4 as a 4-bit two's complement."""
+    seen = set()
+    for S in (1, -1):
+        for I in range(128):
+            c8 = oracle_mod.code8(I, S)
+            a = oracle_mod.anchor_nibble(c8)
+            r = oracle_mod.residual_nibble(c8)
+            assert 0 <= a < 16 and 0 <= r < 16
+            assert (a << 4) | r == c8
+            seen.add((a, r))
+            a_signed = a - 16 if a >= 8 else a
+            V = I >> 4
+            assert a_signed == V * S + min(S, 0)            # Eq. 9
+            if S > 0:
+                assert 0 <= a_signed <= 7
+            else:
+                assert -8 <= a_signed <= -1
+    assert len(seen) == 256
+    # the page's special case: V_mag = 0 with S = -1 maps to Q_anc = -1
+    assert oracle_mod.anchor_nibble(oracle_mod.code8(0, -1)) == 0xF
+
+
+def test_literal_stage4_needs_a_fifth_bit(oracle_mod):
+    """Review, Stage 4: with the +7 bias, I >= 121 gives V_mag = 8, so the
+    Anchor as printed takes 18 values (it states [0,15] and [-16,-1]); the
+    codec therefore applies Eq. 9 to the 8-bit code (the design's reading)."""
+    vals = set()
+    for S in (1, -1):
+        for I in range(128):
+            vals.add(oracle_mod.stage4_literal(I, S)["Q_anc"])
+    assert len(vals) == 18
+    assert oracle_mod.stage4_literal(121, 1)["V_mag"] == 8
+    assert oracle_mod.stage4_literal(120, 1)["V_mag"] == 7
+    # its residual always fits a signed nibble
+    for I in range(128):
+        assert -8 <= oracle_mod.stage4_literal(I, 1)["V_res"] <= 7
+
+
+# ----------------------------------------------------------- Eq. 7 compander
+
+def test_compander_closed_form(oracle_mod):
+    """Eq. 7: Y(0) = 0, Y(1) = 127, strictly increasing."""
+    assert oracle_mod.compand_y(0.0, ALPHA) == 0.0
+    assert abs(oracle_mod.compand_y(1.0, ALPHA) - 127.0) < 1e-12
+    xs = np.linspace(0, 1, 2001, dtype=np.float32)
+    ys = [oracle_mod.compand_y(float(x), ALPHA) for x in xs]
+    assert all(b > a for a, b in zip(ys, ys[1:]))
+    assert oracle_mod.round_code(0.0, ALPHA) == 0
+    assert oracle_mod.round_code(1.0, ALPHA) == 127
+
+
+def test_compander_small_alpha_is_linear_quantizer(oracle_mod):
+    """As alpha -> 0, ln(1+alpha x)/ln(1+alpha) -> x: the code becomes the
+    textbook 7-bit linear magnitude quantizer round(127 |x|)."""
+    rng = np.random.default_rng(1)
+    xs = rng.random(4000).astype(np.float32)
+    frac = (127 * xs.astype(np.float64)) % 1.0
+    keep = np.abs(frac - 0.5) > 1e-3          # away from rounding boundaries
+    for x in xs[keep]:
+        assert oracle_mod.round_code(float(x), 1e-7) == int(np.rint(127 * float(x)))
+
+
+def test_expand_inverts_compand(oracle_mod):
+    """Eq. 14/15 is the inverse of Eq. 7: Round(Y(X(I))) == I for all I."""
+    for alpha in (100.0, 255.0, 2000.0):
+        for I in range(128):
+            x = oracle_mod.expand(I, alpha)
+            assert abs(oracle_mod.compand_y(x, alpha) - I) < 1e-3
+            assert oracle_mod.round_code(x, alpha) == I
+        assert oracle_mod.expand(0, alpha) == 0.0
+        assert abs(oracle_mod.expand(127, alpha) - 1.0) < 1e-6
+
+
+def test_anchor_levels_are_geometric(oracle_mod):
+    """Digest, Method: the Anchor is a geometric-interval exponent,
+    (1+alpha)^q.  With the bucket points 16V+7, (X + 1/alpha) grows by
+    (1+alpha)^(16/127) per Anchor step."""
+    for alpha in (100.0, 255.0):
+        ratio = oracle_mod.anchor_ratio(alpha)
+        for V in range(7):
+            lo = oracle_mod.expand(16 * V + 7, alpha) + 1.0 / alpha
+            hi = oracle_mod.expand(16 * V + 23, alpha) + 1.0 / alpha
+            assert abs(hi / lo - ratio) < 1e-5 * ratio
+    assert abs(oracle_mod.anchor_ratio(255.0) - 2.011) < 1e-3
+
+
+# ----------------------------------------------------------- tiny hand cases
+
+def _bf16_bits(vals):
+    a = np.asarray(vals, dtype=np.float32)
+    return (a.view(np.uint32) >> 16).astype(np.uint16)   # exact for these values
+
+
+def test_encode_hand_case(oracle_mod):
+    """P=4, C=2, D=2.  Channel 0 = [0,1,2,3]: each chunk has two values, so
+    after centring they sit at -sigma and +sigma, |X_final| ~ 1 - 1e-5 and
+    I = 127: code8 = 128 (S=-1) then 127 (S=+1).  Channel 1 is constant:
+    gamma_scale = 0, every value normalises to 0, so I = 0, S = +1, code 0.
+    Channel 0 is the low nibble of each byte."""
+    x = np.stack([_bf16_bits([0, 1, 2, 3]), _bf16_bits([5, 5, 5, 5])], axis=1)
+    anc, res, meta = oracle_mod.encode_block(x, C=2, alpha=ALPHA)
+    assert anc[:, 0].tolist() == [0x08, 0x07, 0x08, 0x07]
+    assert res[:, 0].tolist() == [0x00, 0x0F, 0x00, 0x0F]
+    assert meta[0].tolist() == [0.0, 5.0]          # gamma_min
+    assert meta[1].tolist() == [3.0, 0.0]          # gamma_scale
+    # mu per chunk: (0 + 1/3)/2 and (2/3 + 1)/2 ; sigma = 1/6
+    assert abs(meta[2, 0] - 1 / 6) < 1e-6 and abs(meta[3, 0] - 5 / 6) < 1e-6
+    assert abs(meta[4, 0] - 1 / 6) < 1e-6 and abs(meta[5, 0] - 1 / 6) < 1e-6
+    assert meta[2:, 1].tolist() == [0.0, 0.0, 0.0, 0.0]
+
+
+def test_decode_hand_case(oracle_mod):
+    """Decode of the hand case.  Full: I = 127 decodes to |x_final| = 1, so the
+    values come back within fp32 noise; the constant channel is exact.
+    Anchor-only: V = 7 uses the bucket point 16*7+7 = 119."""
+    x = np.stack([_bf16_bits([0, 1, 2, 3]), _bf16_bits([5, 5, 5, 5])], axis=1)
+    anc, res, meta = oracle_mod.encode_block(x, C=2, alpha=ALPHA)
+    full = oracle_mod.decode_block(anc, res, meta, C=2, alpha=ALPHA)
+    assert np.allclose(full[:, 0], [0, 1, 2, 3], atol=1e-4)
+    assert full[:, 1].tolist() == [5.0] * 4
+    part = oracle_mod.decode_block(anc, None, meta, C=2, alpha=ALPHA)
+    x119 = oracle_mod.expand(119, ALPHA)
+    assert abs(x119 - 0.70402) < 1e-4
+    half = (1 / 6 + 1e-6) * x119
+    want = (3 + 1e-6) * np.array([1 / 6 - half, 1 / 6 + half,
+                                  5 / 6 - half, 5 / 6 + half])
+    assert np.allclose(part[:, 0], want, atol=1e-4), (part[:, 0], want)
+    assert part[:, 1].tolist() == [5.0] * 4
+
+
+# ----------------------------------------------------------- random blocks
+
+def _random_block(seed, P=256, D=128, outliers=(3, 77)):
+    rng = np.random.default_rng(seed)
+    lap = rng.laplace(size=(P, D)).astype(np.float32)
+    s = np.exp(0.5 * rng.standard_normal(D)).astype(np.float32)
+    o = np.ones(D, np.float32)
+    o[list(outliers)] = 100.0
+    import oracle
+    return oracle.f32_to_bf16_bits((lap * s * o).astype(np.float32))
+
+
+def _signed_codes(anc, res):
+    """Q8 as signed int8 for [P][D] from packed nibbles (Anchor<<4|Residual)."""
+    P, half = anc.shape
+    lo_a, hi_a = anc & 0xF, anc >> 4
+    lo_r, hi_r = res & 0xF, res >> 4
+    c = np.empty((P, half * 2), np.uint8)
+    c[:, 0::2] = (lo_a << 4) | lo_r
+    c[:, 1::2] = (hi_a << 4) | hi_r
+    return c.view(np.int8).astype(np.int32)
+
+
+def _magnitudes(q8):
+    S = np.where(q8 >= 0, 1, -1)
+    I = np.where(S > 0, q8, -q8 - 1)
+    return S, I
+
+
+@pytest.mark.parametrize("P,C", [(256, 32), (128, 32), (256, 64), (64, 16)])
+def test_encode_invariants(oracle_mod, P, C):
+    """Stage 1: gamma_min is the page minimum and gamma_scale the range.
+    Stage 2: mu, sigma lie in [0, 1].  Each chunk-channel with sigma > 0
+    reaches |X_final| ~ 1, i.e. I = 127.  Codes are monotone in x within a
+    chunk-channel (the sign map of Eq. 9 keeps order)."""
+    bits = _random_block(P + C, P=P)
+    x = oracle_mod.bf16_bits_to_f32(bits).reshape(P, 128)
+    anc, res, meta = oracle_mod.encode_block(bits.reshape(P, 128), C, ALPHA)
+    NC = P // C
+    assert np.array_equal(meta[0], x.min(axis=0))
+    assert np.array_equal(meta[1], (x.max(axis=0) - x.min(axis=0)).astype(np.float32))
+    mu, sg = meta[2:2 + NC], meta[2 + NC:]
+    assert (mu >= 0).all() and (mu <= 1).all() and (sg >= 0).all() and (sg <= 1).all()
+    q8 = _signed_codes(anc, res)
+    S, I = _magnitudes(q8)
+    for c in range(NC):
+        blkI = I[c * C:(c + 1) * C]
+        assert (blkI.max(axis=0)[sg[c] > 1e-3] == 127).all()
+        for d in range(128):
+            xs = x[c * C:(c + 1) * C, d]
+            qs = q8[c * C:(c + 1) * C, d]
+            order = np.argsort(xs, kind="stable")
+            assert (np.diff(qs[order]) >= 0).all() or np.unique(xs).size < C
+            # ties in x must share a code
+            for v in np.unique(xs):
+                assert np.unique(qs[xs == v]).size == 1
+
+
+def _X(y, alpha=ALPHA):
+    """Continuous inverse of Eq. 7 (for the half-code boundaries)."""
+    return (np.power(1.0 + alpha, np.asarray(y, np.float64) / 127.0) - 1.0) / alpha
+
+
+@pytest.mark.parametrize("P,C", [(256, 32), (128, 32), (256, 64)])
+def test_full_decode_within_one_code_step(oracle_mod, P, C):
+    """Full reconstruction error is at most one code step: x_final lies in
+    [X(I-1/2), X(I+1/2)] and the decoder returns X(I), scaled back by
+    (sigma+eps)(gamma_scale+eps) (plus float32 noise)."""
+    bits = _random_block(11 + P + C, P=P).reshape(P, 128)
+    x = oracle_mod.bf16_bits_to_f32(bits).reshape(P, 128).astype(np.float64)
+    anc, res, meta = oracle_mod.encode_block(bits, C, ALPHA)
+    xh = oracle_mod.decode_block(anc, res, meta, C, ALPHA).astype(np.float64)
+    NC = P // C
+    _, I = _magnitudes(_signed_codes(anc, res))
+    gs = meta[1].astype(np.float64) + 1e-6
+    sg = np.repeat(meta[2 + NC:].astype(np.float64), C, axis=0) + 1e-6
+    step = _X(np.minimum(I + 0.5, 127.0)) - _X(np.maximum(I - 0.5, 0.0))
+    bound = step * sg * gs + 4e-7 * (np.abs(x) + gs)
+    assert (np.abs(xh - x) <= bound).all()
+
+
+@pytest.mark.parametrize("P,C", [(256, 32), (128, 32)])
+def test_anchor_decode_within_its_bucket(oracle_mod, P, C):
+    """Anchor-only reconstruction lies in the same geometric bucket
+    [X(16V - 1/2), X(16V + 15 + 1/2)] as the true value, and its error is
+    never below the full reconstruction's for the same element."""
+    bits = _random_block(23 + P, P=P).reshape(P, 128)
+    x = oracle_mod.bf16_bits_to_f32(bits).reshape(P, 128).astype(np.float64)
+    anc, res, meta = oracle_mod.encode_block(bits, C, ALPHA)
+    xa = oracle_mod.decode_block(anc, None, meta, C, ALPHA).astype(np.float64)
+    NC = P // C
+    _, I = _magnitudes(_signed_codes(anc, res))
+    V = I >> 4
+    gs = meta[1].astype(np.float64) + 1e-6
+    sg = np.repeat(meta[2 + NC:].astype(np.float64), C, axis=0) + 1e-6
+    width = _X(np.minimum(16 * V + 15.5, 127.0)) - _X(np.maximum(16 * V - 0.5, 0.0))
+    bound = width * sg * gs + 4e-7 * (np.abs(x) + gs)
+    assert (np.abs(xa - x) <= bound).all()
+    # anchor-only error is larger on average (it drops the residual bits)
+    xf = oracle_mod.decode_block(anc, res, meta, C, ALPHA).astype(np.float64)
+    assert np.abs(xa - x).mean() > 3 * np.abs(xf - x).mean()
+
+
+def test_sign_flip_symmetry(oracle_mod):
+    """x -> -x mirrors every chunk: S flips and I is kept, so Q8 -> -Q8 - 1,
+    except where float32 rounding moves Y across a half-integer."""
+    bits = _random_block(5).reshape(256, 128)
+    neg = bits ^ np.uint16(0x8000)
+    a1, r1, _ = oracle_mod.encode_block(bits, 32, ALPHA)
+    a2, r2, _ = oracle_mod.encode_block(neg, 32, ALPHA)
+    q1, q2 = _signed_codes(a1, r1), _signed_codes(a2, r2)
+    S1, I1 = _magnitudes(q1)
+    S2, I2 = _magnitudes(q2)
+    same = (q2 == -q1 - 1)
+    assert same.mean() > 0.99
+    assert (np.abs(I1 - I2) <= 1).all()
+
+
+def test_scale_invariance(oracle_mod):
+    """Codes depend on x only through the two normalisations, so scaling a
+    page by 2 keeps them (up to eps and float32 rounding near boundaries)."""
+    bits = _random_block(9).reshape(256, 128)
+    x = oracle_mod.bf16_bits_to_f32(bits).reshape(256, 128)
+    bits2 = oracle_mod.f32_to_bf16_bits(x * 2)
+    a1, r1, m1 = oracle_mod.encode_block(bits, 32, ALPHA)
+    a2, r2, m2 = oracle_mod.encode_block(bits2, 32, ALPHA)
+    assert np.array_equal(m2[0], 2 * m1[0]) and np.array_equal(m2[1], 2 * m1[1])
+    q1, q2 = _signed_codes(a1, r1), _signed_codes(a2, r2)
+    assert (q1 == q2).mean() > 0.99
+    assert (np.abs(q1 - q2) <= 1).all()
+
+
+def test_laplacian_mass_near_zero(oracle_mod):
+    """Review, Stage 3: about half of the centred values have |x| < 0.17.
+    I <= Round(Y(0.17)) counts them on synthetic Laplacian KV."""
+    g = golden("size_examples.json")["laplacian_mass"]
+    import torch
+    from split_stream_kv_gb300 import synth
+    kv = synth.kv_cache(2, 512, 2, 128, seed=0)
+    bits = kv.view(torch.int16).numpy().view(np.uint16)
+    anc, res, meta = oracle_mod.encode(bits, 128, 32, ALPHA)
+    q8 = _signed_codes(anc.reshape(-1, 64), res.reshape(-1, 64))
+    _, I = _magnitudes(q8)
+    cut = oracle_mod.compand_y(g["threshold"], ALPHA)
+    frac = (I < cut).mean()
+    assert abs(frac - g["printed_fraction"]) < 0.08
+
+
+# ----------------------------------------------------------- attention
+
+def test_attention_single_token(oracle_mod):
+    rng = np.random.default_rng(0)
+    q, k, v = (rng.standard_normal((1, 128)).astype(np.float32) for _ in range(3))
+    out = oracle_mod.attention_row(q[0], k, v)
+    assert np.array_equal(out, v[0].astype(np.float64))
+
+
+def test_attention_identical_keys_give_mean(oracle_mod):
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal(128).astype(np.float32)
+    k = np.tile(rng.standard_normal(128).astype(np.float32), (7, 1))
+    v = rng.standard_normal((7, 128)).astype(np.float32)
+    out = oracle_mod.attention_row(q, k, v)
+    assert np.allclose(out, v.astype(np.float64).mean(axis=0), rtol=0, atol=1e-12)
+
+
+def test_attention_two_tokens_hand_weights(oracle_mod):
+    """Scores differing by ln 3 give softmax weights 3/4 and 1/4 (Eq. 1)."""
+    D = 128
+    q = np.zeros(D, np.float32)
+    q[0] = 1.0
+    k = np.zeros((2, D), np.float32)
+    k[0, 0] = np.float32(math.log(3.0) * math.sqrt(D))
+    v = np.zeros((2, D), np.float32)
+    v[0, :] = 4.0
+    v[1, :] = 8.0
+    out = oracle_mod.attention_row(q, k, v)
+    w0 = 3.0 / 4.0
+    assert np.allclose(out, w0 * 4.0 + (1 - w0) * 8.0, atol=1e-6)
+
+
+def test_attention_invariances(oracle_mod):
+    """Token order does not matter; adding one vector to every key shifts all
+    scores equally and leaves the output unchanged."""
+    rng = np.random.default_rng(2)
+    L, D = 50, 128
+    q = rng.standard_normal(D).astype(np.float32)
+    k = rng.standard_normal((L, D)).astype(np.float32)
+    v = rng.standard_normal((L, D)).astype(np.float32)
+    out = oracle_mod.attention_row(q, k, v)
+    perm = rng.permutation(L)
+    assert np.allclose(oracle_mod.attention_row(q, k[perm], v[perm]), out,
+                       atol=1e-12)
+    shift = np.zeros(D, np.float32)
+    shift[3] = 2.0  # exact in float32 addition for these magnitudes
+    out2 = oracle_mod.attention_row(q, (k + shift).astype(np.float32), v)
+    assert np.allclose(out2, out, atol=1e-6)
+
+
+# ----------------------------------------------------------- size formulas
+
+def test_kv_size_example(oracle_mod):
+    """Review, Eq. 3: Qwen3-235B-A22B at 128K is about 23.5 (binary) GB;
+    at 100 / 25 Gbps that takes about 1.9 / 7.5 s."""
+    g = golden("size_examples.json")["kv_size"]
+    n = oracle_mod.kv_size_bytes(g["k_factor"], g["L"], g["H_heads"] * g["D_head"],
+                                 g["n_layers"], g["precision_bytes"])
+    assert n == 25_232_932_864
+    assert abs(n / 2 ** 30 - g["printed_size"]) < 0.01
+    assert abs(23.5e9 * 8 / 100e9 - g["transfer_100gbps_printed_s"]) < 0.05
+    assert abs(23.5e9 * 8 / 25e9 - g["transfer_25gbps_printed_s"]) < 0.05
+
+
+def test_metadata_overhead_example(oracle_mod):
+    """Review, grouped-quantization deep dive: 2304 scalars (9 KB float32) per
+    H=128, P=256, C=32 page against a 65 KB BF16 page: 14%."""
+    g = golden("size_examples.json")["metadata"]
+    n = oracle_mod.metadata_scalars(g["H"], g["P"], g["C"])
+    assert n == g["printed_scalars"]
+    assert round(n * 4 / 1024) == g["printed_meta_kb"]
+    page = g["H"] * g["P"] * 2
+    assert page // 1000 == g["printed_page_kb"]       # 65,536 B printed as 65 KB
+    assert round(100 * n * 4 / page) == g["printed_overhead_percent"]
+    assert oracle_mod.meta_rows(g["P"], g["C"]) * g["H"] == n
+
+
+def test_effective_bins_example(oracle_mod):
+    g = golden("size_examples.json")["effective_bins"]
+    assert abs(oracle_mod.effective_bins(g["B"], 1 / g["m_over_m_i"])
+               - g["printed_bins"]) < 1e-12
