@@ -136,12 +136,19 @@ int oracle_residual_nibble(int code8) { return code8 & 0xf; }
 
 /* --------------------------------------------------------------- encode */
 
+/* Byte index within a token row and nibble shift for channel d (see the
+ * packing note of oracle_encode_block). */
+static size_t nib_byte(int d) { return (size_t)(d >> 3) * 4u + (size_t)(d & 3); }
+static int nib_shift(int d) { return (d & 4) ? 4 : 0; }
+
 /*
  * Algorithm 1 on one page block: P tokens x D channels of one KV head.
  *   x          BF16 bits, element (t, d) at x[t * row_stride + d]
- *   anchor     P x D/2 bytes, token-major; channel 2j -> low nibble of byte j,
- *              channel 2j+1 -> high nibble ([Review, Implementation Notes]:
- *              two 4-bit values packed per uint8)
+ *   anchor     P x D/2 bytes, token-major.  Two 4-bit values per uint8
+ *              ([Review, Implementation Notes]); the pages do not say which
+ *              two, so within each aligned group of 8 channels 8G..8G+7,
+ *              byte 4G + k holds channel 8G+k in its low nibble and channel
+ *              8G+k+4 in its high nibble (k = 0..3).
  *   residual   same layout
  *   meta       (2 + 2 P/C) x D floats: gamma_min[D], gamma_scale[D],
  *              mu[P/C][D], sigma[P/C][D]
@@ -151,7 +158,7 @@ int oracle_encode_block(const uint16_t *x, int64_t row_stride, int P, int D,
                         int C, float alpha, uint8_t *anchor, uint8_t *residual,
                         float *meta)
 {
-    if (P <= 0 || D <= 0 || (D & 1) || C <= 0 || (C & (C - 1)) || P % C)
+    if (P <= 0 || D <= 0 || (D & 7) || C <= 0 || (C & (C - 1)) || P % C)
         return -1;
     const int NC = P / C;
     float *g_min = meta;
@@ -177,6 +184,10 @@ int oracle_encode_block(const uint16_t *x, int64_t row_stride, int P, int D,
             if (xv < lo) lo = xv;
             if (xv > hi) hi = xv;
         }
+        /* min and max do not order +0 and -0; a zero extreme is kept as +0
+         * so that the statistic does not depend on the token order. */
+        lo = lo + 0.0f;
+        hi = hi + 0.0f;
         float gs = hi - lo;
         float rg = 1.0f / (gs + ORACLE_EPS);
         for (int t = 0; t < P; ++t) {
@@ -214,8 +225,8 @@ int oracle_encode_block(const uint16_t *x, int64_t row_stride, int P, int D,
                 /* Stage 4: signed 8-bit code, split into two nibbles. */
                 int code8 = oracle_code8(I, S);
                 int t = c * C + i;
-                size_t byte = (size_t)t * (size_t)(D / 2) + (size_t)(d >> 1);
-                int sh = (d & 1) ? 4 : 0;
+                size_t byte = (size_t)t * (size_t)(D / 2) + nib_byte(d);
+                int sh = nib_shift(d);
                 anchor[byte] |= (uint8_t)(oracle_anchor_nibble(code8) << sh);
                 residual[byte] |= (uint8_t)(oracle_residual_nibble(code8) << sh);
             }
@@ -275,7 +286,7 @@ int oracle_decode_block(const uint8_t *anchor, const uint8_t *residual,
                         const float *meta, int P, int D, int C, float alpha,
                         float *out, int64_t out_stride)
 {
-    if (P <= 0 || D <= 0 || (D & 1) || C <= 0 || P % C) return -1;
+    if (P <= 0 || D <= 0 || (D & 7) || C <= 0 || P % C) return -1;
     const int NC = P / C;
     const float *g_min = meta;
     const float *g_scale = meta + D;
@@ -287,8 +298,8 @@ int oracle_decode_block(const uint8_t *anchor, const uint8_t *residual,
     for (int t = 0; t < P; ++t) {
         int c = t / C;
         for (int d = 0; d < D; ++d) {
-            size_t byte = (size_t)t * (size_t)(D / 2) + (size_t)(d >> 1);
-            int sh = (d & 1) ? 4 : 0;
+            size_t byte = (size_t)t * (size_t)(D / 2) + nib_byte(d);
+            int sh = nib_shift(d);
             int a = (anchor[byte] >> sh) & 0xf;
             int S, I;
             if (residual) {

@@ -167,33 +167,68 @@ def _bf16_bits(vals):
     return (a.view(np.uint32) >> 16).astype(np.uint16)   # exact for these values
 
 
+def _hand_block():
+    """P=4, D=8: channel 0 = [0,1,2,3], channels 1..7 constant."""
+    cols = [_bf16_bits([0, 1, 2, 3])] + [_bf16_bits([5 + k] * 4) for k in range(7)]
+    return np.stack(cols, axis=1)
+
+
 def test_encode_hand_case(oracle_mod):
-    """P=4, C=2, D=2.  Channel 0 = [0,1,2,3]: each chunk has two values, so
+    """P=4, C=2, D=8.  Channel 0 = [0,1,2,3]: each chunk has two values, so
     after centring they sit at -sigma and +sigma, |X_final| ~ 1 - 1e-5 and
-    I = 127: code8 = 128 (S=-1) then 127 (S=+1).  Channel 1 is constant:
+    I = 127: code8 = 128 (S=-1) then 127 (S=+1).  Channels 1..7 are constant:
     gamma_scale = 0, every value normalises to 0, so I = 0, S = +1, code 0.
-    Channel 0 is the low nibble of each byte."""
-    x = np.stack([_bf16_bits([0, 1, 2, 3]), _bf16_bits([5, 5, 5, 5])], axis=1)
-    anc, res, meta = oracle_mod.encode_block(x, C=2, alpha=ALPHA)
+    Channel 0 is the low nibble of byte 0 (it shares the byte with channel 4)."""
+    anc, res, meta = oracle_mod.encode_block(_hand_block(), C=2, alpha=ALPHA)
     assert anc[:, 0].tolist() == [0x08, 0x07, 0x08, 0x07]
     assert res[:, 0].tolist() == [0x00, 0x0F, 0x00, 0x0F]
-    assert meta[0].tolist() == [0.0, 5.0]          # gamma_min
-    assert meta[1].tolist() == [3.0, 0.0]          # gamma_scale
+    assert (anc[:, 1:] == 0).all() and (res[:, 1:] == 0).all()
+    assert meta[0].tolist() == [0.0] + [5.0 + k for k in range(7)]   # gamma_min
+    assert meta[1].tolist() == [3.0] + [0.0] * 7                      # gamma_scale
     # mu per chunk: (0 + 1/3)/2 and (2/3 + 1)/2 ; sigma = 1/6
     assert abs(meta[2, 0] - 1 / 6) < 1e-6 and abs(meta[3, 0] - 5 / 6) < 1e-6
     assert abs(meta[4, 0] - 1 / 6) < 1e-6 and abs(meta[5, 0] - 1 / 6) < 1e-6
-    assert meta[2:, 1].tolist() == [0.0, 0.0, 0.0, 0.0]
+    assert (meta[2:, 1:] == 0).all()
+
+
+def test_encode_nibble_pairing(oracle_mod):
+    """The byte shared by channels 8G+k and 8G+k+4: moving the ramp of the hand
+    case to channel 4 moves its code to the high nibble of byte 0, and to
+    channel 9 the low nibble of byte 5."""
+    base = _hand_block()
+    flat = np.repeat(base[:, 1:2], 8, axis=1)          # constant channels
+    x = np.concatenate([base, flat], axis=1)          # D = 16, ramp at 0
+    x[:, [0, 4]] = x[:, [4, 0]]
+    anc, res, _ = oracle_mod.encode_block(x, C=2, alpha=ALPHA)
+    assert anc[:, 0].tolist() == [0x80, 0x70, 0x80, 0x70]
+    assert res[:, 0].tolist() == [0x00, 0xF0, 0x00, 0xF0]
+    x = np.concatenate([base, flat], axis=1)
+    x[:, [0, 9]] = x[:, [9, 0]]
+    anc, res, _ = oracle_mod.encode_block(x, C=2, alpha=ALPHA)
+    assert anc[:, 5].tolist() == [0x08, 0x07, 0x08, 0x07]
+    assert (np.delete(anc, 5, axis=1) == 0).all()
+
+
+def test_negative_zero_extreme_is_canonical(oracle_mod):
+    """A page whose extreme is a zero stores +0 whichever zero comes first."""
+    a = np.stack([_bf16_bits([-0.0, 0.0, 1.0, 2.0])] * 8, axis=1)
+    b = np.stack([_bf16_bits([0.0, -0.0, 1.0, 2.0])] * 8, axis=1)
+    ra = oracle_mod.encode_block(a, C=2, alpha=ALPHA)
+    rb = oracle_mod.encode_block(b, C=2, alpha=ALPHA)
+    for u, v in zip(ra, rb):
+        assert u.tobytes() == v.tobytes()
+    assert not np.signbit(ra[2][0]).any()
 
 
 def test_decode_hand_case(oracle_mod):
     """Decode of the hand case.  Full: I = 127 decodes to |x_final| = 1, so the
-    values come back within fp32 noise; the constant channel is exact.
+    values come back within fp32 noise; the constant channels are exact.
     Anchor-only: V = 7 uses the bucket point 16*7+7 = 119."""
-    x = np.stack([_bf16_bits([0, 1, 2, 3]), _bf16_bits([5, 5, 5, 5])], axis=1)
+    x = _hand_block()
     anc, res, meta = oracle_mod.encode_block(x, C=2, alpha=ALPHA)
     full = oracle_mod.decode_block(anc, res, meta, C=2, alpha=ALPHA)
     assert np.allclose(full[:, 0], [0, 1, 2, 3], atol=1e-4)
-    assert full[:, 1].tolist() == [5.0] * 4
+    assert (full[:, 1:] == oracle_mod.bf16_bits_to_f32(x[:, 1:]).reshape(4, 7)).all()
     part = oracle_mod.decode_block(anc, None, meta, C=2, alpha=ALPHA)
     x119 = oracle_mod.expand(119, ALPHA)
     assert abs(x119 - 0.70402) < 1e-4
@@ -201,7 +236,7 @@ def test_decode_hand_case(oracle_mod):
     want = (3 + 1e-6) * np.array([1 / 6 - half, 1 / 6 + half,
                                   5 / 6 - half, 5 / 6 + half])
     assert np.allclose(part[:, 0], want, atol=1e-4), (part[:, 0], want)
-    assert part[:, 1].tolist() == [5.0] * 4
+    assert (part[:, 1:] == full[:, 1:]).all()
 
 
 # ----------------------------------------------------------- random blocks
@@ -217,14 +252,15 @@ def _random_block(seed, P=256, D=128, outliers=(3, 77)):
 
 
 def _signed_codes(anc, res):
-    """Q8 as signed int8 for [P][D] from packed nibbles (Anchor<<4|Residual)."""
+    """Q8 as signed int8 for [P][D] from packed nibbles (Anchor<<4|Residual);
+    byte 4G+k of a row holds channels 8G+k (low) and 8G+k+4 (high)."""
     P, half = anc.shape
-    lo_a, hi_a = anc & 0xF, anc >> 4
-    lo_r, hi_r = res & 0xF, res >> 4
-    c = np.empty((P, half * 2), np.uint8)
-    c[:, 0::2] = (lo_a << 4) | lo_r
-    c[:, 1::2] = (hi_a << 4) | hi_r
-    return c.view(np.int8).astype(np.int32)
+    a = anc.reshape(P, half // 4, 4)
+    r = res.reshape(P, half // 4, 4)
+    c = np.empty((P, half // 4, 8), np.uint8)
+    c[:, :, 0:4] = ((a & 0xF) << 4) | (r & 0xF)
+    c[:, :, 4:8] = (a & 0xF0) | (r >> 4)
+    return c.reshape(P, half * 2).view(np.int8).astype(np.int32)
 
 
 def _magnitudes(q8):
