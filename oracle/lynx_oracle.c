@@ -184,10 +184,11 @@ int oracle_encode_block(const uint16_t *x, int64_t row_stride, int P, int D,
             if (xv < lo) lo = xv;
             if (xv > hi) hi = xv;
         }
-        /* min and max do not order +0 and -0; a zero extreme is kept as +0
-         * so that the statistic does not depend on the token order. */
-        lo = lo + 0.0f;
-        hi = hi + 0.0f;
+        /* min and max do not order +0 and -0, so a zero extreme is given one
+         * sign: the minimum becomes -0 (then x - gamma_min of any zero x is
+         * +0, and no -0 reaches the sign test of Stage 3), the maximum +0. */
+        if (lo == 0.0f) lo = -0.0f;
+        if (hi == 0.0f) hi = 0.0f;
         float gs = hi - lo;
         float rg = 1.0f / (gs + ORACLE_EPS);
         for (int t = 0; t < P; ++t) {

@@ -210,14 +210,18 @@ def test_encode_nibble_pairing(oracle_mod):
 
 
 def test_negative_zero_extreme_is_canonical(oracle_mod):
-    """A page whose extreme is a zero stores +0 whichever zero comes first."""
+    """A page whose minimum is a zero stores -0 whichever zero comes first,
+    and zero values then centre to +0: S = +1, I = 0, code 0."""
     a = np.stack([_bf16_bits([-0.0, 0.0, 1.0, 2.0])] * 8, axis=1)
     b = np.stack([_bf16_bits([0.0, -0.0, 1.0, 2.0])] * 8, axis=1)
     ra = oracle_mod.encode_block(a, C=2, alpha=ALPHA)
     rb = oracle_mod.encode_block(b, C=2, alpha=ALPHA)
     for u, v in zip(ra, rb):
         assert u.tobytes() == v.tobytes()
-    assert not np.signbit(ra[2][0]).any()
+    assert np.signbit(ra[2][0]).all()
+    z = np.stack([_bf16_bits([-0.0, 0.0, -0.0, 0.0])] * 8, axis=1)
+    anc, res, meta = oracle_mod.encode_block(z, C=2, alpha=ALPHA)
+    assert (anc == 0).all() and (res == 0).all()
 
 
 def test_decode_hand_case(oracle_mod):
