@@ -1,0 +1,476 @@
+"""Benchmark of the split-stream KV hot path on GB300.
+
+One step = every row of the path on synthetic data resident in HBM:
+  encode        Llama-3-8B-shaped KV: 32 layers x (K, V) = B 64, L 16384,
+                8 KV heads, D 128, page 128, C 32, alpha 255 (2 GiB BF16)
+  decode_anchor the same streams -> BF16 KV
+  decode_full   the same streams -> BF16 KV
+  attn_draft    8 sequences x 32768 tokens, 32 query heads / 8 KV heads,
+                T = 1 over the Anchor codes (+ split combine)
+  attn_verify   the same KV, T = 8 over Anchor + Residual (+ split combine)
+Metric: BF16-equivalent KV GB/s over the whole step (2 bytes per KV element
+each row touches), with per-row times, roofline fractions of the measured HBM
+bandwidth, and decode-attention tokens/s.
+
+Flags: --gpus N (one replica per rank under torchrun; weak scaling),
+--steps K, --warmup W, --impl {lynx,reference}.  --impl reference times the
+CPU oracle (the only reference this path has) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV codec GB/s (BF16-equivalent) and anchor-attention tokens/s; % of HBM roofline"
+ALPHA = 255.0
+CODEC = dict(B=64, L=16384, H=8, D=128, P=128, C=32)
+ATTN = dict(batch=8, L=32768, H_kv=8, H_q=32, D=128, P=128, C=32, T_draft=1, T_verify=8)
+
+
+def meta_bytes_per_elem(P, C):
+    return 8.0 / P + 8.0 / C
+
+
+def codec_elems():
+    return CODEC["B"] * CODEC["L"] * CODEC["H"] * CODEC["D"]
+
+
+def attn_kv_elems():
+    a = ATTN
+    return 2 * a["batch"] * a["L"] * a["H_kv"] * a["D"]   # K and V
+
+
+def algorithmic_bytes():
+    """Bytes each row must move at minimum (per launch)."""
+    n = codec_elems()
+    m = meta_bytes_per_elem(CODEC["P"], CODEC["C"])
+    na = attn_kv_elems()
+    ma = meta_bytes_per_elem(ATTN["P"], ATTN["C"])
+    return {
+        "encode": n * (2 + 0.5 + 0.5 + m),
+        "decode_anchor": n * (0.5 + m + 2),
+        "decode_full": n * (0.5 + 0.5 + m + 2),
+        "attn_draft": na * (0.5 + ma),
+        "attn_verify": na * (1.0 + ma),
+    }
+
+
+def bf16_equiv_bytes():
+    n = codec_elems()
+    na = attn_kv_elems()
+    return {"encode": 2 * n, "decode_anchor": 2 * n, "decode_full": 2 * n,
+            "attn_draft": 2 * na, "attn_verify": 2 * na}
+
+
+ROWS = ["encode", "decode_anchor", "decode_full", "attn_draft", "attn_verify"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def workload_config():
+    return {
+        "workload": ("llama3-8b-shaped KV codec (B=64 = 32 layers x K,V; L=16384; H_kv=8; "
+                     "D=128; page=128; C=32; alpha=255) + packed-KV decode attention "
+                     "(8 seqs x 32768 tokens; H_q=32 over H_kv=8; draft T=1 anchor, "
+                     "verify T=8 full)"),
+        "l2": "inputs larger than L2 (2 GiB BF16 codec input, 0.69 GiB packed attention KV)",
+        "parallelism": "replicas",
+    }
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.path = None
+        if not uuid:
+            return
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- CPU leg
+
+def cpu_sample_run(target_s: float = 12.0, threads: int | None = None):
+    """Time the oracle on a bounded sample of the step, repeated until about
+    target_s seconds of work: page blocks of the codec workload (encode and
+    both decodes of 2 x 4096 tokens x 8 heads) and attention of one
+    (sequence, KV head) pair over 4096 tokens (both decoders of its pages,
+    then the float64 softmax for the 4 draft rows and 32 verify rows).  The
+    codec and attention rates are reweighted to the step's byte mix.  Returns
+    (GB/s BF16-equivalent, threads, description, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from split_stream_kv_gb300 import synth
+
+    threads = threads or (os.cpu_count() or 1)
+    P, C = CODEC["P"], CODEC["C"]
+    Lc = 4096
+    kv = synth.kv_cache(2, Lc, CODEC["H"], 128, seed=11, device="cpu")
+    bits = kv.view(torch.int16).numpy().view(np.uint16)
+    La = 4096
+    kva = synth.kv_cache(2, La, 1, 128, seed=5, device="cpu")
+    ab = kva.view(torch.int16).numpy().view(np.uint16)
+    ea, er, em = oracle.encode(ab, ATTN["P"], ATTN["C"], ALPHA, threads=threads)
+    q = np.random.default_rng(0).standard_normal((ATTN["T_verify"] * 4, 128)).astype(np.float32)
+
+    t_codec = t_attn = 0.0
+    codec_bytes = attn_bytes = 0
+    reps = 0
+    while t_codec + t_attn < target_s or reps == 0:
+        t0 = time.perf_counter()
+        oa, orr, om = oracle.encode(bits, P, C, ALPHA, threads=threads)
+        oracle.decode(oa, None, om, Lc, P, C, ALPHA, threads=threads)
+        oracle.decode(oa, orr, om, Lc, P, C, ALPHA, threads=threads)
+        t_codec += time.perf_counter() - t0
+        codec_bytes += 3 * 2 * bits.size
+        t0 = time.perf_counter()
+        for full, rows in ((False, 4), (True, 4 * ATTN["T_verify"])):
+            x = oracle.decode(ea, er if full else None, em, La, ATTN["P"], ATTN["C"], ALPHA,
+                              threads=threads)
+            xb = oracle.bf16_bits_to_f32(oracle.f32_to_bf16_bits(x)).reshape(x.shape)
+            K, V = xb[0, :, 0], xb[1, :, 0]
+            for r in range(rows):
+                oracle.attention_row(q[r], K, V)
+            attn_bytes += 2 * 2 * La * 128
+        t_attn += time.perf_counter() - t0
+        reps += 1
+    be = bf16_equiv_bytes()
+    w_codec = be["encode"] + be["decode_anchor"] + be["decode_full"]
+    w_attn = be["attn_draft"] + be["attn_verify"]
+    t_step = w_codec / (codec_bytes / t_codec) + w_attn / (attn_bytes / t_attn)
+    value = (w_codec + w_attn) / t_step / 1e9
+    desc = (f"{reps} x [{2 * (Lc // P) * CODEC['H']} page blocks (2 x {Lc} tokens x "
+            f"{CODEC['H']} heads) encoded and decoded both ways + draft (4 rows) and verify "
+            f"(32 rows) attention over one {La}-token (sequence, KV head) pair incl. its "
+            f"decode]; {t_codec + t_attn:.1f} s on {threads} threads; codec and attention "
+            f"rates reweighted to the step's byte mix")
+    return value, threads, desc, t_codec + t_attn
+
+
+# ----------------------------------------------------------------- GPU leg
+
+def run_lynx(args, rank, world, dev):
+    import torch
+
+    from split_stream_kv_gb300 import lynx, synth
+
+    torch.cuda.set_device(dev)
+    c = CODEC
+    a = ATTN
+    kv = synth.kv_cache(c["B"], c["L"], c["H"], c["D"], seed=11 + rank, device=dev)
+    anc, res, meta = lynx.lynx_encode(kv, c["P"], c["C"], ALPHA)
+    dec_a = torch.empty_like(kv)
+    dec_f = torch.empty_like(kv)
+    kva = synth.kv_cache(2 * a["batch"], a["L"], a["H_kv"], a["D"], seed=5 + rank, device=dev)
+    ks = lynx.lynx_encode(kva[0::2].contiguous(), a["P"], a["C"], ALPHA)
+    vs = lynx.lynx_encode(kva[1::2].contiguous(), a["P"], a["C"], ALPHA)
+    del kva
+    q1 = synth.queries(a["batch"], a["T_draft"], a["H_q"], a["D"], seed=1, device=dev)
+    q8 = synth.queries(a["batch"], a["T_verify"], a["H_q"], a["D"], seed=8, device=dev)
+    out1 = torch.empty((a["batch"], a["T_draft"], a["H_q"], a["D"]), device=dev)
+    out8 = torch.empty((a["batch"], a["T_verify"], a["H_q"], a["D"]), device=dev)
+    ws_n = max(lynx.lynx_attn_workspace_bytes(a["batch"], t, a["H_q"], a["L"], a["H_kv"],
+                                              a["D"], a["P"])
+               for t in (a["T_draft"], a["T_verify"]))
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=dev)
+    ks_anchor = (ks[0], None, ks[2])
+    vs_anchor = (vs[0], None, vs[2])
+
+    def row(name):
+        if name == "encode":
+            lynx.lynx_encode(kv, c["P"], c["C"], ALPHA, anc, res, meta)
+        elif name == "decode_anchor":
+            lynx.lynx_decode_anchor(anc, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_a)
+        elif name == "decode_full":
+            lynx.lynx_decode_full(anc, res, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_f)
+        elif name == "attn_draft":
+            lynx.lynx_attn_decode(q1, ks_anchor, vs_anchor, a["L"], a["P"], a["C"], ALPHA,
+                                  lynx.LYNX_ANCHOR, out=out1, workspace=ws)
+        else:
+            lynx.lynx_attn_decode(q8, ks, vs, a["L"], a["P"], a["C"], ALPHA, lynx.LYNX_FULL,
+                                  out=out8, workspace=ws)
+
+    launches_per_step = {"encode": 1, "decode_anchor": 1, "decode_full": 1, "attn_draft": 2,
+                         "attn_verify": 2}
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        for r in ROWS:
+            row(r)
+    torch.cuda.synchronize(dev)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        uuid = None
+    # ---- device-timed region
+    ev = {r: [] for r in ROWS}
+    barrier()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(uuid if rank == 0 else None)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        for r in ROWS:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            row(r)
+            e1.record(stream)
+            ev[r].append((e0, e1))
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    row_ms = {r: sum(e0.elapsed_time(e1) for e0, e1 in ev[r]) / args.steps for r in ROWS}
+
+    # ---- end to end: pinned host buffers in, results out, every step
+    kv_h = torch.empty(kv.shape, dtype=kv.dtype, pin_memory=True)
+    kv_h.copy_(kv)
+    pk_h = [t.cpu().pin_memory() for t in (ks[0], ks[1], ks[2], vs[0], vs[1], vs[2])]
+    pk_d = [torch.empty_like(t, device=dev) for t in pk_h]
+    q1_h, q8_h = q1.cpu().pin_memory(), q8.cpu().pin_memory()
+    anc_h = torch.empty(anc.shape, dtype=anc.dtype, pin_memory=True)
+    res_h = torch.empty(res.shape, dtype=res.dtype, pin_memory=True)
+    meta_h = torch.empty(meta.shape, dtype=meta.dtype, pin_memory=True)
+    o1_h = torch.empty(out1.shape, dtype=out1.dtype, pin_memory=True)
+    o8_h = torch.empty(out8.shape, dtype=out8.dtype, pin_memory=True)
+    h2d = kv_h.nbytes + sum(t.nbytes for t in pk_h) + q1_h.nbytes + q8_h.nbytes
+    d2h = anc_h.nbytes + res_h.nbytes + meta_h.nbytes + o1_h.nbytes + o8_h.nbytes
+
+    def e2e_step():
+        kv.copy_(kv_h, non_blocking=True)
+        for d, hsrc in zip(pk_d, pk_h):
+            d.copy_(hsrc, non_blocking=True)
+        q1.copy_(q1_h, non_blocking=True)
+        q8.copy_(q8_h, non_blocking=True)
+        lynx.lynx_encode(kv, c["P"], c["C"], ALPHA, anc, res, meta)
+        anc_h.copy_(anc, non_blocking=True)
+        res_h.copy_(res, non_blocking=True)
+        meta_h.copy_(meta, non_blocking=True)
+        lynx.lynx_decode_anchor(anc, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_a)
+        lynx.lynx_decode_full(anc, res, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_f)
+        lynx.lynx_attn_decode(q1, (pk_d[0], None, pk_d[2]), (pk_d[3], None, pk_d[5]), a["L"],
+                              a["P"], a["C"], ALPHA, lynx.LYNX_ANCHOR, out=out1, workspace=ws)
+        lynx.lynx_attn_decode(q8, tuple(pk_d[0:3]), tuple(pk_d[3:6]), a["L"], a["P"], a["C"],
+                              ALPHA, lynx.LYNX_FULL, out=out8, workspace=ws)
+        o1_h.copy_(out1, non_blocking=True)
+        o8_h.copy_(out8, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    w0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    e2e_s = (time.perf_counter() - w0) / e2e_steps
+
+    if world > 1:
+        t = torch.tensor([ms_total, e2e_s], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total, e2e_s = float(t[0]), float(t[1])
+    assert lynx.lynx_wait_timeouts() == 0
+    return dict(ms_total=ms_total, row_ms=row_ms, e2e_s=e2e_s, h2d=h2d, d2h=d2h, clocks=clk,
+                launches=sum(launches_per_step.values()) * args.steps)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["lynx", "reference"], default="lynx")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return run_reference(args, world)
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    r = run_lynx(args, rank, world, dev)
+
+    if rank == 0:
+        be = bf16_equiv_bytes()
+        alg = algorithmic_bytes()
+        peak, peak_kind = load_peaks()
+        step_ms = r["ms_total"] / args.steps
+        step_bytes = sum(be.values())
+        value = world * step_bytes / (step_ms / 1e3) / 1e9
+        rows = {}
+        for name in ROWS:
+            ms = r["row_ms"][name]
+            ach = alg[name] / (ms / 1e3) / 1e9
+            d = {"ms": round(ms, 4), "bf16_equiv_GBps": round(be[name] / (ms / 1e3) / 1e9, 1),
+                 "algorithmic_bytes": int(alg[name]), "achieved_GBps": round(ach, 1),
+                 "roofline_frac": round(ach / peak, 4)}
+            if name.startswith("attn"):
+                T = ATTN["T_draft"] if name == "attn_draft" else ATTN["T_verify"]
+                d["tokens_per_s"] = round(ATTN["batch"] * T / (ms / 1e3), 1)
+                d["context_tokens_per_s"] = round(ATTN["batch"] * ATTN["L"] / (ms / 1e3), 1)
+            rows[name] = d
+        dom = max(ROWS, key=lambda n: r["row_ms"][n])
+        ach = alg[dom] / (r["row_ms"][dom] / 1e3) / 1e9
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": workload_config(),
+            "rows": rows,
+            "anchor_attention_tokens_per_s": rows["attn_draft"]["tokens_per_s"],
+            "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1),
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(ach / peak, 4), "traffic": None},
+            "e2e": {"value": round(world * step_bytes / r["e2e_s"] / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
+            "gpu_launches": r["launches"],
+            "clocks": r["clocks"],
+        }
+        if world == 1 and not args.no_cpu:
+            v, cores, desc, _ = cpu_sample_run()
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores,
+                                    "kind": "oracle", "sample": desc}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args, world):
+    """The reference arm: the CPU oracle on the host cores, each step a
+    bounded sample of the same workload."""
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        cpu_sample_run(target_s=1.0)
+    vals, t_all = [], 0.0
+    desc, cores = "", 0
+    for _ in range(args.steps):
+        v, cores, desc, t = cpu_sample_run(target_s=10.0)
+        vals.append(v)
+        t_all += t
+    value = sum(vals) / len(vals)
+    step_bytes = sum(bf16_equiv_bytes().values())
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_bytes / (value * 1e9) * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,168 @@
+/*
+ * lynx.h -- C ABI of the GB300 (sm_103a) split-stream KV codec and of decode
+ * attention over its packed codes.
+ *
+ * Sources, cited by page title and section:
+ *   [Review] "Lynx: Progressive Speculative KV Cache Transfer for
+ *            Disaggregated LLM Inference" (technical review of the paper).
+ *   [Digest] "Lynx: Progressive Speculative Quantization for accelerating KV
+ *            Transfer in Long-Context Inference" (paper digest), "Method".
+ *
+ * Conventions shared by every call
+ *   - Tensors are dense, row-major, in DEVICE memory owned by the caller.  The
+ *     library allocates nothing on the device, keeps no state between calls
+ *     except a per-thread copy of the last error text and a per-thread cache
+ *     of the alpha tables, and is safe to call from several host threads.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is only enqueued: nothing synchronises, so results are
+ *     ready when the stream reaches them.
+ *   - Every argument is checked on the host before anything is enqueued; a
+ *     failed check launches nothing and returns a negative lynx_status.
+ *     lynx_last_error() then holds a one-line reason.  A launch failure
+ *     returns LYNX_ECUDA with the CUDA error text.  Device-side faults are not
+ *     turned into status codes (they surface on the stream, as in CUDA).
+ *   - Shapes: a KV tensor is kv[B][L][H_kv][D] BF16 with B = 2 * layers (or
+ *     any batch of independent tensors), L tokens, H_kv heads, D = 128
+ *     channels per head.  It is cut into page blocks of `page` tokens x D
+ *     channels of one head, ordered (b, page index, head).
+ *   - Encoded streams, per page block, contiguous, in block order:
+ *       anchor   [B][L/page][H_kv][page][D/2] bytes   (4-bit Anchor codes)
+ *       residual [B][L/page][H_kv][page][D/2] bytes   (4-bit Residual codes)
+ *       meta     [B][L/page][H_kv][2 + 2*page/C][D] float32:
+ *                gamma_min[D], gamma_scale[D], mu[page/C][D], sigma[page/C][D]
+ *     Within a token row of D/2 bytes, byte 4G+k holds channel 8G+k in its low
+ *     nibble and channel 8G+k+4 in its high nibble.  Anchor<<4 | Residual is
+ *     the 8-bit two's-complement code Q8 = I*S + min(S, 0) of Eq. 9, I the
+ *     7-bit magnitude code and S the sign.
+ *   - Limits: D == 128; page in {64, 128, 256}; C in {16, 32, 64, 128},
+ *     C <= page; L % page == 0; B * L < 2^31; alpha finite and > 0; every
+ *     pointer 16-byte aligned.
+ */
+#ifndef LYNX_H
+#define LYNX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LYNX_OK = 0,
+    LYNX_EINVAL = -1,       /* null or misaligned pointer, bad alpha or enum */
+    LYNX_ESHAPE = -2,       /* inconsistent sizes (L % page, C, T, heads ...) */
+    LYNX_EUNSUPPORTED = -3, /* valid but not built: D != 128, page/C outside the list */
+    LYNX_ECUDA = -4,        /* a CUDA call or launch failed */
+    LYNX_EWORKSPACE = -5    /* workspace smaller than lynx_attn_workspace_bytes */
+} lynx_status;
+
+typedef enum { LYNX_ANCHOR = 0, LYNX_FULL = 1 } lynx_mode;
+typedef enum { LYNX_OUT_BF16 = 0, LYNX_OUT_FP32 = 1 } lynx_dtype;
+
+/* Host-only.  Byte sizes of the three encoded streams for a kv[B][L][H_kv][D]
+ * tensor (see the layout above; meta holds 2 + 2*page/C float32 rows of D per
+ * page block, [Review, "Why Not Global Grouped Quantization?"]).  Any output
+ * pointer may be NULL.  Returns LYNX_OK or a shape/limit error. */
+int lynx_encoded_sizes(int64_t B, int64_t L, int H_kv, int D, int page, int C,
+                       size_t *anchor_bytes, size_t *residual_bytes,
+                       size_t *meta_bytes);
+
+/* Encode: Algorithm 1 [Review, Mechanism 1] on every page block.
+ *   Stage 1: per channel, gamma_min = min over the page, gamma_scale =
+ *            max - min, n = (x - gamma_min) * rn(1/(gamma_scale + 1e-6)).
+ *   Stage 2: per chunk of C tokens and channel, mu = mean(n) (pairwise-halving
+ *            sum), sigma = max|n - mu|, x_final = (n - mu) * rn(1/(sigma+1e-6)).
+ *   Stage 3: I = Round(127 ln(1 + alpha|x_final|) / ln(1 + alpha)) (Eq. 7),
+ *            S = sign(n - mu) (+1 at zero).
+ *   Stage 4: Q8 = I*S + min(S,0) (Eq. 9); Anchor = Q8 >> 4, Residual = Q8 & 15.
+ * Statistics are float32 with one rounding per operation in the order above;
+ * Round is exact with respect to the float64 value of Eq. 7.
+ *   kv        [B][L][H_kv][D] BF16, device, read only
+ *   anchor    device, lynx_encoded_sizes() bytes, written
+ *   residual  device, written
+ *   meta      device float32, written                                      */
+int lynx_encode(const void *kv, int64_t B, int64_t L, int H_kv, int D,
+                int page, int C, float alpha, void *anchor, void *residual,
+                float *meta, void *stream);
+
+/* Anchor-only decode [Review, Mechanism 2, decode side Anchor Phase:
+ * "Q_approx = dequant(Q_anc, gamma, mu, sigma)"]: the signed Anchor gives S
+ * and V = I >> 4; the value is S * X(16V + 7), X(y) = ((1+alpha)^(y/127) - 1)
+ * / alpha (the geometric-interval exponent of [Digest, Method]; Eq. 14), then
+ *   n = fma(S*X, sigma + 1e-6, mu);  x = fma(n, gamma_scale + 1e-6, gamma_min)
+ * with X(.) rounded once to float32 from float64.
+ *   out  [B][L][H_kv][D], BF16 (round to nearest even) or FP32, device.     */
+int lynx_decode_anchor(const void *anchor, const float *meta, int64_t B,
+                       int64_t L, int H_kv, int D, int page, int C,
+                       float alpha, void *out, int out_dtype, void *stream);
+
+/* Full decode [Review, Mechanism 2, Residual Phase: "Q_full =
+ * dequant(Q_anc + Q_res)"; Eq. 15]: Q8 = Anchor<<4 | Residual gives S and I
+ * exactly; value S * X(I), then the same two fused multiply-adds.          */
+int lynx_decode_full(const void *anchor, const void *residual,
+                     const float *meta, int64_t B, int64_t L, int H_kv, int D,
+                     int page, int C, float alpha, void *out, int out_dtype,
+                     void *stream);
+
+/* Host-only.  Device workspace (bytes) that lynx_attn_decode needs for these
+ * sizes: split-K partial results, float32.  0 is never returned for valid
+ * sizes.  Returns LYNX_OK or a shape/limit error. */
+int lynx_attn_workspace_bytes(int batch, int T, int H_q, int64_t L, int H_kv,
+                              int D, int page, size_t *bytes);
+
+/* Decode attention over packed KV [Review, Prerequisites Eq. 1]:
+ *   O = softmax(q K^T / sqrt(D)) V
+ * for every sequence, query row and query head, grouped-query: query head hq
+ * reads KV head hq / (H_q / H_kv).  K and V are reconstructed in registers
+ * exactly as lynx_decode_anchor (mode LYNX_ANCHOR, the draft step of
+ * [Review, Mechanism 2, Anchor Phase]) or lynx_decode_full (LYNX_FULL, the
+ * T-token verification pass of [Review, Mechanism 3]) would with BF16 output;
+ * every one of the T query rows attends to all L cached tokens.
+ *   q          [batch][T][H_q][D] BF16, device
+ *   k_*, v_*   the encode outputs of the K and V tensors [batch][L][H_kv][D]
+ *              (B = batch); k_residual / v_residual may be NULL in ANCHOR mode
+ *   out        [batch][T][H_q][D] float32, device, written
+ *   workspace  device scratch of >= lynx_attn_workspace_bytes(...) bytes; its
+ *              contents on entry do not matter and are clobbered
+ * Limits: 1 <= T, H_q % H_kv == 0, (H_q / H_kv) * T <= 32, C >= 16, L >= 1. */
+int lynx_attn_decode(const void *q, int batch, int T, int H_q,
+                     const void *k_anchor, const void *k_residual,
+                     const float *k_meta, const void *v_anchor,
+                     const void *v_residual, const float *v_meta, int64_t L,
+                     int H_kv, int D, int page, int C, float alpha, int mode,
+                     float *out, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/* Host-only.  The 127 rounding thresholds of Stage 3 for this alpha:
+ * thresholds[k] is the smallest float32 a >= 0 whose Eq. 7 value (float64)
+ * rounds to more than k, so Round(Y(a)) = #{k : a >= thresholds[k]}.
+ * The encode kernel decides every code this way.  Returns LYNX_OK/EINVAL. */
+int lynx_compander_thresholds(float alpha, float thresholds[127]);
+
+/* Host-only.  The 128 reconstruction magnitudes X(I) = ((1+alpha)^(I/127)-1)
+ * / alpha (Eq. 14/15), float64 rounded to float32, used by both decoders. */
+int lynx_expand_table(float alpha, float table[128]);
+
+/* Checks the encoder's fast Stage-3 rounding against the thresholds for every
+ * float32 a in [0, 1] on the device, for this alpha.  counts (device, 4 x
+ * uint64, zeroed by the call): [0] values checked, [1] values whose fast
+ * result was not exact and was not flagged for the exact path (must be 0),
+ * [2] values flagged for the exact path, [3] max |fast Y - exact Y| in units
+ * of 2^-32 (an error bound of the approximation).  Enqueued on `stream`. */
+int lynx_compander_selfcheck(float alpha, uint64_t *counts, void *stream);
+
+/* Host call, synchronous: *flag = 1 if any kernel of this library in this
+ * process gave up a bounded wait on an asynchronous copy (it then returned
+ * early and its outputs are incomplete), else 0. */
+int lynx_wait_timeouts(unsigned int *flag);
+
+/* Text of a status code, and of the last failure on this host thread. */
+const char *lynx_status_string(int code);
+const char *lynx_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LYNX_H */

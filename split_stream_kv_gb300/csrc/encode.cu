@@ -1,0 +1,490 @@
+// encode.cu -- Algorithm 1 of "Lynx: Progressive Speculative KV Cache Transfer
+// for Disaggregated LLM Inference" (technical review, Mechanism 1, Stages 1-4)
+// as one persistent sm_103a kernel.
+//
+// Work unit: one page block = `page` tokens x 128 channels of one KV head.
+// A 2D TMA load stages the block's BF16 tile (page x 256 bytes, rows strided
+// by H*256 bytes in HBM) in shared memory; up to three tiles are in flight per
+// CTA while the CTA computes on an earlier one.
+//
+// Thread layout for a block (2*page threads): lane = 16*e1 + g.  g selects 8
+// channels (16 bytes of a row, 4 bytes of each packed row); a thread holds 8
+// tokens of one chunk.  With WPC = C/16 warps per chunk, chunk c = warp/WPC,
+// u = warp%WPC, and register m holds chunk token i = m*2*WPC + e1*WPC + u.
+// The chunk mean's pairwise-halving sum (v[i] += v[i+h], h = C/2 .. 1) then
+// reduces the register index first (top bits of i), then e1 (shuffle xor 16),
+// then u (shared memory), which is exactly the order the oracle uses.
+//
+// Arithmetic, each step one IEEE binary32 rounding (no contraction):
+//   gmin = min x (a zero minimum as -0), gmax = max x, gs = gmax - gmin,
+//   rg = rn(1/(gs + eps)), n = (x - gmin) * rg,
+//   mu = tree_sum(n) * (1/C), d = n - mu, sg = max|d|, rs = rn(1/(sg + eps)),
+//   a = |d * rs|, S = sign(d) (+1 at zero).
+// Stage 3 (Eq. 7) is decided against the float64 thresholds of the host:
+// a fast MUFU log2 path gives the code unless its value lies within
+// kAmbiguityK * 2^-16 of a rounding boundary; then the threshold decides.
+// Stage 4 (Eq. 9 at 8 bits): code8 = S > 0 ? I : 255 - I; Anchor = code8 >> 4,
+// Residual = code8 & 15, packed two channels (8G+k, 8G+k+4) per byte.
+#include "common.cuh"
+#include "internal.h"
+
+namespace lynx {
+
+// Set by a kernel whose bounded wait on a TMA stage gave up (the kernel then
+// returns early).  Read through read_wait_timeout(); never reset.
+__device__ unsigned int g_wait_timeout = 0;
+
+cudaError_t read_wait_timeout(unsigned int* flag) {
+  return cudaMemcpyFromSymbol(flag, g_wait_timeout, sizeof(unsigned int));
+}
+
+// s = floor((Y' + 1/2) * 65536 + K) + 2^23 with Y' = lg * c16 / 65536.
+// Byte 2 of the bits is the code (Y' + 1/2 < 128), the low 16 bits locate
+// the value relative to the rounding boundary.
+constexpr float kC0 = 8388608.0f + 32768.0f + (float)kAmbiguityK;
+
+__device__ __forceinline__ uint32_t compand_fast(float a, float alpha, float c16) {
+  const float t = fmaf(alpha, a, 1.0f);
+  const float l = lg2_approx(t);
+  return __float_as_uint(fma_rm(l, c16, kC0));
+}
+__device__ __forceinline__ bool compand_ambiguous(uint32_t bits) {
+  return (bits & 0xffffu) < 2u * kAmbiguityK;
+}
+// Exact code from the thresholds, for a value flagged ambiguous.
+__device__ __forceinline__ uint32_t compand_exact(uint32_t bits, float a, const float* thr) {
+  int I = (int)((bits >> 16) & 0xffu);
+  int b = I > 0 ? I - 1 : 0;
+  return (uint32_t)(b + (a >= thr[b] ? 1 : 0));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+template <int P, int C>
+struct EncGeom {
+  static constexpr int kThreads = 2 * P;
+  static constexpr int kWarps = P / 16;
+  static constexpr int kNC = P / C;
+  static constexpr int kWPC = C / 16;
+  static constexpr int kTileBytes = P * kD * 2;
+  static constexpr int kStages = kTileBytes <= 32768 ? 3 : 2;
+  static constexpr int kMetaRows = 2 + 2 * kNC;
+  static constexpr int kRedFloats = kWarps * kD * (kWPC > 1 ? 4 : 2) + 2 * kD;
+  static constexpr size_t kSmem =
+      (size_t)kStages * kTileBytes + (size_t)kRedFloats * 4 + kStages * 8;
+  static_assert(C >= 16 && C <= P, "chunk");
+  static_assert(P >= 64 && P <= 256, "page");
+};
+
+template <int P, int C>
+__global__ void __launch_bounds__(2 * P, 256 / P)
+encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
+              const int64_t NB, const int H, const int64_t L,
+              uint32_t* __restrict__ anchor, uint32_t* __restrict__ residual,
+              float* __restrict__ meta, const __grid_constant__ CompanderTable tab) {
+  using G = EncGeom<P, C>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* tiles = smem;
+  float* red_mn = reinterpret_cast<float*>(smem + G::kStages * G::kTileBytes);
+  float* red_mx = red_mn + G::kWarps * kD;
+  float* red_sum = red_mx + G::kWarps * kD;      // used when WPC > 1
+  float* red_sg = red_sum + G::kWarps * kD;      // used when WPC > 1
+  float* st_gmin = red_mn + G::kWarps * kD * (G::kWPC > 1 ? 4 : 2);
+  float* st_rg = st_gmin + kD;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(st_rg + kD);
+
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const int g = lane & 15, e1 = lane >> 4;
+  const int c = w / G::kWPC, u = w % G::kWPC;
+
+  if (tid == 0) {
+    for (int i = 0; i < G::kStages; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int64_t blk, int stage) {
+    const int64_t h = blk % H, rest = blk / H;
+    const int64_t p = rest % NB, b = rest / NB;
+    mbar_expect_tx(&bars[stage], G::kTileBytes);
+    tma_load_2d(tiles + stage * G::kTileBytes, &tmap, (int32_t)(h * kD),
+                (int32_t)(b * L + p * P), &bars[stage]);
+  };
+  if (tid == 0)
+    for (int i = 0; i < G::kStages; ++i) {
+      const int64_t blk = blockIdx.x + (int64_t)i * gridDim.x;
+      if (blk < nblk) issue(blk, i);
+    }
+
+  const float alpha = tab.alpha, c16 = tab.c16;
+  const float inv_C = 1.0f / (float)C;
+  int it = 0;
+  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+    const int stage = it % G::kStages;
+    const uint32_t phase = (uint32_t)(it / G::kStages) & 1u;
+    const bool ok = mbar_wait(&bars[stage], phase);
+    const uint4* tile = reinterpret_cast<const uint4*>(tiles + stage * G::kTileBytes);
+
+    // ---- Stage 1a: per-channel page min / max (exact, on bf16 pairs)
+    uint32_t mn[4], mx[4];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int t = c * C + m * 2 * G::kWPC + e1 * G::kWPC + u;
+      const uint4 v = tile[t * 16 + g];
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mn[k] = m == 0 ? vv[k] : bf2_min(mn[k], vv[k]);
+        mx[k] = m == 0 ? vv[k] : bf2_max(mx[k], vv[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      mn[k] = bf2_min(mn[k], __shfl_xor_sync(kFull, mn[k], 16));
+      mx[k] = bf2_max(mx[k], __shfl_xor_sync(kFull, mx[k], 16));
+    }
+    if (e1 == 0) {
+      float4* pm = reinterpret_cast<float4*>(red_mn + w * kD + 8 * g);
+      float4* px = reinterpret_cast<float4*>(red_mx + w * kD + 8 * g);
+      const f2 a0 = bf2_to_f2(mn[0]), a1 = bf2_to_f2(mn[1]);
+      const f2 a2 = bf2_to_f2(mn[2]), a3 = bf2_to_f2(mn[3]);
+      pm[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
+      pm[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
+      const f2 b0 = bf2_to_f2(mx[0]), b1 = bf2_to_f2(mx[1]);
+      const f2 b2 = bf2_to_f2(mx[2]), b3 = bf2_to_f2(mx[3]);
+      px[0] = make_float4(b0.x, b0.y, b1.x, b1.y);
+      px[1] = make_float4(b2.x, b2.y, b3.x, b3.y);
+    }
+    if (!__syncthreads_and(ok)) {
+      // A stage never arrived: record it and stop this CTA (bounded waits
+      // only, so the context stays usable).
+      if (tid == 0) {
+        atomicExch(&g_wait_timeout, 1u);
+        for (int i = 0; i < G::kStages; ++i) (void)mbar_wait(&bars[i], phase);
+      }
+      return;
+    }
+
+    // ---- Stage 1b: gamma_min, gamma_scale, reciprocal (one thread/channel)
+    float* mrow = meta + blk * (int64_t)(G::kMetaRows * kD);
+    if (tid < kD) {
+      float lo = red_mn[tid], hi = red_mx[tid];
+#pragma unroll
+      for (int ww = 1; ww < G::kWarps; ++ww) {
+        lo = fminf(lo, red_mn[ww * kD + tid]);
+        hi = fmaxf(hi, red_mx[ww * kD + tid]);
+      }
+      // one sign for a zero extreme: -0 for the minimum (zero x then centre
+      // to +0), +0 for the maximum
+      if (lo == 0.0f) lo = -0.0f;
+      if (hi == 0.0f) hi = 0.0f;
+      const float gs = __fsub_rn(hi, lo);
+      st_gmin[tid] = lo;
+      st_rg[tid] = __frcp_rn(__fadd_rn(gs, kEps));
+      mrow[tid] = lo;
+      mrow[kD + tid] = gs;
+    }
+    __syncthreads();
+
+    // ---- Stage 1c: n = (x - gmin) * rg for the thread's 8 tokens x 8 ch
+    f2 gm2[4], rg2[4];
+    {
+      const float4* sg4 = reinterpret_cast<const float4*>(st_gmin + 8 * g);
+      const float4* sr4 = reinterpret_cast<const float4*>(st_rg + 8 * g);
+      const float4 q0 = sg4[0], q1 = sg4[1], r0 = sr4[0], r1 = sr4[1];
+      gm2[0] = {q0.x, q0.y}; gm2[1] = {q0.z, q0.w};
+      gm2[2] = {q1.x, q1.y}; gm2[3] = {q1.z, q1.w};
+      rg2[0] = {r0.x, r0.y}; rg2[1] = {r0.z, r0.w};
+      rg2[2] = {r1.x, r1.y}; rg2[3] = {r1.z, r1.w};
+    }
+    f2 n[8][4];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int t = c * C + m * 2 * G::kWPC + e1 * G::kWPC + u;
+      const uint4 v = tile[t * 16 + g];
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) n[m][k] = mul2(sub2(bf2_to_f2(vv[k]), gm2[k]), rg2[k]);
+    }
+    __syncthreads();  // every thread is done with this stage's tile
+    if (tid == 0) {
+      const int64_t nxt = blk + (int64_t)G::kStages * gridDim.x;
+      if (nxt < nblk) {
+        fence_proxy_async();
+        issue(nxt, stage);
+      }
+    }
+
+    // ---- Stage 2a: chunk mean, pairwise-halving order
+    f2 mu2[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f2 t0 = add2(n[0][k], n[4][k]), t1 = add2(n[1][k], n[5][k]);
+      f2 t2 = add2(n[2][k], n[6][k]), t3 = add2(n[3][k], n[7][k]);
+      t0 = add2(t0, t2);
+      t1 = add2(t1, t3);
+      f2 s = add2(t0, t1);
+      f2 o;
+      o.x = __shfl_xor_sync(kFull, s.x, 16);
+      o.y = __shfl_xor_sync(kFull, s.y, 16);
+      mu2[k] = add2(s, o);
+    }
+    if constexpr (G::kWPC > 1) {
+      if (e1 == 0) {
+        float4* ps = reinterpret_cast<float4*>(red_sum + w * kD + 8 * g);
+        ps[0] = make_float4(mu2[0].x, mu2[0].y, mu2[1].x, mu2[1].y);
+        ps[1] = make_float4(mu2[2].x, mu2[2].y, mu2[3].x, mu2[3].y);
+      }
+      __syncthreads();
+      f2 part[G::kWPC][4];
+#pragma unroll
+      for (int uu = 0; uu < G::kWPC; ++uu) {
+        const float4* ps =
+            reinterpret_cast<const float4*>(red_sum + (c * G::kWPC + uu) * kD + 8 * g);
+        const float4 a = ps[0], b = ps[1];
+        part[uu][0] = {a.x, a.y}; part[uu][1] = {a.z, a.w};
+        part[uu][2] = {b.x, b.y}; part[uu][3] = {b.z, b.w};
+      }
+#pragma unroll
+      for (int h = G::kWPC / 2; h >= 1; h /= 2)
+#pragma unroll
+        for (int uu = 0; uu < h; ++uu)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) part[uu][k] = add2(part[uu][k], part[uu + h][k]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mu2[k] = part[0][k];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) mu2[k] = mul2(mu2[k], f2{inv_C, inv_C});
+
+    // ---- Stage 2b: d = n - mu, sigma = max |d|
+    float sg[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sg[i] = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        n[m][k] = sub2(n[m][k], mu2[k]);
+        sg[2 * k] = fmaxf(sg[2 * k], fabsf(n[m][k].x));
+        sg[2 * k + 1] = fmaxf(sg[2 * k + 1], fabsf(n[m][k].y));
+      }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) sg[i] = fmaxf(sg[i], __shfl_xor_sync(kFull, sg[i], 16));
+    if constexpr (G::kWPC > 1) {
+      if (e1 == 0) {
+        float4* ps = reinterpret_cast<float4*>(red_sg + w * kD + 8 * g);
+        ps[0] = make_float4(sg[0], sg[1], sg[2], sg[3]);
+        ps[1] = make_float4(sg[4], sg[5], sg[6], sg[7]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int uu = 0; uu < G::kWPC; ++uu) {
+        const float4* ps =
+            reinterpret_cast<const float4*>(red_sg + (c * G::kWPC + uu) * kD + 8 * g);
+        const float4 a = ps[0], b = ps[1];
+        sg[0] = fmaxf(sg[0], a.x); sg[1] = fmaxf(sg[1], a.y);
+        sg[2] = fmaxf(sg[2], a.z); sg[3] = fmaxf(sg[3], a.w);
+        sg[4] = fmaxf(sg[4], b.x); sg[5] = fmaxf(sg[5], b.y);
+        sg[6] = fmaxf(sg[6], b.z); sg[7] = fmaxf(sg[7], b.w);
+      }
+    }
+    if (e1 == 0 && u == 0) {
+      float4* pmu = reinterpret_cast<float4*>(mrow + (2 + c) * kD + 8 * g);
+      float4* psg = reinterpret_cast<float4*>(mrow + (2 + G::kNC + c) * kD + 8 * g);
+      pmu[0] = make_float4(mu2[0].x, mu2[0].y, mu2[1].x, mu2[1].y);
+      pmu[1] = make_float4(mu2[2].x, mu2[2].y, mu2[3].x, mu2[3].y);
+      psg[0] = make_float4(sg[0], sg[1], sg[2], sg[3]);
+      psg[1] = make_float4(sg[4], sg[5], sg[6], sg[7]);
+    }
+    f2 rs2[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      rs2[k].x = __frcp_rn(__fadd_rn(sg[2 * k], kEps));
+      rs2[k].y = __frcp_rn(__fadd_rn(sg[2 * k + 1], kEps));
+    }
+
+    // ---- Stages 3-4: codes, sign map, nibble split, store one row per m
+    uint32_t* arow = anchor + blk * (int64_t)(P * 16);
+    uint32_t* rrow = residual + blk * (int64_t)(P * 16);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int t = c * C + m * 2 * G::kWPC + e1 * G::kWPC + u;
+      float a[8];
+      uint32_t bits[8], dbits[8];
+      bool amb = false;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const f2 xf = mul2(n[m][k], rs2[k]);
+        a[2 * k] = fabsf(xf.x);
+        a[2 * k + 1] = fabsf(xf.y);
+        dbits[2 * k] = __float_as_uint(n[m][k].x);
+        dbits[2 * k + 1] = __float_as_uint(n[m][k].y);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        bits[i] = compand_fast(a[i], alpha, c16);
+        amb |= compand_ambiguous(bits[i]);
+      }
+      if (__any_sync(kFull, amb)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (compand_ambiguous(bits[i]))
+            bits[i] = (bits[i] & 0xff00ffffu) | (compand_exact(bits[i], a[i], tab.thr) << 16);
+      }
+      // code bytes (byte 2 of bits) xor the replicated sign of d
+      const uint32_t i01 = prmt(bits[0], bits[1], 0x0062u), i23 = prmt(bits[2], bits[3], 0x0062u);
+      const uint32_t i45 = prmt(bits[4], bits[5], 0x0062u), i67 = prmt(bits[6], bits[7], 0x0062u);
+      const uint32_t s01 = prmt(dbits[0], dbits[1], 0x00fbu), s23 = prmt(dbits[2], dbits[3], 0x00fbu);
+      const uint32_t s45 = prmt(dbits[4], dbits[5], 0x00fbu), s67 = prmt(dbits[6], dbits[7], 0x00fbu);
+      const uint32_t W0 = prmt(i01 ^ s01, i23 ^ s23, 0x5410u);
+      const uint32_t W1 = prmt(i45 ^ s45, i67 ^ s67, 0x5410u);
+      // byte k: Anchor = (ch k high nibble) | (ch k+4 high nibble) << 4, etc.
+      const uint32_t Aw = ((W0 >> 4) & 0x0f0f0f0fu) | (W1 & 0xf0f0f0f0u);
+      const uint32_t Rw = (W0 & 0x0f0f0f0fu) | ((W1 << 4) & 0xf0f0f0f0u);
+      arow[t * 16 + g] = Aw;
+      rrow[t * 16 + g] = Rw;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ launch
+
+using EncodeFn = void (*)(const CUtensorMap, int64_t, int64_t, int, int64_t, uint32_t*,
+                          uint32_t*, float*, const CompanderTable);
+
+template <int P, int C>
+static cudaError_t run_encode(const CUtensorMap& map, const Shape& s, const CompanderTable& tab,
+                              void* anchor, void* residual, float* meta, cudaStream_t stream) {
+  using G = EncGeom<P, C>;
+  auto fn = encode_kernel<P, C>;
+  static thread_local int configured_dev = -1;
+  static thread_local int per_sm = 1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kSmem);
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, G::kThreads, G::kSmem);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+    configured_dev = dev;
+  }
+  const int64_t nblk = s.blocks();
+  int64_t grid = (int64_t)sm_count() * per_sm;
+  if (grid > nblk) grid = nblk;
+  fn<<<(unsigned)grid, G::kThreads, G::kSmem, stream>>>(
+      map, nblk, s.NB(), s.H, s.L, static_cast<uint32_t*>(anchor),
+      static_cast<uint32_t*>(residual), meta, tab);
+  return cudaGetLastError();
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+static EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return (EncodeTiledFn) nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+cudaError_t launch_encode(const void* kv, const Shape& s, const CompanderTable& tab,
+                          void* anchor, void* residual, float* meta, cudaStream_t stream) {
+  if (s.blocks() == 0) return cudaSuccess;
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)s.H * kD, (cuuint64_t)(s.B * s.L)};
+  const cuuint64_t strides[1] = {(cuuint64_t)s.H * kD * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)s.page};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+#define LYNX_ENC_CASE(PP, CC) \
+  if (s.page == PP && s.C == CC) return run_encode<PP, CC>(map, s, tab, anchor, residual, meta, stream);
+  LYNX_ENC_CASE(64, 16) LYNX_ENC_CASE(64, 32) LYNX_ENC_CASE(64, 64)
+  LYNX_ENC_CASE(128, 16) LYNX_ENC_CASE(128, 32) LYNX_ENC_CASE(128, 64) LYNX_ENC_CASE(128, 128)
+  LYNX_ENC_CASE(256, 16) LYNX_ENC_CASE(256, 32) LYNX_ENC_CASE(256, 64) LYNX_ENC_CASE(256, 128)
+#undef LYNX_ENC_CASE
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------ self-check
+
+// For every float32 a in [0, 1]: fast path vs threshold count.
+__global__ void compander_selfcheck_kernel(const __grid_constant__ CompanderTable tab,
+                                           unsigned long long* counts) {
+  __shared__ float thr[128];
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) thr[i] = tab.thr[i];
+  __syncthreads();
+  const uint32_t last = 0x3f800000u;  // bits of 1.0f
+  unsigned long long n = 0, bad = 0, amb = 0, maxerr = 0;
+  const double la = log1p((double)tab.alpha);
+  for (uint64_t ub = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; ub <= last;
+       ub += (uint64_t)gridDim.x * blockDim.x) {
+    const float a = __uint_as_float((uint32_t)ub);
+    const uint32_t bits = compand_fast(a, tab.alpha, tab.c16);
+    int lo = 0, hi = 127;  // exact: number of thresholds <= a
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (a >= thr[mid]) lo = mid + 1; else hi = mid;
+    }
+    const uint32_t exact = (uint32_t)lo;
+    ++n;
+    if (compand_ambiguous(bits)) {
+      ++amb;
+      if (compand_exact(bits, a, thr) != exact) ++bad;
+    } else if (((bits >> 16) & 0xffu) != exact) {
+      ++bad;
+    }
+    // approximation error of Y' = lg * c16 / 65536 against float64 Y
+    const double y = 127.0 * log1p((double)tab.alpha * (double)a) / la;
+    const double yf = (double)lg2_approx(fmaf(tab.alpha, a, 1.0f)) * (double)tab.c16 / 65536.0;
+    const double err = fabs(yf - y) * 4294967296.0;
+    const unsigned long long e = (unsigned long long)(err < 1.8e19 ? err : 1.8e19);
+    if (e > maxerr) maxerr = e;
+  }
+  // warp reduce then one atomic per warp
+  for (int o = 16; o; o >>= 1) {
+    n += __shfl_xor_sync(kFull, n, o);
+    bad += __shfl_xor_sync(kFull, bad, o);
+    amb += __shfl_xor_sync(kFull, amb, o);
+    const unsigned long long m2 = __shfl_xor_sync(kFull, maxerr, o);
+    maxerr = m2 > maxerr ? m2 : maxerr;
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&counts[0], n);
+    atomicAdd(&counts[1], bad);
+    atomicAdd(&counts[2], amb);
+    atomicMax(&counts[3], maxerr);
+  }
+}
+
+cudaError_t launch_compander_selfcheck(const CompanderTable& tab, uint64_t* counts,
+                                       cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(counts, 0, 4 * sizeof(uint64_t), stream);
+  if (e != cudaSuccess) return e;
+  compander_selfcheck_kernel<<<sm_count() * 8, 256, 0, stream>>>(
+      tab, reinterpret_cast<unsigned long long*>(counts));
+  return cudaGetLastError();
+}
+
+}  // namespace lynx

@@ -1,0 +1,64 @@
+// internal.h -- host-side interfaces between the C ABI and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lynx {
+
+// Stage-3 tables for one alpha, built on the host in float64.
+struct CompanderTable {
+  float alpha;
+  float c16;        // 65536 * 127 / log2(1 + alpha), float32
+  float thr[128];   // thr[k] = smallest float32 a with Round(Y(a)) > k; thr[127] = +inf
+};
+
+// Reconstruction magnitudes X(I) = ((1+alpha)^(I/127) - 1)/alpha, I = 0..127.
+struct ExpandTable {
+  float x[128];
+};
+
+// Fast-path rounding window of the encoder, in units of 2^-16 of Y:
+// results within this distance of a half-integer take the exact path.
+constexpr uint32_t kAmbiguityK = 8;
+
+struct Shape {
+  int64_t B, L;
+  int H, D, page, C;
+  int64_t NB() const { return L / page; }
+  int64_t blocks() const { return B * NB() * H; }
+  int NC() const { return page / C; }
+};
+
+// Launchers: validated arguments, enqueue on `stream`, return a cudaError_t.
+cudaError_t launch_encode(const void* kv, const Shape& s, const CompanderTable& tab,
+                          void* anchor, void* residual, float* meta, cudaStream_t stream);
+cudaError_t launch_decode(const void* anchor, const void* residual, const float* meta,
+                          const Shape& s, const ExpandTable& tab, void* out, bool bf16_out,
+                          cudaStream_t stream);
+cudaError_t launch_compander_selfcheck(const CompanderTable& tab, uint64_t* counts,
+                                       cudaStream_t stream);
+
+struct AttnArgs {
+  const void* q;
+  int batch, T, H_q;
+  const void *k_anchor, *k_residual;
+  const float* k_meta;
+  const void *v_anchor, *v_residual;
+  const float* v_meta;
+  Shape s;           // B = batch
+  bool full;
+  float* out;
+  void* workspace;
+};
+size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L);
+cudaError_t launch_attn(const AttnArgs& a, const ExpandTable& tab, cudaStream_t stream);
+
+// Host read of the device flag set when a bounded wait gave up.
+cudaError_t read_wait_timeout(unsigned int* flag);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+}  // namespace lynx

@@ -1,0 +1,296 @@
+// lynx_api.cu -- the extern "C" boundary declared in include/lynx.h: argument
+// checks, the float64 alpha tables, and dispatch to the kernel launchers.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "lynx.h"
+
+namespace lynx {
+
+static thread_local char g_last_error[256] = "";
+
+static int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+static int cuda_fail(cudaError_t e, const char* what) {
+  return fail(LYNX_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int sm_count() {
+  static thread_local int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
+// ---------------------------------------------------------- alpha tables
+
+// Round(Y(a)) of Eq. 7 with Y in float64: 127 ln(1 + alpha a) / ln(1 + alpha).
+static int round_code(float a, double al) {
+  const double y = 127.0 * log1p(al * (double)a) / log1p(al);
+  double r = floor(y + 0.5);
+  if (r < 0.0) r = 0.0;
+  if (r > 127.0) r = 127.0;
+  return (int)r;
+}
+
+static void build_thresholds(float alpha, float thr[128]) {
+  const double al = (double)alpha;
+  const double lal = log1p(al);
+  for (int k = 0; k < 127; ++k) {
+    // smallest float a >= 0 with Round(Y(a)) >= k + 1: start at the real
+    // boundary X(k + 1/2) and walk float neighbours until it is exact
+    float c = (float)(expm1((k + 0.5) * lal / 127.0) / al);
+    if (!(c >= 0.0f)) c = 0.0f;
+    if (c > 1.0f) c = 1.0f;
+    if (round_code(c, al) >= k + 1) {
+      while (c > 0.0f) {
+        const float prev = nextafterf(c, 0.0f);
+        if (round_code(prev, al) >= k + 1) c = prev; else break;
+      }
+    } else {
+      while (c < 1.0f && round_code(c, al) < k + 1) c = nextafterf(c, 2.0f);
+    }
+    thr[k] = c;
+  }
+  thr[127] = INFINITY;
+}
+
+static void build_expand(float alpha, float x[128]) {
+  const double al = (double)alpha;
+  for (int I = 0; I < 128; ++I) x[I] = (float)((pow(1.0 + al, (double)I / 127.0) - 1.0) / al);
+}
+
+// Per-thread cache of the last alpha's tables (building them costs a few us).
+struct AlphaCache {
+  uint32_t bits = 0xffffffffu;
+  CompanderTable comp;
+  ExpandTable expand;
+};
+static const AlphaCache& tables_for(float alpha) {
+  static thread_local AlphaCache cache;
+  uint32_t b;
+  memcpy(&b, &alpha, 4);
+  if (b != cache.bits) {
+    cache.comp.alpha = alpha;
+    cache.comp.c16 = (float)(65536.0 * 127.0 / log2(1.0 + (double)alpha));
+    build_thresholds(alpha, cache.comp.thr);
+    build_expand(alpha, cache.expand.x);
+    cache.bits = b;
+  }
+  return cache;
+}
+
+// ---------------------------------------------------------- validation
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_alpha(float alpha) {
+  if (!(alpha > 0.0f) || !isfinite(alpha)) return fail(LYNX_EINVAL, "alpha must be finite and > 0");
+  return LYNX_OK;
+}
+
+static int check_codec_shape(int64_t B, int64_t L, int H, int D, int page, int C) {
+  if (B < 0 || L < 0 || H <= 0) return fail(LYNX_ESHAPE, "need B >= 0, L >= 0, H_kv >= 1");
+  if (D != kD) return fail(LYNX_EUNSUPPORTED, "D = %d: only D = 128 is built", D);
+  if (page != 64 && page != 128 && page != 256)
+    return fail(LYNX_EUNSUPPORTED, "page = %d: built for 64, 128, 256", page);
+  if (C <= 0 || (C & (C - 1))) return fail(LYNX_ESHAPE, "C = %d must be a power of two", C);
+  if (C < 16 || C > 128 || C > page)
+    return fail(LYNX_EUNSUPPORTED, "C = %d: built for 16..128 and C <= page", C);
+  if (L % page) return fail(LYNX_ESHAPE, "L = %lld is not a multiple of page = %d", (long long)L, page);
+  if (B * L > (int64_t)0x7fffffff) return fail(LYNX_EUNSUPPORTED, "B*L must be < 2^31 tokens");
+  return LYNX_OK;
+}
+
+static int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps) {
+    if (!p) return fail(LYNX_EINVAL, "null pointer");
+    if (!aligned16(p)) return fail(LYNX_EINVAL, "pointer not 16-byte aligned");
+  }
+  return LYNX_OK;
+}
+
+static void codec_sizes(int64_t B, int64_t L, int H, int D, int page, int C, size_t* a,
+                        size_t* r, size_t* m) {
+  const size_t elems = (size_t)B * (size_t)L * (size_t)H * (size_t)D;
+  const size_t blocks = (size_t)B * (size_t)(L / page) * (size_t)H;
+  if (a) *a = elems / 2;
+  if (r) *r = elems / 2;
+  if (m) *m = blocks * (size_t)(2 + 2 * (page / C)) * (size_t)D * sizeof(float);
+}
+
+}  // namespace lynx
+
+using namespace lynx;
+
+extern "C" {
+
+const char* lynx_status_string(int code) {
+  switch (code) {
+    case LYNX_OK: return "ok";
+    case LYNX_EINVAL: return "invalid argument";
+    case LYNX_ESHAPE: return "inconsistent shape";
+    case LYNX_EUNSUPPORTED: return "unsupported configuration";
+    case LYNX_ECUDA: return "CUDA error";
+    case LYNX_EWORKSPACE: return "workspace too small";
+    default: return "unknown status";
+  }
+}
+
+const char* lynx_last_error(void) { return g_last_error; }
+
+int lynx_encoded_sizes(int64_t B, int64_t L, int H_kv, int D, int page, int C,
+                       size_t* anchor_bytes, size_t* residual_bytes, size_t* meta_bytes) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, C);
+  if (rc) return rc;
+  codec_sizes(B, L, H_kv, D, page, C, anchor_bytes, residual_bytes, meta_bytes);
+  return LYNX_OK;
+}
+
+int lynx_compander_thresholds(float alpha, float thresholds[127]) {
+  if (!thresholds) return fail(LYNX_EINVAL, "null pointer");
+  int rc = check_alpha(alpha);
+  if (rc) return rc;
+  const AlphaCache& t = tables_for(alpha);
+  memcpy(thresholds, t.comp.thr, 127 * sizeof(float));
+  return LYNX_OK;
+}
+
+int lynx_expand_table(float alpha, float table[128]) {
+  if (!table) return fail(LYNX_EINVAL, "null pointer");
+  int rc = check_alpha(alpha);
+  if (rc) return rc;
+  memcpy(table, tables_for(alpha).expand.x, 128 * sizeof(float));
+  return LYNX_OK;
+}
+
+int lynx_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page, int C,
+                float alpha, void* anchor, void* residual, float* meta, void* stream) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, C);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if ((rc = check_ptrs({kv, anchor, residual, meta}))) return rc;
+  Shape s{B, L, H_kv, D, page, C};
+  cudaError_t e = launch_encode(kv, s, tables_for(alpha).comp, anchor, residual, meta,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_encode");
+}
+
+static int decode_common(const void* anchor, const void* residual, const float* meta, int64_t B,
+                         int64_t L, int H_kv, int D, int page, int C, float alpha, void* out,
+                         int out_dtype, void* stream, const char* what) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, C);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)
+    return fail(LYNX_EINVAL, "out_dtype must be LYNX_OUT_BF16 or LYNX_OUT_FP32");
+  if ((rc = check_ptrs({anchor, meta, out}))) return rc;
+  if (residual && (rc = check_ptrs({residual}))) return rc;
+  Shape s{B, L, H_kv, D, page, C};
+  cudaError_t e = launch_decode(anchor, residual, meta, s, tables_for(alpha).expand, out,
+                                out_dtype == LYNX_OUT_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, what);
+}
+
+int lynx_decode_anchor(const void* anchor, const float* meta, int64_t B, int64_t L, int H_kv,
+                       int D, int page, int C, float alpha, void* out, int out_dtype,
+                       void* stream) {
+  return decode_common(anchor, nullptr, meta, B, L, H_kv, D, page, C, alpha, out, out_dtype,
+                       stream, "lynx_decode_anchor");
+}
+
+int lynx_decode_full(const void* anchor, const void* residual, const float* meta, int64_t B,
+                     int64_t L, int H_kv, int D, int page, int C, float alpha, void* out,
+                     int out_dtype, void* stream) {
+  if (!residual) return fail(LYNX_EINVAL, "null pointer");
+  return decode_common(anchor, residual, meta, B, L, H_kv, D, page, C, alpha, out, out_dtype,
+                       stream, "lynx_decode_full");
+}
+
+static int check_attn_shape(int batch, int T, int H_q, int64_t L, int H_kv, int D, int page,
+                            int C) {
+  int rc = check_codec_shape(batch, L, H_kv, D, page, C);
+  if (rc) return rc;
+  if (batch < 1 || L < 1) return fail(LYNX_ESHAPE, "attention needs batch >= 1 and L >= 1");
+  if (T < 1) return fail(LYNX_ESHAPE, "T = %d must be >= 1", T);
+  if (H_q < 1 || H_q % H_kv) return fail(LYNX_ESHAPE, "H_q = %d is not a multiple of H_kv = %d", H_q, H_kv);
+  if ((H_q / H_kv) * T > 32)
+    return fail(LYNX_EUNSUPPORTED, "(H_q/H_kv)*T = %d: at most 32 query rows per KV head", (H_q / H_kv) * T);
+  return LYNX_OK;
+}
+
+int lynx_attn_workspace_bytes(int batch, int T, int H_q, int64_t L, int H_kv, int D, int page,
+                              size_t* bytes) {
+  if (!bytes) return fail(LYNX_EINVAL, "null pointer");
+  int rc = check_attn_shape(batch, T, H_q, L, H_kv, D, page, page < 16 ? page : 16);
+  if (rc) return rc;
+  *bytes = attn_workspace_bytes(batch, T, H_q, H_kv, L);
+  return LYNX_OK;
+}
+
+int lynx_attn_decode(const void* q, int batch, int T, int H_q, const void* k_anchor,
+                     const void* k_residual, const float* k_meta, const void* v_anchor,
+                     const void* v_residual, const float* v_meta, int64_t L, int H_kv, int D,
+                     int page, int C, float alpha, int mode, float* out, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  int rc = check_attn_shape(batch, T, H_q, L, H_kv, D, page, C);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if (mode != LYNX_ANCHOR && mode != LYNX_FULL)
+    return fail(LYNX_EINVAL, "mode must be LYNX_ANCHOR or LYNX_FULL");
+  if ((rc = check_ptrs({q, k_anchor, k_meta, v_anchor, v_meta, out, workspace}))) return rc;
+  if (mode == LYNX_FULL && (rc = check_ptrs({k_residual, v_residual}))) return rc;
+  const size_t need = attn_workspace_bytes(batch, T, H_q, H_kv, L);
+  if (workspace_bytes < need)
+    return fail(LYNX_EWORKSPACE, "workspace %zu bytes < %zu needed", workspace_bytes, need);
+  AttnArgs a;
+  a.q = q;
+  a.batch = batch;
+  a.T = T;
+  a.H_q = H_q;
+  a.k_anchor = k_anchor;
+  a.k_residual = mode == LYNX_FULL ? k_residual : nullptr;
+  a.k_meta = k_meta;
+  a.v_anchor = v_anchor;
+  a.v_residual = mode == LYNX_FULL ? v_residual : nullptr;
+  a.v_meta = v_meta;
+  a.s = Shape{batch, L, H_kv, D, page, C};
+  a.full = mode == LYNX_FULL;
+  a.out = out;
+  a.workspace = workspace;
+  cudaError_t e = launch_attn(a, tables_for(alpha).expand, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_attn_decode");
+}
+
+int lynx_compander_selfcheck(float alpha, uint64_t* counts, void* stream) {
+  int rc = check_alpha(alpha);
+  if (rc) return rc;
+  if ((rc = check_ptrs({counts}))) return rc;
+  cudaError_t e = launch_compander_selfcheck(tables_for(alpha).comp, counts,
+                                             static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_compander_selfcheck");
+}
+
+int lynx_wait_timeouts(unsigned int* flag) {
+  if (!flag) return fail(LYNX_EINVAL, "null pointer");
+  cudaError_t e = read_wait_timeout(flag);
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_wait_timeouts");
+}
+
+}  // extern "C"

@@ -1,0 +1,222 @@
+"""ctypes binding of liblynx.so (include/lynx.h), one Python function per C
+entry point with the same name.  Only argument marshalling happens here:
+tensors become device pointers and sizes, the current CUDA stream is passed
+along, and output tensors are allocated with torch when the caller gives none.
+There is no CPU path: non-CUDA tensors are rejected.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblynx.so")
+
+LYNX_OK, LYNX_EINVAL, LYNX_ESHAPE, LYNX_EUNSUPPORTED, LYNX_ECUDA, LYNX_EWORKSPACE = (
+    0, -1, -2, -3, -4, -5)
+LYNX_ANCHOR, LYNX_FULL = 0, 1
+LYNX_OUT_BF16, LYNX_OUT_FP32 = 0, 1
+
+_lib = None
+
+
+class LynxError(RuntimeError):
+    def __init__(self, code: int, what: str, detail: str):
+        super().__init__(f"{what}: {detail} ({code})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load liblynx.so (build it first with split_stream_kv_gb300._build)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "split_stream_kv_gb300._build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I64, I, F, SZ = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                        ctypes.c_size_t)
+    PSZ = ctypes.POINTER(ctypes.c_size_t)
+    sig = {
+        "lynx_encoded_sizes": ([I64, I64, I, I, I, I, PSZ, PSZ, PSZ], I),
+        "lynx_encode": ([P, I64, I64, I, I, I, I, F, P, P, P, P], I),
+        "lynx_decode_anchor": ([P, P, I64, I64, I, I, I, I, F, P, I, P], I),
+        "lynx_decode_full": ([P, P, P, I64, I64, I, I, I, I, F, P, I, P], I),
+        "lynx_attn_workspace_bytes": ([I, I, I, I64, I, I, I, PSZ], I),
+        "lynx_attn_decode": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P, SZ, P],
+                             I),
+        "lynx_compander_thresholds": ([F, P], I),
+        "lynx_expand_table": ([F, P], I),
+        "lynx_compander_selfcheck": ([F, P, P], I),
+        "lynx_wait_timeouts": ([ctypes.POINTER(ctypes.c_uint)], I),
+        "lynx_status_string": ([I], ctypes.c_char_p),
+        "lynx_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def _check(rc: int, what: str):
+    if rc != LYNX_OK:
+        detail = lib().lynx_last_error().decode(errors="replace")
+        raise LynxError(rc, what, detail)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("lynx: tensors must be contiguous CUDA tensors")
+
+
+# ----------------------------------------------------------------- codec
+
+def lynx_encoded_sizes(B: int, L: int, H_kv: int, D: int, page: int, C: int):
+    a, r, m = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().lynx_encoded_sizes(B, L, H_kv, D, page, C, ctypes.byref(a), ctypes.byref(r),
+                                    ctypes.byref(m)), "lynx_encoded_sizes")
+    return a.value, r.value, m.value
+
+
+def stream_shapes(B: int, L: int, H_kv: int, D: int, page: int, C: int):
+    """Tensor shapes of (anchor, residual, meta) for a kv[B][L][H_kv][D]."""
+    NB = L // page
+    codes = (B, NB, H_kv, page, D // 2)
+    return codes, codes, (B, NB, H_kv, 2 + 2 * (page // C), D)
+
+
+def lynx_encode(kv: torch.Tensor, page: int, C: int, alpha: float, anchor=None, residual=None,
+                meta=None):
+    """Encode kv[B][L][H_kv][D] (bf16, CUDA).  Returns (anchor, residual, meta)."""
+    _need_cuda(kv, anchor, residual, meta)
+    if kv.dtype != torch.bfloat16 or kv.dim() != 4:
+        raise ValueError("lynx_encode: kv must be a 4-D bfloat16 tensor")
+    B, L, H, D = kv.shape
+    ca, cr, cm = stream_shapes(B, L, H, D, page, C)
+    dev = kv.device
+    if anchor is None:
+        anchor = torch.empty(ca, dtype=torch.uint8, device=dev)
+    if residual is None:
+        residual = torch.empty(cr, dtype=torch.uint8, device=dev)
+    if meta is None:
+        meta = torch.empty(cm, dtype=torch.float32, device=dev)
+    _check(lib().lynx_encode(_ptr(kv), B, L, H, D, page, C, alpha, _ptr(anchor), _ptr(residual),
+                             _ptr(meta), _stream(dev)), "lynx_encode")
+    return anchor, residual, meta
+
+
+def _decode_out(anchor, L, out_dtype, out):
+    B, NB, H, page, half = anchor.shape
+    if out is None:
+        out = torch.empty((B, L, H, half * 2), dtype=out_dtype, device=anchor.device)
+    code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("lynx decode: output must be bfloat16 or float32")
+    return out, code, B, H, page, half * 2
+
+
+def lynx_decode_anchor(anchor, meta, L: int, page: int, C: int, alpha: float,
+                       out_dtype=torch.bfloat16, out=None):
+    """Anchor-only reconstruction -> out[B][L][H_kv][D]."""
+    _need_cuda(anchor, meta, out)
+    out, code, B, H, P, D = _decode_out(anchor, L, out_dtype, out)
+    _check(lib().lynx_decode_anchor(_ptr(anchor), _ptr(meta), B, L, H, D, page, C, alpha,
+                                    _ptr(out), code, _stream(anchor.device)),
+           "lynx_decode_anchor")
+    return out
+
+
+def lynx_decode_full(anchor, residual, meta, L: int, page: int, C: int, alpha: float,
+                     out_dtype=torch.bfloat16, out=None):
+    """Anchor + Residual reconstruction -> out[B][L][H_kv][D]."""
+    _need_cuda(anchor, residual, meta, out)
+    out, code, B, H, P, D = _decode_out(anchor, L, out_dtype, out)
+    _check(lib().lynx_decode_full(_ptr(anchor), _ptr(residual), _ptr(meta), B, L, H, D, page, C,
+                                  alpha, _ptr(out), code, _stream(anchor.device)),
+           "lynx_decode_full")
+    return out
+
+
+# ----------------------------------------------------------------- attention
+
+def lynx_attn_workspace_bytes(batch: int, T: int, H_q: int, L: int, H_kv: int, D: int,
+                              page: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().lynx_attn_workspace_bytes(batch, T, H_q, L, H_kv, D, page, ctypes.byref(n)),
+           "lynx_attn_workspace_bytes")
+    return n.value
+
+
+def lynx_attn_decode(q, k_streams, v_streams, L: int, page: int, C: int, alpha: float,
+                     mode: int, out=None, workspace=None):
+    """q[batch][T][H_q][D] bf16; k_streams / v_streams = (anchor, residual or
+    None, meta) from lynx_encode of K and V.  Returns out[batch][T][H_q][D] f32."""
+    ka, kr, km = k_streams
+    va, vr, vm = v_streams
+    _need_cuda(q, ka, kr, km, va, vr, vm, out, workspace)
+    if q.dtype != torch.bfloat16 or q.dim() != 4:
+        raise ValueError("lynx_attn_decode: q must be a 4-D bfloat16 tensor")
+    batch, T, H_q, D = q.shape
+    H_kv = ka.shape[2]
+    if out is None:
+        out = torch.empty((batch, T, H_q, D), dtype=torch.float32, device=q.device)
+    need = lynx_attn_workspace_bytes(batch, T, H_q, L, H_kv, D, page)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().lynx_attn_decode(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr), _ptr(km),
+                                  _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D, page, C, alpha,
+                                  mode, _ptr(out), _ptr(workspace), workspace.numel(),
+                                  _stream(q.device)), "lynx_attn_decode")
+    return out
+
+
+# ----------------------------------------------------------------- tables
+
+def lynx_compander_thresholds(alpha: float):
+    buf = (ctypes.c_float * 127)()
+    _check(lib().lynx_compander_thresholds(alpha, ctypes.cast(buf, ctypes.c_void_p)),
+           "lynx_compander_thresholds")
+    return list(buf)
+
+
+def lynx_expand_table(alpha: float):
+    buf = (ctypes.c_float * 128)()
+    _check(lib().lynx_expand_table(alpha, ctypes.cast(buf, ctypes.c_void_p)),
+           "lynx_expand_table")
+    return list(buf)
+
+
+def lynx_compander_selfcheck(alpha: float, device="cuda"):
+    """[values checked, wrong unflagged, flagged, max |error| in 2^-32 of Y]."""
+    counts = torch.zeros(4, dtype=torch.int64, device=device)
+    _check(lib().lynx_compander_selfcheck(alpha, _ptr(counts), _stream(counts.device)),
+           "lynx_compander_selfcheck")
+    return [int(v) for v in counts.cpu().tolist()]
+
+
+def lynx_wait_timeouts() -> int:
+    flag = ctypes.c_uint()
+    _check(lib().lynx_wait_timeouts(ctypes.byref(flag)), "lynx_wait_timeouts")
+    return flag.value
+
+
+def lynx_status_string(code: int) -> str:
+    return lib().lynx_status_string(code).decode()
+
+
+def lynx_last_error() -> str:
+    return lib().lynx_last_error().decode(errors="replace")

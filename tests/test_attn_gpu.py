@@ -1,0 +1,104 @@
+"""Parity of the packed-KV decode attention (through the C ABI) with the
+oracle: float64 softmax(q K^T / sqrt(128)) V over the oracle's own decode of
+the same packed streams, rounded to BF16 (the values the kernel sees).
+
+Tolerance: outputs can be as large as the outlier channels of V (|v| up to
+~1e3), so the 2e-3 max-abs bound is applied to the error divided by
+max(1, max_t |V_t,d|) per (sequence, head, channel), and to the raw error of
+the channels whose values stay below 16.
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ALPHA = 255.0
+TOL = 2e-3
+
+
+def _decode_seq_head(oracle_mod, streams, b, h, L, P, C, full):
+    """Oracle decode of all pages of (sequence b, head h) -> float32 [L][128]
+    holding BF16-rounded values."""
+    anc, res, meta = streams
+    NB = L // P
+    out = np.empty((L, 128), np.float32)
+    for p in range(NB):
+        x = oracle_mod.decode_block(anc[b, p, h], res[b, p, h] if full else None,
+                                    meta[b, p, h], C, ALPHA)
+        out[p * P:(p + 1) * P] = oracle_mod.bf16_bits_to_f32(
+            oracle_mod.f32_to_bf16_bits(x)).reshape(P, 128)
+    return out
+
+
+def _check(oracle_mod, q, k_np, v_np, out, L, P, C, full, pairs, H_q, H_kv, T):
+    G = H_q // H_kv
+    qf = q.float().cpu().numpy()
+    o = out.cpu().numpy()
+    worst = 0.0
+    for b, h in pairs:
+        K = _decode_seq_head(oracle_mod, k_np, b, h, L, P, C, full)
+        V = _decode_seq_head(oracle_mod, v_np, b, h, L, P, C, full)
+        norm = np.maximum(1.0, np.abs(V).max(axis=0))
+        small = np.abs(V).max(axis=0) < 16
+        for t in range(T):
+            for gq in range(G):
+                hq = h * G + gq
+                ref = oracle_mod.attention_row(qf[b, t, hq], K, V)
+                err = np.abs(o[b, t, hq].astype(np.float64) - ref)
+                rel = (err / norm).max()
+                worst = max(worst, rel)
+                assert rel <= TOL, (b, t, hq, rel)
+                if small.any():
+                    assert err[small].max() <= TOL, (b, t, hq, err[small].max())
+    return worst
+
+
+def _run(lynx_lib, oracle_mod, dev, batch, L, H_kv, H_q, T, P, C, pairs, seed=0):
+    from split_stream_kv_gb300 import synth
+    kv = synth.kv_cache(2 * batch, L, H_kv, 128, seed=seed, device=dev)
+    k = kv[0::2].contiguous()
+    v = kv[1::2].contiguous()
+    ks = lynx_lib.lynx_encode(k, P, C, ALPHA)
+    vs = lynx_lib.lynx_encode(v, P, C, ALPHA)
+    k_np = tuple(t.cpu().numpy() for t in ks)
+    v_np = tuple(t.cpu().numpy() for t in vs)
+    results = {}
+    for mode, TT in ((lynx_lib.LYNX_ANCHOR, 1), (lynx_lib.LYNX_FULL, T)):
+        q = synth.queries(batch, TT, H_q, 128, seed=seed + TT, device=dev)
+        full = mode == lynx_lib.LYNX_FULL
+        ksm = ks if full else (ks[0], None, ks[2])
+        vsm = vs if full else (vs[0], None, vs[2])
+        out = lynx_lib.lynx_attn_decode(q, ksm, vsm, L, P, C, ALPHA, mode)
+        torch.cuda.synchronize()
+        assert torch.isfinite(out).all()
+        results[mode] = _check(oracle_mod, q, k_np, v_np, out, L, P, C, full, pairs, H_q, H_kv, TT)
+    return results
+
+
+def test_tiny_single_head(lynx_lib, oracle_mod, cuda_dev):
+    """1 layer, 1 KV head, 1 query head, L=256, page 256, C 32."""
+    r = _run(lynx_lib, oracle_mod, cuda_dev, 1, 256, 1, 1, 8, 256, 32, [(0, 0)])
+    print(r)
+
+
+def test_gqa_groups_and_row_groups(lynx_lib, oracle_mod, cuda_dev):
+    """4 query heads per KV head; T=8 gives 32 query rows (4 row groups)."""
+    pairs = [(0, 0), (0, 1), (1, 0), (1, 1)]
+    r = _run(lynx_lib, oracle_mod, cuda_dev, 2, 1024, 2, 8, 8, 128, 32, pairs, seed=3)
+    print(r)
+
+
+@pytest.mark.parametrize("P,C,L", [(64, 16, 1024), (256, 64, 2048), (128, 128, 512),
+                                   (128, 16, 640)])
+def test_page_and_chunk_sizes(lynx_lib, oracle_mod, cuda_dev, P, C, L):
+    _run(lynx_lib, oracle_mod, cuda_dev, 1, L, 2, 4, 2, P, C, [(0, 0), (0, 1)], seed=P + C)
+
+
+def test_decode_attention_full_size_sampled(lynx_lib, oracle_mod, cuda_dev):
+    """8 sequences x 32768 tokens, 32 query heads over 8 KV heads: draft step
+    (T=1, Anchor) and verification (T=8, Anchor+Residual); three sampled
+    (sequence, KV head) pairs checked on every query row."""
+    pairs = [(0, 0), (3, 5), (7, 7)]
+    r = _run(lynx_lib, oracle_mod, cuda_dev, 8, 32768, 8, 32, 8, 128, 32, pairs, seed=5)
+    print(r)
