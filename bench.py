@@ -15,6 +15,8 @@ bandwidth, and decode-attention tokens/s.
 Flags: --gpus N (one replica per rank under torchrun; weak scaling),
 --steps K, --warmup W, --impl {lynx,reference}.  --impl reference times the
 CPU oracle (the only reference this path has) on a bounded sample.
+Profiling aids: --rows a,b selects rows; --small shrinks both workloads (codec
+B = 8, attention batch 2; still larger than L2) and skips the e2e and CPU legs.
 """
 from __future__ import annotations
 
@@ -212,6 +214,22 @@ def cpu_sample_run(target_s: float = 12.0, threads: int | None = None):
 
 # ----------------------------------------------------------------- GPU leg
 
+def max_over_ranks(vals, world, device=None):
+    """Max of each value over all ranks (a timing reduction, not data)."""
+    if world <= 1:
+        return list(vals)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(vals), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_gbps(step_bytes_per_rank, world, seconds_per_step):
+    """Weak scaling: every rank processes its own workload."""
+    return world * step_bytes_per_rank / seconds_per_step / 1e9
+
+
 def run_lynx(args, rank, world, dev):
     import torch
 
@@ -255,6 +273,7 @@ def run_lynx(args, rank, world, dev):
 
     launches_per_step = {"encode": 1, "decode_anchor": 1, "decode_full": 1, "attn_draft": 2,
                          "attn_verify": 2}
+    rows_run = [r for r in ROWS if r in args.rows]
     stream = torch.cuda.current_stream(dev)
 
     def barrier():
@@ -262,7 +281,7 @@ def run_lynx(args, rank, world, dev):
             torch.distributed.barrier()
 
     for _ in range(args.warmup):
-        for r in ROWS:
+        for r in rows_run:
             row(r)
     torch.cuda.synchronize(dev)
 
@@ -272,7 +291,7 @@ def run_lynx(args, rank, world, dev):
     except Exception:
         uuid = None
     # ---- device-timed region
-    ev = {r: [] for r in ROWS}
+    ev = {r: [] for r in rows_run}
     barrier()
     torch.cuda.synchronize(dev)
     clocks = ClockSampler(uuid if rank == 0 else None)
@@ -280,7 +299,7 @@ def run_lynx(args, rank, world, dev):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for _ in range(args.steps):
-        for r in ROWS:
+        for r in rows_run:
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -292,7 +311,12 @@ def run_lynx(args, rank, world, dev):
     barrier()
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
-    row_ms = {r: sum(e0.elapsed_time(e1) for e0, e1 in ev[r]) / args.steps for r in ROWS}
+    row_ms = {r: sum(e0.elapsed_time(e1) for e0, e1 in ev[r]) / args.steps for r in rows_run}
+    launches = sum(launches_per_step[r] for r in rows_run) * args.steps
+    if args.small or rows_run != ROWS:
+        ms_total, = max_over_ranks([ms_total], world, dev)
+        return dict(ms_total=ms_total, row_ms=row_ms, e2e_s=None, h2d=0, d2h=0, clocks=clk,
+                    launches=launches)
 
     # ---- end to end: pinned host buffers in, results out, every step
     kv_h = torch.empty(kv.shape, dtype=kv.dtype, pin_memory=True)
@@ -338,13 +362,10 @@ def run_lynx(args, rank, world, dev):
     barrier()
     e2e_s = (time.perf_counter() - w0) / e2e_steps
 
-    if world > 1:
-        t = torch.tensor([ms_total, e2e_s], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total, e2e_s = float(t[0]), float(t[1])
+    ms_total, e2e_s = max_over_ranks([ms_total, e2e_s], world, dev)
     assert lynx.lynx_wait_timeouts() == 0
     return dict(ms_total=ms_total, row_ms=row_ms, e2e_s=e2e_s, h2d=h2d, d2h=d2h, clocks=clk,
-                launches=sum(launches_per_step.values()) * args.steps)
+                launches=launches)
 
 
 def main():
@@ -354,7 +375,16 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["lynx", "reference"], default="lynx")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--rows", default=",".join(ROWS), help="comma-separated subset of rows")
+    ap.add_argument("--small", action="store_true", help="small workloads for profiling")
     args = ap.parse_args()
+    args.rows = [r for r in args.rows.split(",") if r]
+    unknown = [r for r in args.rows if r not in ROWS]
+    if unknown:
+        ap.error(f"unknown rows {unknown}")
+    if args.small:
+        CODEC["B"] = 8
+        ATTN["batch"] = 2
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -380,11 +410,12 @@ def main():
         be = bf16_equiv_bytes()
         alg = algorithmic_bytes()
         peak, peak_kind = load_peaks()
+        run_rows = list(r["row_ms"].keys())
         step_ms = r["ms_total"] / args.steps
-        step_bytes = sum(be.values())
-        value = world * step_bytes / (step_ms / 1e3) / 1e9
+        step_bytes = sum(be[n] for n in run_rows)
+        value = whole_job_gbps(step_bytes, world, step_ms / 1e3)
         rows = {}
-        for name in ROWS:
+        for name in run_rows:
             ms = r["row_ms"][name]
             ach = alg[name] / (ms / 1e3) / 1e9
             d = {"ms": round(ms, 4), "bf16_equiv_GBps": round(be[name] / (ms / 1e3) / 1e9, 1),
@@ -395,7 +426,7 @@ def main():
                 d["tokens_per_s"] = round(ATTN["batch"] * T / (ms / 1e3), 1)
                 d["context_tokens_per_s"] = round(ATTN["batch"] * ATTN["L"] / (ms / 1e3), 1)
             rows[name] = d
-        dom = max(ROWS, key=lambda n: r["row_ms"][n])
+        dom = max(run_rows, key=lambda n: r["row_ms"][n])
         ach = alg[dom] / (r["row_ms"][dom] / 1e3) / 1e9
         line = {
             "metric": METRIC,
@@ -412,16 +443,20 @@ def main():
             "data": "synthetic",
             "config": workload_config(),
             "rows": rows,
-            "anchor_attention_tokens_per_s": rows["attn_draft"]["tokens_per_s"],
+            "anchor_attention_tokens_per_s": rows.get("attn_draft", {}).get("tokens_per_s"),
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(ach / peak, 4), "traffic": None},
-            "e2e": {"value": round(world * step_bytes / r["e2e_s"] / 1e9, 2), "unit": "GB/s",
-                    "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
+            "e2e": None if r["e2e_s"] is None else {
+                "value": round(whole_job_gbps(step_bytes, world, r["e2e_s"]), 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
-        if world == 1 and not args.no_cpu:
+        if args.small:
+            line["config"]["workload"] = "SMALL profiling case: " + line["config"]["workload"]
+            line["config"]["small"] = {"codec_B": CODEC["B"], "attn_batch": ATTN["batch"]}
+        if world == 1 and not args.no_cpu and not args.small:
             v, cores, desc, _ = cpu_sample_run()
             line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores,
                                     "kind": "oracle", "sample": desc}

@@ -17,7 +17,9 @@
  *     stream).  Work is only enqueued: nothing synchronises, so results are
  *     ready when the stream reaches them.
  *   - Every argument is checked on the host before anything is enqueued; a
- *     failed check launches nothing and returns a negative lynx_status.
+ *     failed check launches nothing and returns a negative lynx_status.  A
+ *     codec call on an empty tensor (B * L == 0) enqueues nothing and returns
+ *     LYNX_OK without examining the pointers.
  *     lynx_last_error() then holds a one-line reason.  A launch failure
  *     returns LYNX_ECUDA with the CUDA error text.  Device-side faults are not
  *     turned into status codes (they surface on the stream, as in CUDA).

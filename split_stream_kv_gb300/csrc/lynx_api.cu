@@ -185,6 +185,7 @@ int lynx_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page,
   int rc = check_codec_shape(B, L, H_kv, D, page, C);
   if (rc) return rc;
   if ((rc = check_alpha(alpha))) return rc;
+  if (B * L == 0) return LYNX_OK;  // nothing to encode; pointers are not examined
   if ((rc = check_ptrs({kv, anchor, residual, meta}))) return rc;
   Shape s{B, L, H_kv, D, page, C};
   cudaError_t e = launch_encode(kv, s, tables_for(alpha).comp, anchor, residual, meta,
@@ -200,6 +201,7 @@ static int decode_common(const void* anchor, const void* residual, const float* 
   if ((rc = check_alpha(alpha))) return rc;
   if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)
     return fail(LYNX_EINVAL, "out_dtype must be LYNX_OUT_BF16 or LYNX_OUT_FP32");
+  if (B * L == 0) return LYNX_OK;  // nothing to decode; pointers are not examined
   if ((rc = check_ptrs({anchor, meta, out}))) return rc;
   if (residual && (rc = check_ptrs({residual}))) return rc;
   Shape s{B, L, H_kv, D, page, C};
@@ -218,7 +220,7 @@ int lynx_decode_anchor(const void* anchor, const float* meta, int64_t B, int64_t
 int lynx_decode_full(const void* anchor, const void* residual, const float* meta, int64_t B,
                      int64_t L, int H_kv, int D, int page, int C, float alpha, void* out,
                      int out_dtype, void* stream) {
-  if (!residual) return fail(LYNX_EINVAL, "null pointer");
+  if (!residual && B * L != 0) return fail(LYNX_EINVAL, "null pointer");
   return decode_common(anchor, residual, meta, B, L, H_kv, D, page, C, alpha, out, out_dtype,
                        stream, "lynx_decode_full");
 }
