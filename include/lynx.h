@@ -136,6 +136,29 @@ int lynx_attn_decode(const void *q, int batch, int T, int H_q,
                      float *out, void *workspace, size_t workspace_bytes,
                      void *stream);
 
+/* lynx_attn_decode without a caller-provided workspace, for callers that
+ * cannot allocate device memory: code that runs while a stream is being
+ * captured into a CUDA graph, real-time or signal paths that must not enter an
+ * allocator, and hosts whose memory manager forbids driver allocations after
+ * start-up.  The split-K scratch is a fixed 8 MiB array in the library's
+ * device image (static, one per GPU that loads the library, held until the
+ * process exits); sizes that need more than that (lynx_attn_workspace_bytes
+ * > 8 MiB) fail with LYNX_EWORKSPACE.  The paper has no counterpart: this is
+ * an interface of this library only.
+ * The first call on a device looks the array's address up once (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Nothing is allocated or freed.  All calls share the one array
+ * and it keeps the last call's contents (no state needs clearing: every
+ * partial is written before it is read), so calls whose work overlaps on the
+ * GPU race with each other: issue them on one stream, or order them.
+ * Arguments, results and the other errors are those of lynx_attn_decode. */
+int lynx_attn_decode_noalloc(const void *q, int batch, int T, int H_q,
+                             const void *k_anchor, const void *k_residual,
+                             const float *k_meta, const void *v_anchor,
+                             const void *v_residual, const float *v_meta,
+                             int64_t L, int H_kv, int D, int page, int C,
+                             float alpha, int mode, float *out, void *stream);
+
 /* Host-only.  The 127 rounding thresholds of Stage 3 for this alpha:
  * thresholds[k] is the smallest float32 a >= 0 whose Eq. 7 value (float64)
  * rounds to more than k, so Round(Y(a)) = #{k : a >= thresholds[k]}.

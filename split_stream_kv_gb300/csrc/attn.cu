@@ -25,9 +25,13 @@
 // own running max / sum / output; the CTA merges its 4 warps and writes one
 // partial (m, l, o) per split; attn_combine merges the splits.
 #include <math.h>
+#include <stdio.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
+#include "lynx.h"
 
 namespace lynx {
 
@@ -487,3 +491,72 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
 }
 
 }  // namespace lynx
+
+// ------------------------------------------------- allocation-free variant
+//
+// Some callers cannot call cudaMalloc at all: code running while a CUDA graph
+// is being captured on a stream, real-time or signal-safe paths that must not
+// enter the allocator, and hosts whose memory manager forbids driver
+// allocations after start-up.  For them lynx_attn_decode_noalloc uses a fixed
+// scratch array that lives in this library's device image, so the caller only
+// passes inputs and outputs.
+
+namespace lynx {
+
+// Split-K partials of one call.  Every GPU that loads the library holds it
+// until the process exits.
+constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
+static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
+
+// Device address of g_attn_scratch for the current device, looked up once
+// per device (cudaGetSymbolAddress with that device current) and cached.
+static cudaError_t noalloc_scratch(void** ptr) {
+  constexpr int kMaxDev = 64;
+  static void* addr[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *ptr = addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace lynx
+
+extern "C" int lynx_attn_decode_noalloc(const void* q, int batch, int T, int H_q,
+                                        const void* k_anchor, const void* k_residual,
+                                        const float* k_meta, const void* v_anchor,
+                                        const void* v_residual, const float* v_meta, int64_t L,
+                                        int H_kv, int D, int page, int C, float alpha, int mode,
+                                        float* out, void* stream) {
+  size_t need = 0;
+  int rc = lynx_attn_workspace_bytes(batch, T, H_q, L, H_kv, D, page, &need);
+  if (rc != LYNX_OK) return rc;
+  if (need > lynx::kNoAllocScratchBytes) {
+    char msg[160];
+    snprintf(msg, sizeof msg,
+             "lynx_attn_decode_noalloc: these sizes need %zu bytes of scratch, more than the "
+             "built-in %zu; use lynx_attn_decode with a workspace",
+             need, lynx::kNoAllocScratchBytes);
+    return lynx::report_error(LYNX_EWORKSPACE, msg);
+  }
+  void* scratch = nullptr;
+  cudaError_t e = lynx::noalloc_scratch(&scratch);
+  if (e != cudaSuccess) {
+    char msg[160];
+    snprintf(msg, sizeof msg, "lynx_attn_decode_noalloc: scratch address: %s",
+             cudaGetErrorString(e));
+    return lynx::report_error(LYNX_ECUDA, msg);
+  }
+  return lynx_attn_decode(q, batch, T, H_q, k_anchor, k_residual, k_meta, v_anchor, v_residual,
+                          v_meta, L, H_kv, D, page, C, alpha, mode, out, scratch,
+                          lynx::kNoAllocScratchBytes, stream);
+}

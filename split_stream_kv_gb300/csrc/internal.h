@@ -55,6 +55,9 @@ struct AttnArgs {
 size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L);
 cudaError_t launch_attn(const AttnArgs& a, const ExpandTable& tab, cudaStream_t stream);
 
+// Record `msg` as this thread's last error and return `code`.
+int report_error(int code, const char* msg);
+
 // Host read of the device flag set when a bounded wait gave up.
 cudaError_t read_wait_timeout(unsigned int* flag);
 

@@ -20,6 +20,8 @@ static int fail(int code, const char* fmt, ...) {
   va_end(ap);
   return code;
 }
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 static int cuda_fail(cudaError_t e, const char* what) {
   return fail(LYNX_ECUDA, "%s: %s", what, cudaGetErrorString(e));
 }

@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
         "lynx_attn_workspace_bytes": ([I, I, I, I64, I, I, I, PSZ], I),
         "lynx_attn_decode": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P, SZ, P],
                              I),
+        "lynx_attn_decode_noalloc": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P],
+                                     I),
         "lynx_compander_thresholds": ([F, P], I),
         "lynx_expand_table": ([F, P], I),
         "lynx_compander_selfcheck": ([F, P, P], I),
@@ -181,6 +183,28 @@ def lynx_attn_decode(q, k_streams, v_streams, L: int, page: int, C: int, alpha: 
                                   _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D, page, C, alpha,
                                   mode, _ptr(out), _ptr(workspace), workspace.numel(),
                                   _stream(q.device)), "lynx_attn_decode")
+    return out
+
+
+def lynx_attn_decode_noalloc(q, k_streams, v_streams, L: int, page: int, C: int,
+                             alpha: float, mode: int, out=None):
+    """lynx_attn_decode with the library's built-in scratch instead of a
+    workspace (for callers that cannot allocate device memory).  `out` must
+    be given by such callers; if it is None it is allocated here for
+    convenience."""
+    ka, kr, km = k_streams
+    va, vr, vm = v_streams
+    _need_cuda(q, ka, kr, km, va, vr, vm, out)
+    if q.dtype != torch.bfloat16 or q.dim() != 4:
+        raise ValueError("lynx_attn_decode_noalloc: q must be a 4-D bfloat16 tensor")
+    batch, T, H_q, D = q.shape
+    H_kv = ka.shape[2]
+    if out is None:
+        out = torch.empty((batch, T, H_q, D), dtype=torch.float32, device=q.device)
+    _check(lib().lynx_attn_decode_noalloc(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr), _ptr(km),
+                                          _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D, page, C,
+                                          alpha, mode, _ptr(out), _stream(q.device)),
+           "lynx_attn_decode_noalloc")
     return out
 
 
