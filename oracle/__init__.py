@@ -45,44 +45,85 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.oracle_compand_y.argtypes = [F, F]
+    lib.oracle_compand_y.restype = ctypes.c_double
+    lib.oracle_round_code.argtypes = [F, F]
+    lib.oracle_round_code.restype = I
+    lib.oracle_expand.argtypes = [I, F]
+    lib.oracle_expand.restype = F
+    lib.oracle_stage4_literal.argtypes = [I, I, P]
+    lib.oracle_stage4_literal.restype = None
+    lib.oracle_code8.argtypes = [I, I]
+    lib.oracle_code8.restype = I
+    lib.oracle_anchor_nibble.argtypes = [I]
+    lib.oracle_anchor_nibble.restype = I
+    lib.oracle_residual_nibble.argtypes = [I]
+    lib.oracle_residual_nibble.restype = I
+    lib.oracle_f32_to_bf16.argtypes = [F]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_encode_block.argtypes = [P, I64, I, I, I, F, P, P, P]
+    lib.oracle_encode_block.restype = I
+    lib.oracle_encode_range.argtypes = [P, I64, I64, I, I, I, I, F, P, P, P,
+                                        I64, I64]
+    lib.oracle_encode_range.restype = I
+    lib.oracle_decode_block.argtypes = [P, P, P, I, I, I, F, P, I64]
+    lib.oracle_decode_block.restype = I
+    lib.oracle_decode_range.argtypes = [P, P, P, I64, I64, I, I, I, I, F, P,
+                                        I64, I64]
+    lib.oracle_decode_range.restype = I
+    lib.oracle_attention_row.argtypes = [P, P, P, I64, I, I64, P]
+    lib.oracle_attention_row.restype = None
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
         build()
-        lib = ctypes.CDLL(_LIB)
-        P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
-        lib.oracle_compand_y.argtypes = [F, F]
-        lib.oracle_compand_y.restype = ctypes.c_double
-        lib.oracle_round_code.argtypes = [F, F]
-        lib.oracle_round_code.restype = I
-        lib.oracle_expand.argtypes = [I, F]
-        lib.oracle_expand.restype = F
-        lib.oracle_stage4_literal.argtypes = [I, I, P]
-        lib.oracle_stage4_literal.restype = None
-        lib.oracle_code8.argtypes = [I, I]
-        lib.oracle_code8.restype = I
-        lib.oracle_anchor_nibble.argtypes = [I]
-        lib.oracle_anchor_nibble.restype = I
-        lib.oracle_residual_nibble.argtypes = [I]
-        lib.oracle_residual_nibble.restype = I
-        lib.oracle_f32_to_bf16.argtypes = [F]
-        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
-        lib.oracle_encode_block.argtypes = [P, I64, I, I, I, F, P, P, P]
-        lib.oracle_encode_block.restype = I
-        lib.oracle_encode_range.argtypes = [P, I64, I64, I, I, I, I, F, P, P, P,
-                                            I64, I64]
-        lib.oracle_encode_range.restype = I
-        lib.oracle_decode_block.argtypes = [P, P, P, I, I, I, F, P, I64]
-        lib.oracle_decode_block.restype = I
-        lib.oracle_decode_range.argtypes = [P, P, P, I64, I64, I, I, I, I, F, P,
-                                            I64, I64]
-        lib.oracle_decode_range.restype = I
-        lib.oracle_attention_row.argtypes = [P, P, P, I64, I, I64, P]
-        lib.oracle_attention_row.restype = None
-        _lib = lib
-        return lib
+        _lib = _bind(ctypes.CDLL(_LIB))
+        return _lib
+
+
+class using_library:
+    """Context manager: route every oracle call through another compiled
+    copy of lynx_oracle.c (the tests build deliberately broken copies to show
+    that the pins catch them)."""
+
+    def __init__(self, path: str):
+        self.lib = _bind(ctypes.CDLL(path))
+
+    def __enter__(self):
+        global _lib
+        _load()
+        self.saved = _lib
+        _lib = self.lib
+        return self
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.saved
+        return False
+
+
+def compile_variant(src_text: str, out_path: str) -> str:
+    """Compile C source text with the oracle's flags into out_path."""
+    c_path = out_path[:-3] + ".c"
+    with open(c_path, "w") as f:
+        f.write(src_text)
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-o", out_path, c_path, "-lm"]
+    subprocess.run(cmd, check=True, capture_output=True)
+    return out_path
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
 
 
 def _ptr(a: np.ndarray):

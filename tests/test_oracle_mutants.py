@@ -1,0 +1,93 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each mutant is a copy of oracle/lynx_oracle.c with one planted mistake (a
+dropped term, a wrong sign, index or constant, a transposed operand),
+compiled on the CPU and swapped in for the real oracle; at least one pin of
+tests/test_oracle_pins.py must then fail.  Nothing here touches a GPU.
+"""
+import inspect
+import os
+import tempfile
+
+import pytest
+
+import oracle
+
+from . import test_oracle_pins as pins
+
+MUTANTS = [
+    ("compander numerator 128 instead of 127",
+     "return 127.0 * log1p(al * (double)a) / log1p(al);",
+     "return 128.0 * log1p(al * (double)a) / log1p(al);"),
+    ("round down instead of to nearest", "double r = floor(y + 0.5);", "double r = floor(y);"),
+    ("inverse exponent over 128", "(double)I / 127.0) - 1.0) / al);",
+     "(double)I / 128.0) - 1.0) / al);"),
+    ("Eq. 9 without the min(S,0) term", "int q8 = I * S + (S < 0 ? S : 0);", "int q8 = I * S;"),
+    ("anchor taken from the low nibble", "{ return (code8 >> 4) & 0xf; }",
+     "{ return code8 & 0xf; }"),
+    ("nibble pairing swapped", "{ return (d & 4) ? 4 : 0; }", "{ return (d & 4) ? 0 : 4; }"),
+    ("page max as a min", "if (xv > hi) hi = xv;", "if (xv < hi) hi = xv;"),
+    ("scale without eps", "float rg = 1.0f / (gs + ORACLE_EPS);", "float rg = 1.0f / (gs);"),
+    ("normalise without subtracting gamma_min", "n[t] = (xv - lo) * rg;", "n[t] = xv * rg;"),
+    ("tree sum off by one", "v[i] = v[i] + v[i + h];", "v[i] = v[i] + v[i + h - 1];"),
+    ("mean over C+1", "float mu = v[0] * (1.0f / (float)C);",
+     "float mu = v[0] * (1.0f / (float)(C + 1));"),
+    ("sigma without abs", "float ad = fabsf(dd);", "float ad = dd;"),
+    ("sign flipped", "int S = dd >= 0.0f ? 1 : -1;", "int S = dd >= 0.0f ? -1 : 1;"),
+    ("decode chunk index wrong", "int c = t / C;", "int c = t % (P / C);"),
+    ("anchor bucket point 16V", "I = 16 * V + 7;", "I = 16 * V;"),
+    ("decode sigma without eps", "float nv = fmaf(xf, sg + ORACLE_EPS, mu);",
+     "float nv = fmaf(xf, sg, mu);"),
+    ("decode affine operands transposed",
+     "float xv = fmaf(nv, g_scale[d] + ORACLE_EPS, g_min[d]);",
+     "float xv = fmaf(nv, g_min[d] + ORACLE_EPS, g_scale[d]);"),
+    ("attention scale 1/D", "double scale = 1.0 / sqrt((double)D);",
+     "double scale = 1.0 / (double)D;"),
+    ("softmax without the max shift", "double w = exp(s[t] - m);", "double w = exp(s[t]);"),
+    ("attention not normalised", "for (int d = 0; d < D; ++d) out[d] /= l;",
+     "for (int d = 0; d < D; ++d) out[d] /= 1.0;"),
+]
+
+# representative arguments for the parametrized pins
+PARAMS = {"P": 256, "C": 32}
+
+
+def _pin_functions():
+    for name, fn in sorted(vars(pins).items()):
+        if name.startswith("test_") and callable(fn):
+            yield name, fn
+
+
+def _run_pins():
+    """Names of the pins that fail with the oracle currently swapped in."""
+    failed = []
+    for name, fn in _pin_functions():
+        sig = inspect.signature(fn)
+        kwargs = {}
+        for p in sig.parameters:
+            if p == "oracle_mod":
+                kwargs[p] = oracle
+            elif p in PARAMS:
+                kwargs[p] = PARAMS[p]
+            elif p == "alpha":
+                kwargs[p] = 255.0
+        try:
+            fn(**kwargs)
+        except Exception:          # noqa: BLE001 - any failure counts
+            failed.append(name)
+    return failed
+
+
+def test_the_real_oracle_passes_every_pin():
+    assert _run_pins() == []
+
+
+@pytest.mark.parametrize("what,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(what, old, new):
+    src = oracle.source_text()
+    assert src.count(old) == 1, f"mutation site not unique: {old}"
+    with tempfile.TemporaryDirectory() as d:
+        lib = oracle.compile_variant(src.replace(old, new), os.path.join(d, "mutant.so"))
+        with oracle.using_library(lib):
+            failed = _run_pins()
+    assert failed, f"no pin caught: {what}"

@@ -243,6 +243,24 @@ def test_decode_hand_case(oracle_mod):
     assert (part[:, 1:] == full[:, 1:]).all()
 
 
+def test_decode_inverts_normalisation_at_chunk_extremes(oracle_mod):
+    """At a chunk's extreme |d| = sigma the code is I = 127 and X(127) = 1
+    exactly (Eq. 14/15), so the decoder must give back
+    gamma_min + (gamma_scale + eps) * (mu +- (sigma + eps)): the exact inverse
+    of dividing by (sigma + eps) and (gamma_scale + eps) (Stages 1-2)."""
+    assert oracle_mod.expand(127, ALPHA) == 1.0
+    anc, res, meta = oracle_mod.encode_block(_hand_block(), C=2, alpha=ALPHA)
+    full = oracle_mod.decode_block(anc, res, meta, C=2, alpha=ALPHA)
+    gm, gs = float(meta[0, 0]), float(meta[1, 0])
+    eps = float(np.float32(1e-6))
+    for t in range(4):
+        c = t // 2
+        mu, sg = float(meta[2 + c, 0]), float(meta[4 + c, 0])
+        sign = -1.0 if t % 2 == 0 else 1.0
+        want = gm + (np.float32(gs + eps)) * (mu + sign * float(np.float32(sg + eps)))
+        assert abs(full[t, 0] - want) <= 2 * np.spacing(np.float32(abs(want)) + 1e-30), (t, full[t, 0], want)
+
+
 # ----------------------------------------------------------- random blocks
 
 def _random_block(seed, P=256, D=128, outliers=(3, 77)):
