@@ -114,7 +114,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", uuid, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
@@ -280,21 +280,24 @@ def run_lynx(args, rank, world, dev):
         if world > 1:
             torch.distributed.barrier()
 
-    for _ in range(args.warmup):
-        for r in rows_run:
-            row(r)
-    torch.cuda.synchronize(dev)
-
     uuid = None
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         uuid = None
+    # clocks are sampled from the warm-up on, through the timed region, and
+    # over untimed repeats of the same step until about 2 s of samples exist
+    clocks = ClockSampler(uuid if rank == 0 else None)
+    t_clock0 = time.perf_counter()
+    for _ in range(args.warmup):
+        for r in rows_run:
+            row(r)
+    torch.cuda.synchronize(dev)
+
     # ---- device-timed region
     ev = {r: [] for r in rows_run}
     barrier()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(uuid if rank == 0 else None)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
@@ -309,6 +312,10 @@ def run_lynx(args, rank, world, dev):
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
+    while time.perf_counter() - t_clock0 < 2.0:
+        for r in rows_run:
+            row(r)
+        torch.cuda.synchronize(dev)
     clk = clocks.stop()
     ms_total = t_start.elapsed_time(t_end)
     row_ms = {r: sum(e0.elapsed_time(e1) for e0, e1 in ev[r]) / args.steps for r in rows_run}

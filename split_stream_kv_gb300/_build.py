@@ -16,8 +16,14 @@ LIB = os.path.join(HERE, "liblynx.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
-         "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+# -fmad=false: no scalar multiply/add pair is contracted into a fused
+# multiply-add behind the source's back.  The codec's binary32 statistics
+# follow a fixed operation order (one rounding per step); every fma the
+# kernels want is written explicitly (fmaf, fma.rn.f32x2, fma.rm.f32).  (The
+# flag does not cover packed f32x2 pairs, so products that feed an add are
+# computed with scalar __fmul_rn in the kernels.)
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-fPIC",
+         "-Xcompiler", "-Wall", "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 
 def _nvcc() -> str:

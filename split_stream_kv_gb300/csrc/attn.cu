@@ -9,21 +9,30 @@
 // even), then fed to mma.sync m16n8k16 (bf16 x bf16 -> f32):
 //   scores  S^T[token][row] = K^[token][:] . q[row][:]     (A = K^, B = Q^T)
 //   output  O^T[ch][row]   += V^[:][ch]^T . P^T[:][row]    (A = V^T, B = P^T)
-// A query "row" is one (query token, query head of the group): up to 8 rows
-// per pass; more rows run as further row groups (grid z).
+// A query "row" is one (query token, query head of the group).
+//
+// Two shapes of one kernel template:
+//  * single (up to 8 rows per KV head, e.g. the draft step): every warp owns
+//    its own 32-token chunks and all 128 channels of K and V.
+//  * pair (up to 32 rows, e.g. the T = 8 verification): two warps share each
+//    32-token chunk.  Each dequantises half of the channels of K (its partial
+//    scores are summed with the partner's through shared memory) and half of
+//    the channels of V (it accumulates that half of O^T), so every packed
+//    element is decoded once.
 // The contraction index (channel) of the scores is permuted so that a lane's
-// fragment bytes are contiguous in a packed row: lane c (= lane % 4) owns the
-// 16 bytes 16c..16c+15 (channels 32c..32c+31) for K; for V, lane g (= lane/4)
-// owns the 8 bytes 8g..8g+7 (channels 16g..16g+15) and m-tile mt takes byte
-// 8g+mt, whose two channels are the rows g and g+8 of that m-tile.
+// fragment bytes are contiguous in a packed row: lane c (= lane % 4) owns KB
+// consecutive bytes of K rows, lane g (= lane / 4) owns VB consecutive bytes
+// of V rows, and V m-tile mt takes byte VB*g + mt, whose two channels are the
+// rows g and g+8 of that m-tile.
 // P is split into bf16 hi + lo parts (two MMAs) so the softmax weights keep
 // about 16 mantissa bits; movmatrix turns the S^T accumulator layout into the
 // P^T operand layout.
 //
 // Work split (flash-decoding): grid = (splits, H_kv, batch * row groups).
-// Each warp walks its own 32-token chunks of the CTA's token range with its
-// own running max / sum / output; the CTA merges its 4 warps and writes one
-// partial (m, l, o) per split; attn_combine merges the splits.
+// Each unit (warp, or warp pair) walks its own 32-token chunks of the CTA's
+// token range with its own running max / sum / output; the CTA merges its
+// units and writes one partial (m, l, o) per split; attn_combine merges the
+// splits.
 #include <math.h>
 #include <stdio.h>
 
@@ -36,9 +45,15 @@
 namespace lynx {
 
 constexpr int kAttnWarps = 4;
-constexpr int kRows = 8;                 // query rows per pass (one n-tile)
-constexpr int kPartFloats = 2 * kRows + kRows * kD;
-constexpr int kScratchFloats = 2 * 6 * kD;  // per warp: K and V constant rows
+constexpr int kLutBytes = 32768;
+// Per-warp constant rows (gamma_min, gamma_scale+eps, mu, sigma+eps for two
+// 16-token halves) of K and V.  A row holds 128 channels in groups of 8,
+// stored as the pairs (k, k+4) of the nibble pairing so that one 16-byte load
+// gives two float2 operands, with 16 bytes of padding after every 4 groups so
+// that lanes reading different groups hit different banks.
+constexpr int kRowFloats = 144;
+constexpr int kScratchRows = 12;
+constexpr int kScratchFloats = kScratchRows * kRowFloats;
 
 struct AttnParams {
   const uint16_t* q;
@@ -70,57 +85,108 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-__device__ __forceinline__ uint4 ldg128(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ uint2 ldg64(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+template <int N>
+struct Bytes;  // N packed bytes loaded from one row
+template <>
+struct Bytes<16> {
+  uint32_t w[4];
+  __device__ __forceinline__ void load(const uint8_t* p) {
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p));
+  }
+};
+template <>
+struct Bytes<8> {
+  uint32_t w[2];
+  __device__ __forceinline__ void load(const uint8_t* p) {
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(w[0]), "=r"(w[1]) : "l"(p));
+  }
+};
+template <>
+struct Bytes<4> {
+  uint32_t w[1];
+  __device__ __forceinline__ void load(const uint8_t* p) {
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(w[0]) : "l"(p));
+  }
+};
+
+// Float offset of the first of channel group grp's 8 values in a row.
+__device__ __forceinline__ int grp_off(int grp) { return grp * 8 + (grp >> 2) * 4; }
+
+struct Consts {  // pairs (k, k+4) of one channel group, k = 0..3
+  f2 gm[4], gs[4], mu[4], sg[4];
+};
+__device__ __forceinline__ void load_consts(Consts& k, const float* rows, int grp, int jrow) {
+  const float* base = rows + grp_off(grp);
+  const float4 g0 = *reinterpret_cast<const float4*>(base + 0 * kRowFloats);
+  const float4 g1 = *reinterpret_cast<const float4*>(base + 0 * kRowFloats + 4);
+  const float4 s0 = *reinterpret_cast<const float4*>(base + 1 * kRowFloats);
+  const float4 s1 = *reinterpret_cast<const float4*>(base + 1 * kRowFloats + 4);
+  const float4 m0 = *reinterpret_cast<const float4*>(base + (2 + 2 * jrow) * kRowFloats);
+  const float4 m1 = *reinterpret_cast<const float4*>(base + (2 + 2 * jrow) * kRowFloats + 4);
+  const float4 a0 = *reinterpret_cast<const float4*>(base + (3 + 2 * jrow) * kRowFloats);
+  const float4 a1 = *reinterpret_cast<const float4*>(base + (3 + 2 * jrow) * kRowFloats + 4);
+  k.gm[0] = {g0.x, g0.y}; k.gm[1] = {g0.z, g0.w}; k.gm[2] = {g1.x, g1.y}; k.gm[3] = {g1.z, g1.w};
+  k.gs[0] = {s0.x, s0.y}; k.gs[1] = {s0.z, s0.w}; k.gs[2] = {s1.x, s1.y}; k.gs[3] = {s1.z, s1.w};
+  k.mu[0] = {m0.x, m0.y}; k.mu[1] = {m0.z, m0.w}; k.mu[2] = {m1.x, m1.y}; k.mu[3] = {m1.z, m1.w};
+  k.sg[0] = {a0.x, a0.y}; k.sg[1] = {a0.z, a0.w}; k.sg[2] = {a1.x, a1.y}; k.sg[3] = {a1.z, a1.w};
 }
 
-// Values of the two channels of one packed byte position (anchor byte a and,
-// in full mode, residual byte r): (low-nibble channel, high-nibble channel).
+// Values of the two channels of byte `pos` (0..3) of an anchor word a (and,
+// in full mode, residual word r): (low-nibble channel, high-nibble channel).
 template <bool FULL>
-__device__ __forceinline__ float2 lookup_pair(const uint8_t* lut, uint32_t a, uint32_t r,
-                                              int lane) {
+__device__ __forceinline__ f2 lookup_pair(const uint8_t* lut, uint32_t a, uint32_t r, int pos,
+                                          uint32_t lane_off) {
   if constexpr (FULL) {
-    const float* t = reinterpret_cast<const float*>(lut);
-    const uint32_t c_lo = ((a & 0x0fu) << 4) | (r & 0x0fu);
-    const uint32_t c_hi = (a & 0xf0u) | (r >> 4);
-    return make_float2(t[c_lo * 32 + lane], t[c_hi * 32 + lane]);
+    const uint32_t E = ((a << 4) & 0xf0f0f0f0u) | (r & 0x0f0f0f0fu);  // low-nibble codes
+    const uint32_t O = (a & 0xf0f0f0f0u) | ((r >> 4) & 0x0f0f0f0fu);  // high-nibble codes
+    // byte pos of E / O times 128 (32 lanes x 4 bytes) + lane * 4
+    const int sh = 8 * pos - 7;
+    const uint32_t ae = ((sh >= 0 ? E >> sh : E << -sh) & 0x7f80u) | lane_off;
+    const uint32_t ao = ((sh >= 0 ? O >> sh : O << -sh) & 0x7f80u) | lane_off;
+    f2 v;
+    v.x = *reinterpret_cast<const float*>(lut + ae);
+    v.y = *reinterpret_cast<const float*>(lut + ao);
+    return v;
   } else {
-    const float2* t = reinterpret_cast<const float2*>(lut);
-    return t[a * 16 + (lane & 15)];
+    // byte pos of a times 128 (16 lane slots x 8 bytes) + (lane % 16) * 8
+    const int sh = 8 * pos - 7;
+    const uint32_t ad = ((sh >= 0 ? a >> sh : a << -sh) & 0x7f80u) | lane_off;
+    const float2 p = *reinterpret_cast<const float2*>(lut + ad);
+    return f2{p.x, p.y};
   }
 }
 
-// One packed byte position -> bf16x2 (low-nibble channel in the low half).
+// One packed byte position -> bf16x2 of the exact decoder output
+// (low-nibble channel in the low half).
 template <bool FULL>
 __device__ __forceinline__ uint32_t dequant_pair(const uint8_t* lut, uint32_t a, uint32_t r,
-                                                 int lane, float gm0, float gm1, float gs0,
-                                                 float gs1, float mu0, float mu1, float sg0,
-                                                 float sg1) {
-  const float2 v = lookup_pair<FULL>(lut, a, r, lane);
-  const float x0 = fmaf(fmaf(v.x, sg0, mu0), gs0, gm0);
-  const float x1 = fmaf(fmaf(v.y, sg1, mu1), gs1, gm1);
-  return f2_to_bf2(x0, x1);
+                                                 int pos, uint32_t lane_off, f2 gm, f2 gs, f2 mu,
+                                                 f2 sg) {
+  const f2 v = lookup_pair<FULL>(lut, a, r, pos, lane_off);
+  const f2 x = fma2(fma2(v, sg, mu), gs, gm);
+  return f2_to_bf2(x.x, x.y);
 }
 
-template <bool FULL>
-__global__ void __launch_bounds__(kAttnWarps * 32, 3)
+template <bool FULL, int NT, bool PAIR>
+__global__ void __launch_bounds__(kAttnWarps * 32, PAIR ? 2 : 3)
 attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ ExpandTable tab) {
+  constexpr int KCH = PAIR ? 64 : 128;  // channels of K and of V per warp
+  constexpr int NKT = KCH / 16;         // score k-tiles = output m-tiles per warp
+  constexpr int KB = KCH / 8;           // K bytes per token row per lane (c)
+  constexpr int VB = KCH / 16;          // V bytes per token row per lane (g)
+  constexpr int NU = PAIR ? kAttnWarps / 2 : kAttnWarps;  // work units per CTA
+  constexpr int RP = 8 * NT;            // query rows per pass
+
   extern __shared__ __align__(16) uint8_t smem[];
-  uint8_t* lut = smem;                                   // 32 KB
-  float* scratch_all = reinterpret_cast<float*>(smem + 32768);
+  uint8_t* lut = smem;
+  float* scratch_all = reinterpret_cast<float*>(smem + kLutBytes);
+  float* xchg_all = scratch_all + kAttnWarps * kScratchFloats;  // pair: partial scores
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
+  const int unit = PAIR ? (w >> 1) : w;
+  const int half = PAIR ? (w & 1) : 0;
+  const int hb = half * 32;             // first byte of this warp's channel half
 
   if constexpr (FULL) {
     float* t = reinterpret_cast<float*>(lut);
@@ -137,281 +203,305 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     }
   }
   __syncthreads();
+  const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 8u;
 
   const int split = blockIdx.x, h = blockIdx.y;
   const int b = blockIdx.z / a.nrg, rg = blockIdx.z % a.nrg;
-  const int row0 = rg * kRows;
+  const int row0 = rg * RP;
 
   // ---- Q^T fragments (B operand), channel order matching the K bytes
-  uint32_t qf[8][2];
-  {
-    const int r = row0 + g;
+  uint32_t qf[NKT][NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int r = row0 + nt * 8 + g;
     const bool valid = r < a.R;
     const int tq = valid ? r / a.G : 0, gq = valid ? r % a.G : 0;
     const uint16_t* qrow = a.q + ((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD;
 #pragma unroll
-    for (int kt = 0; kt < 8; ++kt)
+    for (int kt = 0; kt < NKT; ++kt)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int beta = 16 * c + 2 * kt + hh;
+        const int beta = hb + KB * c + 2 * kt + hh;
         const int lo = 8 * (beta >> 2) + (beta & 3);
-        qf[kt][hh] = valid ? ((uint32_t)qrow[lo] | ((uint32_t)qrow[lo + 4] << 16)) : 0u;
+        qf[kt][nt][hh] = valid ? ((uint32_t)qrow[lo] | ((uint32_t)qrow[lo + 4] << 16)) : 0u;
       }
   }
 
-  float* scr = scratch_all + w * kScratchFloats;   // [tensor][6][128]
+  float* scr = scratch_all + w * kScratchFloats;   // K rows 0..5, V rows 6..11
   const int64_t cb = a.NCH * split / a.S, ce = a.NCH * (split + 1) / a.S;
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
-  float o[8][4];
+  float m_run[NT][2], l_run[NT][2];
+  float o[NKT][NT][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int nt = 0; nt < NT; ++nt) {
+    m_run[nt][0] = m_run[nt][1] = -INFINITY;
+    l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+    for (int i = 0; i < NKT; ++i) o[i][nt][0] = o[i][nt][1] = o[i][nt][2] = o[i][nt][3] = 0.f;
+  }
   const int meta_rows = 2 + 2 * a.NC;
+  const bool one_chunk = a.C >= 32;      // both 16-token halves share mu, sigma
+  int it = 0;
 
-  for (int64_t qc = cb + w; qc < ce; qc += kAttnWarps) {
+  for (int64_t qc = cb + unit; qc < ce; qc += NU, ++it) {
     const int64_t t0 = qc * 32;
     const int64_t p = t0 / a.P;
     const int tp = (int)(t0 - p * a.P);
     const int64_t blk = ((int64_t)b * a.NB + p) * a.Hkv + h;
     const int64_t code_off = (blk * a.P + tp) * (kD / 2);
 
-    // ---- packed codes of this chunk
-    uint4 kA[4], kR[4];
-    uint2 vA[8], vR[8];
+    // ---- packed codes of this chunk (K: 4 rows per lane, V: 8 rows)
+    Bytes<KB> kA[4], kR[4];
+    Bytes<VB> vA[8], vR[8];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const int row = 16 * (jj >> 1) + g + 8 * (jj & 1);
-      kA[jj] = ldg128(a.ka + code_off + row * 64 + 16 * c);
-      if constexpr (FULL) kR[jj] = ldg128(a.kr + code_off + row * 64 + 16 * c);
+      kA[jj].load(a.ka + code_off + row * 64 + hb + KB * c);
+      if constexpr (FULL) kR[jj].load(a.kr + code_off + row * 64 + hb + KB * c);
     }
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) {
       const int kk = ii & 3;
       const int row = 16 * (ii >> 2) + 2 * c + (kk & 1) + 8 * (kk >> 1);
-      vA[ii] = ldg64(a.va + code_off + row * 64 + 8 * g);
-      if constexpr (FULL) vR[ii] = ldg64(a.vr + code_off + row * 64 + 8 * g);
+      vA[ii].load(a.va + code_off + row * 64 + hb + VB * g);
+      if constexpr (FULL) vR[ii].load(a.vr + code_off + row * 64 + hb + VB * g);
     }
-    // ---- constants: gamma_min, gamma_scale+eps, mu (2 sub-tiles), sigma+eps
+    // ---- constant rows -> scratch (pairs (k, k+4) interleaved, +eps folded)
     {
       const int cc0 = tp / a.C, cc1 = (tp + 16) / a.C;
-      const int src_row[6] = {0, 1, 2 + cc0, 2 + cc1, 2 + a.NC + cc0, 2 + a.NC + cc1};
+      const int nrow = one_chunk ? 4 : 6;
+      const int grp = lane >> 1, hf = lane & 1;
 #pragma unroll
       for (int tsr = 0; tsr < 2; ++tsr) {
-        const float* mb = (tsr == 0 ? a.km : a.vm) + blk * (int64_t)meta_rows * kD;
+        const float* mb = (tsr == 0 ? a.km : a.vm) + blk * (int64_t)meta_rows * kD + 8 * grp + 2 * hf;
 #pragma unroll
         for (int rr = 0; rr < 6; ++rr) {
-          float4 v = __ldg(reinterpret_cast<const float4*>(mb + src_row[rr] * kD) + lane);
-          if (rr == 1 || rr >= 4) {
+          if (rr >= nrow) break;
+          const int src = rr == 0 ? 0 : rr == 1 ? 1 : rr == 2 ? 2 + cc0 : rr == 3 ? 2 + a.NC + cc0
+                        : rr == 4 ? 2 + cc1 : 2 + a.NC + cc1;
+          const float2 lo = __ldg(reinterpret_cast<const float2*>(mb + src * kD));
+          const float2 hi = __ldg(reinterpret_cast<const float2*>(mb + src * kD + 4));
+          float4 v = make_float4(lo.x, hi.x, lo.y, hi.y);
+          if (rr == 1 || rr == 3 || rr == 5) {
             v.x = __fadd_rn(v.x, kEps); v.y = __fadd_rn(v.y, kEps);
             v.z = __fadd_rn(v.z, kEps); v.w = __fadd_rn(v.w, kEps);
           }
-          reinterpret_cast<float4*>(scr + (tsr * 6 + rr) * kD)[lane] = v;
+          *reinterpret_cast<float4*>(scr + (tsr * 6 + rr) * kRowFloats + grp_off(grp) + 4 * hf) = v;
         }
       }
     }
     __syncwarp();
 
     // ---- scores: S^T for m-tiles j = 0, 1 (tokens 16j .. 16j+15)
-    float s[2][4];
+    float s[2][NT][4];
 #pragma unroll
-    for (int j = 0; j < 2; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+    for (int j = 0; j < 2; ++j)
 #pragma unroll
-    for (int G4 = 0; G4 < 4; ++G4) {
-      const int grp = 4 * c + G4;  // channels 8grp .. 8grp+7
-      float gm[8], gs[8], mu[2][8], sg[2][8];
+      for (int nt = 0; nt < NT; ++nt) s[j][nt][0] = s[j][nt][1] = s[j][nt][2] = s[j][nt][3] = 0.f;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float4 x0 = reinterpret_cast<const float4*>(scr + 0 * kD + 8 * grp)[i];
-        const float4 x1 = reinterpret_cast<const float4*>(scr + 1 * kD + 8 * grp)[i];
-        gm[4 * i] = x0.x; gm[4 * i + 1] = x0.y; gm[4 * i + 2] = x0.z; gm[4 * i + 3] = x0.w;
-        gs[4 * i] = x1.x; gs[4 * i + 1] = x1.y; gs[4 * i + 2] = x1.z; gs[4 * i + 3] = x1.w;
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float4 y0 = reinterpret_cast<const float4*>(scr + (2 + j) * kD + 8 * grp)[i];
-          const float4 y1 = reinterpret_cast<const float4*>(scr + (4 + j) * kD + 8 * grp)[i];
-          mu[j][4 * i] = y0.x; mu[j][4 * i + 1] = y0.y; mu[j][4 * i + 2] = y0.z; mu[j][4 * i + 3] = y0.w;
-          sg[j][4 * i] = y1.x; sg[j][4 * i + 1] = y1.y; sg[j][4 * i + 2] = y1.z; sg[j][4 * i + 3] = y1.w;
-        }
-      }
+    for (int gi = 0; gi < KB / 4; ++gi) {      // channel groups of this lane (K)
+      const int grp = (hb + KB * c) / 4 + gi;
+      Consts k0, k1;
+      load_consts(k0, scr, grp, 0);
+      if (!one_chunk) load_consts(k1, scr, grp, 1);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
-        const int kt = 2 * G4 + kk;
+        const int kt = 2 * gi + kk;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
+          const Consts& kc = (j == 0 || one_chunk) ? k0 : k1;
           uint32_t af[4];
 #pragma unroll
           for (int i = 0; i < 2; ++i) {       // row g (i=0) / g+8 (i=1)
-            const uint32_t wa = word_of(kA[2 * j + i], G4);
-            const uint32_t wr = FULL ? word_of(kR[2 * j + i], G4) : 0u;
+            const uint32_t wa = kA[2 * j + i].w[gi];
+            const uint32_t wr = FULL ? kR[2 * j + i].w[gi] : 0u;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {  // k 2c..2c+1 (hh=0) / 2c+8.. (hh=1)
-              const int jb = 2 * kk + hh;     // byte within the word = channel 8grp+jb
-              const uint32_t ab = (wa >> (8 * jb)) & 0xffu;
-              const uint32_t rb = (wr >> (8 * jb)) & 0xffu;
-              af[i + 2 * hh] = dequant_pair<FULL>(lut, ab, rb, lane, gm[jb], gm[jb + 4], gs[jb],
-                                                  gs[jb + 4], mu[j][jb], mu[j][jb + 4],
-                                                  sg[j][jb], sg[j][jb + 4]);
+              const int pos = 2 * kk + hh;    // byte in the word = pair (pos, pos+4)
+              af[i + 2 * hh] = dequant_pair<FULL>(lut, wa, wr, pos, lane_off, kc.gm[pos],
+                                                  kc.gs[pos], kc.mu[pos], kc.sg[pos]);
             }
           }
-          mma_bf16(s[j], af, qf[kt][0], qf[kt][1]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(s[j][nt], af, qf[kt][nt][0], qf[kt][nt][1]);
         }
       }
     }
 
-    // ---- online softmax (log2 domain); rows 2c, 2c+1
-    float cmax0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-    float cmax1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+    if constexpr (PAIR) {
+      // partial scores over this warp's channel half + the partner's half
+      float* mine = xchg_all + ((unit * 2 + half) * 2 + (it & 1)) * (32 * 8 * NT);
+      const float* other = xchg_all + ((unit * 2 + (half ^ 1)) * 2 + (it & 1)) * (32 * 8 * NT);
 #pragma unroll
-    for (int x = 4; x <= 16; x <<= 1) {
-      cmax0 = fmaxf(cmax0, __shfl_xor_sync(kFull, cmax0, x));
-      cmax1 = fmaxf(cmax1, __shfl_xor_sync(kFull, cmax1, x));
-    }
-    const float mn0 = fmaxf(m_run[0], cmax0 * a.scale_log2);
-    const float mn1 = fmaxf(m_run[1], cmax1 * a.scale_log2);
-    const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
-    m_run[0] = mn0;
-    m_run[1] = mn1;
-    l_run[0] *= al0;
-    l_run[1] *= al1;
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      o[mt][0] *= al0; o[mt][1] *= al1; o[mt][2] *= al0; o[mt][3] *= al1;
-    }
-    uint32_t pb_hi[2][2], pb_lo[2][2];
+        for (int nt = 0; nt < NT; ++nt)
+          *reinterpret_cast<float4*>(mine + ((j * NT + nt) * 32 + lane) * 4) =
+              make_float4(s[j][nt][0], s[j][nt][1], s[j][nt][2], s[j][nt][3]);
+      asm volatile("bar.sync %0, 64;" :: "r"(1 + unit) : "memory");
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const float p0 = exp2f(fmaf(s[j][0], a.scale_log2, -mn0));
-      const float p1 = exp2f(fmaf(s[j][1], a.scale_log2, -mn1));
-      const float p2 = exp2f(fmaf(s[j][2], a.scale_log2, -mn0));
-      const float p3 = exp2f(fmaf(s[j][3], a.scale_log2, -mn1));
-      l_run[0] += p0 + p2;
-      l_run[1] += p1 + p3;
-      const uint32_t top = f2_to_bf2(p0, p1), bot = f2_to_bf2(p2, p3);
-      const f2 th = bf2_to_f2(top), bh = bf2_to_f2(bot);
-      const uint32_t topl = f2_to_bf2(p0 - th.x, p1 - th.y);
-      const uint32_t botl = f2_to_bf2(p2 - bh.x, p3 - bh.y);
-      pb_hi[j][0] = movtrans(top);
-      pb_hi[j][1] = movtrans(bot);
-      pb_lo[j][0] = movtrans(topl);
-      pb_lo[j][1] = movtrans(botl);
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float4 v = *reinterpret_cast<const float4*>(other + ((j * NT + nt) * 32 + lane) * 4);
+          s[j][nt][0] += v.x; s[j][nt][1] += v.y; s[j][nt][2] += v.z; s[j][nt][3] += v.w;
+        }
     }
 
-    // ---- output: O^T += V^T P^T over V m-tiles mt (byte 8g + mt)
+    // ---- online softmax (log2 domain); rows nt*8 + 2c, nt*8 + 2c + 1
+    uint32_t pb_hi[2][NT][2], pb_lo[2][NT][2];
 #pragma unroll
-    for (int G2 = 0; G2 < 2; ++G2) {
-      const int grp = 2 * g + G2;
-      const float* vs = scr + 6 * kD;
-      float gm[8], gs[8], mu[2][8], sg[2][8];
+    for (int nt = 0; nt < NT; ++nt) {
+      float cmax0 = fmaxf(fmaxf(s[0][nt][0], s[0][nt][2]), fmaxf(s[1][nt][0], s[1][nt][2]));
+      float cmax1 = fmaxf(fmaxf(s[0][nt][1], s[0][nt][3]), fmaxf(s[1][nt][1], s[1][nt][3]));
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float4 x0 = reinterpret_cast<const float4*>(vs + 0 * kD + 8 * grp)[i];
-        const float4 x1 = reinterpret_cast<const float4*>(vs + 1 * kD + 8 * grp)[i];
-        gm[4 * i] = x0.x; gm[4 * i + 1] = x0.y; gm[4 * i + 2] = x0.z; gm[4 * i + 3] = x0.w;
-        gs[4 * i] = x1.x; gs[4 * i + 1] = x1.y; gs[4 * i + 2] = x1.z; gs[4 * i + 3] = x1.w;
+      for (int x = 4; x <= 16; x <<= 1) {
+        cmax0 = fmaxf(cmax0, __shfl_xor_sync(kFull, cmax0, x));
+        cmax1 = fmaxf(cmax1, __shfl_xor_sync(kFull, cmax1, x));
+      }
+      const float mn0 = fmaxf(m_run[nt][0], cmax0 * a.scale_log2);
+      const float mn1 = fmaxf(m_run[nt][1], cmax1 * a.scale_log2);
+      if (mn0 != m_run[nt][0] || mn1 != m_run[nt][1]) {
+        const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+        l_run[nt][0] *= al0;
+        l_run[nt][1] *= al1;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const float4 y0 = reinterpret_cast<const float4*>(vs + (2 + j) * kD + 8 * grp)[i];
-          const float4 y1 = reinterpret_cast<const float4*>(vs + (4 + j) * kD + 8 * grp)[i];
-          mu[j][4 * i] = y0.x; mu[j][4 * i + 1] = y0.y; mu[j][4 * i + 2] = y0.z; mu[j][4 * i + 3] = y0.w;
-          sg[j][4 * i] = y1.x; sg[j][4 * i + 1] = y1.y; sg[j][4 * i + 2] = y1.z; sg[j][4 * i + 3] = y1.w;
+        for (int mt = 0; mt < NKT; ++mt) {
+          o[mt][nt][0] *= al0; o[mt][nt][1] *= al1; o[mt][nt][2] *= al0; o[mt][nt][3] *= al1;
         }
+        m_run[nt][0] = mn0;
+        m_run[nt][1] = mn1;
       }
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int mt = 4 * G2 + kk;
+      for (int j = 0; j < 2; ++j) {
+        const float p0 = exp2f(fmaf(s[j][nt][0], a.scale_log2, -mn0));
+        const float p1 = exp2f(fmaf(s[j][nt][1], a.scale_log2, -mn1));
+        const float p2 = exp2f(fmaf(s[j][nt][2], a.scale_log2, -mn0));
+        const float p3 = exp2f(fmaf(s[j][nt][3], a.scale_log2, -mn1));
+        l_run[nt][0] += p0 + p2;
+        l_run[nt][1] += p1 + p3;
+        const uint32_t top = f2_to_bf2(p0, p1), bot = f2_to_bf2(p2, p3);
+        const f2 th = bf2_to_f2(top), bh = bf2_to_f2(bot);
+        pb_hi[j][nt][0] = movtrans(top);
+        pb_hi[j][nt][1] = movtrans(bot);
+        pb_lo[j][nt][0] = movtrans(f2_to_bf2(p0 - th.x, p1 - th.y));
+        pb_lo[j][nt][1] = movtrans(f2_to_bf2(p2 - bh.x, p3 - bh.y));
+      }
+    }
+
+    // ---- output: O^T += V^T P^T over this warp's V m-tiles (byte VB*g + mt)
+#pragma unroll
+    for (int gi = 0; gi < (VB + 3) / 4; ++gi) {
+      const int grp = (hb + VB * g) / 4 + gi;
+      Consts k0, k1;
+      load_consts(k0, scr + 6 * kRowFloats, grp, 0);
+      if (!one_chunk) load_consts(k1, scr + 6 * kRowFloats, grp, 1);
+#pragma unroll
+      for (int kk = 0; kk < (VB < 4 ? VB : 4); ++kk) {
+        const int mt = 4 * gi + kk;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
+          const Consts& kc = (j == 0 || one_chunk) ? k0 : k1;
           uint32_t W[4];
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {   // tokens 2c, 2c+1, 2c+8, 2c+9
-            const uint2 va = vA[4 * j + q4];
-            const uint32_t wa = G2 == 0 ? va.x : va.y;
-            uint32_t wr = 0;
-            if constexpr (FULL) wr = G2 == 0 ? vR[4 * j + q4].x : vR[4 * j + q4].y;
-            const uint32_t ab = (wa >> (8 * kk)) & 0xffu;
-            const uint32_t rb = (wr >> (8 * kk)) & 0xffu;
-            W[q4] = dequant_pair<FULL>(lut, ab, rb, lane, gm[kk], gm[kk + 4], gs[kk], gs[kk + 4],
-                                       mu[j][kk], mu[j][kk + 4], sg[j][kk], sg[j][kk + 4]);
+            const uint32_t wa = vA[4 * j + q4].w[gi];
+            const uint32_t wr = FULL ? vR[4 * j + q4].w[gi] : 0u;
+            W[q4] = dequant_pair<FULL>(lut, wa, wr, kk, lane_off, kc.gm[kk], kc.gs[kk],
+                                       kc.mu[kk], kc.sg[kk]);
           }
           uint32_t af[4];
           af[0] = prmt(W[0], W[1], 0x5410u);  // row g   (low channel), tokens 2c, 2c+1
           af[1] = prmt(W[0], W[1], 0x7632u);  // row g+8 (high channel)
           af[2] = prmt(W[2], W[3], 0x5410u);  // row g,   tokens 2c+8, 2c+9
           af[3] = prmt(W[2], W[3], 0x7632u);
-          mma_bf16(o[mt], af, pb_hi[j][0], pb_hi[j][1]);
-          mma_bf16(o[mt], af, pb_lo[j][0], pb_lo[j][1]);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_bf16(o[mt][nt], af, pb_hi[j][nt][0], pb_hi[j][nt][1]);
+            mma_bf16(o[mt][nt], af, pb_lo[j][nt][0], pb_lo[j][nt][1]);
+          }
         }
       }
     }
     __syncwarp();
   }
 
-  // ---- merge the 4 warps of the CTA, write this split's partial
+  // ---- merge the units of the CTA, write this split's partial
 #pragma unroll
-  for (int x = 4; x <= 16; x <<= 1) {
-    l_run[0] += __shfl_xor_sync(kFull, l_run[0], x);
-    l_run[1] += __shfl_xor_sync(kFull, l_run[1], x);
-  }
-  __syncthreads();  // everyone is done with the lookup table; reuse it
-  float* sm_m = reinterpret_cast<float*>(smem);                 // [4][8]
-  float* sm_l = sm_m + kAttnWarps * kRows;                       // [4][8]
-  float* sm_o = sm_l + kAttnWarps * kRows;                       // [4][8][128]
-  if (g == 0) {
-    sm_m[w * kRows + 2 * c] = m_run[0];
-    sm_m[w * kRows + 2 * c + 1] = m_run[1];
-    sm_l[w * kRows + 2 * c] = l_run[0];
-    sm_l[w * kRows + 2 * c + 1] = l_run[1];
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int x = 4; x <= 16; x <<= 1) {
+      l_run[nt][0] += __shfl_xor_sync(kFull, l_run[nt][0], x);
+      l_run[nt][1] += __shfl_xor_sync(kFull, l_run[nt][1], x);
+    }
+  __syncthreads();  // every warp is done with the tables and scratch; reuse them
+  float* sm_m = reinterpret_cast<float*>(smem);       // [NU][RP]
+  float* sm_l = sm_m + NU * RP;                        // [NU][RP]
+  float* sm_o = sm_l + NU * RP;                        // [NU][RP][128]
+  if (g == 0 && half == 0) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      sm_m[unit * RP + nt * 8 + 2 * c] = m_run[nt][0];
+      sm_m[unit * RP + nt * 8 + 2 * c + 1] = m_run[nt][1];
+      sm_l[unit * RP + nt * 8 + 2 * c] = l_run[nt][0];
+      sm_l[unit * RP + nt * 8 + 2 * c + 1] = l_run[nt][1];
+    }
   }
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int beta = 8 * g + mt;
+  for (int mt = 0; mt < NKT; ++mt) {
+    const int beta = hb + VB * g + mt;
     const int ch_lo = 8 * (beta >> 2) + (beta & 3), ch_hi = ch_lo + 4;
-    float* ow = sm_o + w * kRows * kD;
-    ow[(2 * c) * kD + ch_lo] = o[mt][0];
-    ow[(2 * c + 1) * kD + ch_lo] = o[mt][1];
-    ow[(2 * c) * kD + ch_hi] = o[mt][2];
-    ow[(2 * c + 1) * kD + ch_hi] = o[mt][3];
+    float* ow = sm_o + unit * RP * kD;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      ow[(nt * 8 + 2 * c) * kD + ch_lo] = o[mt][nt][0];
+      ow[(nt * 8 + 2 * c + 1) * kD + ch_lo] = o[mt][nt][1];
+      ow[(nt * 8 + 2 * c) * kD + ch_hi] = o[mt][nt][2];
+      ow[(nt * 8 + 2 * c + 1) * kD + ch_hi] = o[mt][nt][3];
+    }
   }
   __syncthreads();
-  float* part = a.part + ((((int64_t)b * a.Hkv + h) * a.nrg + rg) * a.S + split) * kPartFloats;
-  for (int i = tid; i < kRows * kD; i += kAttnWarps * 32) {
+  const int part_floats = 2 * RP + RP * kD;
+  float* part = a.part + ((((int64_t)b * a.Hkv + h) * a.nrg + rg) * a.S + split) * part_floats;
+  for (int i = tid; i < RP * kD; i += kAttnWarps * 32) {
     const int r = i / kD, d = i % kD;
     float M = -INFINITY;
 #pragma unroll
-    for (int ww = 0; ww < kAttnWarps; ++ww) M = fmaxf(M, sm_m[ww * kRows + r]);
+    for (int u = 0; u < NU; ++u) M = fmaxf(M, sm_m[u * RP + r]);
     float acc = 0.f, den = 0.f;
 #pragma unroll
-    for (int ww = 0; ww < kAttnWarps; ++ww) {
-      const float mw = sm_m[ww * kRows + r];
-      const float f = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      acc += f * sm_o[(ww * kRows + r) * kD + d];
-      den += f * sm_l[ww * kRows + r];
+    for (int u = 0; u < NU; ++u) {
+      const float mu_ = sm_m[u * RP + r];
+      const float f = mu_ == -INFINITY ? 0.f : exp2f(mu_ - M);
+      acc += f * sm_o[(u * RP + r) * kD + d];
+      den += f * sm_l[u * RP + r];
     }
-    part[2 * kRows + r * kD + d] = acc;
+    part[2 * RP + r * kD + d] = acc;
     if (d == 0) {
       part[r] = M;
-      part[kRows + r] = den;
+      part[RP + r] = den;
     }
   }
 }
 
 // Merge the splits of one (sequence, KV head, row group): out = sum e^(m_s-M)
 // o_s / sum e^(m_s-M) l_s, written to out[b][t][hq][:].
-__global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnParams a) {
+__global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnParams a, int RP) {
   const int z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
   const int rg = z % a.nrg, bh = z / a.nrg, h = bh % a.Hkv, b = bh / a.Hkv;
   const int d = threadIdx.x;
-  const float* part = a.part + (int64_t)z * a.S * kPartFloats;
-  for (int r = 0; r < kRows; ++r) {
-    const int row = rg * kRows + r;
+  const int part_floats = 2 * RP + RP * kD;
+  const float* part = a.part + (int64_t)z * a.S * part_floats;
+  for (int r = 0; r < RP; ++r) {
+    const int row = rg * RP + r;
     if (row >= a.R) break;
     float M = -INFINITY;
-    for (int s = 0; s < a.S; ++s) M = fmaxf(M, part[s * kPartFloats + r]);
+    for (int s = 0; s < a.S; ++s) M = fmaxf(M, part[s * part_floats + r]);
     float num = 0.f, den = 0.f;
     for (int s = 0; s < a.S; ++s) {
-      const float* ps = part + s * kPartFloats;
+      const float* ps = part + s * part_floats;
       const float f = ps[r] == -INFINITY ? 0.f : exp2f(ps[r] - M);
-      num += f * ps[2 * kRows + r * kD + d];
-      den += f * ps[kRows + r];
+      num += f * ps[2 * RP + r * kD + d];
+      den += f * ps[RP + r];
     }
     const int tq = row / a.G, gq = row % a.G;
     a.out[((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + d] = num / den;
@@ -420,30 +510,42 @@ __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnP
 
 // ------------------------------------------------------------------ host
 
-static int row_groups(int G, int T) { return (G * T + kRows - 1) / kRows; }
+// Query rows per pass: one n-tile (8 rows) for small groups, else a warp
+// pair over four n-tiles (32 rows).
+static int rows_per_pass(int R) { return R <= 8 ? 8 : 32; }
+static int row_groups(int R) { const int rp = rows_per_pass(R); return (R + rp - 1) / rp; }
 
-// Splits per (sequence, KV head, row group): about 512 CTAs in all, each
-// with at least 4 chunks of 32 tokens (one per warp).  Device independent,
+// Splits per (sequence, KV head, row group): as many as fit one wave of
+// CTAs on the 152 SMs of a GB300 (3 resident CTAs per SM for the single-warp
+// shape, 2 for the warp-pair shape), so that no partial second wave leaves
+// SMs idle; at least one 32-token chunk per work unit.  Device independent,
 // so the workspace size is a pure function of the shapes.
-static int splits_for(int batch, int Hkv, int nrg, int64_t NCH) {
+constexpr int kGB300SMs = 152;
+static int splits_for(int batch, int Hkv, int nrg, int64_t NCH, int R) {
   const int64_t units = (int64_t)batch * Hkv * nrg;
-  int64_t s = (512 + units - 1) / units;
-  const int64_t cap = NCH / kAttnWarps > 0 ? NCH / kAttnWarps : 1;
+  const int64_t slots = (int64_t)kGB300SMs * (R <= 8 ? 3 : 2);
+  int64_t s = slots / units;
+  const int64_t nu = R <= 8 ? kAttnWarps : kAttnWarps / 2;
+  const int64_t cap = NCH / nu > 0 ? NCH / nu : 1;
   if (s > cap) s = cap;
   if (s < 1) s = 1;
   return (int)s;
 }
 
 size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L) {
-  const int G = H_q / H_kv, nrg = row_groups(G, T);
-  const int S = splits_for(batch, H_kv, nrg, L / 32);
-  return (size_t)batch * H_kv * nrg * S * kPartFloats * sizeof(float);
+  const int R = (H_q / H_kv) * T;
+  const int RP = rows_per_pass(R), nrg = row_groups(R);
+  const int S = splits_for(batch, H_kv, nrg, L / 32, R);
+  return (size_t)batch * H_kv * nrg * S * (2 * RP + RP * kD) * sizeof(float);
 }
 
-template <bool FULL>
+template <bool FULL, int NT, bool PAIR>
 static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
-  auto fn = attn_kernel<FULL>;
-  constexpr size_t smem = 32768 + (size_t)kAttnWarps * kScratchFloats * sizeof(float);
+  auto fn = attn_kernel<FULL, NT, PAIR>;
+  constexpr size_t xchg = PAIR ? (size_t)kAttnWarps * 2 * 32 * 8 * NT * sizeof(float) : 0;
+  constexpr size_t smem = kLutBytes + (size_t)kAttnWarps * kScratchFloats * sizeof(float) + xchg;
+  static_assert((size_t)(kAttnWarps / (PAIR ? 2 : 1)) * (2 + 128) * 8 * NT * sizeof(float) <= smem,
+                "merge buffers fit in the reused tables");
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -451,13 +553,16 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   if (configured_dev != dev) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   dim3 grid((unsigned)prm.S, (unsigned)prm.Hkv, (unsigned)(prm.batch * prm.nrg));
   fn<<<grid, kAttnWarps * 32, smem, stream>>>(prm, tab);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine<<<(unsigned)(prm.batch * prm.Hkv * prm.nrg), kD, 0, stream>>>(prm);
+  attn_combine<<<(unsigned)(prm.batch * prm.Hkv * prm.nrg), kD, 0, stream>>>(prm, 8 * NT);
   return cudaGetLastError();
 }
 
@@ -478,16 +583,19 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
   prm.Hkv = x.s.H;
   prm.G = x.H_q / x.s.H;
   prm.R = prm.G * x.T;
-  prm.nrg = row_groups(prm.G, x.T);
+  prm.nrg = row_groups(prm.R);
   prm.L = x.s.L;
   prm.NB = x.s.NB();
   prm.NCH = x.s.L / 32;
-  prm.S = splits_for(x.batch, prm.Hkv, prm.nrg, prm.NCH);
+  prm.S = splits_for(x.batch, prm.Hkv, prm.nrg, prm.NCH, prm.R);
   prm.P = x.s.page;
   prm.C = x.s.C;
   prm.NC = x.s.NC();
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
-  return x.full ? run_attn<true>(prm, tab, stream) : run_attn<false>(prm, tab, stream);
+  const bool small = prm.R <= 8;
+  if (x.full)
+    return small ? run_attn<true, 1, false>(prm, tab, stream) : run_attn<true, 4, true>(prm, tab, stream);
+  return small ? run_attn<false, 1, false>(prm, tab, stream) : run_attn<false, 4, true>(prm, tab, stream);
 }
 
 }  // namespace lynx

@@ -4,8 +4,8 @@
 //
 // Work unit: one page block = `page` tokens x 128 channels of one KV head.
 // A 2D TMA load stages the block's BF16 tile (page x 256 bytes, rows strided
-// by H*256 bytes in HBM) in shared memory; up to three tiles are in flight per
-// CTA while the CTA computes on an earlier one.
+// by H*256 bytes in HBM) in shared memory; the next one or two tiles are in
+// flight per CTA while the CTA computes on the current one.
 //
 // Thread layout for a block (2*page threads): lane = 16*e1 + g.  g selects 8
 // channels (16 bytes of a row, 4 bytes of each packed row); a thread holds 8
@@ -73,7 +73,10 @@ struct EncGeom {
   static constexpr int kTileBytes = P * kD * 2;
   static constexpr int kStages = kTileBytes <= 32768 ? 3 : 2;
   static constexpr int kMetaRows = 2 + 2 * kNC;
-  static constexpr int kRedFloats = kWarps * kD * (kWPC > 1 ? 4 : 2) + 2 * kD;
+  // min/max partials (2 x kWarps x 128), chunk-sum partials aliased onto
+  // the min partials, sigma partials (kWarps x 128, WPC > 1 only), and the
+  // per-channel gamma_min and 1/(gamma_scale + eps).
+  static constexpr int kRedFloats = kWarps * kD * (kWPC > 1 ? 3 : 2) + 2 * kD;
   static constexpr size_t kSmem =
       (size_t)kStages * kTileBytes + (size_t)kRedFloats * 4 + kStages * 8;
   static_assert(C >= 16 && C <= P, "chunk");
@@ -91,9 +94,13 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
   uint8_t* tiles = smem;
   float* red_mn = reinterpret_cast<float*>(smem + G::kStages * G::kTileBytes);
   float* red_mx = red_mn + G::kWarps * kD;
-  float* red_sum = red_mx + G::kWarps * kD;      // used when WPC > 1
-  float* red_sg = red_sum + G::kWarps * kD;      // used when WPC > 1
-  float* st_gmin = red_mn + G::kWarps * kD * (G::kWPC > 1 ? 4 : 2);
+  // Chunk-sum partials reuse red_mn: red_mn's last reads (stage 1b) are
+  // before the barrier that precedes the first red_sum write, and red_sum's
+  // last reads are before the barrier that precedes the next block's red_mn
+  // writes.
+  float* red_sum = red_mn;                       // used when WPC > 1
+  float* red_sg = red_mx + G::kWarps * kD;       // used when WPC > 1
+  float* st_gmin = red_mn + G::kWarps * kD * (G::kWPC > 1 ? 3 : 2);
   float* st_rg = st_gmin + kD;
   uint64_t* bars = reinterpret_cast<uint64_t*>(st_rg + kD);
 
@@ -168,6 +175,15 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       }
       return;
     }
+    // Every thread has finished the previous block, so its stage can be
+    // refilled with the block kStages-1 iterations ahead of this one.
+    if (tid == 0 && it > 0) {
+      const int64_t nxt = blk + (int64_t)(G::kStages - 1) * gridDim.x;
+      if (nxt < nblk) {
+        fence_proxy_async();
+        issue(nxt, (it - 1) % G::kStages);
+      }
+    }
 
     // ---- Stage 1b: gamma_min, gamma_scale, reciprocal (one thread/channel)
     float* mrow = meta + blk * (int64_t)(G::kMetaRows * kD);
@@ -208,14 +224,12 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       const uint4 v = tile[t * 16 + g];
       const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) n[m][k] = mul2(sub2(bf2_to_f2(vv[k]), gm2[k]), rg2[k]);
-    }
-    __syncthreads();  // every thread is done with this stage's tile
-    if (tid == 0) {
-      const int64_t nxt = blk + (int64_t)G::kStages * gridDim.x;
-      if (nxt < nblk) {
-        fence_proxy_async();
-        issue(nxt, stage);
+      for (int k = 0; k < 4; ++k) {
+        // scalar __fmul_rn, never contracted: a packed mul.rn.f32x2 here was
+        // fused with the first add of the chunk sum below
+        const f2 d = sub2(bf2_to_f2(vv[k]), gm2[k]);
+        n[m][k].x = __fmul_rn(d.x, rg2[k].x);
+        n[m][k].y = __fmul_rn(d.y, rg2[k].y);
       }
     }
 
@@ -369,6 +383,9 @@ static cudaError_t run_encode(const CUtensorMap& map, const Shape& s, const Comp
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, G::kThreads, G::kSmem);

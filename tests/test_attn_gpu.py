@@ -54,7 +54,7 @@ def _check(oracle_mod, q, k_np, v_np, out, L, P, C, full, pairs, H_q, H_kv, T):
     return worst
 
 
-def _run(lynx_lib, oracle_mod, dev, batch, L, H_kv, H_q, T, P, C, pairs, seed=0):
+def _run(lynx_lib, oracle_mod, dev, batch, L, H_kv, H_q, T, P, C, pairs, seed=0, T_anchor=1):
     from split_stream_kv_gb300 import synth
     kv = synth.kv_cache(2 * batch, L, H_kv, 128, seed=seed, device=dev)
     k = kv[0::2].contiguous()
@@ -64,7 +64,7 @@ def _run(lynx_lib, oracle_mod, dev, batch, L, H_kv, H_q, T, P, C, pairs, seed=0)
     k_np = tuple(t.cpu().numpy() for t in ks)
     v_np = tuple(t.cpu().numpy() for t in vs)
     results = {}
-    for mode, TT in ((lynx_lib.LYNX_ANCHOR, 1), (lynx_lib.LYNX_FULL, T)):
+    for mode, TT in ((lynx_lib.LYNX_ANCHOR, T_anchor), (lynx_lib.LYNX_FULL, T)):
         q = synth.queries(batch, TT, H_q, 128, seed=seed + TT, device=dev)
         full = mode == lynx_lib.LYNX_FULL
         ksm = ks if full else (ks[0], None, ks[2])
@@ -93,6 +93,17 @@ def test_gqa_groups_and_row_groups(lynx_lib, oracle_mod, cuda_dev):
                                    (128, 16, 640)])
 def test_page_and_chunk_sizes(lynx_lib, oracle_mod, cuda_dev, P, C, L):
     _run(lynx_lib, oracle_mod, cuda_dev, 1, L, 2, 4, 2, P, C, [(0, 0), (0, 1)], seed=P + C)
+
+
+@pytest.mark.parametrize("P,C,L,H_kv,H_q,T,Ta", [
+    (64, 16, 1024, 2, 8, 3, 2),      # 12 rows: padded warp-pair pass, two chunks per 32 tokens
+    (256, 64, 2048, 1, 8, 4, 1),     # 32 rows
+    (128, 16, 1024, 1, 3, 3, 3),     # 9 rows both modes
+    (128, 32, 768, 1, 16, 2, 1),     # 16 query heads per KV head: anchor mode with 16 rows
+])
+def test_row_counts_and_pairs(lynx_lib, oracle_mod, cuda_dev, P, C, L, H_kv, H_q, T, Ta):
+    pairs = [(0, h) for h in range(H_kv)]
+    _run(lynx_lib, oracle_mod, cuda_dev, 1, L, H_kv, H_q, T, P, C, pairs, seed=L + T, T_anchor=Ta)
 
 
 def test_decode_attention_full_size_sampled(lynx_lib, oracle_mod, cuda_dev):
