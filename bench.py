@@ -76,6 +76,53 @@ def bf16_equiv_bytes():
 ROWS = ["encode", "decode_anchor", "decode_full", "attn_draft", "attn_verify"]
 
 
+# Sources that define each row's kernel; the recorded DRAM traffic of a
+# kernel is only reported while these files are unchanged.
+ROW_SOURCES = {
+    "encode": ["encode.cu", "common.cuh", "internal.h"],
+    "decode_anchor": ["decode.cu", "common.cuh", "internal.h"],
+    "decode_full": ["decode.cu", "common.cuh", "internal.h"],
+    "attn_draft": ["attn.cu", "common.cuh", "internal.h"],
+    "attn_verify": ["attn.cu", "common.cuh", "internal.h"],
+}
+
+
+def sources_hash(row):
+    import hashlib
+    h = hashlib.sha256()
+    for name in ROW_SOURCES[row]:
+        with open(os.path.join(ROOT, "split_stream_kv_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(row, units_per_launch):
+    """DRAM bytes per launch of the row's kernel, scaled from the ncu capture
+    recorded in profiles/traffic.md, or None if there is none for the current
+    sources of the kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        for line in f:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) < 5 or cells[0] != row:
+                continue
+            try:
+                sha, units, nbytes = cells[1], float(cells[2]), float(cells[3])
+            except ValueError:
+                continue
+            if sha != sources_hash(row):
+                return None
+            return int(round(nbytes / units * units_per_launch))
+    return None
+
+
+def units_per_launch(row):
+    """Elements (KV elements read or written) one launch of the row handles."""
+    return codec_elems() if row in ("encode", "decode_anchor", "decode_full") else attn_kv_elems()
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -427,7 +474,8 @@ def main():
             ach = alg[name] / (ms / 1e3) / 1e9
             d = {"ms": round(ms, 4), "bf16_equiv_GBps": round(be[name] / (ms / 1e3) / 1e9, 1),
                  "algorithmic_bytes": int(alg[name]), "achieved_GBps": round(ach, 1),
-                 "roofline_frac": round(ach / peak, 4)}
+                 "roofline_frac": round(ach / peak, 4),
+                 "dram_traffic_bytes": recorded_traffic(name, units_per_launch(name))}
             if name.startswith("attn"):
                 T = ATTN["T_draft"] if name == "attn_draft" else ATTN["T_verify"]
                 d["tokens_per_s"] = round(ATTN["batch"] * T / (ms / 1e3), 1)
@@ -453,7 +501,8 @@ def main():
             "anchor_attention_tokens_per_s": rows.get("attn_draft", {}).get("tokens_per_s"),
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1),
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round(ach / peak, 4), "traffic": None},
+                         "frac": round(ach / peak, 4),
+                         "traffic": recorded_traffic(dom, units_per_launch(dom))},
             "e2e": None if r["e2e_s"] is None else {
                 "value": round(whole_job_gbps(step_bytes, world, r["e2e_s"]), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},

@@ -45,15 +45,31 @@
 namespace lynx {
 
 constexpr int kAttnWarps = 4;
-constexpr int kLutBytes = 32768;
-// Per-warp constant rows (gamma_min, gamma_scale+eps, mu, sigma+eps for two
-// 16-token halves) of K and V.  A row holds 128 channels in groups of 8,
-// stored as the pairs (k, k+4) of the nibble pairing so that one 16-byte load
-// gives two float2 operands, with 16 bytes of padding after every 4 groups so
-// that lanes reading different groups hit different banks.
+// The lookup table has 256 rows of 256 bytes, one per byte value (anchor
+// mode: one anchor byte = two channels; full mode: one 8-bit code).  The
+// first 128 bytes of a row are the lane-replicated entries (anchor: 16
+// lane slots x float2, full: 32 lanes x float), so a lookup address is
+// (byte << 8) | lane_offset: a single byte permute.  The second 128 bytes of
+// every row hold the per-warp constant scratch.
+constexpr int kLutBytes = 65536;
+// Per-warp constant rows (gamma_min, gamma_scale+eps, mu, sigma+eps; mu and
+// sigma once more for the second 16-token half when C = 16) of K and V.  A
+// row holds 128 channels in groups of 8, stored as the pairs (k, k+4) of the
+// nibble pairing so that one 16-byte load gives two float2 operands, with 16
+// bytes of padding after every 4 groups so that lanes reading different
+// groups hit different banks.  Float f of the scratch lives at byte
+// (f / 32) * 256 + 128 + (f % 32) * 4 of the table.
 constexpr int kRowFloats = 144;
-constexpr int kScratchRows = 12;
-constexpr int kScratchFloats = kScratchRows * kRowFloats;
+template <bool ONE>
+struct Scratch {
+  static constexpr int kRows = ONE ? 4 : 6;                 // per tensor
+  static constexpr int kFloats = 2 * kRows * kRowFloats;    // K and V
+};
+static_assert(kAttnWarps * Scratch<false>::kFloats <= 256 * 32, "scratch fits the table rows");
+
+__device__ __forceinline__ uint32_t scr_byte(int f) {
+  return ((uint32_t)(f >> 5) << 8) | 128u | ((uint32_t)(f & 31) << 2);
+}
 
 struct AttnParams {
   const uint16_t* q;
@@ -84,6 +100,14 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
 }
 template <int N>
 struct Bytes;  // N packed bytes loaded from one row
@@ -116,59 +140,60 @@ __device__ __forceinline__ int grp_off(int grp) { return grp * 8 + (grp >> 2) * 
 struct Consts {  // pairs (k, k+4) of one channel group, k = 0..3
   f2 gm[4], gs[4], mu[4], sg[4];
 };
-__device__ __forceinline__ void load_consts(Consts& k, const float* rows, int grp, int jrow) {
-  const float* base = rows + grp_off(grp);
-  const float4 g0 = *reinterpret_cast<const float4*>(base + 0 * kRowFloats);
-  const float4 g1 = *reinterpret_cast<const float4*>(base + 0 * kRowFloats + 4);
-  const float4 s0 = *reinterpret_cast<const float4*>(base + 1 * kRowFloats);
-  const float4 s1 = *reinterpret_cast<const float4*>(base + 1 * kRowFloats + 4);
-  const float4 m0 = *reinterpret_cast<const float4*>(base + (2 + 2 * jrow) * kRowFloats);
-  const float4 m1 = *reinterpret_cast<const float4*>(base + (2 + 2 * jrow) * kRowFloats + 4);
-  const float4 a0 = *reinterpret_cast<const float4*>(base + (3 + 2 * jrow) * kRowFloats);
-  const float4 a1 = *reinterpret_cast<const float4*>(base + (3 + 2 * jrow) * kRowFloats + 4);
+__device__ __forceinline__ float4 ld_scr(const uint8_t* smem, int f) {
+  return *reinterpret_cast<const float4*>(smem + scr_byte(f));
+}
+// rows: first float of this tensor's rows in the warp's scratch.
+__device__ __forceinline__ void load_consts(Consts& k, const uint8_t* smem, int rows, int grp,
+                                            int jrow) {
+  const int base = rows + grp_off(grp);
+  const float4 g0 = ld_scr(smem, base), g1 = ld_scr(smem, base + 4);
+  const float4 s0 = ld_scr(smem, base + kRowFloats), s1 = ld_scr(smem, base + kRowFloats + 4);
+  const int mr = base + (2 + 2 * jrow) * kRowFloats, ar = base + (3 + 2 * jrow) * kRowFloats;
+  const float4 m0 = ld_scr(smem, mr), m1 = ld_scr(smem, mr + 4);
+  const float4 a0 = ld_scr(smem, ar), a1 = ld_scr(smem, ar + 4);
   k.gm[0] = {g0.x, g0.y}; k.gm[1] = {g0.z, g0.w}; k.gm[2] = {g1.x, g1.y}; k.gm[3] = {g1.z, g1.w};
   k.gs[0] = {s0.x, s0.y}; k.gs[1] = {s0.z, s0.w}; k.gs[2] = {s1.x, s1.y}; k.gs[3] = {s1.z, s1.w};
   k.mu[0] = {m0.x, m0.y}; k.mu[1] = {m0.z, m0.w}; k.mu[2] = {m1.x, m1.y}; k.mu[3] = {m1.z, m1.w};
   k.sg[0] = {a0.x, a0.y}; k.sg[1] = {a0.z, a0.w}; k.sg[2] = {a1.x, a1.y}; k.sg[3] = {a1.z, a1.w};
 }
 
-// Values of the two channels of byte `pos` (0..3) of an anchor word a (and,
-// in full mode, residual word r): (low-nibble channel, high-nibble channel).
-template <bool FULL>
-__device__ __forceinline__ f2 lookup_pair(const uint8_t* lut, uint32_t a, uint32_t r, int pos,
+// Table byte address of byte `pos` (0..3) of word w, row-major with lane_off.
+template <int POS>
+__device__ __forceinline__ uint32_t lut_addr(uint32_t w, uint32_t lane_off) {
+  // result bytes: [lane_off.b0, w.b_POS, 0, 0] (lane_off < 256)
+  return prmt(w, lane_off, 0x6504u | ((uint32_t)POS << 4));
+}
+
+// Values of the two channels of byte POS of an anchor word a (and, in full
+// mode, of residual word r): (low-nibble channel, high-nibble channel).
+template <bool FULL, int POS>
+__device__ __forceinline__ f2 lookup_pair(const uint8_t* lut, uint32_t a, uint32_t r,
                                           uint32_t lane_off) {
   if constexpr (FULL) {
     const uint32_t E = ((a << 4) & 0xf0f0f0f0u) | (r & 0x0f0f0f0fu);  // low-nibble codes
     const uint32_t O = (a & 0xf0f0f0f0u) | ((r >> 4) & 0x0f0f0f0fu);  // high-nibble codes
-    // byte pos of E / O times 128 (32 lanes x 4 bytes) + lane * 4
-    const int sh = 8 * pos - 7;
-    const uint32_t ae = ((sh >= 0 ? E >> sh : E << -sh) & 0x7f80u) | lane_off;
-    const uint32_t ao = ((sh >= 0 ? O >> sh : O << -sh) & 0x7f80u) | lane_off;
     f2 v;
-    v.x = *reinterpret_cast<const float*>(lut + ae);
-    v.y = *reinterpret_cast<const float*>(lut + ao);
+    v.x = *reinterpret_cast<const float*>(lut + lut_addr<POS>(E, lane_off));
+    v.y = *reinterpret_cast<const float*>(lut + lut_addr<POS>(O, lane_off));
     return v;
   } else {
-    // byte pos of a times 128 (16 lane slots x 8 bytes) + (lane % 16) * 8
-    const int sh = 8 * pos - 7;
-    const uint32_t ad = ((sh >= 0 ? a >> sh : a << -sh) & 0x7f80u) | lane_off;
-    const float2 p = *reinterpret_cast<const float2*>(lut + ad);
+    const float2 p = *reinterpret_cast<const float2*>(lut + lut_addr<POS>(a, lane_off));
     return f2{p.x, p.y};
   }
 }
 
 // One packed byte position -> bf16x2 of the exact decoder output
 // (low-nibble channel in the low half).
-template <bool FULL>
+template <bool FULL, int POS>
 __device__ __forceinline__ uint32_t dequant_pair(const uint8_t* lut, uint32_t a, uint32_t r,
-                                                 int pos, uint32_t lane_off, f2 gm, f2 gs, f2 mu,
-                                                 f2 sg) {
-  const f2 v = lookup_pair<FULL>(lut, a, r, pos, lane_off);
-  const f2 x = fma2(fma2(v, sg, mu), gs, gm);
+                                                 uint32_t lane_off, const Consts& k) {
+  const f2 v = lookup_pair<FULL, POS>(lut, a, r, lane_off);
+  const f2 x = fma2(fma2(v, k.sg[POS], k.mu[POS]), k.gs[POS], k.gm[POS]);
   return f2_to_bf2(x.x, x.y);
 }
 
-template <bool FULL, int NT, bool PAIR>
+template <bool FULL, int NT, bool PAIR, bool ONE>
 __global__ void __launch_bounds__(kAttnWarps * 32, PAIR ? 2 : 3)
 attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ ExpandTable tab) {
   constexpr int KCH = PAIR ? 64 : 128;  // channels of K and of V per warp
@@ -177,29 +202,27 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   constexpr int VB = KCH / 16;          // V bytes per token row per lane (g)
   constexpr int NU = PAIR ? kAttnWarps / 2 : kAttnWarps;  // work units per CTA
   constexpr int RP = 8 * NT;            // query rows per pass
+  using SC = Scratch<ONE>;
 
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* lut = smem;
-  float* scratch_all = reinterpret_cast<float*>(smem + kLutBytes);
-  float* xchg_all = scratch_all + kAttnWarps * kScratchFloats;  // pair: partial scores
+  float* xchg_all = reinterpret_cast<float*>(smem + kLutBytes);  // pair: partial scores
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   const int unit = PAIR ? (w >> 1) : w;
   const int half = PAIR ? (w & 1) : 0;
   const int hb = half * 32;             // first byte of this warp's channel half
 
-  if constexpr (FULL) {
-    float* t = reinterpret_cast<float*>(lut);
-    for (int i = tid; i < 256 * 32; i += kAttnWarps * 32) {
-      const int code = i >> 5;
-      t[i] = code < 128 ? tab.x[code] : -tab.x[255 - code];
-    }
-  } else {
-    float2* t = reinterpret_cast<float2*>(lut);
-    for (int i = tid; i < 256 * 16; i += kAttnWarps * 32) {
-      const int byte = i >> 4, a0 = byte & 15, a1 = byte >> 4;
-      t[i] = make_float2(a0 < 8 ? tab.x[16 * a0 + 7] : -tab.x[16 * (15 - a0) + 7],
-                         a1 < 8 ? tab.x[16 * a1 + 7] : -tab.x[16 * (15 - a1) + 7]);
+  for (int i = tid; i < 256 * 32; i += kAttnWarps * 32) {
+    const int row = i >> 5, l = i & 31;
+    if constexpr (FULL) {
+      reinterpret_cast<float*>(lut + row * 256)[l] =
+          row < 128 ? tab.x[row] : -tab.x[255 - row];
+    } else if (l < 16) {
+      const int a0 = row & 15, a1 = row >> 4;
+      reinterpret_cast<float2*>(lut + row * 256)[l] =
+          make_float2(a0 < 8 ? tab.x[16 * a0 + 7] : -tab.x[16 * (15 - a0) + 7],
+                      a1 < 8 ? tab.x[16 * a1 + 7] : -tab.x[16 * (15 - a1) + 7]);
     }
   }
   __syncthreads();
@@ -227,7 +250,8 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       }
   }
 
-  float* scr = scratch_all + w * kScratchFloats;   // K rows 0..5, V rows 6..11
+  const int scr = w * SC::kFloats;     // this warp's scratch (K rows, then V rows)
+  const int scrV = scr + SC::kRows * kRowFloats;
   const int64_t cb = a.NCH * split / a.S, ce = a.NCH * (split + 1) / a.S;
   float m_run[NT][2], l_run[NT][2];
   float o[NKT][NT][4];
@@ -239,7 +263,6 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     for (int i = 0; i < NKT; ++i) o[i][nt][0] = o[i][nt][1] = o[i][nt][2] = o[i][nt][3] = 0.f;
   }
   const int meta_rows = 2 + 2 * a.NC;
-  const bool one_chunk = a.C >= 32;      // both 16-token halves share mu, sigma
   int it = 0;
 
   for (int64_t qc = cb + unit; qc < ce; qc += NU, ++it) {
@@ -265,17 +288,29 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       vA[ii].load(a.va + code_off + row * 64 + hb + VB * g);
       if constexpr (FULL) vR[ii].load(a.vr + code_off + row * 64 + hb + VB * g);
     }
+    // ---- warm L2 with the next chunk of this unit (2 KB per stream)
+    if (qc + NU < ce) {
+      const int64_t t1 = (qc + NU) * 32;
+      const int64_t p1 = t1 / a.P;
+      const int64_t blk1 = ((int64_t)b * a.NB + p1) * a.Hkv + h;
+      const int64_t off1 = (blk1 * a.P + (t1 - p1 * a.P)) * (kD / 2) + lane * 64;
+      prefetch_l2(a.ka + off1);
+      prefetch_l2(a.va + off1);
+      if constexpr (FULL) {
+        prefetch_l2(a.kr + off1);
+        prefetch_l2(a.vr + off1);
+      }
+    }
     // ---- constant rows -> scratch (pairs (k, k+4) interleaved, +eps folded)
     {
       const int cc0 = tp / a.C, cc1 = (tp + 16) / a.C;
-      const int nrow = one_chunk ? 4 : 6;
       const int grp = lane >> 1, hf = lane & 1;
 #pragma unroll
       for (int tsr = 0; tsr < 2; ++tsr) {
         const float* mb = (tsr == 0 ? a.km : a.vm) + blk * (int64_t)meta_rows * kD + 8 * grp + 2 * hf;
+        const int rows = tsr == 0 ? scr : scrV;
 #pragma unroll
-        for (int rr = 0; rr < 6; ++rr) {
-          if (rr >= nrow) break;
+        for (int rr = 0; rr < SC::kRows; ++rr) {
           const int src = rr == 0 ? 0 : rr == 1 ? 1 : rr == 2 ? 2 + cc0 : rr == 3 ? 2 + a.NC + cc0
                         : rr == 4 ? 2 + cc1 : 2 + a.NC + cc1;
           const float2 lo = __ldg(reinterpret_cast<const float2*>(mb + src * kD));
@@ -285,7 +320,7 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
             v.x = __fadd_rn(v.x, kEps); v.y = __fadd_rn(v.y, kEps);
             v.z = __fadd_rn(v.z, kEps); v.w = __fadd_rn(v.w, kEps);
           }
-          *reinterpret_cast<float4*>(scr + (tsr * 6 + rr) * kRowFloats + grp_off(grp) + 4 * hf) = v;
+          *reinterpret_cast<float4*>(smem + scr_byte(rows + rr * kRowFloats + grp_off(grp) + 4 * hf)) = v;
         }
       }
     }
@@ -297,32 +332,42 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) s[j][nt][0] = s[j][nt][1] = s[j][nt][2] = s[j][nt][3] = 0.f;
-#pragma unroll
-    for (int gi = 0; gi < KB / 4; ++gi) {      // channel groups of this lane (K)
-      const int grp = (hb + KB * c) / 4 + gi;
-      Consts k0, k1;
-      load_consts(k0, scr, grp, 0);
-      if (!one_chunk) load_consts(k1, scr, grp, 1);
+    // one 16-token m-tile j of the scores with this group's constants
+    auto qk = [&](const Consts& kc, int j, int gi) {
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int kt = 2 * gi + kk;
+        uint32_t af[4];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {       // row g (i=0) / g+8 (i=1)
+          const uint32_t wa = kA[2 * j + i].w[gi];
+          const uint32_t wr = FULL ? kR[2 * j + i].w[gi] : 0u;
+          if (kk == 0) {                    // k 2c..2c+1 / 2c+8..2c+9 = bytes 0 / 1
+            af[i] = dequant_pair<FULL, 0>(lut, wa, wr, lane_off, kc);
+            af[i + 2] = dequant_pair<FULL, 1>(lut, wa, wr, lane_off, kc);
+          } else {                          // bytes 2 / 3
+            af[i] = dequant_pair<FULL, 2>(lut, wa, wr, lane_off, kc);
+            af[i + 2] = dequant_pair<FULL, 3>(lut, wa, wr, lane_off, kc);
+          }
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(s[j][nt], af, qf[kt][nt][0], qf[kt][nt][1]);
+      }
+    };
+#pragma unroll
+    for (int gi = 0; gi < KB / 4; ++gi) {      // channel groups of this lane (K)
+      const int grp = (hb + KB * c) / 4 + gi;
+      if constexpr (ONE) {
+        Consts kc;
+        load_consts(kc, smem, scr, grp, 0);
+        qk(kc, 0, gi);
+        qk(kc, 1, gi);
+      } else {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const Consts& kc = (j == 0 || one_chunk) ? k0 : k1;
-          uint32_t af[4];
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {       // row g (i=0) / g+8 (i=1)
-            const uint32_t wa = kA[2 * j + i].w[gi];
-            const uint32_t wr = FULL ? kR[2 * j + i].w[gi] : 0u;
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {  // k 2c..2c+1 (hh=0) / 2c+8.. (hh=1)
-              const int pos = 2 * kk + hh;    // byte in the word = pair (pos, pos+4)
-              af[i + 2 * hh] = dequant_pair<FULL>(lut, wa, wr, pos, lane_off, kc.gm[pos],
-                                                  kc.gs[pos], kc.mu[pos], kc.sg[pos]);
-            }
-          }
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16(s[j][nt], af, qf[kt][nt][0], qf[kt][nt][1]);
+          Consts kc;
+          load_consts(kc, smem, scr, grp, j);
+          qk(kc, j, gi);
         }
       }
     }
@@ -361,7 +406,7 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       const float mn0 = fmaxf(m_run[nt][0], cmax0 * a.scale_log2);
       const float mn1 = fmaxf(m_run[nt][1], cmax1 * a.scale_log2);
       if (mn0 != m_run[nt][0] || mn1 != m_run[nt][1]) {
-        const float al0 = exp2f(m_run[nt][0] - mn0), al1 = exp2f(m_run[nt][1] - mn1);
+        const float al0 = ex2(m_run[nt][0] - mn0), al1 = ex2(m_run[nt][1] - mn1);
         l_run[nt][0] *= al0;
         l_run[nt][1] *= al1;
 #pragma unroll
@@ -373,10 +418,10 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float p0 = exp2f(fmaf(s[j][nt][0], a.scale_log2, -mn0));
-        const float p1 = exp2f(fmaf(s[j][nt][1], a.scale_log2, -mn1));
-        const float p2 = exp2f(fmaf(s[j][nt][2], a.scale_log2, -mn0));
-        const float p3 = exp2f(fmaf(s[j][nt][3], a.scale_log2, -mn1));
+        const float p0 = ex2(fmaf(s[j][nt][0], a.scale_log2, -mn0));
+        const float p1 = ex2(fmaf(s[j][nt][1], a.scale_log2, -mn1));
+        const float p2 = ex2(fmaf(s[j][nt][2], a.scale_log2, -mn0));
+        const float p3 = ex2(fmaf(s[j][nt][3], a.scale_log2, -mn1));
         l_run[nt][0] += p0 + p2;
         l_run[nt][1] += p1 + p3;
         const uint32_t top = f2_to_bf2(p0, p1), bot = f2_to_bf2(p2, p3);
@@ -389,36 +434,46 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     }
 
     // ---- output: O^T += V^T P^T over this warp's V m-tiles (byte VB*g + mt)
-#pragma unroll
-    for (int gi = 0; gi < (VB + 3) / 4; ++gi) {
-      const int grp = (hb + VB * g) / 4 + gi;
-      Consts k0, k1;
-      load_consts(k0, scr + 6 * kRowFloats, grp, 0);
-      if (!one_chunk) load_consts(k1, scr + 6 * kRowFloats, grp, 1);
+    auto pv = [&](const Consts& kc, int jt, int gi) {
 #pragma unroll
       for (int kk = 0; kk < (VB < 4 ? VB : 4); ++kk) {
         const int mt = 4 * gi + kk;
+        uint32_t W[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {   // tokens 2c, 2c+1, 2c+8, 2c+9
+          const uint32_t wa = vA[4 * jt + q4].w[gi];
+          const uint32_t wr = FULL ? vR[4 * jt + q4].w[gi] : 0u;
+          W[q4] = kk == 0 ? dequant_pair<FULL, 0>(lut, wa, wr, lane_off, kc)
+                : kk == 1 ? dequant_pair<FULL, 1>(lut, wa, wr, lane_off, kc)
+                : kk == 2 ? dequant_pair<FULL, 2>(lut, wa, wr, lane_off, kc)
+                          : dequant_pair<FULL, 3>(lut, wa, wr, lane_off, kc);
+        }
+        uint32_t af[4];
+        af[0] = prmt(W[0], W[1], 0x5410u);  // row g   (low channel), tokens 2c, 2c+1
+        af[1] = prmt(W[0], W[1], 0x7632u);  // row g+8 (high channel)
+        af[2] = prmt(W[2], W[3], 0x5410u);  // row g,   tokens 2c+8, 2c+9
+        af[3] = prmt(W[2], W[3], 0x7632u);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16(o[mt][nt], af, pb_hi[jt][nt][0], pb_hi[jt][nt][1]);
+          mma_bf16(o[mt][nt], af, pb_lo[jt][nt][0], pb_lo[jt][nt][1]);
+        }
+      }
+    };
+#pragma unroll
+    for (int gi = 0; gi < (VB + 3) / 4; ++gi) {
+      const int grp = (hb + VB * g) / 4 + gi;
+      if constexpr (ONE) {
+        Consts kc;
+        load_consts(kc, smem, scrV, grp, 0);
+        pv(kc, 0, gi);
+        pv(kc, 1, gi);
+      } else {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const Consts& kc = (j == 0 || one_chunk) ? k0 : k1;
-          uint32_t W[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {   // tokens 2c, 2c+1, 2c+8, 2c+9
-            const uint32_t wa = vA[4 * j + q4].w[gi];
-            const uint32_t wr = FULL ? vR[4 * j + q4].w[gi] : 0u;
-            W[q4] = dequant_pair<FULL>(lut, wa, wr, kk, lane_off, kc.gm[kk], kc.gs[kk],
-                                       kc.mu[kk], kc.sg[kk]);
-          }
-          uint32_t af[4];
-          af[0] = prmt(W[0], W[1], 0x5410u);  // row g   (low channel), tokens 2c, 2c+1
-          af[1] = prmt(W[0], W[1], 0x7632u);  // row g+8 (high channel)
-          af[2] = prmt(W[2], W[3], 0x5410u);  // row g,   tokens 2c+8, 2c+9
-          af[3] = prmt(W[2], W[3], 0x7632u);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_bf16(o[mt][nt], af, pb_hi[j][nt][0], pb_hi[j][nt][1]);
-            mma_bf16(o[mt][nt], af, pb_lo[j][nt][0], pb_lo[j][nt][1]);
-          }
+          Consts kc;
+          load_consts(kc, smem, scrV, grp, j);
+          pv(kc, j, gi);
         }
       }
     }
@@ -539,11 +594,11 @@ size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L) {
   return (size_t)batch * H_kv * nrg * S * (2 * RP + RP * kD) * sizeof(float);
 }
 
-template <bool FULL, int NT, bool PAIR>
+template <bool FULL, int NT, bool PAIR, bool ONE>
 static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
-  auto fn = attn_kernel<FULL, NT, PAIR>;
+  auto fn = attn_kernel<FULL, NT, PAIR, ONE>;
   constexpr size_t xchg = PAIR ? (size_t)kAttnWarps * 2 * 32 * 8 * NT * sizeof(float) : 0;
-  constexpr size_t smem = kLutBytes + (size_t)kAttnWarps * kScratchFloats * sizeof(float) + xchg;
+  constexpr size_t smem = kLutBytes + xchg;
   static_assert((size_t)(kAttnWarps / (PAIR ? 2 : 1)) * (2 + 128) * 8 * NT * sizeof(float) <= smem,
                 "merge buffers fit in the reused tables");
   static thread_local int configured_dev = -1;
@@ -564,6 +619,12 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   if (e != cudaSuccess) return e;
   attn_combine<<<(unsigned)(prm.batch * prm.Hkv * prm.nrg), kD, 0, stream>>>(prm, 8 * NT);
   return cudaGetLastError();
+}
+
+template <bool FULL, int NT, bool PAIR>
+static cudaError_t run_attn_c(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
+  return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true>(prm, tab, stream)
+                     : run_attn<FULL, NT, PAIR, false>(prm, tab, stream);
 }
 
 cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t stream) {
@@ -594,8 +655,10 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   const bool small = prm.R <= 8;
   if (x.full)
-    return small ? run_attn<true, 1, false>(prm, tab, stream) : run_attn<true, 4, true>(prm, tab, stream);
-  return small ? run_attn<false, 1, false>(prm, tab, stream) : run_attn<false, 4, true>(prm, tab, stream);
+    return small ? run_attn_c<true, 1, false>(prm, tab, stream)
+                 : run_attn_c<true, 4, true>(prm, tab, stream);
+  return small ? run_attn_c<false, 1, false>(prm, tab, stream)
+               : run_attn_c<false, 4, true>(prm, tab, stream);
 }
 
 }  // namespace lynx

@@ -80,6 +80,16 @@ __device__ __forceinline__ uint32_t f2_to_bf2(float x, float y) {
   return r;
 }
 
+// (lo(w) - c, hi(w) - c) for the two bf16 halves of w: each half converted
+// exactly to f32, then one round-to-nearest subtraction.
+__device__ __forceinline__ f2 bf2_sub_f32(uint32_t w, f2 c) {
+  f2 r;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+      " sub.rn.f32.bf16 %0, lo, %3;\n sub.rn.f32.bf16 %1, hi, %4;\n}"
+      : "=f"(r.x), "=f"(r.y) : "r"(w), "f"(c.x), "f"(c.y));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

@@ -227,7 +227,7 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       for (int k = 0; k < 4; ++k) {
         // scalar __fmul_rn, never contracted: a packed mul.rn.f32x2 here was
         // fused with the first add of the chunk sum below
-        const f2 d = sub2(bf2_to_f2(vv[k]), gm2[k]);
+        const f2 d = bf2_sub_f32(vv[k], gm2[k]);
         n[m][k].x = __fmul_rn(d.x, rg2[k].x);
         n[m][k].y = __fmul_rn(d.y, rg2[k].y);
       }
@@ -330,7 +330,6 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       const int t = c * C + m * 2 * G::kWPC + e1 * G::kWPC + u;
       float a[8];
       uint32_t bits[8], dbits[8];
-      bool amb = false;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const f2 xf = mul2(n[m][k], rs2[k]);
@@ -340,10 +339,12 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
         dbits[2 * k + 1] = __float_as_uint(n[m][k].y);
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        bits[i] = compand_fast(a[i], alpha, c16);
-        amb |= compand_ambiguous(bits[i]);
-      }
+      for (int i = 0; i < 8; ++i) bits[i] = compand_fast(a[i], alpha, c16);
+      // smallest distance to a rounding boundary (low 16 bits) of the 8
+      // values, two at a time in 16-bit lanes
+      uint32_t dmin = __vminu2(prmt(bits[0], bits[1], 0x5410u), prmt(bits[2], bits[3], 0x5410u));
+      dmin = __vminu2(dmin, __vminu2(prmt(bits[4], bits[5], 0x5410u), prmt(bits[6], bits[7], 0x5410u)));
+      const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
       if (__any_sync(kFull, amb)) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
