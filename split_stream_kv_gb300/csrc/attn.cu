@@ -44,32 +44,68 @@
 
 namespace lynx {
 
-constexpr int kAttnWarps = 4;
-// The lookup table has 256 rows of 256 bytes, one per byte value (anchor
-// mode: one anchor byte = two channels; full mode: one 8-bit code).  The
-// first 128 bytes of a row are the lane-replicated entries (anchor: 16
-// lane slots x float2, full: 32 lanes x float), so a lookup address is
-// (byte << 8) | lane_offset: a single byte permute.  The second 128 bytes of
-// every row hold the per-warp constant scratch.
+// Shared memory of one CTA (offsets from the start of the dynamic window):
+//  [0, 64 KiB)  lookup table, 256 rows of 256 bytes, one row per byte value
+//               (anchor mode: one anchor byte = two channels; full mode: one
+//               8-bit code).  The first 128 bytes of a row are the
+//               lane-replicated entries (anchor: 16 lane slots x float2, full:
+//               32 lanes x float); the second 128 bytes ("tails") hold the
+//               per-warp constant rows.  A lookup address is
+//               (byte << 8) | lane_offset, one byte permute, plus the
+//               constant shared-window base as the load's immediate offset.
+//  [64 KiB, ..) Q fragments, the partner-score exchange of the warp-pair
+//               shape, and at the end the merge buffers.
 constexpr int kLutBytes = 65536;
-// Per-warp constant rows (gamma_min, gamma_scale+eps, mu, sigma+eps; mu and
-// sigma once more for the second 16-token half when C = 16) of K and V.  A
-// row holds 128 channels in groups of 8, stored as the pairs (k, k+4) of the
-// nibble pairing so that one 16-byte load gives two float2 operands, with 16
-// bytes of padding after every 4 groups so that lanes reading different
-// groups hit different banks.  Float f of the scratch lives at byte
-// (f / 32) * 256 + 128 + (f % 32) * 4 of the table.
-constexpr int kRowFloats = 144;
-template <bool ONE>
-struct Scratch {
-  static constexpr int kRows = ONE ? 4 : 6;                 // per tensor
-  static constexpr int kFloats = 2 * kRows * kRowFloats;    // K and V
-};
-static_assert(kAttnWarps * Scratch<false>::kFloats <= 256 * 32, "scratch fits the table rows");
+// Shared-window address of the first byte of dynamic shared memory for a
+// kernel without static shared memory: the block's reserved shared memory
+// (1 KiB on sm_100-class GPUs) comes first.  The host checks the device
+// attribute before launching and the kernel checks the address itself.
+constexpr uint32_t kSmemBase = 1024;
 
-__device__ __forceinline__ uint32_t scr_byte(int f) {
-  return ((uint32_t)(f >> 5) << 8) | 128u | ((uint32_t)(f & 31) << 2);
+template <bool FULL, bool PAIR, bool ONE>
+struct Cfg {
+  // 8 warps where everything fits 128 registers (anchor codes, up to 8 rows,
+  // C >= 32: two CTAs = 16 warps per SM), else 4 warps at up to 255.
+  static constexpr int kWarps = (!FULL && !PAIR && ONE) ? 8 : 4;
+  static constexpr int kNU = PAIR ? kWarps / 2 : kWarps;  // work units
+  // Constant rows per tensor: gamma_min, gamma_scale, then (mu, sigma) of
+  // the chunk of each 16-token half (one pair when C >= 32).
+  static constexpr int kRows = ONE ? 4 : 6;
+  static constexpr int kTails = 2 * kRows * 4;  // per warp: K then V, 4 tails a row
+  static_assert(kWarps * kTails <= 256, "constant rows fit the table tails");
+};
+
+// Bytes after the table: during the chunk loop the staged Q fragments (one
+// set per segment), the pair exchange and the packed-block bases of the two
+// segments; at the end the merge buffers.
+template <bool FULL, bool PAIR, bool ONE, int NT>
+struct ExtraLayout {
+  using CF = Cfg<FULL, PAIR, ONE>;
+  static constexpr int NKT = PAIR ? 4 : 8;
+  static constexpr size_t kQ = PAIR ? 0 : (size_t)2 * NKT * NT * 32 * 8;
+  static constexpr size_t kXchg = PAIR ? (size_t)CF::kWarps * 2 * 32 * 8 * NT * 4 : 0;
+  static constexpr size_t kInfo = kQ + kXchg;  // int64 block base of segments 0, 1
+  static constexpr size_t kLoop = kInfo + 16;
+  static constexpr size_t kMerge = (size_t)CF::kNU * 8 * NT * (2 + kD) * 4 + (size_t)CF::kNU * 8;
+  static constexpr size_t kBytes = kLoop > kMerge ? kLoop : kMerge;
+};
+template <bool FULL, bool PAIR, bool ONE, int NT>
+constexpr size_t attn_smem_bytes() {
+  return kLutBytes + ExtraLayout<FULL, PAIR, ONE, NT>::kBytes;
 }
+
+// Byte offset (from the table start) of float4 unit h (0, 1) of channel
+// group grp (8 channels) in constant row r of a tensor whose rows start at
+// tail tb.  A row is 4 tails of 128 bytes; tail (grp >> 2) of the row holds
+// groups 4(grp>>2) .. +3 at 32-byte slots XOR-swizzled by the tail index, so
+// that lanes reading the same group slot of different tails hit different
+// banks.  Unit h of a group holds the pairs (k, k+4) and (k+1, k+5) for
+// k = 2h: the channels of nibble positions 2h and 2h+1 of the group's bytes.
+__device__ __forceinline__ uint32_t unit_off(int tb, int r, int grp, int h) {
+  return (uint32_t)((tb + r * 4 + (grp >> 2)) * 256 + 128 + (((grp & 3) ^ ((grp >> 2) & 3)) << 5) +
+                    h * 16);
+}
+constexpr int kRowStride = 4 * 256;  // bytes between constant rows
 
 struct AttnParams {
   const uint16_t* q;
@@ -77,9 +113,11 @@ struct AttnParams {
   const float *km, *vm;
   float* part;
   float* out;
-  int batch, T, Hq, Hkv, G, R, nrg, S;
+  int batch, T, Hq, Hkv, G, R, nrg;
   int64_t L, NB, NCH;
-  int P, C, NC;
+  int64_t n_chunks;  // units x NCH: the flattened (unit, chunk) space
+  int n_cta;         // CTAs of the attention grid
+  int P, C, NC, lgP, lgC;
   float scale_log2;
 };
 
@@ -109,6 +147,28 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
 }
+// Table reads.  The table is written once before the first barrier and never
+// again, so these loads carry no ordering against other memory operations.
+__device__ __forceinline__ float2 lut_f2(uint32_t off) {
+  float2 v;
+  asm("ld.shared.v2.f32 {%0,%1}, [%2+1024];" : "=f"(v.x), "=f"(v.y) : "r"(off));
+  return v;
+}
+__device__ __forceinline__ float lut_f1(uint32_t off) {
+  float v;
+  asm("ld.shared.f32 %0, [%1+1024];" : "=f"(v) : "r"(off));
+  return v;
+}
+static_assert(kSmemBase == 1024, "immediate offset of the table loads");
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory");
+}
+
 template <int N>
 struct Bytes;  // N packed bytes loaded from one row
 template <>
@@ -134,125 +194,192 @@ struct Bytes<4> {
   }
 };
 
-// Float offset of the first of channel group grp's 8 values in a row.
-__device__ __forceinline__ int grp_off(int grp) { return grp * 8 + (grp >> 2) * 4; }
-
-struct Consts {  // pairs (k, k+4) of one channel group, k = 0..3
-  f2 gm[4], gs[4], mu[4], sg[4];
+// Constants of two nibble positions (2hh, 2hh+1) of one channel group: the
+// pairs (k, k+4) for k = 2hh, 2hh+1, with epsilon added to both scales.
+struct Half {
+  f2 gm[2], gs[2], mu[2], sg[2];
 };
-__device__ __forceinline__ float4 ld_scr(const uint8_t* smem, int f) {
-  return *reinterpret_cast<const float4*>(smem + scr_byte(f));
-}
-// rows: first float of this tensor's rows in the warp's scratch.
-__device__ __forceinline__ void load_consts(Consts& k, const uint8_t* smem, int rows, int grp,
-                                            int jrow) {
-  const int base = rows + grp_off(grp);
-  const float4 g0 = ld_scr(smem, base), g1 = ld_scr(smem, base + 4);
-  const float4 s0 = ld_scr(smem, base + kRowFloats), s1 = ld_scr(smem, base + kRowFloats + 4);
-  const int mr = base + (2 + 2 * jrow) * kRowFloats, ar = base + (3 + 2 * jrow) * kRowFloats;
-  const float4 m0 = ld_scr(smem, mr), m1 = ld_scr(smem, mr + 4);
-  const float4 a0 = ld_scr(smem, ar), a1 = ld_scr(smem, ar + 4);
-  k.gm[0] = {g0.x, g0.y}; k.gm[1] = {g0.z, g0.w}; k.gm[2] = {g1.x, g1.y}; k.gm[3] = {g1.z, g1.w};
-  k.gs[0] = {s0.x, s0.y}; k.gs[1] = {s0.z, s0.w}; k.gs[2] = {s1.x, s1.y}; k.gs[3] = {s1.z, s1.w};
-  k.mu[0] = {m0.x, m0.y}; k.mu[1] = {m0.z, m0.w}; k.mu[2] = {m1.x, m1.y}; k.mu[3] = {m1.z, m1.w};
-  k.sg[0] = {a0.x, a0.y}; k.sg[1] = {a0.z, a0.w}; k.sg[2] = {a1.x, a1.y}; k.sg[3] = {a1.z, a1.w};
+// gb: byte offset of unit 0 of the group in row 0 (unit_off(tb, 0, grp, 0)).
+__device__ __forceinline__ void load_half(Half& k, const uint8_t* smem, uint32_t gb, int jrow,
+                                          int hh) {
+  const uint8_t* p = smem + gb + hh * 16;
+  const float4 g = *reinterpret_cast<const float4*>(p);
+  const float4 s = *reinterpret_cast<const float4*>(p + kRowStride);
+  const float4 m = *reinterpret_cast<const float4*>(p + (2 + 2 * jrow) * kRowStride);
+  const float4 a = *reinterpret_cast<const float4*>(p + (3 + 2 * jrow) * kRowStride);
+  const f2 e = make_float2(kEps, kEps);
+  k.gm[0] = make_float2(g.x, g.y);
+  k.gm[1] = make_float2(g.z, g.w);
+  k.gs[0] = add2(make_float2(s.x, s.y), e);
+  k.gs[1] = add2(make_float2(s.z, s.w), e);
+  k.mu[0] = make_float2(m.x, m.y);
+  k.mu[1] = make_float2(m.z, m.w);
+  k.sg[0] = add2(make_float2(a.x, a.y), e);
+  k.sg[1] = add2(make_float2(a.z, a.w), e);
 }
 
-// Table byte address of byte `pos` (0..3) of word w, row-major with lane_off.
+// Table offset of byte `pos` (0..3) of word w: [lane_off, w.b_pos, 0, 0].
 template <int POS>
-__device__ __forceinline__ uint32_t lut_addr(uint32_t w, uint32_t lane_off) {
-  // result bytes: [lane_off.b0, w.b_POS, 0, 0] (lane_off < 256)
-  return prmt(w, lane_off, 0x6504u | ((uint32_t)POS << 4));
+__device__ __forceinline__ uint32_t lut_off(uint32_t w, uint32_t lane_off) {
+  return prmt(w, lane_off, 0x7604u | ((uint32_t)POS << 4));
 }
 
 // Values of the two channels of byte POS of an anchor word a (and, in full
 // mode, of residual word r): (low-nibble channel, high-nibble channel).
 template <bool FULL, int POS>
-__device__ __forceinline__ f2 lookup_pair(const uint8_t* lut, uint32_t a, uint32_t r,
-                                          uint32_t lane_off) {
+__device__ __forceinline__ f2 lookup_pair(uint32_t a, uint32_t r, uint32_t lane_off) {
   if constexpr (FULL) {
     const uint32_t E = ((a << 4) & 0xf0f0f0f0u) | (r & 0x0f0f0f0fu);  // low-nibble codes
     const uint32_t O = (a & 0xf0f0f0f0u) | ((r >> 4) & 0x0f0f0f0fu);  // high-nibble codes
-    f2 v;
-    v.x = *reinterpret_cast<const float*>(lut + lut_addr<POS>(E, lane_off));
-    v.y = *reinterpret_cast<const float*>(lut + lut_addr<POS>(O, lane_off));
-    return v;
+    return make_float2(lut_f1(lut_off<POS>(E, lane_off)), lut_f1(lut_off<POS>(O, lane_off)));
   } else {
-    const float2 p = *reinterpret_cast<const float2*>(lut + lut_addr<POS>(a, lane_off));
-    return f2{p.x, p.y};
+    return lut_f2(lut_off<POS>(a, lane_off));
   }
 }
 
-// One packed byte position -> bf16x2 of the exact decoder output
-// (low-nibble channel in the low half).
+// Byte POS (0..3) of the packed words -> bf16x2 of the exact decoder output
+// (low-nibble channel in the low half); k holds the constants of positions
+// POS & ~1 and POS | 1.
 template <bool FULL, int POS>
-__device__ __forceinline__ uint32_t dequant_pair(const uint8_t* lut, uint32_t a, uint32_t r,
-                                                 uint32_t lane_off, const Consts& k) {
-  const f2 v = lookup_pair<FULL, POS>(lut, a, r, lane_off);
-  const f2 x = fma2(fma2(v, k.sg[POS], k.mu[POS]), k.gs[POS], k.gm[POS]);
+__device__ __forceinline__ uint32_t dequant_pair(uint32_t a, uint32_t r, uint32_t lane_off,
+                                                 const Half& k) {
+  constexpr int i = POS & 1;
+  const f2 v = lookup_pair<FULL, POS>(a, r, lane_off);
+  const f2 x = fma2(fma2(v, k.sg[i], k.mu[i]), k.gs[i], k.gm[i]);
   return f2_to_bf2(x.x, x.y);
 }
 
 template <bool FULL, int NT, bool PAIR, bool ONE>
-__global__ void __launch_bounds__(kAttnWarps * 32, PAIR ? 2 : 3)
+__global__ void __launch_bounds__(Cfg<FULL, PAIR, ONE>::kWarps * 32, 2)
 attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ ExpandTable tab) {
+  using CF = Cfg<FULL, PAIR, ONE>;
+  constexpr int NW = CF::kWarps;
   constexpr int KCH = PAIR ? 64 : 128;  // channels of K and of V per warp
   constexpr int NKT = KCH / 16;         // score k-tiles = output m-tiles per warp
   constexpr int KB = KCH / 8;           // K bytes per token row per lane (c)
   constexpr int VB = KCH / 16;          // V bytes per token row per lane (g)
-  constexpr int NU = PAIR ? kAttnWarps / 2 : kAttnWarps;  // work units per CTA
+  constexpr int NU = CF::kNU;
   constexpr int RP = 8 * NT;            // query rows per pass
-  using SC = Scratch<ONE>;
+  constexpr int GW = KCH / 8;           // channel groups per warp
 
   extern __shared__ __align__(16) uint8_t smem[];
-  uint8_t* lut = smem;
-  float* xchg_all = reinterpret_cast<float*>(smem + kLutBytes);  // pair: partial scores
+  uint8_t* extra = smem + kLutBytes;
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   const int unit = PAIR ? (w >> 1) : w;
   const int half = PAIR ? (w & 1) : 0;
   const int hb = half * 32;             // first byte of this warp's channel half
+  // The CTA's equal share of the flattened (unit, chunk) space, a unit being
+  // one (sequence, KV head, row group); a share is at most NCH chunks long,
+  // so it touches the units u0 and (perhaps) u0 + 1: segments 0 and 1.
+  const int cta = blockIdx.x;
+  const int64_t cta_b = a.n_chunks * cta / a.n_cta, cta_e = a.n_chunks * (cta + 1) / a.n_cta;
+  const int64_t u0 = cta_b / a.NCH;
+  const int part_floats = 2 * RP + RP * kD;
+  float* part = a.part + (int64_t)(2 * cta) * part_floats;               // segments 0, 1
+  float* flush = a.part + ((int64_t)2 * a.n_cta + cta) * part_floats;    // see below
+  // (sequence, KV head, row group) of the two units, packed as
+  // (sequence * Hkv + head) * nrg + row group = the unit index itself
+  const int rg0 = (int)(u0 % a.nrg), rg1 = (int)((u0 + 1) % a.nrg);
+  const int h0 = (int)((u0 / a.nrg) % a.Hkv), h1 = (int)(((u0 + 1) / a.nrg) % a.Hkv);
+  const int b0 = (int)(u0 / a.nrg / a.Hkv), b1 = (int)((u0 + 1) / a.nrg / a.Hkv);
 
-  for (int i = tid; i < 256 * 32; i += kAttnWarps * 32) {
+  if (smem_u32(smem) != kSmemBase) {  // table loads would read the wrong bytes
+    for (int i = tid; i < 2 * part_floats; i += NW * 32) part[i] = __int_as_float(0x7fc00000);
+    return;
+  }
+
+  for (int i = tid; i < 256 * 32; i += NW * 32) {
     const int row = i >> 5, l = i & 31;
     if constexpr (FULL) {
-      reinterpret_cast<float*>(lut + row * 256)[l] =
-          row < 128 ? tab.x[row] : -tab.x[255 - row];
+      reinterpret_cast<float*>(smem + row * 256)[l] = row < 128 ? tab.x[row] : -tab.x[255 - row];
     } else if (l < 16) {
       const int a0 = row & 15, a1 = row >> 4;
-      reinterpret_cast<float2*>(lut + row * 256)[l] =
+      reinterpret_cast<float2*>(smem + row * 256)[l] =
           make_float2(a0 < 8 ? tab.x[16 * a0 + 7] : -tab.x[16 * (15 - a0) + 7],
                       a1 < 8 ? tab.x[16 * a1 + 7] : -tab.x[16 * (15 - a1) + 7]);
     }
   }
+  // ---- Q^T fragments (B operand), channel order matching the K bytes
+  auto q_frag = [&](int sg, int kt, int nt, int gg, int cc) -> uint2 {
+    const int r = (sg ? rg1 : rg0) * RP + nt * 8 + gg;
+    if (r >= a.R || u0 + sg >= a.n_chunks / a.NCH) return make_uint2(0u, 0u);
+    const int tq = r / a.G, gq = r % a.G;
+    const uint16_t* qrow =
+        a.q + ((int64_t)((sg ? b1 : b0) * a.T + tq) * a.Hq + (sg ? h1 : h0) * a.G + gq) * kD;
+    uint32_t v[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int beta = hb + KB * cc + 2 * kt + hh;
+      const int lo = 8 * (beta >> 2) + (beta & 3);
+      v[hh] = (uint32_t)qrow[lo] | ((uint32_t)qrow[lo + 4] << 16);
+    }
+    return make_uint2(v[0], v[1]);
+  };
+  uint32_t qf[PAIR ? NKT : 1][NT][2];
+  auto load_qf = [&](int sg) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int kt = 0; kt < NKT; ++kt) {
+        const uint2 v = q_frag(sg, kt, nt, g, c);
+        qf[kt][nt][0] = v.x;
+        qf[kt][nt][1] = v.y;
+      }
+  };
+  if constexpr (!PAIR) {  // staged once per CTA for both units: [sg][kt][nt][lane] uint2
+    for (int i = tid; i < 2 * NKT * NT * 32; i += NW * 32) {
+      const int ln = i & 31, sg = i / (NKT * NT * 32);
+      const int nt = (i >> 5) % NT, kt = ((i >> 5) / NT) % NKT;
+      reinterpret_cast<uint2*>(extra)[i] = q_frag(sg, kt, nt, ln >> 2, ln & 3);
+    }
+  }
+  if (tid < 2) {
+    reinterpret_cast<int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo)[tid] =
+        (int64_t)(tid ? b1 : b0) * a.NB * a.Hkv + (tid ? h1 : h0);
+  }
   __syncthreads();
   const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 8u;
+  const uint32_t sbase = smem_u32(smem);
 
-  const int split = blockIdx.x, h = blockIdx.y;
-  const int b = blockIdx.z / a.nrg, rg = blockIdx.z % a.nrg;
-  const int row0 = rg * RP;
-
-  // ---- Q^T fragments (B operand), channel order matching the K bytes
-  uint32_t qf[NKT][NT][2];
+  // ---- this work unit's contiguous run [ub, ue) of the CTA's share
+  const int64_t ub = cta_b + (cta_e - cta_b) * unit / NU;
+  const int64_t ue = cta_b + (cta_e - cta_b) * (unit + 1) / NU;
+  const int meta_rows = 2 + 2 * a.NC;
+  const int tbK = w * CF::kTails, tbV = tbK + CF::kRows * 4;
+  // Packed block (sequence, page, KV head) of chunk qc of segment sg.
+  const int64_t* seg_blk =
+      reinterpret_cast<const int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo);
+  auto chunk_blk = [&](int sg, int qc, int& tp) -> int64_t {
+    const int t0 = qc * 32;
+    const int p = t0 >> a.lgP;
+    tp = t0 & (a.P - 1);
+    return seg_blk[sg] + p * a.Hkv;
+  };
+  // Asynchronous copies of the constant rows of chunk qc into the warp's
+  // rows of one tensor (gamma rows only with_gamma); the lane copies 4-byte
+  // words so that the pairs (k, k+4) land side by side.
+  auto copy_consts = [&](const float* meta, int tb, int sg, int qc, bool with_gamma) {
+    int tp;
+    const int64_t blk = chunk_blk(sg, qc, tp);
+    const int cc0 = tp >> a.lgC, cc1 = (tp + 16) >> a.lgC;
+    const float* mb = meta + blk * (int64_t)meta_rows * kD;
+    constexpr int PER = GW * 8 / 32;  // words per lane per row (4 or 2)
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int r = row0 + nt * 8 + g;
-    const bool valid = r < a.R;
-    const int tq = valid ? r / a.G : 0, gq = valid ? r % a.G : 0;
-    const uint16_t* qrow = a.q + ((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD;
+    for (int rr = 0; rr < CF::kRows; ++rr) {
+      if (rr < 2 && !with_gamma) continue;
+      const int src = rr == 0 ? 0 : rr == 1 ? 1 : rr == 2 ? 2 + cc0 : rr == 3 ? 2 + a.NC + cc0
+                    : rr == 4 ? 2 + cc1 : 2 + a.NC + cc1;
 #pragma unroll
-    for (int kt = 0; kt < NKT; ++kt)
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int beta = hb + KB * c + 2 * kt + hh;
-        const int lo = 8 * (beta >> 2) + (beta & 3);
-        qf[kt][nt][hh] = valid ? ((uint32_t)qrow[lo] | ((uint32_t)qrow[lo + 4] << 16)) : 0u;
+      for (int e = 0; e < PER; ++e) {
+        const int idx = lane * PER + e;        // word of the warp's part of the row
+        const int grp = hb / 4 + (idx >> 3), hu = (idx >> 2) & 1, pos = idx & 3;
+        const int ch = 8 * grp + 2 * hu + (pos >> 1) + 4 * (pos & 1);
+        cp_async4(sbase + unit_off(tb, rr, grp, hu) + 4 * pos, mb + src * kD + ch);
       }
-  }
+    }
+  };
 
-  const int scr = w * SC::kFloats;     // this warp's scratch (K rows, then V rows)
-  const int scrV = scr + SC::kRows * kRowFloats;
-  const int64_t cb = a.NCH * split / a.S, ce = a.NCH * (split + 1) / a.S;
   float m_run[NT][2], l_run[NT][2];
   float o[NKT][NT][4];
 #pragma unroll
@@ -262,25 +389,44 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
 #pragma unroll
     for (int i = 0; i < NKT; ++i) o[i][nt][0] = o[i][nt][1] = o[i][nt][2] = o[i][nt][3] = 0.f;
   }
-  const int meta_rows = 2 + 2 * a.NC;
-  int it = 0;
 
-  for (int64_t qc = cb + unit; qc < ce; qc += NU, ++it) {
-    const int64_t t0 = qc * 32;
-    const int64_t p = t0 / a.P;
-    const int tp = (int)(t0 - p * a.P);
-    const int64_t blk = ((int64_t)b * a.NB + p) * a.Hkv + h;
-    const int64_t code_off = (blk * a.P + tp) * (kD / 2);
-
-    // ---- packed codes of this chunk (K: 4 rows per lane, V: 8 rows)
-    Bytes<KB> kA[4], kR[4];
-    Bytes<VB> vA[8], vR[8];
+  Bytes<KB> kA[4], kR[4];
+  auto load_k = [&](int sg, int qc) {
+    int tp;
+    const int64_t blk = chunk_blk(sg, qc, tp);
+    const int64_t off = (blk * a.P + tp) * (kD / 2) + hb + KB * c;
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const int row = 16 * (jj >> 1) + g + 8 * (jj & 1);
-      kA[jj].load(a.ka + code_off + row * 64 + hb + KB * c);
-      if constexpr (FULL) kR[jj].load(a.kr + code_off + row * 64 + hb + KB * c);
+      kA[jj].load(a.ka + off + row * 64);
+      if constexpr (FULL) kR[jj].load(a.kr + off + row * 64);
     }
+  };
+  // segment and chunk (within its unit) of the run's current chunk
+  const int sg_start = (int)(ub / a.NCH - u0);
+  int sg = sg_start;
+  int qc = (int)(ub - (u0 + sg) * a.NCH);
+  if (ub < ue) {
+    copy_consts(a.km, tbK, sg, qc, true);
+    cp_commit();
+    copy_consts(a.vm, tbV, sg, qc, true);
+    cp_commit();
+    load_k(sg, qc);
+    if constexpr (PAIR) load_qf(sg);
+  }
+
+  for (int left = (int)(ue - ub); left > 0; --left) {
+    int tp;
+    const int64_t blk = chunk_blk(sg, qc, tp);
+    const int64_t code_off = (blk * a.P + tp) * (kD / 2);
+    const bool has_next = left > 1;
+    const bool cross = qc + 1 == a.NCH;  // the next chunk starts the next unit
+    const int sg_n = cross ? sg + 1 : sg;
+    const int qc_n = cross ? 0 : qc + 1;
+    const bool next_gamma = cross || ((qc + 1) * 32 >> a.lgP) != (qc * 32 >> a.lgP);
+
+    // ---- V codes of this chunk (used after the scores)
+    Bytes<VB> vA[8], vR[8];
 #pragma unroll
     for (int ii = 0; ii < 8; ++ii) {
       const int kk = ii & 3;
@@ -288,94 +434,86 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       vA[ii].load(a.va + code_off + row * 64 + hb + VB * g);
       if constexpr (FULL) vR[ii].load(a.vr + code_off + row * 64 + hb + VB * g);
     }
-    // ---- warm L2 with the next chunk of this unit (2 KB per stream)
-    if (qc + NU < ce) {
-      const int64_t t1 = (qc + NU) * 32;
-      const int64_t p1 = t1 / a.P;
-      const int64_t blk1 = ((int64_t)b * a.NB + p1) * a.Hkv + h;
-      const int64_t off1 = (blk1 * a.P + (t1 - p1 * a.P)) * (kD / 2) + lane * 64;
-      prefetch_l2(a.ka + off1);
-      prefetch_l2(a.va + off1);
+    // ---- warm L2 with the codes and constant rows two chunks ahead
+    if (left > 2 && qc + 2 < a.NCH) {
+      int tp2;
+      const int64_t blk2 = chunk_blk(sg, qc + 2, tp2);
+      const int64_t off2 = (blk2 * a.P + tp2) * (kD / 2) + lane * 64;
+      prefetch_l2(a.ka + off2);
+      prefetch_l2(a.va + off2);
       if constexpr (FULL) {
-        prefetch_l2(a.kr + off1);
-        prefetch_l2(a.vr + off1);
+        prefetch_l2(a.kr + off2);
+        prefetch_l2(a.vr + off2);
       }
+      const int cc = tp2 >> a.lgC, rsel = lane >> 3;  // mu, sigma rows of K and V
+      const float* mb = ((rsel & 2) ? a.vm : a.km) + blk2 * (int64_t)meta_rows * kD;
+      prefetch_l2(mb + (2 + ((rsel & 1) ? a.NC : 0) + cc) * kD + (lane & 7) * 16);
     }
-    // ---- constant rows -> scratch (pairs (k, k+4) interleaved, +eps folded)
-    {
-      const int cc0 = tp / a.C, cc1 = (tp + 16) / a.C;
-      const int grp = lane >> 1, hf = lane & 1;
-#pragma unroll
-      for (int tsr = 0; tsr < 2; ++tsr) {
-        const float* mb = (tsr == 0 ? a.km : a.vm) + blk * (int64_t)meta_rows * kD + 8 * grp + 2 * hf;
-        const int rows = tsr == 0 ? scr : scrV;
-#pragma unroll
-        for (int rr = 0; rr < SC::kRows; ++rr) {
-          const int src = rr == 0 ? 0 : rr == 1 ? 1 : rr == 2 ? 2 + cc0 : rr == 3 ? 2 + a.NC + cc0
-                        : rr == 4 ? 2 + cc1 : 2 + a.NC + cc1;
-          const float2 lo = __ldg(reinterpret_cast<const float2*>(mb + src * kD));
-          const float2 hi = __ldg(reinterpret_cast<const float2*>(mb + src * kD + 4));
-          float4 v = make_float4(lo.x, hi.x, lo.y, hi.y);
-          if (rr == 1 || rr == 3 || rr == 5) {
-            v.x = __fadd_rn(v.x, kEps); v.y = __fadd_rn(v.y, kEps);
-            v.z = __fadd_rn(v.z, kEps); v.w = __fadd_rn(v.w, kEps);
-          }
-          *reinterpret_cast<float4*>(smem + scr_byte(rows + rr * kRowFloats + grp_off(grp) + 4 * hf)) = v;
-        }
-      }
-    }
-    __syncwarp();
 
     // ---- scores: S^T for m-tiles j = 0, 1 (tokens 16j .. 16j+15)
+    cp_wait<1>();  // constants of K for this chunk have landed
+    __syncwarp();
     float s[2][NT][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) s[j][nt][0] = s[j][nt][1] = s[j][nt][2] = s[j][nt][3] = 0.f;
-    // one 16-token m-tile j of the scores with this group's constants
-    auto qk = [&](const Consts& kc, int j, int gi) {
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int kt = 2 * gi + kk;
-        uint32_t af[4];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {       // row g (i=0) / g+8 (i=1)
-          const uint32_t wa = kA[2 * j + i].w[gi];
-          const uint32_t wr = FULL ? kR[2 * j + i].w[gi] : 0u;
-          if (kk == 0) {                    // k 2c..2c+1 / 2c+8..2c+9 = bytes 0 / 1
-            af[i] = dequant_pair<FULL, 0>(lut, wa, wr, lane_off, kc);
-            af[i + 2] = dequant_pair<FULL, 1>(lut, wa, wr, lane_off, kc);
-          } else {                          // bytes 2 / 3
-            af[i] = dequant_pair<FULL, 2>(lut, wa, wr, lane_off, kc);
-            af[i + 2] = dequant_pair<FULL, 3>(lut, wa, wr, lane_off, kc);
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16(s[j][nt], af, qf[kt][nt][0], qf[kt][nt][1]);
-      }
-    };
 #pragma unroll
     for (int gi = 0; gi < KB / 4; ++gi) {      // channel groups of this lane (K)
       const int grp = (hb + KB * c) / 4 + gi;
-      if constexpr (ONE) {
-        Consts kc;
-        load_consts(kc, smem, scr, grp, 0);
-        qk(kc, 0, gi);
-        qk(kc, 1, gi);
-      } else {
+      const uint32_t gb = unit_off(tbK, 0, grp, 0);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {         // k-tile 2gi+kk: byte positions 2kk, 2kk+1
+        const int kt = 2 * gi + kk;
+        uint32_t qb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if constexpr (PAIR) {
+            qb[nt][0] = qf[kt][nt][0];
+            qb[nt][1] = qf[kt][nt][1];
+          } else {
+            const uint2 v =
+                reinterpret_cast<const uint2*>(extra)[((sg * NKT + kt) * NT + nt) * 32 + lane];
+            qb[nt][0] = v.x;
+            qb[nt][1] = v.y;
+          }
+        }
+        Half kc;
+        if constexpr (ONE) load_half(kc, smem, gb, 0, kk);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          Consts kc;
-          load_consts(kc, smem, scr, grp, j);
-          qk(kc, j, gi);
+          if constexpr (!ONE) load_half(kc, smem, gb, j, kk);
+          uint32_t af[4];
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {        // row g (i=0) / g+8 (i=1)
+            const uint32_t wa = kA[2 * j + i].w[gi];
+            const uint32_t wr = FULL ? kR[2 * j + i].w[gi] : 0u;
+            if (kk == 0) {
+              af[i] = dequant_pair<FULL, 0>(wa, wr, lane_off, kc);
+              af[i + 2] = dequant_pair<FULL, 1>(wa, wr, lane_off, kc);
+            } else {
+              af[i] = dequant_pair<FULL, 2>(wa, wr, lane_off, kc);
+              af[i + 2] = dequant_pair<FULL, 3>(wa, wr, lane_off, kc);
+            }
+          }
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(s[j][nt], af, qb[nt][0], qb[nt][1]);
         }
       }
     }
+    __syncwarp();  // every lane is done with this chunk's K constants and codes
+    if (has_next) {
+      load_k(sg_n, qc_n);
+      copy_consts(a.km, tbK, sg_n, qc_n, next_gamma);
+    }
+    cp_commit();
 
     if constexpr (PAIR) {
       // partial scores over this warp's channel half + the partner's half
-      float* mine = xchg_all + ((unit * 2 + half) * 2 + (it & 1)) * (32 * 8 * NT);
-      const float* other = xchg_all + ((unit * 2 + (half ^ 1)) * 2 + (it & 1)) * (32 * 8 * NT);
+      float* xchg = reinterpret_cast<float*>(extra);
+      const int it = left & 1;
+      float* mine = xchg + ((unit * 2 + half) * 2 + it) * (32 * 8 * NT);
+      const float* other = xchg + ((unit * 2 + (half ^ 1)) * 2 + it) * (32 * 8 * NT);
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
@@ -434,53 +572,101 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     }
 
     // ---- output: O^T += V^T P^T over this warp's V m-tiles (byte VB*g + mt)
-    auto pv = [&](const Consts& kc, int jt, int gi) {
+    cp_wait<1>();  // constants of V for this chunk have landed
+    __syncwarp();
 #pragma unroll
-      for (int kk = 0; kk < (VB < 4 ? VB : 4); ++kk) {
-        const int mt = 4 * gi + kk;
-        uint32_t W[4];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {   // tokens 2c, 2c+1, 2c+8, 2c+9
-          const uint32_t wa = vA[4 * jt + q4].w[gi];
-          const uint32_t wr = FULL ? vR[4 * jt + q4].w[gi] : 0u;
-          W[q4] = kk == 0 ? dequant_pair<FULL, 0>(lut, wa, wr, lane_off, kc)
-                : kk == 1 ? dequant_pair<FULL, 1>(lut, wa, wr, lane_off, kc)
-                : kk == 2 ? dequant_pair<FULL, 2>(lut, wa, wr, lane_off, kc)
-                          : dequant_pair<FULL, 3>(lut, wa, wr, lane_off, kc);
-        }
-        uint32_t af[4];
-        af[0] = prmt(W[0], W[1], 0x5410u);  // row g   (low channel), tokens 2c, 2c+1
-        af[1] = prmt(W[0], W[1], 0x7632u);  // row g+8 (high channel)
-        af[2] = prmt(W[2], W[3], 0x5410u);  // row g,   tokens 2c+8, 2c+9
-        af[3] = prmt(W[2], W[3], 0x7632u);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_bf16(o[mt][nt], af, pb_hi[jt][nt][0], pb_hi[jt][nt][1]);
-          mma_bf16(o[mt][nt], af, pb_lo[jt][nt][0], pb_lo[jt][nt][1]);
-        }
-      }
-    };
-#pragma unroll
-    for (int gi = 0; gi < (VB + 3) / 4; ++gi) {
+    for (int gi = 0; gi < VB / 4; ++gi) {
       const int grp = (hb + VB * g) / 4 + gi;
-      if constexpr (ONE) {
-        Consts kc;
-        load_consts(kc, smem, scrV, grp, 0);
-        pv(kc, 0, gi);
-        pv(kc, 1, gi);
-      } else {
+      const uint32_t gb = unit_off(tbV, 0, grp, 0);
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          Consts kc;
-          load_consts(kc, smem, scrV, grp, j);
-          pv(kc, j, gi);
+      for (int hh = 0; hh < 2; ++hh) {         // byte positions 2hh, 2hh+1
+        Half vc;
+        if constexpr (ONE) load_half(vc, smem, gb, 0, hh);
+#pragma unroll
+        for (int jt = 0; jt < 2; ++jt) {
+          if constexpr (!ONE) load_half(vc, smem, gb, jt, hh);
+#pragma unroll
+          for (int kq = 0; kq < 2; ++kq) {
+            const int kk = 2 * hh + kq, mt = 4 * gi + kk;
+            uint32_t W[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {   // tokens 2c, 2c+1, 2c+8, 2c+9
+              const uint32_t wa = vA[4 * jt + q4].w[gi];
+              const uint32_t wr = FULL ? vR[4 * jt + q4].w[gi] : 0u;
+              W[q4] = kk == 0 ? dequant_pair<FULL, 0>(wa, wr, lane_off, vc)
+                    : kk == 1 ? dequant_pair<FULL, 1>(wa, wr, lane_off, vc)
+                    : kk == 2 ? dequant_pair<FULL, 2>(wa, wr, lane_off, vc)
+                              : dequant_pair<FULL, 3>(wa, wr, lane_off, vc);
+            }
+            uint32_t af[4];
+            af[0] = prmt(W[0], W[1], 0x5410u);  // row g   (low channel), tokens 2c, 2c+1
+            af[1] = prmt(W[0], W[1], 0x7632u);  // row g+8 (high channel)
+            af[2] = prmt(W[2], W[3], 0x5410u);  // row g,   tokens 2c+8, 2c+9
+            af[3] = prmt(W[2], W[3], 0x7632u);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_bf16(o[mt][nt], af, pb_hi[jt][nt][0], pb_hi[jt][nt][1]);
+              mma_bf16(o[mt][nt], af, pb_lo[jt][nt][0], pb_lo[jt][nt][1]);
+            }
+          }
         }
       }
     }
-    __syncwarp();
-  }
+    __syncwarp();  // every lane is done with this chunk's V constants
+    if (has_next) copy_consts(a.vm, tbV, sg_n, qc_n, next_gamma);
+    cp_commit();
 
-  // ---- merge the units of the CTA, write this split's partial
+    if (cross && has_next) {
+      // The run leaves unit u0 (only one work unit of a CTA can): park its
+      // state for unit u0 in the CTA's flush record, start afresh on u0 + 1.
+      float lr[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float v = l_run[nt][e];
+#pragma unroll
+          for (int x = 4; x <= 16; x <<= 1) v += __shfl_xor_sync(kFull, v, x);
+          lr[nt][e] = v;
+        }
+      if (g == 0 && half == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            flush[nt * 8 + 2 * c + e] = m_run[nt][e];
+            flush[RP + nt * 8 + 2 * c + e] = lr[nt][e];
+          }
+      }
+#pragma unroll
+      for (int mt = 0; mt < NKT; ++mt) {
+        const int beta = hb + VB * g + mt;
+        const int ch_lo = 8 * (beta >> 2) + (beta & 3), ch_hi = ch_lo + 4;
+        float* fo = flush + 2 * RP;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          fo[(nt * 8 + 2 * c) * kD + ch_lo] = o[mt][nt][0];
+          fo[(nt * 8 + 2 * c + 1) * kD + ch_lo] = o[mt][nt][1];
+          fo[(nt * 8 + 2 * c) * kD + ch_hi] = o[mt][nt][2];
+          fo[(nt * 8 + 2 * c + 1) * kD + ch_hi] = o[mt][nt][3];
+          o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -INFINITY;
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+      }
+      if constexpr (PAIR) load_qf(sg_n);
+    }
+    if (has_next) {
+      sg = sg_n;
+      qc = qc_n;
+    }
+  }
+  cp_wait<0>();
+
+  // ---- merge the work units of the CTA per segment, write its partials
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -488,10 +674,12 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       l_run[nt][0] += __shfl_xor_sync(kFull, l_run[nt][0], x);
       l_run[nt][1] += __shfl_xor_sync(kFull, l_run[nt][1], x);
     }
-  __syncthreads();  // every warp is done with the tables and scratch; reuse them
-  float* sm_m = reinterpret_cast<float*>(smem);       // [NU][RP]
+  __syncthreads();  // every warp is done with Q, the exchange and the scratch
+  float* sm_m = reinterpret_cast<float*>(extra);      // [NU][RP]
   float* sm_l = sm_m + NU * RP;                        // [NU][RP]
   float* sm_o = sm_l + NU * RP;                        // [NU][RP][128]
+  int* sm_tag = reinterpret_cast<int*>(sm_o + NU * RP * kD);  // [NU] segment of the state
+  int* sm_fl = sm_tag + NU;                                    // [NU] parked a state
   if (g == 0 && half == 0) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -499,6 +687,10 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       sm_m[unit * RP + nt * 8 + 2 * c + 1] = m_run[nt][1];
       sm_l[unit * RP + nt * 8 + 2 * c] = l_run[nt][0];
       sm_l[unit * RP + nt * 8 + 2 * c + 1] = l_run[nt][1];
+    }
+    if (c == 0) {
+      sm_tag[unit] = sg;
+      sm_fl[unit] = (ub < ue && sg != sg_start) ? 1 : 0;  // crossed, so parked a state
     }
   }
 #pragma unroll
@@ -514,46 +706,65 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       ow[(nt * 8 + 2 * c + 1) * kD + ch_hi] = o[mt][nt][3];
     }
   }
-  __syncthreads();
-  const int part_floats = 2 * RP + RP * kD;
-  float* part = a.part + ((((int64_t)b * a.Hkv + h) * a.nrg + rg) * a.S + split) * part_floats;
-  for (int i = tid; i < RP * kD; i += kAttnWarps * 32) {
-    const int r = i / kD, d = i % kD;
-    float M = -INFINITY;
+  __syncthreads();  // (also orders the flush record's global writes before its reads)
+  bool parked = false;
 #pragma unroll
-    for (int u = 0; u < NU; ++u) M = fmaxf(M, sm_m[u * RP + r]);
+  for (int u = 0; u < NU; ++u) parked |= sm_fl[u] != 0;
+  const int nseg = (int)((cta_e - 1) / a.NCH - u0) + 1;
+  for (int i = tid; i < nseg * RP * kD; i += NW * 32) {
+    const int sgm = i / (RP * kD), r = (i / kD) % RP, d = i % kD;
+    const bool use_flush = sgm == 0 && parked;
+    float M = use_flush ? flush[r] : -INFINITY;
+#pragma unroll
+    for (int u = 0; u < NU; ++u)
+      if (sm_tag[u] == sgm) M = fmaxf(M, sm_m[u * RP + r]);
     float acc = 0.f, den = 0.f;
+    if (use_flush && flush[r] != -INFINITY) {
+      const float f = exp2f(flush[r] - M);
+      acc = f * flush[2 * RP + r * kD + d];
+      den = f * flush[RP + r];
+    }
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
       const float mu_ = sm_m[u * RP + r];
-      const float f = mu_ == -INFINITY ? 0.f : exp2f(mu_ - M);
+      if (sm_tag[u] != sgm || mu_ == -INFINITY) continue;
+      const float f = exp2f(mu_ - M);
       acc += f * sm_o[(u * RP + r) * kD + d];
       den += f * sm_l[u * RP + r];
     }
-    part[2 * RP + r * kD + d] = acc;
+    float* ps = part + sgm * part_floats;
+    ps[2 * RP + r * kD + d] = acc;
     if (d == 0) {
-      part[r] = M;
-      part[RP + r] = den;
+      ps[r] = M;
+      ps[RP + r] = den;
     }
   }
 }
 
-// Merge the splits of one (sequence, KV head, row group): out = sum e^(m_s-M)
-// o_s / sum e^(m_s-M) l_s, written to out[b][t][hq][:].
+// Merge the partials of one unit (sequence, KV head, row group): the CTAs
+// whose shares touch it, each through the partial of the matching segment.
+// out = sum e^(m_s-M) o_s / sum e^(m_s-M) l_s, written to out[b][t][hq][:].
 __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnParams a, int RP) {
-  const int z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
-  const int rg = z % a.nrg, bh = z / a.nrg, h = bh % a.Hkv, b = bh / a.Hkv;
+  const int64_t z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
+  const int rg = (int)(z % a.nrg), bh = (int)(z / a.nrg), h = bh % a.Hkv, b = bh / a.Hkv;
   const int d = threadIdx.x;
   const int part_floats = 2 * RP + RP * kD;
-  const float* part = a.part + (int64_t)z * a.S * part_floats;
+  // CTA holding flattened chunk x: floor(((x + 1) n_cta - 1) / n_chunks)
+  const int64_t first = z * a.NCH, last = first + a.NCH - 1;
+  const int k0 = (int)(((first + 1) * a.n_cta - 1) / a.n_chunks);
+  const int k1 = (int)(((last + 1) * a.n_cta - 1) / a.n_chunks);
   for (int r = 0; r < RP; ++r) {
     const int row = rg * RP + r;
     if (row >= a.R) break;
     float M = -INFINITY;
-    for (int s = 0; s < a.S; ++s) M = fmaxf(M, part[s * part_floats + r]);
+    for (int k = k0; k <= k1; ++k) {
+      const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
+      M = fmaxf(M, a.part[(2 * k + seg) * part_floats + r]);
+    }
     float num = 0.f, den = 0.f;
-    for (int s = 0; s < a.S; ++s) {
-      const float* ps = part + s * part_floats;
+    for (int k = k0; k <= k1; ++k) {
+      const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
+      const float* ps = a.part + (2 * k + seg) * part_floats;
       const float f = ps[r] == -INFINITY ? 0.f : exp2f(ps[r] - M);
       num += f * ps[2 * RP + r * kD + d];
       den += f * ps[RP + r];
@@ -570,42 +781,50 @@ __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnP
 static int rows_per_pass(int R) { return R <= 8 ? 8 : 32; }
 static int row_groups(int R) { const int rp = rows_per_pass(R); return (R + rp - 1) / rp; }
 
-// Splits per (sequence, KV head, row group): as many as fit one wave of
-// CTAs on the 152 SMs of a GB300 (3 resident CTAs per SM for the single-warp
-// shape, 2 for the warp-pair shape), so that no partial second wave leaves
-// SMs idle; at least one 32-token chunk per work unit.  Device independent,
-// so the workspace size is a pure function of the shapes.
+// CTAs of the attention grid.  Every shape runs two CTAs per SM, so the
+// 152 SMs of a GB300 hold 304 at once: one wave of equal shares of the
+// flattened (unit, chunk) space, with at least 2 chunks per work unit (8 of
+// them per CTA up to 8 query rows, 2 warp pairs above), and at least one CTA
+// per unit so that a share never exceeds one unit's chunks (several waves
+// when there are more units than that).  Device independent, so the
+// workspace size is a pure function of the shapes.
 constexpr int kGB300SMs = 152;
-static int splits_for(int batch, int Hkv, int nrg, int64_t NCH, int R) {
+static int ctas_for(int batch, int Hkv, int nrg, int64_t NCH, int R) {
   const int64_t units = (int64_t)batch * Hkv * nrg;
-  const int64_t slots = (int64_t)kGB300SMs * (R <= 8 ? 3 : 2);
-  int64_t s = slots / units;
-  const int64_t nu = R <= 8 ? kAttnWarps : kAttnWarps / 2;
-  const int64_t cap = NCH / nu > 0 ? NCH / nu : 1;
-  if (s > cap) s = cap;
-  if (s < 1) s = 1;
-  return (int)s;
+  const int64_t n_chunks = units * NCH;
+  const int64_t nu = R <= 8 ? 8 : 2;
+  int64_t n = (int64_t)kGB300SMs * 2;
+  if (n > n_chunks / (2 * nu)) n = n_chunks / (2 * nu);
+  if (n < units) n = units;
+  return (int)n;
 }
 
+// Workspace: two partials per CTA (its segments) and one parked state per
+// CTA (a work unit's state for the first unit when its run crosses into the
+// second).
 size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L) {
   const int R = (H_q / H_kv) * T;
   const int RP = rows_per_pass(R), nrg = row_groups(R);
-  const int S = splits_for(batch, H_kv, nrg, L / 32, R);
-  return (size_t)batch * H_kv * nrg * S * (2 * RP + RP * kD) * sizeof(float);
+  const int n = ctas_for(batch, H_kv, nrg, L / 32, R);
+  return (size_t)3 * n * (2 * RP + RP * kD) * sizeof(float);
 }
 
 template <bool FULL, int NT, bool PAIR, bool ONE>
 static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
   auto fn = attn_kernel<FULL, NT, PAIR, ONE>;
-  constexpr size_t xchg = PAIR ? (size_t)kAttnWarps * 2 * 32 * 8 * NT * sizeof(float) : 0;
-  constexpr size_t smem = kLutBytes + xchg;
-  static_assert((size_t)(kAttnWarps / (PAIR ? 2 : 1)) * (2 + 128) * 8 * NT * sizeof(float) <= smem,
-                "merge buffers fit in the reused tables");
+  constexpr size_t smem = attn_smem_bytes<FULL, PAIR, ONE, NT>();
+  constexpr int threads = Cfg<FULL, PAIR, ONE>::kWarps * 32;
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
+    // The table loads assume dynamic shared memory starts right after the
+    // block's reserved shared memory at kSmemBase.
+    int reserved = -1;
+    e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
+    if (reserved != (int)kSmemBase) return cudaErrorNotSupported;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -613,8 +832,7 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
-  dim3 grid((unsigned)prm.S, (unsigned)prm.Hkv, (unsigned)(prm.batch * prm.nrg));
-  fn<<<grid, kAttnWarps * 32, smem, stream>>>(prm, tab);
+  fn<<<(unsigned)prm.n_cta, threads, smem, stream>>>(prm, tab);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_combine<<<(unsigned)(prm.batch * prm.Hkv * prm.nrg), kD, 0, stream>>>(prm, 8 * NT);
@@ -648,10 +866,13 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
   prm.L = x.s.L;
   prm.NB = x.s.NB();
   prm.NCH = x.s.L / 32;
-  prm.S = splits_for(x.batch, prm.Hkv, prm.nrg, prm.NCH, prm.R);
+  prm.n_chunks = (int64_t)x.batch * prm.Hkv * prm.nrg * prm.NCH;
+  prm.n_cta = ctas_for(x.batch, prm.Hkv, prm.nrg, prm.NCH, prm.R);
   prm.P = x.s.page;
   prm.C = x.s.C;
   prm.NC = x.s.NC();
+  prm.lgP = __builtin_ctz((unsigned)x.s.page);
+  prm.lgC = __builtin_ctz((unsigned)x.s.C);
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   const bool small = prm.R <= 8;
   if (x.full)

@@ -16,41 +16,15 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // --------------------------------------------------------------- f32x2
 
-struct f2 {
-  float x, y;
-};
+// Packed pair of floats; the arithmetic below maps to the sm_100 float2
+// intrinsics, whose per-lane behaviour is that of the scalar _rn intrinsics
+// (one IEEE rounding, never contracted into a fused multiply-add).
+using f2 = float2;
 
-__device__ __forceinline__ unsigned long long pk(f2 a) {
-  unsigned long long r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
-  return r;
-}
-__device__ __forceinline__ f2 upk(unsigned long long r) {
-  f2 a;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
-  return a;
-}
-// Round-to-nearest packed ops: one IEEE rounding per lane, never contracted.
-__device__ __forceinline__ f2 add2(f2 a, f2 b) {
-  unsigned long long r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
-  return upk(r);
-}
-__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
-  unsigned long long r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
-  return upk(r);
-}
-__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
-  unsigned long long r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
-  return upk(r);
-}
-__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
-  unsigned long long r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
-  return upk(r);
-}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) { return __fadd2_rn(a, make_float2(-b.x, -b.y)); }
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) { return __ffma2_rn(a, b, c); }
 
 // --------------------------------------------------------------- scalar
 

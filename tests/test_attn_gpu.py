@@ -113,3 +113,13 @@ def test_decode_attention_full_size_sampled(lynx_lib, oracle_mod, cuda_dev):
     pairs = [(0, 0), (3, 5), (7, 7)]
     r = _run(lynx_lib, oracle_mod, cuda_dev, 8, 32768, 8, 32, 8, 128, 32, pairs, seed=5)
     print(r)
+
+
+def test_shares_straddling_units_all_heads(lynx_lib, oracle_mod, cuda_dev):
+    """4 sequences x 4 KV heads x 10240 tokens: 5120 chunks of 32 tokens over
+    304 CTAs, so most CTA shares (16-17 chunks) start or end inside a head and
+    one work unit of such a CTA carries its state across; every (sequence, KV
+    head) is checked, draft (T=1 Anchor) and verification (T=8 full)."""
+    pairs = [(b, h) for b in range(4) for h in range(4)]
+    r = _run(lynx_lib, oracle_mod, cuda_dev, 4, 10240, 4, 16, 8, 128, 32, pairs, seed=11)
+    print(r)
