@@ -82,9 +82,11 @@ template <bool FULL, bool PAIR, bool ONE, int NT>
 struct ExtraLayout {
   using CF = Cfg<FULL, PAIR, ONE>;
   static constexpr int NKT = PAIR ? 4 : 8;
-  static constexpr size_t kQ = PAIR ? 0 : (size_t)2 * NKT * NT * 32 * 8;
+  static constexpr int kHalves = PAIR ? 2 : 1;
+  static constexpr size_t kQ = (size_t)2 * kHalves * NKT * NT * 32 * 8;  // [seg][half][kt][nt][lane]
   static constexpr size_t kXchg = PAIR ? (size_t)CF::kWarps * 2 * 32 * 8 * NT * 4 : 0;
   static constexpr size_t kInfo = kQ + kXchg;  // int64 block base of segments 0, 1
+  static_assert(kLutBytes + kInfo + 16 + 1024 <= 116 * 1024, "two CTAs per SM");
   static constexpr size_t kLoop = kInfo + 16;
   static constexpr size_t kMerge = (size_t)CF::kNU * 8 * NT * (2 + kD) * 4 + (size_t)CF::kNU * 8;
   static constexpr size_t kBytes = kLoop > kMerge ? kLoop : kMerge;
@@ -301,7 +303,7 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     }
   }
   // ---- Q^T fragments (B operand), channel order matching the K bytes
-  auto q_frag = [&](int sg, int kt, int nt, int gg, int cc) -> uint2 {
+  auto q_frag = [&](int sg, int hf, int kt, int nt, int gg, int cc) -> uint2 {
     const int r = (sg ? rg1 : rg0) * RP + nt * 8 + gg;
     if (r >= a.R || u0 + sg >= a.n_chunks / a.NCH) return make_uint2(0u, 0u);
     const int tq = r / a.G, gq = r % a.G;
@@ -310,28 +312,20 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     uint32_t v[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const int beta = hb + KB * cc + 2 * kt + hh;
+      const int beta = hf * 32 + KB * cc + 2 * kt + hh;
       const int lo = 8 * (beta >> 2) + (beta & 3);
       v[hh] = (uint32_t)qrow[lo] | ((uint32_t)qrow[lo + 4] << 16);
     }
     return make_uint2(v[0], v[1]);
   };
-  uint32_t qf[PAIR ? NKT : 1][NT][2];
-  auto load_qf = [&](int sg) {
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int kt = 0; kt < NKT; ++kt) {
-        const uint2 v = q_frag(sg, kt, nt, g, c);
-        qf[kt][nt][0] = v.x;
-        qf[kt][nt][1] = v.y;
-      }
-  };
-  if constexpr (!PAIR) {  // staged once per CTA for both units: [sg][kt][nt][lane] uint2
-    for (int i = tid; i < 2 * NKT * NT * 32; i += NW * 32) {
-      const int ln = i & 31, sg = i / (NKT * NT * 32);
-      const int nt = (i >> 5) % NT, kt = ((i >> 5) / NT) % NKT;
-      reinterpret_cast<uint2*>(extra)[i] = q_frag(sg, kt, nt, ln >> 2, ln & 3);
+  // Q^T fragments of both segments, staged once per CTA:
+  // [seg][half][kt][nt][lane] uint2
+  {
+    constexpr int NH = PAIR ? 2 : 1;
+    for (int i = tid; i < 2 * NH * NKT * NT * 32; i += NW * 32) {
+      const int ln = i & 31, nt = (i >> 5) % NT, kt = (i >> 5) / NT % NKT;
+      const int hf = (i >> 5) / (NT * NKT) % NH, sg = (i >> 5) / (NT * NKT * NH);
+      reinterpret_cast<uint2*>(extra)[i] = q_frag(sg, hf, kt, nt, ln >> 2, ln & 3);
     }
   }
   if (tid < 2) {
@@ -357,25 +351,28 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     return seg_blk[sg] + p * a.Hkv;
   };
   // Asynchronous copies of the constant rows of chunk qc into the warp's
-  // rows of one tensor (gamma rows only with_gamma); the lane copies 4-byte
-  // words so that the pairs (k, k+4) land side by side.
+  // rows of one tensor (gamma rows only with_gamma).  Each copy instruction
+  // fills one 128-byte tail (32 words, 32 banks): lane = slot * 8 + unit * 4
+  // + word, the slot holding group 4T + (slot ^ T) of tail T; the words are
+  // copied one by one so that the pairs (k, k+4) land side by side.
   auto copy_consts = [&](const float* meta, int tb, int sg, int qc, bool with_gamma) {
     int tp;
     const int64_t blk = chunk_blk(sg, qc, tp);
     const int cc0 = tp >> a.lgC, cc1 = (tp + 16) >> a.lgC;
     const float* mb = meta + blk * (int64_t)meta_rows * kD;
-    constexpr int PER = GW * 8 / 32;  // words per lane per row (4 or 2)
+    const int slot = lane >> 3, hu = (lane >> 2) & 1, pos = lane & 3;
+    const int ch_in = 2 * hu + (pos >> 1) + 4 * (pos & 1);  // channel within the group
 #pragma unroll
     for (int rr = 0; rr < CF::kRows; ++rr) {
       if (rr < 2 && !with_gamma) continue;
       const int src = rr == 0 ? 0 : rr == 1 ? 1 : rr == 2 ? 2 + cc0 : rr == 3 ? 2 + a.NC + cc0
                     : rr == 4 ? 2 + cc1 : 2 + a.NC + cc1;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const int idx = lane * PER + e;        // word of the warp's part of the row
-        const int grp = hb / 4 + (idx >> 3), hu = (idx >> 2) & 1, pos = idx & 3;
-        const int ch = 8 * grp + 2 * hu + (pos >> 1) + 4 * (pos & 1);
-        cp_async4(sbase + unit_off(tb, rr, grp, hu) + 4 * pos, mb + src * kD + ch);
+      for (int e = 0; e < GW / 4; ++e) {       // tails of the row this warp fills
+        const int T = hb / 16 + e;
+        const int grp = 4 * T + (slot ^ (T & 3));
+        cp_async4(sbase + (uint32_t)((tb + rr * 4 + T) * 256 + 128 + lane * 4),
+                  mb + src * kD + 8 * grp + ch_in);
       }
     }
   };
@@ -412,7 +409,6 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     copy_consts(a.vm, tbV, sg, qc, true);
     cp_commit();
     load_k(sg, qc);
-    if constexpr (PAIR) load_qf(sg);
   }
 
   for (int left = (int)(ue - ub); left > 0; --left) {
@@ -420,10 +416,11 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     const int64_t blk = chunk_blk(sg, qc, tp);
     const int64_t code_off = (blk * a.P + tp) * (kD / 2);
     const bool has_next = left > 1;
-    const bool cross = qc + 1 == a.NCH;  // the next chunk starts the next unit
-    const int sg_n = cross ? sg + 1 : sg;
-    const int qc_n = cross ? 0 : qc + 1;
-    const bool next_gamma = cross || ((qc + 1) * 32 >> a.lgP) != (qc * 32 >> a.lgP);
+    // the next chunk (recomputed where used, to keep registers free)
+    auto cross = [&] { return qc + 1 == a.NCH; };  // it starts the next unit
+    auto sg_n = [&] { return cross() ? sg + 1 : sg; };
+    auto qc_n = [&] { return cross() ? 0 : qc + 1; };
+    auto next_gamma = [&] { return cross() || ((qc + 1) * 32 >> a.lgP) != (qc * 32 >> a.lgP); };
 
     // ---- V codes of this chunk (used after the scores)
     Bytes<VB> vA[8], vR[8];
@@ -468,15 +465,10 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
         uint32_t qb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          if constexpr (PAIR) {
-            qb[nt][0] = qf[kt][nt][0];
-            qb[nt][1] = qf[kt][nt][1];
-          } else {
-            const uint2 v =
-                reinterpret_cast<const uint2*>(extra)[((sg * NKT + kt) * NT + nt) * 32 + lane];
-            qb[nt][0] = v.x;
-            qb[nt][1] = v.y;
-          }
+          const uint2 v = reinterpret_cast<const uint2*>(
+              extra)[((((sg * (PAIR ? 2 : 1) + half) * NKT + kt) * NT + nt) * 32 + lane)];
+          qb[nt][0] = v.x;
+          qb[nt][1] = v.y;
         }
         Half kc;
         if constexpr (ONE) load_half(kc, smem, gb, 0, kk);
@@ -503,14 +495,14 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     }
     __syncwarp();  // every lane is done with this chunk's K constants and codes
     if (has_next) {
-      load_k(sg_n, qc_n);
-      copy_consts(a.km, tbK, sg_n, qc_n, next_gamma);
+      load_k(sg_n(), qc_n());
+      copy_consts(a.km, tbK, sg_n(), qc_n(), next_gamma());
     }
     cp_commit();
 
     if constexpr (PAIR) {
       // partial scores over this warp's channel half + the partner's half
-      float* xchg = reinterpret_cast<float*>(extra);
+      float* xchg = reinterpret_cast<float*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kQ);
       const int it = left & 1;
       float* mine = xchg + ((unit * 2 + half) * 2 + it) * (32 * 8 * NT);
       const float* other = xchg + ((unit * 2 + (half ^ 1)) * 2 + it) * (32 * 8 * NT);
@@ -613,10 +605,10 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       }
     }
     __syncwarp();  // every lane is done with this chunk's V constants
-    if (has_next) copy_consts(a.vm, tbV, sg_n, qc_n, next_gamma);
+    if (has_next) copy_consts(a.vm, tbV, sg_n(), qc_n(), next_gamma());
     cp_commit();
 
-    if (cross && has_next) {
+    if (cross() && has_next) {
       // The run leaves unit u0 (only one work unit of a CTA can): park its
       // state for unit u0 in the CTA's flush record, start afresh on u0 + 1.
       float lr[NT][2];
@@ -657,11 +649,11 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
         m_run[nt][0] = m_run[nt][1] = -INFINITY;
         l_run[nt][0] = l_run[nt][1] = 0.f;
       }
-      if constexpr (PAIR) load_qf(sg_n);
     }
     if (has_next) {
-      sg = sg_n;
-      qc = qc_n;
+      const int sgn = sg_n(), qcn = qc_n();
+      sg = sgn;
+      qc = qcn;
     }
   }
   cp_wait<0>();

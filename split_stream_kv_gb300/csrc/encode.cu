@@ -7,13 +7,16 @@
 // by H*256 bytes in HBM) in shared memory; the next one or two tiles are in
 // flight per CTA while the CTA computes on the current one.
 //
-// Thread layout for a block (2*page threads): lane = 16*e1 + g.  g selects 8
-// channels (16 bytes of a row, 4 bytes of each packed row); a thread holds 8
-// tokens of one chunk.  With WPC = C/16 warps per chunk, chunk c = warp/WPC,
-// u = warp%WPC, and register m holds chunk token i = m*2*WPC + e1*WPC + u.
-// The chunk mean's pairwise-halving sum (v[i] += v[i+h], h = C/2 .. 1) then
-// reduces the register index first (top bits of i), then e1 (shuffle xor 16),
-// then u (shared memory), which is exactly the order the oracle uses.
+// Thread layout for a block (2*page threads): every chunk of C tokens is
+// covered by C/16 warps, each owning a slice of 2048/C channels of all C
+// tokens, so a chunk's statistics never leave the warp.  In a warp, lane =
+// tl * CG + cg with TL = C/8 token lanes and CG = 256/C channel groups of 8
+// channels (16 bytes of a BF16 row, 4 bytes of each packed row); register m
+// holds chunk token i = TL*m + tl.  The chunk mean's pairwise-halving sum
+// (v[i] += v[i+h], h = C/2 .. 1) then reduces the register index first (the
+// top bits of i), then the token lanes by shuffles with h = TL/2 .. 1: exactly
+// the order the oracle uses.  Only the page minimum and maximum cross warps
+// (two block barriers per page block).
 //
 // Arithmetic, each step one IEEE binary32 rounding (no contraction):
 //   gmin = min x (a zero minimum as -0), gmax = max x, gs = gmax - gmin,
@@ -43,10 +46,15 @@ cudaError_t read_wait_timeout(unsigned int* flag) {
 // the value relative to the rounding boundary.
 constexpr float kC0 = 8388608.0f + 32768.0f + (float)kAmbiguityK;
 
-__device__ __forceinline__ uint32_t compand_fast(float a, float alpha, float c16) {
-  const float t = fmaf(alpha, a, 1.0f);
-  const float l = lg2_approx(t);
-  return __float_as_uint(fma_rm(l, c16, kC0));
+// Two values at once: per lane the same roundings as t = rn(alpha*a + 1),
+// s = rm(lg2(t)*c16 + kC0), issued as packed pairs.
+__device__ __forceinline__ void compand_fast2(f2 a, f2 alpha2, f2 c16_2, uint32_t& b0,
+                                              uint32_t& b1) {
+  const f2 t = __ffma2_rn(alpha2, a, make_float2(1.0f, 1.0f));
+  const f2 l = make_float2(lg2_approx(t.x), lg2_approx(t.y));
+  const f2 s = __ffma2_rd(l, c16_2, make_float2(kC0, kC0));
+  b0 = __float_as_uint(s.x);
+  b1 = __float_as_uint(s.y);
 }
 __device__ __forceinline__ bool compand_ambiguous(uint32_t bits) {
   return (bits & 0xffffu) < 2u * kAmbiguityK;
@@ -69,14 +77,15 @@ struct EncGeom {
   static constexpr int kThreads = 2 * P;
   static constexpr int kWarps = P / 16;
   static constexpr int kNC = P / C;
-  static constexpr int kWPC = C / 16;
+  static constexpr int kTL = C / 8;         // token lanes
+  static constexpr int kCG = 256 / C;       // channel groups of 8 per warp
+  static constexpr int kSlices = C / 16;    // warps per chunk
   static constexpr int kTileBytes = P * kD * 2;
   static constexpr int kStages = kTileBytes <= 32768 ? 3 : 2;
   static constexpr int kMetaRows = 2 + 2 * kNC;
-  // min/max partials (2 x kWarps x 128), chunk-sum partials aliased onto
-  // the min partials, sigma partials (kWarps x 128, WPC > 1 only), and the
-  // per-channel gamma_min and 1/(gamma_scale + eps).
-  static constexpr int kRedFloats = kWarps * kD * (kWPC > 1 ? 3 : 2) + 2 * kD;
+  // per-chunk min/max partials (2 x kNC x 128) and the per-channel gamma_min
+  // and 1/(gamma_scale + eps).
+  static constexpr int kRedFloats = 2 * kNC * kD + 2 * kD;
   static constexpr size_t kSmem =
       (size_t)kStages * kTileBytes + (size_t)kRedFloats * 4 + kStages * 8;
   static_assert(C >= 16 && C <= P, "chunk");
@@ -93,20 +102,15 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   float* red_mn = reinterpret_cast<float*>(smem + G::kStages * G::kTileBytes);
-  float* red_mx = red_mn + G::kWarps * kD;
-  // Chunk-sum partials reuse red_mn: red_mn's last reads (stage 1b) are
-  // before the barrier that precedes the first red_sum write, and red_sum's
-  // last reads are before the barrier that precedes the next block's red_mn
-  // writes.
-  float* red_sum = red_mn;                       // used when WPC > 1
-  float* red_sg = red_mx + G::kWarps * kD;       // used when WPC > 1
-  float* st_gmin = red_mn + G::kWarps * kD * (G::kWPC > 1 ? 3 : 2);
+  float* red_mx = red_mn + G::kNC * kD;
+  float* st_gmin = red_mx + G::kNC * kD;
   float* st_rg = st_gmin + kD;
   uint64_t* bars = reinterpret_cast<uint64_t*>(st_rg + kD);
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int g = lane & 15, e1 = lane >> 4;
-  const int c = w / G::kWPC, u = w % G::kWPC;
+  const int cg = lane % G::kCG, tl = lane / G::kCG;
+  const int c = w / G::kSlices;                      // chunk of the warp
+  const int g = (w % G::kSlices) * G::kCG + cg;      // channel group (8 channels)
 
   if (tid == 0) {
     for (int i = 0; i < G::kStages; ++i) mbar_init(&bars[i], 1);
@@ -127,7 +131,7 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       if (blk < nblk) issue(blk, i);
     }
 
-  const float alpha = tab.alpha, c16 = tab.c16;
+  const f2 alpha2 = make_float2(tab.alpha, tab.alpha), c16_2 = make_float2(tab.c16, tab.c16);
   const float inv_C = 1.0f / (float)C;
   int it = 0;
   for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
@@ -140,7 +144,7 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
     uint32_t mn[4], mx[4];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const int t = c * C + m * 2 * G::kWPC + e1 * G::kWPC + u;
+      const int t = c * C + G::kTL * m + tl;
       const uint4 v = tile[t * 16 + g];
       const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -150,13 +154,15 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       }
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      mn[k] = bf2_min(mn[k], __shfl_xor_sync(kFull, mn[k], 16));
-      mx[k] = bf2_max(mx[k], __shfl_xor_sync(kFull, mx[k], 16));
-    }
-    if (e1 == 0) {
-      float4* pm = reinterpret_cast<float4*>(red_mn + w * kD + 8 * g);
-      float4* px = reinterpret_cast<float4*>(red_mx + w * kD + 8 * g);
+    for (int x = G::kCG; x < 32; x <<= 1)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mn[k] = bf2_min(mn[k], __shfl_xor_sync(kFull, mn[k], x));
+        mx[k] = bf2_max(mx[k], __shfl_xor_sync(kFull, mx[k], x));
+      }
+    if (tl == 0) {
+      float4* pm = reinterpret_cast<float4*>(red_mn + c * kD + 8 * g);
+      float4* px = reinterpret_cast<float4*>(red_mx + c * kD + 8 * g);
       const f2 a0 = bf2_to_f2(mn[0]), a1 = bf2_to_f2(mn[1]);
       const f2 a2 = bf2_to_f2(mn[2]), a3 = bf2_to_f2(mn[3]);
       pm[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
@@ -190,9 +196,9 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
     if (tid < kD) {
       float lo = red_mn[tid], hi = red_mx[tid];
 #pragma unroll
-      for (int ww = 1; ww < G::kWarps; ++ww) {
-        lo = fminf(lo, red_mn[ww * kD + tid]);
-        hi = fmaxf(hi, red_mx[ww * kD + tid]);
+      for (int cc = 1; cc < G::kNC; ++cc) {
+        lo = fminf(lo, red_mn[cc * kD + tid]);
+        hi = fmaxf(hi, red_mx[cc * kD + tid]);
       }
       // one sign for a zero extreme: -0 for the minimum (zero x then centre
       // to +0), +0 for the maximum
@@ -220,7 +226,7 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
     f2 n[8][4];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const int t = c * C + m * 2 * G::kWPC + e1 * G::kWPC + u;
+      const int t = c * C + G::kTL * m + tl;
       const uint4 v = tile[t * 16 + g];
       const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -242,38 +248,15 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       t0 = add2(t0, t2);
       t1 = add2(t1, t3);
       f2 s = add2(t0, t1);
-      f2 o;
-      o.x = __shfl_xor_sync(kFull, s.x, 16);
-      o.y = __shfl_xor_sync(kFull, s.y, 16);
-      mu2[k] = add2(s, o);
-    }
-    if constexpr (G::kWPC > 1) {
-      if (e1 == 0) {
-        float4* ps = reinterpret_cast<float4*>(red_sum + w * kD + 8 * g);
-        ps[0] = make_float4(mu2[0].x, mu2[0].y, mu2[1].x, mu2[1].y);
-        ps[1] = make_float4(mu2[2].x, mu2[2].y, mu2[3].x, mu2[3].y);
+#pragma unroll
+      for (int hh = G::kTL / 2; hh >= 1; hh /= 2) {  // token lanes tl and tl ^ hh
+        f2 o;
+        o.x = __shfl_xor_sync(kFull, s.x, hh * G::kCG);
+        o.y = __shfl_xor_sync(kFull, s.y, hh * G::kCG);
+        s = add2(s, o);
       }
-      __syncthreads();
-      f2 part[G::kWPC][4];
-#pragma unroll
-      for (int uu = 0; uu < G::kWPC; ++uu) {
-        const float4* ps =
-            reinterpret_cast<const float4*>(red_sum + (c * G::kWPC + uu) * kD + 8 * g);
-        const float4 a = ps[0], b = ps[1];
-        part[uu][0] = {a.x, a.y}; part[uu][1] = {a.z, a.w};
-        part[uu][2] = {b.x, b.y}; part[uu][3] = {b.z, b.w};
-      }
-#pragma unroll
-      for (int h = G::kWPC / 2; h >= 1; h /= 2)
-#pragma unroll
-        for (int uu = 0; uu < h; ++uu)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) part[uu][k] = add2(part[uu][k], part[uu + h][k]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) mu2[k] = part[0][k];
+      mu2[k] = mul2(s, f2{inv_C, inv_C});
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) mu2[k] = mul2(mu2[k], f2{inv_C, inv_C});
 
     // ---- Stage 2b: d = n - mu, sigma = max |d|
     float sg[8];
@@ -288,26 +271,10 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
         sg[2 * k + 1] = fmaxf(sg[2 * k + 1], fabsf(n[m][k].y));
       }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sg[i] = fmaxf(sg[i], __shfl_xor_sync(kFull, sg[i], 16));
-    if constexpr (G::kWPC > 1) {
-      if (e1 == 0) {
-        float4* ps = reinterpret_cast<float4*>(red_sg + w * kD + 8 * g);
-        ps[0] = make_float4(sg[0], sg[1], sg[2], sg[3]);
-        ps[1] = make_float4(sg[4], sg[5], sg[6], sg[7]);
-      }
-      __syncthreads();
+    for (int x = G::kCG; x < 32; x <<= 1)
 #pragma unroll
-      for (int uu = 0; uu < G::kWPC; ++uu) {
-        const float4* ps =
-            reinterpret_cast<const float4*>(red_sg + (c * G::kWPC + uu) * kD + 8 * g);
-        const float4 a = ps[0], b = ps[1];
-        sg[0] = fmaxf(sg[0], a.x); sg[1] = fmaxf(sg[1], a.y);
-        sg[2] = fmaxf(sg[2], a.z); sg[3] = fmaxf(sg[3], a.w);
-        sg[4] = fmaxf(sg[4], b.x); sg[5] = fmaxf(sg[5], b.y);
-        sg[6] = fmaxf(sg[6], b.z); sg[7] = fmaxf(sg[7], b.w);
-      }
-    }
-    if (e1 == 0 && u == 0) {
+      for (int i = 0; i < 8; ++i) sg[i] = fmaxf(sg[i], __shfl_xor_sync(kFull, sg[i], x));
+    if (tl == 0) {
       float4* pmu = reinterpret_cast<float4*>(mrow + (2 + c) * kD + 8 * g);
       float4* psg = reinterpret_cast<float4*>(mrow + (2 + G::kNC + c) * kD + 8 * g);
       pmu[0] = make_float4(mu2[0].x, mu2[0].y, mu2[1].x, mu2[1].y);
@@ -327,7 +294,7 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
     uint32_t* rrow = residual + blk * (int64_t)(P * 16);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-      const int t = c * C + m * 2 * G::kWPC + e1 * G::kWPC + u;
+      const int t = c * C + G::kTL * m + tl;
       float a[8];
       uint32_t bits[8], dbits[8];
 #pragma unroll
@@ -337,9 +304,9 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
         a[2 * k + 1] = fabsf(xf.y);
         dbits[2 * k] = __float_as_uint(n[m][k].x);
         dbits[2 * k + 1] = __float_as_uint(n[m][k].y);
+        compand_fast2(make_float2(a[2 * k], a[2 * k + 1]), alpha2, c16_2, bits[2 * k],
+                      bits[2 * k + 1]);
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) bits[i] = compand_fast(a[i], alpha, c16);
       // smallest distance to a rounding boundary (low 16 bits) of the 8
       // values, two at a time in 16-bit lanes
       uint32_t dmin = __vminu2(prmt(bits[0], bits[1], 0x5410u), prmt(bits[2], bits[3], 0x5410u));
@@ -459,7 +426,9 @@ __global__ void compander_selfcheck_kernel(const __grid_constant__ CompanderTabl
   for (uint64_t ub = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; ub <= last;
        ub += (uint64_t)gridDim.x * blockDim.x) {
     const float a = __uint_as_float((uint32_t)ub);
-    const uint32_t bits = compand_fast(a, tab.alpha, tab.c16);
+    uint32_t bits, unused;
+    compand_fast2(make_float2(a, a), make_float2(tab.alpha, tab.alpha),
+                  make_float2(tab.c16, tab.c16), bits, unused);
     int lo = 0, hi = 127;  // exact: number of thresholds <= a
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;
