@@ -83,9 +83,12 @@ struct EncGeom {
   static constexpr int kTileBytes = P * kD * 2;
   static constexpr int kStages = kTileBytes <= 32768 ? 3 : 2;
   static constexpr int kMetaRows = 2 + 2 * kNC;
-  // per-chunk min/max partials (2 x kNC x 128) and the per-channel gamma_min
-  // and 1/(gamma_scale + eps).
-  static constexpr int kRedFloats = 2 * kNC * kD + 2 * kD;
+  // per-chunk min/max partials (2 x kNC x 128), double-buffered by block
+  // parity: a warp may still read one block's partials while a faster warp
+  // writes the next block's.
+  static constexpr int kRedFloats = 2 * 2 * kNC * kD;
+  // page-statistic channels each token lane computes (of its group's 8)
+  static constexpr int kCPL = kTL >= 8 ? 1 : 8 / kTL;
   static constexpr size_t kSmem =
       (size_t)kStages * kTileBytes + (size_t)kRedFloats * 4 + kStages * 8;
   static_assert(C >= 16 && C <= P, "chunk");
@@ -102,10 +105,7 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   float* red_mn = reinterpret_cast<float*>(smem + G::kStages * G::kTileBytes);
-  float* red_mx = red_mn + G::kNC * kD;
-  float* st_gmin = red_mx + G::kNC * kD;
-  float* st_rg = st_gmin + kD;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(st_rg + kD);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(red_mn + G::kRedFloats);
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int cg = lane % G::kCG, tl = lane / G::kCG;
@@ -141,6 +141,8 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
     const uint4* tile = reinterpret_cast<const uint4*>(tiles + stage * G::kTileBytes);
 
     // ---- Stage 1a: per-channel page min / max (exact, on bf16 pairs)
+    float* pmn = red_mn + (it & 1) * (2 * G::kNC * kD);   // [kNC][128]
+    float* pmx = pmn + G::kNC * kD;                        // [kNC][128]
     uint32_t mn[4], mx[4];
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
@@ -161,8 +163,8 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
         mx[k] = bf2_max(mx[k], __shfl_xor_sync(kFull, mx[k], x));
       }
     if (tl == 0) {
-      float4* pm = reinterpret_cast<float4*>(red_mn + c * kD + 8 * g);
-      float4* px = reinterpret_cast<float4*>(red_mx + c * kD + 8 * g);
+      float4* pm = reinterpret_cast<float4*>(pmn + c * kD + 8 * g);
+      float4* px = reinterpret_cast<float4*>(pmx + c * kD + 8 * g);
       const f2 a0 = bf2_to_f2(mn[0]), a1 = bf2_to_f2(mn[1]);
       const f2 a2 = bf2_to_f2(mn[2]), a3 = bf2_to_f2(mn[3]);
       pm[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
@@ -191,37 +193,41 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       }
     }
 
-    // ---- Stage 1b: gamma_min, gamma_scale, reciprocal (one thread/channel)
+    // ---- Stage 1b: gamma_min, gamma_scale, reciprocal.  The TL lanes that
+    // share a channel group split its 8 channels (kCPL each; with 16 token
+    // lanes two lanes compute each channel) and exchange them by shuffles.
     float* mrow = meta + blk * (int64_t)(G::kMetaRows * kD);
-    if (tid < kD) {
-      float lo = red_mn[tid], hi = red_mx[tid];
+    float lo_q[G::kCPL], rg_q[G::kCPL];
+#pragma unroll
+    for (int q = 0; q < G::kCPL; ++q) {
+      const int ch = 8 * g + ((tl * G::kCPL) & 7) + q;
+      float lo = pmn[ch], hi = pmx[ch];
 #pragma unroll
       for (int cc = 1; cc < G::kNC; ++cc) {
-        lo = fminf(lo, red_mn[cc * kD + tid]);
-        hi = fmaxf(hi, red_mx[cc * kD + tid]);
+        lo = fminf(lo, pmn[cc * kD + ch]);
+        hi = fmaxf(hi, pmx[cc * kD + ch]);
       }
       // one sign for a zero extreme: -0 for the minimum (zero x then centre
       // to +0), +0 for the maximum
       if (lo == 0.0f) lo = -0.0f;
       if (hi == 0.0f) hi = 0.0f;
       const float gs = __fsub_rn(hi, lo);
-      st_gmin[tid] = lo;
-      st_rg[tid] = __frcp_rn(__fadd_rn(gs, kEps));
-      mrow[tid] = lo;
-      mrow[kD + tid] = gs;
+      lo_q[q] = lo;
+      rg_q[q] = __frcp_rn(__fadd_rn(gs, kEps));
+      if (c == 0 && tl * G::kCPL < 8) {   // one writer per channel
+        mrow[ch] = lo;
+        mrow[kD + ch] = gs;
+      }
     }
-    __syncthreads();
-
     // ---- Stage 1c: n = (x - gmin) * rg for the thread's 8 tokens x 8 ch
     f2 gm2[4], rg2[4];
-    {
-      const float4* sg4 = reinterpret_cast<const float4*>(st_gmin + 8 * g);
-      const float4* sr4 = reinterpret_cast<const float4*>(st_rg + 8 * g);
-      const float4 q0 = sg4[0], q1 = sg4[1], r0 = sr4[0], r1 = sr4[1];
-      gm2[0] = {q0.x, q0.y}; gm2[1] = {q0.z, q0.w};
-      gm2[2] = {q1.x, q1.y}; gm2[3] = {q1.z, q1.w};
-      rg2[0] = {r0.x, r0.y}; rg2[1] = {r0.z, r0.w};
-      rg2[2] = {r1.x, r1.y}; rg2[3] = {r1.z, r1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {        // channel 8g + j comes from token lane j / kCPL
+      const int src = (j / G::kCPL) * G::kCG + cg;
+      const float lo = __shfl_sync(kFull, lo_q[j % G::kCPL], src);
+      const float rg = __shfl_sync(kFull, rg_q[j % G::kCPL], src);
+      if (j & 1) { gm2[j >> 1].y = lo; rg2[j >> 1].y = rg; }
+      else       { gm2[j >> 1].x = lo; rg2[j >> 1].x = rg; }
     }
     f2 n[8][4];
 #pragma unroll

@@ -54,6 +54,7 @@ CASES = [
     (2, 512, 2, 128, 64),
     (1, 768, 3, 256, 128),
     (5, 384, 1, 128, 16),
+    (2, 320, 3, 64, 32),       # five pages of 64
 ]
 
 
