@@ -264,22 +264,27 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       mu2[k] = mul2(s, f2{inv_C, inv_C});
     }
 
-    // ---- Stage 2b: d = n - mu, sigma = max |d|
+    // ---- Stage 2b: d = n - mu; sigma = max |d| over the chunk.  Every step
+    // x -> x - gmin -> * rg -> - mu rounds monotonically (rg > 0), so the
+    // largest |d| is that of the chunk's largest or smallest x, which stage
+    // 1a already holds per channel (mn, mx after the token-lane reduction).
     float sg[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sg[i] = 0.0f;
+    for (int k = 0; k < 4; ++k) {
+      const f2 lo = bf2_sub_f32(mn[k], gm2[k]), hi = bf2_sub_f32(mx[k], gm2[k]);
+      f2 nlo, nhi;
+      nlo.x = __fmul_rn(lo.x, rg2[k].x);
+      nlo.y = __fmul_rn(lo.y, rg2[k].y);
+      nhi.x = __fmul_rn(hi.x, rg2[k].x);
+      nhi.y = __fmul_rn(hi.y, rg2[k].y);
+      const f2 dlo = sub2(nlo, mu2[k]), dhi = sub2(nhi, mu2[k]);
+      sg[2 * k] = fmaxf(fabsf(dlo.x), fabsf(dhi.x));
+      sg[2 * k + 1] = fmaxf(fabsf(dlo.y), fabsf(dhi.y));
+    }
 #pragma unroll
     for (int m = 0; m < 8; ++m)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        n[m][k] = sub2(n[m][k], mu2[k]);
-        sg[2 * k] = fmaxf(sg[2 * k], fabsf(n[m][k].x));
-        sg[2 * k + 1] = fmaxf(sg[2 * k + 1], fabsf(n[m][k].y));
-      }
-#pragma unroll
-    for (int x = G::kCG; x < 32; x <<= 1)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sg[i] = fmaxf(sg[i], __shfl_xor_sync(kFull, sg[i], x));
+      for (int k = 0; k < 4; ++k) n[m][k] = sub2(n[m][k], mu2[k]);
     if (tl == 0) {
       float4* pmu = reinterpret_cast<float4*>(mrow + (2 + c) * kD + 8 * g);
       float4* psg = reinterpret_cast<float4*>(mrow + (2 + G::kNC + c) * kD + 8 * g);
@@ -288,11 +293,22 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       psg[0] = make_float4(sg[0], sg[1], sg[2], sg[3]);
       psg[1] = make_float4(sg[4], sg[5], sg[6], sg[7]);
     }
+    // rs = rn(1/(sigma + eps)): the token lanes of a channel group split the
+    // 8 channels as in stage 1b and exchange the reciprocals by shuffles.
+    float rs_q[G::kCPL];
+#pragma unroll
+    for (int q = 0; q < G::kCPL; ++q) {
+      const int j = ((tl * G::kCPL) & 7) + q;
+      float sj = sg[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) sj = j == i ? sg[i] : sj;
+      rs_q[q] = __frcp_rn(__fadd_rn(sj, kEps));
+    }
     f2 rs2[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      rs2[k].x = __frcp_rn(__fadd_rn(sg[2 * k], kEps));
-      rs2[k].y = __frcp_rn(__fadd_rn(sg[2 * k + 1], kEps));
+    for (int j = 0; j < 8; ++j) {
+      const float r = __shfl_sync(kFull, rs_q[j % G::kCPL], (j / G::kCPL) * G::kCG + cg);
+      if (j & 1) rs2[j >> 1].y = r; else rs2[j >> 1].x = r;
     }
 
     // ---- Stages 3-4: codes, sign map, nibble split, store one row per m
