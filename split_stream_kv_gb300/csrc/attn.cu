@@ -733,37 +733,37 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   }
 }
 
-// Merge the partials of one unit (sequence, KV head, row group): the CTAs
-// whose shares touch it, each through the partial of the matching segment.
+// Merge the partials of one query row of one unit (sequence, KV head, row
+// group): the CTAs whose shares touch the unit, each through the partial of
+// the matching segment.  One block per (unit, row), one thread per channel:
 // out = sum e^(m_s-M) o_s / sum e^(m_s-M) l_s, written to out[b][t][hq][:].
 __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnParams a, int RP) {
   const int64_t z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
+  const int r = blockIdx.y;
   const int rg = (int)(z % a.nrg), bh = (int)(z / a.nrg), h = bh % a.Hkv, b = bh / a.Hkv;
+  const int row = rg * RP + r;
+  if (row >= a.R) return;
   const int d = threadIdx.x;
   const int part_floats = 2 * RP + RP * kD;
   // CTA holding flattened chunk x: floor(((x + 1) n_cta - 1) / n_chunks)
   const int64_t first = z * a.NCH, last = first + a.NCH - 1;
   const int k0 = (int)(((first + 1) * a.n_cta - 1) / a.n_chunks);
   const int k1 = (int)(((last + 1) * a.n_cta - 1) / a.n_chunks);
-  for (int r = 0; r < RP; ++r) {
-    const int row = rg * RP + r;
-    if (row >= a.R) break;
-    float M = -INFINITY;
-    for (int k = k0; k <= k1; ++k) {
-      const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
-      M = fmaxf(M, a.part[(2 * k + seg) * part_floats + r]);
-    }
-    float num = 0.f, den = 0.f;
-    for (int k = k0; k <= k1; ++k) {
-      const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
-      const float* ps = a.part + (2 * k + seg) * part_floats;
-      const float f = ps[r] == -INFINITY ? 0.f : exp2f(ps[r] - M);
-      num += f * ps[2 * RP + r * kD + d];
-      den += f * ps[RP + r];
-    }
-    const int tq = row / a.G, gq = row % a.G;
-    a.out[((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + d] = num / den;
+  float M = -INFINITY;
+  for (int k = k0; k <= k1; ++k) {
+    const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
+    M = fmaxf(M, a.part[(2 * k + seg) * part_floats + r]);
   }
+  float num = 0.f, den = 0.f;
+  for (int k = k0; k <= k1; ++k) {
+    const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
+    const float* ps = a.part + (2 * k + seg) * part_floats;
+    const float f = ps[r] == -INFINITY ? 0.f : exp2f(ps[r] - M);
+    num += f * ps[2 * RP + r * kD + d];
+    den += f * ps[RP + r];
+  }
+  const int tq = row / a.G, gq = row % a.G;
+  a.out[((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + d] = num / den;
 }
 
 // ------------------------------------------------------------------ host
@@ -827,7 +827,8 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   fn<<<(unsigned)prm.n_cta, threads, smem, stream>>>(prm, tab);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine<<<(unsigned)(prm.batch * prm.Hkv * prm.nrg), kD, 0, stream>>>(prm, 8 * NT);
+  attn_combine<<<dim3((unsigned)(prm.batch * prm.Hkv * prm.nrg), (unsigned)(8 * NT)), kD, 0,
+                 stream>>>(prm, 8 * NT);
   return cudaGetLastError();
 }
 
