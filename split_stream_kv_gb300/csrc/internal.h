@@ -60,6 +60,7 @@ int report_error(int code, const char* msg);
 
 // Host read of the device flag set when a bounded wait gave up.
 cudaError_t read_wait_timeout(unsigned int* flag);
+cudaError_t read_decode_wait_timeout(unsigned int* flag);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -293,8 +293,12 @@ int lynx_compander_selfcheck(float alpha, uint64_t* counts, void* stream) {
 
 int lynx_wait_timeouts(unsigned int* flag) {
   if (!flag) return fail(LYNX_EINVAL, "null pointer");
-  cudaError_t e = read_wait_timeout(flag);
-  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_wait_timeouts");
+  unsigned int enc = 0, dec = 0;
+  cudaError_t e = read_wait_timeout(&enc);
+  if (e == cudaSuccess) e = read_decode_wait_timeout(&dec);
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_wait_timeouts");
+  *flag = (enc | dec) ? 1u : 0u;
+  return LYNX_OK;
 }
 
 }  // extern "C"
