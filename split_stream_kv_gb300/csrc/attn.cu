@@ -500,67 +500,169 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     }
     cp_commit();
 
+    // ---- the warp's own n-tiles: all NT of them for a single warp; for a
+    // warp pair, half of them each (tiles half*OWN .. +OWN-1), so that the
+    // two warps split the softmax.  Their full scores: the pair swaps the
+    // partial scores of the partner's tiles (a reduce-scatter).
+    constexpr int OWN = PAIR ? NT / 2 : NT;
+    float sc[2][OWN][4];
     if constexpr (PAIR) {
-      // partial scores over this warp's channel half + the partner's half
-      float* xchg = reinterpret_cast<float*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kQ);
-      const int it = left & 1;
-      float* mine = xchg + ((unit * 2 + half) * 2 + it) * (32 * 8 * NT);
-      const float* other = xchg + ((unit * 2 + (half ^ 1)) * 2 + it) * (32 * 8 * NT);
+      float* xs = reinterpret_cast<float*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kQ);
+      float* mine = xs + (unit * 2 + half) * (2 * OWN * 32 * 4);
+      const float* other = xs + (unit * 2 + (half ^ 1)) * (2 * OWN * 32 * 4);
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          *reinterpret_cast<float4*>(mine + ((j * NT + nt) * 32 + lane) * 4) =
-              make_float4(s[j][nt][0], s[j][nt][1], s[j][nt][2], s[j][nt][3]);
+        for (int q = 0; q < OWN; ++q) {            // the partner's tile (1-half)*OWN + q
+          float4 v;
+          v.x = half ? s[j][q][0] : s[j][OWN + q][0];
+          v.y = half ? s[j][q][1] : s[j][OWN + q][1];
+          v.z = half ? s[j][q][2] : s[j][OWN + q][2];
+          v.w = half ? s[j][q][3] : s[j][OWN + q][3];
+          *reinterpret_cast<float4*>(mine + ((j * OWN + q) * 32 + lane) * 4) = v;
+        }
       asm volatile("bar.sync %0, 64;" :: "r"(1 + unit) : "memory");
 #pragma unroll
       for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float4 v = *reinterpret_cast<const float4*>(other + ((j * NT + nt) * 32 + lane) * 4);
-          s[j][nt][0] += v.x; s[j][nt][1] += v.y; s[j][nt][2] += v.z; s[j][nt][3] += v.w;
+        for (int q = 0; q < OWN; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(other + ((j * OWN + q) * 32 + lane) * 4);
+          sc[j][q][0] = (half ? s[j][OWN + q][0] : s[j][q][0]) + v.x;
+          sc[j][q][1] = (half ? s[j][OWN + q][1] : s[j][q][1]) + v.y;
+          sc[j][q][2] = (half ? s[j][OWN + q][2] : s[j][q][2]) + v.z;
+          sc[j][q][3] = (half ? s[j][OWN + q][3] : s[j][q][3]) + v.w;
         }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < OWN; ++q)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[j][q][e] = s[j][q][e];
     }
 
-    // ---- online softmax (log2 domain); rows nt*8 + 2c, nt*8 + 2c + 1
-    uint32_t pb_hi[2][NT][2], pb_lo[2][NT][2];
+    // ---- online softmax (log2 domain) of the own tiles; rows tile*8 + 2c,
+    // tile*8 + 2c + 1.  m_run / l_run hold the own tiles' rows.  al: the
+    // factor that rescales the output of each own row (1 if its max holds).
+    uint32_t ph[2][OWN][2], pl[2][OWN][2];
+    float al[OWN][2];
+    bool rescale = false;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float cmax0 = fmaxf(fmaxf(s[0][nt][0], s[0][nt][2]), fmaxf(s[1][nt][0], s[1][nt][2]));
-      float cmax1 = fmaxf(fmaxf(s[0][nt][1], s[0][nt][3]), fmaxf(s[1][nt][1], s[1][nt][3]));
+    for (int q = 0; q < OWN; ++q) {
+      float cmax0 = fmaxf(fmaxf(sc[0][q][0], sc[0][q][2]), fmaxf(sc[1][q][0], sc[1][q][2]));
+      float cmax1 = fmaxf(fmaxf(sc[0][q][1], sc[0][q][3]), fmaxf(sc[1][q][1], sc[1][q][3]));
 #pragma unroll
       for (int x = 4; x <= 16; x <<= 1) {
         cmax0 = fmaxf(cmax0, __shfl_xor_sync(kFull, cmax0, x));
         cmax1 = fmaxf(cmax1, __shfl_xor_sync(kFull, cmax1, x));
       }
-      const float mn0 = fmaxf(m_run[nt][0], cmax0 * a.scale_log2);
-      const float mn1 = fmaxf(m_run[nt][1], cmax1 * a.scale_log2);
-      if (mn0 != m_run[nt][0] || mn1 != m_run[nt][1]) {
-        const float al0 = ex2(m_run[nt][0] - mn0), al1 = ex2(m_run[nt][1] - mn1);
-        l_run[nt][0] *= al0;
-        l_run[nt][1] *= al1;
+      const float mn0 = fmaxf(m_run[q][0], cmax0 * a.scale_log2);
+      const float mn1 = fmaxf(m_run[q][1], cmax1 * a.scale_log2);
+      al[q][0] = al[q][1] = 1.0f;
+      if (mn0 != m_run[q][0] || mn1 != m_run[q][1]) {
+        al[q][0] = ex2(m_run[q][0] - mn0);
+        al[q][1] = ex2(m_run[q][1] - mn1);
+        l_run[q][0] *= al[q][0];
+        l_run[q][1] *= al[q][1];
+        m_run[q][0] = mn0;
+        m_run[q][1] = mn1;
+        rescale = true;
+        if constexpr (!PAIR) {                 // own tiles are all tiles: rescale here
 #pragma unroll
-        for (int mt = 0; mt < NKT; ++mt) {
-          o[mt][nt][0] *= al0; o[mt][nt][1] *= al1; o[mt][nt][2] *= al0; o[mt][nt][3] *= al1;
+          for (int mt = 0; mt < NKT; ++mt) {
+            o[mt][q][0] *= al[q][0]; o[mt][q][1] *= al[q][1];
+            o[mt][q][2] *= al[q][0]; o[mt][q][3] *= al[q][1];
+          }
         }
-        m_run[nt][0] = mn0;
-        m_run[nt][1] = mn1;
       }
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const float p0 = ex2(fmaf(s[j][nt][0], a.scale_log2, -mn0));
-        const float p1 = ex2(fmaf(s[j][nt][1], a.scale_log2, -mn1));
-        const float p2 = ex2(fmaf(s[j][nt][2], a.scale_log2, -mn0));
-        const float p3 = ex2(fmaf(s[j][nt][3], a.scale_log2, -mn1));
-        l_run[nt][0] += p0 + p2;
-        l_run[nt][1] += p1 + p3;
+        const float p0 = ex2(fmaf(sc[j][q][0], a.scale_log2, -mn0));
+        const float p1 = ex2(fmaf(sc[j][q][1], a.scale_log2, -mn1));
+        const float p2 = ex2(fmaf(sc[j][q][2], a.scale_log2, -mn0));
+        const float p3 = ex2(fmaf(sc[j][q][3], a.scale_log2, -mn1));
+        l_run[q][0] += p0 + p2;
+        l_run[q][1] += p1 + p3;
         const uint32_t top = f2_to_bf2(p0, p1), bot = f2_to_bf2(p2, p3);
         const f2 th = bf2_to_f2(top), bh = bf2_to_f2(bot);
-        pb_hi[j][nt][0] = movtrans(top);
-        pb_hi[j][nt][1] = movtrans(bot);
-        pb_lo[j][nt][0] = movtrans(f2_to_bf2(p0 - th.x, p1 - th.y));
-        pb_lo[j][nt][1] = movtrans(f2_to_bf2(p2 - bh.x, p3 - bh.y));
+        ph[j][q][0] = movtrans(top);
+        ph[j][q][1] = movtrans(bot);
+        pl[j][q][0] = movtrans(f2_to_bf2(p0 - th.x, p1 - th.y));
+        pl[j][q][1] = movtrans(f2_to_bf2(p2 - bh.x, p3 - bh.y));
       }
+    }
+
+    // ---- P^T operands (hi, lo) and row factors of all NT tiles
+    uint32_t pb_hi[2][NT][2], pb_lo[2][NT][2];
+    float alf[NT][2];
+    if constexpr (PAIR) {
+      // swap the own tiles' P operands and factors with the partner
+      uint32_t* pxs = reinterpret_cast<uint32_t*>(
+          extra + ExtraLayout<FULL, PAIR, ONE, NT>::kQ + (size_t)NU * 2 * (2 * OWN * 32 * 16));
+      constexpr int PW = 2 * 2 * OWN * 2 + 2 * OWN;  // words per lane: P hi, lo; factors
+      uint32_t* mine = pxs + (unit * 2 + half) * (PW * 32);
+      const uint32_t* other = pxs + (unit * 2 + (half ^ 1)) * (PW * 32);
+      rescale = __any_sync(kFull, rescale);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < OWN; ++q)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            mine[(((j * OWN + q) * 2 + e) * 2 + 0) * 32 + lane] = ph[j][q][e];
+            mine[(((j * OWN + q) * 2 + e) * 2 + 1) * 32 + lane] = pl[j][q][e];
+          }
+#pragma unroll
+      for (int q = 0; q < OWN; ++q)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          mine[(2 * 2 * OWN * 2 + q * 2 + e) * 32 + lane] = __float_as_uint(al[q][e]);
+      // the partner's vote travels with its factors: a rescale anywhere
+      // in the pair shows as a factor other than 1
+      asm volatile("bar.sync %0, 64;" :: "r"(1 + unit) : "memory");
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < OWN; ++q)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t oh = other[(((j * OWN + q) * 2 + e) * 2 + 0) * 32 + lane];
+            const uint32_t ol = other[(((j * OWN + q) * 2 + e) * 2 + 1) * 32 + lane];
+            pb_hi[j][q][e] = half ? oh : ph[j][q][e];
+            pb_lo[j][q][e] = half ? ol : pl[j][q][e];
+            pb_hi[j][OWN + q][e] = half ? ph[j][q][e] : oh;
+            pb_lo[j][OWN + q][e] = half ? pl[j][q][e] : ol;
+          }
+      bool other_rescale = false;
+#pragma unroll
+      for (int q = 0; q < OWN; ++q)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float of = __uint_as_float(other[(2 * 2 * OWN * 2 + q * 2 + e) * 32 + lane]);
+          other_rescale |= of != 1.0f;
+          alf[q][e] = half ? of : al[q][e];
+          alf[OWN + q][e] = half ? al[q][e] : of;
+        }
+      rescale = rescale || __any_sync(kFull, other_rescale);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+#pragma unroll
+        for (int q = 0; q < OWN; ++q)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            pb_hi[j][q][e] = ph[j][q][e];
+            pb_lo[j][q][e] = pl[j][q][e];
+          }
+    }
+    if (PAIR && rescale) {
+#pragma unroll
+      for (int mt = 0; mt < NKT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[mt][nt][0] *= alf[nt][0]; o[mt][nt][1] *= alf[nt][1];
+          o[mt][nt][2] *= alf[nt][0]; o[mt][nt][3] *= alf[nt][1];
+        }
     }
 
     // ---- output: O^T += V^T P^T over this warp's V m-tiles (byte VB*g + mt)
@@ -611,23 +713,24 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     if (cross() && has_next) {
       // The run leaves unit u0 (only one work unit of a CTA can): park its
       // state for unit u0 in the CTA's flush record, start afresh on u0 + 1.
-      float lr[NT][2];
+      float lr[OWN][2];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
+      for (int q = 0; q < OWN; ++q)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          float v = l_run[nt][e];
+          float v = l_run[q][e];
 #pragma unroll
           for (int x = 4; x <= 16; x <<= 1) v += __shfl_xor_sync(kFull, v, x);
-          lr[nt][e] = v;
+          lr[q][e] = v;
         }
-      if (g == 0 && half == 0) {
+      if (g == 0) {                            // the own tiles' rows
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int q = 0; q < OWN; ++q)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            flush[nt * 8 + 2 * c + e] = m_run[nt][e];
-            flush[RP + nt * 8 + 2 * c + e] = lr[nt][e];
+            const int row = (half * OWN + q) * 8 + 2 * c + e;
+            flush[row] = m_run[q][e];
+            flush[RP + row] = lr[q][e];
           }
       }
 #pragma unroll
@@ -645,9 +748,9 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
         }
       }
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt][0] = m_run[nt][1] = -INFINITY;
-        l_run[nt][0] = l_run[nt][1] = 0.f;
+      for (int q = 0; q < OWN; ++q) {
+        m_run[q][0] = m_run[q][1] = -INFINITY;
+        l_run[q][0] = l_run[q][1] = 0.f;
       }
     }
     if (has_next) {
@@ -659,12 +762,13 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   cp_wait<0>();
 
   // ---- merge the work units of the CTA per segment, write its partials
+  constexpr int OWNF = PAIR ? NT / 2 : NT;   // own tiles of a warp (see the loop)
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
+  for (int q = 0; q < OWNF; ++q)
 #pragma unroll
     for (int x = 4; x <= 16; x <<= 1) {
-      l_run[nt][0] += __shfl_xor_sync(kFull, l_run[nt][0], x);
-      l_run[nt][1] += __shfl_xor_sync(kFull, l_run[nt][1], x);
+      l_run[q][0] += __shfl_xor_sync(kFull, l_run[q][0], x);
+      l_run[q][1] += __shfl_xor_sync(kFull, l_run[q][1], x);
     }
   __syncthreads();  // every warp is done with Q, the exchange and the scratch
   float* sm_m = reinterpret_cast<float*>(extra);      // [NU][RP]
@@ -672,15 +776,16 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   float* sm_o = sm_l + NU * RP;                        // [NU][RP][128]
   int* sm_tag = reinterpret_cast<int*>(sm_o + NU * RP * kD);  // [NU] segment of the state
   int* sm_fl = sm_tag + NU;                                    // [NU] parked a state
-  if (g == 0 && half == 0) {
+  if (g == 0) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      sm_m[unit * RP + nt * 8 + 2 * c] = m_run[nt][0];
-      sm_m[unit * RP + nt * 8 + 2 * c + 1] = m_run[nt][1];
-      sm_l[unit * RP + nt * 8 + 2 * c] = l_run[nt][0];
-      sm_l[unit * RP + nt * 8 + 2 * c + 1] = l_run[nt][1];
+    for (int q = 0; q < OWNF; ++q) {
+      const int row = (half * OWNF + q) * 8 + 2 * c;
+      sm_m[unit * RP + row] = m_run[q][0];
+      sm_m[unit * RP + row + 1] = m_run[q][1];
+      sm_l[unit * RP + row] = l_run[q][0];
+      sm_l[unit * RP + row + 1] = l_run[q][1];
     }
-    if (c == 0) {
+    if (c == 0 && half == 0) {
       sm_tag[unit] = sg;
       sm_fl[unit] = (ub < ue && sg != sg_start) ? 1 : 0;  // crossed, so parked a state
     }
