@@ -386,24 +386,69 @@ def run_lynx(args, rank, world, dev):
     h2d = kv_h.nbytes + sum(t.nbytes for t in pk_h) + q1_h.nbytes + q8_h.nbytes
     d2h = anc_h.nbytes + res_h.nbytes + meta_h.nbytes + o1_h.nbytes + o8_h.nbytes
 
+    # The step is pipelined over three streams, as the pages' serializer
+    # overlaps the transfer of one page with the quantisation of the next:
+    # the BF16 input arrives in slices and each slice is encoded as soon as
+    # it has landed; the code streams of a slice go back to the host while
+    # later slices are encoded and the decoders and attention run.  Events
+    # keep the reuse of the device buffers across steps ordered.
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    nsl = 8 if c["B"] % 8 == 0 else 1
+    bs = c["B"] // nsl
+    ev_in = [torch.cuda.Event() for _ in range(nsl)]
+    ev_enc = [torch.cuda.Event() for _ in range(nsl)]
+    ev_back = [torch.cuda.Event() for _ in range(nsl)]
+    ev_attn_in, ev_cmp, ev_res_back = (torch.cuda.Event() for _ in range(3))
+    first = [True]
+
     def e2e_step():
-        kv.copy_(kv_h, non_blocking=True)
-        for d, hsrc in zip(pk_d, pk_h):
-            d.copy_(hsrc, non_blocking=True)
-        q1.copy_(q1_h, non_blocking=True)
-        q8.copy_(q8_h, non_blocking=True)
-        lynx.lynx_encode(kv, c["P"], c["C"], ALPHA, anc, res, meta)
-        anc_h.copy_(anc, non_blocking=True)
-        res_h.copy_(res, non_blocking=True)
-        meta_h.copy_(meta, non_blocking=True)
-        lynx.lynx_decode_anchor(anc, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_a)
-        lynx.lynx_decode_full(anc, res, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_f)
-        lynx.lynx_attn_decode(q1, (pk_d[0], None, pk_d[2]), (pk_d[3], None, pk_d[5]), a["L"],
-                              a["P"], a["C"], ALPHA, lynx.LYNX_ANCHOR, out=out1, workspace=ws)
-        lynx.lynx_attn_decode(q8, tuple(pk_d[0:3]), tuple(pk_d[3:6]), a["L"], a["P"], a["C"],
-                              ALPHA, lynx.LYNX_FULL, out=out8, workspace=ws)
-        o1_h.copy_(out1, non_blocking=True)
-        o8_h.copy_(out8, non_blocking=True)
+        for k in range(nsl):
+            sl = slice(k * bs, (k + 1) * bs)
+            with torch.cuda.stream(s_in):
+                if not first[0]:
+                    s_in.wait_event(ev_enc[k])        # last step's encode has read kv[sl]
+                kv[sl].copy_(kv_h[sl], non_blocking=True)
+                ev_in[k].record(s_in)
+        with torch.cuda.stream(s_in):
+            if not first[0]:
+                s_in.wait_event(ev_cmp)               # last step's attention is done
+            for d, hsrc in zip(pk_d, pk_h):
+                d.copy_(hsrc, non_blocking=True)
+            q1.copy_(q1_h, non_blocking=True)
+            q8.copy_(q8_h, non_blocking=True)
+            ev_attn_in.record(s_in)
+        with torch.cuda.stream(s_cmp):
+            for k in range(nsl):
+                sl = slice(k * bs, (k + 1) * bs)
+                s_cmp.wait_event(ev_in[k])
+                if not first[0]:
+                    s_cmp.wait_event(ev_back[k])      # last step's codes of sl are home
+                lynx.lynx_encode(kv[sl], c["P"], c["C"], ALPHA, anc[sl], res[sl], meta[sl])
+                ev_enc[k].record(s_cmp)
+            lynx.lynx_decode_anchor(anc, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_a)
+            lynx.lynx_decode_full(anc, res, meta, c["L"], c["P"], c["C"], ALPHA, out=dec_f)
+            s_cmp.wait_event(ev_attn_in)
+            if not first[0]:
+                s_cmp.wait_event(ev_res_back)         # last step's outputs are home
+            lynx.lynx_attn_decode(q1, (pk_d[0], None, pk_d[2]), (pk_d[3], None, pk_d[5]),
+                                  a["L"], a["P"], a["C"], ALPHA, lynx.LYNX_ANCHOR, out=out1,
+                                  workspace=ws)
+            lynx.lynx_attn_decode(q8, tuple(pk_d[0:3]), tuple(pk_d[3:6]), a["L"], a["P"],
+                                  a["C"], ALPHA, lynx.LYNX_FULL, out=out8, workspace=ws)
+            ev_cmp.record(s_cmp)
+        with torch.cuda.stream(s_out):
+            for k in range(nsl):
+                sl = slice(k * bs, (k + 1) * bs)
+                s_out.wait_event(ev_enc[k])
+                anc_h[sl].copy_(anc[sl], non_blocking=True)
+                res_h[sl].copy_(res[sl], non_blocking=True)
+                meta_h[sl].copy_(meta[sl], non_blocking=True)
+                ev_back[k].record(s_out)
+            s_out.wait_event(ev_cmp)
+            o1_h.copy_(out1, non_blocking=True)
+            o8_h.copy_(out8, non_blocking=True)
+            ev_res_back.record(s_out)
+        first[0] = False
 
     e2e_steps = max(1, min(args.steps, 5))
     e2e_step()
