@@ -76,6 +76,8 @@ def _bind(lib):
     lib.oracle_decode_range.restype = I
     lib.oracle_attention_row.argtypes = [P, P, P, I64, I, I64, P]
     lib.oracle_attention_row.restype = None
+    lib.oracle_attention_row_tail.argtypes = [P, P, P, I64, P, P, I, I, I64, I64, P]
+    lib.oracle_attention_row_tail.restype = None
     return lib
 
 
@@ -305,6 +307,26 @@ def attention_row(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
     L, D = K.shape
     out = np.zeros(D, np.float64)
     _load().oracle_attention_row(_ptr(q), _ptr(K), _ptr(V), L, D, D, _ptr(out))
+    return out
+
+
+def attention_row_tail(q: np.ndarray, K: np.ndarray, V: np.ndarray, Kt: np.ndarray,
+                       Vt: np.ndarray, n_tail: int) -> np.ndarray:
+    """float64 attention of the verification row of draft position n_tail - 1
+    over the L cached tokens K, V and the draft's own tokens Kt[:n_tail],
+    Vt[:n_tail] [Review, Mechanism 3, single parallel verification pass;
+    Eq. 1].  All inputs float32 (the values the attention sees)."""
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    K = np.ascontiguousarray(K, dtype=np.float32)
+    V = np.ascontiguousarray(V, dtype=np.float32)
+    Kt = np.ascontiguousarray(Kt, dtype=np.float32)
+    Vt = np.ascontiguousarray(Vt, dtype=np.float32)
+    L, D = K.shape
+    if not 0 <= n_tail <= Kt.shape[0]:
+        raise ValueError("n_tail out of range")
+    out = np.zeros(D, np.float64)
+    _load().oracle_attention_row_tail(_ptr(q), _ptr(K), _ptr(V), L, _ptr(Kt), _ptr(Vt),
+                                      n_tail, D, D, D, _ptr(out))
     return out
 
 

@@ -382,3 +382,39 @@ void oracle_attention_row(const float *q, const float *K, const float *V,
     for (int d = 0; d < D; ++d) out[d] /= l;
     free(s);
 }
+
+/* One query row of the verification pass with the draft tokens' own keys
+ * and values [Review, Mechanism 3, "Single parallel verification pass": one
+ * forward pass over the whole draft sequence]: the row of draft position t
+ * attends to the L cached tokens (K, V, rows kv_stride apart) and to the
+ * fresh tokens 0..t of the draft (Kt, Vt, rows tail_stride apart), i.e.
+ * n_tail = t + 1 of them; one float64 softmax over all L + n_tail scores,
+ * each scaled by 1/sqrt(D) [Eq. 1]. */
+void oracle_attention_row_tail(const float *q, const float *K, const float *V,
+                               int64_t L, const float *Kt, const float *Vt,
+                               int n_tail, int D, int64_t kv_stride,
+                               int64_t tail_stride, double *out)
+{
+    double scale = 1.0 / sqrt((double)D);
+    int64_t n = L + n_tail;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double m = -HUGE_VAL;
+    for (int64_t t = 0; t < n; ++t) {
+        const float *k = t < L ? K + t * kv_stride : Kt + (t - L) * tail_stride;
+        double acc = 0.0;
+        for (int d = 0; d < D; ++d)
+            acc += (double)q[d] * (double)k[d];
+        s[t] = acc * scale;
+        if (s[t] > m) m = s[t];
+    }
+    double l = 0.0;
+    for (int d = 0; d < D; ++d) out[d] = 0.0;
+    for (int64_t t = 0; t < n; ++t) {
+        const float *v = t < L ? V + t * kv_stride : Vt + (t - L) * tail_stride;
+        double w = exp(s[t] - m);
+        l += w;
+        for (int d = 0; d < D; ++d) out[d] += w * (double)v[d];
+    }
+    for (int d = 0; d < D; ++d) out[d] /= l;
+    free(s);
+}

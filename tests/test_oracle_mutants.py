@@ -41,11 +41,18 @@ MUTANTS = [
     ("decode affine operands transposed",
      "float xv = fmaf(nv, g_scale[d] + ORACLE_EPS, g_min[d]);",
      "float xv = fmaf(nv, g_min[d] + ORACLE_EPS, g_scale[d]);"),
-    ("attention scale 1/D", "double scale = 1.0 / sqrt((double)D);",
-     "double scale = 1.0 / (double)D;"),
-    ("softmax without the max shift", "double w = exp(s[t] - m);", "double w = exp(s[t]);"),
-    ("attention not normalised", "for (int d = 0; d < D; ++d) out[d] /= l;",
-     "for (int d = 0; d < D; ++d) out[d] /= 1.0;"),
+    ("attention scale 1/D",
+     "double scale = 1.0 / sqrt((double)D);\n    double *s = (double *)malloc(sizeof(double) * (size_t)L);",
+     "double scale = 1.0 / (double)D;\n    double *s = (double *)malloc(sizeof(double) * (size_t)L);"),
+    ("softmax without the max shift",
+     "double w = exp(s[t] - m);\n        l += w;\n        for (int d = 0; d < D; ++d) out[d] += w * (double)V[",
+     "double w = exp(s[t]);\n        l += w;\n        for (int d = 0; d < D; ++d) out[d] += w * (double)V["),
+    ("attention not normalised", "for (int d = 0; d < D; ++d) out[d] /= l;\n    free(s);\n}\n\n/* One query row",
+     "for (int d = 0; d < D; ++d) out[d] /= 1.0;\n    free(s);\n}\n\n/* One query row"),
+    ("verification row ignores the draft tokens", "int64_t n = L + n_tail;", "int64_t n = L;"),
+    ("draft tokens take the cached values",
+     "const float *v = t < L ? V + t * kv_stride : Vt + (t - L) * tail_stride;",
+     "const float *v = t < L ? V + t * kv_stride : V + (t - L) * kv_stride;"),
 ]
 
 # representative arguments for the parametrized pins

@@ -461,6 +461,53 @@ def test_attention_invariances(oracle_mod):
     assert np.allclose(out2, out, atol=1e-6)
 
 
+def test_attention_tail_is_the_concatenated_sequence(oracle_mod):
+    """The verification row of draft position t attends to the cached tokens
+    and to the draft's own tokens 0..t (Review, Mechanism 3, single parallel
+    verification pass): the same as plain attention over the concatenation."""
+    rng = np.random.default_rng(3)
+    L, T, D = 20, 4, 128
+    q = rng.standard_normal(D).astype(np.float32)
+    k, v = (rng.standard_normal((L, D)).astype(np.float32) for _ in range(2))
+    kt, vt = (rng.standard_normal((T, D)).astype(np.float32) for _ in range(2))
+    for n in range(T + 1):
+        got = oracle_mod.attention_row_tail(q, k, v, kt, vt, n)
+        want = oracle_mod.attention_row(q, np.concatenate([k, kt[:n]]), np.concatenate([v, vt[:n]]))
+        assert np.allclose(got, want, rtol=0, atol=1e-12), n
+
+
+def test_attention_tail_is_causal(oracle_mod):
+    """Draft tokens after the row's own position take no part: changing the
+    later tail tokens leaves the row unchanged, and a dominant later token
+    changes only the rows that see it."""
+    rng = np.random.default_rng(4)
+    L, T, D = 9, 3, 128
+    q = rng.standard_normal(D).astype(np.float32)
+    k, v = (rng.standard_normal((L, D)).astype(np.float32) for _ in range(2))
+    kt, vt = (rng.standard_normal((T, D)).astype(np.float32) for _ in range(2))
+    row1 = oracle_mod.attention_row_tail(q, k, v, kt, vt, 2)
+    kt2, vt2 = kt.copy(), vt.copy()
+    kt2[2] = (q * 50.0).astype(np.float32)      # dominant score for draft token 2
+    vt2[2] = 7.0
+    assert np.array_equal(oracle_mod.attention_row_tail(q, k, v, kt2, vt2, 2), row1)
+    assert np.allclose(oracle_mod.attention_row_tail(q, k, v, kt2, vt2, 3), 7.0, atol=1e-9)
+
+
+def test_attention_tail_hand_weights(oracle_mod):
+    """One cached token with score 0 and one draft token with score ln 3:
+    weights 1/4 and 3/4 (Eq. 1)."""
+    D = 128
+    q = np.zeros(D, np.float32)
+    q[0] = 1.0
+    k = np.zeros((1, D), np.float32)
+    kt = np.zeros((1, D), np.float32)
+    kt[0, 0] = np.float32(math.log(3.0) * math.sqrt(D))
+    v = np.full((1, D), 4.0, np.float32)
+    vt = np.full((1, D), 8.0, np.float32)
+    out = oracle_mod.attention_row_tail(q, k, v, kt, vt, 1)
+    assert np.allclose(out, 0.25 * 4.0 + 0.75 * 8.0, atol=1e-6)
+
+
 # ----------------------------------------------------------- size formulas
 
 def test_kv_size_example(oracle_mod):
