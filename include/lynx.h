@@ -136,6 +136,25 @@ int lynx_attn_decode(const void *q, int batch, int T, int H_q,
                      float *out, void *workspace, size_t workspace_bytes,
                      void *stream);
 
+/* lynx_attn_decode with the draft tokens' own keys and values: the single
+ * parallel verification pass of [Review, Mechanism 3] runs one forward pass
+ * over the whole draft s_1..s_T, so query token t (t = 0..T-1) attends to the
+ * L cached tokens and, causally, to draft tokens 0..t, whose keys and values
+ * that pass has just computed in BF16 (not quantised):
+ *   O_t = softmax(q_t [K; Kt_0..t]^T / sqrt(D)) [V; Vt_0..t]
+ *   k_tail, v_tail  [batch][T][H_kv][D] BF16, device, read only; token t of
+ *                   sequence b for KV head h at ((b*T + t)*H_kv + h)*D
+ * Everything else, the workspace size included, is as lynx_attn_decode; the
+ * draft tokens are merged in the split combine.  Null tails: LYNX_EINVAL. */
+int lynx_attn_decode_tail(const void *q, int batch, int T, int H_q,
+                          const void *k_anchor, const void *k_residual,
+                          const float *k_meta, const void *v_anchor,
+                          const void *v_residual, const float *v_meta,
+                          int64_t L, int H_kv, int D, int page, int C,
+                          float alpha, int mode, const void *k_tail,
+                          const void *v_tail, float *out, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
 /* lynx_attn_decode without a caller-provided workspace, for callers that
  * cannot allocate device memory: code that runs while a stream is being
  * captured into a CUDA graph, real-time or signal paths that must not enter an

@@ -113,6 +113,7 @@ struct AttnParams {
   const uint16_t* q;
   const uint8_t *ka, *kr, *va, *vr;
   const float *km, *vm;
+  const uint16_t *kt, *vt;  // draft tokens' own keys / values, or null
   float* part;
   float* out;
   int batch, T, Hq, Hkv, G, R, nrg;
@@ -842,13 +843,22 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
 // group): the CTAs whose shares touch the unit, each through the partial of
 // the matching segment.  One block per (unit, row), one thread per channel:
 // out = sum e^(m_s-M) o_s / sum e^(m_s-M) l_s, written to out[b][t][hq][:].
+// With the draft tokens' own keys and values, query token t also attends to
+// draft tokens 0..t ("Lynx", Mechanism 3, single parallel verification
+// pass): their scores join the same softmax.
+__device__ __forceinline__ float bf16_to_f32(uint16_t x) {
+  return __uint_as_float((uint32_t)x << 16);
+}
 __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnParams a, int RP) {
+  __shared__ float red[kD / 32];
+  __shared__ float s_tail[32];
   const int64_t z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
   const int r = blockIdx.y;
   const int rg = (int)(z % a.nrg), bh = (int)(z / a.nrg), h = bh % a.Hkv, b = bh / a.Hkv;
   const int row = rg * RP + r;
   if (row >= a.R) return;
   const int d = threadIdx.x;
+  const int tq = row / a.G, gq = row % a.G;
   const int part_floats = 2 * RP + RP * kD;
   // CTA holding flattened chunk x: floor(((x + 1) n_cta - 1) / n_chunks)
   const int64_t first = z * a.NCH, last = first + a.NCH - 1;
@@ -859,6 +869,20 @@ __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnP
     const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
     M = fmaxf(M, a.part[(2 * k + seg) * part_floats + r]);
   }
+  const int ntail = a.kt ? tq + 1 : 0;
+  if (ntail) {
+    const float qd = bf16_to_f32(a.q[((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + d]);
+    for (int j = 0; j < ntail; ++j) {
+      float prod = qd * bf16_to_f32(a.kt[((int64_t)(b * a.T + j) * a.Hkv + h) * kD + d]);
+#pragma unroll
+      for (int o = 16; o; o >>= 1) prod += __shfl_xor_sync(kFull, prod, o);
+      if ((d & 31) == 0) red[d >> 5] = prod;
+      __syncthreads();
+      if (d == 0) s_tail[j] = (red[0] + red[1] + red[2] + red[3]) * a.scale_log2;
+      __syncthreads();
+    }
+    for (int j = 0; j < ntail; ++j) M = fmaxf(M, s_tail[j]);
+  }
   float num = 0.f, den = 0.f;
   for (int k = k0; k <= k1; ++k) {
     const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
@@ -867,7 +891,11 @@ __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnP
     num += f * ps[2 * RP + r * kD + d];
     den += f * ps[RP + r];
   }
-  const int tq = row / a.G, gq = row % a.G;
+  for (int j = 0; j < ntail; ++j) {
+    const float f = exp2f(s_tail[j] - M);
+    num += f * bf16_to_f32(a.vt[((int64_t)(b * a.T + j) * a.Hkv + h) * kD + d]);
+    den += f;
+  }
   a.out[((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + d] = num / den;
 }
 
@@ -952,6 +980,8 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
   prm.vr = static_cast<const uint8_t*>(x.v_residual);
   prm.km = x.k_meta;
   prm.vm = x.v_meta;
+  prm.kt = static_cast<const uint16_t*>(x.k_tail);
+  prm.vt = static_cast<const uint16_t*>(x.v_tail);
   prm.part = static_cast<float*>(x.workspace);
   prm.out = x.out;
   prm.batch = x.batch;

@@ -51,6 +51,10 @@ struct AttnArgs {
   bool full;
   float* out;
   void* workspace;
+  // optional: the draft tokens' own keys and values [batch][T][H_kv][D] BF16;
+  // query token t then also attends to draft tokens 0..t
+  const void* k_tail = nullptr;
+  const void* v_tail = nullptr;
 };
 size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L);
 cudaError_t launch_attn(const AttnArgs& a, const ExpandTable& tab, cudaStream_t stream);

@@ -248,11 +248,12 @@ int lynx_attn_workspace_bytes(int batch, int T, int H_q, int64_t L, int H_kv, in
   return LYNX_OK;
 }
 
-int lynx_attn_decode(const void* q, int batch, int T, int H_q, const void* k_anchor,
-                     const void* k_residual, const float* k_meta, const void* v_anchor,
-                     const void* v_residual, const float* v_meta, int64_t L, int H_kv, int D,
-                     int page, int C, float alpha, int mode, float* out, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+static int attn_common(const void* q, int batch, int T, int H_q, const void* k_anchor,
+                       const void* k_residual, const float* k_meta, const void* v_anchor,
+                       const void* v_residual, const float* v_meta, int64_t L, int H_kv, int D,
+                       int page, int C, float alpha, int mode, const void* k_tail,
+                       const void* v_tail, float* out, void* workspace, size_t workspace_bytes,
+                       void* stream, const char* what) {
   int rc = check_attn_shape(batch, T, H_q, L, H_kv, D, page, C);
   if (rc) return rc;
   if ((rc = check_alpha(alpha))) return rc;
@@ -278,8 +279,35 @@ int lynx_attn_decode(const void* q, int batch, int T, int H_q, const void* k_anc
   a.full = mode == LYNX_FULL;
   a.out = out;
   a.workspace = workspace;
+  a.k_tail = k_tail;
+  a.v_tail = v_tail;
   cudaError_t e = launch_attn(a, tables_for(alpha).expand, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_attn_decode");
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, what);
+}
+
+int lynx_attn_decode(const void* q, int batch, int T, int H_q, const void* k_anchor,
+                     const void* k_residual, const float* k_meta, const void* v_anchor,
+                     const void* v_residual, const float* v_meta, int64_t L, int H_kv, int D,
+                     int page, int C, float alpha, int mode, float* out, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return attn_common(q, batch, T, H_q, k_anchor, k_residual, k_meta, v_anchor, v_residual,
+                     v_meta, L, H_kv, D, page, C, alpha, mode, nullptr, nullptr, out, workspace,
+                     workspace_bytes, stream, "lynx_attn_decode");
+}
+
+int lynx_attn_decode_tail(const void* q, int batch, int T, int H_q, const void* k_anchor,
+                          const void* k_residual, const float* k_meta, const void* v_anchor,
+                          const void* v_residual, const float* v_meta, int64_t L, int H_kv,
+                          int D, int page, int C, float alpha, int mode, const void* k_tail,
+                          const void* v_tail, float* out, void* workspace,
+                          size_t workspace_bytes, void* stream) {
+  if (batch > 0 && T > 0) {
+    int rc = check_ptrs({k_tail, v_tail});
+    if (rc) return rc;
+  }
+  return attn_common(q, batch, T, H_q, k_anchor, k_residual, k_meta, v_anchor, v_residual,
+                     v_meta, L, H_kv, D, page, C, alpha, mode, k_tail, v_tail, out, workspace,
+                     workspace_bytes, stream, "lynx_attn_decode_tail");
 }
 
 int lynx_compander_selfcheck(float alpha, uint64_t* counts, void* stream) {

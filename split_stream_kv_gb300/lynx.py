@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
         "lynx_attn_workspace_bytes": ([I, I, I, I64, I, I, I, PSZ], I),
         "lynx_attn_decode": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P, SZ, P],
                              I),
+        "lynx_attn_decode_tail": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P, P, P,
+                                   SZ, P], I),
         "lynx_attn_decode_noalloc": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P],
                                      I),
         "lynx_compander_thresholds": ([F, P], I),
@@ -164,12 +166,17 @@ def lynx_attn_workspace_bytes(batch: int, T: int, H_q: int, L: int, H_kv: int, D
 
 
 def lynx_attn_decode(q, k_streams, v_streams, L: int, page: int, C: int, alpha: float,
-                     mode: int, out=None, workspace=None):
+                     mode: int, out=None, workspace=None, k_tail=None, v_tail=None):
     """q[batch][T][H_q][D] bf16; k_streams / v_streams = (anchor, residual or
-    None, meta) from lynx_encode of K and V.  Returns out[batch][T][H_q][D] f32."""
+    None, meta) from lynx_encode of K and V.  With k_tail / v_tail
+    ([batch][T][H_kv][D] bf16, the draft tokens' own keys and values) query
+    token t also attends to draft tokens 0..t (lynx_attn_decode_tail).
+    Returns out[batch][T][H_q][D] f32."""
     ka, kr, km = k_streams
     va, vr, vm = v_streams
-    _need_cuda(q, ka, kr, km, va, vr, vm, out, workspace)
+    _need_cuda(q, ka, kr, km, va, vr, vm, out, workspace, k_tail, v_tail)
+    if (k_tail is None) != (v_tail is None):
+        raise ValueError("lynx_attn_decode: give both k_tail and v_tail, or neither")
     if q.dtype != torch.bfloat16 or q.dim() != 4:
         raise ValueError("lynx_attn_decode: q must be a 4-D bfloat16 tensor")
     batch, T, H_q, D = q.shape
@@ -179,11 +186,33 @@ def lynx_attn_decode(q, k_streams, v_streams, L: int, page: int, C: int, alpha: 
     need = lynx_attn_workspace_bytes(batch, T, H_q, L, H_kv, D, page)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if k_tail is not None:
+        for t in (k_tail, v_tail):
+            if t.dtype != torch.bfloat16 or tuple(t.shape) != (batch, T, H_kv, D) or \
+                    not t.is_contiguous():
+                raise ValueError("lynx_attn_decode: tails must be contiguous bfloat16 "
+                                 "[batch][T][H_kv][D]")
+        _check(lib().lynx_attn_decode_tail(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr),
+                                           _ptr(km), _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D,
+                                           page, C, alpha, mode, _ptr(k_tail), _ptr(v_tail),
+                                           _ptr(out), _ptr(workspace), workspace.numel(),
+                                           _stream(q.device)), "lynx_attn_decode_tail")
+        return out
     _check(lib().lynx_attn_decode(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr), _ptr(km),
                                   _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D, page, C, alpha,
                                   mode, _ptr(out), _ptr(workspace), workspace.numel(),
                                   _stream(q.device)), "lynx_attn_decode")
     return out
+
+
+def lynx_attn_decode_tail(q, k_streams, v_streams, L: int, page: int, C: int, alpha: float,
+                          mode: int, k_tail, v_tail, out=None, workspace=None):
+    """lynx_attn_decode_tail: query token t attends to the L cached tokens and
+    to the draft tokens 0..t given by k_tail / v_tail ([batch][T][H_kv][D] bf16)."""
+    if k_tail is None or v_tail is None:
+        raise ValueError("lynx_attn_decode_tail: k_tail and v_tail are required")
+    return lynx_attn_decode(q, k_streams, v_streams, L, page, C, alpha, mode, out=out,
+                            workspace=workspace, k_tail=k_tail, v_tail=v_tail)
 
 
 def lynx_attn_decode_noalloc(q, k_streams, v_streams, L: int, page: int, C: int,

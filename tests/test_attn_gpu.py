@@ -123,3 +123,66 @@ def test_shares_straddling_units_all_heads(lynx_lib, oracle_mod, cuda_dev):
     pairs = [(b, h) for b in range(4) for h in range(4)]
     r = _run(lynx_lib, oracle_mod, cuda_dev, 4, 10240, 4, 16, 8, 128, 32, pairs, seed=11)
     print(r)
+
+
+def _run_tail(lynx_lib, oracle_mod, dev, batch, L, H_kv, H_q, T, P, C, pairs, mode, seed):
+    """Attention with the draft tokens' own keys and values (causal tail)."""
+    from split_stream_kv_gb300 import synth
+    kv = synth.kv_cache(2 * batch, L, H_kv, 128, seed=seed, device=dev)
+    k = kv[0::2].contiguous()
+    v = kv[1::2].contiguous()
+    tail = synth.kv_cache(2 * batch, T, H_kv, 128, seed=seed + 1, device=dev)
+    kt = tail[0::2].contiguous()
+    vt = tail[1::2].contiguous()
+    ks = lynx_lib.lynx_encode(k, P, C, ALPHA)
+    vs = lynx_lib.lynx_encode(v, P, C, ALPHA)
+    full = mode == lynx_lib.LYNX_FULL
+    q = synth.queries(batch, T, H_q, 128, seed=seed + 2, device=dev)
+    out = lynx_lib.lynx_attn_decode_tail(q, ks if full else (ks[0], None, ks[2]),
+                                         vs if full else (vs[0], None, vs[2]),
+                                         L, P, C, ALPHA, mode, kt, vt)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    k_np = tuple(t.cpu().numpy() for t in ks)
+    v_np = tuple(t.cpu().numpy() for t in vs)
+    qf, o = q.float().cpu().numpy(), out.cpu().numpy()
+    ktf, vtf = kt.float().cpu().numpy(), vt.float().cpu().numpy()
+    G = H_q // H_kv
+    worst = 0.0
+    for b, h in pairs:
+        K = _decode_seq_head(oracle_mod, k_np, b, h, L, P, C, full)
+        V = _decode_seq_head(oracle_mod, v_np, b, h, L, P, C, full)
+        norm = np.maximum(1.0, np.maximum(np.abs(V).max(axis=0), np.abs(vtf[b, :, h]).max(axis=0)))
+        for t in range(T):
+            for gq in range(G):
+                hq = h * G + gq
+                ref = oracle_mod.attention_row_tail(qf[b, t, hq], K, V, ktf[b, :, h], vtf[b, :, h],
+                                                    t + 1)
+                rel = (np.abs(o[b, t, hq].astype(np.float64) - ref) / norm).max()
+                worst = max(worst, rel)
+                assert rel <= TOL, (b, t, hq, rel)
+    return worst
+
+
+@pytest.mark.parametrize("mode_name,batch,L,H_kv,H_q,T,P,C", [
+    ("full", 2, 1024, 2, 8, 8, 128, 32),     # 32 rows: warp-pair shape, draft length 8
+    ("anchor", 1, 2048, 2, 4, 2, 256, 64),   # 4 rows: single shape
+    ("full", 1, 768, 1, 3, 3, 128, 16),      # 9 rows, C = 16
+    ("anchor", 2, 512, 2, 2, 1, 64, 16),     # T = 1: the draft step sees its own token
+])
+def test_attention_with_draft_tokens(lynx_lib, oracle_mod, cuda_dev, mode_name, batch, L, H_kv,
+                                     H_q, T, P, C):
+    mode = lynx_lib.LYNX_FULL if mode_name == "full" else lynx_lib.LYNX_ANCHOR
+    pairs = [(b, h) for b in range(batch) for h in range(H_kv)]
+    r = _run_tail(lynx_lib, oracle_mod, cuda_dev, batch, L, H_kv, H_q, T, P, C, pairs, mode,
+                  seed=L + T)
+    print(r)
+
+
+def test_attention_with_draft_tokens_full_size_sampled(lynx_lib, oracle_mod, cuda_dev):
+    """The verification step of the bench workload (8 x 32768 tokens, 32
+    query heads over 8 KV heads, T = 8) with the draft tokens' own keys and
+    values; two sampled (sequence, KV head) pairs."""
+    r = _run_tail(lynx_lib, oracle_mod, cuda_dev, 8, 32768, 8, 32, 8, 128, 32, [(1, 2), (6, 7)],
+                  lynx_lib.LYNX_FULL, seed=9)
+    print(r)
