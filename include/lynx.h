@@ -127,7 +127,10 @@ int lynx_attn_workspace_bytes(int batch, int T, int H_q, int64_t L, int H_kv,
  *   out        [batch][T][H_q][D] float32, device, written
  *   workspace  device scratch of >= lynx_attn_workspace_bytes(...) bytes; its
  *              contents on entry do not matter and are clobbered
- * Limits: 1 <= T, H_q % H_kv == 0, (H_q / H_kv) * T <= 32, C >= 16, L >= 1. */
+ * Limits: 1 <= T <= 64 (the pages' speculative cap), H_q % H_kv == 0,
+ * (H_q / H_kv) * T <= 256, C >= 16, L >= 1.  Up to 8 query rows per KV head
+ * take the single-warp shape, up to 32 the warp-pair shape; beyond 32 the
+ * rows form groups of 32, each of which reads the packed K and V once. */
 int lynx_attn_decode(const void *q, int batch, int T, int H_q,
                      const void *k_anchor, const void *k_residual,
                      const float *k_meta, const void *v_anchor,

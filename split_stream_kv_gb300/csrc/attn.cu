@@ -851,7 +851,7 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t x) {
 }
 __global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnParams a, int RP) {
   __shared__ float red[kD / 32];
-  __shared__ float s_tail[32];
+  __shared__ float s_tail[64];               // draft tokens: T <= 64
   const int64_t z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
   const int r = blockIdx.y;
   const int rg = (int)(z % a.nrg), bh = (int)(z / a.nrg), h = bh % a.Hkv, b = bh / a.Hkv;

@@ -234,8 +234,9 @@ static int check_attn_shape(int batch, int T, int H_q, int64_t L, int H_kv, int 
   if (batch < 1 || L < 1) return fail(LYNX_ESHAPE, "attention needs batch >= 1 and L >= 1");
   if (T < 1) return fail(LYNX_ESHAPE, "T = %d must be >= 1", T);
   if (H_q < 1 || H_q % H_kv) return fail(LYNX_ESHAPE, "H_q = %d is not a multiple of H_kv = %d", H_q, H_kv);
-  if ((H_q / H_kv) * T > 32)
-    return fail(LYNX_EUNSUPPORTED, "(H_q/H_kv)*T = %d: at most 32 query rows per KV head", (H_q / H_kv) * T);
+  if (T > 64) return fail(LYNX_EUNSUPPORTED, "T = %d: at most 64 query tokens", T);
+  if ((H_q / H_kv) * T > 256)
+    return fail(LYNX_EUNSUPPORTED, "(H_q/H_kv)*T = %d: at most 256 query rows per KV head", (H_q / H_kv) * T);
   return LYNX_OK;
 }
 

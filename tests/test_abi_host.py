@@ -84,7 +84,8 @@ def test_attention_rejects(lynx_lib):
 
     assert call(Hq=6, Hkv=4) == -2            # H_q % H_kv
     assert call(T=0) == -2
-    assert call(T=9, Hq=4) == -3              # 36 rows > 32
+    assert call(T=65, Hq=1) == -3             # more than 64 query tokens
+    assert call(T=64, Hq=8, Hkv=1) == -3      # 512 rows > 256
     assert call(mode=1) == -1                 # full mode needs residuals
     assert call(mode=3) == -1
     assert call(ws=0) == -5

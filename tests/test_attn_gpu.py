@@ -100,6 +100,7 @@ def test_page_and_chunk_sizes(lynx_lib, oracle_mod, cuda_dev, P, C, L):
     (256, 64, 2048, 1, 8, 4, 1),     # 32 rows
     (128, 16, 1024, 1, 3, 3, 3),     # 9 rows both modes
     (128, 32, 768, 1, 16, 2, 1),     # 16 query heads per KV head: anchor mode with 16 rows
+    (128, 32, 1024, 2, 8, 16, 2),    # 64 rows: two row groups of 32
 ])
 def test_row_counts_and_pairs(lynx_lib, oracle_mod, cuda_dev, P, C, L, H_kv, H_q, T, Ta):
     pairs = [(0, h) for h in range(H_kv)]
@@ -169,6 +170,8 @@ def _run_tail(lynx_lib, oracle_mod, dev, batch, L, H_kv, H_q, T, P, C, pairs, mo
     ("anchor", 1, 2048, 2, 4, 2, 256, 64),   # 4 rows: single shape
     ("full", 1, 768, 1, 3, 3, 128, 16),      # 9 rows, C = 16
     ("anchor", 2, 512, 2, 2, 1, 64, 16),     # T = 1: the draft step sees its own token
+    ("full", 1, 1024, 2, 8, 64, 128, 32),    # T = 64, the pages' cap: 256 rows, 8 row groups
+    ("full", 1, 768, 1, 1, 40, 256, 32),     # 40 rows: a full and a partial row group
 ])
 def test_attention_with_draft_tokens(lynx_lib, oracle_mod, cuda_dev, mode_name, batch, L, H_kv,
                                      H_q, T, P, C):
