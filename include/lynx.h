@@ -107,6 +107,42 @@ int lynx_decode_full(const void *anchor, const void *residual,
                      int page, int C, float alpha, void *out, int out_dtype,
                      void *stream);
 
+/* ---- Paged streams.  The pages' prototype keeps KV in pages aligned with
+ * paged attention and scatters the decoded pages into device memory
+ * [Review, Implementation Notes; Mechanism 2, Anchor Phase step 3].  Paged
+ * variants keep the three streams in pools of num_blocks physical pages, each
+ * holding the H_kv head blocks of one page exactly as the dense layout does
+ * for one (b, page): anchor / residual pool [num_blocks][H_kv][page][D/2],
+ * meta pool [num_blocks][H_kv][2 + 2*page/C][D] float32 (the sizes
+ * lynx_encoded_sizes gives for B = 1, L = num_blocks * page).  A block table
+ * block_table[B][L/page] (int32, device, 16-byte aligned) names the physical
+ * page of each (sequence, logical page); K and V pools share one table.
+ * Entries must lie in [0, num_blocks); an entry outside is replaced by 0 and
+ * reported by lynx_device_errors (bit 2), so it gives wrong numbers, never a
+ * stray memory access.  Distinct (sequence, page) pairs should name distinct
+ * pages when encoding (pages written twice race). */
+
+/* lynx_encode writing each page block to its physical page in the pools. */
+int lynx_encode_paged(const void *kv, int64_t B, int64_t L, int H_kv, int D,
+                      int page, int C, float alpha, const int32_t *block_table,
+                      int64_t num_blocks, void *anchor_pool, void *residual_pool,
+                      float *meta_pool, void *stream);
+
+/* lynx_decode_anchor (mode LYNX_ANCHOR, residual_pool may be NULL) or
+ * lynx_decode_full (LYNX_FULL) reading each page through the block table;
+ * out is the dense [B][L][H_kv][D] tensor. */
+int lynx_decode_paged(const void *anchor_pool, const void *residual_pool,
+                      const float *meta_pool, const int32_t *block_table,
+                      int64_t num_blocks, int64_t B, int64_t L, int H_kv, int D,
+                      int page, int C, float alpha, int mode, void *out,
+                      int out_dtype, void *stream);
+
+/* Host call, synchronous: *bits = OR of the conditions any kernel of this
+ * library in this process has reported: 1 = a bounded wait on an
+ * asynchronous copy gave up (the kernel returned early, its outputs are
+ * incomplete), 2 = a block-table entry was outside [0, num_blocks). */
+int lynx_device_errors(unsigned int *bits);
+
 /* Host-only.  Device workspace (bytes) that lynx_attn_decode needs for these
  * sizes: split-K partial results, float32.  0 is never returned for valid
  * sizes.  Returns LYNX_OK or a shape/limit error. */
@@ -157,6 +193,19 @@ int lynx_attn_decode_tail(const void *q, int batch, int T, int H_q,
                           float alpha, int mode, const void *k_tail,
                           const void *v_tail, float *out, void *workspace,
                           size_t workspace_bytes, void *stream);
+
+/* lynx_attn_decode_tail over paged streams: the K and V pools are read
+ * through block_table (see the paged layout above).  k_tail and v_tail may
+ * both be NULL (no draft tokens: the pass of lynx_attn_decode). */
+int lynx_attn_decode_paged(const void *q, int batch, int T, int H_q,
+                           const void *k_anchor_pool, const void *k_residual_pool,
+                           const float *k_meta_pool, const void *v_anchor_pool,
+                           const void *v_residual_pool, const float *v_meta_pool,
+                           const int32_t *block_table, int64_t num_blocks,
+                           int64_t L, int H_kv, int D, int page, int C,
+                           float alpha, int mode, const void *k_tail,
+                           const void *v_tail, float *out, void *workspace,
+                           size_t workspace_bytes, void *stream);
 
 /* lynx_attn_decode without a caller-provided workspace, for callers that
  * cannot allocate device memory: code that runs while a stream is being

@@ -85,9 +85,9 @@ struct ExtraLayout {
   static constexpr int kHalves = PAIR ? 2 : 1;
   static constexpr size_t kQ = (size_t)2 * kHalves * NKT * NT * 32 * 8;  // [seg][half][kt][nt][lane]
   static constexpr size_t kXchg = PAIR ? (size_t)CF::kWarps * 2 * 32 * 8 * NT * 4 : 0;
-  static constexpr size_t kInfo = kQ + kXchg;  // int64 block base of segments 0, 1
-  static_assert(kLutBytes + kInfo + 16 + 1024 <= 116 * 1024, "two CTAs per SM");
-  static constexpr size_t kLoop = kInfo + 16;
+  static constexpr size_t kInfo = kQ + kXchg;  // int64 page-row base and head of segments 0, 1
+  static_assert(kLutBytes + kInfo + 32 + 1024 <= 116 * 1024, "two CTAs per SM");
+  static constexpr size_t kLoop = kInfo + 32;
   static constexpr size_t kMerge = (size_t)CF::kNU * 8 * NT * (2 + kD) * 4 + (size_t)CF::kNU * 8;
   static constexpr size_t kBytes = kLoop > kMerge ? kLoop : kMerge;
 };
@@ -109,11 +109,21 @@ __device__ __forceinline__ uint32_t unit_off(int tb, int r, int grp, int h) {
 }
 constexpr int kRowStride = 4 * 256;  // bytes between constant rows
 
+// Set when a block-table entry was out of range (bit kFlagBadBlock); read
+// through read_attn_flags(), never reset.
+__device__ unsigned int g_attn_flags = 0;
+
+cudaError_t read_attn_flags(unsigned int* flag) {
+  return cudaMemcpyFromSymbol(flag, g_attn_flags, sizeof(unsigned int));
+}
+
 struct AttnParams {
   const uint16_t* q;
   const uint8_t *ka, *kr, *va, *vr;
   const float *km, *vm;
   const uint16_t *kt, *vt;  // draft tokens' own keys / values, or null
+  const int32_t* bt;        // block table [batch][NB] of physical pages, or null (dense)
+  int64_t nphys;            // physical pages behind the table
   float* part;
   float* out;
   int batch, T, Hq, Hkv, G, R, nrg;
@@ -329,9 +339,10 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       reinterpret_cast<uint2*>(extra)[i] = q_frag(sg, hf, kt, nt, ln >> 2, ln & 3);
     }
   }
-  if (tid < 2) {
-    reinterpret_cast<int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo)[tid] =
-        (int64_t)(tid ? b1 : b0) * a.NB * a.Hkv + (tid ? h1 : h0);
+  if (tid < 2) {  // [0..1]: first page row (b * NB) of each segment, [2..3]: its KV head
+    int64_t* info = reinterpret_cast<int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo);
+    info[tid] = (int64_t)(tid ? b1 : b0) * a.NB;
+    info[2 + tid] = tid ? h1 : h0;
   }
   __syncthreads();
   const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 8u;
@@ -349,7 +360,16 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     const int t0 = qc * 32;
     const int p = t0 >> a.lgP;
     tp = t0 & (a.P - 1);
-    return seg_blk[sg] + p * a.Hkv;
+    const int64_t row = seg_blk[sg] + p;
+    int64_t pg = row;
+    if (a.bt) {  // paged streams: the table names the physical page
+      pg = __ldg(a.bt + row);
+      if (pg < 0 || pg >= a.nphys) {
+        atomicOr(&g_attn_flags, kFlagBadBlock);
+        pg = 0;
+      }
+    }
+    return pg * a.Hkv + seg_blk[2 + sg];
   };
   // Asynchronous copies of the constant rows of chunk qc into the warp's
   // rows of one tensor (gamma rows only with_gamma).  Each copy instruction
@@ -980,6 +1000,8 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
   prm.vr = static_cast<const uint8_t*>(x.v_residual);
   prm.km = x.k_meta;
   prm.vm = x.v_meta;
+  prm.bt = x.paging.table;
+  prm.nphys = x.paging.nphys;
   prm.kt = static_cast<const uint16_t*>(x.k_tail);
   prm.vt = static_cast<const uint16_t*>(x.v_tail);
   prm.part = static_cast<float*>(x.workspace);

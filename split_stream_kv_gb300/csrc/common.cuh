@@ -93,6 +93,29 @@ __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
                :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// --------------------------------------------------------------- paging
+
+// Bits of the per-file device flag words (read through lynx_device_errors).
+constexpr unsigned kFlagWaitTimeout = 1u;   // a bounded wait gave up
+constexpr unsigned kFlagBadBlock = 2u;      // a block-table entry was out of range
+
+// Physical page block of logical block blk = (b*NB + p)*H + h.  Without a
+// block table the streams are dense and the two coincide; with one, row
+// b*NB + p of the table names the physical page, whose H head blocks are
+// contiguous.  An entry outside [0, nphys) is replaced by 0 and reported in
+// *flag, so a bad table gives wrong numbers, never a stray access.
+__device__ __forceinline__ int64_t phys_block(const int32_t* bt, int64_t nphys, int64_t blk,
+                                              int H, unsigned int* flag) {
+  if (!bt) return blk;
+  const int64_t h = blk % H, row = blk / H;
+  int64_t pg = __ldg(bt + row);
+  if (pg < 0 || pg >= nphys) {
+    atomicOr(flag, kFlagBadBlock);
+    pg = 0;
+  }
+  return pg * H + h;
+}
+
 // --------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

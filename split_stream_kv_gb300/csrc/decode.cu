@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ residual,
               const float* __restrict__ meta, const int64_t nblk, const int64_t NB,
               const int H, const int64_t L, const int P, const int C,
-              void* __restrict__ out, const __grid_constant__ ExpandTable tab) {
+              void* __restrict__ out, const int32_t* __restrict__ bt, const int64_t nphys,
+              const __grid_constant__ ExpandTable tab) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31;
   const int g = tid & 15, slot = tid >> 4;
@@ -137,7 +138,8 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
   __syncthreads();
   const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 8u;
 
-  auto issue = [&](int64_t blk, int stage) {
+  auto issue = [&](int64_t lblk, int stage) {
+    const int64_t blk = phys_block(bt, nphys, lblk, H, &g_dec_wait_timeout);
     uint8_t* st = stages + stage * stage_bytes;
     mbar_expect_tx(&bars[stage], stage_bytes);
     bulk_load(st, anchor + blk * code_bytes, code_bytes, &bars[stage]);
@@ -236,7 +238,7 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
       // A stage never arrived: record it and stop this CTA (bounded waits
       // only, so the context stays usable).
       if (tid == 0) {
-        atomicExch(&g_dec_wait_timeout, 1u);
+        atomicOr(&g_dec_wait_timeout, kFlagWaitTimeout);
         for (int i = 0; i < kDecStages; ++i) (void)mbar_wait(&bars[i], phase);
       }
       return;
@@ -255,7 +257,7 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
 template <bool FULL, bool BF16OUT>
 static cudaError_t run_decode(const void* anchor, const void* residual, const float* meta,
                               const Shape& s, const ExpandTable& tab, void* out,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const Paging& pg) {
   auto fn = decode_kernel<FULL, BF16OUT>;
   const size_t stage = (size_t)s.page * (kD / 2) * (FULL ? 2 : 1) +
                        (size_t)(2 + 2 * (s.page / s.C)) * kD * 4;
@@ -291,20 +293,20 @@ static cudaError_t run_decode(const void* anchor, const void* residual, const fl
   if (grid > nblk) grid = nblk;
   fn<<<(unsigned)grid, kDecThreads, smem, stream>>>(
       static_cast<const uint8_t*>(anchor), static_cast<const uint8_t*>(residual), meta, nblk,
-      s.NB(), s.H, s.L, s.page, s.C, out, tab);
+      s.NB(), s.H, s.L, s.page, s.C, out, pg.table, pg.nphys, tab);
   return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const void* anchor, const void* residual, const float* meta,
                           const Shape& s, const ExpandTable& tab, void* out, bool bf16_out,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const Paging& pg) {
   if (s.blocks() == 0) return cudaSuccess;
   const bool full = residual != nullptr;
   if (full)
-    return bf16_out ? run_decode<true, true>(anchor, residual, meta, s, tab, out, stream)
-                    : run_decode<true, false>(anchor, residual, meta, s, tab, out, stream);
-  return bf16_out ? run_decode<false, true>(anchor, nullptr, meta, s, tab, out, stream)
-                  : run_decode<false, false>(anchor, nullptr, meta, s, tab, out, stream);
+    return bf16_out ? run_decode<true, true>(anchor, residual, meta, s, tab, out, stream, pg)
+                    : run_decode<true, false>(anchor, residual, meta, s, tab, out, stream, pg);
+  return bf16_out ? run_decode<false, true>(anchor, nullptr, meta, s, tab, out, stream, pg)
+                  : run_decode<false, false>(anchor, nullptr, meta, s, tab, out, stream, pg);
 }
 
 }  // namespace lynx

@@ -100,7 +100,8 @@ __global__ void __launch_bounds__(2 * P, 256 / P)
 encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
               const int64_t NB, const int H, const int64_t L,
               uint32_t* __restrict__ anchor, uint32_t* __restrict__ residual,
-              float* __restrict__ meta, const __grid_constant__ CompanderTable tab) {
+              float* __restrict__ meta, const int32_t* __restrict__ bt, const int64_t nphys,
+              const __grid_constant__ CompanderTable tab) {
   using G = EncGeom<P, C>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
@@ -178,7 +179,7 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       // A stage never arrived: record it and stop this CTA (bounded waits
       // only, so the context stays usable).
       if (tid == 0) {
-        atomicExch(&g_wait_timeout, 1u);
+        atomicOr(&g_wait_timeout, kFlagWaitTimeout);
         for (int i = 0; i < G::kStages; ++i) (void)mbar_wait(&bars[i], phase);
       }
       return;
@@ -196,7 +197,8 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
     // ---- Stage 1b: gamma_min, gamma_scale, reciprocal.  The TL lanes that
     // share a channel group split its 8 channels (kCPL each; with 16 token
     // lanes two lanes compute each channel) and exchange them by shuffles.
-    float* mrow = meta + blk * (int64_t)(G::kMetaRows * kD);
+    const int64_t pb = phys_block(bt, nphys, blk, H, &g_wait_timeout);  // output block
+    float* mrow = meta + pb * (int64_t)(G::kMetaRows * kD);
     float lo_q[G::kCPL], rg_q[G::kCPL];
 #pragma unroll
     for (int q = 0; q < G::kCPL; ++q) {
@@ -312,8 +314,8 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
     }
 
     // ---- Stages 3-4: codes, sign map, nibble split, store one row per m
-    uint32_t* arow = anchor + blk * (int64_t)(P * 16);
-    uint32_t* rrow = residual + blk * (int64_t)(P * 16);
+    uint32_t* arow = anchor + pb * (int64_t)(P * 16);
+    uint32_t* rrow = residual + pb * (int64_t)(P * 16);
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int t = c * C + G::kTL * m + tl;
@@ -358,12 +360,10 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
 
 // ------------------------------------------------------------------ launch
 
-using EncodeFn = void (*)(const CUtensorMap, int64_t, int64_t, int, int64_t, uint32_t*,
-                          uint32_t*, float*, const CompanderTable);
-
 template <int P, int C>
 static cudaError_t run_encode(const CUtensorMap& map, const Shape& s, const CompanderTable& tab,
-                              void* anchor, void* residual, float* meta, cudaStream_t stream) {
+                              void* anchor, void* residual, float* meta, cudaStream_t stream,
+                              const Paging& pg) {
   using G = EncGeom<P, C>;
   auto fn = encode_kernel<P, C>;
   static thread_local int configured_dev = -1;
@@ -388,7 +388,7 @@ static cudaError_t run_encode(const CUtensorMap& map, const Shape& s, const Comp
   if (grid > nblk) grid = nblk;
   fn<<<(unsigned)grid, G::kThreads, G::kSmem, stream>>>(
       map, nblk, s.NB(), s.H, s.L, static_cast<uint32_t*>(anchor),
-      static_cast<uint32_t*>(residual), meta, tab);
+      static_cast<uint32_t*>(residual), meta, pg.table, pg.nphys, tab);
   return cudaGetLastError();
 }
 
@@ -411,7 +411,8 @@ static EncodeTiledFn get_encode_tiled() {
 }
 
 cudaError_t launch_encode(const void* kv, const Shape& s, const CompanderTable& tab,
-                          void* anchor, void* residual, float* meta, cudaStream_t stream) {
+                          void* anchor, void* residual, float* meta, cudaStream_t stream,
+                          const Paging& pg) {
   if (s.blocks() == 0) return cudaSuccess;
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return cudaErrorNotSupported;
@@ -426,7 +427,8 @@ cudaError_t launch_encode(const void* kv, const Shape& s, const CompanderTable& 
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 #define LYNX_ENC_CASE(PP, CC) \
-  if (s.page == PP && s.C == CC) return run_encode<PP, CC>(map, s, tab, anchor, residual, meta, stream);
+  if (s.page == PP && s.C == CC)                                            \
+    return run_encode<PP, CC>(map, s, tab, anchor, residual, meta, stream, pg);
   LYNX_ENC_CASE(64, 16) LYNX_ENC_CASE(64, 32) LYNX_ENC_CASE(64, 64)
   LYNX_ENC_CASE(128, 16) LYNX_ENC_CASE(128, 32) LYNX_ENC_CASE(128, 64) LYNX_ENC_CASE(128, 128)
   LYNX_ENC_CASE(256, 16) LYNX_ENC_CASE(256, 32) LYNX_ENC_CASE(256, 64) LYNX_ENC_CASE(256, 128)

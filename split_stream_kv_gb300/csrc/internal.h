@@ -31,12 +31,21 @@ struct Shape {
   int NC() const { return page / C; }
 };
 
+// Page-block addressing of the streams: dense (no table; block (b, p, h) at
+// index (b*NB + p)*H + h) or through a block table [B][NB] of physical pages
+// in [0, nphys), each holding the H head blocks of one page.
+struct Paging {
+  const int32_t* table = nullptr;
+  int64_t nphys = 0;
+};
+
 // Launchers: validated arguments, enqueue on `stream`, return a cudaError_t.
 cudaError_t launch_encode(const void* kv, const Shape& s, const CompanderTable& tab,
-                          void* anchor, void* residual, float* meta, cudaStream_t stream);
+                          void* anchor, void* residual, float* meta, cudaStream_t stream,
+                          const Paging& pg = Paging());
 cudaError_t launch_decode(const void* anchor, const void* residual, const float* meta,
                           const Shape& s, const ExpandTable& tab, void* out, bool bf16_out,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const Paging& pg = Paging());
 cudaError_t launch_compander_selfcheck(const CompanderTable& tab, uint64_t* counts,
                                        cudaStream_t stream);
 
@@ -55,6 +64,7 @@ struct AttnArgs {
   // query token t then also attends to draft tokens 0..t
   const void* k_tail = nullptr;
   const void* v_tail = nullptr;
+  Paging paging;  // of k_* and v_* (both use the same block table)
 };
 size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L);
 cudaError_t launch_attn(const AttnArgs& a, const ExpandTable& tab, cudaStream_t stream);
@@ -65,6 +75,7 @@ int report_error(int code, const char* msg);
 // Host read of the device flag set when a bounded wait gave up.
 cudaError_t read_wait_timeout(unsigned int* flag);
 cudaError_t read_decode_wait_timeout(unsigned int* flag);
+cudaError_t read_attn_flags(unsigned int* flag);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -182,6 +182,55 @@ int lynx_expand_table(float alpha, float table[128]) {
   return LYNX_OK;
 }
 
+static int check_paging(const int32_t* block_table, int64_t num_blocks, Paging* pg) {
+  if (num_blocks < 1 || num_blocks > INT32_MAX)
+    return fail(LYNX_ESHAPE, "num_blocks = %lld: must be in [1, 2^31)", (long long)num_blocks);
+  int rc = check_ptrs({block_table});
+  if (rc) return rc;
+  pg->table = block_table;
+  pg->nphys = num_blocks;
+  return LYNX_OK;
+}
+
+int lynx_encode_paged(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page, int C,
+                      float alpha, const int32_t* block_table, int64_t num_blocks,
+                      void* anchor_pool, void* residual_pool, float* meta_pool, void* stream) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, C);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if (B * L == 0) return LYNX_OK;
+  Paging pg;
+  if ((rc = check_paging(block_table, num_blocks, &pg))) return rc;
+  if ((rc = check_ptrs({kv, anchor_pool, residual_pool, meta_pool}))) return rc;
+  Shape s{B, L, H_kv, D, page, C};
+  cudaError_t e = launch_encode(kv, s, tables_for(alpha).comp, anchor_pool, residual_pool,
+                                meta_pool, static_cast<cudaStream_t>(stream), pg);
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_encode_paged");
+}
+
+int lynx_decode_paged(const void* anchor_pool, const void* residual_pool, const float* meta_pool,
+                      const int32_t* block_table, int64_t num_blocks, int64_t B, int64_t L,
+                      int H_kv, int D, int page, int C, float alpha, int mode, void* out,
+                      int out_dtype, void* stream) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, C);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if (mode != LYNX_ANCHOR && mode != LYNX_FULL)
+    return fail(LYNX_EINVAL, "mode must be LYNX_ANCHOR or LYNX_FULL");
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)
+    return fail(LYNX_EINVAL, "out_dtype must be LYNX_OUT_BF16 or LYNX_OUT_FP32");
+  if (B * L == 0) return LYNX_OK;
+  Paging pg;
+  if ((rc = check_paging(block_table, num_blocks, &pg))) return rc;
+  if ((rc = check_ptrs({anchor_pool, meta_pool, out}))) return rc;
+  if (mode == LYNX_FULL && (rc = check_ptrs({residual_pool}))) return rc;
+  Shape s{B, L, H_kv, D, page, C};
+  cudaError_t e = launch_decode(anchor_pool, mode == LYNX_FULL ? residual_pool : nullptr,
+                                meta_pool, s, tables_for(alpha).expand, out,
+                                out_dtype == LYNX_OUT_BF16, static_cast<cudaStream_t>(stream), pg);
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_decode_paged");
+}
+
 int lynx_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page, int C,
                 float alpha, void* anchor, void* residual, float* meta, void* stream) {
   int rc = check_codec_shape(B, L, H_kv, D, page, C);
@@ -254,7 +303,7 @@ static int attn_common(const void* q, int batch, int T, int H_q, const void* k_a
                        const void* v_residual, const float* v_meta, int64_t L, int H_kv, int D,
                        int page, int C, float alpha, int mode, const void* k_tail,
                        const void* v_tail, float* out, void* workspace, size_t workspace_bytes,
-                       void* stream, const char* what) {
+                       void* stream, const char* what, const Paging& pg = Paging()) {
   int rc = check_attn_shape(batch, T, H_q, L, H_kv, D, page, C);
   if (rc) return rc;
   if ((rc = check_alpha(alpha))) return rc;
@@ -282,6 +331,7 @@ static int attn_common(const void* q, int batch, int T, int H_q, const void* k_a
   a.workspace = workspace;
   a.k_tail = k_tail;
   a.v_tail = v_tail;
+  a.paging = pg;
   cudaError_t e = launch_attn(a, tables_for(alpha).expand, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? LYNX_OK : cuda_fail(e, what);
 }
@@ -311,6 +361,35 @@ int lynx_attn_decode_tail(const void* q, int batch, int T, int H_q, const void* 
                      workspace_bytes, stream, "lynx_attn_decode_tail");
 }
 
+int lynx_attn_decode_paged(const void* q, int batch, int T, int H_q, const void* k_anchor_pool,
+                           const void* k_residual_pool, const float* k_meta_pool,
+                           const void* v_anchor_pool, const void* v_residual_pool,
+                           const float* v_meta_pool, const int32_t* block_table,
+                           int64_t num_blocks, int64_t L, int H_kv, int D, int page, int C,
+                           float alpha, int mode, const void* k_tail, const void* v_tail,
+                           float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  if ((k_tail == nullptr) != (v_tail == nullptr))
+    return fail(LYNX_EINVAL, "give both k_tail and v_tail, or neither");
+  Paging pg;
+  int rc = check_paging(block_table, num_blocks, &pg);
+  if (rc) return rc;
+  return attn_common(q, batch, T, H_q, k_anchor_pool, k_residual_pool, k_meta_pool,
+                     v_anchor_pool, v_residual_pool, v_meta_pool, L, H_kv, D, page, C, alpha,
+                     mode, k_tail, v_tail, out, workspace, workspace_bytes, stream,
+                     "lynx_attn_decode_paged", pg);
+}
+
+int lynx_device_errors(unsigned int* bits) {
+  if (!bits) return fail(LYNX_EINVAL, "null pointer");
+  unsigned int enc = 0, dec = 0, att = 0;
+  cudaError_t e = read_wait_timeout(&enc);
+  if (e == cudaSuccess) e = read_decode_wait_timeout(&dec);
+  if (e == cudaSuccess) e = read_attn_flags(&att);
+  if (e != cudaSuccess) return cuda_fail(e, "lynx_device_errors");
+  *bits = enc | dec | att;
+  return LYNX_OK;
+}
+
 int lynx_compander_selfcheck(float alpha, uint64_t* counts, void* stream) {
   int rc = check_alpha(alpha);
   if (rc) return rc;
@@ -326,7 +405,7 @@ int lynx_wait_timeouts(unsigned int* flag) {
   cudaError_t e = read_wait_timeout(&enc);
   if (e == cudaSuccess) e = read_decode_wait_timeout(&dec);
   if (e != cudaSuccess) return cuda_fail(e, "lynx_wait_timeouts");
-  *flag = (enc | dec) ? 1u : 0u;
+  *flag = ((enc | dec) & kFlagWaitTimeout) ? 1u : 0u;
   return LYNX_OK;
 }
 

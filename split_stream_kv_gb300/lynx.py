@@ -50,6 +50,11 @@ def lib() -> ctypes.CDLL:
                              I),
         "lynx_attn_decode_tail": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P, P, P,
                                    SZ, P], I),
+        "lynx_attn_decode_paged": ([P, I, I, I, P, P, P, P, P, P, P, I64, I64, I, I, I, I, F, I,
+                                    P, P, P, P, SZ, P], I),
+        "lynx_encode_paged": ([P, I64, I64, I, I, I, I, F, P, I64, P, P, P, P], I),
+        "lynx_decode_paged": ([P, P, P, P, I64, I64, I64, I, I, I, I, F, I, P, I, P], I),
+        "lynx_device_errors": ([ctypes.POINTER(ctypes.c_uint)], I),
         "lynx_attn_decode_noalloc": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P],
                                      I),
         "lynx_compander_thresholds": ([F, P], I),
@@ -155,6 +160,67 @@ def lynx_decode_full(anchor, residual, meta, L: int, page: int, C: int, alpha: f
     return out
 
 
+# ----------------------------------------------------------------- paged
+
+def paged_pool_shapes(num_blocks: int, H_kv: int, D: int, page: int, C: int):
+    """Tensor shapes of the (anchor, residual, meta) pools of num_blocks pages."""
+    codes = (num_blocks, H_kv, page, D // 2)
+    return codes, codes, (num_blocks, H_kv, 2 + 2 * (page // C), D)
+
+
+def _check_table(block_table, B, NB):
+    if block_table.dtype != torch.int32 or tuple(block_table.shape) != (B, NB):
+        raise ValueError(f"block_table must be int32 [{B}][{NB}]")
+
+
+def lynx_encode_paged(kv: torch.Tensor, page: int, C: int, alpha: float, block_table,
+                      num_blocks: int, anchor_pool=None, residual_pool=None, meta_pool=None):
+    """lynx_encode into pools of num_blocks pages through block_table [B][L/page]
+    (int32).  Returns (anchor_pool, residual_pool, meta_pool)."""
+    _need_cuda(kv, block_table, anchor_pool, residual_pool, meta_pool)
+    if kv.dtype != torch.bfloat16 or kv.dim() != 4:
+        raise ValueError("lynx_encode_paged: kv must be a 4-D bfloat16 tensor")
+    B, L, H, D = kv.shape
+    _check_table(block_table, B, L // page)
+    ca, cr, cm = paged_pool_shapes(num_blocks, H, D, page, C)
+    dev = kv.device
+    if anchor_pool is None:
+        anchor_pool = torch.empty(ca, dtype=torch.uint8, device=dev)
+    if residual_pool is None:
+        residual_pool = torch.empty(cr, dtype=torch.uint8, device=dev)
+    if meta_pool is None:
+        meta_pool = torch.empty(cm, dtype=torch.float32, device=dev)
+    _check(lib().lynx_encode_paged(_ptr(kv), B, L, H, D, page, C, alpha, _ptr(block_table),
+                                   num_blocks, _ptr(anchor_pool), _ptr(residual_pool),
+                                   _ptr(meta_pool), _stream(dev)), "lynx_encode_paged")
+    return anchor_pool, residual_pool, meta_pool
+
+
+def lynx_decode_paged(anchor_pool, residual_pool, meta_pool, block_table, L: int, page: int,
+                      C: int, alpha: float, mode: int, out_dtype=torch.bfloat16, out=None):
+    """Decode paged streams (mode LYNX_ANCHOR or LYNX_FULL) -> out[B][L][H_kv][D]."""
+    _need_cuda(anchor_pool, residual_pool, meta_pool, block_table, out)
+    num_blocks, H, P, half = anchor_pool.shape
+    B = block_table.shape[0]
+    _check_table(block_table, B, L // page)
+    if out is None:
+        out = torch.empty((B, L, H, half * 2), dtype=out_dtype, device=anchor_pool.device)
+    if out.dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("lynx decode: output must be bfloat16 or float32")
+    code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
+    _check(lib().lynx_decode_paged(_ptr(anchor_pool), _ptr(residual_pool), _ptr(meta_pool),
+                                   _ptr(block_table), num_blocks, B, L, H, half * 2, page, C,
+                                   alpha, mode, _ptr(out), code, _stream(anchor_pool.device)),
+           "lynx_decode_paged")
+    return out
+
+
+def lynx_device_errors() -> int:
+    bits = ctypes.c_uint()
+    _check(lib().lynx_device_errors(ctypes.byref(bits)), "lynx_device_errors")
+    return bits.value
+
+
 # ----------------------------------------------------------------- attention
 
 def lynx_attn_workspace_bytes(batch: int, T: int, H_q: int, L: int, H_kv: int, D: int,
@@ -213,6 +279,35 @@ def lynx_attn_decode_tail(q, k_streams, v_streams, L: int, page: int, C: int, al
         raise ValueError("lynx_attn_decode_tail: k_tail and v_tail are required")
     return lynx_attn_decode(q, k_streams, v_streams, L, page, C, alpha, mode, out=out,
                             workspace=workspace, k_tail=k_tail, v_tail=v_tail)
+
+
+def lynx_attn_decode_paged(q, k_pools, v_pools, block_table, L: int, page: int, C: int,
+                           alpha: float, mode: int, out=None, workspace=None, k_tail=None,
+                           v_tail=None):
+    """lynx_attn_decode(_tail) over paged K and V pools (anchor, residual or None,
+    meta) read through block_table [batch][L/page] (int32)."""
+    ka, kr, km = k_pools
+    va, vr, vm = v_pools
+    _need_cuda(q, ka, kr, km, va, vr, vm, block_table, out, workspace, k_tail, v_tail)
+    if (k_tail is None) != (v_tail is None):
+        raise ValueError("lynx_attn_decode_paged: give both k_tail and v_tail, or neither")
+    if q.dtype != torch.bfloat16 or q.dim() != 4:
+        raise ValueError("lynx_attn_decode_paged: q must be a 4-D bfloat16 tensor")
+    batch, T, H_q, D = q.shape
+    num_blocks, H_kv = ka.shape[0], ka.shape[1]
+    _check_table(block_table, batch, L // page)
+    if out is None:
+        out = torch.empty((batch, T, H_q, D), dtype=torch.float32, device=q.device)
+    need = lynx_attn_workspace_bytes(batch, T, H_q, L, H_kv, D, page)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().lynx_attn_decode_paged(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr), _ptr(km),
+                                        _ptr(va), _ptr(vr), _ptr(vm), _ptr(block_table),
+                                        num_blocks, L, H_kv, D, page, C, alpha, mode,
+                                        _ptr(k_tail), _ptr(v_tail), _ptr(out), _ptr(workspace),
+                                        workspace.numel(), _stream(q.device)),
+           "lynx_attn_decode_paged")
+    return out
 
 
 def lynx_attn_decode_noalloc(q, k_streams, v_streams, L: int, page: int, C: int,
