@@ -262,7 +262,7 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t a, uint32_t r, uint32_
   return f2_to_bf2(x.x, x.y);
 }
 
-template <bool FULL, int NT, bool PAIR, bool ONE>
+template <bool FULL, int NT, bool PAIR, bool ONE, bool PAGED>
 __global__ void __launch_bounds__(Cfg<FULL, PAIR, ONE>::kWarps * 32, 2)
 attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ ExpandTable tab) {
   using CF = Cfg<FULL, PAIR, ONE>;
@@ -339,10 +339,17 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       reinterpret_cast<uint2*>(extra)[i] = q_frag(sg, hf, kt, nt, ln >> 2, ln & 3);
     }
   }
-  if (tid < 2) {  // [0..1]: first page row (b * NB) of each segment, [2..3]: its KV head
+  if (tid < 2) {
+    // dense: [0..1] block index of page 0 of each segment, (b*NB)*Hkv + h;
+    // paged: [0..1] first table row b*NB of each segment, [2..3] its KV head
     int64_t* info = reinterpret_cast<int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo);
-    info[tid] = (int64_t)(tid ? b1 : b0) * a.NB;
-    info[2 + tid] = tid ? h1 : h0;
+    const int64_t row = (int64_t)(tid ? b1 : b0) * a.NB, hh = tid ? h1 : h0;
+    if constexpr (PAGED) {
+      info[tid] = row;
+      info[2 + tid] = hh;
+    } else {
+      info[tid] = row * a.Hkv + hh;
+    }
   }
   __syncthreads();
   const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 8u;
@@ -360,16 +367,16 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     const int t0 = qc * 32;
     const int p = t0 >> a.lgP;
     tp = t0 & (a.P - 1);
-    const int64_t row = seg_blk[sg] + p;
-    int64_t pg = row;
-    if (a.bt) {  // paged streams: the table names the physical page
-      pg = __ldg(a.bt + row);
+    if constexpr (PAGED) {  // the table names the physical page
+      int64_t pg = __ldg(a.bt + seg_blk[sg] + p);
       if (pg < 0 || pg >= a.nphys) {
         atomicOr(&g_attn_flags, kFlagBadBlock);
         pg = 0;
       }
+      return pg * a.Hkv + seg_blk[2 + sg];
+    } else {
+      return seg_blk[sg] + p * a.Hkv;
     }
-    return pg * a.Hkv + seg_blk[2 + sg];
   };
   // Asynchronous copies of the constant rows of chunk qc into the warp's
   // rows of one tensor (gamma rows only with_gamma).  Each copy instruction
@@ -954,9 +961,9 @@ size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L) {
   return (size_t)3 * n * (2 * RP + RP * kD) * sizeof(float);
 }
 
-template <bool FULL, int NT, bool PAIR, bool ONE>
+template <bool FULL, int NT, bool PAIR, bool ONE, bool PAGED>
 static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
-  auto fn = attn_kernel<FULL, NT, PAIR, ONE>;
+  auto fn = attn_kernel<FULL, NT, PAIR, ONE, PAGED>;
   constexpr size_t smem = attn_smem_bytes<FULL, PAIR, ONE, NT>();
   constexpr int threads = Cfg<FULL, PAIR, ONE>::kWarps * 32;
   static thread_local int configured_dev = -1;
@@ -987,8 +994,11 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
 
 template <bool FULL, int NT, bool PAIR>
 static cudaError_t run_attn_c(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
-  return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true>(prm, tab, stream)
-                     : run_attn<FULL, NT, PAIR, false>(prm, tab, stream);
+  if (prm.bt)
+    return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true, true>(prm, tab, stream)
+                       : run_attn<FULL, NT, PAIR, false, true>(prm, tab, stream);
+  return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true, false>(prm, tab, stream)
+                     : run_attn<FULL, NT, PAIR, false, false>(prm, tab, stream);
 }
 
 cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t stream) {
