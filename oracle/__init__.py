@@ -78,6 +78,10 @@ def _bind(lib):
     lib.oracle_attention_row.restype = None
     lib.oracle_attention_row_tail.argtypes = [P, P, P, I64, P, P, I, I, I64, I64, P]
     lib.oracle_attention_row_tail.restype = None
+    lib.oracle_spec_verify.argtypes = [P, P, P, P, ctypes.c_uint32, I, I64, P]
+    lib.oracle_spec_verify.restype = I
+    lib.oracle_spec_verify_batch.argtypes = [P, P, P, P, P, I, I, I64, P, P]
+    lib.oracle_spec_verify_batch.restype = None
     return lib
 
 
@@ -328,6 +332,28 @@ def attention_row_tail(q: np.ndarray, K: np.ndarray, V: np.ndarray, Kt: np.ndarr
     _load().oracle_attention_row_tail(_ptr(q), _ptr(K), _ptr(V), L, _ptr(Kt), _ptr(Vt),
                                       n_tail, D, D, D, _ptr(out))
     return out
+
+
+def spec_verify(p: np.ndarray, q: np.ndarray, s: np.ndarray, u: np.ndarray,
+                r: np.ndarray):
+    """Speculative verification and correction [Review, Mechanism 3, Eq. 10,
+    Eq. 11] for a batch: p [batch][T+1][V], q [batch][T][V] float32
+    distributions, s [batch][T] draft tokens, u [batch][T] uniforms, r [batch]
+    uint32.  Returns (n_accepted [batch], next_token [batch]) as int32."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    s = np.ascontiguousarray(s, dtype=np.int32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    r = np.ascontiguousarray(r, dtype=np.uint32)
+    batch, T1, V = p.shape
+    T = T1 - 1
+    if q.shape != (batch, T, V) or s.shape != (batch, T) or u.shape != (batch, T):
+        raise ValueError("spec_verify: shapes")
+    k = np.empty(batch, np.int32)
+    tok = np.empty(batch, np.int32)
+    _load().oracle_spec_verify_batch(_ptr(p), _ptr(q), _ptr(s), _ptr(u), _ptr(r), batch, T, V,
+                                     _ptr(k), _ptr(tok))
+    return k, tok
 
 
 # ------------------------------------------------------------ size formulas

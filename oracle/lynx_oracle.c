@@ -418,3 +418,77 @@ void oracle_attention_row_tail(const float *q, const float *K, const float *V,
     for (int d = 0; d < D; ++d) out[d] /= l;
     free(s);
 }
+
+/* ---------------------------------------------------------------- Eq. 10-11
+ * Speculative verification and correction [Review, Mechanism 3, Eq. 10 and
+ * Eq. 11], the draft-then-verify rule the pages adapt from Chen et al. 2023,
+ * for one sequence:
+ *   p  [T+1][V]  target distributions p(. | s_<t, Q_full), t = 1..T+1
+ *   q  [T][V]    draft distributions p(. | s_<t, Q_approx), t = 1..T
+ *   s  [T]       draft tokens, u [T] uniforms in [0, 1), r a uniform uint32.
+ * Draft token s_t is accepted with probability min(1, p_t(s_t) / q_t(s_t))
+ * (Eq. 10): with u_t uniform that is u_t * q_t(s_t) < p_t(s_t), one float32
+ * product and compare.  k = the length of the accepted prefix.  At the first
+ * rejected position k+1 the next token is drawn from
+ * p'(x) ∝ max(0, p_{k+1}(x) - q_{k+1}(x)) (Eq. 11); when every draft token is
+ * accepted it is drawn from p_{T+1} (the verification pass's next-token
+ * distribution).  The draw is an inverse CDF over integer weights
+ * W(x) = floor(w(x) * 2^40) (w the float32 weight), target floor(r * Z / 2^32)
+ * with Z = sum W: the smallest x whose running sum of W exceeds the target.
+ * If Z = 0 the weights of p at that position are used instead; if those sum
+ * to 0 too, the token is -1.  Returns k; *token receives the drawn token. */
+static uint64_t spec_weight(float w)
+{
+    return w > 0.0f ? (uint64_t)(w * 1099511627776.0f) : 0u;
+}
+
+/* float32 weight of token x: max(0, p - q) (Eq. 11) with a draft
+ * distribution, p itself without one */
+static float spec_w(const float *pk, const float *qk, int64_t x)
+{
+    return qk ? fmaxf(pk[x] - qk[x], 0.0f) : pk[x];
+}
+
+int oracle_spec_verify(const float *p, const float *q, const int32_t *s,
+                       const float *u, uint32_t r, int T, int64_t V,
+                       int32_t *token)
+{
+    int k = 0;
+    while (k < T) {
+        int64_t x = s[k];
+        float pv = p[(int64_t)k * V + x], qv = q[(int64_t)k * V + x];
+        if (!(u[k] * qv < pv)) break;
+        ++k;
+    }
+    const float *pk = p + (int64_t)k * V;
+    const float *qk = k < T ? q + (int64_t)k * V : NULL;
+    for (int pass = 0; pass < 2; ++pass) {
+        const float *qw = pass == 0 ? qk : NULL;
+        uint64_t Z = 0;
+        for (int64_t x = 0; x < V; ++x)
+            Z += spec_weight(spec_w(pk, qw, x));
+        if (Z == 0) continue;
+        uint64_t target = (uint64_t)(((unsigned __int128)r * Z) >> 32);
+        uint64_t run = 0;
+        for (int64_t x = 0; x < V; ++x) {
+            run += spec_weight(spec_w(pk, qw, x));
+            if (run > target) {
+                *token = (int32_t)x;
+                return k;
+            }
+        }
+    }
+    *token = -1;
+    return k;
+}
+
+/* oracle_spec_verify for each of `batch` sequences (arrays batch-major). */
+void oracle_spec_verify_batch(const float *p, const float *q, const int32_t *s,
+                              const float *u, const uint32_t *r, int batch, int T,
+                              int64_t V, int32_t *k, int32_t *token)
+{
+    for (int b = 0; b < batch; ++b)
+        k[b] = oracle_spec_verify(p + (int64_t)b * (T + 1) * V, q + (int64_t)b * T * V,
+                                  s + (int64_t)b * T, u + (int64_t)b * T, r[b], T, V,
+                                  token + b);
+}

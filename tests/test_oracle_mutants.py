@@ -50,6 +50,12 @@ MUTANTS = [
     ("attention not normalised", "for (int d = 0; d < D; ++d) out[d] /= l;\n    free(s);\n}\n\n/* One query row",
      "for (int d = 0; d < D; ++d) out[d] /= 1.0;\n    free(s);\n}\n\n/* One query row"),
     ("verification row ignores the draft tokens", "int64_t n = L + n_tail;", "int64_t n = L;"),
+    ("acceptance ratio inverted (q/p)", "if (!(u[k] * qv < pv)) break;",
+     "if (!(u[k] * pv < qv)) break;"),
+    ("correction from max(0, q - p)", "return qk ? fmaxf(pk[x] - qk[x], 0.0f) : pk[x];",
+     "return qk ? fmaxf(qk[x] - pk[x], 0.0f) : pk[x];"),
+    ("no bonus token: the last draft distribution is reused",
+     "const float *pk = p + (int64_t)k * V;", "const float *pk = p + (int64_t)(k < T ? k : T - 1) * V;"),
     ("draft tokens take the cached values",
      "const float *v = t < L ? V + t * kv_stride : Vt + (t - L) * tail_stride;",
      "const float *v = t < L ? V + t * kv_stride : V + (t - L) * kv_stride;"),

@@ -508,6 +508,68 @@ def test_attention_tail_hand_weights(oracle_mod):
     assert np.allclose(out, 0.25 * 4.0 + 0.75 * 8.0, atol=1e-6)
 
 
+# ---------------------------------------------------- Eq. 10-11 (Mechanism 3)
+
+def _one(oracle_mod, p, q, s, u, r):
+    k, tok = oracle_mod.spec_verify(np.array([p], np.float32), np.array([q], np.float32),
+                                    np.array([s], np.int32), np.array([u], np.float32),
+                                    np.array([r], np.uint32))
+    return int(k[0]), int(tok[0])
+
+
+def test_spec_inverse_cdf_on_exact_weights(oracle_mod):
+    """Every draft token accepted (p = q), so the next token comes from
+    p_{T+1} = (1/8, 3/8, 0, 1/2): r = j * 2^29 lands on the j/8 quantile."""
+    same = [0.25, 0.25, 0.25, 0.25]
+    last = [0.125, 0.375, 0.0, 0.5]
+    got = [_one(oracle_mod, [same, last], [same], [2], [0.999], j << 29) for j in range(8)]
+    assert got == [(1, t) for t in (0, 1, 1, 1, 3, 3, 3, 3)]
+
+
+def test_spec_accept_rule(oracle_mod):
+    """Eq. 10: accepted iff u < p(s)/q(s), decided as u*q < p in float32."""
+    p = [0.2, 0.8]
+    nxt = [1.0, 0.0]
+    assert _one(oracle_mod, [p, nxt], [[0.4, 0.6]], [0], [0.5], 0)[0] == 0   # 0.5*0.4 = 0.2
+    p_up = [float(np.nextafter(np.float32(0.2), np.float32(1))), 0.8]
+    assert _one(oracle_mod, [p_up, nxt], [[0.4, 0.6]], [0], [0.5], 0)[0] == 1
+    assert _one(oracle_mod, [[0.0, 1.0], nxt], [[0.5, 0.5]], [0], [0.0], 0)[0] == 0
+    assert _one(oracle_mod, [[0.3, 0.7], nxt], [[0.3, 0.7]], [1], [0.99999994], 0)[0] == 1
+
+
+def test_spec_correction_is_the_positive_part(oracle_mod):
+    """Eq. 11: after a rejection only tokens with p > q can be drawn, with
+    weight p - q."""
+    p, q = [0.5, 0.5, 0.0, 0.0], [0.25, 0.75, 0.0, 0.0]
+    for r in (0, 1 << 31, (1 << 32) - 1):
+        assert _one(oracle_mod, [p, p], [q], [1], [0.9], r) == (0, 0)
+
+
+def test_spec_output_follows_the_target_distribution(oracle_mod):
+    """Losslessness (Mechanism 3): with drafts drawn from q, the emitted tokens
+    follow p.  Two draft positions with independent distributions: the first
+    emitted token ~ p_1, and the second (whenever the first draft was kept)
+    ~ p_2.  200,000 seeded sequences, every frequency within 5 sigma."""
+    rng = np.random.default_rng(12)
+    V, T, N = 6, 2, 200_000
+    p = rng.dirichlet(np.ones(V), size=T + 1).astype(np.float32)
+    q = rng.dirichlet(np.ones(V), size=T).astype(np.float32)
+    s = np.stack([rng.choice(V, size=N, p=q[t] / q[t].sum()) for t in range(T)], axis=1)
+    u = rng.random((N, T), dtype=np.float32)
+    r = rng.integers(0, 2 ** 32, size=N, dtype=np.uint64).astype(np.uint32)
+    k, tok = oracle_mod.spec_verify(np.broadcast_to(p, (N, T + 1, V)),
+                                    np.broadcast_to(q, (N, T, V)), s, u, r)
+    first = np.where(k >= 1, s[:, 0], tok)
+    kept = k >= 1
+    second = np.where(k[kept] >= 2, s[kept, 1], tok[kept])
+    for emitted, target in ((first, p[0]), (second, p[1])):
+        n = emitted.size
+        freq = np.bincount(emitted, minlength=V) / n
+        pt = target.astype(np.float64) / target.sum()
+        sigma = np.sqrt(pt * (1 - pt) / n)
+        assert np.all(np.abs(freq - pt) <= 5 * sigma + 1e-12), (freq, pt)
+
+
 # ----------------------------------------------------------- size formulas
 
 def test_kv_size_example(oracle_mod):
