@@ -137,10 +137,36 @@ int lynx_decode_paged(const void *anchor_pool, const void *residual_pool,
                       int page, int C, float alpha, int mode, void *out,
                       int out_dtype, void *stream);
 
+/* Speculative verification and correction [Review, Mechanism 3, Eq. 10 and
+ * Eq. 11], for every sequence b of the batch, on distributions the caller's
+ * verification pass (p, over the full KV) and draft steps (q, over the
+ * Anchor-only KV) produced:
+ *   p_target      [batch][T+1][V] float32, p(. | s_<t, Q_full), t = 1..T+1
+ *   q_draft       [batch][T][V] float32, p(. | s_<t, Q_approx), t = 1..T
+ *   draft_tokens  [batch][T] int32, s_1..s_T
+ *   u_accept      [batch][T] float32 uniforms in [0, 1)
+ *   r_sample      [batch] uint32 uniforms
+ *   n_accepted    [batch] int32, written: k, the accepted prefix length
+ *   next_token    [batch] int32, written: the token that follows s_k
+ * s_t is accepted iff u_t * q_t(s_t) < p_t(s_t) (float32; i.e. with
+ * probability min(1, p/q)) and every earlier one was.  The next token is
+ * drawn from max(0, p_{k+1} - q_{k+1}) after a rejection, or from p_{T+1}
+ * after a fully accepted draft, by inverse CDF over the integer weights
+ * floor(w * 2^40) with target floor(r * Z / 2^32), Z their sum; if Z = 0 the
+ * weights of p are used, and if they sum to 0 too the token is -1.  A draft
+ * token outside [0, V) counts as rejected and is reported by
+ * lynx_device_errors (bit 4).  1 <= T <= 64, 1 <= V < 2^31; all device
+ * pointers, 16-byte aligned.  One CTA per sequence, enqueued on `stream`. */
+int lynx_spec_verify(const float *p_target, const float *q_draft,
+                     const int32_t *draft_tokens, const float *u_accept,
+                     const uint32_t *r_sample, int batch, int T, int64_t V,
+                     int32_t *n_accepted, int32_t *next_token, void *stream);
+
 /* Host call, synchronous: *bits = OR of the conditions any kernel of this
  * library in this process has reported: 1 = a bounded wait on an
  * asynchronous copy gave up (the kernel returned early, its outputs are
- * incomplete), 2 = a block-table entry was outside [0, num_blocks). */
+ * incomplete), 2 = a block-table entry was outside [0, num_blocks), 4 = a
+ * draft token of lynx_spec_verify was outside [0, V). */
 int lynx_device_errors(unsigned int *bits);
 
 /* Host-only.  Device workspace (bytes) that lynx_attn_decode needs for these

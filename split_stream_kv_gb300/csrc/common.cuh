@@ -98,6 +98,7 @@ __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
 // Bits of the per-file device flag words (read through lynx_device_errors).
 constexpr unsigned kFlagWaitTimeout = 1u;   // a bounded wait gave up
 constexpr unsigned kFlagBadBlock = 2u;      // a block-table entry was out of range
+constexpr unsigned kFlagBadToken = 4u;      // a draft token was outside the vocabulary
 
 // Physical page block of logical block blk = (b*NB + p)*H + h.  Without a
 // block table the streams are dense and the two coincide; with one, row

@@ -76,6 +76,10 @@ int report_error(int code, const char* msg);
 cudaError_t read_wait_timeout(unsigned int* flag);
 cudaError_t read_decode_wait_timeout(unsigned int* flag);
 cudaError_t read_attn_flags(unsigned int* flag);
+cudaError_t read_spec_flags(unsigned int* flag);
+cudaError_t launch_spec_verify(const float* p, const float* q, const int32_t* s, const float* u,
+                               const uint32_t* r, int batch, int T, int64_t V, int32_t* n_acc,
+                               int32_t* next_tok, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -381,13 +381,28 @@ int lynx_attn_decode_paged(const void* q, int batch, int T, int H_q, const void*
 
 int lynx_device_errors(unsigned int* bits) {
   if (!bits) return fail(LYNX_EINVAL, "null pointer");
-  unsigned int enc = 0, dec = 0, att = 0;
+  unsigned int enc = 0, dec = 0, att = 0, spc = 0;
   cudaError_t e = read_wait_timeout(&enc);
   if (e == cudaSuccess) e = read_decode_wait_timeout(&dec);
   if (e == cudaSuccess) e = read_attn_flags(&att);
+  if (e == cudaSuccess) e = read_spec_flags(&spc);
   if (e != cudaSuccess) return cuda_fail(e, "lynx_device_errors");
-  *bits = enc | dec | att;
+  *bits = enc | dec | att | spc;
   return LYNX_OK;
+}
+
+int lynx_spec_verify(const float* p_target, const float* q_draft, const int32_t* draft_tokens,
+                     const float* u_accept, const uint32_t* r_sample, int batch, int T,
+                     int64_t V, int32_t* n_accepted, int32_t* next_token, void* stream) {
+  if (batch < 0) return fail(LYNX_ESHAPE, "batch = %d < 0", batch);
+  if (T < 1 || T > 64) return fail(LYNX_EUNSUPPORTED, "T = %d: 1..64 draft tokens", T);
+  if (V < 1 || V > INT32_MAX) return fail(LYNX_ESHAPE, "V = %lld: must be in [1, 2^31)", (long long)V);
+  if (batch == 0) return LYNX_OK;
+  int rc = check_ptrs({p_target, q_draft, draft_tokens, u_accept, r_sample, n_accepted, next_token});
+  if (rc) return rc;
+  cudaError_t e = launch_spec_verify(p_target, q_draft, draft_tokens, u_accept, r_sample, batch, T,
+                                     V, n_accepted, next_token, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_spec_verify");
 }
 
 int lynx_compander_selfcheck(float alpha, uint64_t* counts, void* stream) {

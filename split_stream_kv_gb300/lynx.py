@@ -55,6 +55,7 @@ def lib() -> ctypes.CDLL:
         "lynx_encode_paged": ([P, I64, I64, I, I, I, I, F, P, I64, P, P, P, P], I),
         "lynx_decode_paged": ([P, P, P, P, I64, I64, I64, I, I, I, I, F, I, P, I, P], I),
         "lynx_device_errors": ([ctypes.POINTER(ctypes.c_uint)], I),
+        "lynx_spec_verify": ([P, P, P, P, P, I, I, I64, P, P, P], I),
         "lynx_attn_decode_noalloc": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P],
                                      I),
         "lynx_compander_thresholds": ([F, P], I),
@@ -213,6 +214,30 @@ def lynx_decode_paged(anchor_pool, residual_pool, meta_pool, block_table, L: int
                                    alpha, mode, _ptr(out), code, _stream(anchor_pool.device)),
            "lynx_decode_paged")
     return out
+
+
+def lynx_spec_verify(p, q, draft_tokens, u, r, n_accepted=None, next_token=None):
+    """Eq. 10-11 for a batch: p [batch][T+1][V] f32, q [batch][T][V] f32,
+    draft_tokens [batch][T] int32, u [batch][T] f32, r [batch] int32 holding
+    uint32 bits.  Returns (n_accepted, next_token), int32 [batch]."""
+    _need_cuda(p, q, draft_tokens, u, r, n_accepted, next_token)
+    batch, T1, V = p.shape
+    T = T1 - 1
+    if p.dtype != torch.float32 or q.dtype != torch.float32 or u.dtype != torch.float32:
+        raise ValueError("lynx_spec_verify: p, q and u must be float32")
+    if draft_tokens.dtype != torch.int32 or r.dtype != torch.int32:
+        raise ValueError("lynx_spec_verify: draft_tokens and r must be int32 tensors")
+    if tuple(q.shape) != (batch, T, V) or tuple(draft_tokens.shape) != (batch, T) or \
+            tuple(u.shape) != (batch, T) or tuple(r.shape) != (batch,):
+        raise ValueError("lynx_spec_verify: shapes")
+    if n_accepted is None:
+        n_accepted = torch.empty(batch, dtype=torch.int32, device=p.device)
+    if next_token is None:
+        next_token = torch.empty(batch, dtype=torch.int32, device=p.device)
+    _check(lib().lynx_spec_verify(_ptr(p), _ptr(q), _ptr(draft_tokens), _ptr(u), _ptr(r), batch,
+                                  T, V, _ptr(n_accepted), _ptr(next_token), _stream(p.device)),
+           "lynx_spec_verify")
+    return n_accepted, next_token
 
 
 def lynx_device_errors() -> int:

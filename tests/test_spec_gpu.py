@@ -1,0 +1,58 @@
+"""Speculative verification and correction (Eq. 10-11) through the C ABI,
+bit-exact against the oracle: the accepted prefix length and the next token
+of every sequence."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(batch, T, V, temp, seed, same=False):
+    """Target and draft distributions that agree more or less (temp scales the
+    draft's perturbation), drafts drawn from q, seeded uniforms."""
+    rng = np.random.default_rng(seed)
+    logits = rng.standard_normal((batch, T + 1, V)).astype(np.float32) * 3.0
+    p = np.exp(logits - logits.max(axis=-1, keepdims=True))
+    p = (p / p.sum(axis=-1, keepdims=True)).astype(np.float32)
+    if same:
+        q = p[:, :T].copy()
+    else:
+        ql = logits[:, :T] + temp * rng.standard_normal((batch, T, V)).astype(np.float32)
+        q = np.exp(ql - ql.max(axis=-1, keepdims=True))
+        q = (q / q.sum(axis=-1, keepdims=True)).astype(np.float32)
+    s = np.empty((batch, T), np.int32)
+    for b in range(batch):
+        for t in range(T):
+            qq = q[b, t].astype(np.float64)
+            s[b, t] = rng.choice(V, p=qq / qq.sum())
+    u = rng.random((batch, T), dtype=np.float32)
+    r = rng.integers(0, 2 ** 32, size=batch, dtype=np.uint64).astype(np.uint32)
+    return p, q, s, u, r
+
+
+def _check(lynx_lib, oracle_mod, dev, p, q, s, u, r):
+    kt, tt = lynx_lib.lynx_spec_verify(
+        torch.from_numpy(p).to(dev), torch.from_numpy(q).to(dev), torch.from_numpy(s).to(dev),
+        torch.from_numpy(u).to(dev), torch.from_numpy(r.view(np.int32)).to(dev))
+    torch.cuda.synchronize()
+    ko, to = oracle_mod.spec_verify(p, q, s, u, r)
+    assert np.array_equal(kt.cpu().numpy(), ko), (kt.cpu().numpy(), ko)
+    assert np.array_equal(tt.cpu().numpy(), to), (tt.cpu().numpy(), to)
+    return ko
+
+
+@pytest.mark.parametrize("batch,T,V,temp", [(16, 8, 1000, 0.3), (8, 8, 128003, 0.05),
+                                            (4, 64, 5000, 0.02), (32, 1, 77, 1.0)])
+def test_spec_verify_matches_oracle(lynx_lib, oracle_mod, cuda_dev, batch, T, V, temp):
+    ko = _check(lynx_lib, oracle_mod, cuda_dev, *_inputs(batch, T, V, temp, seed=V + T))
+    print("accepted", ko)
+
+
+def test_spec_verify_full_acceptance_draws_the_bonus_token(lynx_lib, oracle_mod, cuda_dev):
+    """q = p on every position: the whole draft is kept and the next token is
+    drawn from p_{T+1}."""
+    p, q, s, u, r = _inputs(8, 5, 3000, 0.0, seed=1, same=True)
+    ko = _check(lynx_lib, oracle_mod, cuda_dev, p, q, s, u, r)
+    assert np.all(ko == 5)
+    assert lynx_lib.lynx_device_errors() & 4 == 0
