@@ -462,9 +462,93 @@ def run_lynx(args, rank, world, dev):
     e2e_s = (time.perf_counter() - w0) / e2e_steps
 
     ms_total, e2e_s = max_over_ranks([ms_total, e2e_s], world, dev)
+    extras = measure_extras(ks, vs, q8, ws, dev) if rank == 0 else None
     assert lynx.lynx_wait_timeouts() == 0
     return dict(ms_total=ms_total, row_ms=row_ms, e2e_s=e2e_s, h2d=h2d, d2h=d2h, clocks=clk,
-                launches=launches)
+                launches=launches, extras=extras)
+
+
+def measure_extras(ks, vs, q8, ws, dev, reps=10):
+    """Capabilities beyond the headline step, timed on their own with CUDA
+    events (3 warm-up calls; an L2 flush between timed calls): verification
+    with the draft tokens' own keys and values, verification over paged
+    streams through a scattered block table, and speculative verification
+    (Eq. 10-11) over a 128,256-token vocabulary."""
+    import torch
+
+    from split_stream_kv_gb300 import lynx, synth
+    a = ATTN
+    peak, _ = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ms = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms += e0.elapsed_time(e1)
+        return ms / reps
+
+    def entry(ms, nbytes, **kw):
+        ach = nbytes / (ms / 1e3) / 1e9
+        return dict(ms=round(ms, 4), algorithmic_bytes=int(nbytes), achieved_GBps=round(ach, 1),
+                    roofline_frac=round(ach / peak, 4), **kw)
+
+    out = {}
+    verify_bytes = algorithmic_bytes()["attn_verify"]
+    T = a["T_verify"]
+    tail = synth.kv_cache(2 * a["batch"], T, a["H_kv"], a["D"], seed=77, device=dev)
+    kt, vt = tail[0::2].contiguous(), tail[1::2].contiguous()
+    o8 = torch.empty((a["batch"], T, a["H_q"], a["D"]), device=dev)
+    ms = timed(lambda: lynx.lynx_attn_decode(q8, ks, vs, a["L"], a["P"], a["C"], ALPHA,
+                                             lynx.LYNX_FULL, out=o8, workspace=ws, k_tail=kt,
+                                             v_tail=vt))
+    out["attn_verify_tail"] = entry(ms, verify_bytes + 2 * kt.nbytes,
+                                    what=f"T={T} verification with the draft tokens' own BF16 "
+                                         "keys and values (causal)")
+    NB = a["L"] // a["P"]
+    nblocks = a["batch"] * NB + 64
+    g = torch.Generator().manual_seed(5)
+    table = torch.randperm(nblocks, generator=g)[: a["batch"] * NB].view(a["batch"], NB)
+    table = table.to(torch.int32).to(dev)
+    idx = table.view(-1).long()
+
+    def pool(t):  # dense [batch][NB][H][...] -> pool [nblocks][H][...] scattered by the table
+        p = torch.zeros((nblocks,) + tuple(t.shape[2:]), dtype=t.dtype, device=dev)
+        p[idx] = t.reshape((-1,) + tuple(t.shape[2:]))
+        return p
+    kp = tuple(pool(t) for t in ks)
+    vp = tuple(pool(t) for t in vs)
+    ms = timed(lambda: lynx.lynx_attn_decode_paged(q8, kp, vp, table, a["L"], a["P"], a["C"],
+                                                   ALPHA, lynx.LYNX_FULL, out=o8, workspace=ws))
+    out["attn_verify_paged"] = entry(ms, verify_bytes + table.nbytes,
+                                     what=f"T={T} verification over paged streams, "
+                                          f"{nblocks} physical pages behind a scattered table")
+    del kp, vp
+    V, B = 128256, a["batch"]
+    gen = torch.Generator(device=dev).manual_seed(3)
+    logits = torch.randn((B, T + 1, V), generator=gen, device=dev) * 3.0
+    p = torch.softmax(logits, dim=-1)
+    q = torch.softmax(logits[:, :T] + 0.05 * torch.randn((B, T, V), generator=gen, device=dev),
+                      dim=-1)
+    s = torch.multinomial(q.reshape(-1, V), 1, generator=gen).view(B, T).to(torch.int32)
+    u = torch.rand((B, T), generator=gen, device=dev)
+    r = torch.randint(-2 ** 31, 2 ** 31 - 1, (B,), generator=gen, device=dev, dtype=torch.int32)
+    ms = timed(lambda: lynx.lynx_spec_verify(p, q, s, u, r))
+    k, _ = lynx.lynx_spec_verify(p, q, s, u, r)
+    # a sequence that rejects at k reads the rows p_k and q_k; one that accepts
+    # every draft token reads p_{T+1} alone
+    rows_read = int((k < T).sum()) * 2 + int((k == T).sum())
+    out["spec_verify"] = entry(ms, rows_read * V * 4,
+                               what=f"Eq. 10-11: batch {B}, T={T}, V={V}; mean accepted "
+                                    f"{float(k.float().mean()):.2f} of {T}")
+    return out
 
 
 def main():
@@ -554,6 +638,8 @@ def main():
             "gpu_launches": r["launches"],
             "clocks": r["clocks"],
         }
+        if r.get("extras"):
+            line["extras"] = r["extras"]
         if args.small:
             line["config"]["workload"] = "SMALL profiling case: " + line["config"]["workload"]
             line["config"]["small"] = {"codec_B": CODEC["B"], "attn_batch": ATTN["batch"]}

@@ -363,17 +363,31 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   // Packed block (sequence, page, KV head) of chunk qc of segment sg.
   const int64_t* seg_blk =
       reinterpret_cast<const int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo);
+  // Paged streams: a two-entry cache of (table row -> page) per lane.  Chunks
+  // walk pages in order and the L2 prefetch two chunks ahead meets each new
+  // page first, so the loads that need a chunk's address rarely wait on the
+  // table.
+  int64_t c_row0 = -1, c_pg0 = 0, c_row1 = -1, c_pg1 = 0;
+  auto page_of = [&](int64_t row) -> int64_t {
+    if (row == c_row1) return c_pg1;
+    if (row == c_row0) return c_pg0;
+    int64_t pg = __ldg(a.bt + row);
+    if (pg < 0 || pg >= a.nphys) {
+      atomicOr(&g_attn_flags, kFlagBadBlock);
+      pg = 0;
+    }
+    c_row0 = c_row1;
+    c_pg0 = c_pg1;
+    c_row1 = row;
+    c_pg1 = pg;
+    return pg;
+  };
   auto chunk_blk = [&](int sg, int qc, int& tp) -> int64_t {
     const int t0 = qc * 32;
     const int p = t0 >> a.lgP;
     tp = t0 & (a.P - 1);
     if constexpr (PAGED) {  // the table names the physical page
-      int64_t pg = __ldg(a.bt + seg_blk[sg] + p);
-      if (pg < 0 || pg >= a.nphys) {
-        atomicOr(&g_attn_flags, kFlagBadBlock);
-        pg = 0;
-      }
-      return pg * a.Hkv + seg_blk[2 + sg];
+      return page_of(seg_blk[sg] + p) * a.Hkv + seg_blk[2 + sg];
     } else {
       return seg_blk[sg] + p * a.Hkv;
     }

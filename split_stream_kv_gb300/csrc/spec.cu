@@ -1,6 +1,6 @@
 // spec.cu -- speculative verification and correction of "Lynx: Progressive
 // Speculative KV Cache Transfer for Disaggregated LLM Inference" (technical
-// review, Mechanism 3, Eq. 10 and Eq. 11), one CTA per sequence.
+// review, Mechanism 3, Eq. 10 and Eq. 11), one cluster of CTAs per sequence.
 //
 // Draft token s_t (t = 1..T) is accepted with probability min(1, p_t(s_t) /
 // q_t(s_t)) (Eq. 10), tested as u_t * q_t(s_t) < p_t(s_t) in float32; the
@@ -11,16 +11,22 @@
 // Z = sum W: the smallest x whose running sum exceeds the target.  Integer
 // sums make the token independent of the summation order.
 //
-// The 32 warps of the CTA each own a contiguous segment of the vocabulary:
-// one coalesced pass gives the segment totals; the warp whose segment holds
-// the target rescans it 32 tokens at a time with a warp-wide prefix sum.
+// A cluster of CTAs per sequence: every warp owns a contiguous segment of the
+// vocabulary; one coalesced pass gives the segment totals, shared through
+// distributed shared memory; the warp whose segment holds the target rescans
+// it 32 tokens at a time with a warp-wide prefix sum.
 #include "common.cuh"
 #include "internal.h"
 
 namespace lynx {
 
-constexpr int kSpecThreads = 1024;
+// A sequence is one cluster of kSpecCtas CTAs (thread-block cluster with
+// distributed shared memory); CTA c owns vocabulary slice c, each of its
+// warps a contiguous segment of the slice.
+constexpr int kSpecCtas = 8;
+constexpr int kSpecThreads = 512;
 constexpr int kSpecWarps = kSpecThreads / 32;
+constexpr int kSpecSegs = kSpecCtas * kSpecWarps;  // segments of the vocabulary
 
 // Set when a draft token lay outside [0, V) (treated as rejected); read
 // through read_spec_flags(), never reset.
@@ -34,17 +40,38 @@ __device__ __forceinline__ uint64_t spec_weight(float w) {
   return w > 0.0f ? __float2ull_rz(w * 1099511627776.0f) : 0ull;  // floor(w * 2^40)
 }
 
-__global__ void __launch_bounds__(kSpecThreads)
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Read a 64-bit word at the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ unsigned long long ld_peer_u64(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(remote) : "r"((uint32_t)__cvta_generic_to_shared(local)), "r"(rank));
+  unsigned long long v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+__global__ void __cluster_dims__(kSpecCtas, 1, 1) __launch_bounds__(kSpecThreads)
 spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
                    const int32_t* __restrict__ s, const float* __restrict__ u,
                    const uint32_t* __restrict__ rs, const int T, const int64_t V,
                    int32_t* __restrict__ n_acc, int32_t* __restrict__ next_tok) {
-  __shared__ unsigned long long wtot[kSpecWarps];
-  __shared__ int k_sh, seg_w, done;
+  __shared__ unsigned long long wtot[2][kSpecWarps];  // per pass: this CTA's segment totals
+  __shared__ unsigned long long all[kSpecSegs];
+  __shared__ int k_sh, seg_sh, done;
   __shared__ unsigned long long base_sh, target_sh;
-  const int b = blockIdx.x, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_rank();
+  const int b = blockIdx.x / kSpecCtas, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
 
-  // ---- Eq. 10: the accepted prefix (warp 0, 32 positions at a time)
+  // ---- Eq. 10: the accepted prefix (warp 0 of every CTA, 32 positions at a time)
   if (w == 0) {
     int k = T;
     for (int t0 = 0; t0 < T; t0 += 32) {
@@ -53,7 +80,7 @@ spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
       if (t < T) {
         const int64_t x = s[(int64_t)b * T + t];
         if (x < 0 || x >= V) {
-          atomicOr(&g_spec_flags, kFlagBadToken);
+          if (crank == 0) atomicOr(&g_spec_flags, kFlagBadToken);
           reject = true;
         } else {
           const float pv = p[((int64_t)b * (T + 1) + t) * V + x];
@@ -67,21 +94,22 @@ spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
         break;
       }
     }
-    if (lane == 0) {
-      k_sh = k;
-      done = 0;
-    }
+    if (lane == 0) k_sh = k;
   }
   __syncthreads();
   const int k = k_sh;
   const float* pk = p + ((int64_t)b * (T + 1) + k) * V;
   const float* qk = k < T ? q + ((int64_t)b * T + k) * V : nullptr;
   const uint32_t r = rs[b];
-  const int64_t seg = (V + kSpecWarps - 1) / kSpecWarps;
-  const int64_t x0 = (int64_t)w * seg, x1 = x0 + seg < V ? x0 + seg : V;
+  const int64_t seg = (V + kSpecSegs - 1) / kSpecSegs;
+  const int gseg = (int)crank * kSpecWarps + w;       // this warp's segment
+  const int64_t x0 = (int64_t)gseg * seg < V ? (int64_t)gseg * seg : V;
+  const int64_t x1 = x0 + seg < V ? x0 + seg : V;
+  int32_t result = -1;
+  bool have = false;
 
   // ---- Eq. 11 (or p_{T+1}); with zero total weight, the weights of p
-  for (int pass = 0; pass < 2; ++pass) {
+  for (int pass = 0; pass < 2 && !have; ++pass) {
     const float* qw = pass == 0 ? qk : nullptr;
     auto weight = [&](int64_t x) -> uint64_t {
       const float pv = __ldg(pk + x);
@@ -91,36 +119,40 @@ spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
     for (int64_t x = x0 + lane; x < x1; x += 32) acc += weight(x);
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
-    if (lane == 0) wtot[w] = acc;
+    if (lane == 0) wtot[pass][w] = acc;
+    cluster_sync_all();                                // every CTA's totals are written
+    for (int i = tid; i < kSpecSegs; i += kSpecThreads)
+      all[i] = ld_peer_u64(&wtot[pass][i % kSpecWarps], (uint32_t)(i / kSpecWarps));
     __syncthreads();
     if (tid == 0) {
       unsigned long long Z = 0;
-      for (int i = 0; i < kSpecWarps; ++i) Z += wtot[i];
+      for (int i = 0; i < kSpecSegs; ++i) Z += all[i];
+      done = Z != 0;
       if (Z != 0) {
         // floor(r * Z / 2^32) exactly: r * Zhi + floor(r * Zlo / 2^32)
         const unsigned long long target =
             (unsigned long long)r * (Z >> 32) + (((unsigned long long)r * (Z & 0xffffffffull)) >> 32);
         unsigned long long run = 0;
-        int ws = kSpecWarps - 1;
-        for (int i = 0; i < kSpecWarps; ++i) {
-          if (run + wtot[i] > target) {
-            ws = i;
+        int sg = kSpecSegs - 1;
+        for (int i = 0; i < kSpecSegs; ++i) {
+          if (run + all[i] > target) {
+            sg = i;
             break;
           }
-          run += wtot[i];
+          run += all[i];
         }
-        seg_w = ws;
+        seg_sh = sg;
         base_sh = run;
         target_sh = target;
-        done = 1;
       }
     }
     __syncthreads();
     if (done) {
-      if (w == seg_w) {
+      have = true;
+      if (gseg == seg_sh) {                           // this warp's segment holds the target
         const unsigned long long target = target_sh;
         unsigned long long run = base_sh;
-        int32_t tok = (int32_t)(x1 - 1);
+        result = (int32_t)(x1 - 1);
         for (int64_t xs = x0; xs < x1; xs += 32) {
           const int64_t x = xs + lane;
           unsigned long long v = x < x1 ? weight(x) : 0ull;
@@ -131,31 +163,31 @@ spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
           }
           const unsigned hit = __ballot_sync(kFull, x < x1 && run + v > target);
           if (hit) {
-            tok = (int32_t)(xs + __ffs(hit) - 1);
+            result = (int32_t)(xs + __ffs(hit) - 1);
             break;
           }
           run += __shfl_sync(kFull, v, 31);
         }
         if (lane == 0) {
           n_acc[b] = k;
-          next_tok[b] = tok;
+          next_tok[b] = result;
         }
       }
-      return;
     }
   }
-  if (tid == 0) {
+  if (!have && crank == 0 && tid == 0) {
     n_acc[b] = k;
     next_tok[b] = -1;
   }
+  cluster_sync_all();  // peers may still read this CTA's totals
 }
 
 cudaError_t launch_spec_verify(const float* p, const float* q, const int32_t* s, const float* u,
                                const uint32_t* r, int batch, int T, int64_t V, int32_t* n_acc,
                                int32_t* next_tok, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
-  spec_verify_kernel<<<(unsigned)batch, kSpecThreads, 0, stream>>>(p, q, s, u, r, T, V, n_acc,
-                                                                    next_tok);
+  spec_verify_kernel<<<(unsigned)(batch * kSpecCtas), kSpecThreads, 0, stream>>>(
+      p, q, s, u, r, T, V, n_acc, next_tok);
   return cudaGetLastError();
 }
 
