@@ -383,10 +383,44 @@ def anchor_ratio(alpha: float) -> float:
     return (1.0 + alpha) ** (16.0 / 127.0)
 
 
+# ------------------------------------------------------------ request format
+
+def stream_bytes(B: int, L: int, H: int, P: int, C: int, D: int = 128):
+    """Bytes of the Anchor, Residual and meta streams: 4 bits per element for
+    each code stream [Review, Implementation Notes: two 4-bit values per
+    uint8], (2 + 2P/C) float32 rows of D per page block (the metadata above)."""
+    elems = B * L * H * D
+    return elems // 2, elems // 2, B * (L // P) * metadata_scalars(H, P, C) * D * 4
+
+
+def request_header(B: int, L: int, H: int, P: int, C: int, alpha: float,
+                   with_residual: bool = True, D: int = 128, version: int = 1,
+                   sizes=None) -> bytes:
+    """The 128-byte header of a serialized request, written out field by
+    field: the Anchor stream and its metadata first, so the Anchor phase is
+    one contiguous range ("Q_anc and metadata contiguous", [Review],
+    Implementation Notes), then the Residual stream.  The last field is the
+    CRC-32 (zlib's) of the 124 bytes before it.  `sizes` overrides the
+    stream sizes (to build inconsistent headers for tests)."""
+    import struct
+    import zlib
+    a, r, m = sizes if sizes is not None else stream_bytes(B, L, H, P, C, D)
+    if not with_residual and sizes is None:
+        r = 0
+    a_off = 128
+    m_off = a_off + a
+    r_off = m_off + m
+    body = struct.pack("<8sIIqqiiiifIQQQQQQQIII", b"LYNXKV\x00\x01", version, 128, B, L, H, D,
+                       P, C, alpha, 1 if with_residual else 0, a_off, a, m_off, m, r_off, r,
+                       r_off + r, 0, 0, 0)
+    assert len(body) == 124
+    return body + struct.pack("<I", zlib.crc32(body) & 0xFFFFFFFF)
+
+
 __all__ = [
     "EPS", "build", "compand_y", "round_code", "expand", "expand_table",
     "stage4_literal", "code8", "anchor_nibble", "residual_nibble",
     "f32_to_bf16_bits", "bf16_bits_to_f32", "meta_rows", "encode_block",
     "encode", "decode_block", "decode", "attention_row", "kv_size_bytes",
-    "metadata_scalars", "effective_bins", "anchor_ratio",
+    "metadata_scalars", "effective_bins", "anchor_ratio", "stream_bytes", "request_header",
 ]
