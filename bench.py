@@ -463,6 +463,9 @@ def run_lynx(args, rank, world, dev):
 
     ms_total, e2e_s = max_over_ranks([ms_total, e2e_s], world, dev)
     extras = measure_extras(ks, vs, q8, ws, dev) if rank == 0 else None
+    if extras is not None:
+        extras["split_stream"] = measure_split(kv, kv_h, (anc, res, meta),
+                                               (anc_h, res_h, meta_h), dec_a, dev)
     assert lynx.lynx_wait_timeouts() == 0
     return dict(ms_total=ms_total, row_ms=row_ms, e2e_s=e2e_s, h2d=h2d, d2h=d2h, clocks=clk,
                 launches=launches, extras=extras)
@@ -549,6 +552,83 @@ def measure_extras(ks, vs, q8, ws, dev, reps=10):
                                what=f"Eq. 10-11: batch {B}, T={T}, V={V}; mean accepted "
                                     f"{float(k.float().mean()):.2f} of {T}")
     return out
+
+
+def measure_split(kv, kv_h, dev_streams, host_streams, out, dev, reps=3, pages_per_group=256):
+    """The split-stream timeline on the codec workload, one GPU as either end
+    of the link (pinned host memory standing in for it): the receiver's time
+    until every Anchor group is on the device and decoded (when drafting can
+    start) and until every group is upgraded to the full decode, against the
+    time the BF16 tensor alone takes over the same link; and the sender's
+    times for encode + copy-out.  Medians over `reps`, each from an event on
+    the copy stream recorded before the first operation."""
+    import statistics
+
+    import torch
+
+    from split_stream_kv_gb300 import lynx
+    c = CODEC
+    copy_s = torch.cuda.Stream(dev)
+    hi = torch.cuda.Stream(dev, priority=-1)
+    lo = torch.cuda.Stream(dev, priority=0)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, n_marks):
+        res = []
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0 = ev()
+            marks = [ev() for _ in range(n_marks)]
+            e0.record(copy_s)
+            fn(marks)
+            torch.cuda.synchronize(dev)
+            res.append([e0.elapsed_time(m) for m in marks])
+        return [statistics.median(r[i] for r in res) for i in range(n_marks)]
+
+    def bf16_in(m):
+        with torch.cuda.stream(copy_s):
+            kv.copy_(kv_h, non_blocking=True)
+            m[0].record(copy_s)
+
+    def bf16_out(m):
+        with torch.cuda.stream(copy_s):
+            kv_h.copy_(kv, non_blocking=True)
+            m[0].record(copy_s)
+
+    def receive(m, with_out):
+        lynx.lynx_split_receive(host_streams, dev_streams, c["L"], c["P"], c["C"], ALPHA,
+                                pages_per_group, out=out if with_out else None,
+                                copy_stream=copy_s, hi_stream=hi, lo_stream=lo,
+                                anchor_ready=m[0], full_ready=m[1])
+
+    def send(m):
+        lynx.lynx_split_send(kv, c["P"], c["C"], ALPHA, dev_streams, host_streams,
+                             pages_per_group, hi_stream=hi, copy_stream=copy_s,
+                             anchor_sent=m[0], all_sent=m[1])
+
+    t_in, = timed(bf16_in, 1)
+    t_out, = timed(bf16_out, 1)
+    r_anchor, r_full = timed(lambda m: receive(m, True), 2)
+    c_anchor, c_all = timed(lambda m: receive(m, False), 2)
+    s_anchor, s_all = timed(send, 2)
+    a_bytes = sum(t.nbytes for t in (host_streams[0], host_streams[2]))
+    all_bytes = a_bytes + host_streams[1].nbytes
+    return {
+        "pages_per_group": pages_per_group,
+        "bf16_bytes": kv_h.nbytes, "anchor_phase_bytes": a_bytes, "all_bytes": all_bytes,
+        "bf16_h2d_ms": round(t_in, 4), "bf16_d2h_ms": round(t_out, 4),
+        "receive_anchor_ready_ms": round(r_anchor, 4),
+        "receive_full_ready_ms": round(r_full, 4),
+        "receive_copies_anchor_ms": round(c_anchor, 4), "receive_copies_all_ms": round(c_all, 4),
+        "send_anchor_sent_ms": round(s_anchor, 4), "send_all_sent_ms": round(s_all, 4),
+        "time_to_anchor_speedup_vs_bf16": round(t_in / r_anchor, 3),
+        "link_h2d_GBps": round(kv_h.nbytes / t_in / 1e6, 1),
+        "what": "one GPU as either end of the link: pinned host memory in between; receiver "
+                "times to every Anchor decoded and to every group upgraded in place, sender "
+                "times for encode + copy-out, against the BF16 tensor over the same link",
+    }
 
 
 def main():

@@ -137,6 +137,118 @@ int lynx_decode_paged(const void *anchor_pool, const void *residual_pool,
                       int page, int C, float alpha, int mode, void *out,
                       int out_dtype, void *stream);
 
+/* ---------------------------------------------------------------------
+ * Split-stream transfer [Review, Mechanism 2 (Figure 4, Implementation
+ * Notes): the Anchor stream on a high-priority queue, the Residual stream on
+ * a low-priority one, decoding as soon as the Anchor lands; Anchor buffers
+ * are drained before Residual buffers at the page level; the serializer
+ * quantises page i+1 while page i is in flight].
+ *
+ * The unit of transfer is a group of `pages_per_group` consecutive pages of
+ * the flattened (b, page) order (H_kv page blocks each; the last group may be
+ * shorter).  Because the three streams are stored in (b, page, head) order,
+ * a group is one contiguous byte range of each stream (and of the BF16
+ * tensor), so it moves with one copy per stream.
+ *
+ * A schedule is a list of operations on three queues:
+ *   LYNX_Q_COPY     the one copy queue: every Anchor and meta copy of every
+ *                   group comes before the first Residual copy (the drain
+ *                   rule, taken strictly);
+ *   LYNX_Q_HI       high-priority kernels: encode (sender) or anchor decode
+ *                   (receiver);
+ *   LYNX_Q_LO       low-priority kernels: the in-place upgrade to the full
+ *                   decode (receiver).
+ * An operation may wait for up to two earlier operations on other queues,
+ * named by (kind, group); group -1 there means "every group of that kind". */
+enum {
+  LYNX_OP_ENCODE = 0,        /* sender: encode the group on the device       */
+  LYNX_OP_COPY_ANCHOR = 1,   /* Anchor bytes of the group                    */
+  LYNX_OP_COPY_META = 2,     /* metadata bytes of the group                  */
+  LYNX_OP_COPY_RESIDUAL = 3, /* Residual bytes of the group                  */
+  LYNX_OP_DECODE_ANCHOR = 4, /* receiver: Anchor-only decode into out        */
+  LYNX_OP_UPGRADE = 5,       /* receiver: full decode over the same out      */
+  LYNX_OP_NONE = -1
+};
+enum { LYNX_Q_COPY = 0, LYNX_Q_HI = 1, LYNX_Q_LO = 2 };
+
+typedef struct {
+  int32_t kind, queue;
+  int64_t group;
+  int64_t page0, n_pages;     /* flattened page range [page0, page0 + n_pages) */
+  int64_t offset, bytes;      /* byte range of the copied stream (copies only) */
+  int32_t wait_kind[2];       /* LYNX_OP_NONE when unused                       */
+  int64_t wait_group[2];      /* -1: every group of wait_kind                   */
+} lynx_split_op;
+
+/* The schedule lynx_split_receive (send = 0) or lynx_split_send (send = 1)
+ * enqueues, in issue order.  with_decode (receiver only): 1 adds the anchor
+ * decode and upgrade kernels.  Host-only; writes at most max_ops entries and
+ * sets *n_ops to the full count.  LYNX_EWORKSPACE if max_ops is too small. */
+int lynx_split_plan(int64_t B, int64_t L, int H_kv, int D, int page, int C,
+                    int64_t pages_per_group, int send, int with_decode,
+                    lynx_split_op *ops, int64_t max_ops, int64_t *n_ops);
+
+/* Receiver.  Copies the encoded streams from host memory (h_*, page-locked
+ * for the copies to overlap) to the device (anchor, meta, residual), group
+ * by group in the drain order above, on copy_stream.  If out is not NULL,
+ * each group is decoded from its Anchor on hi_stream as soon as its Anchor
+ * and meta have landed (lynx_decode_anchor of that page range), and, once
+ * every Anchor group is decoded, upgraded in place on lo_stream as soon as
+ * its Residual has landed (lynx_decode_full of that page range over the
+ * same out).  Events (may be NULL): anchor_ready is recorded on hi_stream
+ * when every Anchor and meta byte is on the device (and decoded, with out);
+ * full_ready on lo_stream when every Residual byte is (and out holds the
+ * full decode).  Streams may be NULL (the legacy default stream).  Returns
+ * after enqueueing; sizes as lynx_encoded_sizes. */
+int lynx_split_receive(const void *h_anchor, const float *h_meta,
+                       const void *h_residual, void *anchor, float *meta,
+                       void *residual, int64_t B, int64_t L, int H_kv, int D,
+                       int page, int C, float alpha, int64_t pages_per_group,
+                       void *out, int out_dtype, void *copy_stream,
+                       void *hi_stream, void *lo_stream, void *anchor_ready,
+                       void *full_ready);
+
+/* Sender.  Encodes kv group by group on hi_stream into the device streams
+ * (anchor, meta, residual) and copies each group's Anchor and meta to host
+ * memory (h_*) on copy_stream as soon as it is encoded, so encoding group
+ * g+1 overlaps the copy of group g; every Residual copy follows the last
+ * Anchor copy.  Events (may be NULL): anchor_sent on copy_stream after the
+ * last Anchor and meta byte, all_sent after the last Residual byte. */
+int lynx_split_send(const void *kv, int64_t B, int64_t L, int H_kv, int D,
+                    int page, int C, float alpha, void *anchor, float *meta,
+                    void *residual, void *h_anchor, float *h_meta,
+                    void *h_residual, int64_t pages_per_group,
+                    void *hi_stream, void *copy_stream, void *anchor_sent,
+                    void *all_sent);
+
+/* Format header of a serialized request: header, then the Anchor stream,
+ * the meta stream and the Residual stream, so the Anchor phase (codes and
+ * the metadata needed to decode them) is one contiguous byte range.  All
+ * integers little-endian as laid out here; 128 bytes. */
+typedef struct {
+  char magic[8];          /* "LYNXKV" 0 1                                  */
+  uint32_t version;       /* 1                                             */
+  uint32_t header_bytes;  /* 128                                           */
+  int64_t B, L;
+  int32_t H_kv, D, page, C;
+  float alpha;
+  uint32_t flags;         /* bit 0: Residual stream present                */
+  uint64_t anchor_offset, anchor_bytes;
+  uint64_t meta_offset, meta_bytes;
+  uint64_t residual_offset, residual_bytes;
+  uint64_t total_bytes;   /* header + the three streams                    */
+  uint32_t reserved[3];   /* zero                                          */
+  uint32_t header_crc;    /* CRC-32 (IEEE 802.3) of the 124 bytes before it */
+} lynx_header;
+
+/* Fill *h for these dimensions (validated as for lynx_encode). */
+int lynx_header_init(lynx_header *h, int64_t B, int64_t L, int H_kv, int D,
+                     int page, int C, float alpha, int with_residual);
+/* LYNX_OK if *h is a well-formed version-1 header whose sizes and offsets
+ * follow from its dimensions; LYNX_EINVAL (bad magic, version, CRC or
+ * sizes) or the codes of lynx_encode for bad dimensions otherwise. */
+int lynx_header_check(const lynx_header *h);
+
 /* Speculative verification and correction [Review, Mechanism 3, Eq. 10 and
  * Eq. 11], for every sequence b of the batch, on distributions the caller's
  * verification pass (p, over the full KV) and draft steps (q, over the
@@ -156,7 +268,8 @@ int lynx_decode_paged(const void *anchor_pool, const void *residual_pool,
  * weights of p are used, and if they sum to 0 too the token is -1.  A draft
  * token outside [0, V) counts as rejected and is reported by
  * lynx_device_errors (bit 4).  1 <= T <= 64, 1 <= V < 2^31; all device
- * pointers, 16-byte aligned.  One CTA per sequence, enqueued on `stream`. */
+ * pointers, 16-byte aligned.  One cluster of 8 CTAs per sequence, enqueued
+ * on `stream`. */
 int lynx_spec_verify(const float *p_target, const float *q_draft,
                      const int32_t *draft_tokens, const float *u_accept,
                      const uint32_t *r_sample, int batch, int T, int64_t V,

@@ -58,6 +58,13 @@ def lib() -> ctypes.CDLL:
         "lynx_spec_verify": ([P, P, P, P, P, I, I, I64, P, P, P], I),
         "lynx_attn_decode_noalloc": ([P, I, I, I, P, P, P, P, P, P, I64, I, I, I, I, F, I, P, P],
                                      I),
+        "lynx_split_plan": ([I64, I64, I, I, I, I, I64, I, I, P, I64,
+                             ctypes.POINTER(ctypes.c_int64)], I),
+        "lynx_split_receive": ([P, P, P, P, P, P, I64, I64, I, I, I, I, F, I64, P, I, P, P, P,
+                                P, P], I),
+        "lynx_split_send": ([P, I64, I64, I, I, I, I, F, P, P, P, P, P, P, I64, P, P, P, P], I),
+        "lynx_header_init": ([P, I64, I64, I, I, I, I, F, I], I),
+        "lynx_header_check": ([P], I),
         "lynx_compander_thresholds": ([F, P], I),
         "lynx_expand_table": ([F, P], I),
         "lynx_compander_selfcheck": ([F, P, P], I),
@@ -244,6 +251,131 @@ def lynx_device_errors() -> int:
     bits = ctypes.c_uint()
     _check(lib().lynx_device_errors(ctypes.byref(bits)), "lynx_device_errors")
     return bits.value
+
+
+# ------------------------------------------------------- split-stream transfer
+
+LYNX_OP_ENCODE, LYNX_OP_COPY_ANCHOR, LYNX_OP_COPY_META, LYNX_OP_COPY_RESIDUAL = 0, 1, 2, 3
+LYNX_OP_DECODE_ANCHOR, LYNX_OP_UPGRADE, LYNX_OP_NONE = 4, 5, -1
+LYNX_Q_COPY, LYNX_Q_HI, LYNX_Q_LO = 0, 1, 2
+
+
+class SplitOp(ctypes.Structure):
+    """lynx_split_op of include/lynx.h."""
+    _fields_ = [("kind", ctypes.c_int32), ("queue", ctypes.c_int32), ("group", ctypes.c_int64),
+                ("page0", ctypes.c_int64), ("n_pages", ctypes.c_int64),
+                ("offset", ctypes.c_int64), ("bytes", ctypes.c_int64),
+                ("wait_kind", ctypes.c_int32 * 2), ("wait_group", ctypes.c_int64 * 2)]
+
+
+class LynxHeader(ctypes.Structure):
+    """lynx_header of include/lynx.h (128 bytes)."""
+    _fields_ = [("magic", ctypes.c_char * 8), ("version", ctypes.c_uint32),
+                ("header_bytes", ctypes.c_uint32), ("B", ctypes.c_int64), ("L", ctypes.c_int64),
+                ("H_kv", ctypes.c_int32), ("D", ctypes.c_int32), ("page", ctypes.c_int32),
+                ("C", ctypes.c_int32), ("alpha", ctypes.c_float), ("flags", ctypes.c_uint32),
+                ("anchor_offset", ctypes.c_uint64), ("anchor_bytes", ctypes.c_uint64),
+                ("meta_offset", ctypes.c_uint64), ("meta_bytes", ctypes.c_uint64),
+                ("residual_offset", ctypes.c_uint64), ("residual_bytes", ctypes.c_uint64),
+                ("total_bytes", ctypes.c_uint64), ("reserved", ctypes.c_uint32 * 3),
+                ("header_crc", ctypes.c_uint32)]
+
+
+def lynx_split_plan(B: int, L: int, H_kv: int, D: int, page: int, C: int, pages_per_group: int,
+                    send: bool = False, with_decode: bool = True):
+    """The transfer schedule as a list of dicts, in issue order."""
+    n = ctypes.c_int64()
+    rc = lib().lynx_split_plan(B, L, H_kv, D, page, C, pages_per_group, int(send),
+                               int(with_decode), None, 0, ctypes.byref(n))
+    if rc not in (LYNX_OK, LYNX_EWORKSPACE):
+        _check(rc, "lynx_split_plan")
+    buf = (SplitOp * max(1, n.value))()
+    _check(lib().lynx_split_plan(B, L, H_kv, D, page, C, pages_per_group, int(send),
+                                 int(with_decode), buf, n.value, ctypes.byref(n)),
+           "lynx_split_plan")
+    return [{"kind": o.kind, "queue": o.queue, "group": o.group, "page0": o.page0,
+             "n_pages": o.n_pages, "offset": o.offset, "bytes": o.bytes,
+             "waits": [(o.wait_kind[i], o.wait_group[i]) for i in range(2)
+                       if o.wait_kind[i] != LYNX_OP_NONE]} for o in buf[:n.value]]
+
+
+def _need_host(*ts):
+    for t in ts:
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("lynx: host buffers must be contiguous CPU tensors (pinned)")
+
+
+def _raw_stream(s):
+    return ctypes.c_void_p(s.cuda_stream) if s is not None else None
+
+
+def _raw_event(ev, stream):
+    """Handle of a torch.cuda.Event, created (by a first record) if still lazy."""
+    if ev is None:
+        return None
+    if not ev.cuda_event:
+        ev.record(stream if stream is not None else torch.cuda.current_stream())
+    return ctypes.c_void_p(ev.cuda_event)
+
+
+def lynx_split_receive(host, dev, L: int, page: int, C: int, alpha: float, pages_per_group: int,
+                       out=None, copy_stream=None, hi_stream=None, lo_stream=None,
+                       anchor_ready=None, full_ready=None):
+    """Receiver side: host = (anchor, residual, meta) CPU tensors, dev = the
+    same three CUDA tensors (stream_shapes); out (optional) is decoded from
+    the Anchor as it lands and upgraded in place to the full decode."""
+    ha, hr, hm = host
+    da, dr, dm = dev
+    _need_host(ha, hr, hm)
+    _need_cuda(da, dr, dm, out)
+    B, NB, H, P, half = da.shape
+    code = LYNX_OUT_BF16
+    if out is not None:
+        if out.dtype not in (torch.bfloat16, torch.float32):
+            raise ValueError("lynx_split_receive: out must be bfloat16 or float32")
+        code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
+    _check(lib().lynx_split_receive(_ptr(ha), _ptr(hm), _ptr(hr), _ptr(da), _ptr(dm), _ptr(dr),
+                                    B, L, H, half * 2, page, C, alpha, pages_per_group, _ptr(out),
+                                    code, _raw_stream(copy_stream), _raw_stream(hi_stream),
+                                    _raw_stream(lo_stream), _raw_event(anchor_ready, hi_stream),
+                                    _raw_event(full_ready, lo_stream)),
+           "lynx_split_receive")
+
+
+def lynx_split_send(kv, page: int, C: int, alpha: float, dev, host, pages_per_group: int,
+                    hi_stream=None, copy_stream=None, anchor_sent=None, all_sent=None):
+    """Sender side: encode kv into dev = (anchor, residual, meta) group by
+    group and copy each group to host = (anchor, residual, meta) CPU tensors,
+    every Residual after the last Anchor."""
+    da, dr, dm = dev
+    ha, hr, hm = host
+    _need_cuda(kv, da, dr, dm)
+    _need_host(ha, hr, hm)
+    B, L, H, D = kv.shape
+    _check(lib().lynx_split_send(_ptr(kv), B, L, H, D, page, C, alpha, _ptr(da), _ptr(dm),
+                                 _ptr(dr), _ptr(ha), _ptr(hm), _ptr(hr), pages_per_group,
+                                 _raw_stream(hi_stream), _raw_stream(copy_stream),
+                                 _raw_event(anchor_sent, copy_stream),
+                                 _raw_event(all_sent, copy_stream)),
+           "lynx_split_send")
+
+
+def lynx_header_init(B: int, L: int, H_kv: int, D: int, page: int, C: int, alpha: float,
+                     with_residual: bool = True) -> bytes:
+    """The 128-byte header of a serialized request."""
+    h = LynxHeader()
+    _check(lib().lynx_header_init(ctypes.byref(h), B, L, H_kv, D, page, C, alpha,
+                                  int(with_residual)), "lynx_header_init")
+    return bytes(h)
+
+
+def lynx_header_check(buf: bytes) -> LynxHeader:
+    """Validate a header; returns it parsed, or raises LynxError."""
+    if len(buf) < ctypes.sizeof(LynxHeader):
+        raise ValueError("lynx_header_check: fewer than 128 bytes")
+    h = LynxHeader.from_buffer_copy(bytes(buf[:ctypes.sizeof(LynxHeader)]))
+    _check(lib().lynx_header_check(ctypes.byref(h)), "lynx_header_check")
+    return h
 
 
 # ----------------------------------------------------------------- attention
