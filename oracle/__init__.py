@@ -82,6 +82,14 @@ def _bind(lib):
     lib.oracle_spec_verify.restype = I
     lib.oracle_spec_verify_batch.argtypes = [P, P, P, P, P, I, I, I64, P, P]
     lib.oracle_spec_verify_batch.restype = None
+    lib.oracle_split_bits.argtypes = [P, P, I64, I, I, P, P]
+    lib.oracle_split_bits.restype = I
+    lib.oracle_decode_anchor_bits_range.argtypes = [P, P, I64, I64, I, I, I, I, F, I, P]
+    lib.oracle_decode_anchor_bits_range.restype = I
+    lib.oracle_int_encode_rows.argtypes = [P, I64, I, I, P, P]
+    lib.oracle_int_encode_rows.restype = I
+    lib.oracle_int_decode_rows.argtypes = [P, P, I64, I, I, P]
+    lib.oracle_int_decode_rows.restype = I
     return lib
 
 
@@ -356,6 +364,95 @@ def spec_verify(p: np.ndarray, q: np.ndarray, s: np.ndarray, u: np.ndarray,
     return k, tok
 
 
+# ------------------------------------------------------------ variants
+
+def split_bits(anc4: np.ndarray, res4: np.ndarray, k: int):
+    """Re-split 4+4 streams [..][P][D/2] into a k + (8-k) split: returns the
+    Anchor [..][P][D*k/8] and Residual [..][P][D*(8-k)/8] streams."""
+    lib = _load()
+    a = np.ascontiguousarray(anc4, dtype=np.uint8)
+    r = np.ascontiguousarray(res4, dtype=np.uint8)
+    D = a.shape[-1] * 2
+    rows = a.size // (D // 2)
+    ak = np.zeros(a.shape[:-1] + (D * k // 8,), dtype=np.uint8)
+    rk = np.zeros(a.shape[:-1] + (D * (8 - k) // 8,), dtype=np.uint8)
+    rc = lib.oracle_split_bits(_ptr(a), _ptr(r), rows, D, k, _ptr(ak), _ptr(rk))
+    if rc:
+        raise ValueError("oracle_split_bits: bad arguments")
+    return ak, rk
+
+
+def decode_anchor_bits(ak: np.ndarray, meta: np.ndarray, L: int, P: int, C: int, alpha: float,
+                       k: int) -> np.ndarray:
+    """Anchor-only decode of a k-bit Anchor stream [B][NB][H][P][D*k/8]."""
+    lib = _load()
+    a = np.ascontiguousarray(ak, dtype=np.uint8)
+    m = np.ascontiguousarray(meta, dtype=np.float32)
+    B, NB, H = a.shape[:3]
+    D = a.shape[-1] * 8 // k
+    out = np.zeros((B, L, H, D), dtype=np.float32)
+    rc = lib.oracle_decode_anchor_bits_range(_ptr(a), _ptr(m), B, L, H, D, P, C, alpha, k,
+                                             _ptr(out))
+    if rc:
+        raise ValueError("oracle_decode_anchor_bits_range: bad arguments")
+    return out
+
+
+def int_encode(kv_bits: np.ndarray, bits: int):
+    """Linear INT-`bits` baseline (Eq. 4) of a bf16 tensor [..][D] (uint16
+    bit patterns): codes [..][D*bits/8] uint8 and meta [..][2] float32."""
+    lib = _load()
+    x = np.ascontiguousarray(kv_bits, dtype=np.uint16)
+    D = x.shape[-1]
+    rows = x.size // D
+    codes = np.zeros(x.shape[:-1] + (D * bits // 8,), dtype=np.uint8)
+    meta = np.zeros(x.shape[:-1] + (2,), dtype=np.float32)
+    rc = lib.oracle_int_encode_rows(_ptr(x), rows, D, bits, _ptr(codes), _ptr(meta))
+    if rc:
+        raise ValueError("oracle_int_encode_rows: bad arguments")
+    return codes, meta
+
+
+def int_decode(codes: np.ndarray, meta: np.ndarray, bits: int) -> np.ndarray:
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    m = np.ascontiguousarray(meta, dtype=np.float32)
+    D = c.shape[-1] * 8 // bits
+    rows = c.size // (D * bits // 8)
+    out = np.zeros(c.shape[:-1] + (D,), dtype=np.float32)
+    rc = lib.oracle_int_decode_rows(_ptr(c), _ptr(m), rows, D, bits, _ptr(out))
+    if rc:
+        raise ValueError("oracle_int_decode_rows: bad arguments")
+    return out
+
+
+def vnmse(approx: np.ndarray, ref: np.ndarray) -> float:
+    """Normalised mean-square error of attention outputs (the metric of the
+    pages' accuracy table, [Review], Mechanism 3 "Why is the acceptance rate
+    high?"): sum |o - o_ref|^2 / sum |o_ref|^2 over all outputs, float64."""
+    a = np.asarray(approx, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    return float(np.sum((a - r) ** 2) / np.sum(r ** 2))
+
+
+def attention_rows(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """attention_row for every (sequence, query token, query head): q
+    [batch][T][H_q][D], K, V [batch][L][H_kv][D] float32 (GQA: query head h
+    reads KV head h // (H_q/H_kv)); float64 out [batch][T][H_q][D]."""
+    batch, T, Hq, D = q.shape
+    Hkv = K.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((batch, T, Hq, D), dtype=np.float64)
+    for b in range(batch):
+        for h in range(Hkv):
+            Kh = np.ascontiguousarray(K[b, :, h, :], dtype=np.float32)
+            Vh = np.ascontiguousarray(V[b, :, h, :], dtype=np.float32)
+            for t in range(T):
+                for g in range(G):
+                    out[b, t, h * G + g] = attention_row(q[b, t, h * G + g], Kh, Vh)
+    return out
+
+
 # ------------------------------------------------------------ size formulas
 
 def kv_size_bytes(k_factor: int, L: int, D: int, n_layers: int,
@@ -423,4 +520,5 @@ __all__ = [
     "f32_to_bf16_bits", "bf16_bits_to_f32", "meta_rows", "encode_block",
     "encode", "decode_block", "decode", "attention_row", "kv_size_bytes",
     "metadata_scalars", "effective_bins", "anchor_ratio", "stream_bytes", "request_header",
+    "split_bits", "decode_anchor_bits", "int_encode", "int_decode", "vnmse", "attention_rows",
 ]

@@ -352,6 +352,179 @@ int oracle_decode_range(const uint8_t *anchor, const uint8_t *residual,
     return 0;
 }
 
+/* ------------------------------------------------- bit-split variants */
+
+/*
+ * Other Anchor/Residual bit splits ([Review], "Concrete Improvement
+ * Suggestions", items 4-5: the split 3+5, 4+4, 5+3 or 6+2 as one axis of an
+ * ablation, and its Pareto frontier).  The code is
+ * the same signed 8-bit Q8 of Stage 4; a k-bit Anchor is its arithmetic top
+ * k bits and the Residual its low 8-k bits, so (Anchor << (8-k)) | Residual
+ * == Q8, as for the 4+4 split (the extraction of [Review] Appendix A.1 with
+ * a shift of 8-k).  The Anchor-only reconstruction point generalises the
+ * 4+4 bucket point 16 V + 7: the round-half-down centre of the 2^(8-k)
+ * codes of a bucket, I_rep = 2^(8-k) V + 2^(7-k) - 1, V = the Anchor's
+ * magnitude (a >= 0 ? a : -a - 1).
+ * Layout (a reading; the pages fix none): per token, the aligned group of 8
+ * channels 8G..8G+7 fills k Anchor bytes and 8-k Residual bytes, channel
+ * 8G+j in bits j*w .. j*w + w - 1 (w = the field width) of the group's
+ * bytes read as one little-endian integer.  Blocks keep the (b, page, head)
+ * order of the 4+4 streams.
+ */
+static int field_get(const uint8_t *p, int j, int w)
+{
+    int v = 0;
+    for (int i = 0; i < w; ++i) {
+        int b = j * w + i;
+        v |= ((p[b >> 3] >> (b & 7)) & 1) << i;
+    }
+    return v;
+}
+
+static void field_put(uint8_t *p, int j, int w, int v)
+{
+    for (int i = 0; i < w; ++i) {
+        int b = j * w + i;
+        uint8_t m = (uint8_t)(1u << (b & 7));
+        if ((v >> i) & 1) p[b >> 3] |= m; else p[b >> 3] &= (uint8_t)~m;
+    }
+}
+
+/* Re-split `rows` token rows of D channels from the 4+4 streams (nibble
+ * pairing of Stage 4) into a k / (8-k) split, 3 <= k <= 6. */
+int oracle_split_bits(const uint8_t *anchor4, const uint8_t *residual4, int64_t rows, int D,
+                      int k, uint8_t *ak, uint8_t *rk)
+{
+    if (k < 3 || k > 6 || D <= 0 || (D & 7)) return -1;
+    const int rw = 8 - k;
+    for (int64_t t = 0; t < rows; ++t) {
+        for (int d = 0; d < D; ++d) {
+            size_t byte = (size_t)t * (size_t)(D / 2) + nib_byte(d);
+            int sh = nib_shift(d);
+            int q8 = (((anchor4[byte] >> sh) & 0xf) << 4) | ((residual4[byte] >> sh) & 0xf);
+            uint8_t *pa = ak + (size_t)t * (size_t)(D / 8) * (size_t)k + (size_t)(d / 8) * (size_t)k;
+            uint8_t *pr = rk + (size_t)t * (size_t)(D / 8) * (size_t)rw + (size_t)(d / 8) * (size_t)rw;
+            field_put(pa, d % 8, k, (q8 >> rw) & ((1 << k) - 1));
+            field_put(pr, d % 8, rw, q8 & ((1 << rw) - 1));
+        }
+    }
+    return 0;
+}
+
+/* Anchor-only decode of one page block from a k-bit Anchor stream. */
+int oracle_decode_anchor_bits_block(const uint8_t *ak, const float *meta, int P, int D, int C,
+                                    float alpha, int k, float *out, int64_t out_stride)
+{
+    if (k < 3 || k > 6 || P <= 0 || D <= 0 || (D & 7) || C <= 0 || P % C) return -1;
+    const int NC = P / C;
+    const float *g_min = meta;
+    const float *g_scale = meta + D;
+    const float *mu_rows = meta + 2 * D;
+    const float *sg_rows = meta + (size_t)(2 + NC) * D;
+    float table[128];
+    for (int I = 0; I < 128; ++I) table[I] = oracle_expand(I, alpha);
+    for (int t = 0; t < P; ++t) {
+        int c = t / C;
+        for (int d = 0; d < D; ++d) {
+            const uint8_t *pa = ak + (size_t)t * (size_t)(D / 8) * (size_t)k + (size_t)(d / 8) * (size_t)k;
+            int a = field_get(pa, d % 8, k);
+            int qa = a >= (1 << (k - 1)) ? a - (1 << k) : a;
+            int S = qa >= 0 ? 1 : -1;
+            int V = S > 0 ? qa : -qa - 1;
+            int I = (1 << (8 - k)) * V + (1 << (7 - k)) - 1;
+            float xf = S > 0 ? table[I] : -table[I];
+            float sg = sg_rows[(size_t)c * D + d];
+            float mu = mu_rows[(size_t)c * D + d];
+            float nv = fmaf(xf, sg + ORACLE_EPS, mu);
+            out[(int64_t)t * out_stride + d] = fmaf(nv, g_scale[d] + ORACLE_EPS, g_min[d]);
+        }
+    }
+    return 0;
+}
+
+/* The same over a whole [B][L][H][D] tensor (float32 out). */
+int oracle_decode_anchor_bits_range(const uint8_t *ak, const float *meta, int64_t B, int64_t L,
+                                    int H, int D, int P, int C, float alpha, int k, float *out)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || P <= 0 || L % P || C <= 0 || P % C) return -1;
+    const int64_t NB = L / P;
+    const size_t code_blk = (size_t)P * (size_t)(D / 8) * (size_t)k;
+    const size_t meta_blk = (size_t)(2 + 2 * (P / C)) * (size_t)D;
+    for (int64_t blk = 0; blk < B * NB * H; ++blk) {
+        int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
+        int rc = oracle_decode_anchor_bits_block(ak + blk * code_blk, meta + blk * meta_blk, P, D,
+                                                 C, alpha, k, out + ((b * L + p * P) * H + h) * D,
+                                                 (int64_t)H * D);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------ linear INT-B baseline */
+
+/*
+ * The linear quantizer the pages compare against ([Review], Prerequisites,
+ * "KV Cache Quantization and the Outlier Problem", Eq. 4):
+ *   Q(x) = round(x / S + Z),  S = (x_max - x_min) / (2^B - 1).
+ * Readings (the pages fix none of them): one (S, Z) per token and KV head,
+ * over its D channels (the grouping in which an outlier channel sets the
+ * scale of the others, Eq. 5); Z = -x_min / S, so Q = round((x - x_min)/S),
+ * the division taken as a multiplication by the correctly rounded float32
+ * reciprocal of S (of 0 for a constant row, S = 0: every code is then 0);
+ * round to nearest, ties to even; Q clamped to [0, 2^B - 1]; a zero x_min
+ * is stored as +0.  Reconstruction
+ * x = Q * S + x_min in one fused multiply-add.  B = 8: one byte a value;
+ * B = 4: byte j holds channels 2j (low nibble) and 2j+1 (high nibble).
+ * meta: (x_min, S) float32 per row.
+ */
+int oracle_int_encode_rows(const uint16_t *x, int64_t rows, int D, int bits, uint8_t *codes,
+                           float *meta)
+{
+    if ((bits != 4 && bits != 8) || D <= 0 || (D & 1)) return -1;
+    const int qmax = (1 << bits) - 1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + r * D;
+        float lo = bf16_bits_to_f32(xr[0]), hi = lo;
+        for (int d = 1; d < D; ++d) {
+            float v = bf16_bits_to_f32(xr[d]);
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        lo = lo + 0.0f;
+        float S = (hi - lo) / (float)qmax;
+        float rs = S > 0.0f ? 1.0f / S : 0.0f;
+        uint8_t *cr = codes + r * (int64_t)(bits == 8 ? D : D / 2);
+        if (bits == 4) memset(cr, 0, (size_t)(D / 2));
+        for (int d = 0; d < D; ++d) {
+            float dd = bf16_bits_to_f32(xr[d]) - lo;
+            float qf = rintf(dd * rs);
+            if (qf > (float)qmax) qf = (float)qmax;
+            if (qf < 0.0f) qf = 0.0f;
+            int q = (int)qf;
+            if (bits == 8) cr[d] = (uint8_t)q;
+            else cr[d / 2] |= (uint8_t)(q << ((d & 1) ? 4 : 0));
+        }
+        meta[2 * r] = lo;
+        meta[2 * r + 1] = S;
+    }
+    return 0;
+}
+
+int oracle_int_decode_rows(const uint8_t *codes, const float *meta, int64_t rows, int D, int bits,
+                           float *out)
+{
+    if ((bits != 4 && bits != 8) || D <= 0 || (D & 1)) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const uint8_t *cr = codes + r * (int64_t)(bits == 8 ? D : D / 2);
+        float lo = meta[2 * r], S = meta[2 * r + 1];
+        for (int d = 0; d < D; ++d) {
+            int q = bits == 8 ? cr[d] : (cr[d / 2] >> ((d & 1) ? 4 : 0)) & 0xf;
+            out[r * D + d] = fmaf((float)q, S, lo);
+        }
+    }
+    return 0;
+}
+
 /* ------------------------------------------------------------ attention */
 
 /*

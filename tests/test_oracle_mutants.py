@@ -34,10 +34,17 @@ MUTANTS = [
      "float mu = v[0] * (1.0f / (float)(C + 1));"),
     ("sigma without abs", "float ad = fabsf(dd);", "float ad = dd;"),
     ("sign flipped", "int S = dd >= 0.0f ? 1 : -1;", "int S = dd >= 0.0f ? -1 : 1;"),
-    ("decode chunk index wrong", "int c = t / C;", "int c = t % (P / C);"),
+    ("decode chunk index wrong", "int c = t / C;\n        for (int d = 0; d < D; ++d) {\n            size_t byte",
+     "int c = t % (P / C);\n        for (int d = 0; d < D; ++d) {\n            size_t byte"),
+    ("k-bit decode chunk index wrong",
+     "int c = t / C;\n        for (int d = 0; d < D; ++d) {\n            const uint8_t *pa",
+     "int c = t % (P / C);\n        for (int d = 0; d < D; ++d) {\n            const uint8_t *pa"),
     ("anchor bucket point 16V", "I = 16 * V + 7;", "I = 16 * V;"),
-    ("decode sigma without eps", "float nv = fmaf(xf, sg + ORACLE_EPS, mu);",
-     "float nv = fmaf(xf, sg, mu);"),
+    ("decode sigma without eps", "float nv = fmaf(xf, sg + ORACLE_EPS, mu);\n            float xv",
+     "float nv = fmaf(xf, sg, mu);\n            float xv"),
+    ("k-bit decode sigma without eps",
+     "float nv = fmaf(xf, sg + ORACLE_EPS, mu);\n            out[(int64_t)t",
+     "float nv = fmaf(xf, sg, mu);\n            out[(int64_t)t"),
     ("decode affine operands transposed",
      "float xv = fmaf(nv, g_scale[d] + ORACLE_EPS, g_min[d]);",
      "float xv = fmaf(nv, g_min[d] + ORACLE_EPS, g_scale[d]);"),
@@ -59,6 +66,20 @@ MUTANTS = [
     ("draft tokens take the cached values",
      "const float *v = t < L ? V + t * kv_stride : Vt + (t - L) * tail_stride;",
      "const float *v = t < L ? V + t * kv_stride : V + (t - L) * kv_stride;"),
+    ("INT-B rounds down", "float qf = rintf(dd * rs);", "float qf = floorf(dd * rs);"),
+    ("INT-B decode drops the minimum", "out[r * D + d] = fmaf((float)q, S, lo);",
+     "out[r * D + d] = fmaf((float)q, S, 0.0f);"),
+    ("INT-B with 2^B levels", "const int qmax = (1 << bits) - 1;", "const int qmax = (1 << bits);"),
+    ("INT-4 nibbles swapped", "cr[d / 2] |= (uint8_t)(q << ((d & 1) ? 4 : 0));",
+     "cr[d / 2] |= (uint8_t)(q << ((d & 1) ? 0 : 4));"),
+    ("INT-B scale from the maximum alone", "float S = (hi - lo) / (float)qmax;",
+     "float S = hi / (float)qmax;"),
+    ("k-bit Anchor shifted by k", "field_put(pa, d % 8, k, (q8 >> rw) & ((1 << k) - 1));",
+     "field_put(pa, d % 8, k, (q8 >> k) & ((1 << k) - 1));"),
+    ("k-bit bucket point without the -1", "int I = (1 << (8 - k)) * V + (1 << (7 - k)) - 1;",
+     "int I = (1 << (8 - k)) * V + (1 << (7 - k));"),
+    ("bit fields written high bit first", "uint8_t m = (uint8_t)(1u << (b & 7));",
+     "uint8_t m = (uint8_t)(1u << (7 - (b & 7)));"),
 ]
 
 # representative arguments for the parametrized pins

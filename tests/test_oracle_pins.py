@@ -601,3 +601,165 @@ def test_effective_bins_example(oracle_mod):
     g = golden("size_examples.json")["effective_bins"]
     assert abs(oracle_mod.effective_bins(g["B"], 1 / g["m_over_m_i"])
                - g["printed_bins"]) < 1e-12
+
+
+# ----------------------------------------------------------- bit splits
+
+def _fields(packed, w):
+    """Little-endian w-bit fields of each aligned group of 8 channels:
+    [rows][D*w/8] bytes -> [rows][D] unsigned values."""
+    rows, nbytes = packed.shape
+    groups = nbytes // w
+    out = np.zeros((rows, groups * 8), np.int64)
+    for g in range(groups):
+        word = np.zeros(rows, np.int64)
+        for i in range(w):
+            word |= packed[:, g * w + i].astype(np.int64) << (8 * i)
+        for j in range(8):
+            out[:, g * 8 + j] = (word >> (j * w)) & ((1 << w) - 1)
+    return out
+
+
+def test_bit_splits_recompose_the_code(oracle_mod):
+    """Concrete Improvement Suggestions, items 4-5 (splits 3+5 .. 6+2): for
+    every split, Anchor << (8-k) | Residual is the same signed 8-bit code,
+    the Anchor is its arithmetic top k bits, and k = 4 gives the 4+4
+    Anchor of Stage 4."""
+    P = 64
+    bits = _random_block(11, P=P)
+    anc, res, meta = oracle_mod.encode(bits.reshape(1, P, 1, 128), P, 16, ALPHA)
+    q8 = _signed_codes(anc.reshape(P, 64), res.reshape(P, 64))
+    assert set(np.unique(q8 & 0xFF)) == set(range(256)) or len(np.unique(q8)) > 200
+    for k in (3, 4, 5, 6):
+        ak, rk = oracle_mod.split_bits(anc, res, k)
+        assert ak.shape[-1] == 128 * k // 8 and rk.shape[-1] == 128 * (8 - k) // 8
+        a = _fields(ak.reshape(P, -1), k)
+        r = _fields(rk.reshape(P, -1), 8 - k)
+        a_signed = np.where(a >= 1 << (k - 1), a - (1 << k), a)
+        assert np.array_equal(a_signed, q8 >> (8 - k))            # arithmetic shift
+        assert np.array_equal(a_signed * (1 << (8 - k)) + r, q8)
+        if k == 4:
+            assert np.array_equal(a_signed, q8 >> 4)
+
+
+def test_k_bit_anchor_decode_is_the_bucket_point(oracle_mod):
+    """Anchor-only reconstruction of a k-bit Anchor is the full decode of the
+    code whose residual is the bucket point: 2^(7-k) - 1 below a
+    non-negative Anchor (I_rep = 2^(8-k) V + 2^(7-k) - 1), 2^(7-k) below a
+    negative one (the same magnitude, Eq. 9's sign map).  k = 4 is the
+    Anchor decode of Stage 4 (16 V + 7)."""
+    P, C = 64, 16
+    bits = _random_block(12, P=P)
+    anc, res, meta = oracle_mod.encode(bits.reshape(1, P, 1, 128), P, C, ALPHA)
+    q8 = _signed_codes(anc.reshape(P, 64), res.reshape(P, 64))
+    for k in (3, 4, 5, 6):
+        ak, _ = oracle_mod.split_bits(anc, res, k)
+        got = oracle_mod.decode_anchor_bits(ak, meta, P, P, C, ALPHA, k)
+        a = q8 >> (8 - k)
+        rep = a * (1 << (8 - k)) + np.where(a >= 0, (1 << (7 - k)) - 1, 1 << (7 - k))
+        u = (rep & 0xFF).astype(np.uint8)
+        # back to the 4+4 nibble streams (byte 4G+j: channels 8G+j, 8G+j+4)
+        u = u.reshape(P, 16, 8)
+        a4 = ((u[:, :, 0:4] >> 4) | (u[:, :, 4:8] & 0xF0)).reshape(1, 1, 1, P, 64)
+        r4 = ((u[:, :, 0:4] & 0xF) | ((u[:, :, 4:8] & 0xF) << 4)).reshape(1, 1, 1, P, 64)
+        want = oracle_mod.decode(a4.astype(np.uint8), r4.astype(np.uint8), meta, P, P, C, ALPHA)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), k
+        if k == 4:
+            plain = oracle_mod.decode(anc, None, meta, P, P, C, ALPHA)
+            assert np.array_equal(got.view(np.uint32), plain.view(np.uint32))
+
+
+# ----------------------------------------------------------- INT-B baseline
+
+def test_int_baseline_grid_rows_round_trip(oracle_mod):
+    """Eq. 4 on rows whose range is exactly 2^B - 1: S = 1, Z = -x_min, so
+    every integer value is its own code and decodes exactly; nibble j of a
+    B = 4 row is channel 2j (low) then 2j + 1 (high)."""
+    d = np.arange(128)
+    # every value has at most 8 significant bits, so it is exact in BF16
+    rows = {4: (d % 16).astype(np.float32) - 3.0,
+            8: np.where(d == 127, 255, 2 * d).astype(np.float32) - 100.0}
+    for B, x in rows.items():
+        xb = oracle_mod.f32_to_bf16_bits(x).reshape(1, 128)
+        codes, meta = oracle_mod.int_encode(xb, B)
+        assert meta[0, 0] == x.min() and meta[0, 1] == 1.0
+        q = codes[0] if B == 8 else np.stack([codes[0] & 0xF, codes[0] >> 4], 1).reshape(-1)
+        assert np.array_equal(q.astype(np.float32), x - x.min())
+        assert np.array_equal(oracle_mod.int_decode(codes, meta, B)[0], x)
+    x = np.zeros(128, np.float32)
+    x[0], x[1] = 15.0, 0.0
+    x[2:] = 7.0
+    codes, _ = oracle_mod.int_encode(oracle_mod.f32_to_bf16_bits(x).reshape(1, 128), 4)
+    assert codes[0, 0] == 0x0F
+
+
+def test_int_baseline_error_bound_and_extremes(oracle_mod):
+    """|x^ - x| <= S/2 (+ float32 rounding); the row minimum codes to 0 and
+    the maximum to 2^B - 1; a constant row (S = 0) codes to 0 and decodes
+    exactly; a zero minimum is stored as +0."""
+    rng = np.random.default_rng(3)
+    x = (rng.laplace(size=(64, 128)) * np.exp(rng.standard_normal((64, 1)))).astype(np.float32)
+    xb = oracle_mod.f32_to_bf16_bits(x)
+    xf = oracle_mod.bf16_bits_to_f32(xb)
+    for B in (4, 8):
+        codes, meta = oracle_mod.int_encode(xb, B)
+        y = oracle_mod.int_decode(codes, meta, B)
+        S = meta[:, 1:2].astype(np.float64)
+        err = np.abs(y.astype(np.float64) - xf)
+        assert (err <= S / 2 * (1 + 1e-5) + np.abs(xf) * 2.0 ** -22).all()
+        q = codes if B == 8 else np.stack([codes & 0xF, codes >> 4], -1).reshape(64, 128)
+        assert (q[np.arange(64), xf.argmin(1)] == 0).all()
+        assert (q[np.arange(64), xf.argmax(1)] == (1 << B) - 1).all()
+    c = oracle_mod.f32_to_bf16_bits(np.full((2, 128), -2.5, np.float32))
+    z = oracle_mod.f32_to_bf16_bits(np.where(np.arange(128) % 2 == 0, -0.0, 0.0)
+                                    .astype(np.float32).reshape(1, 128))
+    for B in (4, 8):
+        codes, meta = oracle_mod.int_encode(c, B)
+        assert (codes == 0).all() and meta[0, 1] == 0.0
+        assert (oracle_mod.int_decode(codes, meta, B) == -2.5).all()
+        _, mz = oracle_mod.int_encode(z, B)
+        assert mz[0, 0].view(np.uint32) == 0
+
+
+def test_int_baseline_outlier_starves_ordinary_channels(oracle_mod):
+    """Eq. 5: with one channel about 100x the others, the ordinary channels
+    of a row share about 2^B m_i / m bins (2.56 for INT8 at m = 100 m_i)."""
+    rng = np.random.default_rng(9)
+    x = rng.uniform(-1, 1, size=(256, 128)).astype(np.float32)
+    x[:, 5] = 100.0
+    xb = oracle_mod.f32_to_bf16_bits(x)
+    for B in (8, 4):
+        codes, meta = oracle_mod.int_encode(xb, B)
+        q = codes if B == 8 else np.stack([codes & 0xF, codes >> 4], -1).reshape(256, 128)
+        ordinary = np.delete(q, 5, axis=1)
+        used = np.array([len(np.unique(r)) for r in ordinary])
+        span = (1 << B) * 2.0 / 101.0       # the ordinary range 2 of a row range ~101
+        assert used.max() <= math.ceil(span) + 1
+        assert used.min() >= 1
+    assert abs(oracle_mod.effective_bins(8, 1 / 100) - 2.56) < 1e-12
+
+
+# ----------------------------------------------------------- vNMSE
+
+def test_vnmse_closed_forms(oracle_mod):
+    rng = np.random.default_rng(4)
+    r = rng.standard_normal((3, 5, 128))
+    assert oracle_mod.vnmse(r, r) == 0.0
+    assert abs(oracle_mod.vnmse(2 * r, r) - 1.0) < 1e-12
+    assert abs(oracle_mod.vnmse(np.zeros_like(r), r) - 1.0) < 1e-12
+    assert abs(oracle_mod.vnmse(r + 0.1 * r, r) - 0.01) < 1e-12
+
+
+def test_attention_rows_gqa_mapping(oracle_mod):
+    """Query head h reads KV head h // (H_q / H_kv): with each KV head's
+    values constant (c_h), every output of query head j is c_{j // G}."""
+    rng = np.random.default_rng(6)
+    B, L, Hkv, G, T = 2, 16, 3, 2, 2
+    K = rng.standard_normal((B, L, Hkv, 128)).astype(np.float32)
+    c = np.arange(1, B * Hkv + 1, dtype=np.float32).reshape(B, 1, Hkv, 1)
+    V = np.broadcast_to(c, (B, L, Hkv, 128)).astype(np.float32)
+    q = rng.standard_normal((B, T, Hkv * G, 128)).astype(np.float32)
+    o = oracle_mod.attention_rows(q, K, V)
+    for b in range(B):
+        for j in range(Hkv * G):
+            assert np.allclose(o[b, :, j], c[b, 0, j // G, 0], rtol=0, atol=1e-12)
