@@ -472,7 +472,7 @@ int oracle_decode_anchor_bits_range(const uint8_t *ak, const float *meta, int64_
  * the division taken as a multiplication by the correctly rounded float32
  * reciprocal of S (of 0 for a constant row, S = 0: every code is then 0);
  * round to nearest, ties to even; Q clamped to [0, 2^B - 1]; a zero x_min
- * is stored as +0.  Reconstruction
+ * or x_max counts as +0 (so S of an all-zero row is +0).  Reconstruction
  * x = Q * S + x_min in one fused multiply-add.  B = 8: one byte a value;
  * B = 4: byte j holds channels 2j (low nibble) and 2j+1 (high nibble).
  * meta: (x_min, S) float32 per row.
@@ -491,6 +491,7 @@ int oracle_int_encode_rows(const uint16_t *x, int64_t rows, int D, int bits, uin
             if (v > hi) hi = v;
         }
         lo = lo + 0.0f;
+        hi = hi + 0.0f;
         float S = (hi - lo) / (float)qmax;
         float rs = S > 0.0f ? 1.0f / S : 0.0f;
         uint8_t *cr = codes + r * (int64_t)(bits == 8 ? D : D / 2);

@@ -718,7 +718,7 @@ def test_int_baseline_error_bound_and_extremes(oracle_mod):
         assert (codes == 0).all() and meta[0, 1] == 0.0
         assert (oracle_mod.int_decode(codes, meta, B) == -2.5).all()
         _, mz = oracle_mod.int_encode(z, B)
-        assert mz[0, 0].view(np.uint32) == 0
+        assert mz[0, 0].view(np.uint32) == 0 and mz[0, 1].view(np.uint32) == 0
 
 
 def test_int_baseline_outlier_starves_ordinary_channels(oracle_mod):
