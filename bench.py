@@ -466,6 +466,15 @@ def run_lynx(args, rank, world, dev):
     if extras is not None:
         extras["split_stream"] = measure_split(kv, kv_h, (anc, res, meta),
                                                (anc_h, res_h, meta_h), dec_a, dev)
+        extras["variants"] = measure_variants(kv, anc, res, meta, dev)
+        kva = synth.kv_cache(4, a["L"], a["H_kv"], a["D"], seed=5 + rank, device=dev)
+        qa = synth.queries(2, a["T_verify"], a["H_q"], a["D"], seed=8, device=dev)
+        extras["accuracy"] = accuracy_table(kva[0::2].contiguous(), kva[1::2].contiguous(), qa,
+                                            a["P"], a["C"], ALPHA)
+        extras["accuracy"]["what"] = (
+            "vNMSE of attention outputs (2 sequences x 32768 tokens x 8 KV heads, 8 query "
+            "tokens x 32 heads) against attention over the BF16 KV; codecs on the GPU")
+        del kva
     assert lynx.lynx_wait_timeouts() == 0
     return dict(ms_total=ms_total, row_ms=row_ms, e2e_s=e2e_s, h2d=h2d, d2h=d2h, clocks=clk,
                 launches=launches, extras=extras)
@@ -551,6 +560,137 @@ def measure_extras(ks, vs, q8, ws, dev, reps=10):
     out["spec_verify"] = entry(ms, rows_read * V * 4,
                                what=f"Eq. 10-11: batch {B}, T={T}, V={V}; mean accepted "
                                     f"{float(k.float().mean()):.2f} of {T}")
+    return out
+
+
+def _attention_f64(q, K, V):
+    """softmax(q K^T / sqrt(D)) V in float64 on the device, for the accuracy
+    table only (GQA: query head h reads KV head h // (H_q / H_kv))."""
+    import torch
+    B, T, Hq, D = q.shape
+    Hkv = K.shape[2]
+    qf = q.double().view(B, T, Hkv, Hq // Hkv, D)
+    s = torch.einsum("bthgd,blhd->bhtgl", qf, K.double()) / math.sqrt(D)
+    p = torch.softmax(s, dim=-1)
+    return torch.einsum("bhtgl,blhd->bthgd", p, V.double()).reshape(B, T, Hq, D)
+
+
+def accuracy_table(K, V, q, P=128, C=32, alpha=255.0, sweep=True):
+    """vNMSE of the attention output (the metric of the pages' Table 3,
+    [Review], Mechanism 3) for each codec, against attention over the BF16
+    K and V: the linear INT8 / INT4 baselines (Eq. 4), the full Lynx code,
+    and its Anchor alone at every bit split.  The codecs run through the
+    library's kernels; only this evaluation's attention is plain float64.
+    With `sweep`, the full code and the 4-bit Anchor over alpha x C x page.
+    Bytes per element count the codes and their metadata."""
+    import torch
+
+    from split_stream_kv_gb300 import lynx
+    L = K.shape[1]
+    ref = _attention_f64(q, K, V)
+    den = float((ref * ref).sum())
+
+    def vn(Kh, Vh):
+        o = _attention_f64(q, Kh, Vh)
+        return float(((o - ref) ** 2).sum()) / den
+
+    table = {}
+    for bits in (8, 4):
+        Kh = lynx.lynx_int_decode(*lynx.lynx_int_encode(K, bits), bits)
+        Vh = lynx.lynx_int_decode(*lynx.lynx_int_encode(V, bits), bits)
+        table[f"int{bits}"] = {"vnmse": vn(Kh, Vh), "bytes_per_elem": bits / 8 + 8 / 128}
+
+    def lynx_rows(P_, C_, a_, splits):
+        ks = lynx.lynx_encode(K, P_, C_, a_)
+        vs = lynx.lynx_encode(V, P_, C_, a_)
+        meta_b = 8 / P_ + 8 / C_
+        out = {"full": {"vnmse": vn(lynx.lynx_decode_full(*ks, L, P_, C_, a_),
+                                    lynx.lynx_decode_full(*vs, L, P_, C_, a_)),
+                        "bytes_per_elem": 1 + meta_b}}
+        for k in splits:
+            kk, _ = lynx.lynx_split_bits(ks[0], ks[1], k)
+            vk, _ = lynx.lynx_split_bits(vs[0], vs[1], k)
+            out[k] = {"vnmse": vn(lynx.lynx_decode_anchor_bits(kk, ks[2], L, P_, C_, a_, k),
+                                  lynx.lynx_decode_anchor_bits(vk, vs[2], L, P_, C_, a_, k)),
+                      "anchor_bytes_per_elem": k / 8 + meta_b,
+                      "total_bytes_per_elem": 1 + meta_b}
+        return out
+
+    rows = lynx_rows(P, C, alpha, (3, 4, 5, 6))
+    table["lynx_full"] = rows["full"]
+    for k in (3, 4, 5, 6):
+        table[f"lynx_anchor_{k}bit"] = rows[k]
+    if sweep:
+        sw = []
+        for a_ in (100.0, 500.0, 2000.0):
+            for C_ in (16, 32, 64):
+                for P_ in (128, 256):
+                    r = lynx_rows(P_, C_, a_, (4,))
+                    sw.append({"alpha": a_, "C": C_, "page": P_,
+                               "full_vnmse": r["full"]["vnmse"],
+                               "anchor4_vnmse": r[4]["vnmse"],
+                               "anchor_bytes_per_elem": r[4]["anchor_bytes_per_elem"]})
+        table["sweep"] = sw
+    torch.cuda.synchronize()
+    return table
+
+
+def measure_variants(kv, anc, res, meta, dev, reps=5):
+    """HBM throughput of the comparison-point kernels on the codec workload:
+    INT8 / INT4 encode and decode, the 6+2 and 3+5 re-splits and the k-bit
+    Anchor decode.  Algorithmic bytes: what each kernel must read and write."""
+    import statistics
+
+    import torch
+
+    from split_stream_kv_gb300 import lynx
+    c = CODEC
+    n = kv.numel()
+    peak = load_peaks()[0]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 2):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if i >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    out = {}
+
+    def row(name, fn, nbytes):
+        ms = timed(fn)
+        gbps = nbytes / ms / 1e6
+        out[name] = {"ms": round(ms, 4), "algorithmic_bytes": int(nbytes),
+                     "achieved_GBps": round(gbps, 1),
+                     "roofline_frac": round(gbps / peak, 4) if peak else None}
+
+    meta_b = n * (8 / c["P"] + 8 / c["C"])
+    for bits in (8, 4):
+        codes, m = lynx.lynx_int_encode(kv, bits)
+        dec = torch.empty_like(kv)
+        row(f"int{bits}_encode", lambda: lynx.lynx_int_encode(kv, bits, codes, m),
+            n * (2 + bits / 8 + 8 / 128))
+        row(f"int{bits}_decode", lambda: lynx.lynx_int_decode(codes, m, bits, out=dec),
+            n * (bits / 8 + 8 / 128 + 2))
+        del codes, m, dec
+    for k in (6, 3):
+        ak, rk = lynx.lynx_split_bits(anc, res, k)
+        row(f"split_{k}+{8 - k}", lambda: lynx.lynx_split_bits(anc, res, k, ak, rk), n * 2)
+        dec = torch.empty_like(kv)
+        row(f"decode_anchor_{k}bit",
+            lambda: lynx.lynx_decode_anchor_bits(ak, meta, c["L"], c["P"], c["C"], ALPHA, k,
+                                                 out=dec),
+            n * (k / 8 + 2) + meta_b)
+        del ak, rk, dec
+    del flush
     return out
 
 

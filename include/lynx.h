@@ -249,6 +249,49 @@ int lynx_header_init(lynx_header *h, int64_t B, int64_t L, int H_kv, int D,
  * sizes) or the codes of lynx_encode for bad dimensions otherwise. */
 int lynx_header_check(const lynx_header *h);
 
+/* ---------------------------------------------------------------------
+ * Comparison points.
+ *
+ * Linear INT-B baseline [Review, Prerequisites, Eq. 4: Q(x) = round(x/S +
+ * Z), S = (x_max - x_min)/(2^B - 1)], the INT8 / INT4 of the pages' tables:
+ * one (S, Z) per row of D = 128 channels (a token of one KV head), Z =
+ * -x_min/S, Q = round((x - x_min) * rcp(S)) to nearest even, clamped to
+ * [0, 2^B - 1] (rcp(0) = 0: a constant row codes to 0); a zero extreme
+ * counts as +0.  Decode: x = fma(Q, S, x_min).
+ *   kv     [rows][128] BF16 (a [B][L][H_kv][128] tensor has rows = B*L*H_kv)
+ *   codes  [rows][128 * bits / 8] uint8; bits = 4: byte j holds channels 2j
+ *          (low nibble) and 2j+1 (high nibble)
+ *   meta   [rows][2] float32: (x_min, S)
+ *   out    [rows][128] BF16 or float32 (out_dtype)
+ * bits must be 4 or 8; device pointers, 16-byte aligned; one pass each,
+ * enqueued on `stream`. */
+int lynx_int_encode(const void *kv, int64_t rows, int D, int bits, void *codes,
+                    float *meta, void *stream);
+int lynx_int_decode(const void *codes, const float *meta, int64_t rows, int D,
+                    int bits, void *out, int out_dtype, void *stream);
+
+/* Other Anchor/Residual bit splits [Review, Concrete Improvement
+ * Suggestions, items 4-5: 3+5, 4+4, 5+3, 6+2].  The code is the same signed
+ * 8-bit Q8; a k-bit Anchor is its arithmetic top k bits and the Residual its
+ * low 8-k bits.  Layout of a k-split: per token row and aligned group of 8
+ * channels 8G..8G+7, k Anchor bytes and 8-k Residual bytes, channel 8G+j in
+ * bits j*w .. j*w + w - 1 (w the field width) of the group's bytes read as
+ * one little-endian integer; page blocks in the (b, page, head) order of the
+ * 4+4 streams.  rows = B * L * H_kv token rows.
+ * lynx_split_bits re-splits 4+4 streams; lynx_join_bits is its inverse. */
+int lynx_split_bits(const void *anchor, const void *residual, int64_t rows,
+                    int D, int k, void *anchor_k, void *residual_k,
+                    void *stream);
+int lynx_join_bits(const void *anchor_k, const void *residual_k, int64_t rows,
+                   int D, int k, void *anchor, void *residual, void *stream);
+/* Anchor-only decode of a k-bit Anchor stream, 3 <= k <= 6: bucket point
+ * I = 2^(8-k) V + 2^(7-k) - 1 (16 V + 7 for k = 4), then the
+ * reconstruction of lynx_decode_anchor; out as lynx_decode_anchor. */
+int lynx_decode_anchor_bits(const void *anchor_k, const float *meta, int64_t B,
+                            int64_t L, int H_kv, int D, int page, int C,
+                            float alpha, int k, void *out, int out_dtype,
+                            void *stream);
+
 /* Speculative verification and correction [Review, Mechanism 3, Eq. 10 and
  * Eq. 11], for every sequence b of the batch, on distributions the caller's
  * verification pass (p, over the full KV) and draft steps (q, over the

@@ -46,6 +46,10 @@ cudaError_t launch_encode(const void* kv, const Shape& s, const CompanderTable& 
 cudaError_t launch_decode(const void* anchor, const void* residual, const float* meta,
                           const Shape& s, const ExpandTable& tab, void* out, bool bf16_out,
                           cudaStream_t stream, const Paging& pg = Paging());
+// Anchor-only decode of a k-bit Anchor stream (3 <= k <= 6), see variants.cu.
+cudaError_t launch_decode_anchor_bits(const void* anchor_k, const float* meta, const Shape& s,
+                                      int k, const ExpandTable& tab, void* out, bool bf16_out,
+                                      cudaStream_t stream);
 cudaError_t launch_compander_selfcheck(const CompanderTable& tab, uint64_t* counts,
                                        cudaStream_t stream);
 

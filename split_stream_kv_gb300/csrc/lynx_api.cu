@@ -276,6 +276,24 @@ int lynx_decode_full(const void* anchor, const void* residual, const float* meta
                        stream, "lynx_decode_full");
 }
 
+int lynx_decode_anchor_bits(const void* anchor_k, const float* meta, int64_t B, int64_t L,
+                            int H_kv, int D, int page, int C, float alpha, int k, void* out,
+                            int out_dtype, void* stream) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, C);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if (k < 3 || k > 6) return fail(LYNX_EUNSUPPORTED, "k = %d: built for 3..6", k);
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)
+    return fail(LYNX_EINVAL, "out_dtype must be LYNX_OUT_BF16 or LYNX_OUT_FP32");
+  if (B * L == 0) return LYNX_OK;
+  if ((rc = check_ptrs({anchor_k, meta, out}))) return rc;
+  Shape s{B, L, H_kv, D, page, C};
+  cudaError_t e = launch_decode_anchor_bits(anchor_k, meta, s, k, tables_for(alpha).expand, out,
+                                            out_dtype == LYNX_OUT_BF16,
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_decode_anchor_bits");
+}
+
 static int check_attn_shape(int batch, int T, int H_q, int64_t L, int H_kv, int D, int page,
                             int C) {
   int rc = check_codec_shape(batch, L, H_kv, D, page, C);

@@ -1,0 +1,402 @@
+// variants.cu -- the comparison points of "Lynx: Progressive Speculative KV
+// Cache Transfer for Disaggregated LLM Inference" (technical review):
+//
+//  * the linear INT-B quantizer of Prerequisites Eq. 4 (the INT8 / INT4
+//    baselines of the pages' tables), one scale and zero point per token and
+//    KV head over its 128 channels;
+//  * other Anchor/Residual bit splits (Concrete Improvement Suggestions,
+//    items 4-5: 3+5, 5+3, 6+2): a re-split of the 4+4 streams into a k-bit
+//    Anchor and an (8-k)-bit Residual of the same signed 8-bit code, the
+//    inverse join, and the Anchor-only decode of a k-bit Anchor.
+//
+// All of it is streaming work, one pass over HBM: a warp per token row for
+// INT-B (lane = 4 channels), a thread per (token, group of 8 channels) for
+// the bit splits.  Grids are sized in whole waves of the SMs.
+#include "common.cuh"
+#include "internal.h"
+#include "lynx.h"
+
+namespace lynx {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+               : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+
+// ----------------------------------------------------------------- INT-B
+
+// One token row of 128 BF16 channels per warp, 4 channels a lane; R rows in
+// flight per warp.
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) int_encode_kernel(const uint8_t* __restrict__ x,
+                                                              const int64_t rows,
+                                                              uint8_t* __restrict__ codes,
+                                                              float2* __restrict__ meta) {
+  constexpr int R = 4;
+  constexpr int qmax = (1 << BITS) - 1;
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  for (int64_t r0 = warp * R; r0 < rows; r0 += nwarps * R) {
+    uint2 v[R];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+      v[i] = r0 + i < rows ? ldg_stream8(x + (r0 + i) * 256 + lane * 8) : make_uint2(0u, 0u);
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int64_t row = r0 + i;
+      if (row >= rows) break;  // uniform across the warp
+      const float f[4] = {bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y)};
+      float lo = fminf(fminf(f[0], f[1]), fminf(f[2], f[3]));
+      float hi = fmaxf(fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(kFull, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, o));
+      }
+      lo = __fadd_rn(lo, 0.0f);  // a zero extreme counts as +0
+      hi = __fadd_rn(hi, 0.0f);
+      const float S = __fdiv_rn(__fsub_rn(hi, lo), (float)qmax);
+      const float rs = S > 0.0f ? __frcp_rn(S) : 0.0f;
+      uint32_t q[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        int c = __float2int_rn(__fmul_rn(__fsub_rn(f[j], lo), rs));
+        q[j] = (uint32_t)(c < 0 ? 0 : c > qmax ? qmax : c);
+      }
+      if constexpr (BITS == 8) {
+        *reinterpret_cast<uint32_t*>(codes + row * 128 + lane * 4) =
+            q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+      } else {
+        *reinterpret_cast<uint16_t*>(codes + row * 64 + lane * 2) =
+            (uint16_t)(q[0] | (q[1] << 4) | (q[2] << 8) | (q[3] << 12));
+      }
+      if (lane == 0) meta[row] = make_float2(lo, S);
+    }
+  }
+}
+
+template <int BITS, bool BF16OUT>
+__global__ void __launch_bounds__(kThreads) int_decode_kernel(const uint8_t* __restrict__ codes,
+                                                              const float2* __restrict__ meta,
+                                                              const int64_t rows,
+                                                              void* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+  for (int64_t row = warp; row < rows; row += nwarps) {
+    uint32_t q[4];
+    if constexpr (BITS == 8) {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(codes + row * 128 + lane * 4));
+      q[0] = w & 0xff; q[1] = (w >> 8) & 0xff; q[2] = (w >> 16) & 0xff; q[3] = w >> 24;
+    } else {
+      const uint32_t w = __ldg(reinterpret_cast<const uint16_t*>(codes + row * 64 + lane * 2));
+      q[0] = w & 0xf; q[1] = (w >> 4) & 0xf; q[2] = (w >> 8) & 0xf; q[3] = (w >> 12) & 0xf;
+    }
+    const float2 m = __ldg(meta + row);
+    float y[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) y[j] = __fmaf_rn((float)q[j], m.y, m.x);
+    if constexpr (BF16OUT) {
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(out) + row * 256 + lane * 8) =
+          make_uint2(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]));
+    } else {
+      *reinterpret_cast<float4*>(static_cast<uint8_t*>(out) + row * 512 + lane * 16) =
+          make_float4(y[0], y[1], y[2], y[3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------- bit splits
+
+// The signed 8-bit codes of one group of 8 channels (8G..8G+7) of one token
+// from the 4+4 nibble streams: byte j of the group holds channel 8G+j (low
+// nibble) and 8G+j+4 (high nibble).  code j in byte j of the result.
+__device__ __forceinline__ uint64_t group_codes(uint32_t a, uint32_t r) {
+  const uint32_t lo = ((a << 4) & 0xf0f0f0f0u) | (r & 0x0f0f0f0fu);  // channels 8G+0..3
+  const uint32_t hi = (a & 0xf0f0f0f0u) | ((r >> 4) & 0x0f0f0f0fu);  // channels 8G+4..7
+  return (uint64_t)lo | ((uint64_t)hi << 32);
+}
+
+// One thread per (token row, group): the k-bit fields of the 8 codes'
+// top bits into K bytes, the low 8-K bits into 8-K bytes (channel j at bits
+// j*w .. j*w + w - 1, little-endian).
+template <int K>
+__global__ void __launch_bounds__(kThreads) split_bits_kernel(const uint8_t* __restrict__ anchor,
+                                                              const uint8_t* __restrict__ residual,
+                                                              const int64_t groups,
+                                                              uint8_t* __restrict__ ak,
+                                                              uint8_t* __restrict__ rk) {
+  constexpr int RW = 8 - K;
+  for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < groups;
+       gi += (int64_t)gridDim.x * kThreads) {
+    const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(anchor) + gi);
+    const uint32_t r = __ldg(reinterpret_cast<const uint32_t*>(residual) + gi);
+    const uint64_t c = group_codes(a, r);
+    uint64_t fa = 0, fr = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t q8 = (uint32_t)(c >> (8 * j)) & 0xffu;
+      fa |= (uint64_t)(q8 >> RW) << (j * K);
+      fr |= (uint64_t)(q8 & ((1u << RW) - 1u)) << (j * RW);
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i) ak[gi * K + i] = (uint8_t)(fa >> (8 * i));
+#pragma unroll
+    for (int i = 0; i < RW; ++i) rk[gi * RW + i] = (uint8_t)(fr >> (8 * i));
+  }
+}
+
+template <int K>
+__global__ void __launch_bounds__(kThreads) join_bits_kernel(const uint8_t* __restrict__ ak,
+                                                             const uint8_t* __restrict__ rk,
+                                                             const int64_t groups,
+                                                             uint32_t* __restrict__ anchor,
+                                                             uint32_t* __restrict__ residual) {
+  constexpr int RW = 8 - K;
+  for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < groups;
+       gi += (int64_t)gridDim.x * kThreads) {
+    uint64_t fa = 0, fr = 0;
+#pragma unroll
+    for (int i = 0; i < K; ++i) fa |= (uint64_t)__ldg(ak + gi * K + i) << (8 * i);
+#pragma unroll
+    for (int i = 0; i < RW; ++i) fr |= (uint64_t)__ldg(rk + gi * RW + i) << (8 * i);
+    uint32_t a = 0, r = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t q8 = ((uint32_t)(fa >> (j * K)) & ((1u << K) - 1u)) << RW |
+                          ((uint32_t)(fr >> (j * RW)) & ((1u << RW) - 1u));
+      const int sh = 8 * (j & 3) + ((j & 4) ? 4 : 0);  // byte j&3, high nibble for j >= 4
+      a |= (q8 >> 4) << sh;
+      r |= (q8 & 15u) << sh;
+    }
+    anchor[gi] = a;
+    residual[gi] = r;
+  }
+}
+
+// Anchor-only decode of a K-bit Anchor: one thread per (run of kRun tokens,
+// group of 8 channels), the same reconstruction as the 4+4 Anchor decoder
+// with the bucket point I = 2^(8-K) V + 2^(7-K) - 1.  A run lies in one
+// chunk (C >= 16), so its 32 constants load once for kRun tokens.
+constexpr int kRun = 8;
+
+template <int K, bool BF16OUT>
+__global__ void __launch_bounds__(kThreads)
+decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restrict__ meta,
+                          const int64_t nblk, const int64_t NB, const int H, const int64_t L,
+                          const int P, const int C, void* __restrict__ out,
+                          const __grid_constant__ ExpandTable tab) {
+  __shared__ float x[128];
+  for (int i = threadIdx.x; i < 128; i += kThreads) x[i] = tab.x[i];
+  __syncthreads();
+  const int NC = P / C, meta_rows = 2 + 2 * NC;
+  const int runs = P / kRun;
+  const int64_t items = nblk * runs * 16;
+  for (int64_t it = (int64_t)blockIdx.x * kThreads + threadIdx.x; it < items;
+       it += (int64_t)gridDim.x * kThreads) {
+    const int G = (int)(it & 15);
+    const int64_t rr = it >> 4;                     // run index in block order
+    const int t0 = (int)(rr % runs) * kRun;
+    const int64_t blk = rr / runs;
+    const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
+    const float* mb = meta + blk * (int64_t)meta_rows * kD + 8 * G;
+    const int c = t0 / C;
+    float gm[8], gs[8], mu[8], sg[8];
+    auto row8 = [&](const float* r, float (&v)[8]) {
+      const float4 u0 = __ldg(reinterpret_cast<const float4*>(r));
+      const float4 u1 = __ldg(reinterpret_cast<const float4*>(r) + 1);
+      v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
+      v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
+    };
+    row8(mb, gm);
+    row8(mb + kD, gs);
+    row8(mb + (2 + c) * kD, mu);
+    row8(mb + (2 + NC + c) * kD, sg);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      gs[j] = __fadd_rn(gs[j], kEps);
+      sg[j] = __fadd_rn(sg[j], kEps);
+    }
+    const uint8_t* src = ak + ((blk * P + t0) * 16 + G) * K;
+#pragma unroll 2
+    for (int u = 0; u < kRun; ++u) {
+      uint64_t fa = 0;
+#pragma unroll
+      for (int i = 0; i < K; ++i) fa |= (uint64_t)__ldg(src + u * 16 * K + i) << (8 * i);
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        int a = (int)((fa >> (j * K)) & ((1u << K) - 1u));
+        if (a >= (1 << (K - 1))) a -= (1 << K);
+        const int V = a >= 0 ? a : -a - 1;
+        const float v = x[(1 << (8 - K)) * V + (1 << (7 - K)) - 1];
+        const float n = __fmaf_rn(a >= 0 ? v : -v, sg[j], mu[j]);
+        y[j] = __fmaf_rn(n, gs[j], gm[j]);
+      }
+      const int64_t o = ((b * L + p * P + t0 + u) * H + h) * kD + 8 * G;
+      if constexpr (BF16OUT) {
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) =
+            make_uint4(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]), f2_to_bf2(y[4], y[5]),
+                       f2_to_bf2(y[6], y[7]));
+      } else {
+        float4* q = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+        q[0] = make_float4(y[0], y[1], y[2], y[3]);
+        q[1] = make_float4(y[4], y[5], y[6], y[7]);
+      }
+    }
+  }
+}
+
+unsigned grid_for(int64_t work_items, int per_block) {
+  const int64_t waves = (int64_t)sm_count() * 8;  // 8 CTAs of 256 threads per SM
+  const int64_t need = (work_items + per_block - 1) / per_block;
+  return (unsigned)(need < waves ? (need > 0 ? need : 1) : waves);
+}
+
+bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+cudaError_t launch_decode_anchor_bits(const void* ak, const float* meta, const Shape& s, int k,
+                                      const ExpandTable& tab, void* out, bool bf16_out,
+                                      cudaStream_t stream) {
+  const int64_t nblk = s.blocks();
+  const unsigned grid = grid_for(nblk * (s.page / kRun) * 16, kThreads);
+  const uint8_t* a = static_cast<const uint8_t*>(ak);
+#define LYNX_DAB(KK)                                                                        \
+  if (k == KK) {                                                                            \
+    if (bf16_out)                                                                           \
+      decode_anchor_bits_kernel<KK, true><<<grid, kThreads, 0, stream>>>(                   \
+          a, meta, nblk, s.NB(), s.H, s.L, s.page, s.C, out, tab);                          \
+    else                                                                                    \
+      decode_anchor_bits_kernel<KK, false><<<grid, kThreads, 0, stream>>>(                  \
+          a, meta, nblk, s.NB(), s.H, s.L, s.page, s.C, out, tab);                          \
+    return cudaGetLastError();                                                              \
+  }
+  LYNX_DAB(3)
+  LYNX_DAB(4)
+  LYNX_DAB(5)
+  LYNX_DAB(6)
+#undef LYNX_DAB
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lynx
+
+using namespace lynx;
+
+extern "C" {
+
+int lynx_int_encode(const void* kv, int64_t rows, int D, int bits, void* codes, float* meta,
+                    void* stream) {
+  if (D != kD) return report_error(LYNX_EUNSUPPORTED, "only D = 128 is built");
+  if (bits != 4 && bits != 8) return report_error(LYNX_EUNSUPPORTED, "bits must be 4 or 8");
+  if (rows < 0) return report_error(LYNX_ESHAPE, "rows must be >= 0");
+  if (rows == 0) return LYNX_OK;
+  if (!kv || !codes || !meta) return report_error(LYNX_EINVAL, "null pointer");
+  if (!aligned(kv, 16) || !aligned(codes, 16) || !aligned(meta, 16))
+    return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned grid = grid_for((rows + 3) / 4, kThreads / 32);
+  if (bits == 8)
+    int_encode_kernel<8><<<grid, kThreads, 0, st>>>(static_cast<const uint8_t*>(kv), rows,
+                                                    static_cast<uint8_t*>(codes),
+                                                    reinterpret_cast<float2*>(meta));
+  else
+    int_encode_kernel<4><<<grid, kThreads, 0, st>>>(static_cast<const uint8_t*>(kv), rows,
+                                                    static_cast<uint8_t*>(codes),
+                                                    reinterpret_cast<float2*>(meta));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return report_error(LYNX_ECUDA, cudaGetErrorString(e));
+  return LYNX_OK;
+}
+
+int lynx_int_decode(const void* codes, const float* meta, int64_t rows, int D, int bits,
+                    void* out, int out_dtype, void* stream) {
+  if (D != kD) return report_error(LYNX_EUNSUPPORTED, "only D = 128 is built");
+  if (bits != 4 && bits != 8) return report_error(LYNX_EUNSUPPORTED, "bits must be 4 or 8");
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)
+    return report_error(LYNX_EINVAL, "out_dtype must be LYNX_OUT_BF16 or LYNX_OUT_FP32");
+  if (rows < 0) return report_error(LYNX_ESHAPE, "rows must be >= 0");
+  if (rows == 0) return LYNX_OK;
+  if (!codes || !meta || !out) return report_error(LYNX_EINVAL, "null pointer");
+  if (!aligned(codes, 16) || !aligned(meta, 16) || !aligned(out, 16))
+    return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const unsigned grid = grid_for(rows, kThreads / 32);
+  const uint8_t* c = static_cast<const uint8_t*>(codes);
+  const float2* m = reinterpret_cast<const float2*>(meta);
+  const bool b16 = out_dtype == LYNX_OUT_BF16;
+  if (bits == 8 && b16) int_decode_kernel<8, true><<<grid, kThreads, 0, st>>>(c, m, rows, out);
+  if (bits == 8 && !b16) int_decode_kernel<8, false><<<grid, kThreads, 0, st>>>(c, m, rows, out);
+  if (bits == 4 && b16) int_decode_kernel<4, true><<<grid, kThreads, 0, st>>>(c, m, rows, out);
+  if (bits == 4 && !b16) int_decode_kernel<4, false><<<grid, kThreads, 0, st>>>(c, m, rows, out);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return report_error(LYNX_ECUDA, cudaGetErrorString(e));
+  return LYNX_OK;
+}
+
+int lynx_split_bits(const void* anchor, const void* residual, int64_t rows, int D, int k,
+                    void* anchor_k, void* residual_k, void* stream) {
+  if (D != kD) return report_error(LYNX_EUNSUPPORTED, "only D = 128 is built");
+  if (k < 3 || k > 6) return report_error(LYNX_EUNSUPPORTED, "k must be 3, 4, 5 or 6");
+  if (rows < 0) return report_error(LYNX_ESHAPE, "rows must be >= 0");
+  if (rows == 0) return LYNX_OK;
+  if (!anchor || !residual || !anchor_k || !residual_k)
+    return report_error(LYNX_EINVAL, "null pointer");
+  if (!aligned(anchor, 16) || !aligned(residual, 16) || !aligned(anchor_k, 16) ||
+      !aligned(residual_k, 16))
+    return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t groups = rows * (kD / 8);
+  const unsigned grid = grid_for(groups, kThreads);
+  const uint8_t* a = static_cast<const uint8_t*>(anchor);
+  const uint8_t* r = static_cast<const uint8_t*>(residual);
+  uint8_t* ao = static_cast<uint8_t*>(anchor_k);
+  uint8_t* ro = static_cast<uint8_t*>(residual_k);
+  if (k == 3) split_bits_kernel<3><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  if (k == 4) split_bits_kernel<4><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  if (k == 5) split_bits_kernel<5><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  if (k == 6) split_bits_kernel<6><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return report_error(LYNX_ECUDA, cudaGetErrorString(e));
+  return LYNX_OK;
+}
+
+int lynx_join_bits(const void* anchor_k, const void* residual_k, int64_t rows, int D, int k,
+                   void* anchor, void* residual, void* stream) {
+  if (D != kD) return report_error(LYNX_EUNSUPPORTED, "only D = 128 is built");
+  if (k < 3 || k > 6) return report_error(LYNX_EUNSUPPORTED, "k must be 3, 4, 5 or 6");
+  if (rows < 0) return report_error(LYNX_ESHAPE, "rows must be >= 0");
+  if (rows == 0) return LYNX_OK;
+  if (!anchor || !residual || !anchor_k || !residual_k)
+    return report_error(LYNX_EINVAL, "null pointer");
+  if (!aligned(anchor, 16) || !aligned(residual, 16) || !aligned(anchor_k, 16) ||
+      !aligned(residual_k, 16))
+    return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t groups = rows * (kD / 8);
+  const unsigned grid = grid_for(groups, kThreads);
+  const uint8_t* a = static_cast<const uint8_t*>(anchor_k);
+  const uint8_t* r = static_cast<const uint8_t*>(residual_k);
+  uint32_t* ao = static_cast<uint32_t*>(anchor);
+  uint32_t* ro = static_cast<uint32_t*>(residual);
+  if (k == 3) join_bits_kernel<3><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  if (k == 4) join_bits_kernel<4><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  if (k == 5) join_bits_kernel<5><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  if (k == 6) join_bits_kernel<6><<<grid, kThreads, 0, st>>>(a, r, groups, ao, ro);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return report_error(LYNX_ECUDA, cudaGetErrorString(e));
+  return LYNX_OK;
+}
+
+}  // extern "C"

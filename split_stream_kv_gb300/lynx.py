@@ -65,6 +65,11 @@ def lib() -> ctypes.CDLL:
         "lynx_split_send": ([P, I64, I64, I, I, I, I, F, P, P, P, P, P, P, I64, P, P, P, P], I),
         "lynx_header_init": ([P, I64, I64, I, I, I, I, F, I], I),
         "lynx_header_check": ([P], I),
+        "lynx_int_encode": ([P, I64, I, I, P, P, P], I),
+        "lynx_int_decode": ([P, P, I64, I, I, P, I, P], I),
+        "lynx_split_bits": ([P, P, I64, I, I, P, P, P], I),
+        "lynx_join_bits": ([P, P, I64, I, I, P, P, P], I),
+        "lynx_decode_anchor_bits": ([P, P, I64, I64, I, I, I, I, F, I, P, I, P], I),
         "lynx_compander_thresholds": ([F, P], I),
         "lynx_expand_table": ([F, P], I),
         "lynx_compander_selfcheck": ([F, P, P], I),
@@ -376,6 +381,78 @@ def lynx_header_check(buf: bytes) -> LynxHeader:
     h = LynxHeader.from_buffer_copy(bytes(buf[:ctypes.sizeof(LynxHeader)]))
     _check(lib().lynx_header_check(ctypes.byref(h)), "lynx_header_check")
     return h
+
+
+# ------------------------------------------------------- comparison points
+
+def lynx_int_encode(kv, bits: int, codes=None, meta=None):
+    """Linear INT-`bits` baseline (Eq. 4) of kv[..][128] BF16: one scale and
+    zero point per row of 128 channels.  Returns (codes, meta)."""
+    _need_cuda(kv, codes, meta)
+    if kv.dtype != torch.bfloat16 or kv.shape[-1] != 128:
+        raise ValueError("lynx_int_encode: kv must be bfloat16 with 128 channels")
+    rows = kv.numel() // 128
+    if codes is None:
+        codes = torch.empty(kv.shape[:-1] + (128 * bits // 8,), dtype=torch.uint8,
+                            device=kv.device)
+    if meta is None:
+        meta = torch.empty(kv.shape[:-1] + (2,), dtype=torch.float32, device=kv.device)
+    _check(lib().lynx_int_encode(_ptr(kv), rows, 128, bits, _ptr(codes), _ptr(meta),
+                                 _stream(kv.device)), "lynx_int_encode")
+    return codes, meta
+
+
+def lynx_int_decode(codes, meta, bits: int, out_dtype=torch.bfloat16, out=None):
+    _need_cuda(codes, meta, out)
+    rows = meta.numel() // 2
+    if out is None:
+        out = torch.empty(meta.shape[:-1] + (128,), dtype=out_dtype, device=codes.device)
+    code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
+    _check(lib().lynx_int_decode(_ptr(codes), _ptr(meta), rows, 128, bits, _ptr(out), code,
+                                 _stream(codes.device)), "lynx_int_decode")
+    return out
+
+
+def lynx_split_bits(anchor, residual, k: int, anchor_k=None, residual_k=None):
+    """Re-split 4+4 streams [B][NB][H][P][64] into a k + (8-k) split:
+    returns (anchor_k [B][NB][H][P][16k], residual_k [..][16(8-k)])."""
+    _need_cuda(anchor, residual, anchor_k, residual_k)
+    shp = anchor.shape[:-1]
+    rows = anchor.numel() // 64
+    if anchor_k is None:
+        anchor_k = torch.empty(shp + (16 * k,), dtype=torch.uint8, device=anchor.device)
+    if residual_k is None:
+        residual_k = torch.empty(shp + (16 * (8 - k),), dtype=torch.uint8, device=anchor.device)
+    _check(lib().lynx_split_bits(_ptr(anchor), _ptr(residual), rows, 128, k, _ptr(anchor_k),
+                                 _ptr(residual_k), _stream(anchor.device)), "lynx_split_bits")
+    return anchor_k, residual_k
+
+
+def lynx_join_bits(anchor_k, residual_k, k: int, anchor=None, residual=None):
+    _need_cuda(anchor_k, residual_k, anchor, residual)
+    shp = anchor_k.shape[:-1]
+    rows = anchor_k.numel() // (16 * k)
+    if anchor is None:
+        anchor = torch.empty(shp + (64,), dtype=torch.uint8, device=anchor_k.device)
+    if residual is None:
+        residual = torch.empty(shp + (64,), dtype=torch.uint8, device=anchor_k.device)
+    _check(lib().lynx_join_bits(_ptr(anchor_k), _ptr(residual_k), rows, 128, k, _ptr(anchor),
+                                _ptr(residual), _stream(anchor_k.device)), "lynx_join_bits")
+    return anchor, residual
+
+
+def lynx_decode_anchor_bits(anchor_k, meta, L: int, page: int, C: int, alpha: float, k: int,
+                            out_dtype=torch.bfloat16, out=None):
+    """Anchor-only decode of a k-bit Anchor stream [B][NB][H][P][16k]."""
+    _need_cuda(anchor_k, meta, out)
+    B, NB, H = anchor_k.shape[:3]
+    if out is None:
+        out = torch.empty((B, L, H, 128), dtype=out_dtype, device=anchor_k.device)
+    code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
+    _check(lib().lynx_decode_anchor_bits(_ptr(anchor_k), _ptr(meta), B, L, H, 128, page, C, alpha,
+                                         k, _ptr(out), code, _stream(anchor_k.device)),
+           "lynx_decode_anchor_bits")
+    return out
 
 
 # ----------------------------------------------------------------- attention
