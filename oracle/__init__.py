@@ -86,6 +86,10 @@ def _bind(lib):
     lib.oracle_split_bits.restype = I
     lib.oracle_decode_anchor_bits_range.argtypes = [P, P, I64, I64, I, I, I, I, F, I, P]
     lib.oracle_decode_anchor_bits_range.restype = I
+    lib.oracle_a1_encode_range.argtypes = [P, I64, I64, I, I, I, F, P, P, P]
+    lib.oracle_a1_encode_range.restype = I
+    lib.oracle_a1_decode_range.argtypes = [P, P, P, I64, I64, I, I, I, F, P]
+    lib.oracle_a1_decode_range.restype = I
     lib.oracle_int_encode_rows.argtypes = [P, I64, I, I, P, P]
     lib.oracle_int_encode_rows.restype = I
     lib.oracle_int_decode_rows.argtypes = [P, P, I64, I, I, P]
@@ -398,6 +402,42 @@ def decode_anchor_bits(ak: np.ndarray, meta: np.ndarray, L: int, P: int, C: int,
     return out
 
 
+def a1_encode(kv_bits: np.ndarray, P: int, alpha: float = 100.0):
+    """The Appendix A.1 variant of a bf16 tensor [B][L][H][D] (uint16 bit
+    patterns): anchor, residual [B][NB][H][P][D/2] and meta
+    [B][NB][H][1 + P/16][D]."""
+    lib = _load()
+    x = np.ascontiguousarray(kv_bits, dtype=np.uint16)
+    B, L, H, D = x.shape
+    NB = L // P
+    anc = np.zeros((B, NB, H, P, D // 2), np.uint8)
+    res = np.zeros_like(anc)
+    meta = np.zeros((B, NB, H, 1 + P // 16, D), np.float32)
+    rc = lib.oracle_a1_encode_range(_ptr(x), B, L, H, D, P, alpha, _ptr(anc), _ptr(res),
+                                    _ptr(meta))
+    if rc:
+        raise ValueError("oracle_a1_encode_range: bad arguments")
+    return anc, res, meta
+
+
+def a1_decode(anc: np.ndarray, res, meta: np.ndarray, L: int, P: int,
+              alpha: float = 100.0) -> np.ndarray:
+    """Decode of the A.1 variant (res None: Anchor only) to float32
+    [B][L][H][D]."""
+    lib = _load()
+    a = np.ascontiguousarray(anc, dtype=np.uint8)
+    r = None if res is None else np.ascontiguousarray(res, dtype=np.uint8)
+    m = np.ascontiguousarray(meta, dtype=np.float32)
+    B, NB, H = a.shape[:3]
+    D = a.shape[-1] * 2
+    out = np.zeros((B, L, H, D), np.float32)
+    rc = lib.oracle_a1_decode_range(_ptr(a), None if r is None else _ptr(r), _ptr(m), B, L, H, D,
+                                    P, alpha, _ptr(out))
+    if rc:
+        raise ValueError("oracle_a1_decode_range: bad arguments")
+    return out
+
+
 def int_encode(kv_bits: np.ndarray, bits: int):
     """Linear INT-`bits` baseline (Eq. 4) of a bf16 tensor [..][D] (uint16
     bit patterns): codes [..][D*bits/8] uint8 and meta [..][2] float32."""
@@ -521,4 +561,5 @@ __all__ = [
     "encode", "decode_block", "decode", "attention_row", "kv_size_bytes",
     "metadata_scalars", "effective_bins", "anchor_ratio", "stream_bytes", "request_header",
     "split_bits", "decode_anchor_bits", "int_encode", "int_decode", "vnmse", "attention_rows",
+    "a1_encode", "a1_decode",
 ]

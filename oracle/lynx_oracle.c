@@ -460,6 +460,130 @@ int oracle_decode_anchor_bits_range(const uint8_t *ak, const float *meta, int64_
     return 0;
 }
 
+/* ------------------------------------------------- Appendix A.1 variant */
+
+/*
+ * The variant of [Review] Appendix A.1 ("Hierarchical Quantization: Full
+ * Derivation"), which differs from Algorithm 1: no centring, scaling by
+ * magnitudes only.
+ *   Step 1  x'  = x / m,    m   = max |x| of the channel over the page;
+ *   Step 2  x'' = x' / m_i, m_i = max |x'| of the channel over a chunk of 16
+ *           consecutive tokens;
+ *   Step 3  y = sgn(x'') ln(1 + alpha |x''|) / ln(1 + alpha);
+ *   Step 4  Q = clip(round(127 y), -127, 127); Q_anc = Q >> 4 (arithmetic),
+ *           Q_res = Q & 0xF.
+ * Readings: each division is a multiplication by the correctly rounded
+ * float32 reciprocal, and a zero maximum gives 0 (its channel or chunk codes
+ * to 0); |Q| = Round(Y(|x''|)) with Y of Eq. 7 in float64 (nearest, ties
+ * up), so |Q| <= 127 and the clip never acts; Q keeps the sign of x'' (0 for
+ * x'' = 0).  The nibbles are packed as the 4+4 streams of Stage 4 (byte 4G+j:
+ * channels 8G+j low, 8G+j+4 high).  meta per block: m [D], then m_i
+ * [P/16][D], float32.  Decode: |x''| = X(|Q|) (Eq. 14/15), x = sgn X m_i m
+ * (two float32 products).  Anchor-only: Q is taken as 16 Q_anc + 7, the
+ * round-half-down point of the bucket as in Stage 4.
+ */
+#define A1_CHUNK 16
+
+int oracle_a1_encode_block(const uint16_t *x, int64_t row_stride, int P, int D, float alpha,
+                           uint8_t *anchor, uint8_t *residual, float *meta)
+{
+    if (P <= 0 || P % A1_CHUNK || D <= 0 || (D & 7)) return -1;
+    memset(anchor, 0, (size_t)P * (size_t)(D / 2));
+    memset(residual, 0, (size_t)P * (size_t)(D / 2));
+    for (int d = 0; d < D; ++d) {
+        float m = 0.0f;
+        for (int t = 0; t < P; ++t) {
+            float a = fabsf(bf16_bits_to_f32(x[(int64_t)t * row_stride + d]));
+            if (a > m) m = a;
+        }
+        float rm = m > 0.0f ? 1.0f / m : 0.0f;
+        meta[d] = m;
+        for (int c = 0; c < P / A1_CHUNK; ++c) {
+            float xp[A1_CHUNK];
+            float mi = 0.0f;
+            for (int i = 0; i < A1_CHUNK; ++i) {
+                int t = c * A1_CHUNK + i;
+                xp[i] = bf16_bits_to_f32(x[(int64_t)t * row_stride + d]) * rm;
+                float a = fabsf(xp[i]);
+                if (a > mi) mi = a;
+            }
+            float rmi = mi > 0.0f ? 1.0f / mi : 0.0f;
+            meta[(size_t)(1 + c) * D + d] = mi;
+            for (int i = 0; i < A1_CHUNK; ++i) {
+                int t = c * A1_CHUNK + i;
+                float xpp = xp[i] * rmi;
+                int I = oracle_round_code(fabsf(xpp), alpha);
+                if (I > 127) I = 127;
+                int Q = xpp > 0.0f ? I : (xpp < 0.0f ? -I : 0);
+                int qa = Q >> 4;                    /* arithmetic shift */
+                int qr = Q & 0xF;
+                size_t byte = (size_t)t * (size_t)(D / 2) + nib_byte(d);
+                anchor[byte] |= (uint8_t)((qa & 0xF) << nib_shift(d));
+                residual[byte] |= (uint8_t)(qr << nib_shift(d));
+            }
+        }
+    }
+    return 0;
+}
+
+int oracle_a1_decode_block(const uint8_t *anchor, const uint8_t *residual, const float *meta,
+                           int P, int D, float alpha, float *out, int64_t out_stride)
+{
+    if (P <= 0 || P % A1_CHUNK || D <= 0 || (D & 7)) return -1;
+    float table[128];
+    for (int I = 0; I < 128; ++I) table[I] = oracle_expand(I, alpha);
+    for (int t = 0; t < P; ++t) {
+        int c = t / A1_CHUNK;
+        for (int d = 0; d < D; ++d) {
+            size_t byte = (size_t)t * (size_t)(D / 2) + nib_byte(d);
+            int a = (anchor[byte] >> nib_shift(d)) & 0xF;
+            int qa = a >= 8 ? a - 16 : a;
+            int Q = residual ? qa * 16 + ((residual[byte] >> nib_shift(d)) & 0xF) : qa * 16 + 7;
+            int I = Q < 0 ? -Q : Q;
+            if (I > 127) I = 127;
+            float v = Q < 0 ? -table[I] : table[I];
+            out[(int64_t)t * out_stride + d] = (v * meta[(size_t)(1 + c) * D + d]) * meta[d];
+        }
+    }
+    return 0;
+}
+
+/* Whole [B][L][H][D] tensors, blocks in (b, page, h) order. */
+int oracle_a1_encode_range(const uint16_t *kv, int64_t B, int64_t L, int H, int D, int P,
+                           float alpha, uint8_t *anchor, uint8_t *residual, float *meta)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || P <= 0 || L % P) return -1;
+    const int64_t NB = L / P;
+    const size_t code_blk = (size_t)P * (size_t)(D / 2);
+    const size_t meta_blk = (size_t)(1 + P / A1_CHUNK) * (size_t)D;
+    for (int64_t blk = 0; blk < B * NB * H; ++blk) {
+        int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
+        int rc = oracle_a1_encode_block(kv + ((b * L + p * P) * H + h) * D, (int64_t)H * D, P, D,
+                                        alpha, anchor + blk * code_blk, residual + blk * code_blk,
+                                        meta + blk * meta_blk);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
+int oracle_a1_decode_range(const uint8_t *anchor, const uint8_t *residual, const float *meta,
+                           int64_t B, int64_t L, int H, int D, int P, float alpha, float *out)
+{
+    if (B <= 0 || L <= 0 || H <= 0 || P <= 0 || L % P) return -1;
+    const int64_t NB = L / P;
+    const size_t code_blk = (size_t)P * (size_t)(D / 2);
+    const size_t meta_blk = (size_t)(1 + P / A1_CHUNK) * (size_t)D;
+    for (int64_t blk = 0; blk < B * NB * H; ++blk) {
+        int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
+        int rc = oracle_a1_decode_block(anchor + blk * code_blk,
+                                        residual ? residual + blk * code_blk : NULL,
+                                        meta + blk * meta_blk, P, D, alpha,
+                                        out + ((b * L + p * P) * H + h) * D, (int64_t)H * D);
+        if (rc) return rc;
+    }
+    return 0;
+}
+
 /* ------------------------------------------------ linear INT-B baseline */
 
 /*

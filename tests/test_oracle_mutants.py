@@ -80,6 +80,15 @@ MUTANTS = [
      "int I = (1 << (8 - k)) * V + (1 << (7 - k));"),
     ("bit fields written high bit first", "uint8_t m = (uint8_t)(1u << (b & 7));",
      "uint8_t m = (uint8_t)(1u << (7 - (b & 7)));"),
+    ("A.1 sign dropped", "int Q = xpp > 0.0f ? I : (xpp < 0.0f ? -I : 0);", "int Q = I;"),
+    ("A.1 decode without the page maximum",
+     "out[(int64_t)t * out_stride + d] = (v * meta[(size_t)(1 + c) * D + d]) * meta[d];",
+     "out[(int64_t)t * out_stride + d] = (v * meta[(size_t)(1 + c) * D + d]);"),
+    ("A.1 page maximum without |.|", "float a = fabsf(bf16_bits_to_f32(x[(int64_t)t * row_stride + d]));",
+     "float a = bf16_bits_to_f32(x[(int64_t)t * row_stride + d]);"),
+    ("A.1 Anchor point 16 Q_anc + 8", "qa * 16 + 7;", "qa * 16 + 8;"),
+    ("A.1 chunk maximum of x instead of x'", "float a = fabsf(xp[i]);",
+     "float a = fabsf(bf16_bits_to_f32(x[(int64_t)t * row_stride + d]));"),
 ]
 
 # representative arguments for the parametrized pins

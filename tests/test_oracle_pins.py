@@ -763,3 +763,98 @@ def test_attention_rows_gqa_mapping(oracle_mod):
     for b in range(B):
         for j in range(Hkv * G):
             assert np.allclose(o[b, :, j], c[b, 0, j // G, 0], rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------- Appendix A.1
+
+def _a1_block(seed=5, P=128):
+    """[1][P][1][128] bf16: Laplace channels, one all-negative channel, one
+    zero channel, one channel of a repeated value."""
+    rng = np.random.default_rng(seed)
+    x = rng.laplace(size=(P, 128)).astype(np.float32) * np.exp(rng.standard_normal(128)).astype(np.float32)
+    x[:, 3] = -np.abs(x[:, 3]) - 0.5
+    x[:, 4] = 0.0
+    x[:, 5] = 2.5
+    import oracle
+    return oracle.f32_to_bf16_bits(x).reshape(1, P, 1, 128)
+
+
+def _a1_codes(anc, res):
+    """Signed Q from the packed nibbles: Q = Q_anc * 16 + Q_res (Q_anc signed)."""
+    a = _signed_codes(anc.reshape(anc.shape[-2], -1), res.reshape(res.shape[-2], -1))
+    return a      # the nibble pairing of Stage 4 read back as one signed byte
+
+
+def test_a1_chunk_maxima_and_signs(oracle_mod):
+    """Appendix A.1: x'' = x / (m m_i) is +-1 at the largest |x| of each
+    16-token chunk of a channel, so |Q| = 127 there with the sign of x; a zero
+    channel codes to 0 and stores m = 0; Q = Q_anc * 16 + Q_res lies in
+    [-127, 127] with Q_anc = Q >> 4 (arithmetic)."""
+    P = 128
+    x = _a1_block(P=P)
+    anc, res, meta = oracle_mod.a1_encode(x, P)
+    Q = _a1_codes(anc, res)
+    xf = oracle_mod.bf16_bits_to_f32(x)[0, :, 0, :]
+    assert Q.min() >= -127 and Q.max() <= 127
+    for c in range(P // 16):
+        blk = xf[16 * c:16 * (c + 1)]
+        t = np.abs(blk).argmax(0)
+        for d in range(128):
+            v = blk[t[d], d]
+            if v != 0:
+                assert Q[16 * c + t[d], d] == (127 if v > 0 else -127), (c, d)
+    assert (Q[:, 4] == 0).all() and meta[0, 0, 0, 0, 4] == 0
+    assert (Q[:, 5] == 127).all()                 # a constant positive channel
+    assert (Q[:, 3] <= 0).all()                   # the all-negative channel
+    np.testing.assert_array_equal(meta[0, 0, 0, 0], np.abs(xf).max(0))
+
+
+def test_a1_scale_invariance_and_small_alpha(oracle_mod):
+    """Scaling a channel by a power of two leaves its codes unchanged (every
+    step is a ratio); as alpha -> 0 the alpha-law is the identity and
+    |Q| = round(127 |x''|), the textbook linear quantizer."""
+    P = 64
+    x = _a1_block(seed=8, P=P)
+    xf = oracle_mod.bf16_bits_to_f32(x)
+    anc, res, meta = oracle_mod.a1_encode(x, P)
+    anc2, res2, meta2 = oracle_mod.a1_encode(oracle_mod.f32_to_bf16_bits(xf * 4.0), P)
+    assert np.array_equal(anc, anc2) and np.array_equal(res, res2)
+    np.testing.assert_array_equal(meta2[..., 0, :], 4 * meta[..., 0, :])
+    a_s, r_s, m_s = oracle_mod.a1_encode(x, P, alpha=1e-7)
+    Q = _a1_codes(a_s, r_s)
+    xs = xf[0, :, 0, :].astype(np.float64)
+    for c in range(P // 16):
+        blk = xs[16 * c:16 * (c + 1)]
+        mx = np.abs(blk).max(0)
+        xpp = np.divide(blk, mx, out=np.zeros_like(blk), where=mx > 0)
+        want = np.sign(xpp) * np.rint(127 * np.abs(xpp))
+        frac = (127 * np.abs(xpp)) % 1.0
+        keep = np.abs(frac - 0.5) > 1e-3
+        assert np.array_equal(Q[16 * c:16 * (c + 1)][keep], want[keep].astype(int))
+
+
+def test_a1_decode_error_bound_and_anchor_point(oracle_mod):
+    """Full decode is within half a code step of x: |x - x^| <= m m_i
+    max(X(|Q| + 1/2) - X(|Q|), X(|Q|) - X(|Q| - 1/2)) with X of Eq. 14/15 (the
+    steps are geometric, so the two half-steps differ); the Anchor-only
+    decode equals the full decode of Q = 16 Q_anc + 7."""
+    P = 128
+    alpha = 100.0
+    x = _a1_block(seed=3, P=P)
+    xf = oracle_mod.bf16_bits_to_f32(x).astype(np.float64)[0, :, 0, :]
+    anc, res, meta = oracle_mod.a1_encode(x, P, alpha)
+    y = oracle_mod.a1_decode(anc, res, meta, P, P, alpha)[0, :, 0, :].astype(np.float64)
+    Q = _a1_codes(anc, res)
+    I = np.abs(Q).astype(np.float64)
+
+    def X(v):
+        return ((1 + alpha) ** (np.clip(v, 0, 127) / 127.0) - 1) / alpha
+
+    m = meta[0, 0, 0, 0].astype(np.float64)
+    mi = np.repeat(meta[0, 0, 0, 1:].astype(np.float64), 16, axis=0)
+    half = np.maximum(X(I + 0.5) - X(I), X(I) - X(I - 0.5))
+    assert (np.abs(y - xf) <= m * mi * half * 1.001 + np.abs(xf) * 2.0 ** -20).all()
+    r7 = np.full_like(res, 0x77)
+    full7 = oracle_mod.a1_decode(anc, r7, meta, P, P, alpha)
+    anchor_only = oracle_mod.a1_decode(anc, None, meta, P, P, alpha)
+    assert np.array_equal(full7.view(np.uint32), anchor_only.view(np.uint32))
