@@ -616,6 +616,16 @@ def accuracy_table(K, V, q, P=128, C=32, alpha=255.0, sweep=True):
                       "total_bytes_per_elem": 1 + meta_b}
         return out
 
+    ka1 = lynx.lynx_a1_encode(K, P, 100.0)
+    va1 = lynx.lynx_a1_encode(V, P, 100.0)
+    a1_meta = 4 * (1 + P // 16) / P
+    table["a1_full"] = {"vnmse": vn(lynx.lynx_a1_decode(*ka1, L, P, 100.0),
+                                    lynx.lynx_a1_decode(*va1, L, P, 100.0)),
+                        "bytes_per_elem": 1 + a1_meta}
+    table["a1_anchor"] = {"vnmse": vn(lynx.lynx_a1_decode(ka1[0], None, ka1[2], L, P, 100.0),
+                                      lynx.lynx_a1_decode(va1[0], None, va1[2], L, P, 100.0)),
+                          "anchor_bytes_per_elem": 0.5 + a1_meta}
+    del ka1, va1
     rows = lynx_rows(P, C, alpha, (3, 4, 5, 6))
     table["lynx_full"] = rows["full"]
     for k in (3, 4, 5, 6):
@@ -681,6 +691,13 @@ def measure_variants(kv, anc, res, meta, dev, reps=5):
         row(f"int{bits}_decode", lambda: lynx.lynx_int_decode(codes, m, bits, out=dec),
             n * (bits / 8 + 8 / 128 + 2))
         del codes, m, dec
+    a1 = lynx.lynx_a1_encode(kv, c["P"], 100.0)
+    dec = torch.empty_like(kv)
+    a1_meta = n * 4 * (1 + c["P"] // 16) / c["P"]
+    row("a1_encode", lambda: lynx.lynx_a1_encode(kv, c["P"], 100.0), n * 3 + a1_meta)
+    row("a1_decode_full", lambda: lynx.lynx_a1_decode(*a1, c["L"], c["P"], 100.0, out=dec),
+        n * 3 + a1_meta)
+    del a1, dec
     for k in (6, 3):
         ak, rk = lynx.lynx_split_bits(anc, res, k)
         row(f"split_{k}+{8 - k}", lambda: lynx.lynx_split_bits(anc, res, k, ak, rk), n * 2)

@@ -292,6 +292,23 @@ int lynx_decode_anchor_bits(const void *anchor_k, const float *meta, int64_t B,
                             float alpha, int k, void *out, int out_dtype,
                             void *stream);
 
+/* The variant of [Review] Appendix A.1: x' = x / m (m = max |x| of the
+ * channel over the page), x'' = x' / m_i (m_i = max |x'| over 16 consecutive
+ * tokens), y = sgn(x'') ln(1 + alpha |x''|) / ln(1 + alpha), Q = sgn(x'')
+ * Round(127 |y|) in [-127, 127] (exact, as Stage 3), Q_anc = Q >> 4
+ * (arithmetic), Q_res = Q & 0xF.  Divisions are multiplications by correctly
+ * rounded reciprocals, of 0 for a zero maximum.  Streams as lynx_encode
+ * (same nibble pairing); meta [B][L/page][H_kv][1 + page/16][D] float32 =
+ * m, then m_i per chunk.  Decode: x = (sgn X(|Q|) * m_i) * m (Eq. 14/15
+ * inverse, two float32 products); with residual = NULL the Anchor-only
+ * point Q = 16 Q_anc + 7.  The pages use alpha = 100 for this variant. */
+int lynx_a1_encode(const void *kv, int64_t B, int64_t L, int H_kv, int D,
+                   int page, float alpha, void *anchor, void *residual,
+                   float *meta, void *stream);
+int lynx_a1_decode(const void *anchor, const void *residual, const float *meta,
+                   int64_t B, int64_t L, int H_kv, int D, int page, float alpha,
+                   void *out, int out_dtype, void *stream);
+
 /* Speculative verification and correction [Review, Mechanism 3, Eq. 10 and
  * Eq. 11], for every sequence b of the batch, on distributions the caller's
  * verification pass (p, over the full KV) and draft steps (q, over the

@@ -50,6 +50,13 @@ cudaError_t launch_decode(const void* anchor, const void* residual, const float*
 cudaError_t launch_decode_anchor_bits(const void* anchor_k, const float* meta, const Shape& s,
                                       int k, const ExpandTable& tab, void* out, bool bf16_out,
                                       cudaStream_t stream);
+// The Appendix A.1 variant (variants.cu): meta = m [D], then m_i [P/16][D]
+// per block; residual may be null for the Anchor-only decode.
+cudaError_t launch_a1_encode(const void* kv, const Shape& s, const CompanderTable& tab,
+                             void* anchor, void* residual, float* meta, cudaStream_t stream);
+cudaError_t launch_a1_decode(const void* anchor, const void* residual, const float* meta,
+                             const Shape& s, const ExpandTable& tab, void* out, bool bf16_out,
+                             cudaStream_t stream);
 cudaError_t launch_compander_selfcheck(const CompanderTable& tab, uint64_t* counts,
                                        cudaStream_t stream);
 

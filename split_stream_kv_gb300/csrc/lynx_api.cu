@@ -294,6 +294,36 @@ int lynx_decode_anchor_bits(const void* anchor_k, const float* meta, int64_t B, 
   return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_decode_anchor_bits");
 }
 
+int lynx_a1_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page, float alpha,
+                   void* anchor, void* residual, float* meta, void* stream) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, 16);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if (B * L == 0) return LYNX_OK;
+  if ((rc = check_ptrs({kv, anchor, residual, meta}))) return rc;
+  Shape s{B, L, H_kv, D, page, 16};
+  cudaError_t e = launch_a1_encode(kv, s, tables_for(alpha).comp, anchor, residual, meta,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_a1_encode");
+}
+
+int lynx_a1_decode(const void* anchor, const void* residual, const float* meta, int64_t B,
+                   int64_t L, int H_kv, int D, int page, float alpha, void* out, int out_dtype,
+                   void* stream) {
+  int rc = check_codec_shape(B, L, H_kv, D, page, 16);
+  if (rc) return rc;
+  if ((rc = check_alpha(alpha))) return rc;
+  if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)
+    return fail(LYNX_EINVAL, "out_dtype must be LYNX_OUT_BF16 or LYNX_OUT_FP32");
+  if (B * L == 0) return LYNX_OK;
+  if ((rc = check_ptrs({anchor, meta, out}))) return rc;
+  if (residual && (rc = check_ptrs({residual}))) return rc;
+  Shape s{B, L, H_kv, D, page, 16};
+  cudaError_t e = launch_a1_decode(anchor, residual, meta, s, tables_for(alpha).expand, out,
+                                   out_dtype == LYNX_OUT_BF16, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? LYNX_OK : cuda_fail(e, "lynx_a1_decode");
+}
+
 static int check_attn_shape(int batch, int T, int H_q, int64_t L, int H_kv, int D, int page,
                             int C) {
   int rc = check_codec_shape(batch, L, H_kv, D, page, C);

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) int_encode_kernel(const uint8_t* __r
                                                               const int64_t rows,
                                                               uint8_t* __restrict__ codes,
                                                               float2* __restrict__ meta) {
-  constexpr int R = 4;
+  constexpr int R = 8;
   constexpr int qmax = (1 << BITS) - 1;
   const int lane = threadIdx.x & 31;
   const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
@@ -256,6 +256,127 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
   }
 }
 
+// ---------------------------------------------------------- Appendix A.1
+
+// One CTA per page block, kA1Split threads per channel, each owning a
+// quarter of the page's tokens (whole 16-token chunks).  The block's BF16
+// tile is staged in shared memory; the page maximum of a channel combines
+// the quarters' maxima through shared memory; each thread then walks its
+// chunks for the chunk maximum and the codes, decided against the host
+// thresholds of Eq. 7 (|Q| = #{k : a >= thr[k]}).  The codes gather in
+// shared memory in the 4+4 nibble layout and leave as 16-byte rows.
+constexpr int kA1Chunk = 16;
+constexpr int kA1Split = 4;
+constexpr int kA1Threads = 128 * kA1Split;
+
+__global__ void __launch_bounds__(kA1Threads)
+a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, const int64_t L,
+                 const int P, uint8_t* __restrict__ anchor, uint8_t* __restrict__ residual,
+                 float* __restrict__ meta, const __grid_constant__ CompanderTable tab) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  uint16_t* tile = reinterpret_cast<uint16_t*>(sm);                 // [P][128]
+  uint8_t* ca = sm + (size_t)P * 256;                               // [P][64]
+  uint8_t* cr = ca + (size_t)P * 64;                                // [P][64]
+  float* thr = reinterpret_cast<float*>(cr + (size_t)P * 64);       // [128]
+  float* pmax = thr + 128;                                          // [kA1Split][128]
+  const int tid = threadIdx.x, d = tid & 127, qt = tid >> 7;
+  const int64_t blk = blockIdx.x;
+  const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
+  const uint8_t* src = kv + ((b * L + p * P) * H + h) * 256;
+  for (int i = tid; i < P * 16; i += kA1Threads) {                  // 16 B of a 256 B row
+    const int t = i >> 4, w = i & 15;
+    reinterpret_cast<uint4*>(tile)[i] =
+        __ldg(reinterpret_cast<const uint4*>(src + (int64_t)t * H * 256) + w);
+  }
+  if (tid < 128) thr[tid] = tab.thr[tid];
+  __syncthreads();
+  auto xv = [&](int t) { return __uint_as_float((uint32_t)tile[t * 128 + d] << 16); };
+  const int span = P / kA1Split, t_lo = qt * span;
+  float m = 0.0f;
+  for (int t = t_lo; t < t_lo + span; ++t) m = fmaxf(m, fabsf(xv(t)));
+  pmax[qt * 128 + d] = m;
+  __syncthreads();
+#pragma unroll
+  for (int q = 0; q < kA1Split; ++q) m = fmaxf(m, pmax[q * 128 + d]);
+  const float rm = m > 0.0f ? __frcp_rn(m) : 0.0f;
+  const int NCk = P / kA1Chunk;
+  float* mrow = meta + blk * (int64_t)(1 + NCk) * kD;
+  if (qt == 0) mrow[d] = m;
+  const int byte = (d >> 3) * 4 + (d & 3), sh = (d & 4) ? 4 : 0;
+  for (int c = t_lo / kA1Chunk; c < (t_lo + span) / kA1Chunk; ++c) {
+    float xp[kA1Chunk];
+    float mi = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kA1Chunk; ++i) {
+      xp[i] = __fmul_rn(xv(c * kA1Chunk + i), rm);
+      mi = fmaxf(mi, fabsf(xp[i]));
+    }
+    const float rmi = mi > 0.0f ? __frcp_rn(mi) : 0.0f;
+    mrow[(1 + c) * kD + d] = mi;
+#pragma unroll
+    for (int i = 0; i < kA1Chunk; ++i) {
+      const float xpp = __fmul_rn(xp[i], rmi);
+      const float a = fabsf(xpp);
+      int I = 0;                                     // #{k < 127 : a >= thr[k]}
+#pragma unroll
+      for (int step = 64; step; step >>= 1)
+        if (I + step <= 127 && a >= thr[I + step - 1]) I += step;
+      const int Q = xpp > 0.0f ? I : (xpp < 0.0f ? -I : 0);
+      const uint32_t na = (uint32_t)(Q >> 4) & 0xfu, nr = (uint32_t)Q & 0xfu;
+      // channel d and d^4 share a byte: the low-nibble thread writes both
+      const uint32_t oa = __shfl_xor_sync(kFull, na, 4), orr = __shfl_xor_sync(kFull, nr, 4);
+      if (!sh) {
+        const int t = c * kA1Chunk + i;
+        ca[t * 64 + byte] = (uint8_t)(na | (oa << 4));
+        cr[t * 64 + byte] = (uint8_t)(nr | (orr << 4));
+      }
+    }
+  }
+  __syncthreads();
+  uint4* da = reinterpret_cast<uint4*>(anchor + blk * (int64_t)P * 64);
+  uint4* dr = reinterpret_cast<uint4*>(residual + blk * (int64_t)P * 64);
+  for (int i = tid; i < P * 4; i += kA1Threads) {
+    da[i] = reinterpret_cast<const uint4*>(ca)[i];
+    dr[i] = reinterpret_cast<const uint4*>(cr)[i];
+  }
+}
+
+template <bool BF16OUT>
+__global__ void __launch_bounds__(kA1Threads)
+a1_decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ residual,
+                 const float* __restrict__ meta, const int64_t NB, const int H, const int64_t L,
+                 const int P, void* __restrict__ out, const __grid_constant__ ExpandTable tab) {
+  __shared__ float x[128];
+  const int tid = threadIdx.x, d = tid & 127, qt = tid >> 7;
+  if (tid < 128) x[tid] = tab.x[tid];
+  __syncthreads();
+  const int64_t blk = blockIdx.x;
+  const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
+  const int NCk = P / kA1Chunk;
+  const float* mrow = meta + blk * (int64_t)(1 + NCk) * kD;
+  const float m = __ldg(mrow + d);
+  const int byte = (d >> 3) * 4 + (d & 3), sh = (d & 4) ? 4 : 0;
+  const uint8_t* a8 = anchor + blk * (int64_t)P * 64;
+  const uint8_t* r8 = residual ? residual + blk * (int64_t)P * 64 : nullptr;
+  const int span = P / kA1Split, t_lo = qt * span;
+#pragma unroll 4
+  for (int t = t_lo; t < t_lo + span; ++t) {
+    const float mi = __ldg(mrow + (1 + t / kA1Chunk) * kD + d);
+    int qa = (__ldg(a8 + t * 64 + byte) >> sh) & 0xf;
+    if (qa >= 8) qa -= 16;
+    const int Q = qa * 16 + (r8 ? (__ldg(r8 + t * 64 + byte) >> sh) & 0xf : 7);
+    int I = Q < 0 ? -Q : Q;
+    I = I > 127 ? 127 : I;
+    const float v = Q < 0 ? -x[I] : x[I];
+    const float y = __fmul_rn(__fmul_rn(v, mi), m);
+    const int64_t o = ((b * L + p * P + t) * H + h) * kD + d;
+    if constexpr (BF16OUT)
+      static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(y);
+    else
+      static_cast<float*>(out)[o] = y;
+  }
+}
+
 unsigned grid_for(int64_t work_items, int per_block) {
   const int64_t waves = (int64_t)sm_count() * 8;  // 8 CTAs of 256 threads per SM
   const int64_t need = (work_items + per_block - 1) / per_block;
@@ -290,6 +411,43 @@ cudaError_t launch_decode_anchor_bits(const void* ak, const float* meta, const S
   return cudaErrorInvalidValue;
 }
 
+cudaError_t launch_a1_encode(const void* kv, const Shape& s, const CompanderTable& tab,
+                             void* anchor, void* residual, float* meta, cudaStream_t stream) {
+  const size_t smem = (size_t)s.page * 384 + (128 + 128 * kA1Split) * 4;
+  static thread_local int configured = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured != dev) {
+    e = cudaFuncSetAttribute(a1_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             256 * 384 + (128 + 128 * kA1Split) * 4);
+    if (e != cudaSuccess) return e;
+    configured = dev;
+  }
+  const int64_t nblk = s.blocks();
+  if (nblk > 0x7fffffff) return cudaErrorInvalidValue;
+  a1_encode_kernel<<<(unsigned)nblk, kA1Threads, smem, stream>>>(
+      static_cast<const uint8_t*>(kv), s.NB(), s.H, s.L, s.page, static_cast<uint8_t*>(anchor),
+      static_cast<uint8_t*>(residual), meta, tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_a1_decode(const void* anchor, const void* residual, const float* meta,
+                             const Shape& s, const ExpandTable& tab, void* out, bool bf16_out,
+                             cudaStream_t stream) {
+  const int64_t nblk = s.blocks();
+  if (nblk > 0x7fffffff) return cudaErrorInvalidValue;
+  const uint8_t* a = static_cast<const uint8_t*>(anchor);
+  const uint8_t* r = static_cast<const uint8_t*>(residual);
+  if (bf16_out)
+    a1_decode_kernel<true><<<(unsigned)nblk, kA1Threads, 0, stream>>>(a, r, meta, s.NB(), s.H,
+                                                                      s.L, s.page, out, tab);
+  else
+    a1_decode_kernel<false><<<(unsigned)nblk, kA1Threads, 0, stream>>>(a, r, meta, s.NB(), s.H,
+                                                                       s.L, s.page, out, tab);
+  return cudaGetLastError();
+}
+
 }  // namespace lynx
 
 using namespace lynx;
@@ -306,7 +464,7 @@ int lynx_int_encode(const void* kv, int64_t rows, int D, int bits, void* codes, 
   if (!aligned(kv, 16) || !aligned(codes, 16) || !aligned(meta, 16))
     return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const unsigned grid = grid_for((rows + 3) / 4, kThreads / 32);
+  const unsigned grid = grid_for((rows + 7) / 8, kThreads / 32);
   if (bits == 8)
     int_encode_kernel<8><<<grid, kThreads, 0, st>>>(static_cast<const uint8_t*>(kv), rows,
                                                     static_cast<uint8_t*>(codes),

@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
         "lynx_split_bits": ([P, P, I64, I, I, P, P, P], I),
         "lynx_join_bits": ([P, P, I64, I, I, P, P, P], I),
         "lynx_decode_anchor_bits": ([P, P, I64, I64, I, I, I, I, F, I, P, I, P], I),
+        "lynx_a1_encode": ([P, I64, I64, I, I, I, F, P, P, P, P], I),
+        "lynx_a1_decode": ([P, P, P, I64, I64, I, I, I, F, P, I, P], I),
         "lynx_compander_thresholds": ([F, P], I),
         "lynx_expand_table": ([F, P], I),
         "lynx_compander_selfcheck": ([F, P, P], I),
@@ -452,6 +454,37 @@ def lynx_decode_anchor_bits(anchor_k, meta, L: int, page: int, C: int, alpha: fl
     _check(lib().lynx_decode_anchor_bits(_ptr(anchor_k), _ptr(meta), B, L, H, 128, page, C, alpha,
                                          k, _ptr(out), code, _stream(anchor_k.device)),
            "lynx_decode_anchor_bits")
+    return out
+
+
+def lynx_a1_encode(kv, page: int, alpha: float = 100.0):
+    """The Appendix A.1 variant of kv[B][L][H][128] BF16: returns (anchor,
+    residual, meta[B][L/page][H][1 + page/16][128])."""
+    _need_cuda(kv)
+    if kv.dtype != torch.bfloat16 or kv.dim() != 4:
+        raise ValueError("lynx_a1_encode: kv must be a 4-D bfloat16 tensor")
+    B, L, H, D = kv.shape
+    codes = (B, L // page, H, page, D // 2)
+    anchor = torch.empty(codes, dtype=torch.uint8, device=kv.device)
+    residual = torch.empty(codes, dtype=torch.uint8, device=kv.device)
+    meta = torch.empty((B, L // page, H, 1 + page // 16, D), dtype=torch.float32,
+                       device=kv.device)
+    _check(lib().lynx_a1_encode(_ptr(kv), B, L, H, D, page, alpha, _ptr(anchor), _ptr(residual),
+                                _ptr(meta), _stream(kv.device)), "lynx_a1_encode")
+    return anchor, residual, meta
+
+
+def lynx_a1_decode(anchor, residual, meta, L: int, page: int, alpha: float = 100.0,
+                   out_dtype=torch.bfloat16, out=None):
+    """Decode of the A.1 variant; residual None gives the Anchor-only decode."""
+    _need_cuda(anchor, residual, meta, out)
+    B, NB, H, P, half = anchor.shape
+    if out is None:
+        out = torch.empty((B, L, H, half * 2), dtype=out_dtype, device=anchor.device)
+    code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
+    _check(lib().lynx_a1_decode(_ptr(anchor), _ptr(residual), _ptr(meta), B, L, H, half * 2, page,
+                                alpha, _ptr(out), code, _stream(anchor.device)),
+           "lynx_a1_decode")
     return out
 
 

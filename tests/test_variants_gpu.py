@@ -149,6 +149,14 @@ def test_vnmse_harness_matches_the_oracle(lynx_lib, oracle_mod, cuda_dev):
             qf, bf(oracle_mod.decode_anchor_bits(kk, kmeta, L, 128, 32, ALPHA, k)),
             bf(oracle_mod.decode_anchor_bits(vk, vmeta, L, 128, 32, ALPHA, k)))
         want[f"lynx_anchor_{k}bit"] = oracle_mod.vnmse(o, ref)
+    a1k = oracle_mod.a1_encode(kb, 128, 100.0)
+    a1v = oracle_mod.a1_encode(vb, 128, 100.0)
+    o = oracle_mod.attention_rows(qf, bf(oracle_mod.a1_decode(*a1k, L, 128, 100.0)),
+                                  bf(oracle_mod.a1_decode(*a1v, L, 128, 100.0)))
+    want["a1_full"] = oracle_mod.vnmse(o, ref)
+    o = oracle_mod.attention_rows(qf, bf(oracle_mod.a1_decode(a1k[0], None, a1k[2], L, 128, 100.0)),
+                                  bf(oracle_mod.a1_decode(a1v[0], None, a1v[2], L, 128, 100.0)))
+    want["a1_anchor"] = oracle_mod.vnmse(o, ref)
     for name, w in want.items():
         got = table[name]["vnmse"]
         assert abs(got - w) <= 1e-3 * w + 1e-9, (name, got, w)
@@ -157,3 +165,27 @@ def test_vnmse_harness_matches_the_oracle(lynx_lib, oracle_mod, cuda_dev):
     assert want["lynx_full"] < want["int8"]
     assert want["lynx_anchor_4bit"] < want["int4"]
     print({n: f"{v:.3g}" for n, v in want.items()})
+
+
+A1_CASES = [(2, 512, 2, 128), (1, 512, 3, 256), (3, 256, 1, 64)]
+
+
+@pytest.mark.parametrize("B,L,H,P", A1_CASES)
+@pytest.mark.parametrize("alpha", [100.0, 255.0])
+def test_a1_variant_matches_oracle(lynx_lib, oracle_mod, cuda_dev, B, L, H, P, alpha):
+    from split_stream_kv_gb300 import synth
+    kv = synth.kv_cache(B, L, H, 128, seed=B * 3 + L + P, device=cuda_dev, n_outlier=2)
+    kv[0, :P, 0, 5] = 0          # a zero channel in one page block
+    anc, res, meta = lynx_lib.lynx_a1_encode(kv, P, alpha)
+    torch.cuda.synchronize()
+    oa, orr, om = oracle_mod.a1_encode(bits_of(kv), P, alpha)
+    same_bytes(anc, oa, "a1 anchor")
+    same_bytes(res, orr, "a1 residual")
+    same_bytes(meta, om, "a1 meta")
+    for r_gpu, r_or, what in ((res, orr, "full"), (None, None, "anchor")):
+        ref = oracle_mod.a1_decode(oa, r_or, om, L, P, alpha)
+        f32 = lynx_lib.lynx_a1_decode(anc, r_gpu, meta, L, P, alpha, torch.float32)
+        b16 = lynx_lib.lynx_a1_decode(anc, r_gpu, meta, L, P, alpha, torch.bfloat16)
+        torch.cuda.synchronize()
+        same_bytes(f32, ref, f"a1 decode {what}")
+        assert np.array_equal(bits_of(b16), oracle_mod.f32_to_bf16_bits(ref)), what
