@@ -341,39 +341,67 @@ a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, 
   }
 }
 
+// Decode of the A.1 variant: one thread per (run of 8 tokens, group of 8
+// channels); a run lies in one 16-token chunk, so m and m_i load once.
 template <bool BF16OUT>
-__global__ void __launch_bounds__(kA1Threads)
+__global__ void __launch_bounds__(kThreads)
 a1_decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ residual,
-                 const float* __restrict__ meta, const int64_t NB, const int H, const int64_t L,
-                 const int P, void* __restrict__ out, const __grid_constant__ ExpandTable tab) {
+                 const float* __restrict__ meta, const int64_t nblk, const int64_t NB,
+                 const int H, const int64_t L, const int P, void* __restrict__ out,
+                 const __grid_constant__ ExpandTable tab) {
   __shared__ float x[128];
-  const int tid = threadIdx.x, d = tid & 127, qt = tid >> 7;
-  if (tid < 128) x[tid] = tab.x[tid];
+  for (int i = threadIdx.x; i < 128; i += kThreads) x[i] = tab.x[i];
   __syncthreads();
-  const int64_t blk = blockIdx.x;
-  const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
-  const int NCk = P / kA1Chunk;
-  const float* mrow = meta + blk * (int64_t)(1 + NCk) * kD;
-  const float m = __ldg(mrow + d);
-  const int byte = (d >> 3) * 4 + (d & 3), sh = (d & 4) ? 4 : 0;
-  const uint8_t* a8 = anchor + blk * (int64_t)P * 64;
-  const uint8_t* r8 = residual ? residual + blk * (int64_t)P * 64 : nullptr;
-  const int span = P / kA1Split, t_lo = qt * span;
-#pragma unroll 4
-  for (int t = t_lo; t < t_lo + span; ++t) {
-    const float mi = __ldg(mrow + (1 + t / kA1Chunk) * kD + d);
-    int qa = (__ldg(a8 + t * 64 + byte) >> sh) & 0xf;
-    if (qa >= 8) qa -= 16;
-    const int Q = qa * 16 + (r8 ? (__ldg(r8 + t * 64 + byte) >> sh) & 0xf : 7);
-    int I = Q < 0 ? -Q : Q;
-    I = I > 127 ? 127 : I;
-    const float v = Q < 0 ? -x[I] : x[I];
-    const float y = __fmul_rn(__fmul_rn(v, mi), m);
-    const int64_t o = ((b * L + p * P + t) * H + h) * kD + d;
-    if constexpr (BF16OUT)
-      static_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(y);
-    else
-      static_cast<float*>(out)[o] = y;
+  const int NCk = P / kA1Chunk, runs = P / 8;
+  const int64_t items = nblk * runs * 16;
+  for (int64_t it = (int64_t)blockIdx.x * kThreads + threadIdx.x; it < items;
+       it += (int64_t)gridDim.x * kThreads) {
+    const int G = (int)(it & 15);
+    const int64_t rr = it >> 4;
+    const int t0 = (int)(rr % runs) * 8;
+    const int64_t blk = rr / runs;
+    const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
+    const float* mrow = meta + blk * (int64_t)(1 + NCk) * kD + 8 * G;
+    float m[8], mi[8];
+    {
+      const float4* p0 = reinterpret_cast<const float4*>(mrow);
+      const float4* p1 = reinterpret_cast<const float4*>(mrow + (1 + t0 / kA1Chunk) * kD);
+      const float4 u0 = __ldg(p0), u1 = __ldg(p0 + 1), v0 = __ldg(p1), v1 = __ldg(p1 + 1);
+      m[0] = u0.x; m[1] = u0.y; m[2] = u0.z; m[3] = u0.w;
+      m[4] = u1.x; m[5] = u1.y; m[6] = u1.z; m[7] = u1.w;
+      mi[0] = v0.x; mi[1] = v0.y; mi[2] = v0.z; mi[3] = v0.w;
+      mi[4] = v1.x; mi[5] = v1.y; mi[6] = v1.z; mi[7] = v1.w;
+    }
+    const int64_t code0 = (blk * P + t0) * 16 + G;   // 32-bit word of (token t0, group G)
+#pragma unroll 2
+    for (int u = 0; u < 8; ++u) {
+      const uint32_t wa = __ldg(reinterpret_cast<const uint32_t*>(anchor) + code0 + u * 16);
+      const uint32_t wr =
+          residual ? __ldg(reinterpret_cast<const uint32_t*>(residual) + code0 + u * 16)
+                   : 0x77777777u;                     // Anchor only: residual 7
+      float y[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int sh = 8 * (j & 3) + ((j & 4) ? 4 : 0);
+        int qa = (int)((wa >> sh) & 0xfu);
+        if (qa >= 8) qa -= 16;
+        const int Q = qa * 16 + (int)((wr >> sh) & 0xfu);
+        int I = Q < 0 ? -Q : Q;
+        I = I > 127 ? 127 : I;
+        const float v = Q < 0 ? -x[I] : x[I];
+        y[j] = __fmul_rn(__fmul_rn(v, mi[j]), m[j]);
+      }
+      const int64_t o = ((b * L + p * P + t0 + u) * H + h) * kD + 8 * G;
+      if constexpr (BF16OUT) {
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) =
+            make_uint4(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]), f2_to_bf2(y[4], y[5]),
+                       f2_to_bf2(y[6], y[7]));
+      } else {
+        float4* q = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+        q[0] = make_float4(y[0], y[1], y[2], y[3]);
+        q[1] = make_float4(y[4], y[5], y[6], y[7]);
+      }
+    }
   }
 }
 
@@ -439,12 +467,13 @@ cudaError_t launch_a1_decode(const void* anchor, const void* residual, const flo
   if (nblk > 0x7fffffff) return cudaErrorInvalidValue;
   const uint8_t* a = static_cast<const uint8_t*>(anchor);
   const uint8_t* r = static_cast<const uint8_t*>(residual);
+  const unsigned grid = grid_for(nblk * (s.page / 8) * 16, kThreads);
   if (bf16_out)
-    a1_decode_kernel<true><<<(unsigned)nblk, kA1Threads, 0, stream>>>(a, r, meta, s.NB(), s.H,
-                                                                      s.L, s.page, out, tab);
+    a1_decode_kernel<true><<<grid, kThreads, 0, stream>>>(a, r, meta, nblk, s.NB(), s.H, s.L,
+                                                          s.page, out, tab);
   else
-    a1_decode_kernel<false><<<(unsigned)nblk, kA1Threads, 0, stream>>>(a, r, meta, s.NB(), s.H,
-                                                                       s.L, s.page, out, tab);
+    a1_decode_kernel<false><<<grid, kThreads, 0, stream>>>(a, r, meta, nblk, s.NB(), s.H, s.L,
+                                                           s.page, out, tab);
   return cudaGetLastError();
 }
 
