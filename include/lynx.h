@@ -79,7 +79,8 @@ int lynx_encoded_sizes(int64_t B, int64_t L, int H_kv, int D, int page, int C,
  *            S = sign(n - mu) (+1 at zero).
  *   Stage 4: Q8 = I*S + min(S,0) (Eq. 9); Anchor = Q8 >> 4, Residual = Q8 & 15.
  * Statistics are float32 with one rounding per operation in the order above;
- * Round is exact with respect to the float64 value of Eq. 7.
+ * Round is exact with respect to the float64 value of Eq. 7.  alpha must be
+ * >= 1 (the pages use 100 to 2000); smaller values give LYNX_EUNSUPPORTED.
  *   kv        [B][L][H_kv][D] BF16, device, read only
  *   anchor    device, lynx_encoded_sizes() bytes, written
  *   residual  device, written

@@ -20,8 +20,13 @@ struct ExpandTable {
 };
 
 // Fast-path rounding window of the encoder, in units of 2^-16 of Y:
-// results within this distance of a half-integer take the exact path.
-constexpr uint32_t kAmbiguityK = 8;
+// results within this distance of a half-integer take the exact path.  The
+// fast path's error grows with c16 = 65536 * 127 / log2(1 + alpha); over all
+// float32 inputs it stays below 2 units for every alpha >= 1 checked (largest
+// at alpha = 1), so the encoder accepts alpha >= 1 and keeps a window of
+// twice that.
+constexpr uint32_t kAmbiguityK = 4;
+constexpr float kMinEncodeAlpha = 1.0f;
 
 struct Shape {
   int64_t B, L;

@@ -107,6 +107,15 @@ static int check_alpha(float alpha) {
   return LYNX_OK;
 }
 
+// The encoder's fast Stage-3 rounding is exact (with its window) for alpha >= 1.
+static int check_encode_alpha(float alpha) {
+  int rc = check_alpha(alpha);
+  if (rc) return rc;
+  if (alpha < kMinEncodeAlpha)
+    return fail(LYNX_EUNSUPPORTED, "alpha = %g: the encoder is built for alpha >= 1", alpha);
+  return LYNX_OK;
+}
+
 static int check_codec_shape(int64_t B, int64_t L, int H, int D, int page, int C) {
   if (B < 0 || L < 0 || H <= 0) return fail(LYNX_ESHAPE, "need B >= 0, L >= 0, H_kv >= 1");
   if (D != kD) return fail(LYNX_EUNSUPPORTED, "D = %d: only D = 128 is built", D);
@@ -197,7 +206,7 @@ int lynx_encode_paged(const void* kv, int64_t B, int64_t L, int H_kv, int D, int
                       void* anchor_pool, void* residual_pool, float* meta_pool, void* stream) {
   int rc = check_codec_shape(B, L, H_kv, D, page, C);
   if (rc) return rc;
-  if ((rc = check_alpha(alpha))) return rc;
+  if ((rc = check_encode_alpha(alpha))) return rc;
   if (B * L == 0) return LYNX_OK;
   Paging pg;
   if ((rc = check_paging(block_table, num_blocks, &pg))) return rc;
@@ -235,7 +244,7 @@ int lynx_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page,
                 float alpha, void* anchor, void* residual, float* meta, void* stream) {
   int rc = check_codec_shape(B, L, H_kv, D, page, C);
   if (rc) return rc;
-  if ((rc = check_alpha(alpha))) return rc;
+  if ((rc = check_encode_alpha(alpha))) return rc;
   if (B * L == 0) return LYNX_OK;  // nothing to encode; pointers are not examined
   if ((rc = check_ptrs({kv, anchor, residual, meta}))) return rc;
   Shape s{B, L, H_kv, D, page, C};

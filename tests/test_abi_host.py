@@ -53,6 +53,7 @@ OK = ctypes.c_void_p(0x10000)     # aligned, never dereferenced: every call belo
     (dict(alpha=0.0), -1),
     (dict(alpha=float("nan")), -1),
     (dict(alpha=float("inf")), -1),
+    (dict(alpha=0.5), -3),            # the encoder is built for alpha >= 1
     (dict(kv=None), -1),
     (dict(kv=BAD), -1),
     (dict(H=0), -2),
