@@ -72,50 +72,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
-// Stages 3-4 for one token row of a thread's 8 channels: d (centred
-// values, as (k, k+1) pairs of channels 8g+2k..) scaled by rs, companded,
-// sign-mapped, split into the Anchor word w0 and the Residual word w1 of
-// the nibble layout.  Returns whether a fast code lay within the ambiguity
-// window; with `exact`, such codes are decided against the thresholds.
-__device__ __forceinline__ bool code_row(const f2 (&d)[4], const f2 (&rs2)[4], f2 alpha2,
-                                         f2 c16_2, const CompanderTable& tab, bool exact,
-                                         uint32_t& w0, uint32_t& w1) {
-  float a[8];
-  uint32_t bits[8], dbits[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const f2 xf = mul2(d[k], rs2[k]);
-    a[2 * k] = fabsf(xf.x);
-    a[2 * k + 1] = fabsf(xf.y);
-    dbits[2 * k] = __float_as_uint(d[k].x);
-    dbits[2 * k + 1] = __float_as_uint(d[k].y);
-    compand_fast2(make_float2(a[2 * k], a[2 * k + 1]), alpha2, c16_2, bits[2 * k],
-                  bits[2 * k + 1]);
-  }
-  // smallest distance to a rounding boundary (low 16 bits) of the 8 values,
-  // two at a time in 16-bit lanes
-  uint32_t dmin = __vminu2(prmt(bits[0], bits[1], 0x5410u), prmt(bits[2], bits[3], 0x5410u));
-  dmin = __vminu2(dmin, __vminu2(prmt(bits[4], bits[5], 0x5410u), prmt(bits[6], bits[7], 0x5410u)));
-  const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
-  if (exact) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (compand_ambiguous(bits[i]))
-        bits[i] = (bits[i] & 0xff00ffffu) | (compand_exact(bits[i], a[i], tab.thr) << 16);
-  }
-  // code bytes (byte 2 of bits) xor the replicated sign of d
-  const uint32_t i01 = prmt(bits[0], bits[1], 0x0062u), i23 = prmt(bits[2], bits[3], 0x0062u);
-  const uint32_t i45 = prmt(bits[4], bits[5], 0x0062u), i67 = prmt(bits[6], bits[7], 0x0062u);
-  const uint32_t s01 = prmt(dbits[0], dbits[1], 0x00fbu), s23 = prmt(dbits[2], dbits[3], 0x00fbu);
-  const uint32_t s45 = prmt(dbits[4], dbits[5], 0x00fbu), s67 = prmt(dbits[6], dbits[7], 0x00fbu);
-  const uint32_t W0 = prmt(i01 ^ s01, i23 ^ s23, 0x5410u);
-  const uint32_t W1 = prmt(i45 ^ s45, i67 ^ s67, 0x5410u);
-  // byte k: Anchor = (ch k high nibble) | (ch k+4 high nibble) << 4, etc.
-  w0 = ((W0 >> 4) & 0x0f0f0f0fu) | (W1 & 0xf0f0f0f0u);
-  w1 = (W0 & 0x0f0f0f0fu) | ((W1 << 4) & 0xf0f0f0f0u);
-  return amb;
-}
-
 template <int P, int C>
 struct EncGeom {
   static constexpr int kThreads = 2 * P;
@@ -357,65 +313,47 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       if (j & 1) rs2[j >> 1].y = r; else rs2[j >> 1].x = r;
     }
 
-    // ---- Stages 3-4: codes, sign map, nibble split, store one row per m.
-    // The fast path decides every code; a value within the ambiguity window
-    // only sets its row's bit in ambm.  The rows so marked are redone exactly
-    // after the loop, so the loop itself has no branch and its iterations
-    // interleave.
+    // ---- Stages 3-4: codes, sign map, nibble split, store one row per m
     uint32_t* arow = anchor + pb * (int64_t)(P * 16);
     uint32_t* rrow = residual + pb * (int64_t)(P * 16);
-    uint32_t ambm = 0;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
       const int t = c * C + G::kTL * m + tl;
-      uint32_t w0, w1;
-      const bool amb = code_row(n[m], rs2, alpha2, c16_2, tab, false, w0, w1);
-      ambm |= amb ? (1u << m) : 0u;
-      arow[t * 16 + g] = w0;
-      rrow[t * 16 + g] = w1;
-    }
-    if (__any_sync(kFull, ambm != 0u)) {
-      // Recompute the marked rows from the staged tile, the page partials in
-      // shared memory and this warp's chunk means (written to meta above),
-      // with the same operations as stages 1-2, and decide their codes
-      // against the thresholds.
-      __syncwarp();
-      f2 gmf[4], rgf[4], muf[4];
+      float a[8];
+      uint32_t bits[8], dbits[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int ch = 8 * g + j;
-        float lo = pmn[ch], hi = pmx[ch];
-#pragma unroll 1
-        for (int cc = 1; cc < G::kNC; ++cc) {
-          lo = fminf(lo, pmn[cc * kD + ch]);
-          hi = fmaxf(hi, pmx[cc * kD + ch]);
-        }
-        if (lo == 0.0f) lo = -0.0f;
-        if (hi == 0.0f) hi = 0.0f;
-        const float rg = __frcp_rn(__fadd_rn(__fsub_rn(hi, lo), kEps));
-        const float mu = mrow[(2 + c) * kD + ch];
-        if (j & 1) { gmf[j >> 1].y = lo; rgf[j >> 1].y = rg; muf[j >> 1].y = mu; }
-        else       { gmf[j >> 1].x = lo; rgf[j >> 1].x = rg; muf[j >> 1].x = mu; }
+      for (int k = 0; k < 4; ++k) {
+        const f2 xf = mul2(n[m][k], rs2[k]);
+        a[2 * k] = fabsf(xf.x);
+        a[2 * k + 1] = fabsf(xf.y);
+        dbits[2 * k] = __float_as_uint(n[m][k].x);
+        dbits[2 * k + 1] = __float_as_uint(n[m][k].y);
+        compand_fast2(make_float2(a[2 * k], a[2 * k + 1]), alpha2, c16_2, bits[2 * k],
+                      bits[2 * k + 1]);
       }
-#pragma unroll 1
-      for (int m = 0; m < 8; ++m) {
-        if (!((ambm >> m) & 1u)) continue;
-        const int t = c * C + G::kTL * m + tl;
-        const uint4 v = tile[t * 16 + g];
-        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-        f2 nm[4];
+      // smallest distance to a rounding boundary (low 16 bits) of the 8
+      // values, two at a time in 16-bit lanes
+      uint32_t dmin = __vminu2(prmt(bits[0], bits[1], 0x5410u), prmt(bits[2], bits[3], 0x5410u));
+      dmin = __vminu2(dmin, __vminu2(prmt(bits[4], bits[5], 0x5410u), prmt(bits[6], bits[7], 0x5410u)));
+      const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
+      if (__any_sync(kFull, amb)) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const f2 d = bf2_sub_f32(vv[k], gmf[k]);
-          nm[k].x = __fmul_rn(d.x, rgf[k].x);
-          nm[k].y = __fmul_rn(d.y, rgf[k].y);
-          nm[k] = sub2(nm[k], muf[k]);
-        }
-        uint32_t w0, w1;
-        (void)code_row(nm, rs2, alpha2, c16_2, tab, true, w0, w1);
-        arow[t * 16 + g] = w0;
-        rrow[t * 16 + g] = w1;
+        for (int i = 0; i < 8; ++i)
+          if (compand_ambiguous(bits[i]))
+            bits[i] = (bits[i] & 0xff00ffffu) | (compand_exact(bits[i], a[i], tab.thr) << 16);
       }
+      // code bytes (byte 2 of bits) xor the replicated sign of d
+      const uint32_t i01 = prmt(bits[0], bits[1], 0x0062u), i23 = prmt(bits[2], bits[3], 0x0062u);
+      const uint32_t i45 = prmt(bits[4], bits[5], 0x0062u), i67 = prmt(bits[6], bits[7], 0x0062u);
+      const uint32_t s01 = prmt(dbits[0], dbits[1], 0x00fbu), s23 = prmt(dbits[2], dbits[3], 0x00fbu);
+      const uint32_t s45 = prmt(dbits[4], dbits[5], 0x00fbu), s67 = prmt(dbits[6], dbits[7], 0x00fbu);
+      const uint32_t W0 = prmt(i01 ^ s01, i23 ^ s23, 0x5410u);
+      const uint32_t W1 = prmt(i45 ^ s45, i67 ^ s67, 0x5410u);
+      // byte k: Anchor = (ch k high nibble) | (ch k+4 high nibble) << 4, etc.
+      const uint32_t Aw = ((W0 >> 4) & 0x0f0f0f0fu) | (W1 & 0xf0f0f0f0u);
+      const uint32_t Rw = (W0 & 0x0f0f0f0fu) | ((W1 << 4) & 0xf0f0f0f0u);
+      arow[t * 16 + g] = Aw;
+      rrow[t * 16 + g] = Rw;
     }
   }
 }
