@@ -882,7 +882,9 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
 
 // Merge the partials of one query row of one unit (sequence, KV head, row
 // group): the CTAs whose shares touch the unit, each through the partial of
-// the matching segment.  One block per (unit, row), one thread per channel:
+// the matching segment.  One warp per (unit, row), four channels a lane; the
+// splits merge online (running max, rescaled sums), kCombineBatch of them per
+// round of independent loads:
 // out = sum e^(m_s-M) o_s / sum e^(m_s-M) l_s, written to out[b][t][hq][:].
 // With the draft tokens' own keys and values, query token t also attends to
 // draft tokens 0..t ("Lynx", Mechanism 3, single parallel verification
@@ -890,54 +892,74 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
 __device__ __forceinline__ float bf16_to_f32(uint16_t x) {
   return __uint_as_float((uint32_t)x << 16);
 }
-__global__ void __launch_bounds__(kD) attn_combine(const __grid_constant__ AttnParams a, int RP) {
-  __shared__ float red[kD / 32];
-  __shared__ float s_tail[64];               // draft tokens: T <= 64
+constexpr int kCombineWarps = 4;
+constexpr int kCombineBatch = 8;
+__global__ void __launch_bounds__(32 * kCombineWarps)
+attn_combine(const __grid_constant__ AttnParams a, int RP) {
+  const int lane = threadIdx.x & 31;
   const int64_t z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
-  const int r = blockIdx.y;
+  const int r = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
+  if (r >= RP) return;
   const int rg = (int)(z % a.nrg), bh = (int)(z / a.nrg), h = bh % a.Hkv, b = bh / a.Hkv;
   const int row = rg * RP + r;
   if (row >= a.R) return;
-  const int d = threadIdx.x;
   const int tq = row / a.G, gq = row % a.G;
   const int part_floats = 2 * RP + RP * kD;
   // CTA holding flattened chunk x: floor(((x + 1) n_cta - 1) / n_chunks)
   const int64_t first = z * a.NCH, last = first + a.NCH - 1;
   const int k0 = (int)(((first + 1) * a.n_cta - 1) / a.n_chunks);
   const int k1 = (int)(((last + 1) * a.n_cta - 1) / a.n_chunks);
-  float M = -INFINITY;
-  for (int k = k0; k <= k1; ++k) {
-    const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
-    M = fmaxf(M, a.part[(2 * k + seg) * part_floats + r]);
+  float M = -INFINITY, Lsum = 0.f;
+  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto merge = [&](float m, float l, float4 o) {
+    if (m == -INFINITY) return;                 // a share with no chunk of this unit
+    const float Mn = fmaxf(M, m);
+    const float fo = exp2f(M - Mn), fn = exp2f(m - Mn);  // exp2(-inf) = 0 on the first
+    O.x = O.x * fo + fn * o.x; O.y = O.y * fo + fn * o.y;
+    O.z = O.z * fo + fn * o.z; O.w = O.w * fo + fn * o.w;
+    Lsum = Lsum * fo + fn * l;
+    M = Mn;
+  };
+  for (int kb = k0; kb <= k1; kb += kCombineBatch) {
+    float mv[kCombineBatch], lv[kCombineBatch];
+    float4 ov[kCombineBatch];
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) {
+      const int k = kb + i;
+      if (k <= k1) {
+        const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
+        const float* ps = a.part + (2 * k + seg) * part_floats;
+        mv[i] = ps[r];
+        lv[i] = ps[RP + r];
+        ov[i] = *reinterpret_cast<const float4*>(ps + 2 * RP + r * kD + 4 * lane);
+      } else {
+        mv[i] = -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kCombineBatch; ++i) merge(mv[i], lv[i], ov[i]);
   }
-  const int ntail = a.kt ? tq + 1 : 0;
-  if (ntail) {
-    const float qd = bf16_to_f32(a.q[((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + d]);
-    for (int j = 0; j < ntail; ++j) {
-      float prod = qd * bf16_to_f32(a.kt[((int64_t)(b * a.T + j) * a.Hkv + h) * kD + d]);
+  if (a.kt) {
+    const uint2 qw = *reinterpret_cast<const uint2*>(
+        a.q + ((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + 4 * lane);
+    const float q0 = bf16_to_f32((uint16_t)qw.x), q1 = bf16_to_f32((uint16_t)(qw.x >> 16));
+    const float q2 = bf16_to_f32((uint16_t)qw.y), q3 = bf16_to_f32((uint16_t)(qw.y >> 16));
+    for (int j = 0; j <= tq; ++j) {
+      const int64_t off = ((int64_t)(b * a.T + j) * a.Hkv + h) * kD + 4 * lane;
+      const uint2 kw = *reinterpret_cast<const uint2*>(a.kt + off);
+      float prod = q0 * bf16_to_f32((uint16_t)kw.x) + q1 * bf16_to_f32((uint16_t)(kw.x >> 16)) +
+                   q2 * bf16_to_f32((uint16_t)kw.y) + q3 * bf16_to_f32((uint16_t)(kw.y >> 16));
 #pragma unroll
       for (int o = 16; o; o >>= 1) prod += __shfl_xor_sync(kFull, prod, o);
-      if ((d & 31) == 0) red[d >> 5] = prod;
-      __syncthreads();
-      if (d == 0) s_tail[j] = (red[0] + red[1] + red[2] + red[3]) * a.scale_log2;
-      __syncthreads();
+      const uint2 vw = *reinterpret_cast<const uint2*>(a.vt + off);
+      merge(prod * a.scale_log2, 1.0f,
+            make_float4(bf16_to_f32((uint16_t)vw.x), bf16_to_f32((uint16_t)(vw.x >> 16)),
+                        bf16_to_f32((uint16_t)vw.y), bf16_to_f32((uint16_t)(vw.y >> 16))));
     }
-    for (int j = 0; j < ntail; ++j) M = fmaxf(M, s_tail[j]);
   }
-  float num = 0.f, den = 0.f;
-  for (int k = k0; k <= k1; ++k) {
-    const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
-    const float* ps = a.part + (2 * k + seg) * part_floats;
-    const float f = ps[r] == -INFINITY ? 0.f : exp2f(ps[r] - M);
-    num += f * ps[2 * RP + r * kD + d];
-    den += f * ps[RP + r];
-  }
-  for (int j = 0; j < ntail; ++j) {
-    const float f = exp2f(s_tail[j] - M);
-    num += f * bf16_to_f32(a.vt[((int64_t)(b * a.T + j) * a.Hkv + h) * kD + d]);
-    den += f;
-  }
-  a.out[((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD + d] = num / den;
+  *reinterpret_cast<float4*>(a.out + ((int64_t)(b * a.T + tq) * a.Hq + h * a.G + gq) * kD +
+                             4 * lane) =
+      make_float4(O.x / Lsum, O.y / Lsum, O.z / Lsum, O.w / Lsum);
 }
 
 // ------------------------------------------------------------------ host
@@ -1001,8 +1023,9 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   fn<<<(unsigned)prm.n_cta, threads, smem, stream>>>(prm, tab);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine<<<dim3((unsigned)(prm.batch * prm.Hkv * prm.nrg), (unsigned)(8 * NT)), kD, 0,
-                 stream>>>(prm, 8 * NT);
+  attn_combine<<<dim3((unsigned)(prm.batch * prm.Hkv * prm.nrg),
+                      (unsigned)((8 * NT + kCombineWarps - 1) / kCombineWarps)),
+                 32 * kCombineWarps, 0, stream>>>(prm, 8 * NT);
   return cudaGetLastError();
 }
 
