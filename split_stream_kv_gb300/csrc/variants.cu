@@ -269,6 +269,34 @@ constexpr int kA1Chunk = 16;
 constexpr int kA1Split = 4;
 constexpr int kA1Threads = 128 * kA1Split;
 
+// |Q| = Round(Y(a)) of Eq. 7.  FAST (alpha >= 1): the encoder's Stage-3 fast
+// path per lane (t = rn(alpha a + 1), MUFU lg2, s = rd(lg2(t) c16 + C0): the
+// code in byte 2, its distance to the rounding boundary in the low 16 bits),
+// the same operations whose window the exhaustive self-check verifies, with
+// the threshold deciding inside the window; otherwise a binary search over
+// the thresholds.
+constexpr float kA1C0 = 8388608.0f + 32768.0f + (float)kAmbiguityK;
+template <bool FAST>
+__device__ __forceinline__ int a1_round(float a, float alpha, float c16, const float* thr) {
+  if constexpr (FAST) {
+    const float t = __fmaf_rn(alpha, a, 1.0f);
+    const uint32_t bits = __float_as_uint(fma_rm(lg2_approx(t), c16, kA1C0));
+    int I = (int)((bits >> 16) & 0xffu);
+    if ((bits & 0xffffu) < 2u * kAmbiguityK) {
+      const int b = I > 0 ? I - 1 : 0;
+      I = b + (a >= thr[b] ? 1 : 0);
+    }
+    return I;
+  } else {
+    int I = 0;                                     // #{k < 127 : a >= thr[k]}
+#pragma unroll
+    for (int step = 64; step; step >>= 1)
+      if (I + step <= 127 && a >= thr[I + step - 1]) I += step;
+    return I;
+  }
+}
+
+template <bool FAST>
 __global__ void __launch_bounds__(kA1Threads)
 a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, const int64_t L,
                  const int P, uint8_t* __restrict__ anchor, uint8_t* __restrict__ residual,
@@ -316,11 +344,7 @@ a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, 
 #pragma unroll
     for (int i = 0; i < kA1Chunk; ++i) {
       const float xpp = __fmul_rn(xp[i], rmi);
-      const float a = fabsf(xpp);
-      int I = 0;                                     // #{k < 127 : a >= thr[k]}
-#pragma unroll
-      for (int step = 64; step; step >>= 1)
-        if (I + step <= 127 && a >= thr[I + step - 1]) I += step;
+      const int I = a1_round<FAST>(fabsf(xpp), tab.alpha, tab.c16, thr);
       const int Q = xpp > 0.0f ? I : (xpp < 0.0f ? -I : 0);
       const uint32_t na = (uint32_t)(Q >> 4) & 0xfu, nr = (uint32_t)Q & 0xfu;
       // channel d and d^4 share a byte: the low-nibble thread writes both
@@ -447,14 +471,18 @@ cudaError_t launch_a1_encode(const void* kv, const Shape& s, const CompanderTabl
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured != dev) {
-    e = cudaFuncSetAttribute(a1_encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(a1_encode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             256 * 384 + (128 + 128 * kA1Split) * 4);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(a1_encode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              256 * 384 + (128 + 128 * kA1Split) * 4);
     if (e != cudaSuccess) return e;
     configured = dev;
   }
   const int64_t nblk = s.blocks();
   if (nblk > 0x7fffffff) return cudaErrorInvalidValue;
-  a1_encode_kernel<<<(unsigned)nblk, kA1Threads, smem, stream>>>(
+  auto fn = tab.alpha >= kMinEncodeAlpha ? a1_encode_kernel<true> : a1_encode_kernel<false>;
+  fn<<<(unsigned)nblk, kA1Threads, smem, stream>>>(
       static_cast<const uint8_t*>(kv), s.NB(), s.H, s.L, s.page, static_cast<uint8_t*>(anchor),
       static_cast<uint8_t*>(residual), meta, tab);
   return cudaGetLastError();

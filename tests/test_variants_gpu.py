@@ -171,7 +171,7 @@ A1_CASES = [(2, 512, 2, 128), (1, 512, 3, 256), (3, 256, 1, 64)]
 
 
 @pytest.mark.parametrize("B,L,H,P", A1_CASES)
-@pytest.mark.parametrize("alpha", [100.0, 255.0])
+@pytest.mark.parametrize("alpha", [100.0, 255.0, 1.0, 0.5])
 def test_a1_variant_matches_oracle(lynx_lib, oracle_mod, cuda_dev, B, L, H, P, alpha):
     from split_stream_kv_gb300 import synth
     kv = synth.kv_cache(B, L, H, 128, seed=B * 3 + L + P, device=cuda_dev, n_outlier=2)
