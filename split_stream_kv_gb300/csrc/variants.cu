@@ -33,53 +33,71 @@ __device__ __forceinline__ uint2 ldg_stream8(const void* p) {
 
 // ----------------------------------------------------------------- INT-B
 
-// One token row of 128 BF16 channels per warp, 4 channels a lane; R rows in
-// flight per warp.
+// One token row of 128 BF16 channels per half-warp, 8 channels a lane (one
+// 16-byte load), so a warp instruction serves two rows and the per-row work
+// (min / max reduction, scale, reciprocal) spreads over 256 elements; R rows
+// in flight per half-warp.
 template <int BITS>
 __global__ void __launch_bounds__(kThreads) int_encode_kernel(const uint8_t* __restrict__ x,
                                                               const int64_t rows,
                                                               uint8_t* __restrict__ codes,
                                                               float2* __restrict__ meta) {
-  constexpr int R = 8;
+  constexpr int R = 4;
   constexpr int qmax = (1 << BITS) - 1;
-  const int lane = threadIdx.x & 31;
-  const int64_t warp = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-  const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
-  for (int64_t r0 = warp * R; r0 < rows; r0 += nwarps * R) {
-    uint2 v[R];
+  const int lane = threadIdx.x & 31, hl = lane & 15;
+  const int64_t half = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 4;
+  const int64_t nhalves = ((int64_t)gridDim.x * kThreads) >> 4;
+  // both halves of a warp iterate the same number of times (rows are
+  // assigned in whole warps), so the shuffles below always see 32 lanes
+  const int64_t base0 = (half & ~1ll) * R;
+  for (int64_t r0 = base0; r0 < rows; r0 += nhalves * R) {
+    const int64_t myr0 = r0 + (half & 1) * R;
+    uint4 v[R];
 #pragma unroll
     for (int i = 0; i < R; ++i)
-      v[i] = r0 + i < rows ? ldg_stream8(x + (r0 + i) * 256 + lane * 8) : make_uint2(0u, 0u);
+      v[i] = myr0 + i < rows ? ldg_stream(x + (myr0 + i) * 256 + hl * 16) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int i = 0; i < R; ++i) {
-      const int64_t row = r0 + i;
-      if (row >= rows) break;  // uniform across the warp
-      const float f[4] = {bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y)};
-      float lo = fminf(fminf(f[0], f[1]), fminf(f[2], f[3]));
-      float hi = fmaxf(fmaxf(f[0], f[1]), fmaxf(f[2], f[3]));
+      const int64_t row = myr0 + i;
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+      float f[8];
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
+      for (int j = 0; j < 4; ++j) {
+        f[2 * j] = bf16_lo(w[j]);
+        f[2 * j + 1] = bf16_hi(w[j]);
+      }
+      float lo = f[0], hi = f[0];
+#pragma unroll
+      for (int j = 1; j < 8; ++j) {
+        lo = fminf(lo, f[j]);
+        hi = fmaxf(hi, f[j]);
+      }
+#pragma unroll
+      for (int o = 8; o; o >>= 1) {                // within the half-warp
         lo = fminf(lo, __shfl_xor_sync(kFull, lo, o));
         hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, o));
       }
+      if (row >= rows) continue;
       lo = __fadd_rn(lo, 0.0f);  // a zero extreme counts as +0
       hi = __fadd_rn(hi, 0.0f);
       const float S = __fdiv_rn(__fsub_rn(hi, lo), (float)qmax);
       const float rs = S > 0.0f ? __frcp_rn(S) : 0.0f;
-      uint32_t q[4];
+      uint32_t q[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        int c = __float2int_rn(__fmul_rn(__fsub_rn(f[j], lo), rs));
+      for (int j = 0; j < 8; ++j) {
+        const int c = __float2int_rn(__fmul_rn(__fsub_rn(f[j], lo), rs));
         q[j] = (uint32_t)(c < 0 ? 0 : c > qmax ? qmax : c);
       }
       if constexpr (BITS == 8) {
-        *reinterpret_cast<uint32_t*>(codes + row * 128 + lane * 4) =
-            q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24);
+        *reinterpret_cast<uint2*>(codes + row * 128 + hl * 8) =
+            make_uint2(q[0] | (q[1] << 8) | (q[2] << 16) | (q[3] << 24),
+                       q[4] | (q[5] << 8) | (q[6] << 16) | (q[7] << 24));
       } else {
-        *reinterpret_cast<uint16_t*>(codes + row * 64 + lane * 2) =
-            (uint16_t)(q[0] | (q[1] << 4) | (q[2] << 8) | (q[3] << 12));
+        *reinterpret_cast<uint32_t*>(codes + row * 64 + hl * 4) =
+            q[0] | (q[1] << 4) | (q[2] << 8) | (q[3] << 12) | (q[4] << 16) | (q[5] << 20) |
+            (q[6] << 24) | (q[7] << 28);
       }
-      if (lane == 0) meta[row] = make_float2(lo, S);
+      if (hl == 0) meta[row] = make_float2(lo, S);
     }
   }
 }
@@ -521,7 +539,7 @@ int lynx_int_encode(const void* kv, int64_t rows, int D, int bits, void* codes, 
   if (!aligned(kv, 16) || !aligned(codes, 16) || !aligned(meta, 16))
     return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const unsigned grid = grid_for((rows + 7) / 8, kThreads / 32);
+  const unsigned grid = grid_for((rows + 7) / 8, kThreads / 32);  // 2 halves x 4 rows a warp
   if (bits == 8)
     int_encode_kernel<8><<<grid, kThreads, 0, st>>>(static_cast<const uint8_t*>(kv), rows,
                                                     static_cast<uint8_t*>(codes),
