@@ -144,9 +144,10 @@ __device__ __forceinline__ uint64_t group_codes(uint32_t a, uint32_t r) {
   return (uint64_t)lo | ((uint64_t)hi << 32);
 }
 
-// One thread per (token row, group): the k-bit fields of the 8 codes'
-// top bits into K bytes, the low 8-K bits into 8-K bytes (channel j at bits
-// j*w .. j*w + w - 1, little-endian).
+// One thread per 4 consecutive groups (32 channels of one token row): the
+// k-bit fields of the 8 codes' top bits of a group fill K bytes, the low 8-K
+// bits 8-K bytes (channel j at bits j*w .. j*w + w - 1, little-endian), so 4
+// groups are K and 8-K whole 32-bit words.
 template <int K>
 __global__ void __launch_bounds__(kThreads) split_bits_kernel(const uint8_t* __restrict__ anchor,
                                                               const uint8_t* __restrict__ residual,
@@ -154,22 +155,43 @@ __global__ void __launch_bounds__(kThreads) split_bits_kernel(const uint8_t* __r
                                                               uint8_t* __restrict__ ak,
                                                               uint8_t* __restrict__ rk) {
   constexpr int RW = 8 - K;
-  for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < groups;
-       gi += (int64_t)gridDim.x * kThreads) {
-    const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(anchor) + gi);
-    const uint32_t r = __ldg(reinterpret_cast<const uint32_t*>(residual) + gi);
-    const uint64_t c = group_codes(a, r);
-    uint64_t fa = 0, fr = 0;
+  const int64_t quads = groups / 4;
+  for (int64_t qi = (int64_t)blockIdx.x * kThreads + threadIdx.x; qi < quads;
+       qi += (int64_t)gridDim.x * kThreads) {
+    const uint4 a4 = __ldg(reinterpret_cast<const uint4*>(anchor) + qi);
+    const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(residual) + qi);
+    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w}, rw[4] = {r4.x, r4.y, r4.z, r4.w};
+    uint32_t oa[K], orr[RW];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t q8 = (uint32_t)(c >> (8 * j)) & 0xffu;
-      fa |= (uint64_t)(q8 >> RW) << (j * K);
-      fr |= (uint64_t)(q8 & ((1u << RW) - 1u)) << (j * RW);
+    for (int i = 0; i < K; ++i) oa[i] = 0;
+#pragma unroll
+    for (int i = 0; i < RW; ++i) orr[i] = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint64_t c = group_codes(aw[q], rw[q]);
+      uint64_t fa = 0, fr = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t q8 = (uint32_t)(c >> (8 * j)) & 0xffu;
+        fa |= (uint64_t)(q8 >> RW) << (j * K);
+        fr |= (uint64_t)(q8 & ((1u << RW) - 1u)) << (j * RW);
+      }
+      // bytes q*K .. q*K+K-1 of the thread's 4K anchor bytes
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int byte = q * K + i;
+        oa[byte >> 2] |= (uint32_t)((fa >> (8 * i)) & 0xffu) << (8 * (byte & 3));
+      }
+#pragma unroll
+      for (int i = 0; i < RW; ++i) {
+        const int byte = q * RW + i;
+        orr[byte >> 2] |= (uint32_t)((fr >> (8 * i)) & 0xffu) << (8 * (byte & 3));
+      }
     }
 #pragma unroll
-    for (int i = 0; i < K; ++i) ak[gi * K + i] = (uint8_t)(fa >> (8 * i));
+    for (int i = 0; i < K; ++i) reinterpret_cast<uint32_t*>(ak)[qi * K + i] = oa[i];
 #pragma unroll
-    for (int i = 0; i < RW; ++i) rk[gi * RW + i] = (uint8_t)(fr >> (8 * i));
+    for (int i = 0; i < RW; ++i) reinterpret_cast<uint32_t*>(rk)[qi * RW + i] = orr[i];
   }
 }
 
@@ -180,24 +202,42 @@ __global__ void __launch_bounds__(kThreads) join_bits_kernel(const uint8_t* __re
                                                              uint32_t* __restrict__ anchor,
                                                              uint32_t* __restrict__ residual) {
   constexpr int RW = 8 - K;
-  for (int64_t gi = (int64_t)blockIdx.x * kThreads + threadIdx.x; gi < groups;
-       gi += (int64_t)gridDim.x * kThreads) {
-    uint64_t fa = 0, fr = 0;
+  const int64_t quads = groups / 4;
+  for (int64_t qi = (int64_t)blockIdx.x * kThreads + threadIdx.x; qi < quads;
+       qi += (int64_t)gridDim.x * kThreads) {
+    uint32_t ia[K], ir[RW];
 #pragma unroll
-    for (int i = 0; i < K; ++i) fa |= (uint64_t)__ldg(ak + gi * K + i) << (8 * i);
+    for (int i = 0; i < K; ++i) ia[i] = __ldg(reinterpret_cast<const uint32_t*>(ak) + qi * K + i);
 #pragma unroll
-    for (int i = 0; i < RW; ++i) fr |= (uint64_t)__ldg(rk + gi * RW + i) << (8 * i);
-    uint32_t a = 0, r = 0;
+    for (int i = 0; i < RW; ++i) ir[i] = __ldg(reinterpret_cast<const uint32_t*>(rk) + qi * RW + i);
+    uint32_t a[4], r[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t q8 = ((uint32_t)(fa >> (j * K)) & ((1u << K) - 1u)) << RW |
-                          ((uint32_t)(fr >> (j * RW)) & ((1u << RW) - 1u));
-      const int sh = 8 * (j & 3) + ((j & 4) ? 4 : 0);  // byte j&3, high nibble for j >= 4
-      a |= (q8 >> 4) << sh;
-      r |= (q8 & 15u) << sh;
+    for (int q = 0; q < 4; ++q) {
+      uint64_t fa = 0, fr = 0;
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        const int byte = q * K + i;
+        fa |= (uint64_t)((ia[byte >> 2] >> (8 * (byte & 3))) & 0xffu) << (8 * i);
+      }
+#pragma unroll
+      for (int i = 0; i < RW; ++i) {
+        const int byte = q * RW + i;
+        fr |= (uint64_t)((ir[byte >> 2] >> (8 * (byte & 3))) & 0xffu) << (8 * i);
+      }
+      uint32_t wa = 0, wr = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t q8 = ((uint32_t)(fa >> (j * K)) & ((1u << K) - 1u)) << RW |
+                            ((uint32_t)(fr >> (j * RW)) & ((1u << RW) - 1u));
+        const int sh = 8 * (j & 3) + ((j & 4) ? 4 : 0);  // byte j&3, high nibble for j >= 4
+        wa |= (q8 >> 4) << sh;
+        wr |= (q8 & 15u) << sh;
+      }
+      a[q] = wa;
+      r[q] = wr;
     }
-    anchor[gi] = a;
-    residual[gi] = r;
+    reinterpret_cast<uint4*>(anchor)[qi] = make_uint4(a[0], a[1], a[2], a[3]);
+    reinterpret_cast<uint4*>(residual)[qi] = make_uint4(r[0], r[1], r[2], r[3]);
   }
 }
 
@@ -591,7 +631,7 @@ int lynx_split_bits(const void* anchor, const void* residual, int64_t rows, int 
     return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t groups = rows * (kD / 8);
-  const unsigned grid = grid_for(groups, kThreads);
+  const unsigned grid = grid_for(groups / 4, kThreads);
   const uint8_t* a = static_cast<const uint8_t*>(anchor);
   const uint8_t* r = static_cast<const uint8_t*>(residual);
   uint8_t* ao = static_cast<uint8_t*>(anchor_k);
@@ -618,7 +658,7 @@ int lynx_join_bits(const void* anchor_k, const void* residual_k, int64_t rows, i
     return report_error(LYNX_EINVAL, "pointer not 16-byte aligned");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int64_t groups = rows * (kD / 8);
-  const unsigned grid = grid_for(groups, kThreads);
+  const unsigned grid = grid_for(groups / 4, kThreads);
   const uint8_t* a = static_cast<const uint8_t*>(anchor_k);
   const uint8_t* r = static_cast<const uint8_t*>(residual_k);
   uint32_t* ao = static_cast<uint32_t*>(anchor);
