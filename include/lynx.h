@@ -453,6 +453,14 @@ int lynx_compander_selfcheck(float alpha, uint64_t *counts, void *stream);
  * early and its outputs are incomplete), else 0. */
 int lynx_wait_timeouts(unsigned int *flag);
 
+/* Check of the bounded wait every asynchronous-copy wait in the library
+ * uses: one CTA initialises an mbarrier, arrives on it (arrive != 0) or not,
+ * and waits with a limit of limit_ns nanoseconds (0 < limit_ns <= 1e9) on
+ * the global timer.  *status (device) = 1 if the barrier completed, 2 if the
+ * wait gave up.  Nothing faults or hangs either way.  Enqueued on `stream`. */
+int lynx_wait_selftest(uint64_t limit_ns, int arrive, unsigned int *status,
+                       void *stream);
+
 /* Text of a status code, and of the last failure on this host thread. */
 const char *lynx_status_string(int code);
 const char *lynx_last_error(void);

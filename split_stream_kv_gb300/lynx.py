@@ -72,6 +72,7 @@ def lib() -> ctypes.CDLL:
         "lynx_decode_anchor_bits": ([P, P, I64, I64, I, I, I, I, F, I, P, I, P], I),
         "lynx_a1_encode": ([P, I64, I64, I, I, I, F, P, P, P, P], I),
         "lynx_a1_decode": ([P, P, P, I64, I64, I, I, I, F, P, I, P], I),
+        "lynx_wait_selftest": ([ctypes.c_uint64, I, P, P], I),
         "lynx_compander_thresholds": ([F, P], I),
         "lynx_expand_table": ([F, P], I),
         "lynx_compander_selfcheck": ([F, P, P], I),
@@ -252,6 +253,15 @@ def lynx_spec_verify(p, q, draft_tokens, u, r, n_accepted=None, next_token=None)
                                   T, V, _ptr(n_accepted), _ptr(next_token), _stream(p.device)),
            "lynx_spec_verify")
     return n_accepted, next_token
+
+
+def lynx_wait_selftest(limit_ns: int, arrive: bool, device) -> int:
+    """Run the bounded-wait check; returns 1 (barrier completed) or 2 (the
+    wait gave up after limit_ns)."""
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    _check(lib().lynx_wait_selftest(limit_ns, int(arrive), _ptr(st), _stream(st.device)),
+           "lynx_wait_selftest")
+    return int(st.item())
 
 
 def lynx_device_errors() -> int:
