@@ -12,9 +12,11 @@
 // sums make the token independent of the summation order.
 //
 // A cluster of CTAs per sequence: every warp owns a contiguous segment of the
-// vocabulary; one coalesced pass gives the segment totals, shared through
-// distributed shared memory; the warp whose segment holds the target rescans
-// it 32 tokens at a time with a warp-wide prefix sum.
+// vocabulary; one pass, with all of a lane's loads in flight at once, gives
+// the segment totals in exact integer arithmetic, shared through distributed
+// shared memory; one warp finds the segment holding the target with a prefix
+// sum over the totals, and the CTA owning that segment rescans it, two tokens
+// a thread, with a block-wide prefix sum.
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,6 +29,7 @@ constexpr int kSpecCtas = 8;
 constexpr int kSpecThreads = 512;
 constexpr int kSpecWarps = kSpecThreads / 32;
 constexpr int kSpecSegs = kSpecCtas * kSpecWarps;  // segments of the vocabulary
+constexpr int kSpecPerLane = 32;  // tokens a lane loads at once
 
 // Set when a draft token lay outside [0, V) (treated as rejected); read
 // through read_spec_flags(), never reset.
@@ -36,8 +39,37 @@ cudaError_t read_spec_flags(unsigned int* flag) {
   return cudaMemcpyFromSymbol(flag, g_spec_flags, sizeof(unsigned int));
 }
 
+// Weights W(x) = floor(w * 2^40) of a float w, two ways.  spec_weight_int
+// reads W off the bits of w: w = M * 2^(E - 150) with M the 24-bit significand
+// (implicit bit included; subnormals have E = 1 and none), so W = M * 2^(E-110)
+// (saturating at 2^64 - 1 from w = 2^24 on).  For 0 <= w < 8 the split form is
+// cheaper: W = A * 2^20 + L with A = floor(w * 2^20) and L = floor(f * 2^20),
+// f = w * 2^20 - A; each of A and L is read off the bits of 2^23 + (value)
+// rounded toward zero, where one unit in the last place is 1, so their sums
+// accumulate in 32-bit integers with the 2^23 bias taken out once.
+__device__ __forceinline__ uint64_t spec_weight_int(float w) {
+  if (!(w > 0.0f)) return 0ull;
+  const uint32_t bits = __float_as_uint(w), e = bits >> 23;
+  const uint32_t m = e ? (bits & 0x7fffffu) | 0x800000u : bits;
+  const int sh = (int)(e ? e : 1u) - 110;
+  if (sh >= 0) return sh > 40 ? ~0ull : (uint64_t)m << sh;
+  return sh <= -24 ? 0ull : (uint64_t)(m >> -sh);
+}
+constexpr float kTwo20 = 1048576.0f, kTwo23 = 8388608.0f;
+constexpr uint32_t kBias = 0x4B000000u;  // the bits of 2^23
+constexpr float kSplitMax = 8.0f;        // the split form holds below this
+// the biased bits of 2^23 + A and 2^23 + L for 0 <= w < kSplitMax
+__device__ __forceinline__ void spec_parts(float w, uint32_t& ab, uint32_t& lb) {
+  const float t1 = __fmaf_rz(w, kTwo20, kTwo23);
+  const float f = __fmaf_rn(w, kTwo20, -__fsub_rn(t1, kTwo23));  // exact
+  ab = __float_as_uint(t1);
+  lb = __float_as_uint(__fmaf_rz(f, kTwo20, kTwo23));
+}
 __device__ __forceinline__ uint64_t spec_weight(float w) {
-  return w > 0.0f ? __float2ull_rz(w * 1099511627776.0f) : 0ull;  // floor(w * 2^40)
+  if (!(w < kSplitMax)) return spec_weight_int(w);
+  uint32_t ab, lb;
+  spec_parts(fmaxf(w, 0.0f), ab, lb);
+  return ((uint64_t)(ab - kBias) << 20) + (lb - kBias);
 }
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -58,6 +90,14 @@ __device__ __forceinline__ unsigned long long ld_peer_u64(const void* local, uin
   asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(remote) : "memory");
   return v;
 }
+__device__ __forceinline__ unsigned long long warp_incl_scan(unsigned long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long n = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
 
 __global__ void __cluster_dims__(kSpecCtas, 1, 1) __launch_bounds__(kSpecThreads)
 spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
@@ -66,7 +106,10 @@ spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
                    int32_t* __restrict__ n_acc, int32_t* __restrict__ next_tok) {
   __shared__ unsigned long long wtot[2][kSpecWarps];  // per pass: this CTA's segment totals
   __shared__ unsigned long long all[kSpecSegs];
-  __shared__ int k_sh, seg_sh, done;
+  static_assert(kSpecSegs % 32 == 0, "segments split evenly over a warp");
+  __shared__ unsigned long long wsum[kSpecWarps];
+  __shared__ int k_sh, seg_sh, done, found;
+  __shared__ int32_t result_sh;
   __shared__ unsigned long long base_sh, target_sh;
   const uint32_t crank = cluster_rank();
   const int b = blockIdx.x / kSpecCtas, tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
@@ -105,18 +148,78 @@ spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
   const int gseg = (int)crank * kSpecWarps + w;       // this warp's segment
   const int64_t x0 = (int64_t)gseg * seg < V ? (int64_t)gseg * seg : V;
   const int64_t x1 = x0 + seg < V ? x0 + seg : V;
-  int32_t result = -1;
-  bool have = false;
+
+  // A segment of up to 32 * kSpecPerLane tokens is read with all of a lane's
+  // loads in flight at once; longer ones stream.
+  const bool batched = seg <= 32 * kSpecPerLane;
 
   // ---- Eq. 11 (or p_{T+1}); with zero total weight, the weights of p
+  bool have = false;
   for (int pass = 0; pass < 2 && !have; ++pass) {
-    const float* qw = pass == 0 ? qk : nullptr;
-    auto weight = [&](int64_t x) -> uint64_t {
-      const float pv = __ldg(pk + x);
-      return spec_weight(qw ? fmaxf(__fsub_rn(pv, __ldg(qw + x)), 0.0f) : pv);
+    const bool resid = pass == 0 && qk;                // max(0, p - q) rather than p
+    auto wval = [&](int64_t x) -> float {            // the float weight of token x
+      const float pv = __ldg(pk + x), qv = resid ? __ldg(qk + x) : 0.0f;
+      return resid ? fmaxf(__fsub_rn(pv, qv), 0.0f) : fmaxf(pv, 0.0f);
     };
+    // this warp's segment total, split form; any weight past its range sends
+    // the warp through the integer form
     unsigned long long acc = 0;
-    for (int64_t x = x0 + lane; x < x1; x += 32) acc += weight(x);
+    float mx = 0.0f;
+    if (batched) {
+      // out-of-segment lanes read token 0 of the row and drop it
+      float wv[kSpecPerLane];
+      if (resid) {
+        float qv[kSpecPerLane];
+#pragma unroll
+        for (int i = 0; i < kSpecPerLane; ++i) {
+          const int64_t x = x0 + 32 * i + lane, xi = x < x1 ? x : 0;
+          wv[i] = __ldg(pk + xi);
+          qv[i] = __ldg(qk + xi);
+        }
+#pragma unroll
+        for (int i = 0; i < kSpecPerLane; ++i)
+          wv[i] = x0 + 32 * i + lane < x1 ? fmaxf(__fsub_rn(wv[i], qv[i]), 0.0f) : 0.0f;
+      } else {
+#pragma unroll
+        for (int i = 0; i < kSpecPerLane; ++i) {
+          const int64_t x = x0 + 32 * i + lane, xi = x < x1 ? x : 0;
+          wv[i] = __ldg(pk + xi);
+        }
+#pragma unroll
+        for (int i = 0; i < kSpecPerLane; ++i)
+          wv[i] = x0 + 32 * i + lane < x1 ? fmaxf(wv[i], 0.0f) : 0.0f;
+      }
+      uint32_t sa = 0, sl = 0;
+#pragma unroll
+      for (int i = 0; i < kSpecPerLane; ++i) {
+        mx = fmaxf(mx, wv[i]);
+        uint32_t ab, lb;
+        spec_parts(wv[i], ab, lb);
+        sa += ab;
+        sl += lb;
+      }
+      acc = ((unsigned long long)(sa - kSpecPerLane * kBias) << 20) + (sl - kSpecPerLane * kBias);
+    } else {
+      // (32-bit part sums fold into the total every 256 tokens a lane: A < 2^23)
+      for (int64_t xb = x0 + lane; xb < x1; xb += 32 * 256) {
+        const int64_t xe = xb + 32 * 256 < x1 ? xb + 32 * 256 : x1;
+        uint32_t sa = 0, sl = 0, cnt = 0;
+        for (int64_t x = xb; x < xe; x += 32) {
+          const float wv = wval(x);
+          mx = fmaxf(mx, wv);
+          uint32_t ab, lb;
+          spec_parts(wv, ab, lb);
+          sa += ab;
+          sl += lb;
+          ++cnt;
+        }
+        acc += ((unsigned long long)(sa - cnt * kBias) << 20) + (sl - cnt * kBias);
+      }
+    }
+    if (__any_sync(kFull, !(mx < kSplitMax))) {
+      acc = 0;
+      for (int64_t x = x0 + lane; x < x1; x += 32) acc += spec_weight(wval(x));
+    }
 #pragma unroll
     for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
     if (lane == 0) wtot[pass][w] = acc;
@@ -124,55 +227,82 @@ spec_verify_kernel(const float* __restrict__ p, const float* __restrict__ q,
     for (int i = tid; i < kSpecSegs; i += kSpecThreads)
       all[i] = ld_peer_u64(&wtot[pass][i % kSpecWarps], (uint32_t)(i / kSpecWarps));
     __syncthreads();
-    if (tid == 0) {
-      unsigned long long Z = 0;
-      for (int i = 0; i < kSpecSegs; ++i) Z += all[i];
-      done = Z != 0;
+    if (w == 0) {
+      // Lane l holds segments kPerLane*l .. kPerLane*l + kPerLane-1; a prefix
+      // sum of the lane totals gives Z and the lane, then the segment, whose
+      // running sum first exceeds the target.
+      constexpr int kPerLane = kSpecSegs / 32;
+      unsigned long long part[kPerLane], own = 0;
+#pragma unroll
+      for (int i = 0; i < kPerLane; ++i) {
+        part[i] = all[kPerLane * lane + i];
+        own += part[i];
+      }
+      const unsigned long long inc = warp_incl_scan(own, lane);
+      const unsigned long long Z = __shfl_sync(kFull, inc, 31);
+      if (lane == 0) done = Z != 0;
       if (Z != 0) {
-        // floor(r * Z / 2^32) exactly: r * Zhi + floor(r * Zlo / 2^32)
+        // floor(r * Z / 2^32) exactly: r * Zhi + floor(r * Zlo / 2^32); below Z
         const unsigned long long target =
             (unsigned long long)r * (Z >> 32) + (((unsigned long long)r * (Z & 0xffffffffull)) >> 32);
-        unsigned long long run = 0;
-        int sg = kSpecSegs - 1;
-        for (int i = 0; i < kSpecSegs; ++i) {
-          if (run + all[i] > target) {
-            sg = i;
-            break;
+        const int owner = __ffs(__ballot_sync(kFull, inc > target)) - 1;
+        if (lane == owner) {
+          unsigned long long run = inc - own;
+          int sg = kPerLane * lane + kPerLane - 1;
+#pragma unroll
+          for (int i = 0; i < kPerLane; ++i) {
+            if (run + part[i] > target) {
+              sg = kPerLane * lane + i;
+              break;
+            }
+            run += part[i];
           }
-          run += all[i];
+          seg_sh = sg;
+          base_sh = run;
+          target_sh = target;
         }
-        seg_sh = sg;
-        base_sh = run;
-        target_sh = target;
       }
     }
     __syncthreads();
-    if (done) {
-      have = true;
-      if (gseg == seg_sh) {                           // this warp's segment holds the target
-        const unsigned long long target = target_sh;
-        unsigned long long run = base_sh;
-        result = (int32_t)(x1 - 1);
-        for (int64_t xs = x0; xs < x1; xs += 32) {
-          const int64_t x = xs + lane;
-          unsigned long long v = x < x1 ? weight(x) : 0ull;
+    if (!done) continue;
+    have = true;
+    if ((int)crank != seg_sh / kSpecWarps) continue;
+    // ---- the CTA holding the target segment rescans it, 2 tokens a thread
+    // per round: the first token whose running sum exceeds the target
+    const int64_t xs0 = (int64_t)seg_sh * seg < V ? (int64_t)seg_sh * seg : V;
+    const int64_t xs1 = xs0 + seg < V ? xs0 + seg : V;
+    const unsigned long long target = target_sh;
+    unsigned long long base = base_sh;
+    if (tid == 0) {
+      result_sh = (int32_t)(xs1 - 1);
+      found = 0;
+    }
+    for (int64_t c0 = xs0; c0 < xs1; c0 += 2 * kSpecThreads) {
+      const int64_t xa = c0 + 2 * tid, xb = xa + 1;
+      const unsigned long long wa = xa < xs1 ? spec_weight(wval(xa)) : 0ull;
+      const unsigned long long wb = xb < xs1 ? spec_weight(wval(xb)) : 0ull;
+      const unsigned long long inc = warp_incl_scan(wa + wb, lane);
+      if (lane == 31) wsum[w] = inc;
+      __syncthreads();
+      unsigned long long before = base, total = 0;
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {  // inclusive prefix sum over the lanes
-            const unsigned long long n = __shfl_up_sync(kFull, v, o);
-            if (lane >= o) v += n;
-          }
-          const unsigned hit = __ballot_sync(kFull, x < x1 && run + v > target);
-          if (hit) {
-            result = (int32_t)(xs + __ffs(hit) - 1);
-            break;
-          }
-          run += __shfl_sync(kFull, v, 31);
-        }
-        if (lane == 0) {
-          n_acc[b] = k;
-          next_tok[b] = result;
-        }
+      for (int i = 0; i < kSpecWarps; ++i) {
+        const unsigned long long v = wsum[i];
+        if (i < w) before += v;
+        total += v;
       }
+      const unsigned long long run = before + inc - (wa + wb);   // before token xa
+      if (run <= target && target < run + wa + wb) {             // one thread at most
+        result_sh = (int32_t)(target < run + wa ? xa : xb);
+        found = 1;
+      }
+      __syncthreads();
+      if (found) break;
+      base += total;
+    }
+    if (tid == 0) {
+      n_acc[b] = k;
+      next_tok[b] = result_sh;
     }
   }
   if (!have && crank == 0 && tid == 0) {

@@ -56,3 +56,20 @@ def test_spec_verify_full_acceptance_draws_the_bonus_token(lynx_lib, oracle_mod,
     ko = _check(lynx_lib, oracle_mod, cuda_dev, p, q, s, u, r)
     assert np.all(ko == 5)
     assert lynx_lib.lynx_device_errors() & 4 == 0
+
+
+@pytest.mark.parametrize("batch,T,V", [(20, 3, 131072), (2, 2, 131073), (3, 4, 200003)])
+def test_spec_verify_segment_length_boundaries(lynx_lib, oracle_mod, cuda_dev, batch, T, V):
+    """Segments of exactly 1024 tokens (V = 131072: every lane's tokens read in
+    one batch of loads), of 1025 and of 1563 (read as a stream)."""
+    _check(lynx_lib, oracle_mod, cuda_dev, *_inputs(batch, T, V, 0.05, seed=V % 97))
+
+
+def test_spec_verify_zero_residual_draws_from_p(lynx_lib, oracle_mod, cuda_dev):
+    """q = p and u = 1 at position 3: that draft token is rejected (u q < p
+    fails), yet max(0, p - q) is 0 everywhere, so the next token is drawn from
+    p at position 3."""
+    p, q, s, u, r = _inputs(6, 4, 3001, 0.0, seed=2, same=True)
+    u[:, 2] = 1.0
+    ko = _check(lynx_lib, oracle_mod, cuda_dev, p, q, s, u, r)
+    assert np.all(ko == 2)
