@@ -326,11 +326,13 @@ int lynx_a1_decode(const void *anchor, const void *residual, const float *meta,
  * drawn from max(0, p_{k+1} - q_{k+1}) after a rejection, or from p_{T+1}
  * after a fully accepted draft, by inverse CDF over the integer weights
  * floor(w * 2^40) with target floor(r * Z / 2^32), Z their sum; if Z = 0 the
- * weights of p are used, and if they sum to 0 too the token is -1.  A draft
- * token outside [0, V) counts as rejected and is reported by
- * lynx_device_errors (bit 4).  1 <= T <= 64, 1 <= V < 2^31; all device
- * pointers, 16-byte aligned.  One cluster of 8 CTAs per sequence, enqueued
- * on `stream`. */
+ * weights of p are used, and if they sum to 0 too the token is -1.  The
+ * rows need not be normalised, but each row's weights must sum below 2^24
+ * so that Z fits in 64 bits (distributions sum to 1); NaN and negative
+ * weights count as 0.  A draft token outside [0, V) counts as rejected and
+ * is reported by lynx_device_errors (bit 4).  1 <= T <= 64, 1 <= V < 2^31;
+ * all device pointers, 16-byte aligned.  One cluster of 8 CTAs per sequence,
+ * enqueued on `stream`. */
 int lynx_spec_verify(const float *p_target, const float *q_draft,
                      const int32_t *draft_tokens, const float *u_accept,
                      const uint32_t *r_sample, int batch, int T, int64_t V,

@@ -73,3 +73,22 @@ def test_spec_verify_zero_residual_draws_from_p(lynx_lib, oracle_mod, cuda_dev):
     u[:, 2] = 1.0
     ko = _check(lynx_lib, oracle_mod, cuda_dev, p, q, s, u, r)
     assert np.all(ko == 2)
+
+
+def test_spec_verify_unnormalised_and_tiny_weights(lynx_lib, oracle_mod, cuda_dev):
+    """Weights that are not distributions: p and q up to 100 (a warp meeting a
+    weight of 8 or more sums with the integer-only form of floor(w 2^40); the
+    totals stay far below 2^64), and rows sprinkled with subnormal and zero
+    entries.  Tokens as the oracle's."""
+    rng = np.random.default_rng(17)
+    batch, T, V = 6, 4, 70001
+    p = (rng.random((batch, T + 1, V)) ** 4 * 100.0).astype(np.float32)
+    q = (rng.random((batch, T, V)) ** 4 * 100.0).astype(np.float32)
+    tiny = rng.random((batch, T + 1, V)) < 0.2
+    p[tiny] = np.float32(1e-40)
+    p[:, :, ::97] = 0.0
+    p[2] *= np.float32(1e-6)                       # one sequence entirely below 8
+    s = rng.integers(0, V, size=(batch, T)).astype(np.int32)
+    u = rng.random((batch, T), dtype=np.float32)
+    r = rng.integers(0, 2 ** 32, size=batch, dtype=np.uint64).astype(np.uint32)
+    _check(lynx_lib, oracle_mod, cuda_dev, p, q, s, u, r)
