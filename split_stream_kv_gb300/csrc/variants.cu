@@ -316,16 +316,25 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
 
 // ---------------------------------------------------------- Appendix A.1
 
-// One CTA per page block, kA1Split threads per channel, each owning a
-// quarter of the page's tokens (whole 16-token chunks).  The block's BF16
-// tile is staged in shared memory; the page maximum of a channel combines
-// the quarters' maxima through shared memory; each thread then walks its
-// chunks for the chunk maximum and the codes, decided against the host
-// thresholds of Eq. 7 (|Q| = #{k : a >= thr[k]}).  The codes gather in
-// shared memory in the 4+4 nibble layout and leave as 16-byte rows.
+// One CTA per page block, one thread per (16-token chunk k, group G of 8
+// channels): P threads.  A thread holds its chunk's 16 rows of 16 bytes in
+// registers.  The page maximum of |x| (exact, on bf16 pairs) combines the
+// chunks' maxima through shared memory.  The chunk maximum of |x'| = |x| rm
+// is rn(max|x| rm): rounding is monotone.  |Q| comes from the encoder's fast
+// rounding, run on pairs of channels, with the host thresholds of Eq. 7
+// (|Q| = #{k : a >= thr[k]}) deciding inside its window, or from a binary
+// search over the thresholds for alpha < 1.  The codes leave as one 32-bit
+// word per stream and token: byte j holds channel 8G + j in the low nibble
+// and 8G + j + 4 in the high one.
 constexpr int kA1Chunk = 16;
-constexpr int kA1Split = 4;
-constexpr int kA1Threads = 128 * kA1Split;
+
+// prmt.b32 in its default mode: a selector digit of 8 or more replicates
+// the sign bit of the byte it names.
+__device__ __forceinline__ uint32_t a1_prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
 
 // |Q| = Round(Y(a)) of Eq. 7.  FAST (alpha >= 1): the encoder's Stage-3 fast
 // path per lane (t = rn(alpha a + 1), MUFU lg2, s = rd(lg2(t) c16 + C0): the
@@ -355,71 +364,118 @@ __device__ __forceinline__ int a1_round(float a, float alpha, float c16, const f
 }
 
 template <bool FAST>
-__global__ void __launch_bounds__(kA1Threads)
+__global__ void __launch_bounds__(256)
 a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, const int64_t L,
-                 const int P, uint8_t* __restrict__ anchor, uint8_t* __restrict__ residual,
+                 const int P, uint32_t* __restrict__ anchor, uint32_t* __restrict__ residual,
                  float* __restrict__ meta, const __grid_constant__ CompanderTable tab) {
-  extern __shared__ __align__(16) uint8_t sm[];
-  uint16_t* tile = reinterpret_cast<uint16_t*>(sm);                 // [P][128]
-  uint8_t* ca = sm + (size_t)P * 256;                               // [P][64]
-  uint8_t* cr = ca + (size_t)P * 64;                                // [P][64]
-  float* thr = reinterpret_cast<float*>(cr + (size_t)P * 64);       // [128]
-  float* pmax = thr + 128;                                          // [kA1Split][128]
-  const int tid = threadIdx.x, d = tid & 127, qt = tid >> 7;
+  __shared__ float thr[128];
+  __shared__ uint4 pmx[16][16];                  // [chunk][group]: bf16x2 maxima of |x|
+  const int tid = threadIdx.x, G = tid & 15, k = tid >> 4;
   const int64_t blk = blockIdx.x;
   const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
-  const uint8_t* src = kv + ((b * L + p * P) * H + h) * 256;
-  for (int i = tid; i < P * 16; i += kA1Threads) {                  // 16 B of a 256 B row
-    const int t = i >> 4, w = i & 15;
-    reinterpret_cast<uint4*>(tile)[i] =
-        __ldg(reinterpret_cast<const uint4*>(src + (int64_t)t * H * 256) + w);
+  for (int i = tid; i < 128; i += P) thr[i] = tab.thr[i];   // P >= 64 threads
+  const uint8_t* src = kv + ((b * L + p * P + k * kA1Chunk) * H + h) * 256 + 16 * G;
+  uint4 w[kA1Chunk];
+#pragma unroll
+  for (int t = 0; t < kA1Chunk; ++t)
+    w[t] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)t * H * 256));
+  uint32_t cm[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int t = 0; t < kA1Chunk; ++t) {
+    cm[0] = bf2_max(cm[0], w[t].x & 0x7fff7fffu);
+    cm[1] = bf2_max(cm[1], w[t].y & 0x7fff7fffu);
+    cm[2] = bf2_max(cm[2], w[t].z & 0x7fff7fffu);
+    cm[3] = bf2_max(cm[3], w[t].w & 0x7fff7fffu);
   }
-  if (tid < 128) thr[tid] = tab.thr[tid];
+  pmx[k][G] = make_uint4(cm[0], cm[1], cm[2], cm[3]);
   __syncthreads();
-  auto xv = [&](int t) { return __uint_as_float((uint32_t)tile[t * 128 + d] << 16); };
-  const int span = P / kA1Split, t_lo = qt * span;
-  float m = 0.0f;
-  for (int t = t_lo; t < t_lo + span; ++t) m = fmaxf(m, fabsf(xv(t)));
-  pmax[qt * 128 + d] = m;
-  __syncthreads();
-#pragma unroll
-  for (int q = 0; q < kA1Split; ++q) m = fmaxf(m, pmax[q * 128 + d]);
-  const float rm = m > 0.0f ? __frcp_rn(m) : 0.0f;
+  uint32_t pm[4] = {0u, 0u, 0u, 0u};
+  for (int c = 0; c < P / kA1Chunk; ++c) {
+    const uint4 v = pmx[c][G];
+    pm[0] = bf2_max(pm[0], v.x);
+    pm[1] = bf2_max(pm[1], v.y);
+    pm[2] = bf2_max(pm[2], v.z);
+    pm[3] = bf2_max(pm[3], v.w);
+  }
+  // per channel pair j: page max m, rm = 1/m, chunk max mi, rmi = 1/mi
   const int NCk = P / kA1Chunk;
-  float* mrow = meta + blk * (int64_t)(1 + NCk) * kD;
-  if (qt == 0) mrow[d] = m;
-  const int byte = (d >> 3) * 4 + (d & 3), sh = (d & 4) ? 4 : 0;
-  for (int c = t_lo / kA1Chunk; c < (t_lo + span) / kA1Chunk; ++c) {
-    float xp[kA1Chunk];
-    float mi = 0.0f;
+  float* mrow = meta + blk * (int64_t)(1 + NCk) * kD + 8 * G;
+  f2 rm2[4], rmi2[4];
+  float mv[8], miv[8];
 #pragma unroll
-    for (int i = 0; i < kA1Chunk; ++i) {
-      xp[i] = __fmul_rn(xv(c * kA1Chunk + i), rm);
-      mi = fmaxf(mi, fabsf(xp[i]));
-    }
-    const float rmi = mi > 0.0f ? __frcp_rn(mi) : 0.0f;
-    mrow[(1 + c) * kD + d] = mi;
+  for (int j = 0; j < 4; ++j) {
+    const f2 m = bf2_to_f2(pm[j]), cx = bf2_to_f2(cm[j]);
+    rm2[j] = make_float2(m.x > 0.0f ? __frcp_rn(m.x) : 0.0f, m.y > 0.0f ? __frcp_rn(m.y) : 0.0f);
+    // an infinite input makes rm 0 and this product NaN; the chunk's finite
+    // values then give 0
+    const float m0 = fmaxf(__fmul_rn(cx.x, rm2[j].x), 0.0f);
+    const float m1 = fmaxf(__fmul_rn(cx.y, rm2[j].y), 0.0f);
+    rmi2[j] = make_float2(m0 > 0.0f ? __frcp_rn(m0) : 0.0f, m1 > 0.0f ? __frcp_rn(m1) : 0.0f);
+    mv[2 * j] = m.x;
+    mv[2 * j + 1] = m.y;
+    miv[2 * j] = m0;
+    miv[2 * j + 1] = m1;
+  }
+  if (k == 0) {
+    reinterpret_cast<float4*>(mrow)[0] = make_float4(mv[0], mv[1], mv[2], mv[3]);
+    reinterpret_cast<float4*>(mrow)[1] = make_float4(mv[4], mv[5], mv[6], mv[7]);
+  }
+  reinterpret_cast<float4*>(mrow + (1 + k) * kD)[0] = make_float4(miv[0], miv[1], miv[2], miv[3]);
+  reinterpret_cast<float4*>(mrow + (1 + k) * kD)[1] = make_float4(miv[4], miv[5], miv[6], miv[7]);
+
+  const f2 alpha2 = make_float2(tab.alpha, tab.alpha), c16_2 = make_float2(tab.c16, tab.c16);
+  uint32_t* arow = anchor + (blk * P + k * kA1Chunk) * 16 + G;
+  uint32_t* rrow = residual + (blk * P + k * kA1Chunk) * 16 + G;
 #pragma unroll
-    for (int i = 0; i < kA1Chunk; ++i) {
-      const float xpp = __fmul_rn(xp[i], rmi);
-      const int I = a1_round<FAST>(fabsf(xpp), tab.alpha, tab.c16, thr);
-      const int Q = xpp > 0.0f ? I : (xpp < 0.0f ? -I : 0);
-      const uint32_t na = (uint32_t)(Q >> 4) & 0xfu, nr = (uint32_t)Q & 0xfu;
-      // channel d and d^4 share a byte: the low-nibble thread writes both
-      const uint32_t oa = __shfl_xor_sync(kFull, na, 4), orr = __shfl_xor_sync(kFull, nr, 4);
-      if (!sh) {
-        const int t = c * kA1Chunk + i;
-        ca[t * 64 + byte] = (uint8_t)(na | (oa << 4));
-        cr[t * 64 + byte] = (uint8_t)(nr | (orr << 4));
+  for (int t = 0; t < kA1Chunk; ++t) {
+    const uint32_t wj[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
+    uint32_t bits[8], sbits[8];
+    float av[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const f2 xpp = mul2(mul2(bf2_to_f2(wj[j]), rm2[j]), rmi2[j]);
+      sbits[2 * j] = __float_as_uint(xpp.x);
+      sbits[2 * j + 1] = __float_as_uint(xpp.y);
+      // |x''| <= 1 up to rounding; a NaN (only) fails the test and codes as 0
+      float a0 = fabsf(xpp.x), a1 = fabsf(xpp.y);
+      a0 = a0 <= 2.0f ? a0 : 0.0f;
+      a1 = a1 <= 2.0f ? a1 : 0.0f;
+      av[2 * j] = a0;
+      av[2 * j + 1] = a1;
+      if constexpr (FAST) {
+        const f2 tt = __ffma2_rn(alpha2, make_float2(a0, a1), make_float2(1.0f, 1.0f));
+        const f2 s = __ffma2_rd(make_float2(lg2_approx(tt.x), lg2_approx(tt.y)), c16_2,
+                                make_float2(kA1C0, kA1C0));
+        bits[2 * j] = __float_as_uint(s.x);
+        bits[2 * j + 1] = __float_as_uint(s.y);
+      } else {
+        bits[2 * j] = (uint32_t)a1_round<false>(a0, tab.alpha, tab.c16, thr) << 16;
+        bits[2 * j + 1] = (uint32_t)a1_round<false>(a1, tab.alpha, tab.c16, thr) << 16;
       }
     }
-  }
-  __syncthreads();
-  uint4* da = reinterpret_cast<uint4*>(anchor + blk * (int64_t)P * 64);
-  uint4* dr = reinterpret_cast<uint4*>(residual + blk * (int64_t)P * 64);
-  for (int i = tid; i < P * 4; i += kA1Threads) {
-    da[i] = reinterpret_cast<const uint4*>(ca)[i];
-    dr[i] = reinterpret_cast<const uint4*>(cr)[i];
+    if constexpr (FAST) {
+      uint32_t dmin = __vminu2(a1_prmt(bits[0], bits[1], 0x5410u), a1_prmt(bits[2], bits[3], 0x5410u));
+      dmin = __vminu2(dmin, __vminu2(a1_prmt(bits[4], bits[5], 0x5410u), a1_prmt(bits[6], bits[7], 0x5410u)));
+      const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
+      if (__any_sync(kFull, amb)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if ((bits[i] & 0xffffu) < 2u * kAmbiguityK) {
+            const int I = (int)((bits[i] >> 16) & 0xffu), bb = I > 0 ? I - 1 : 0;
+            bits[i] = (bits[i] & 0xff00ffffu) | ((uint32_t)(bb + (av[i] >= thr[bb] ? 1 : 0)) << 16);
+          }
+      }
+    }
+    // |Q| bytes of channels 0-3 and 4-7, negated where x'' < 0 (two's complement)
+    const uint32_t i01 = a1_prmt(bits[0], bits[1], 0x0062u), i23 = a1_prmt(bits[2], bits[3], 0x0062u);
+    const uint32_t i45 = a1_prmt(bits[4], bits[5], 0x0062u), i67 = a1_prmt(bits[6], bits[7], 0x0062u);
+    const uint32_t s01 = a1_prmt(sbits[0], sbits[1], 0x00fbu), s23 = a1_prmt(sbits[2], sbits[3], 0x00fbu);
+    const uint32_t s45 = a1_prmt(sbits[4], sbits[5], 0x00fbu), s67 = a1_prmt(sbits[6], sbits[7], 0x00fbu);
+    const uint32_t I0 = a1_prmt(i01, i23, 0x5410u), S0 = a1_prmt(s01, s23, 0x5410u);
+    const uint32_t I1 = a1_prmt(i45, i67, 0x5410u), S1 = a1_prmt(s45, s67, 0x5410u);
+    const uint32_t W0 = __vsub4(I0 ^ S0, S0), W1 = __vsub4(I1 ^ S1, S1);
+    arow[t * 16] = ((W0 >> 4) & 0x0f0f0f0fu) | (W1 & 0xf0f0f0f0u);
+    rrow[t * 16] = (W0 & 0x0f0f0f0fu) | ((W1 << 4) & 0xf0f0f0f0u);
   }
 }
 
@@ -523,26 +579,12 @@ cudaError_t launch_decode_anchor_bits(const void* ak, const float* meta, const S
 
 cudaError_t launch_a1_encode(const void* kv, const Shape& s, const CompanderTable& tab,
                              void* anchor, void* residual, float* meta, cudaStream_t stream) {
-  const size_t smem = (size_t)s.page * 384 + (128 + 128 * kA1Split) * 4;
-  static thread_local int configured = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (configured != dev) {
-    e = cudaFuncSetAttribute(a1_encode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             256 * 384 + (128 + 128 * kA1Split) * 4);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(a1_encode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             256 * 384 + (128 + 128 * kA1Split) * 4);
-    if (e != cudaSuccess) return e;
-    configured = dev;
-  }
   const int64_t nblk = s.blocks();
   if (nblk > 0x7fffffff) return cudaErrorInvalidValue;
   auto fn = tab.alpha >= kMinEncodeAlpha ? a1_encode_kernel<true> : a1_encode_kernel<false>;
-  fn<<<(unsigned)nblk, kA1Threads, smem, stream>>>(
-      static_cast<const uint8_t*>(kv), s.NB(), s.H, s.L, s.page, static_cast<uint8_t*>(anchor),
-      static_cast<uint8_t*>(residual), meta, tab);
+  fn<<<(unsigned)nblk, (unsigned)s.page, 0, stream>>>(
+      static_cast<const uint8_t*>(kv), s.NB(), s.H, s.L, s.page, static_cast<uint32_t*>(anchor),
+      static_cast<uint32_t*>(residual), meta, tab);
   return cudaGetLastError();
 }
 

@@ -189,3 +189,26 @@ def test_a1_variant_matches_oracle(lynx_lib, oracle_mod, cuda_dev, B, L, H, P, a
         torch.cuda.synchronize()
         same_bytes(f32, ref, f"a1 decode {what}")
         assert np.array_equal(bits_of(b16), oracle_mod.f32_to_bf16_bits(ref)), what
+
+
+def test_a1_variant_special_values(lynx_lib, oracle_mod, cuda_dev):
+    """Infinities (a page maximum of inf makes every scale 0), a NaN (coded
+    0, left out of the maxima), signed zeros, an all-zero channel, the
+    largest finite BF16 and a subnormal: codes and metadata as the oracle's."""
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn((1, 256, 2, 128), generator=g)
+    x[0, 3, 0, 5] = float("inf")
+    x[0, 40, 1, 9] = float("-inf")
+    x[0, 77, 0, 17] = float("nan")
+    x[0, 100, 1, 33] = -0.0
+    x[0, :, 0, 60] = 0.0
+    x[0, 200, 1, 70] = 3.3895e38
+    x[0, 5, 1, 90] = 1e-40
+    kv = x.to(torch.bfloat16).to(cuda_dev)
+    for P in (64, 128, 256):
+        anc, res, meta = lynx_lib.lynx_a1_encode(kv, P, 100.0)
+        torch.cuda.synchronize()
+        oa, orr, om = oracle_mod.a1_encode(bits_of(kv), P, 100.0)
+        same_bytes(anc, oa, f"a1 anchor P={P}")
+        same_bytes(res, orr, f"a1 residual P={P}")
+        same_bytes(meta, om, f"a1 meta P={P}")
