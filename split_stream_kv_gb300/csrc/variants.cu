@@ -285,7 +285,7 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
       sg[j] = __fadd_rn(sg[j], kEps);
     }
     const uint8_t* src = ak + ((blk * P + t0) * 16 + G) * K;
-#pragma unroll 2
+#pragma unroll  // every token's code loads in flight at once
     for (int u = 0; u < kRun; ++u) {
       uint64_t fa = 0;
 #pragma unroll
