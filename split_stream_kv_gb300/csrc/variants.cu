@@ -511,7 +511,7 @@ a1_decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__
       mi[4] = v1.x; mi[5] = v1.y; mi[6] = v1.z; mi[7] = v1.w;
     }
     const int64_t code0 = (blk * P + t0) * 16 + G;   // 32-bit word of (token t0, group G)
-#pragma unroll 2
+#pragma unroll  // every token's code loads in flight at once
     for (int u = 0; u < 8; ++u) {
       const uint32_t wa = __ldg(reinterpret_cast<const uint32_t*>(anchor) + code0 + u * 16);
       const uint32_t wr =
