@@ -279,7 +279,10 @@ int lynx_int_decode(const void *codes, const float *meta, int64_t rows, int D,
  * bits j*w .. j*w + w - 1 (w the field width) of the group's bytes read as
  * one little-endian integer; page blocks in the (b, page, head) order of the
  * 4+4 streams.  rows = B * L * H_kv token rows.
- * lynx_split_bits re-splits 4+4 streams; lynx_join_bits is its inverse. */
+ * lynx_split_bits re-splits 4+4 streams; lynx_join_bits is its inverse.
+ * Device pointers, 16-byte aligned (LYNX_EINVAL otherwise); D must be 128
+ * and 3 <= k <= 6 (LYNX_EUNSUPPORTED), rows >= 0 (LYNX_ESHAPE); one pass,
+ * enqueued on `stream`. */
 int lynx_split_bits(const void *anchor, const void *residual, int64_t rows,
                     int D, int k, void *anchor_k, void *residual_k,
                     void *stream);
@@ -287,7 +290,8 @@ int lynx_join_bits(const void *anchor_k, const void *residual_k, int64_t rows,
                    int D, int k, void *anchor, void *residual, void *stream);
 /* Anchor-only decode of a k-bit Anchor stream, 3 <= k <= 6: bucket point
  * I = 2^(8-k) V + 2^(7-k) - 1 (16 V + 7 for k = 4), then the
- * reconstruction of lynx_decode_anchor; out as lynx_decode_anchor. */
+ * reconstruction of lynx_decode_anchor; out, shape checks and errors as
+ * lynx_decode_anchor, and LYNX_EUNSUPPORTED for k outside 3..6. */
 int lynx_decode_anchor_bits(const void *anchor_k, const float *meta, int64_t B,
                             int64_t L, int H_kv, int D, int page, int C,
                             float alpha, int k, void *out, int out_dtype,
@@ -302,7 +306,10 @@ int lynx_decode_anchor_bits(const void *anchor_k, const float *meta, int64_t B,
  * (same nibble pairing); meta [B][L/page][H_kv][1 + page/16][D] float32 =
  * m, then m_i per chunk.  Decode: x = (sgn X(|Q|) * m_i) * m (Eq. 14/15
  * inverse, two float32 products); with residual = NULL the Anchor-only
- * point Q = 16 Q_anc + 7.  The pages use alpha = 100 for this variant. */
+ * point Q = 16 Q_anc + 7.  A NaN element codes as 0 and is left out of
+ * the maxima; an infinite page maximum makes the channel's scales 0.  The
+ * pages use alpha = 100 for this variant.  Shape checks and errors as
+ * lynx_encode / lynx_decode_full (C fixed at 16); alpha > 0 and finite. */
 int lynx_a1_encode(const void *kv, int64_t B, int64_t L, int H_kv, int D,
                    int page, float alpha, void *anchor, void *residual,
                    float *meta, void *stream);
