@@ -91,6 +91,7 @@ int report_error(int code, const char* msg);
 // Host read of the device flag set when a bounded wait gave up.
 cudaError_t read_wait_timeout(unsigned int* flag);
 cudaError_t read_decode_wait_timeout(unsigned int* flag);
+cudaError_t read_variant_wait_timeout(unsigned int* flag);
 cudaError_t read_attn_flags(unsigned int* flag);
 cudaError_t read_spec_flags(unsigned int* flag);
 cudaError_t launch_spec_verify(const float* p, const float* q, const int32_t* s, const float* u,

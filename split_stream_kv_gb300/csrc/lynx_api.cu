@@ -438,13 +438,14 @@ int lynx_attn_decode_paged(const void* q, int batch, int T, int H_q, const void*
 
 int lynx_device_errors(unsigned int* bits) {
   if (!bits) return fail(LYNX_EINVAL, "null pointer");
-  unsigned int enc = 0, dec = 0, att = 0, spc = 0;
+  unsigned int enc = 0, dec = 0, att = 0, spc = 0, var = 0;
   cudaError_t e = read_wait_timeout(&enc);
   if (e == cudaSuccess) e = read_decode_wait_timeout(&dec);
+  if (e == cudaSuccess) e = read_variant_wait_timeout(&var);
   if (e == cudaSuccess) e = read_attn_flags(&att);
   if (e == cudaSuccess) e = read_spec_flags(&spc);
   if (e != cudaSuccess) return cuda_fail(e, "lynx_device_errors");
-  *bits = enc | dec | att | spc;
+  *bits = enc | dec | var | att | spc;
   return LYNX_OK;
 }
 
@@ -473,11 +474,12 @@ int lynx_compander_selfcheck(float alpha, uint64_t* counts, void* stream) {
 
 int lynx_wait_timeouts(unsigned int* flag) {
   if (!flag) return fail(LYNX_EINVAL, "null pointer");
-  unsigned int enc = 0, dec = 0;
+  unsigned int enc = 0, dec = 0, var = 0;
   cudaError_t e = read_wait_timeout(&enc);
   if (e == cudaSuccess) e = read_decode_wait_timeout(&dec);
+  if (e == cudaSuccess) e = read_variant_wait_timeout(&var);
   if (e != cudaSuccess) return cuda_fail(e, "lynx_wait_timeouts");
-  *flag = ((enc | dec) & kFlagWaitTimeout) ? 1u : 0u;
+  *flag = ((enc | dec | var) & kFlagWaitTimeout) ? 1u : 0u;
   return LYNX_OK;
 }
 

@@ -241,74 +241,138 @@ __global__ void __launch_bounds__(kThreads) join_bits_kernel(const uint8_t* __re
   }
 }
 
-// Anchor-only decode of a K-bit Anchor: one thread per (run of kRun tokens,
-// group of 8 channels), the same reconstruction as the 4+4 Anchor decoder
-// with the bucket point I = 2^(8-K) V + 2^(7-K) - 1.  A run lies in one
-// chunk (C >= 16), so its 32 constants load once for kRun tokens.
-constexpr int kRun = 8;
+// Anchor-only decode of a K-bit Anchor, the same reconstruction as the 4+4
+// Anchor decoder with the bucket point I = 2^(8-K) V + 2^(7-K) - 1.  One
+// persistent kernel: a CTA walks page blocks, whose K-bit codes (page x 16 K
+// bytes) and metadata rows arrive in shared memory by bulk asynchronous
+// copies, one stage ahead of the block being decoded.  Thread (slot, G) of
+// 256 decodes a run of page/16 tokens (inside one chunk) of channels
+// 8G..8G+7.  The K bytes of (token t, group G) start at byte (16 t + G) K of
+// the block and lie in two consecutive 32-bit words ((o mod 4) + K <= 8: o
+// is even when K = 6); the word after a block's last code is still inside
+// the stage (its metadata follows), and the shift drops its bytes.
+constexpr int kBitsStages = 2;
+
+// Set by a kernel of this file whose bounded wait on a stage gave up (it
+// then returns early).  Read through read_variant_wait_timeout(); never reset.
+__device__ unsigned int g_variant_wait_timeout = 0;
+
+template <int K>
+__host__ __device__ constexpr size_t bits_table_bytes() { return (size_t)(1 << K) * 32 * 4; }
 
 template <int K, bool BF16OUT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restrict__ meta,
                           const int64_t nblk, const int64_t NB, const int H, const int64_t L,
                           const int P, const int C, void* __restrict__ out,
                           const __grid_constant__ ExpandTable tab) {
-  __shared__ float x[128];
-  for (int i = threadIdx.x; i < 128; i += kThreads) x[i] = tab.x[i];
-  __syncthreads();
+  static_assert(K >= 3 && K <= 6, "the K bytes of a code fit two 32-bit words");
+  constexpr int NCODE = 1 << K;
+  extern __shared__ __align__(16) uint8_t smem[];
+  // the signed value of every K-bit Anchor code a (two's complement): S X(I)
+  // with V = S > 0 ? a : -a - 1 and I = 2^(8-K) V + 2^(7-K) - 1; one copy a
+  // lane (row a, column lane), so that every lane reads its own bank
+  float* xk = reinterpret_cast<float*>(smem);
+  const uint32_t code_bytes = (uint32_t)P * 16 * K;
   const int NC = P / C, meta_rows = 2 + 2 * NC;
-  const int runs = P / kRun;
-  const int64_t items = nblk * runs * 16;
-  for (int64_t it = (int64_t)blockIdx.x * kThreads + threadIdx.x; it < items;
-       it += (int64_t)gridDim.x * kThreads) {
-    const int G = (int)(it & 15);
-    const int64_t rr = it >> 4;                     // run index in block order
-    const int t0 = (int)(rr % runs) * kRun;
-    const int64_t blk = rr / runs;
-    const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
-    const float* mb = meta + blk * (int64_t)meta_rows * kD + 8 * G;
-    const int c = t0 / C;
-    float gm[8], gs[8], mu[8], sg[8];
-    auto row8 = [&](const float* r, float (&v)[8]) {
-      const float4 u0 = __ldg(reinterpret_cast<const float4*>(r));
-      const float4 u1 = __ldg(reinterpret_cast<const float4*>(r) + 1);
-      v[0] = u0.x; v[1] = u0.y; v[2] = u0.z; v[3] = u0.w;
-      v[4] = u1.x; v[5] = u1.y; v[6] = u1.z; v[7] = u1.w;
-    };
-    row8(mb, gm);
-    row8(mb + kD, gs);
-    row8(mb + (2 + c) * kD, mu);
-    row8(mb + (2 + NC + c) * kD, sg);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      gs[j] = __fadd_rn(gs[j], kEps);
-      sg[j] = __fadd_rn(sg[j], kEps);
+  const uint32_t meta_bytes = (uint32_t)meta_rows * kD * 4;
+  const uint32_t stage_bytes = code_bytes + meta_bytes;
+  uint8_t* stages = smem + bits_table_bytes<K>();
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + kBitsStages * stage_bytes);
+  const int tid = threadIdx.x, lane = tid & 31, G = tid & 15, slot = tid >> 4;
+  const int run = P >> 4, t0 = slot * run, chunk = t0 / C;
+  const int64_t ostride = (int64_t)H * kD;
+
+  for (int i = tid; i < NCODE * 32; i += kThreads) {
+    const int a = (i >> 5) >= NCODE / 2 ? (i >> 5) - NCODE : (i >> 5);
+    const float m = tab.x[(1 << (8 - K)) * (a >= 0 ? a : -a - 1) + (1 << (7 - K)) - 1];
+    xk[i] = a >= 0 ? m : -m;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kBitsStages; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const float* xl = xk + lane;
+
+  auto issue = [&](int64_t blk, int stage) {
+    uint8_t* st = stages + stage * stage_bytes;
+    mbar_expect_tx(&bars[stage], stage_bytes);
+    bulk_load(st, ak + blk * code_bytes, code_bytes, &bars[stage]);
+    bulk_load(st + code_bytes, meta + blk * (int64_t)meta_rows * kD, meta_bytes, &bars[stage]);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kBitsStages; ++i) {
+      const int64_t blk = blockIdx.x + (int64_t)i * gridDim.x;
+      if (blk < nblk) issue(blk, i);
     }
-    const uint8_t* src = ak + ((blk * P + t0) * 16 + G) * K;
-#pragma unroll  // every token's code loads in flight at once
-    for (int u = 0; u < kRun; ++u) {
-      uint64_t fa = 0;
+
+  int it = 0;
+  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+    const int stage = it % kBitsStages;
+    const uint32_t phase = (uint32_t)(it / kBitsStages) & 1u;
+    const bool ok = mbar_wait(&bars[stage], phase);
+    const uint8_t* st = stages + stage * stage_bytes;
+    const float* mrow = reinterpret_cast<const float*>(st + code_bytes) + 8 * G;
+    f2 gm[4], gs[4], mu[4], sg[4];
+    auto row8 = [&](const float* r, f2 (&v)[4], bool eps) {
+      const float4 u0 = reinterpret_cast<const float4*>(r)[0];
+      const float4 u1 = reinterpret_cast<const float4*>(r)[1];
+      v[0] = make_float2(u0.x, u0.y);
+      v[1] = make_float2(u0.z, u0.w);
+      v[2] = make_float2(u1.x, u1.y);
+      v[3] = make_float2(u1.z, u1.w);
+      if (eps) {
 #pragma unroll
-      for (int i = 0; i < K; ++i) fa |= (uint64_t)__ldg(src + u * 16 * K + i) << (8 * i);
-      float y[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        int a = (int)((fa >> (j * K)) & ((1u << K) - 1u));
-        if (a >= (1 << (K - 1))) a -= (1 << K);
-        const int V = a >= 0 ? a : -a - 1;
-        const float v = x[(1 << (8 - K)) * V + (1 << (7 - K)) - 1];
-        const float n = __fmaf_rn(a >= 0 ? v : -v, sg[j], mu[j]);
-        y[j] = __fmaf_rn(n, gs[j], gm[j]);
+        for (int j = 0; j < 4; ++j) v[j] = add2(v[j], make_float2(kEps, kEps));
       }
-      const int64_t o = ((b * L + p * P + t0 + u) * H + h) * kD + 8 * G;
+    };
+    row8(mrow, gm, false);
+    row8(mrow + kD, gs, true);
+    row8(mrow + (2 + chunk) * kD, mu, false);
+    row8(mrow + (2 + NC + chunk) * kD, sg, true);
+    const int64_t h = blk % H, rest = blk / H;
+    const int64_t p = rest % NB, b = rest / NB;
+    const int64_t orow0 = ((b * L + p * P + t0) * H + h) * kD + 8 * G;
+#pragma unroll 4
+    for (int r = 0; r < run; ++r) {
+      const uint32_t o = (uint32_t)((t0 + r) * 16 + G) * K;
+      const uint32_t* w = reinterpret_cast<const uint32_t*>(st) + (o >> 2);
+      const uint64_t fa = (((uint64_t)w[1] << 32) | w[0]) >> (8 * (o & 3));
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = xl[((uint32_t)(fa >> (j * K)) & (NCODE - 1u)) * 32u];
+      f2 y[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        y[j] = fma2(fma2(make_float2(v[2 * j], v[2 * j + 1]), sg[j], mu[j]), gs[j], gm[j]);
+      char* ob = reinterpret_cast<char*>(out);
+      const int64_t oe = orow0 + (int64_t)r * ostride;
       if constexpr (BF16OUT) {
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) =
-            make_uint4(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]), f2_to_bf2(y[4], y[5]),
-                       f2_to_bf2(y[6], y[7]));
+        stg_stream(ob + oe * 2, make_uint4(f2_to_bf2(y[0].x, y[0].y), f2_to_bf2(y[1].x, y[1].y),
+                                           f2_to_bf2(y[2].x, y[2].y), f2_to_bf2(y[3].x, y[3].y)));
       } else {
-        float4* q = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
-        q[0] = make_float4(y[0], y[1], y[2], y[3]);
-        q[1] = make_float4(y[4], y[5], y[6], y[7]);
+        stg_stream(ob + oe * 4, make_uint4(__float_as_uint(y[0].x), __float_as_uint(y[0].y),
+                                           __float_as_uint(y[1].x), __float_as_uint(y[1].y)));
+        stg_stream(ob + oe * 4 + 16, make_uint4(__float_as_uint(y[2].x), __float_as_uint(y[2].y),
+                                                __float_as_uint(y[3].x), __float_as_uint(y[3].y)));
+      }
+    }
+
+    if (!__syncthreads_and(ok)) {
+      // a stage never arrived: record it and stop this CTA (bounded waits)
+      if (tid == 0) {
+        atomicOr(&g_variant_wait_timeout, kFlagWaitTimeout);
+        for (int i = 0; i < kBitsStages; ++i) (void)mbar_wait(&bars[i], phase);
+      }
+      return;
+    }
+    // every thread is done with this stage: refill it kBitsStages blocks ahead
+    if (tid == 0) {
+      const int64_t nxt = blk + (int64_t)kBitsStages * gridDim.x;
+      if (nxt < nblk) {
+        fence_proxy_async();
+        issue(nxt, stage);
       }
     }
   }
@@ -553,22 +617,53 @@ bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p)
 
 }  // namespace
 
+cudaError_t read_variant_wait_timeout(unsigned int* flag) {
+  return cudaMemcpyFromSymbol(flag, g_variant_wait_timeout, sizeof(unsigned int));
+}
+
+template <int K, bool BF16OUT>
+static cudaError_t run_decode_bits(const uint8_t* ak, const float* meta, const Shape& s,
+                                   const ExpandTable& tab, void* out, cudaStream_t stream) {
+  auto fn = decode_anchor_bits_kernel<K, BF16OUT>;
+  const size_t stage = (size_t)s.page * 16 * K + (size_t)(2 + 2 * (s.page / s.C)) * kD * 4;
+  const size_t smem = bits_table_bytes<K>() + kBitsStages * stage + kBitsStages * 8;
+  constexpr size_t kMaxSmem = bits_table_bytes<K>() + kBitsStages * (256 * 16 * K + 34 * kD * 4) + 64;
+  static thread_local int configured_dev = -1;
+  static thread_local size_t last_smem = 0;
+  static thread_local int per_sm = 1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+    last_smem = 0;
+  }
+  if (smem != last_smem) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+    last_smem = smem;
+  }
+  const int64_t nblk = s.blocks();
+  int64_t grid = (int64_t)sm_count() * per_sm;
+  if (grid > nblk) grid = nblk;
+  fn<<<(unsigned)grid, kThreads, smem, stream>>>(ak, meta, nblk, s.NB(), s.H, s.L, s.page, s.C,
+                                                 out, tab);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_anchor_bits(const void* ak, const float* meta, const Shape& s, int k,
                                       const ExpandTable& tab, void* out, bool bf16_out,
                                       cudaStream_t stream) {
-  const int64_t nblk = s.blocks();
-  const unsigned grid = grid_for(nblk * (s.page / kRun) * 16, kThreads);
+  if (s.blocks() == 0) return cudaSuccess;
   const uint8_t* a = static_cast<const uint8_t*>(ak);
-#define LYNX_DAB(KK)                                                                        \
-  if (k == KK) {                                                                            \
-    if (bf16_out)                                                                           \
-      decode_anchor_bits_kernel<KK, true><<<grid, kThreads, 0, stream>>>(                   \
-          a, meta, nblk, s.NB(), s.H, s.L, s.page, s.C, out, tab);                          \
-    else                                                                                    \
-      decode_anchor_bits_kernel<KK, false><<<grid, kThreads, 0, stream>>>(                  \
-          a, meta, nblk, s.NB(), s.H, s.L, s.page, s.C, out, tab);                          \
-    return cudaGetLastError();                                                              \
-  }
+#define LYNX_DAB(KK)                                                                      \
+  if (k == KK)                                                                            \
+    return bf16_out ? run_decode_bits<KK, true>(a, meta, s, tab, out, stream)             \
+                    : run_decode_bits<KK, false>(a, meta, s, tab, out, stream);
   LYNX_DAB(3)
   LYNX_DAB(4)
   LYNX_DAB(5)
