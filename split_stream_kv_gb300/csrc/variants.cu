@@ -543,65 +543,126 @@ a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, 
   }
 }
 
-// Decode of the A.1 variant: one thread per (run of 8 tokens, group of 8
-// channels); a run lies in one 16-token chunk, so m and m_i load once.
-template <bool BF16OUT>
-__global__ void __launch_bounds__(kThreads)
+// Decode of the A.1 variant, persistent, like the 4+4 decoders: a block's
+// Anchor and Residual codes and its metadata rows (m, then m_i per 16-token
+// chunk) arrive in shared memory by bulk asynchronous copies, one stage
+// ahead; thread (slot, G) of 256 decodes a run of page/16 tokens (inside one
+// chunk) of channels 8G..8G+7.  The 8-bit code of a channel, Anchor nibble
+// above Residual nibble (Residual 7 in Anchor-only mode), read as an int8 is
+// Q; a lane-replicated table over that byte gives sgn(Q) X(min(|Q|, 127)).
+constexpr int kA1Stages = 2;
+constexpr size_t kA1Table = 256 * 32 * 4;
+
+template <bool FULL, bool BF16OUT>
+__global__ void __launch_bounds__(kThreads, 2)
 a1_decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ residual,
                  const float* __restrict__ meta, const int64_t nblk, const int64_t NB,
                  const int H, const int64_t L, const int P, void* __restrict__ out,
                  const __grid_constant__ ExpandTable tab) {
-  __shared__ float x[128];
-  for (int i = threadIdx.x; i < 128; i += kThreads) x[i] = tab.x[i];
+  extern __shared__ __align__(16) uint8_t smem[];
+  float* xq = reinterpret_cast<float*>(smem);     // [byte][lane]
+  const uint32_t code_bytes = (uint32_t)P * (kD / 2);
+  const int NCk = P / kA1Chunk;
+  const uint32_t meta_bytes = (uint32_t)(1 + NCk) * kD * 4;
+  const uint32_t stage_bytes = code_bytes * (FULL ? 2 : 1) + meta_bytes;
+  uint8_t* stages = smem + kA1Table;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + kA1Stages * stage_bytes);
+  const int tid = threadIdx.x, lane = tid & 31, G = tid & 15, slot = tid >> 4;
+  const int run = P >> 4, t0 = slot * run, chunk = t0 / kA1Chunk;
+  const int64_t ostride = (int64_t)H * kD;
+
+  for (int i = tid; i < 256 * 32; i += kThreads) {
+    const int Q = (int)(int8_t)(uint8_t)(i >> 5);
+    const int I = Q < 0 ? (-Q > 127 ? 127 : -Q) : Q;
+    xq[i] = Q < 0 ? -tab.x[I] : tab.x[I];
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kA1Stages; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
   __syncthreads();
-  const int NCk = P / kA1Chunk, runs = P / 8;
-  const int64_t items = nblk * runs * 16;
-  for (int64_t it = (int64_t)blockIdx.x * kThreads + threadIdx.x; it < items;
-       it += (int64_t)gridDim.x * kThreads) {
-    const int G = (int)(it & 15);
-    const int64_t rr = it >> 4;
-    const int t0 = (int)(rr % runs) * 8;
-    const int64_t blk = rr / runs;
-    const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
-    const float* mrow = meta + blk * (int64_t)(1 + NCk) * kD + 8 * G;
-    float m[8], mi[8];
-    {
-      const float4* p0 = reinterpret_cast<const float4*>(mrow);
-      const float4* p1 = reinterpret_cast<const float4*>(mrow + (1 + t0 / kA1Chunk) * kD);
-      const float4 u0 = __ldg(p0), u1 = __ldg(p0 + 1), v0 = __ldg(p1), v1 = __ldg(p1 + 1);
-      m[0] = u0.x; m[1] = u0.y; m[2] = u0.z; m[3] = u0.w;
-      m[4] = u1.x; m[5] = u1.y; m[6] = u1.z; m[7] = u1.w;
-      mi[0] = v0.x; mi[1] = v0.y; mi[2] = v0.z; mi[3] = v0.w;
-      mi[4] = v1.x; mi[5] = v1.y; mi[6] = v1.z; mi[7] = v1.w;
+  const uint32_t tbase = smem_u32(xq) + (uint32_t)lane * 4u;
+  // table value of byte POS of w
+  auto lut = [&](uint32_t w, int pos) -> float {
+    float v;
+    const uint32_t addr = tbase + (((w >> (8 * pos)) & 0xffu) << 7);
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+  };
+
+  auto issue = [&](int64_t blk, int stage) {
+    uint8_t* st = stages + stage * stage_bytes;
+    mbar_expect_tx(&bars[stage], stage_bytes);
+    bulk_load(st, anchor + blk * code_bytes, code_bytes, &bars[stage]);
+    if constexpr (FULL) bulk_load(st + code_bytes, residual + blk * code_bytes, code_bytes, &bars[stage]);
+    bulk_load(st + code_bytes * (FULL ? 2 : 1), meta + blk * (int64_t)(1 + NCk) * kD, meta_bytes,
+              &bars[stage]);
+  };
+  if (tid == 0)
+    for (int i = 0; i < kA1Stages; ++i) {
+      const int64_t blk = blockIdx.x + (int64_t)i * gridDim.x;
+      if (blk < nblk) issue(blk, i);
     }
-    const int64_t code0 = (blk * P + t0) * 16 + G;   // 32-bit word of (token t0, group G)
-#pragma unroll  // every token's code loads in flight at once
-    for (int u = 0; u < 8; ++u) {
-      const uint32_t wa = __ldg(reinterpret_cast<const uint32_t*>(anchor) + code0 + u * 16);
-      const uint32_t wr =
-          residual ? __ldg(reinterpret_cast<const uint32_t*>(residual) + code0 + u * 16)
-                   : 0x77777777u;                     // Anchor only: residual 7
-      float y[8];
+
+  int it = 0;
+  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+    const int stage = it % kA1Stages;
+    const uint32_t phase = (uint32_t)(it / kA1Stages) & 1u;
+    const bool ok = mbar_wait(&bars[stage], phase);
+    const uint8_t* st = stages + stage * stage_bytes;
+    const uint32_t* aw = reinterpret_cast<const uint32_t*>(st) + t0 * 16 + G;
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(st + code_bytes) + t0 * 16 + G;
+    const float* mrow = reinterpret_cast<const float*>(st + code_bytes * (FULL ? 2 : 1)) + 8 * G;
+    f2 m2[4], mi2[4];
+    {
+      const float4 u0 = reinterpret_cast<const float4*>(mrow)[0];
+      const float4 u1 = reinterpret_cast<const float4*>(mrow)[1];
+      const float4 v0 = reinterpret_cast<const float4*>(mrow + (1 + chunk) * kD)[0];
+      const float4 v1 = reinterpret_cast<const float4*>(mrow + (1 + chunk) * kD)[1];
+      m2[0] = make_float2(u0.x, u0.y); m2[1] = make_float2(u0.z, u0.w);
+      m2[2] = make_float2(u1.x, u1.y); m2[3] = make_float2(u1.z, u1.w);
+      mi2[0] = make_float2(v0.x, v0.y); mi2[1] = make_float2(v0.z, v0.w);
+      mi2[2] = make_float2(v1.x, v1.y); mi2[3] = make_float2(v1.z, v1.w);
+    }
+    const int64_t h = blk % H, rest = blk / H;
+    const int64_t p = rest % NB, b = rest / NB;
+    const int64_t orow0 = ((b * L + p * P + t0) * H + h) * kD + 8 * G;
+#pragma unroll 4
+    for (int r = 0; r < run; ++r) {
+      const uint32_t a = aw[r * 16], rr = FULL ? rw[r * 16] : 0x77777777u;
+      const uint32_t E = ((a << 4) & 0xf0f0f0f0u) | (rr & 0x0f0f0f0fu);  // codes of ch 0-3
+      const uint32_t O = (a & 0xf0f0f0f0u) | ((rr >> 4) & 0x0f0f0f0fu);  // codes of ch 4-7
+      const f2 v[4] = {make_float2(lut(E, 0), lut(E, 1)), make_float2(lut(E, 2), lut(E, 3)),
+                       make_float2(lut(O, 0), lut(O, 1)), make_float2(lut(O, 2), lut(O, 3))};
+      f2 y[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int sh = 8 * (j & 3) + ((j & 4) ? 4 : 0);
-        int qa = (int)((wa >> sh) & 0xfu);
-        if (qa >= 8) qa -= 16;
-        const int Q = qa * 16 + (int)((wr >> sh) & 0xfu);
-        int I = Q < 0 ? -Q : Q;
-        I = I > 127 ? 127 : I;
-        const float v = Q < 0 ? -x[I] : x[I];
-        y[j] = __fmul_rn(__fmul_rn(v, mi[j]), m[j]);
-      }
-      const int64_t o = ((b * L + p * P + t0 + u) * H + h) * kD + 8 * G;
+      for (int k = 0; k < 4; ++k) y[k] = mul2(mul2(v[k], mi2[k]), m2[k]);
+      char* ob = reinterpret_cast<char*>(out);
+      const int64_t oe = orow0 + (int64_t)r * ostride;
       if constexpr (BF16OUT) {
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + o) =
-            make_uint4(f2_to_bf2(y[0], y[1]), f2_to_bf2(y[2], y[3]), f2_to_bf2(y[4], y[5]),
-                       f2_to_bf2(y[6], y[7]));
+        stg_stream(ob + oe * 2, make_uint4(f2_to_bf2(y[0].x, y[0].y), f2_to_bf2(y[1].x, y[1].y),
+                                           f2_to_bf2(y[2].x, y[2].y), f2_to_bf2(y[3].x, y[3].y)));
       } else {
-        float4* q = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
-        q[0] = make_float4(y[0], y[1], y[2], y[3]);
-        q[1] = make_float4(y[4], y[5], y[6], y[7]);
+        stg_stream(ob + oe * 4, make_uint4(__float_as_uint(y[0].x), __float_as_uint(y[0].y),
+                                           __float_as_uint(y[1].x), __float_as_uint(y[1].y)));
+        stg_stream(ob + oe * 4 + 16, make_uint4(__float_as_uint(y[2].x), __float_as_uint(y[2].y),
+                                                __float_as_uint(y[3].x), __float_as_uint(y[3].y)));
+      }
+    }
+
+    if (!__syncthreads_and(ok)) {
+      // a stage never arrived: record it and stop this CTA (bounded waits)
+      if (tid == 0) {
+        atomicOr(&g_variant_wait_timeout, kFlagWaitTimeout);
+        for (int i = 0; i < kA1Stages; ++i) (void)mbar_wait(&bars[i], phase);
+      }
+      return;
+    }
+    if (tid == 0) {
+      const int64_t nxt = blk + (int64_t)kA1Stages * gridDim.x;
+      if (nxt < nblk) {
+        fence_proxy_async();
+        issue(nxt, stage);
       }
     }
   }
@@ -683,21 +744,53 @@ cudaError_t launch_a1_encode(const void* kv, const Shape& s, const CompanderTabl
   return cudaGetLastError();
 }
 
+template <bool FULL, bool BF16OUT>
+static cudaError_t run_a1_decode(const uint8_t* a, const uint8_t* r, const float* meta,
+                                 const Shape& s, const ExpandTable& tab, void* out,
+                                 cudaStream_t stream) {
+  auto fn = a1_decode_kernel<FULL, BF16OUT>;
+  const size_t stage = (size_t)s.page * (kD / 2) * (FULL ? 2 : 1) +
+                       (size_t)(1 + s.page / kA1Chunk) * kD * 4;
+  const size_t smem = kA1Table + kA1Stages * stage + kA1Stages * 8;
+  constexpr size_t kMaxSmem = kA1Table + kA1Stages * (256 * 64 * 2 + 17 * kD * 4) + 64;
+  static thread_local int configured_dev = -1;
+  static thread_local size_t last_smem = 0;
+  static thread_local int per_sm = 1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_dev != dev) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+    last_smem = 0;
+  }
+  if (smem != last_smem) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, smem);
+    if (e != cudaSuccess) return e;
+    per_sm = n > 0 ? n : 1;
+    last_smem = smem;
+  }
+  const int64_t nblk = s.blocks();
+  int64_t grid = (int64_t)sm_count() * per_sm;
+  if (grid > nblk) grid = nblk;
+  fn<<<(unsigned)grid, kThreads, smem, stream>>>(a, r, meta, nblk, s.NB(), s.H, s.L, s.page,
+                                                 out, tab);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_a1_decode(const void* anchor, const void* residual, const float* meta,
                              const Shape& s, const ExpandTable& tab, void* out, bool bf16_out,
                              cudaStream_t stream) {
-  const int64_t nblk = s.blocks();
-  if (nblk > 0x7fffffff) return cudaErrorInvalidValue;
+  if (s.blocks() == 0) return cudaSuccess;
   const uint8_t* a = static_cast<const uint8_t*>(anchor);
   const uint8_t* r = static_cast<const uint8_t*>(residual);
-  const unsigned grid = grid_for(nblk * (s.page / 8) * 16, kThreads);
-  if (bf16_out)
-    a1_decode_kernel<true><<<grid, kThreads, 0, stream>>>(a, r, meta, nblk, s.NB(), s.H, s.L,
-                                                          s.page, out, tab);
-  else
-    a1_decode_kernel<false><<<grid, kThreads, 0, stream>>>(a, r, meta, nblk, s.NB(), s.H, s.L,
-                                                           s.page, out, tab);
-  return cudaGetLastError();
+  if (r)
+    return bf16_out ? run_a1_decode<true, true>(a, r, meta, s, tab, out, stream)
+                    : run_a1_decode<true, false>(a, r, meta, s, tab, out, stream);
+  return bf16_out ? run_a1_decode<false, true>(a, nullptr, meta, s, tab, out, stream)
+                  : run_a1_decode<false, false>(a, nullptr, meta, s, tab, out, stream);
 }
 
 }  // namespace lynx
