@@ -148,6 +148,14 @@ __device__ __forceinline__ uint64_t group_codes(uint32_t a, uint32_t r) {
 // k-bit fields of the 8 codes' top bits of a group fill K bytes, the low 8-K
 // bits 8-K bytes (channel j at bits j*w .. j*w + w - 1, little-endian), so 4
 // groups are K and 8-K whole 32-bit words.
+// Four W-bit fields held in the low bits of the four bytes of x, packed
+// into the low 4W bits: byte pairs into 16-bit lanes, then the two lanes.
+template <int W>
+__device__ __forceinline__ uint32_t pack4(uint32_t x) {
+  const uint32_t y = (x & 0x00ff00ffu) | ((x & 0xff00ff00u) >> (8 - W));
+  return (y & 0x0000ffffu) | ((y & 0xffff0000u) >> (16 - 2 * W));
+}
+
 template <int K>
 __global__ void __launch_bounds__(kThreads) split_bits_kernel(const uint8_t* __restrict__ anchor,
                                                               const uint8_t* __restrict__ residual,
@@ -155,43 +163,57 @@ __global__ void __launch_bounds__(kThreads) split_bits_kernel(const uint8_t* __r
                                                               uint8_t* __restrict__ ak,
                                                               uint8_t* __restrict__ rk) {
   constexpr int RW = 8 - K;
+  constexpr uint32_t kMaskA = 0x01010101u * ((1u << K) - 1u);
+  constexpr uint32_t kMaskR = 0x01010101u * ((1u << RW) - 1u);
   const int64_t quads = groups / 4;
   for (int64_t qi = (int64_t)blockIdx.x * kThreads + threadIdx.x; qi < quads;
        qi += (int64_t)gridDim.x * kThreads) {
     const uint4 a4 = __ldg(reinterpret_cast<const uint4*>(anchor) + qi);
     const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(residual) + qi);
     const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w}, rw[4] = {r4.x, r4.y, r4.z, r4.w};
+    // the four groups' k-bit (and 8-k bit) fields as one bit stream each, in
+    // 32-bit words: group q's 8 fields fill bits 8K q .. 8K q + 8K - 1
     uint32_t oa[K], orr[RW];
-#pragma unroll
-    for (int i = 0; i < K; ++i) oa[i] = 0;
-#pragma unroll
-    for (int i = 0; i < RW; ++i) orr[i] = 0;
+    uint64_t acc_a = 0, acc_r = 0;
+    int na = 0, nr = 0, ia = 0, ir = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint64_t c = group_codes(aw[q], rw[q]);
-      uint64_t fa = 0, fr = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t q8 = (uint32_t)(c >> (8 * j)) & 0xffu;
-        fa |= (uint64_t)(q8 >> RW) << (j * K);
-        fr |= (uint64_t)(q8 & ((1u << RW) - 1u)) << (j * RW);
+      // 8-bit codes of channels 0-3 (E) and 4-7 (O) of the group
+      const uint32_t E = ((aw[q] << 4) & 0xf0f0f0f0u) | (rw[q] & 0x0f0f0f0fu);
+      const uint32_t O = (aw[q] & 0xf0f0f0f0u) | ((rw[q] >> 4) & 0x0f0f0f0fu);
+      const uint64_t fa = (uint64_t)pack4<K>((E >> RW) & kMaskA) |
+                          ((uint64_t)pack4<K>((O >> RW) & kMaskA) << (4 * K));
+      const uint64_t fr = (uint64_t)pack4<RW>(E & kMaskR) |
+                          ((uint64_t)pack4<RW>(O & kMaskR) << (4 * RW));
+      acc_a |= fa << na;
+      na += 8 * K;
+      while (na >= 32) {
+        oa[ia++] = (uint32_t)acc_a;
+        acc_a >>= 32;
+        na -= 32;
       }
-      // bytes q*K .. q*K+K-1 of the thread's 4K anchor bytes
-#pragma unroll
-      for (int i = 0; i < K; ++i) {
-        const int byte = q * K + i;
-        oa[byte >> 2] |= (uint32_t)((fa >> (8 * i)) & 0xffu) << (8 * (byte & 3));
-      }
-#pragma unroll
-      for (int i = 0; i < RW; ++i) {
-        const int byte = q * RW + i;
-        orr[byte >> 2] |= (uint32_t)((fr >> (8 * i)) & 0xffu) << (8 * (byte & 3));
+      acc_r |= fr << nr;
+      nr += 8 * RW;
+      while (nr >= 32) {
+        orr[ir++] = (uint32_t)acc_r;
+        acc_r >>= 32;
+        nr -= 32;
       }
     }
+    // 4K and 4(8-K) bytes a thread: 8-byte stores when K is even
+    if constexpr (K % 2 == 0) {
 #pragma unroll
-    for (int i = 0; i < K; ++i) reinterpret_cast<uint32_t*>(ak)[qi * K + i] = oa[i];
+      for (int i = 0; i < K; i += 2)
+        reinterpret_cast<uint2*>(ak)[(qi * K + i) / 2] = make_uint2(oa[i], oa[i + 1]);
 #pragma unroll
-    for (int i = 0; i < RW; ++i) reinterpret_cast<uint32_t*>(rk)[qi * RW + i] = orr[i];
+      for (int i = 0; i < RW; i += 2)
+        reinterpret_cast<uint2*>(rk)[(qi * RW + i) / 2] = make_uint2(orr[i], orr[i + 1]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < K; ++i) reinterpret_cast<uint32_t*>(ak)[qi * K + i] = oa[i];
+#pragma unroll
+      for (int i = 0; i < RW; ++i) reinterpret_cast<uint32_t*>(rk)[qi * RW + i] = orr[i];
+    }
   }
 }
 
