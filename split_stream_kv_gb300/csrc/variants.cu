@@ -60,33 +60,35 @@ __global__ void __launch_bounds__(kThreads) int_encode_kernel(const uint8_t* __r
     for (int i = 0; i < R; ++i) {
       const int64_t row = myr0 + i;
       const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-      float f[8];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        f[2 * j] = bf16_lo(w[j]);
-        f[2 * j + 1] = bf16_hi(w[j]);
-      }
-      float lo = f[0], hi = f[0];
-#pragma unroll
-      for (int j = 1; j < 8; ++j) {
-        lo = fminf(lo, f[j]);
-        hi = fmaxf(hi, f[j]);
-      }
+      // row minimum and maximum on bf16 pairs (exact), then the half-warp
+      uint32_t mn2 = bf2_min(bf2_min(w[0], w[1]), bf2_min(w[2], w[3]));
+      uint32_t mx2 = bf2_max(bf2_max(w[0], w[1]), bf2_max(w[2], w[3]));
 #pragma unroll
       for (int o = 8; o; o >>= 1) {                // within the half-warp
-        lo = fminf(lo, __shfl_xor_sync(kFull, lo, o));
-        hi = fmaxf(hi, __shfl_xor_sync(kFull, hi, o));
+        mn2 = bf2_min(mn2, __shfl_xor_sync(kFull, mn2, o));
+        mx2 = bf2_max(mx2, __shfl_xor_sync(kFull, mx2, o));
       }
+      float lo = fminf(bf16_lo(mn2), bf16_hi(mn2));
+      float hi = fmaxf(bf16_lo(mx2), bf16_hi(mx2));
       if (row >= rows) continue;
       lo = __fadd_rn(lo, 0.0f);  // a zero extreme counts as +0
       hi = __fadd_rn(hi, 0.0f);
       const float S = __fdiv_rn(__fsub_rn(hi, lo), (float)qmax);
       const float rs = S > 0.0f ? __frcp_rn(S) : 0.0f;
       uint32_t q[8];
+      const f2 lo2 = make_float2(lo, lo);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int c = __float2int_rn(__fmul_rn(__fsub_rn(f[j], lo), rs));
-        q[j] = (uint32_t)(c < 0 ? 0 : c > qmax ? qmax : c);
+      for (int j = 0; j < 4; ++j) {
+        // (x - lo) rs per lane: the differences as a packed pair, the products
+        // scalar __fmul_rn (never contracted into the add that follows); then
+        // round to nearest even on the FMA pipe: for 0 <= y < 2^22 the bits of
+        // y + 1.5 * 2^23 hold round(y) above 0x4B400000
+        const f2 d = sub2(bf2_to_f2(w[j]), lo2);
+        const f2 y = make_float2(__fmul_rn(d.x, rs), __fmul_rn(d.y, rs));
+        const f2 t = add2(y, make_float2(12582912.0f, 12582912.0f));
+        const int c0 = (int)__float_as_uint(t.x) - 0x4B400000, c1 = (int)__float_as_uint(t.y) - 0x4B400000;
+        q[2 * j] = (uint32_t)(c0 < 0 ? 0 : c0 > qmax ? qmax : c0);
+        q[2 * j + 1] = (uint32_t)(c1 < 0 ? 0 : c1 > qmax ? qmax : c1);
       }
       if constexpr (BITS == 8) {
         *reinterpret_cast<uint2*>(codes + row * 128 + hl * 8) =
