@@ -24,13 +24,6 @@ constexpr int kThreads = 256;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__device__ __forceinline__ uint2 ldg_stream8(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-               : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
-
 // ----------------------------------------------------------------- INT-B
 
 // One token row of 128 BF16 channels per half-warp, 8 channels a lane (one
@@ -136,15 +129,6 @@ __global__ void __launch_bounds__(kThreads) int_decode_kernel(const uint8_t* __r
 }
 
 // ---------------------------------------------------------- bit splits
-
-// The signed 8-bit codes of one group of 8 channels (8G..8G+7) of one token
-// from the 4+4 nibble streams: byte j of the group holds channel 8G+j (low
-// nibble) and 8G+j+4 (high nibble).  code j in byte j of the result.
-__device__ __forceinline__ uint64_t group_codes(uint32_t a, uint32_t r) {
-  const uint32_t lo = ((a << 4) & 0xf0f0f0f0u) | (r & 0x0f0f0f0fu);  // channels 8G+0..3
-  const uint32_t hi = (a & 0xf0f0f0f0u) | ((r >> 4) & 0x0f0f0f0fu);  // channels 8G+4..7
-  return (uint64_t)lo | ((uint64_t)hi << 32);
-}
 
 // One thread per 4 consecutive groups (32 channels of one token row): the
 // k-bit fields of the 8 codes' top bits of a group fill K bytes, the low 8-K
