@@ -389,9 +389,11 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
 // ---------------------------------------------------------- Appendix A.1
 
 // One CTA per page block, one thread per (16-token chunk k, group G of 8
-// channels): P threads.  A thread holds its chunk's 16 rows of 16 bytes in
-// registers.  The page maximum of |x| (exact, on bf16 pairs) combines the
-// chunks' maxima through shared memory.  The chunk maximum of |x'| = |x| rm
+// channels): P threads.  A thread reads its chunk's 16 rows of 16 bytes
+// twice: once for the maxima, once (from L1/L2) for the codes, which keeps
+// its registers, and so the warps an SM holds, at twice what keeping the
+// rows would allow.  The page maximum of |x| (exact, on bf16 pairs) combines
+// the chunks' maxima through shared memory.  The chunk maximum of |x'| = |x| rm
 // is rn(max|x| rm): rounding is monotone.  |Q| comes from the encoder's fast
 // rounding, run on pairs of channels, with the host thresholds of Eq. 7
 // (|Q| = #{k : a >= thr[k]}) deciding inside its window, or from a binary
@@ -447,17 +449,16 @@ a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, 
   const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
   for (int i = tid; i < 128; i += P) thr[i] = tab.thr[i];   // P >= 64 threads
   const uint8_t* src = kv + ((b * L + p * P + k * kA1Chunk) * H + h) * 256 + 16 * G;
-  uint4 w[kA1Chunk];
-#pragma unroll
-  for (int t = 0; t < kA1Chunk; ++t)
-    w[t] = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)t * H * 256));
+  // pass 1: the chunk maxima only; pass 2 reads the rows again (from L1/L2)
+  // rather than holding them, to keep registers low
   uint32_t cm[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int t = 0; t < kA1Chunk; ++t) {
-    cm[0] = bf2_max(cm[0], w[t].x & 0x7fff7fffu);
-    cm[1] = bf2_max(cm[1], w[t].y & 0x7fff7fffu);
-    cm[2] = bf2_max(cm[2], w[t].z & 0x7fff7fffu);
-    cm[3] = bf2_max(cm[3], w[t].w & 0x7fff7fffu);
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)t * H * 256));
+    cm[0] = bf2_max(cm[0], v.x & 0x7fff7fffu);
+    cm[1] = bf2_max(cm[1], v.y & 0x7fff7fffu);
+    cm[2] = bf2_max(cm[2], v.z & 0x7fff7fffu);
+    cm[3] = bf2_max(cm[3], v.w & 0x7fff7fffu);
   }
   pmx[k][G] = make_uint4(cm[0], cm[1], cm[2], cm[3]);
   __syncthreads();
@@ -498,9 +499,10 @@ a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, 
   const f2 alpha2 = make_float2(tab.alpha, tab.alpha), c16_2 = make_float2(tab.c16, tab.c16);
   uint32_t* arow = anchor + (blk * P + k * kA1Chunk) * 16 + G;
   uint32_t* rrow = residual + (blk * P + k * kA1Chunk) * 16 + G;
-#pragma unroll
+#pragma unroll 4
   for (int t = 0; t < kA1Chunk; ++t) {
-    const uint32_t wj[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
+    const uint4 wt = __ldg(reinterpret_cast<const uint4*>(src + (int64_t)t * H * 256));
+    const uint32_t wj[4] = {wt.x, wt.y, wt.z, wt.w};
     uint32_t bits[8], sbits[8];
     float av[8];
 #pragma unroll
