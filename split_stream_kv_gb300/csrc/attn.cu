@@ -878,6 +878,8 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       ps[RP + r] = den;
     }
   }
+  // the split combine may launch now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Merge the partials of one query row of one unit (sequence, KV head, row
@@ -896,6 +898,9 @@ constexpr int kCombineWarps = 4;
 constexpr int kCombineBatch = 8;
 __global__ void __launch_bounds__(32 * kCombineWarps)
 attn_combine(const __grid_constant__ AttnParams a, int RP) {
+  // launched as a programmatic dependent of the attention kernel: wait until
+  // that grid has completed and its partials are visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t z = blockIdx.x;  // (b * Hkv + h) * nrg + rg
   const int r = blockIdx.y * kCombineWarps + (threadIdx.x >> 5);
@@ -1023,9 +1028,18 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   fn<<<(unsigned)prm.n_cta, threads, smem, stream>>>(prm, tab);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_combine<<<dim3((unsigned)(prm.batch * prm.Hkv * prm.nrg),
-                      (unsigned)((8 * NT + kCombineWarps - 1) / kCombineWarps)),
-                 32 * kCombineWarps, 0, stream>>>(prm, 8 * NT);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(prm.batch * prm.Hkv * prm.nrg),
+                     (unsigned)((8 * NT + kCombineWarps - 1) / kCombineWarps));
+  cfg.blockDim = dim3(32 * kCombineWarps);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_combine, prm, 8 * NT);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
