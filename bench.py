@@ -698,7 +698,7 @@ def measure_variants(kv, anc, res, meta, dev, reps=5):
     row("a1_decode_full", lambda: lynx.lynx_a1_decode(*a1, c["L"], c["P"], 100.0, out=dec),
         n * 3 + a1_meta)
     del a1, dec
-    for k in (6, 3):
+    for k in (6, 5, 3):
         ak, rk = lynx.lynx_split_bits(anc, res, k)
         row(f"split_{k}+{8 - k}", lambda: lynx.lynx_split_bits(anc, res, k, ak, rk), n * 2)
         dec = torch.empty_like(kv)

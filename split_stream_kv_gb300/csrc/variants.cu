@@ -142,6 +142,21 @@ __device__ __forceinline__ uint32_t pack4(uint32_t x) {
   return (y & 0x0000ffffu) | ((y & 0xffff0000u) >> (16 - 2 * W));
 }
 
+// n words from shared to global memory, 16 bytes an instruction where the
+// destination allows (it does for every tile start: see the caller).
+__device__ __forceinline__ void copy_out_words(const uint32_t* s, uint32_t* g, int n) {
+  const int n4 = n >> 2;
+  for (int j = threadIdx.x; j < n4; j += kThreads)
+    reinterpret_cast<uint4*>(g)[j] = reinterpret_cast<const uint4*>(s)[j];
+  for (int j = (n4 << 2) + threadIdx.x; j < n; j += kThreads) g[j] = s[j];
+}
+
+// A thread packs one quad (4 groups of 8 channels) into K words of the
+// k-bit stream and 8-K words of the (8-k)-bit stream.  The words of a tile
+// of kThreads quads are contiguous in each stream, so they are staged in
+// shared memory and written out as whole 16-byte stores: written straight
+// from the threads, every store instruction would hit K (or 8-K) partial
+// sectors per 128 bytes.
 template <int K>
 __global__ void __launch_bounds__(kThreads) split_bits_kernel(const uint8_t* __restrict__ anchor,
                                                               const uint8_t* __restrict__ residual,
@@ -151,55 +166,58 @@ __global__ void __launch_bounds__(kThreads) split_bits_kernel(const uint8_t* __r
   constexpr int RW = 8 - K;
   constexpr uint32_t kMaskA = 0x01010101u * ((1u << K) - 1u);
   constexpr uint32_t kMaskR = 0x01010101u * ((1u << RW) - 1u);
+  __shared__ __align__(16) uint32_t stage[kThreads * 8];
+  uint32_t* sa = stage;                  // [kThreads][K]
+  uint32_t* sr = stage + kThreads * K;   // [kThreads][8-K]
   const int64_t quads = groups / 4;
-  for (int64_t qi = (int64_t)blockIdx.x * kThreads + threadIdx.x; qi < quads;
-       qi += (int64_t)gridDim.x * kThreads) {
-    const uint4 a4 = __ldg(reinterpret_cast<const uint4*>(anchor) + qi);
-    const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(residual) + qi);
-    const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w}, rw[4] = {r4.x, r4.y, r4.z, r4.w};
-    // the four groups' k-bit (and 8-k bit) fields as one bit stream each, in
-    // 32-bit words: group q's 8 fields fill bits 8K q .. 8K q + 8K - 1
-    uint32_t oa[K], orr[RW];
-    uint64_t acc_a = 0, acc_r = 0;
-    int na = 0, nr = 0, ia = 0, ir = 0;
+  const int64_t ntiles = (quads + kThreads - 1) / kThreads;
+  for (int64_t ti = blockIdx.x; ti < ntiles; ti += gridDim.x) {
+    const int64_t q0 = ti * kThreads, qi = q0 + threadIdx.x;
+    const int nq = (int)(quads - q0 < kThreads ? quads - q0 : kThreads);
+    if (qi < quads) {
+      const uint4 a4 = __ldg(reinterpret_cast<const uint4*>(anchor) + qi);
+      const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(residual) + qi);
+      const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w}, rw[4] = {r4.x, r4.y, r4.z, r4.w};
+      // the four groups' k-bit (and 8-k bit) fields as one bit stream each, in
+      // 32-bit words: group q's 8 fields fill bits 8K q .. 8K q + 8K - 1
+      uint32_t oa[K], orr[RW];
+      uint64_t acc_a = 0, acc_r = 0;
+      int na = 0, nr = 0, ia = 0, ir = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      // 8-bit codes of channels 0-3 (E) and 4-7 (O) of the group
-      const uint32_t E = ((aw[q] << 4) & 0xf0f0f0f0u) | (rw[q] & 0x0f0f0f0fu);
-      const uint32_t O = (aw[q] & 0xf0f0f0f0u) | ((rw[q] >> 4) & 0x0f0f0f0fu);
-      const uint64_t fa = (uint64_t)pack4<K>((E >> RW) & kMaskA) |
-                          ((uint64_t)pack4<K>((O >> RW) & kMaskA) << (4 * K));
-      const uint64_t fr = (uint64_t)pack4<RW>(E & kMaskR) |
-                          ((uint64_t)pack4<RW>(O & kMaskR) << (4 * RW));
-      acc_a |= fa << na;
-      na += 8 * K;
-      while (na >= 32) {
-        oa[ia++] = (uint32_t)acc_a;
-        acc_a >>= 32;
-        na -= 32;
+      for (int q = 0; q < 4; ++q) {
+        // 8-bit codes of channels 0-3 (E) and 4-7 (O) of the group
+        const uint32_t E = ((aw[q] << 4) & 0xf0f0f0f0u) | (rw[q] & 0x0f0f0f0fu);
+        const uint32_t O = (aw[q] & 0xf0f0f0f0u) | ((rw[q] >> 4) & 0x0f0f0f0fu);
+        const uint64_t fa = (uint64_t)pack4<K>((E >> RW) & kMaskA) |
+                            ((uint64_t)pack4<K>((O >> RW) & kMaskA) << (4 * K));
+        const uint64_t fr = (uint64_t)pack4<RW>(E & kMaskR) |
+                            ((uint64_t)pack4<RW>(O & kMaskR) << (4 * RW));
+        acc_a |= fa << na;
+        na += 8 * K;
+        while (na >= 32) {
+          oa[ia++] = (uint32_t)acc_a;
+          acc_a >>= 32;
+          na -= 32;
+        }
+        acc_r |= fr << nr;
+        nr += 8 * RW;
+        while (nr >= 32) {
+          orr[ir++] = (uint32_t)acc_r;
+          acc_r >>= 32;
+          nr -= 32;
+        }
       }
-      acc_r |= fr << nr;
-      nr += 8 * RW;
-      while (nr >= 32) {
-        orr[ir++] = (uint32_t)acc_r;
-        acc_r >>= 32;
-        nr -= 32;
-      }
+#pragma unroll
+      for (int i = 0; i < K; ++i) sa[threadIdx.x * K + i] = oa[i];
+#pragma unroll
+      for (int i = 0; i < RW; ++i) sr[threadIdx.x * RW + i] = orr[i];
     }
-    // 4K and 4(8-K) bytes a thread: 8-byte stores when K is even
-    if constexpr (K % 2 == 0) {
-#pragma unroll
-      for (int i = 0; i < K; i += 2)
-        reinterpret_cast<uint2*>(ak)[(qi * K + i) / 2] = make_uint2(oa[i], oa[i + 1]);
-#pragma unroll
-      for (int i = 0; i < RW; i += 2)
-        reinterpret_cast<uint2*>(rk)[(qi * RW + i) / 2] = make_uint2(orr[i], orr[i + 1]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < K; ++i) reinterpret_cast<uint32_t*>(ak)[qi * K + i] = oa[i];
-#pragma unroll
-      for (int i = 0; i < RW; ++i) reinterpret_cast<uint32_t*>(rk)[qi * RW + i] = orr[i];
-    }
+    __syncthreads();
+    // tile ti starts at word q0*K (q0*(8-K)): byte offsets that are
+    // multiples of 4 * kThreads, so 16-byte aligned
+    copy_out_words(sa, reinterpret_cast<uint32_t*>(ak) + q0 * K, nq * K);
+    copy_out_words(sr, reinterpret_cast<uint32_t*>(rk) + q0 * RW, nq * RW);
+    __syncthreads();   // the stage is refilled by the next tile
   }
 }
 

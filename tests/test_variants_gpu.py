@@ -88,6 +88,23 @@ CASES = [(2, 512, 2, 128, 32), (1, 512, 3, 256, 64), (3, 256, 1, 64, 16), (2, 38
 
 
 @pytest.mark.parametrize("k", [3, 4, 5, 6])
+@pytest.mark.parametrize("rows", [1, 63, 100, 64 * 3 + 17, 64 * 40])
+def test_bit_splits_ragged_rows(lynx_lib, oracle_mod, cuda_dev, k, rows):
+    """Raw 4+4 streams of any row count: the kernel stages 64 rows (256 quads)
+    at a time, so counts that are not a multiple of 64 end in a partial tile."""
+    g = torch.Generator(device="cpu").manual_seed(1000 * k + rows)
+    anc = torch.randint(0, 256, (rows, 64), generator=g, dtype=torch.uint8)
+    res = torch.randint(0, 256, (rows, 64), generator=g, dtype=torch.uint8)
+    ak, rk = lynx_lib.lynx_split_bits(anc.to(cuda_dev), res.to(cuda_dev), k)
+    a4, r4 = lynx_lib.lynx_join_bits(ak, rk, k)
+    torch.cuda.synchronize()
+    ok_, okr = oracle_mod.split_bits(anc.numpy(), res.numpy(), k)
+    same_bytes(ak, ok_, "anchor_k")
+    same_bytes(rk, okr, "residual_k")
+    assert torch.equal(a4.cpu(), anc) and torch.equal(r4.cpu(), res)
+
+
+@pytest.mark.parametrize("k", [3, 4, 5, 6])
 @pytest.mark.parametrize("B,L,H,P,C", CASES)
 def test_bit_splits_match_oracle(lynx_lib, oracle_mod, cuda_dev, k, B, L, H, P, C):
     from split_stream_kv_gb300 import synth
