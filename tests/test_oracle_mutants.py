@@ -16,6 +16,13 @@ import oracle
 from . import test_oracle_pins as pins
 
 MUTANTS = [
+    ("range encode: page and head swapped",
+     '        int64_t h = blk % H;\n        int64_t p = (blk / H) % NB;\n        int64_t b = blk / (H * NB);\n        const uint16_t *x',
+     '        int64_t p = blk % NB;\n        int64_t h = (blk / NB) % H;\n        int64_t b = blk / (H * NB);\n        const uint16_t *x'),
+    ("range encode: rows read at stride D", 'oracle_encode_block(x, (int64_t)H * D, P, D, C, alpha,',
+     'oracle_encode_block(x, (int64_t)D, P, D, C, alpha,'),
+    ("range decode: rows written at stride D", 'alpha, o,\n                                     (int64_t)H * D);',
+     'alpha, o,\n                                     (int64_t)D);'),
     ("compander numerator 128 instead of 127",
      "return 127.0 * log1p(al * (double)a) / log1p(al);",
      "return 128.0 * log1p(al * (double)a) / log1p(al);"),

@@ -320,6 +320,29 @@ def test_encode_invariants(oracle_mod, P, C):
                 assert np.unique(qs[xs == v]).size == 1
 
 
+
+def test_range_layout_is_batch_page_head(oracle_mod):
+    """encode() / decode() over a [B][L][H][D] tensor: block (b, p, h) of the
+    streams is tokens p*P .. p*P + P - 1 of head h of batch b, encoded alone,
+    and decode() writes it back to the same tokens and head."""
+    B, NB, H, P, C = 2, 3, 2, 64, 16
+    L = NB * P
+    rng = np.random.default_rng(11)
+    x = (rng.laplace(size=(B, L, H, 128)) *
+         rng.uniform(0.5, 4.0, size=(1, 1, H, 128))).astype(np.float32)
+    bits = oracle_mod.f32_to_bf16_bits(x).reshape(B, L, H, 128)
+    anc, res, meta = oracle_mod.encode(bits, P, C, ALPHA)
+    dec = oracle_mod.decode(anc, res, meta, L, P, C, ALPHA)
+    for b in range(B):
+        for p in range(NB):
+            for h in range(H):
+                a1, r1, m1 = oracle_mod.encode_block(bits[b, p * P:(p + 1) * P, h], C, ALPHA)
+                assert np.array_equal(anc[b, p, h], a1), (b, p, h)
+                assert np.array_equal(res[b, p, h], r1), (b, p, h)
+                assert np.array_equal(meta[b, p, h], m1), (b, p, h)
+                d1 = oracle_mod.decode_block(a1, r1, m1, C, ALPHA)
+                assert np.array_equal(dec[b, p * P:(p + 1) * P, h], d1), (b, p, h)
+
 def _X(y, alpha=ALPHA):
     """Continuous inverse of Eq. 7 (for the half-code boundaries)."""
     return (np.power(1.0 + alpha, np.asarray(y, np.float64) / 127.0) - 1.0) / alpha
