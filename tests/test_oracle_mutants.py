@@ -16,6 +16,15 @@ import oracle
 from . import test_oracle_pins as pins
 
 MUTANTS = [
+    ('k-bit decode range: page and head swapped',
+     '        int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);\n        int rc = oracle_decode_anchor_bits_block(ak + blk * code_blk, meta + blk * meta_blk, P, D,',
+     '        int64_t p = blk % NB, h = (blk / NB) % H, b = blk / (H * NB);\n        int rc = oracle_decode_anchor_bits_block(ak + blk * code_blk, meta + blk * meta_blk, P, D,'),
+    ('A.1 encode range: page and head swapped',
+     '        int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);\n        int rc = oracle_a1_encode_block(kv + ((b * L + p * P) * H + h) * D, (int64_t)H * D, P, D,',
+     '        int64_t p = blk % NB, h = (blk / NB) % H, b = blk / (H * NB);\n        int rc = oracle_a1_encode_block(kv + ((b * L + p * P) * H + h) * D, (int64_t)H * D, P, D,'),
+    ('A.1 decode range: page and head swapped',
+     '        int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);\n        int rc = oracle_a1_decode_block(anchor + blk * code_blk,',
+     '        int64_t p = blk % NB, h = (blk / NB) % H, b = blk / (H * NB);\n        int rc = oracle_a1_decode_block(anchor + blk * code_blk,'),
     ("range encode: page and head swapped",
      '        int64_t h = blk % H;\n        int64_t p = (blk / H) % NB;\n        int64_t b = blk / (H * NB);\n        const uint16_t *x',
      '        int64_t p = blk % NB;\n        int64_t h = (blk / NB) % H;\n        int64_t b = blk / (H * NB);\n        const uint16_t *x'),

@@ -343,6 +343,34 @@ def test_range_layout_is_batch_page_head(oracle_mod):
                 d1 = oracle_mod.decode_block(a1, r1, m1, C, ALPHA)
                 assert np.array_equal(dec[b, p * P:(p + 1) * P, h], d1), (b, p, h)
 
+
+def test_variant_range_layouts(oracle_mod):
+    """The k-bit Anchor decode and the A.1 codec over a [B][L][H][D] tensor
+    agree, block by block, with the same call on that block alone (a single
+    block has no batch, page or head index to get wrong)."""
+    B, NB, H, P, C, k = 2, 3, 2, 64, 16, 5
+    L = NB * P
+    rng = np.random.default_rng(13)
+    x = (rng.laplace(size=(B, L, H, 128)) *
+         rng.uniform(0.5, 4.0, size=(1, 1, H, 128))).astype(np.float32)
+    bits = oracle_mod.f32_to_bf16_bits(x).reshape(B, L, H, 128)
+    anc, res, meta = oracle_mod.encode(bits, P, C, ALPHA)
+    ak, _ = oracle_mod.split_bits(anc, res, k)
+    dk = oracle_mod.decode_anchor_bits(ak, meta, L, P, C, ALPHA, k)
+    a1 = oracle_mod.a1_encode(bits, P)
+    d1 = oracle_mod.a1_decode(*a1, L, P)
+    for b in range(B):
+        for p in range(NB):
+            for h in range(H):
+                blk = (slice(b, b + 1), slice(p, p + 1), slice(h, h + 1))
+                tok = (b, slice(p * P, (p + 1) * P), h)
+                one = oracle_mod.decode_anchor_bits(ak[blk], meta[blk], P, P, C, ALPHA, k)
+                assert np.array_equal(dk[tok], one[0, :, 0]), (b, p, h)
+                e1 = oracle_mod.a1_encode(bits[b:b + 1, p * P:(p + 1) * P, h:h + 1], P)
+                for full, part in zip(a1, e1):
+                    assert np.array_equal(full[blk], part), (b, p, h)
+                assert np.array_equal(d1[tok], oracle_mod.a1_decode(*e1, P, P)[0, :, 0]), (b, p, h)
+
 def _X(y, alpha=ALPHA):
     """Continuous inverse of Eq. 7 (for the half-code boundaries)."""
     return (np.power(1.0 + alpha, np.asarray(y, np.float64) / 127.0) - 1.0) / alpha
