@@ -16,6 +16,10 @@ import oracle
 from . import test_oracle_pins as pins
 
 MUTANTS = [
+    ("spec batch: p at stride T*V", 'k[b] = oracle_spec_verify(p + (int64_t)b * (T + 1) * V,',
+     'k[b] = oracle_spec_verify(p + (int64_t)b * T * V,'),
+    ("spec batch: every sequence seeded by r[0]", 's + (int64_t)b * T, u + (int64_t)b * T, r[b], T, V,',
+     's + (int64_t)b * T, u + (int64_t)b * T, r[0], T, V,'),
     ('k-bit decode range: page and head swapped',
      '        int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);\n        int rc = oracle_decode_anchor_bits_block(ak + blk * code_blk, meta + blk * meta_blk, P, D,',
      '        int64_t p = blk % NB, h = (blk / NB) % H, b = blk / (H * NB);\n        int rc = oracle_decode_anchor_bits_block(ak + blk * code_blk, meta + blk * meta_blk, P, D,'),

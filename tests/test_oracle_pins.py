@@ -621,6 +621,25 @@ def test_spec_output_follows_the_target_distribution(oracle_mod):
         assert np.all(np.abs(freq - pt) <= 5 * sigma + 1e-12), (freq, pt)
 
 
+
+def test_spec_batch_is_its_sequences(oracle_mod):
+    """A batch of sequences with their own p, q, drafts, uniforms and seeds
+    gives, sequence by sequence, what each gives alone (a batch of one has
+    no stride or seed to get wrong)."""
+    rng = np.random.default_rng(14)
+    N, T, V = 24, 3, 7
+    p = rng.dirichlet(np.ones(V), size=(N, T + 1)).astype(np.float32)
+    q = rng.dirichlet(np.ones(V), size=(N, T)).astype(np.float32)
+    s = rng.integers(0, V, size=(N, T)).astype(np.int32)
+    u = rng.random((N, T), dtype=np.float32)
+    r = rng.integers(0, 2 ** 32, size=N, dtype=np.uint64).astype(np.uint32)
+    k, tok = oracle_mod.spec_verify(p, q, s, u, r)
+    for b in range(N):
+        kb, tb = oracle_mod.spec_verify(p[b:b + 1], q[b:b + 1], s[b:b + 1], u[b:b + 1],
+                                        r[b:b + 1])
+        assert (k[b], tok[b]) == (kb[0], tb[0]), b
+    assert len(set(zip(k.tolist(), tok.tolist()))) > 1   # the sequences differ
+
 # ----------------------------------------------------------- size formulas
 
 def test_kv_size_example(oracle_mod):
