@@ -16,6 +16,10 @@ import oracle
 from . import test_oracle_pins as pins
 
 MUTANTS = [
+    ("INT-B minimum stored at row r, not 2r", '        meta[2 * r] = lo;',
+     '        meta[r] = lo;'),
+    ("INT-8 rows written at the 4-bit stride", '\n        uint8_t *cr = codes + r * (int64_t)(bits == 8 ? D : D / 2);',
+     '\n        uint8_t *cr = codes + r * (int64_t)(D / 2);'),
     ("spec batch: p at stride T*V", 'k[b] = oracle_spec_verify(p + (int64_t)b * (T + 1) * V,',
      'k[b] = oracle_spec_verify(p + (int64_t)b * T * V,'),
     ("spec batch: every sequence seeded by r[0]", 's + (int64_t)b * T, u + (int64_t)b * T, r[b], T, V,',
