@@ -64,6 +64,8 @@ def _bind(lib):
     lib.oracle_residual_nibble.restype = I
     lib.oracle_f32_to_bf16.argtypes = [F]
     lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_f32_to_bf16_array.argtypes = [P, P, I64]
+    lib.oracle_f32_to_bf16_array.restype = None
     lib.oracle_encode_block.argtypes = [P, I64, I, I, I, F, P, P, P]
     lib.oracle_encode_block.restype = I
     lib.oracle_encode_range.argtypes = [P, I64, I64, I, I, I, I, F, P, P, P,
@@ -192,11 +194,12 @@ def residual_nibble(c8: int) -> int:
 
 
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """Round-to-nearest-even float32 -> bf16 bit patterns (uint16)."""
+    """float32 -> bf16 bit patterns (uint16), round to nearest even, NaN kept
+    a NaN: the oracle's oracle_f32_to_bf16 applied elementwise."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    u = u + 0x7FFF + ((u >> 16) & 1)
-    return (u >> 16).astype(np.uint16)
+    out = np.empty(x.shape, np.uint16)
+    _load().oracle_f32_to_bf16_array(_ptr(x), _ptr(out), x.size)
+    return out
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:

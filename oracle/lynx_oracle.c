@@ -57,14 +57,28 @@ static float bf16_bits_to_f32(uint16_t h)
     return f;
 }
 
-/* Round-to-nearest-even float32 -> bfloat16 bit pattern (finite inputs). */
+/* float32 -> bfloat16 bit pattern, IEEE round to nearest, ties to even: the
+ * decoders' BF16 output and every attention operand are the float32
+ * reconstruction rounded this way.  Adding 0x7fff plus the lowest kept bit
+ * and dropping the low 16 bits rounds ties to the even neighbour; a carry out
+ * of the kept mantissa steps the exponent (past the largest finite bf16 it
+ * lands on infinity, as round to nearest does).  A NaN stays a NaN: it keeps
+ * its sign and top payload bits and is made quiet (the addition could carry
+ * its payload into the exponent and return an infinity or a zero). */
 uint16_t oracle_f32_to_bf16(float f)
 {
     uint32_t u;
     memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
     uint32_t lsb = (u >> 16) & 1u;
     u += 0x7fffu + lsb;
     return (uint16_t)(u >> 16);
+}
+
+void oracle_f32_to_bf16_array(const float *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_bf16(x[i]);
 }
 
 float oracle_bf16_to_f32(uint16_t h) { return bf16_bits_to_f32(h); }

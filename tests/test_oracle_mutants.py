@@ -113,6 +113,30 @@ MUTANTS = [
     ("A.1 Anchor point 16 Q_anc + 8", "qa * 16 + 7;", "qa * 16 + 8;"),
     ("A.1 chunk maximum of x instead of x'", "float a = fabsf(xp[i]);",
      "float a = fabsf(bf16_bits_to_f32(x[(int64_t)t * row_stride + d]));"),
+    ("bf16 rounds ties up", "    u += 0x7fffu + lsb;\n    return (uint16_t)(u >> 16);",
+     "    u += 0x8000u + 0u * lsb;\n    return (uint16_t)(u >> 16);"),
+    ("bf16 truncates", "    u += 0x7fffu + lsb;\n    return (uint16_t)(u >> 16);",
+     "    u += 0u * lsb;\n    return (uint16_t)(u >> 16);"),
+    ("bf16 tie parity from the dropped bit", "uint32_t lsb = (u >> 16) & 1u;",
+     "uint32_t lsb = (u >> 15) & 1u;"),
+    ("bf16 NaN not kept", "if ((u & 0x7fffffffu) > 0x7f800000u)\n        return",
+     "if (0)\n        return"),
+    ("Stage-1 eps 1e-3 in the encoder", "float rg = 1.0f / (gs + ORACLE_EPS);",
+     "float rg = 1.0f / (gs + 1e-3f);"),
+    ("Stage-2 eps 1e-3 in the encoder", "float rs = 1.0f / (sg + ORACLE_EPS);",
+     "float rs = 1.0f / (sg + 1e-3f);"),
+    ("Stage-2 eps 1e-5 in the encoder", "float rs = 1.0f / (sg + ORACLE_EPS);",
+     "float rs = 1.0f / (sg + 1e-5f);"),
+    ("decode Stage-2 eps 1e-3", "float nv = fmaf(xf, sg + ORACLE_EPS, mu);\n            float xv",
+     "float nv = fmaf(xf, sg + 1e-3f, mu);\n            float xv"),
+    ("decode Stage-1 eps 1e-3", "float xv = fmaf(nv, g_scale[d] + ORACLE_EPS, g_min[d]);",
+     "float xv = fmaf(nv, g_scale[d] + 1e-3f, g_min[d]);"),
+    ("A.1 chunk maximum + 1e-6 instead of the zero rule",
+     "float rmi = mi > 0.0f ? 1.0f / mi : 0.0f;", "float rmi = 1.0f / (mi + 1e-6f);"),
+    ("A.1 page maximum + 1e-6 instead of the zero rule",
+     "float rm = m > 0.0f ? 1.0f / m : 0.0f;", "float rm = 1.0f / (m + 1e-6f);"),
+    ("spec integer weights at 2^32", "(uint64_t)(w * 1099511627776.0f)",
+     "(uint64_t)(w * 4294967296.0f)"),
 ]
 
 # representative arguments for the parametrized pins

@@ -928,3 +928,195 @@ def test_a1_decode_error_bound_and_anchor_point(oracle_mod):
     full7 = oracle_mod.a1_decode(anc, r7, meta, P, P, alpha)
     anchor_only = oracle_mod.a1_decode(anc, None, meta, P, P, alpha)
     assert np.array_equal(full7.view(np.uint32), anchor_only.view(np.uint32))
+
+
+# ------------------------------------------ BF16 rounding of the reconstruction
+
+# (float32 bit pattern, bf16 bit pattern) worked out by hand for IEEE round to
+# nearest, ties to even.  A bf16 keeps the top 16 bits of the float32; the
+# dropped 16 bits decide the rounding: below 0x8000 down, above it up, at
+# exactly 0x8000 (a tie) towards the even kept pattern.
+BF16_HAND = [
+    (0x3F800000, 0x3F80),   # 1.0, exact
+    (0x3F808000, 0x3F80),   # 1 + 2^-8: tie between 1 and 1 + 2^-7, 0x3F80 is even
+    (0x3F818000, 0x3F82),   # 1 + 3*2^-8: tie between 0x3F81 (odd) and 0x3F82 (even)
+    (0x3F808001, 0x3F81),   # one float ulp above a tie: up
+    (0x3F807FFF, 0x3F80),   # one float ulp below a tie: down
+    (0x3F817FFF, 0x3F81),   # below the tie that would round an odd pattern up
+    (0x3FFF8000, 0x4000),   # tie from odd 0x3FFF: the carry steps the exponent, 2.0
+    (0xBF818000, 0xBF82),   # negatives round by magnitude
+    (0xBF808000, 0xBF80),
+    (0x00000000, 0x0000),   # +0
+    (0x80000000, 0x8000),   # -0 keeps its sign
+    (0x00018000, 0x0002),   # subnormal tie from odd: up
+    (0x00008000, 0x0000),   # subnormal tie from even (zero): down
+    (0x7F7F7FFF, 0x7F7F),   # just below the tie above the largest finite bf16
+    (0x7F7F8000, 0x7F80),   # that tie (0x7F7F odd) rounds up to +infinity
+    (0xFF7FFFFF, 0xFF80),   # -FLT_MAX rounds to -infinity
+    (0x7F800000, 0x7F80),   # infinities are exact
+    (0xFF800000, 0xFF80),
+]
+
+
+def test_bf16_rounding_hand_values(oracle_mod):
+    """The rounding that defines the decoders' BF16 output and every attention
+    operand (the float32 reconstruction rounded to nearest even) on ties,
+    near-ties, a carry into the exponent, signed zeros, subnormals and the
+    overflow to infinity."""
+    src = np.array([s for s, _ in BF16_HAND], np.uint32).view(np.float32)
+    got = oracle_mod.f32_to_bf16_bits(src)
+    assert got.tolist() == [d for _, d in BF16_HAND]
+
+
+def test_bf16_rounding_keeps_nan(oracle_mod):
+    """A NaN stays a NaN (all-ones exponent, non-zero mantissa) with its sign,
+    for quiet and signalling payloads; none turns into an infinity or a zero."""
+    src = np.array([0x7FC00000, 0x7F800001, 0x7FFFFFFF, 0xFFFFFFFF, 0xFF800001],
+                   np.uint32).view(np.float32)
+    got = oracle_mod.f32_to_bf16_bits(src).astype(np.uint32)
+    assert ((got & 0x7F80) == 0x7F80).all() and ((got & 0x007F) != 0).all(), got
+    assert (got >> 15).tolist() == [0, 0, 0, 1, 1]
+
+
+def test_bf16_rounding_matches_the_ieee_bound(oracle_mod):
+    """On random finite float32 values, each result is one of the two bf16
+    neighbours and lies within half a bf16 ulp (a float64 check of the
+    round-to-nearest bound)."""
+    rng = np.random.default_rng(11)
+    u = rng.integers(0, 0x7F7F0000, size=20000, dtype=np.uint32)
+    u |= (rng.integers(0, 2, size=u.size, dtype=np.uint32) << 31)
+    x = u.view(np.float32)
+    h = oracle_mod.f32_to_bf16_bits(x)
+    y = oracle_mod.bf16_bits_to_f32(h).astype(np.float64)
+    down = (u & 0xFFFF0000).view(np.float32).astype(np.float64)
+    up = ((u & 0xFFFF0000) + 0x10000).view(np.float32).astype(np.float64)
+    xd = x.astype(np.float64)
+    assert ((y == down) | (y == up)).all()
+    assert (np.abs(y - xd) <= np.abs(up - down) / 2).all()
+
+
+# ------------------------------------------------------------- the epsilons
+
+def _eps_block():
+    """P = 64, C = 32, D = 8, built so that both epsilons of Stages 1-2 (1e-6,
+    the reading where the pages leave it open) move codes and metadata.
+    Channel 0: token 0 = 2^20, tokens 1..31 = 0; chunk 1 alternates 0 (even
+      t) and 1 (odd t).  gamma_scale = 2^20, and 2^20 + 1e-6 rounds to 2^20
+      in float32, so n = x 2^-20: chunk 1 holds {0, 2^-20}, mu = 2^-21 and
+      d = -+2^-21 exactly, sigma = 2^-21.  Then |X_final| = 2^-21 /
+      (2^-21 + 1e-6) = 0.32288 and Y = 127 ln(1 + 255 * 0.32288) / ln 256 =
+      101.296: I = 101 (sigma + eps = 1e-3 would give I = 3, eps = 2e-6
+      I = 90, eps = 1e-7 I = 123).  Chunk 0: mu = 1/32, sigma = 31/32, the
+      spike has |X_final| = 0.999999 (I = 127) and the zeros 1/31
+      (Y = 50.89, I = 51).
+    Channel 1: alternating 0 and 2^-20 over the whole page.  gamma_scale =
+      2^-20 is comparable to eps: n = 2^-20 / (2^-20 + 1e-6) = 0.488144 on the
+      non-zeros, so mu = 0.244072 in both chunks (eps = 0 would store 0.5).
+      Both signs then sit at +-sigma: I = 127 everywhere.
+    Channels 2..7 are zero."""
+    P = 64
+    x = np.zeros((P, 8), np.float32)
+    x[0, 0] = 2.0 ** 20
+    x[33:64:2, 0] = 1.0
+    x[1::2, 1] = 2.0 ** -20
+    return _bf16_bits(x.ravel()).reshape(P, 8), x
+
+
+def test_epsilons_hand_block(oracle_mod):
+    bits, _ = _eps_block()
+    anc, res, meta = oracle_mod.encode_block(bits, C=32, alpha=ALPHA)
+    Q = _signed_codes(anc, res).astype(int)
+    # channel 0: signed codes Q8 = I (S = +1) or -I - 1 (S = -1)
+    assert Q[0, 0] == 127 and (Q[1:32, 0] == -52).all()
+    assert (Q[32:64:2, 0] == -102).all() and (Q[33:64:2, 0] == 101).all()
+    # channel 1: every value at +-sigma of its chunk
+    assert (Q[0::2, 1] == -128).all() and (Q[1::2, 1] == 127).all()
+    assert (Q[:, 2:] == 0).all()
+    # metadata rows: gamma_min, gamma_scale, mu[2], sigma[2]
+    assert meta[1, 0] == 2.0 ** 20 and meta[1, 1] == 2.0 ** -20
+    assert meta[2, 0] == 1 / 32 and meta[3, 0] == 2.0 ** -21
+    assert meta[5, 0] == 2.0 ** -21
+    mu1 = 0.5 * 2.0 ** -20 / (2.0 ** -20 + 1e-6)
+    assert abs(meta[2, 1] - mu1) < 1e-6 * mu1 and abs(meta[3, 1] - mu1) < 1e-6 * mu1
+
+
+def test_epsilons_round_trip(oracle_mod):
+    """Encode and decode agree on both epsilons: the full decode of the hand
+    block lies within half a code step of every value, the step taken from
+    the closed form X(I) = ((1 + alpha)^(I/127) - 1) / alpha scaled by
+    (sigma + 1e-6)(gamma_scale + 1e-6) from the hand derivation (at I = 101
+    in channel 0's chunk 1 that is 0.0071 * 1.4768e-6 * 2^20 = 0.011).  A
+    decoder with another epsilon lands orders of magnitude away (sigma + 1e-3
+    instead of 2^-21 + 1e-6 scales the spread by 680)."""
+    bits, x = _eps_block()
+    anc, res, meta = oracle_mod.encode_block(bits, C=32, alpha=ALPHA)
+    y = oracle_mod.decode_block(anc, res, meta, C=32, alpha=ALPHA).astype(np.float64)
+    I = np.abs(_signed_codes(anc, res).astype(np.float64) + 0.5) - 0.5
+
+    def X(v):
+        return ((1 + ALPHA) ** (np.clip(v, 0, 127) / 127.0) - 1) / ALPHA
+
+    half = np.maximum(X(I + 0.5) - X(I), X(I) - X(I - 0.5))
+    # (sigma + eps)(gamma_scale + eps) per token, from the hand derivation
+    scale = np.zeros((64, 8))
+    scale[:32, 0] = (31 / 32 + 1e-6) * 2.0 ** 20
+    scale[32:, 0] = (2.0 ** -21 + 1e-6) * 2.0 ** 20
+    mu1 = 0.5 * 2.0 ** -20 / (2.0 ** -20 + 1e-6)
+    scale[:, 1] = (mu1 + 1e-6) * (2.0 ** -20 + 1e-6)
+    err = np.abs(y - x.astype(np.float64))
+    assert (err <= half * scale * 1.001 + 1e-12).all(), err.max(0)
+    assert abs(y[33, 0] - 1.0) < 0.011 and abs(y[1, 1] - 2.0 ** -20) < 1e-2 * 2.0 ** -20
+    assert (y[:, 2:] == 0).all()
+
+
+# ------------------------------------------------ Appendix A.1 zero maxima
+
+def test_a1_zero_and_tiny_maxima(oracle_mod):
+    """Appendix A.1 with maxima of 0 and maxima far below 1e-6 (P = 64, chunks
+    of 16; reading: a zero maximum gives a zero reciprocal, any other maximum
+    its exact reciprocal, nothing added).
+    Channel 0: token 0 = 2^20 (the page maximum m), chunk 1 alternates +1 and
+      -1, chunks 2-3 are zero.  rm = 2^-20 exactly, so chunk 1 has
+      x' = +-2^-20 and m_1 = 2^-20, x'' = +-1: Q = +-127 (Anchor 7 / -8,
+      Residual 15 / 1).  Chunks 2-3: m_i = 0 and Q = 0.
+    Channel 1: token 0 = 2^-24 (the page maximum), the rest 0: rm = 2^24,
+      x' = 1 at token 0, so m_0 = 1 exactly.
+    Decode: chunk 1 is X(127) * 2^-20 * 2^20 = +-1 exactly, the zero chunks
+    +0."""
+    P = 64
+    x = np.zeros((P, 128), np.float32)
+    x[0, 0] = 2.0 ** 20
+    x[16:32, 0] = np.where(np.arange(16) % 2 == 0, 1.0, -1.0)
+    x[0, 1] = 2.0 ** -24
+    bits = _bf16_bits(x.ravel()).reshape(1, P, 1, 128)
+    anc, res, meta = oracle_mod.a1_encode(bits, P)
+    Q = _a1_codes(anc, res).astype(int)
+    m = meta[0, 0, 0]
+    assert m[0, 0] == 2.0 ** 20 and m[1, 0] == 1.0 and m[2, 0] == 2.0 ** -20
+    assert m[3, 0] == 0.0 and m[4, 0] == 0.0 and not np.signbit(m[3:, 0]).any()
+    assert m[0, 1] == 2.0 ** -24 and m[1, 1] == 1.0
+    assert Q[0, 0] == 127 and (Q[1:16, 0] == 0).all()
+    assert Q[16:32, 0].tolist() == [127, -127] * 8
+    assert (Q[32:, 0] == 0).all() and Q[0, 1] == 127 and (Q[1:, 1] == 0).all()
+    y = oracle_mod.a1_decode(anc, res, meta, P, P)[0, :, 0, :]
+    assert y[16:32, 0].tolist() == [1.0, -1.0] * 8
+    assert (y[32:, 0] == 0).all() and not np.signbit(y[32:, 0]).any()
+    assert y[0, 1] == 2.0 ** -24
+
+
+# ------------------------------------------- Eq. 10-11 weights below 2^-32
+
+def test_spec_tiny_weights_keep_their_share(oracle_mod):
+    """The inverse CDF keeps weights down to 2^-40 (reading: integer weights
+    floor(w 2^40)).  Both drafts accepted, next distribution
+    (2^-36, 2^-36, 2^-35): integer weights 16, 16, 32, Z = 64, target
+    floor(r 64 / 2^32).  r = 0, 2^30, 2^31, 3 2^30 give targets 0, 16, 32, 48:
+    tokens 0, 1, 2, 2.  (At 2^32 every weight would floor to 0: no token.)
+    A weight below 2^-40 floors to 0 and is never drawn."""
+    same = [0.5, 0.25, 0.25]
+    tiny = [2.0 ** -36, 2.0 ** -36, 2.0 ** -35]
+    got = [_one(oracle_mod, [same, tiny], [same], [0], [0.0], r)
+           for r in (0, 1 << 30, 1 << 31, 3 << 30)]
+    assert got == [(1, 0), (1, 1), (1, 2), (1, 2)]
+    below = [2.0 ** -41, 2.0 ** -36, 0.0]
+    assert _one(oracle_mod, [same, below], [same], [0], [0.0], 0) == (1, 1)
