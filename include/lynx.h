@@ -36,9 +36,12 @@
  *     nibble and channel 8G+k+4 in its high nibble.  Anchor<<4 | Residual is
  *     the 8-bit two's-complement code Q8 = I*S + min(S, 0) of Eq. 9, I the
  *     7-bit magnitude code and S the sign.
- *   - Limits: D == 128; page in {64, 128, 256}; C in {16, 32, 64, 128},
- *     C <= page; L % page == 0; B * L < 2^31; alpha finite and > 0; every
- *     pointer 16-byte aligned.
+ *   - Limits: D == 128; page in {64, 128, 256, 512} for the codec (encode,
+ *     both decoders, the k-bit Anchor decode; the page sizes of the pages'
+ *     ablation grid, [Review], "Concrete Improvement Suggestions", item 4),
+ *     page <= 256 for attention and the Appendix A.1 variant; C in
+ *     {16, 32, 64, 128}, C <= page; L % page == 0; B * L < 2^31; alpha
+ *     finite and > 0; every pointer 16-byte aligned.
  */
 #ifndef LYNX_H
 #define LYNX_H
@@ -425,9 +428,12 @@ int lynx_attn_decode_paged(const void *q, int batch, int T, int H_q,
  * process exits); sizes that need more than that (lynx_attn_workspace_bytes
  * > 8 MiB) fail with LYNX_EWORKSPACE.  The paper has no counterpart: this is
  * an interface of this library only.
- * The first call on a device looks the array's address up once (with that
- * device current) and caches it; make that first call before any stream
- * capture.  Nothing is allocated or freed.  All calls share the one array
+ * The first call on a device looks the array's address up (with that device
+ * current; this also loads the library's device image, which places the
+ * array) and caches it per device; a call that finds a different current
+ * context than the cached address belongs to (after cudaDeviceReset) looks it
+ * up again.  Make the first call on each device, and the first after a reset,
+ * before any stream capture.  Nothing else is allocated or freed.  All calls share the one array
  * and it keeps the last call's contents (no state needs clearing: every
  * partial is written before it is read), so calls whose work overlaps on the
  * GPU race with each other: issue them on one stream, or order them.

@@ -3,12 +3,14 @@
 // Anchor Phase "Q_approx = dequant(Q_anc, gamma, mu, sigma)" and Residual
 // Phase "Q_full = dequant(Q_anc + Q_res)"; Worked Example Eq. 14-15).
 //
-// One persistent kernel per (mode, output type).  A CTA walks page blocks;
-// the block's anchor codes, residual codes and metadata rows (contiguous in
-// HBM) arrive in shared memory by bulk asynchronous copies, one stage ahead
-// of the block being decoded.  Thread (slot, g) of 256 decodes a run of
-// page/16 consecutive tokens (always inside one chunk) for channels
-// 8g..8g+7, so it reads its chunk's constants once per block.
+// One persistent kernel per (mode, output type).  A CTA walks units of up to
+// 256 tokens: a whole page block, or one half of a 512-token page.  The
+// unit's anchor codes, residual codes and metadata rows (contiguous in HBM;
+// for a half page, the gamma rows and the mu and sigma rows of its chunks)
+// arrive in shared memory by bulk asynchronous copies, one stage ahead of
+// the unit being decoded.  Thread (slot, g) of 256 decodes a run of unit/16
+// consecutive tokens (always inside one chunk) for channels 8g..8g+7, so it
+// reads its chunk's constants once per unit.
 //
 // Reconstruction of one element (identical in both modes once v is known):
 //   v = S * X(I), X(I) = ((1+alpha)^(I/127) - 1)/alpha rounded to float32,
@@ -28,6 +30,7 @@
 namespace lynx {
 
 constexpr int kDecThreads = 256;
+constexpr int kDecUnit = 256;   // most tokens of a decode unit
 constexpr int kDecStages = 2;
 constexpr int kDecLut = 65536;
 // Shared-window address of the first byte of dynamic shared memory for a
@@ -94,14 +97,17 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31;
   const int g = tid & 15, slot = tid >> 4;
-  const int NC = P / C;
-  const int meta_rows = 2 + 2 * NC;
-  const uint32_t code_bytes = (uint32_t)P * (kD / 2);          // one stream of a block
-  const uint32_t meta_bytes = (uint32_t)meta_rows * kD * 4;
+  const int U = P < kDecUnit ? P : kDecUnit;   // tokens of a unit
+  const int parts = P / U;                     // units of a page block
+  const int64_t nunit = nblk * parts;
+  const int NC = U / C;                        // chunks of a unit
+  const int blk_meta_rows = 2 + 2 * (P / C);
+  const uint32_t code_bytes = (uint32_t)U * (kD / 2);          // one stream of a unit
+  const uint32_t meta_bytes = (uint32_t)(2 + 2 * NC) * kD * 4;
   const uint32_t stage_bytes = code_bytes * (FULL ? 2 : 1) + meta_bytes;
   uint8_t* stages = smem + kDecLut;
   uint64_t* bars = reinterpret_cast<uint64_t*>(stages + kDecStages * stage_bytes);
-  const int run = P >> 4;                 // tokens per thread per block (4, 8 or 16)
+  const int run = U >> 4;                 // tokens per thread per unit (4, 8 or 16)
   const int t0 = slot * run;
   const int chunk = t0 / C;
   const int64_t ostride = (int64_t)H * kD;
@@ -110,11 +116,12 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
     float x[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) x[i] = __int_as_float(0x7fc00000);
-    for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    for (int64_t un = blockIdx.x; un < nunit; un += gridDim.x) {
+      const int64_t blk = un / parts, part = un % parts;
       const int64_t h = blk % H, rest = blk / H;
       const int64_t p = rest % NB, b = rest / NB;
       for (int r = 0; r < run; ++r)
-        store8<BF16OUT>(out, ((b * L + p * P + t0 + r) * H + h) * kD + 8 * g, x);
+        store8<BF16OUT>(out, ((b * L + p * P + part * U + t0 + r) * H + h) * kD + 8 * g, x);
     }
     return;
   }
@@ -138,23 +145,33 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
   __syncthreads();
   const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 8u;
 
-  auto issue = [&](int64_t lblk, int stage) {
-    const int64_t blk = phys_block(bt, nphys, lblk, H, &g_dec_wait_timeout);
+  auto issue = [&](int64_t un, int stage) {
+    const int64_t part = un % parts;
+    const int64_t blk = phys_block(bt, nphys, un / parts, H, &g_dec_wait_timeout);
     uint8_t* st = stages + stage * stage_bytes;
+    const int64_t code_off = (blk * parts + part) * code_bytes;
     mbar_expect_tx(&bars[stage], stage_bytes);
-    bulk_load(st, anchor + blk * code_bytes, code_bytes, &bars[stage]);
-    if constexpr (FULL) bulk_load(st + code_bytes, residual + blk * code_bytes, code_bytes, &bars[stage]);
-    bulk_load(st + code_bytes * (FULL ? 2 : 1), meta + blk * (int64_t)meta_rows * kD, meta_bytes,
-              &bars[stage]);
+    bulk_load(st, anchor + code_off, code_bytes, &bars[stage]);
+    if constexpr (FULL) bulk_load(st + code_bytes, residual + code_off, code_bytes, &bars[stage]);
+    uint8_t* sm = st + code_bytes * (FULL ? 2 : 1);
+    const float* mb = meta + blk * (int64_t)blk_meta_rows * kD;
+    if (parts == 1) {
+      bulk_load(sm, mb, meta_bytes, &bars[stage]);
+    } else {  // gamma rows, then the unit's mu rows and sigma rows
+      const uint32_t rows = (uint32_t)NC * kD * 4;
+      bulk_load(sm, mb, 2 * kD * 4, &bars[stage]);
+      bulk_load(sm + 2 * kD * 4, mb + (2 + part * NC) * kD, rows, &bars[stage]);
+      bulk_load(sm + 2 * kD * 4 + rows, mb + (2 + P / C + part * NC) * kD, rows, &bars[stage]);
+    }
   };
   if (tid == 0)
     for (int i = 0; i < kDecStages; ++i) {
-      const int64_t blk = blockIdx.x + (int64_t)i * gridDim.x;
-      if (blk < nblk) issue(blk, i);
+      const int64_t un = blockIdx.x + (int64_t)i * gridDim.x;
+      if (un < nunit) issue(un, i);
     }
 
   int it = 0;
-  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+  for (int64_t un = blockIdx.x; un < nunit; un += gridDim.x, ++it) {
     const int stage = it % kDecStages;
     const uint32_t phase = (uint32_t)(it / kDecStages) & 1u;
     const bool ok = mbar_wait(&bars[stage], phase);
@@ -170,9 +187,10 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
     const float4 mu_b = *reinterpret_cast<const float4*>(mrow + (2 + chunk) * kD + 4);
     const float4 sg_a = *reinterpret_cast<const float4*>(mrow + (2 + NC + chunk) * kD);
     const float4 sg_b = *reinterpret_cast<const float4*>(mrow + (2 + NC + chunk) * kD + 4);
+    const int64_t blk = un / parts, part = un % parts;
     const int64_t h = blk % H, rest = blk / H;
     const int64_t p = rest % NB, b = rest / NB;
-    const int64_t orow0 = ((b * L + p * P + t0) * H + h) * kD + 8 * g;
+    const int64_t orow0 = ((b * L + p * P + part * U + t0) * H + h) * kD + 8 * g;
 
     if constexpr (FULL) {
       // pairs (k, k+1) in channel order
@@ -243,10 +261,10 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
       }
       return;
     }
-    // every thread is done with this stage: refill it kDecStages blocks ahead
+    // every thread is done with this stage: refill it kDecStages units ahead
     if (tid == 0) {
-      const int64_t nxt = blk + (int64_t)kDecStages * gridDim.x;
-      if (nxt < nblk) {
+      const int64_t nxt = un + (int64_t)kDecStages * gridDim.x;
+      if (nxt < nunit) {
         fence_proxy_async();
         issue(nxt, stage);
       }
@@ -259,8 +277,8 @@ static cudaError_t run_decode(const void* anchor, const void* residual, const fl
                               const Shape& s, const ExpandTable& tab, void* out,
                               cudaStream_t stream, const Paging& pg) {
   auto fn = decode_kernel<FULL, BF16OUT>;
-  const size_t stage = (size_t)s.page * (kD / 2) * (FULL ? 2 : 1) +
-                       (size_t)(2 + 2 * (s.page / s.C)) * kD * 4;
+  const int U = s.page < kDecUnit ? s.page : kDecUnit;
+  const size_t stage = (size_t)U * (kD / 2) * (FULL ? 2 : 1) + (size_t)(2 + 2 * (U / s.C)) * kD * 4;
   const size_t smem = kDecLut + kDecStages * stage + kDecStages * 8;
   constexpr size_t kMaxSmem = kDecLut + kDecStages * (256 * 64 * 2 + 34 * kD * 4) + 64;
   static thread_local int configured_dev = -1;
@@ -290,7 +308,7 @@ static cudaError_t run_decode(const void* anchor, const void* residual, const fl
   }
   const int64_t nblk = s.blocks();
   int64_t grid = (int64_t)sm_count() * per_sm;
-  if (grid > nblk) grid = nblk;
+  if (grid > nblk * (s.page / U)) grid = nblk * (s.page / U);
   fn<<<(unsigned)grid, kDecThreads, smem, stream>>>(
       static_cast<const uint8_t*>(anchor), static_cast<const uint8_t*>(residual), meta, nblk,
       s.NB(), s.H, s.L, s.page, s.C, out, pg.table, pg.nphys, tab);

@@ -72,108 +72,182 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return r;
 }
 
+// Channel width of a work unit.  The statistics are per channel, so a page
+// block splits into independent ranges of W channels.  A warp covers C
+// tokens x 2048/C channels (TL = C/8 token lanes x 8 registers, CG = 256/C
+// groups of 8 channels), so W >= 2048/C; below that bound W is chosen so that
+// a tile (P x W BF16) is 32 KiB where possible: three stages of it and the
+// statistics of two CTAs fit one SM.
+template <int P, int C>
+constexpr int enc_width() {
+  constexpr int lo = 2048 / C;
+  constexpr int want = P <= 128 ? 128 : 16384 / P;
+  return lo > want ? (lo > 128 ? 128 : lo) : want;
+}
+
 template <int P, int C>
 struct EncGeom {
-  static constexpr int kThreads = 2 * P;
-  static constexpr int kWarps = P / 16;
+  static constexpr int kW = enc_width<P, C>();
+  static constexpr int kUnits = kD / kW;        // work units per page block
   static constexpr int kNC = P / C;
-  static constexpr int kTL = C / 8;         // token lanes
-  static constexpr int kCG = 256 / C;       // channel groups of 8 per warp
-  static constexpr int kSlices = C / 16;    // warps per chunk
-  static constexpr int kTileBytes = P * kD * 2;
-  static constexpr int kStages = kTileBytes <= 32768 ? 3 : 2;
+  static constexpr int kTL = C / 8;             // token lanes
+  static constexpr int kCG = 256 / C;           // channel groups of 8 per warp
+  static constexpr int kSlices = P * kW / 2048; // (chunk, channel range) slices of a unit
+  static constexpr int kSlicesPerChunk = kW * C / 2048;
+  static constexpr int kWarps = kSlices < 8 ? kSlices : 8;
+  static constexpr int kSlicesPerWarp = kSlices / kWarps;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kRowBytes = kW * 2;
+  static constexpr int kTileBytes = P * kRowBytes;
+  static constexpr int kStages = kTileBytes <= 32768 ? 3 : kTileBytes <= 65536 ? 2 : 1;
+  // 128-byte tile rows are loaded with the TMA's 128-byte swizzle (16-byte
+  // chunk j of row r lands at chunk j ^ (r & 7)), so that the token lanes of
+  // a quarter-warp, which read the same chunks of different rows, hit
+  // different banks.
+  static constexpr bool kSwizzle = kRowBytes == 128;
   static constexpr int kMetaRows = 2 + 2 * kNC;
-  // per-chunk min/max partials (2 x kNC x 128), double-buffered by block
-  // parity: a warp may still read one block's partials while a faster warp
-  // writes the next block's.
-  static constexpr int kRedFloats = 2 * 2 * kNC * kD;
+  // per-chunk min/max partials (2 x kNC x kW), double-buffered by block parity
+  // when the next tile is in flight (a warp may still read one block's
+  // partials while a faster warp writes the next block's)
+  static constexpr int kRedSets = kStages > 1 ? 2 : 1;
+  static constexpr int kRedFloats = kRedSets * 2 * kNC * kW;
   // page-statistic channels each token lane computes (of its group's 8)
   static constexpr int kCPL = kTL >= 8 ? 1 : 8 / kTL;
   static constexpr size_t kSmem =
       (size_t)kStages * kTileBytes + (size_t)kRedFloats * 4 + kStages * 8;
   static_assert(C >= 16 && C <= P, "chunk");
-  static_assert(P >= 64 && P <= 256, "page");
+  static_assert(P >= 64 && P <= 512, "page");
+  static_assert(kSlices % kWarps == 0 && kW * C % 2048 == 0, "slices");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
+// Token lane of lane slot k (lane / CG).  With swizzled tiles the 8 lanes of
+// a quarter-warp hold 8/CG token lanes whose rows must differ in the row bits
+// that select the swizzle, not in the low ones: slot k = (8/CG) q + j takes
+// token lane CG j + (q mod CG) + 8 (q div CG).  Otherwise the identity.
+template <int TL, int CG, bool SW>
+__device__ __forceinline__ constexpr int enc_tl(int k) {
+  if constexpr (!SW || TL < 8) {
+    return k;
+  } else {
+    constexpr int nq = 8 / CG;
+    const int q = k / nq, j = k % nq;
+    return CG * j + q % CG + 8 * (q / CG);
+  }
+}
+// Lane-slot xor that moves token lane tl to tl ^ hh (hh a power of two).
+// The permutation above only reorders the bits of k, so this is the slot
+// that holds token lane hh.
+template <int TL, int CG, bool SW>
+__device__ __forceinline__ constexpr int enc_kxor(int hh) {
+  int k = 0;
+  for (int b = 0; b < TL; ++b)
+    if (enc_tl<TL, CG, SW>(b) == hh) k = b;
+  return k;
+}
+
 template <int P, int C>
-__global__ void __launch_bounds__(2 * P, 256 / P)
-encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
+__global__ void __launch_bounds__(EncGeom<P, C>::kThreads, (EncGeom<P, C>::kThreads <= 256 ? 2 : 1))
+encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
               const int64_t NB, const int H, const int64_t L,
               uint32_t* __restrict__ anchor, uint32_t* __restrict__ residual,
               float* __restrict__ meta, const int32_t* __restrict__ bt, const int64_t nphys,
               const __grid_constant__ CompanderTable tab) {
   using G = EncGeom<P, C>;
+  constexpr int W = G::kW;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   float* red_mn = reinterpret_cast<float*>(smem + G::kStages * G::kTileBytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(red_mn + G::kRedFloats);
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
-  const int cg = lane % G::kCG, tl = lane / G::kCG;
-  const int c = w / G::kSlices;                      // chunk of the warp
-  const int g = (w % G::kSlices) * G::kCG + cg;      // channel group (8 channels)
+  const int cg = lane % G::kCG, kl = lane / G::kCG;     // lane slot of the token lanes
+  const int tl = enc_tl<G::kTL, G::kCG, G::kSwizzle>(kl);  // token offset in the chunk
 
+  if (G::kSwizzle && (smem_u32(tiles) & 1023u) != 0u) {
+    // the swizzled reads assume 1024-byte aligned tiles; the host checks the
+    // reserved shared memory before launching, so this is never taken
+    if (tid == 0) atomicOr(&g_wait_timeout, kFlagWaitTimeout);
+    return;
+  }
   if (tid == 0) {
     for (int i = 0; i < G::kStages; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
   }
   __syncthreads();
 
-  auto issue = [&](int64_t blk, int stage) {
+  auto issue = [&](int64_t u, int stage) {
+    const int64_t blk = u / G::kUnits, half = u % G::kUnits;
     const int64_t h = blk % H, rest = blk / H;
     const int64_t p = rest % NB, b = rest / NB;
     mbar_expect_tx(&bars[stage], G::kTileBytes);
-    tma_load_2d(tiles + stage * G::kTileBytes, &tmap, (int32_t)(h * kD),
-                (int32_t)(b * L + p * P), &bars[stage]);
+#pragma unroll
+    for (int r0 = 0; r0 < P; r0 += 256)   // a box is at most 256 rows
+      tma_load_2d(tiles + stage * G::kTileBytes + r0 * G::kRowBytes, &tmap,
+                  (int32_t)(h * kD + half * W), (int32_t)(b * L + p * P + r0), &bars[stage]);
   };
   if (tid == 0)
     for (int i = 0; i < G::kStages; ++i) {
-      const int64_t blk = blockIdx.x + (int64_t)i * gridDim.x;
-      if (blk < nblk) issue(blk, i);
+      const int64_t u = blockIdx.x + (int64_t)i * gridDim.x;
+      if (u < nunit) issue(u, i);
     }
+
+  // 16-byte chunk g of tile row t
+  auto tile_at = [&](const uint4* tile, int t, int g) -> uint4 {
+    if constexpr (G::kSwizzle) return tile[t * 8 + (g ^ (t & 7))];
+    else return tile[t * (W / 8) + g];
+  };
 
   const f2 alpha2 = make_float2(tab.alpha, tab.alpha), c16_2 = make_float2(tab.c16, tab.c16);
   const float inv_C = 1.0f / (float)C;
   int it = 0;
-  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+  for (int64_t u = blockIdx.x; u < nunit; u += gridDim.x, ++it) {
     const int stage = it % G::kStages;
     const uint32_t phase = (uint32_t)(it / G::kStages) & 1u;
     const bool ok = mbar_wait(&bars[stage], phase);
     const uint4* tile = reinterpret_cast<const uint4*>(tiles + stage * G::kTileBytes);
+    const int64_t blk = u / G::kUnits;
+    const int wofs = (int)(u % G::kUnits) * (W / 8);   // first channel group of the unit
 
-    // ---- Stage 1a: per-channel page min / max (exact, on bf16 pairs)
-    float* pmn = red_mn + (it & 1) * (2 * G::kNC * kD);   // [kNC][128]
-    float* pmx = pmn + G::kNC * kD;                        // [kNC][128]
-    uint32_t mn[4], mx[4];
+    // ---- Stage 1a: per-chunk min / max of each channel (exact, on bf16
+    // pairs) for every slice of the warp, into the partials
+    float* pmn = red_mn + (G::kRedSets > 1 ? (it & 1) : 0) * (2 * G::kNC * W);  // [kNC][W]
+    float* pmx = pmn + G::kNC * W;                                              // [kNC][W]
+#pragma unroll 1
+    for (int sl = 0; sl < G::kSlicesPerWarp; ++sl) {
+      const int slice = w + G::kWarps * sl;
+      const int c = slice / G::kSlicesPerChunk;
+      const int g = (slice % G::kSlicesPerChunk) * G::kCG + cg;   // group within the unit
+      uint32_t mn[4], mx[4];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int t = c * C + G::kTL * m + tl;
-      const uint4 v = tile[t * 16 + g];
-      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+      for (int m = 0; m < 8; ++m) {
+        const uint4 v = tile_at(tile, c * C + G::kTL * m + tl, g);
+        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        mn[k] = m == 0 ? vv[k] : bf2_min(mn[k], vv[k]);
-        mx[k] = m == 0 ? vv[k] : bf2_max(mx[k], vv[k]);
+        for (int k = 0; k < 4; ++k) {
+          mn[k] = m == 0 ? vv[k] : bf2_min(mn[k], vv[k]);
+          mx[k] = m == 0 ? vv[k] : bf2_max(mx[k], vv[k]);
+        }
       }
-    }
 #pragma unroll
-    for (int x = G::kCG; x < 32; x <<= 1)
+      for (int x = G::kCG; x < 32; x <<= 1)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        mn[k] = bf2_min(mn[k], __shfl_xor_sync(kFull, mn[k], x));
-        mx[k] = bf2_max(mx[k], __shfl_xor_sync(kFull, mx[k], x));
+        for (int k = 0; k < 4; ++k) {
+          mn[k] = bf2_min(mn[k], __shfl_xor_sync(kFull, mn[k], x));
+          mx[k] = bf2_max(mx[k], __shfl_xor_sync(kFull, mx[k], x));
+        }
+      if (kl == 0) {
+        float4* pm = reinterpret_cast<float4*>(pmn + c * W + 8 * g);
+        float4* px = reinterpret_cast<float4*>(pmx + c * W + 8 * g);
+        const f2 a0 = bf2_to_f2(mn[0]), a1 = bf2_to_f2(mn[1]);
+        const f2 a2 = bf2_to_f2(mn[2]), a3 = bf2_to_f2(mn[3]);
+        pm[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
+        pm[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
+        const f2 b0 = bf2_to_f2(mx[0]), b1 = bf2_to_f2(mx[1]);
+        const f2 b2 = bf2_to_f2(mx[2]), b3 = bf2_to_f2(mx[3]);
+        px[0] = make_float4(b0.x, b0.y, b1.x, b1.y);
+        px[1] = make_float4(b2.x, b2.y, b3.x, b3.y);
       }
-    if (tl == 0) {
-      float4* pm = reinterpret_cast<float4*>(pmn + c * kD + 8 * g);
-      float4* px = reinterpret_cast<float4*>(pmx + c * kD + 8 * g);
-      const f2 a0 = bf2_to_f2(mn[0]), a1 = bf2_to_f2(mn[1]);
-      const f2 a2 = bf2_to_f2(mn[2]), a3 = bf2_to_f2(mn[3]);
-      pm[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
-      pm[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
-      const f2 b0 = bf2_to_f2(mx[0]), b1 = bf2_to_f2(mx[1]);
-      const f2 b2 = bf2_to_f2(mx[2]), b3 = bf2_to_f2(mx[3]);
-      px[0] = make_float4(b0.x, b0.y, b1.x, b1.y);
-      px[1] = make_float4(b2.x, b2.y, b3.x, b3.y);
     }
     if (!__syncthreads_and(ok)) {
       // A stage never arrived: record it and stop this CTA (bounded waits
@@ -184,176 +258,205 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nblk,
       }
       return;
     }
-    // Every thread has finished the previous block, so its stage can be
-    // refilled with the block kStages-1 iterations ahead of this one.
-    if (tid == 0 && it > 0) {
-      const int64_t nxt = blk + (int64_t)(G::kStages - 1) * gridDim.x;
-      if (nxt < nblk) {
+    // Every thread has finished the previous unit, so its stage can be
+    // refilled with the unit kStages-1 iterations ahead of this one.  (With
+    // one stage the refill waits for the end of this unit instead.)
+    if (G::kStages > 1 && tid == 0 && it > 0) {
+      const int64_t nxt = u + (int64_t)(G::kStages - 1) * gridDim.x;
+      if (nxt < nunit) {
         fence_proxy_async();
         issue(nxt, (it - 1) % G::kStages);
       }
     }
 
-    // ---- Stage 1b: gamma_min, gamma_scale, reciprocal.  The TL lanes that
-    // share a channel group split its 8 channels (kCPL each; with 16 token
-    // lanes two lanes compute each channel) and exchange them by shuffles.
     const int64_t pb = phys_block(bt, nphys, blk, H, &g_wait_timeout);  // output block
-    float* mrow = meta + pb * (int64_t)(G::kMetaRows * kD);
-    float lo_q[G::kCPL], rg_q[G::kCPL];
+    float* mrow = meta + pb * (int64_t)(G::kMetaRows * kD) + 8 * wofs;
+    uint32_t* arow = anchor + pb * (int64_t)(P * 16) + wofs;
+    uint32_t* rrow = residual + pb * (int64_t)(P * 16) + wofs;
+#pragma unroll 1
+    for (int sl = 0; sl < G::kSlicesPerWarp; ++sl) {
+      const int slice = w + G::kWarps * sl;
+      const int c = slice / G::kSlicesPerChunk;
+      const int g = (slice % G::kSlicesPerChunk) * G::kCG + cg;
+
+      // ---- Stage 1b: gamma_min, gamma_scale, reciprocal.  The token lanes
+      // that share a channel group split its 8 channels (kCPL each; with 16
+      // token lanes two lanes compute each channel) and exchange them by
+      // shuffles.
+      float lo_q[G::kCPL], rg_q[G::kCPL];
 #pragma unroll
-    for (int q = 0; q < G::kCPL; ++q) {
-      const int ch = 8 * g + ((tl * G::kCPL) & 7) + q;
-      float lo = pmn[ch], hi = pmx[ch];
+      for (int q = 0; q < G::kCPL; ++q) {
+        const int ch = 8 * g + ((kl * G::kCPL) & 7) + q;
+        float lo = pmn[ch], hi = pmx[ch];
 #pragma unroll
-      for (int cc = 1; cc < G::kNC; ++cc) {
-        lo = fminf(lo, pmn[cc * kD + ch]);
-        hi = fmaxf(hi, pmx[cc * kD + ch]);
+        for (int cc = 1; cc < G::kNC; ++cc) {
+          lo = fminf(lo, pmn[cc * W + ch]);
+          hi = fmaxf(hi, pmx[cc * W + ch]);
+        }
+        // one sign for a zero extreme: -0 for the minimum (zero x then
+        // centre to +0), +0 for the maximum
+        if (lo == 0.0f) lo = -0.0f;
+        if (hi == 0.0f) hi = 0.0f;
+        const float gs = __fsub_rn(hi, lo);
+        lo_q[q] = lo;
+        rg_q[q] = __frcp_rn(__fadd_rn(gs, kEps));
+        if (c == 0 && kl * G::kCPL < 8) {   // one writer per channel
+          mrow[ch] = lo;
+          mrow[kD + ch] = gs;
+        }
       }
-      // one sign for a zero extreme: -0 for the minimum (zero x then centre
-      // to +0), +0 for the maximum
-      if (lo == 0.0f) lo = -0.0f;
-      if (hi == 0.0f) hi = 0.0f;
-      const float gs = __fsub_rn(hi, lo);
-      lo_q[q] = lo;
-      rg_q[q] = __frcp_rn(__fadd_rn(gs, kEps));
-      if (c == 0 && tl * G::kCPL < 8) {   // one writer per channel
-        mrow[ch] = lo;
-        mrow[kD + ch] = gs;
+      // ---- Stage 1c: n = (x - gmin) * rg for the thread's 8 tokens x 8 ch
+      f2 gm2[4], rg2[4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {      // channel 8g + j comes from lane slot j / kCPL
+        const int src = (j / G::kCPL) * G::kCG + cg;
+        const float lo = __shfl_sync(kFull, lo_q[j % G::kCPL], src);
+        const float rg = __shfl_sync(kFull, rg_q[j % G::kCPL], src);
+        if (j & 1) { gm2[j >> 1].y = lo; rg2[j >> 1].y = rg; }
+        else       { gm2[j >> 1].x = lo; rg2[j >> 1].x = rg; }
       }
-    }
-    // ---- Stage 1c: n = (x - gmin) * rg for the thread's 8 tokens x 8 ch
-    f2 gm2[4], rg2[4];
+      f2 n[8][4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {        // channel 8g + j comes from token lane j / kCPL
-      const int src = (j / G::kCPL) * G::kCG + cg;
-      const float lo = __shfl_sync(kFull, lo_q[j % G::kCPL], src);
-      const float rg = __shfl_sync(kFull, rg_q[j % G::kCPL], src);
-      if (j & 1) { gm2[j >> 1].y = lo; rg2[j >> 1].y = rg; }
-      else       { gm2[j >> 1].x = lo; rg2[j >> 1].x = rg; }
-    }
-    f2 n[8][4];
+      for (int m = 0; m < 8; ++m) {
+        const uint4 v = tile_at(tile, c * C + G::kTL * m + tl, g);
+        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int t = c * C + G::kTL * m + tl;
-      const uint4 v = tile[t * 16 + g];
-      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+        for (int k = 0; k < 4; ++k) {
+          // scalar __fmul_rn, never contracted: a packed mul.rn.f32x2 here
+          // was fused with the first add of the chunk sum below
+          const f2 d = bf2_sub_f32(vv[k], gm2[k]);
+          n[m][k].x = __fmul_rn(d.x, rg2[k].x);
+          n[m][k].y = __fmul_rn(d.y, rg2[k].y);
+        }
+      }
+
+      // ---- Stage 2a: chunk mean, pairwise-halving order
+      f2 mu2[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        // scalar __fmul_rn, never contracted: a packed mul.rn.f32x2 here was
-        // fused with the first add of the chunk sum below
-        const f2 d = bf2_sub_f32(vv[k], gm2[k]);
-        n[m][k].x = __fmul_rn(d.x, rg2[k].x);
-        n[m][k].y = __fmul_rn(d.y, rg2[k].y);
+        f2 t0 = add2(n[0][k], n[4][k]), t1 = add2(n[1][k], n[5][k]);
+        f2 t2 = add2(n[2][k], n[6][k]), t3 = add2(n[3][k], n[7][k]);
+        t0 = add2(t0, t2);
+        t1 = add2(t1, t3);
+        f2 s = add2(t0, t1);
+#pragma unroll
+        for (int hh = G::kTL / 2; hh >= 1; hh /= 2) {  // token lanes tl and tl ^ hh
+          const int x = enc_kxor<G::kTL, G::kCG, G::kSwizzle>(hh) * G::kCG;
+          f2 o;
+          o.x = __shfl_xor_sync(kFull, s.x, x);
+          o.y = __shfl_xor_sync(kFull, s.y, x);
+          s = add2(s, o);
+        }
+        mu2[k] = mul2(s, f2{inv_C, inv_C});
       }
-    }
 
-    // ---- Stage 2a: chunk mean, pairwise-halving order
-    f2 mu2[4];
+      // ---- Stage 2b: d = n - mu; sigma = max |d| over the chunk.  Every
+      // step x -> x - gmin -> * rg -> - mu rounds monotonically (rg > 0), so
+      // the largest |d| is that of the chunk's largest or smallest x, which
+      // stage 1a left in the partials.
+      float sg[8];
+      {
+        const float4* pm = reinterpret_cast<const float4*>(pmn + c * W + 8 * g);
+        const float4* px = reinterpret_cast<const float4*>(pmx + c * W + 8 * g);
+        const float4 ma = pm[0], mb = pm[1], xa = px[0], xb = px[1];
+        const float lov[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+        const float hiv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      f2 t0 = add2(n[0][k], n[4][k]), t1 = add2(n[1][k], n[5][k]);
-      f2 t2 = add2(n[2][k], n[6][k]), t3 = add2(n[3][k], n[7][k]);
-      t0 = add2(t0, t2);
-      t1 = add2(t1, t3);
-      f2 s = add2(t0, t1);
-#pragma unroll
-      for (int hh = G::kTL / 2; hh >= 1; hh /= 2) {  // token lanes tl and tl ^ hh
-        f2 o;
-        o.x = __shfl_xor_sync(kFull, s.x, hh * G::kCG);
-        o.y = __shfl_xor_sync(kFull, s.y, hh * G::kCG);
-        s = add2(s, o);
+        for (int k = 0; k < 4; ++k) {
+          const f2 lo = sub2(make_float2(lov[2 * k], lov[2 * k + 1]), gm2[k]);
+          const f2 hi = sub2(make_float2(hiv[2 * k], hiv[2 * k + 1]), gm2[k]);
+          f2 nlo, nhi;
+          nlo.x = __fmul_rn(lo.x, rg2[k].x);
+          nlo.y = __fmul_rn(lo.y, rg2[k].y);
+          nhi.x = __fmul_rn(hi.x, rg2[k].x);
+          nhi.y = __fmul_rn(hi.y, rg2[k].y);
+          const f2 dlo = sub2(nlo, mu2[k]), dhi = sub2(nhi, mu2[k]);
+          sg[2 * k] = fmaxf(fabsf(dlo.x), fabsf(dhi.x));
+          sg[2 * k + 1] = fmaxf(fabsf(dlo.y), fabsf(dhi.y));
+        }
       }
-      mu2[k] = mul2(s, f2{inv_C, inv_C});
-    }
+#pragma unroll
+      for (int m = 0; m < 8; ++m)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) n[m][k] = sub2(n[m][k], mu2[k]);
+      if (kl == 0) {
+        float4* pmu = reinterpret_cast<float4*>(mrow + (2 + c) * kD + 8 * g);
+        float4* psg = reinterpret_cast<float4*>(mrow + (2 + G::kNC + c) * kD + 8 * g);
+        pmu[0] = make_float4(mu2[0].x, mu2[0].y, mu2[1].x, mu2[1].y);
+        pmu[1] = make_float4(mu2[2].x, mu2[2].y, mu2[3].x, mu2[3].y);
+        psg[0] = make_float4(sg[0], sg[1], sg[2], sg[3]);
+        psg[1] = make_float4(sg[4], sg[5], sg[6], sg[7]);
+      }
+      // rs = rn(1/(sigma + eps)): the token lanes of a channel group split
+      // the 8 channels as in stage 1b and exchange the reciprocals by shuffles.
+      float rs_q[G::kCPL];
+#pragma unroll
+      for (int q = 0; q < G::kCPL; ++q) {
+        const int j = ((kl * G::kCPL) & 7) + q;
+        float sj = sg[0];
+#pragma unroll
+        for (int i = 1; i < 8; ++i) sj = j == i ? sg[i] : sj;
+        rs_q[q] = __frcp_rn(__fadd_rn(sj, kEps));
+      }
+      f2 rs2[4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float r = __shfl_sync(kFull, rs_q[j % G::kCPL], (j / G::kCPL) * G::kCG + cg);
+        if (j & 1) rs2[j >> 1].y = r; else rs2[j >> 1].x = r;
+      }
 
-    // ---- Stage 2b: d = n - mu; sigma = max |d| over the chunk.  Every step
-    // x -> x - gmin -> * rg -> - mu rounds monotonically (rg > 0), so the
-    // largest |d| is that of the chunk's largest or smallest x, which stage
-    // 1a already holds per channel (mn, mx after the token-lane reduction).
-    float sg[8];
+      // ---- Stages 3-4: codes, sign map, nibble split, store one row per m
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const f2 lo = bf2_sub_f32(mn[k], gm2[k]), hi = bf2_sub_f32(mx[k], gm2[k]);
-      f2 nlo, nhi;
-      nlo.x = __fmul_rn(lo.x, rg2[k].x);
-      nlo.y = __fmul_rn(lo.y, rg2[k].y);
-      nhi.x = __fmul_rn(hi.x, rg2[k].x);
-      nhi.y = __fmul_rn(hi.y, rg2[k].y);
-      const f2 dlo = sub2(nlo, mu2[k]), dhi = sub2(nhi, mu2[k]);
-      sg[2 * k] = fmaxf(fabsf(dlo.x), fabsf(dhi.x));
-      sg[2 * k + 1] = fmaxf(fabsf(dlo.y), fabsf(dhi.y));
-    }
+      for (int m = 0; m < 8; ++m) {
+        const int t = c * C + G::kTL * m + tl;
+        float a[8];
+        uint32_t bits[8], dbits[8];
 #pragma unroll
-    for (int m = 0; m < 8; ++m)
+        for (int k = 0; k < 4; ++k) {
+          const f2 xf = mul2(n[m][k], rs2[k]);
+          a[2 * k] = fabsf(xf.x);
+          a[2 * k + 1] = fabsf(xf.y);
+          dbits[2 * k] = __float_as_uint(n[m][k].x);
+          dbits[2 * k + 1] = __float_as_uint(n[m][k].y);
+          compand_fast2(make_float2(a[2 * k], a[2 * k + 1]), alpha2, c16_2, bits[2 * k],
+                        bits[2 * k + 1]);
+        }
+        // smallest distance to a rounding boundary (low 16 bits) of the 8
+        // values, two at a time in 16-bit lanes
+        uint32_t dmin = __vminu2(prmt(bits[0], bits[1], 0x5410u), prmt(bits[2], bits[3], 0x5410u));
+        dmin = __vminu2(dmin, __vminu2(prmt(bits[4], bits[5], 0x5410u), prmt(bits[6], bits[7], 0x5410u)));
+        const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
+        if (__any_sync(kFull, amb)) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) n[m][k] = sub2(n[m][k], mu2[k]);
-    if (tl == 0) {
-      float4* pmu = reinterpret_cast<float4*>(mrow + (2 + c) * kD + 8 * g);
-      float4* psg = reinterpret_cast<float4*>(mrow + (2 + G::kNC + c) * kD + 8 * g);
-      pmu[0] = make_float4(mu2[0].x, mu2[0].y, mu2[1].x, mu2[1].y);
-      pmu[1] = make_float4(mu2[2].x, mu2[2].y, mu2[3].x, mu2[3].y);
-      psg[0] = make_float4(sg[0], sg[1], sg[2], sg[3]);
-      psg[1] = make_float4(sg[4], sg[5], sg[6], sg[7]);
-    }
-    // rs = rn(1/(sigma + eps)): the token lanes of a channel group split the
-    // 8 channels as in stage 1b and exchange the reciprocals by shuffles.
-    float rs_q[G::kCPL];
-#pragma unroll
-    for (int q = 0; q < G::kCPL; ++q) {
-      const int j = ((tl * G::kCPL) & 7) + q;
-      float sj = sg[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i) sj = j == i ? sg[i] : sj;
-      rs_q[q] = __frcp_rn(__fadd_rn(sj, kEps));
-    }
-    f2 rs2[4];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const float r = __shfl_sync(kFull, rs_q[j % G::kCPL], (j / G::kCPL) * G::kCG + cg);
-      if (j & 1) rs2[j >> 1].y = r; else rs2[j >> 1].x = r;
-    }
-
-    // ---- Stages 3-4: codes, sign map, nibble split, store one row per m
-    uint32_t* arow = anchor + pb * (int64_t)(P * 16);
-    uint32_t* rrow = residual + pb * (int64_t)(P * 16);
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const int t = c * C + G::kTL * m + tl;
-      float a[8];
-      uint32_t bits[8], dbits[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const f2 xf = mul2(n[m][k], rs2[k]);
-        a[2 * k] = fabsf(xf.x);
-        a[2 * k + 1] = fabsf(xf.y);
-        dbits[2 * k] = __float_as_uint(n[m][k].x);
-        dbits[2 * k + 1] = __float_as_uint(n[m][k].y);
-        compand_fast2(make_float2(a[2 * k], a[2 * k + 1]), alpha2, c16_2, bits[2 * k],
-                      bits[2 * k + 1]);
+          for (int i = 0; i < 8; ++i)
+            if (compand_ambiguous(bits[i]))
+              bits[i] = (bits[i] & 0xff00ffffu) | (compand_exact(bits[i], a[i], tab.thr) << 16);
+        }
+        // code bytes (byte 2 of bits) xor the replicated sign of d
+        const uint32_t i01 = prmt(bits[0], bits[1], 0x0062u), i23 = prmt(bits[2], bits[3], 0x0062u);
+        const uint32_t i45 = prmt(bits[4], bits[5], 0x0062u), i67 = prmt(bits[6], bits[7], 0x0062u);
+        const uint32_t s01 = prmt(dbits[0], dbits[1], 0x00fbu), s23 = prmt(dbits[2], dbits[3], 0x00fbu);
+        const uint32_t s45 = prmt(dbits[4], dbits[5], 0x00fbu), s67 = prmt(dbits[6], dbits[7], 0x00fbu);
+        const uint32_t W0 = prmt(i01 ^ s01, i23 ^ s23, 0x5410u);
+        const uint32_t W1 = prmt(i45 ^ s45, i67 ^ s67, 0x5410u);
+        // byte k: Anchor = (ch k high nibble) | (ch k+4 high nibble) << 4, etc.
+        const uint32_t Aw = ((W0 >> 4) & 0x0f0f0f0fu) | (W1 & 0xf0f0f0f0u);
+        const uint32_t Rw = (W0 & 0x0f0f0f0fu) | ((W1 << 4) & 0xf0f0f0f0u);
+        arow[t * 16 + g] = Aw;
+        rrow[t * 16 + g] = Rw;
       }
-      // smallest distance to a rounding boundary (low 16 bits) of the 8
-      // values, two at a time in 16-bit lanes
-      uint32_t dmin = __vminu2(prmt(bits[0], bits[1], 0x5410u), prmt(bits[2], bits[3], 0x5410u));
-      dmin = __vminu2(dmin, __vminu2(prmt(bits[4], bits[5], 0x5410u), prmt(bits[6], bits[7], 0x5410u)));
-      const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
-      if (__any_sync(kFull, amb)) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (compand_ambiguous(bits[i]))
-            bits[i] = (bits[i] & 0xff00ffffu) | (compand_exact(bits[i], a[i], tab.thr) << 16);
+    }
+    if constexpr (G::kStages == 1) {
+      // one stage: every warp has read the tile and the partials of this
+      // unit; refill the stage with the next unit
+      __syncthreads();
+      if (tid == 0) {
+        const int64_t nxt = u + gridDim.x;
+        if (nxt < nunit) {
+          fence_proxy_async();
+          issue(nxt, 0);
+        }
       }
-      // code bytes (byte 2 of bits) xor the replicated sign of d
-      const uint32_t i01 = prmt(bits[0], bits[1], 0x0062u), i23 = prmt(bits[2], bits[3], 0x0062u);
-      const uint32_t i45 = prmt(bits[4], bits[5], 0x0062u), i67 = prmt(bits[6], bits[7], 0x0062u);
-      const uint32_t s01 = prmt(dbits[0], dbits[1], 0x00fbu), s23 = prmt(dbits[2], dbits[3], 0x00fbu);
-      const uint32_t s45 = prmt(dbits[4], dbits[5], 0x00fbu), s67 = prmt(dbits[6], dbits[7], 0x00fbu);
-      const uint32_t W0 = prmt(i01 ^ s01, i23 ^ s23, 0x5410u);
-      const uint32_t W1 = prmt(i45 ^ s45, i67 ^ s67, 0x5410u);
-      // byte k: Anchor = (ch k high nibble) | (ch k+4 high nibble) << 4, etc.
-      const uint32_t Aw = ((W0 >> 4) & 0x0f0f0f0fu) | (W1 & 0xf0f0f0f0u);
-      const uint32_t Rw = (W0 & 0x0f0f0f0fu) | ((W1 << 4) & 0xf0f0f0f0u);
-      arow[t * 16 + g] = Aw;
-      rrow[t * 16 + g] = Rw;
     }
   }
 }
@@ -372,6 +475,14 @@ static cudaError_t run_encode(const CUtensorMap& map, const Shape& s, const Comp
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_dev != dev) {
+    if (G::kSwizzle) {
+      // swizzled tiles start 1024-byte aligned only if dynamic shared memory
+      // does (it follows the block's reserved shared memory)
+      int reserved = -1;
+      e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+      if (e != cudaSuccess) return e;
+      if (reserved % 1024 != 0) return cudaErrorNotSupported;
+    }
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)G::kSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -383,11 +494,11 @@ static cudaError_t run_encode(const CUtensorMap& map, const Shape& s, const Comp
     per_sm = n > 0 ? n : 1;
     configured_dev = dev;
   }
-  const int64_t nblk = s.blocks();
+  const int64_t nunit = s.blocks() * G::kUnits;
   int64_t grid = (int64_t)sm_count() * per_sm;
-  if (grid > nblk) grid = nblk;
+  if (grid > nunit) grid = nunit;
   fn<<<(unsigned)grid, G::kThreads, G::kSmem, stream>>>(
-      map, nblk, s.NB(), s.H, s.L, static_cast<uint32_t*>(anchor),
+      map, nunit, s.NB(), s.H, s.L, static_cast<uint32_t*>(anchor),
       static_cast<uint32_t*>(residual), meta, pg.table, pg.nphys, tab);
   return cudaGetLastError();
 }
@@ -410,28 +521,37 @@ static EncodeTiledFn get_encode_tiled() {
   return fn;
 }
 
+template <int P, int C>
+static cudaError_t encode_case(EncodeTiledFn enc, const void* kv, const Shape& s,
+                               const CompanderTable& tab, void* anchor, void* residual,
+                               float* meta, cudaStream_t stream, const Paging& pg) {
+  using G = EncGeom<P, C>;
+  CUtensorMap map;
+  const cuuint64_t dims[2] = {(cuuint64_t)s.H * kD, (cuuint64_t)(s.B * s.L)};
+  const cuuint64_t strides[1] = {(cuuint64_t)s.H * kD * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)G::kW, (cuuint32_t)(P < 256 ? P : 256)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   G::kSwizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  return run_encode<P, C>(map, s, tab, anchor, residual, meta, stream, pg);
+}
+
 cudaError_t launch_encode(const void* kv, const Shape& s, const CompanderTable& tab,
                           void* anchor, void* residual, float* meta, cudaStream_t stream,
                           const Paging& pg) {
   if (s.blocks() == 0) return cudaSuccess;
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return cudaErrorNotSupported;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)s.H * kD, (cuuint64_t)(s.B * s.L)};
-  const cuuint64_t strides[1] = {(cuuint64_t)s.H * kD * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kD, (cuuint32_t)s.page};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(kv), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 #define LYNX_ENC_CASE(PP, CC) \
   if (s.page == PP && s.C == CC)                                            \
-    return run_encode<PP, CC>(map, s, tab, anchor, residual, meta, stream, pg);
+    return encode_case<PP, CC>(enc, kv, s, tab, anchor, residual, meta, stream, pg);
   LYNX_ENC_CASE(64, 16) LYNX_ENC_CASE(64, 32) LYNX_ENC_CASE(64, 64)
   LYNX_ENC_CASE(128, 16) LYNX_ENC_CASE(128, 32) LYNX_ENC_CASE(128, 64) LYNX_ENC_CASE(128, 128)
   LYNX_ENC_CASE(256, 16) LYNX_ENC_CASE(256, 32) LYNX_ENC_CASE(256, 64) LYNX_ENC_CASE(256, 128)
+  LYNX_ENC_CASE(512, 16) LYNX_ENC_CASE(512, 32) LYNX_ENC_CASE(512, 64) LYNX_ENC_CASE(512, 128)
 #undef LYNX_ENC_CASE
   return cudaErrorInvalidValue;
 }

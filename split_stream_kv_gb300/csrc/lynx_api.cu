@@ -116,11 +116,16 @@ static int check_encode_alpha(float alpha) {
   return LYNX_OK;
 }
 
-static int check_codec_shape(int64_t B, int64_t L, int H, int D, int page, int C) {
+// Pages of 64 ... 512 tokens for the Algorithm 1 codec (encode, both
+// decoders, the k-bit Anchor decode); the attention kernel and the
+// Appendix A.1 variant are built for pages up to 256.
+static int check_codec_shape(int64_t B, int64_t L, int H, int D, int page, int C,
+                             int max_page = 512) {
   if (B < 0 || L < 0 || H <= 0) return fail(LYNX_ESHAPE, "need B >= 0, L >= 0, H_kv >= 1");
   if (D != kD) return fail(LYNX_EUNSUPPORTED, "D = %d: only D = 128 is built", D);
-  if (page != 64 && page != 128 && page != 256)
-    return fail(LYNX_EUNSUPPORTED, "page = %d: built for 64, 128, 256", page);
+  if ((page != 64 && page != 128 && page != 256 && page != 512) || page > max_page)
+    return fail(LYNX_EUNSUPPORTED, "page = %d: built for 64 ... %d (powers of two)", page,
+                max_page);
   if (C <= 0 || (C & (C - 1))) return fail(LYNX_ESHAPE, "C = %d must be a power of two", C);
   if (C < 16 || C > 128 || C > page)
     return fail(LYNX_EUNSUPPORTED, "C = %d: built for 16..128 and C <= page", C);
@@ -305,7 +310,7 @@ int lynx_decode_anchor_bits(const void* anchor_k, const float* meta, int64_t B, 
 
 int lynx_a1_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page, float alpha,
                    void* anchor, void* residual, float* meta, void* stream) {
-  int rc = check_codec_shape(B, L, H_kv, D, page, 16);
+  int rc = check_codec_shape(B, L, H_kv, D, page, 16, 256);
   if (rc) return rc;
   if ((rc = check_alpha(alpha))) return rc;
   if (B * L == 0) return LYNX_OK;
@@ -319,7 +324,7 @@ int lynx_a1_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int pa
 int lynx_a1_decode(const void* anchor, const void* residual, const float* meta, int64_t B,
                    int64_t L, int H_kv, int D, int page, float alpha, void* out, int out_dtype,
                    void* stream) {
-  int rc = check_codec_shape(B, L, H_kv, D, page, 16);
+  int rc = check_codec_shape(B, L, H_kv, D, page, 16, 256);
   if (rc) return rc;
   if ((rc = check_alpha(alpha))) return rc;
   if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)
@@ -335,7 +340,7 @@ int lynx_a1_decode(const void* anchor, const void* residual, const float* meta, 
 
 static int check_attn_shape(int batch, int T, int H_q, int64_t L, int H_kv, int D, int page,
                             int C) {
-  int rc = check_codec_shape(batch, L, H_kv, D, page, C);
+  int rc = check_codec_shape(batch, L, H_kv, D, page, C, 256);
   if (rc) return rc;
   if (batch < 1 || L < 1) return fail(LYNX_ESHAPE, "attention needs batch >= 1 and L >= 1");
   if (T < 1) return fail(LYNX_ESHAPE, "T = %d must be >= 1", T);

@@ -269,15 +269,17 @@ __global__ void __launch_bounds__(kThreads) join_bits_kernel(const uint8_t* __re
 
 // Anchor-only decode of a K-bit Anchor, the same reconstruction as the 4+4
 // Anchor decoder with the bucket point I = 2^(8-K) V + 2^(7-K) - 1.  One
-// persistent kernel: a CTA walks page blocks, whose K-bit codes (page x 16 K
-// bytes) and metadata rows arrive in shared memory by bulk asynchronous
-// copies, one stage ahead of the block being decoded.  Thread (slot, G) of
-// 256 decodes a run of page/16 tokens (inside one chunk) of channels
-// 8G..8G+7.  The K bytes of (token t, group G) start at byte (16 t + G) K of
+// persistent kernel: a CTA walks units of up to 256 tokens (a page block, or
+// one half of a 512-token page), whose K-bit codes (unit x 16 K bytes) and
+// metadata rows (for a half page: the gamma rows and the mu and sigma rows of
+// its chunks) arrive in shared memory by bulk asynchronous copies, one stage
+// ahead of the unit being decoded.  Thread (slot, G) of 256 decodes a run of
+// unit/16 tokens (inside one chunk) of channels 8G..8G+7.  The K bytes of (token t, group G) start at byte (16 t + G) K of
 // the block and lie in two consecutive 32-bit words ((o mod 4) + K <= 8: o
 // is even when K = 6); the word after a block's last code is still inside
 // the stage (its metadata follows), and the shift drops its bytes.
 constexpr int kBitsStages = 2;
+constexpr int kBitsUnit = 256;   // most tokens of a decode unit
 
 // Set by a kernel of this file whose bounded wait on a stage gave up (it
 // then returns early).  Read through read_variant_wait_timeout(); never reset.
@@ -299,14 +301,17 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
   // with V = S > 0 ? a : -a - 1 and I = 2^(8-K) V + 2^(7-K) - 1; one copy a
   // lane (row a, column lane), so that every lane reads its own bank
   float* xk = reinterpret_cast<float*>(smem);
-  const uint32_t code_bytes = (uint32_t)P * 16 * K;
-  const int NC = P / C, meta_rows = 2 + 2 * NC;
-  const uint32_t meta_bytes = (uint32_t)meta_rows * kD * 4;
+  const int U = P < kBitsUnit ? P : kBitsUnit;    // tokens of a unit
+  const int parts = P / U;
+  const int64_t nunit = nblk * parts;
+  const uint32_t code_bytes = (uint32_t)U * 16 * K;
+  const int NC = U / C, blk_meta_rows = 2 + 2 * (P / C);
+  const uint32_t meta_bytes = (uint32_t)(2 + 2 * NC) * kD * 4;
   const uint32_t stage_bytes = code_bytes + meta_bytes;
   uint8_t* stages = smem + bits_table_bytes<K>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(stages + kBitsStages * stage_bytes);
   const int tid = threadIdx.x, lane = tid & 31, G = tid & 15, slot = tid >> 4;
-  const int run = P >> 4, t0 = slot * run, chunk = t0 / C;
+  const int run = U >> 4, t0 = slot * run, chunk = t0 / C;
   const int64_t ostride = (int64_t)H * kD;
 
   for (int i = tid; i < NCODE * 32; i += kThreads) {
@@ -321,20 +326,30 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
   __syncthreads();
   const float* xl = xk + lane;
 
-  auto issue = [&](int64_t blk, int stage) {
+  auto issue = [&](int64_t un, int stage) {
+    const int64_t blk = un / parts, part = un % parts;
     uint8_t* st = stages + stage * stage_bytes;
     mbar_expect_tx(&bars[stage], stage_bytes);
-    bulk_load(st, ak + blk * code_bytes, code_bytes, &bars[stage]);
-    bulk_load(st + code_bytes, meta + blk * (int64_t)meta_rows * kD, meta_bytes, &bars[stage]);
+    bulk_load(st, ak + un * code_bytes, code_bytes, &bars[stage]);
+    const float* mb = meta + blk * (int64_t)blk_meta_rows * kD;
+    if (parts == 1) {
+      bulk_load(st + code_bytes, mb, meta_bytes, &bars[stage]);
+    } else {  // gamma rows, then the unit's mu rows and sigma rows
+      const uint32_t rows = (uint32_t)NC * kD * 4;
+      bulk_load(st + code_bytes, mb, 2 * kD * 4, &bars[stage]);
+      bulk_load(st + code_bytes + 2 * kD * 4, mb + (2 + part * NC) * kD, rows, &bars[stage]);
+      bulk_load(st + code_bytes + 2 * kD * 4 + rows, mb + (2 + P / C + part * NC) * kD, rows,
+                &bars[stage]);
+    }
   };
   if (tid == 0)
     for (int i = 0; i < kBitsStages; ++i) {
-      const int64_t blk = blockIdx.x + (int64_t)i * gridDim.x;
-      if (blk < nblk) issue(blk, i);
+      const int64_t un = blockIdx.x + (int64_t)i * gridDim.x;
+      if (un < nunit) issue(un, i);
     }
 
   int it = 0;
-  for (int64_t blk = blockIdx.x; blk < nblk; blk += gridDim.x, ++it) {
+  for (int64_t un = blockIdx.x; un < nunit; un += gridDim.x, ++it) {
     const int stage = it % kBitsStages;
     const uint32_t phase = (uint32_t)(it / kBitsStages) & 1u;
     const bool ok = mbar_wait(&bars[stage], phase);
@@ -357,9 +372,10 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
     row8(mrow + kD, gs, true);
     row8(mrow + (2 + chunk) * kD, mu, false);
     row8(mrow + (2 + NC + chunk) * kD, sg, true);
+    const int64_t blk = un / parts, part = un % parts;
     const int64_t h = blk % H, rest = blk / H;
     const int64_t p = rest % NB, b = rest / NB;
-    const int64_t orow0 = ((b * L + p * P + t0) * H + h) * kD + 8 * G;
+    const int64_t orow0 = ((b * L + p * P + part * U + t0) * H + h) * kD + 8 * G;
 #pragma unroll 4
     for (int r = 0; r < run; ++r) {
       const uint32_t o = (uint32_t)((t0 + r) * 16 + G) * K;
@@ -393,10 +409,10 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
       }
       return;
     }
-    // every thread is done with this stage: refill it kBitsStages blocks ahead
+    // every thread is done with this stage: refill it kBitsStages units ahead
     if (tid == 0) {
-      const int64_t nxt = blk + (int64_t)kBitsStages * gridDim.x;
-      if (nxt < nblk) {
+      const int64_t nxt = un + (int64_t)kBitsStages * gridDim.x;
+      if (nxt < nunit) {
         fence_proxy_async();
         issue(nxt, stage);
       }
@@ -714,7 +730,8 @@ template <int K, bool BF16OUT>
 static cudaError_t run_decode_bits(const uint8_t* ak, const float* meta, const Shape& s,
                                    const ExpandTable& tab, void* out, cudaStream_t stream) {
   auto fn = decode_anchor_bits_kernel<K, BF16OUT>;
-  const size_t stage = (size_t)s.page * 16 * K + (size_t)(2 + 2 * (s.page / s.C)) * kD * 4;
+  const int U = s.page < kBitsUnit ? s.page : kBitsUnit;
+  const size_t stage = (size_t)U * 16 * K + (size_t)(2 + 2 * (U / s.C)) * kD * 4;
   const size_t smem = bits_table_bytes<K>() + kBitsStages * stage + kBitsStages * 8;
   constexpr size_t kMaxSmem = bits_table_bytes<K>() + kBitsStages * (256 * 16 * K + 34 * kD * 4) + 64;
   static thread_local int configured_dev = -1;
@@ -738,7 +755,7 @@ static cudaError_t run_decode_bits(const uint8_t* ak, const float* meta, const S
   }
   const int64_t nblk = s.blocks();
   int64_t grid = (int64_t)sm_count() * per_sm;
-  if (grid > nblk) grid = nblk;
+  if (grid > nblk * (s.page / U)) grid = nblk * (s.page / U);
   fn<<<(unsigned)grid, kThreads, smem, stream>>>(ak, meta, nblk, s.NB(), s.H, s.L, s.page, s.C,
                                                  out, tab);
   return cudaGetLastError();

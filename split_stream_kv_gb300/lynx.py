@@ -108,6 +108,20 @@ def _need_cuda(*ts):
             raise ValueError("lynx: tensors must be contiguous CUDA tensors")
 
 
+def _expect(t, shape, dtype, device, what):
+    """The C ABI sees pointers only: a caller's tensor of the wrong size or
+    type would be read or written out of bounds on the device, so every
+    tensor is checked against the sizes the call implies before it is
+    passed."""
+    if t is None:
+        raise ValueError(f"{what} is required")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what}: expected {dtype} of shape {tuple(shape)}, got {t.dtype} "
+                         f"of shape {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{what}: on {t.device}, expected {device}")
+
+
 # ----------------------------------------------------------------- codec
 
 def lynx_encoded_sizes(B: int, L: int, H_kv: int, D: int, page: int, C: int):
@@ -139,6 +153,9 @@ def lynx_encode(kv: torch.Tensor, page: int, C: int, alpha: float, anchor=None, 
         residual = torch.empty(cr, dtype=torch.uint8, device=dev)
     if meta is None:
         meta = torch.empty(cm, dtype=torch.float32, device=dev)
+    _expect(anchor, ca, torch.uint8, dev, "lynx_encode: anchor")
+    _expect(residual, cr, torch.uint8, dev, "lynx_encode: residual")
+    _expect(meta, cm, torch.float32, dev, "lynx_encode: meta")
     _check(lib().lynx_encode(_ptr(kv), B, L, H, D, page, C, alpha, _ptr(anchor), _ptr(residual),
                              _ptr(meta), _stream(dev)), "lynx_encode")
     return anchor, residual, meta
@@ -148,16 +165,29 @@ def _decode_out(anchor, L, out_dtype, out):
     B, NB, H, page, half = anchor.shape
     if out is None:
         out = torch.empty((B, L, H, half * 2), dtype=out_dtype, device=anchor.device)
-    code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
     if out.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("lynx decode: output must be bfloat16 or float32")
+    _expect(out, (B, L, H, half * 2), out.dtype, anchor.device, "lynx decode: out")
+    code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
     return out, code, B, H, page, half * 2
+
+
+def _check_decode_streams(what, anchor, residual, meta, L, page, C):
+    if anchor.dim() != 5 or anchor.dtype != torch.uint8:
+        raise ValueError(f"{what}: anchor must be uint8 [B][L/page][H_kv][page][D/2]")
+    B, _, H, _, half = anchor.shape
+    ca, cr, cm = stream_shapes(B, L, H, half * 2, page, C)
+    _expect(anchor, ca, torch.uint8, anchor.device, f"{what}: anchor")
+    if residual is not None:
+        _expect(residual, cr, torch.uint8, anchor.device, f"{what}: residual")
+    _expect(meta, cm, torch.float32, anchor.device, f"{what}: meta")
 
 
 def lynx_decode_anchor(anchor, meta, L: int, page: int, C: int, alpha: float,
                        out_dtype=torch.bfloat16, out=None):
     """Anchor-only reconstruction -> out[B][L][H_kv][D]."""
     _need_cuda(anchor, meta, out)
+    _check_decode_streams("lynx_decode_anchor", anchor, None, meta, L, page, C)
     out, code, B, H, P, D = _decode_out(anchor, L, out_dtype, out)
     _check(lib().lynx_decode_anchor(_ptr(anchor), _ptr(meta), B, L, H, D, page, C, alpha,
                                     _ptr(out), code, _stream(anchor.device)),
@@ -169,6 +199,9 @@ def lynx_decode_full(anchor, residual, meta, L: int, page: int, C: int, alpha: f
                      out_dtype=torch.bfloat16, out=None):
     """Anchor + Residual reconstruction -> out[B][L][H_kv][D]."""
     _need_cuda(anchor, residual, meta, out)
+    _check_decode_streams("lynx_decode_full", anchor, residual, meta, L, page, C)
+    if residual is None:
+        raise ValueError("lynx_decode_full: residual is required")
     out, code, B, H, P, D = _decode_out(anchor, L, out_dtype, out)
     _check(lib().lynx_decode_full(_ptr(anchor), _ptr(residual), _ptr(meta), B, L, H, D, page, C,
                                   alpha, _ptr(out), code, _stream(anchor.device)),
@@ -206,6 +239,9 @@ def lynx_encode_paged(kv: torch.Tensor, page: int, C: int, alpha: float, block_t
         residual_pool = torch.empty(cr, dtype=torch.uint8, device=dev)
     if meta_pool is None:
         meta_pool = torch.empty(cm, dtype=torch.float32, device=dev)
+    _expect(anchor_pool, ca, torch.uint8, dev, "lynx_encode_paged: anchor pool")
+    _expect(residual_pool, cr, torch.uint8, dev, "lynx_encode_paged: residual pool")
+    _expect(meta_pool, cm, torch.float32, dev, "lynx_encode_paged: meta pool")
     _check(lib().lynx_encode_paged(_ptr(kv), B, L, H, D, page, C, alpha, _ptr(block_table),
                                    num_blocks, _ptr(anchor_pool), _ptr(residual_pool),
                                    _ptr(meta_pool), _stream(dev)), "lynx_encode_paged")
@@ -223,6 +259,13 @@ def lynx_decode_paged(anchor_pool, residual_pool, meta_pool, block_table, L: int
         out = torch.empty((B, L, H, half * 2), dtype=out_dtype, device=anchor_pool.device)
     if out.dtype not in (torch.bfloat16, torch.float32):
         raise ValueError("lynx decode: output must be bfloat16 or float32")
+    dev = anchor_pool.device
+    shapes = paged_pool_shapes(num_blocks, H, half * 2, page, C)
+    _expect(anchor_pool, shapes[0], torch.uint8, dev, "lynx_decode_paged: anchor pool")
+    if mode == LYNX_FULL:
+        _expect(residual_pool, shapes[1], torch.uint8, dev, "lynx_decode_paged: residual pool")
+    _expect(meta_pool, shapes[2], torch.float32, dev, "lynx_decode_paged: meta pool")
+    _expect(out, (B, L, H, half * 2), out.dtype, dev, "lynx_decode_paged: out")
     code = LYNX_OUT_BF16 if out.dtype == torch.bfloat16 else LYNX_OUT_FP32
     _check(lib().lynx_decode_paged(_ptr(anchor_pool), _ptr(residual_pool), _ptr(meta_pool),
                                    _ptr(block_table), num_blocks, B, L, H, half * 2, page, C,
@@ -508,6 +551,42 @@ def lynx_attn_workspace_bytes(batch: int, T: int, H_q: int, L: int, H_kv: int, D
     return n.value
 
 
+def _check_attn_io(what, q, ks, vs, L, page, C, mode, out, workspace, need, pools=False):
+    """Shapes, types and devices of everything an attention call reads or
+    writes: q [batch][T][H_q][D] bf16; K and V streams of one layout (dense
+    [batch][L/page][H_kv][...], or pools [num_blocks][H_kv][...]); residuals
+    present in full mode; out [batch][T][H_q][D] float32; a workspace of at
+    least `need` bytes."""
+    batch, T, H_q, D = q.shape
+    dev = q.device
+    for name, (a, r, m) in (("k", ks), ("v", vs)):
+        if a.dtype != torch.uint8 or a.dim() != (4 if pools else 5):
+            raise ValueError(f"{what}: {name} anchor must be uint8 "
+                             + ("[num_blocks][H_kv][page][D/2]" if pools
+                                else "[batch][L/page][H_kv][page][D/2]"))
+        if pools:
+            nb, H_kv = a.shape[0], a.shape[1]
+            codes = (nb, H_kv, page, D // 2)
+            mshape = (nb, H_kv, 2 + 2 * (page // C), D)
+        else:
+            H_kv = a.shape[2]
+            codes, _, mshape = stream_shapes(batch, L, H_kv, D, page, C)
+        _expect(a, codes, torch.uint8, dev, f"{what}: {name} anchor")
+        if mode == LYNX_FULL:
+            _expect(r, codes, torch.uint8, dev, f"{what}: {name} residual")
+        _expect(m, mshape, torch.float32, dev, f"{what}: {name} meta")
+    if tuple(ks[0].shape) != tuple(vs[0].shape):
+        raise ValueError(f"{what}: K and V streams differ in shape")
+    _expect(out, (batch, T, H_q, D), torch.float32, dev, f"{what}: out")
+    if workspace is not None:
+        if workspace.device != dev:
+            raise ValueError(f"{what}: workspace on {workspace.device}, expected {dev}")
+        if workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"{what}: workspace holds "
+                             f"{workspace.numel() * workspace.element_size()} bytes, "
+                             f"the call needs {need}")
+
+
 def lynx_attn_decode(q, k_streams, v_streams, L: int, page: int, C: int, alpha: float,
                      mode: int, out=None, workspace=None, k_tail=None, v_tail=None):
     """q[batch][T][H_q][D] bf16; k_streams / v_streams = (anchor, residual or
@@ -523,12 +602,16 @@ def lynx_attn_decode(q, k_streams, v_streams, L: int, page: int, C: int, alpha: 
     if q.dtype != torch.bfloat16 or q.dim() != 4:
         raise ValueError("lynx_attn_decode: q must be a 4-D bfloat16 tensor")
     batch, T, H_q, D = q.shape
+    if ka.dim() != 5:
+        raise ValueError("lynx_attn_decode: streams must be [batch][L/page][H_kv][...]")
     H_kv = ka.shape[2]
     if out is None:
         out = torch.empty((batch, T, H_q, D), dtype=torch.float32, device=q.device)
     need = lynx_attn_workspace_bytes(batch, T, H_q, L, H_kv, D, page)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_attn_io("lynx_attn_decode", q, k_streams, v_streams, L, page, C, mode, out,
+                   workspace, need)
     if k_tail is not None:
         for t in (k_tail, v_tail):
             if t.dtype != torch.bfloat16 or tuple(t.shape) != (batch, T, H_kv, D) or \
@@ -538,12 +621,14 @@ def lynx_attn_decode(q, k_streams, v_streams, L: int, page: int, C: int, alpha: 
         _check(lib().lynx_attn_decode_tail(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr),
                                            _ptr(km), _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D,
                                            page, C, alpha, mode, _ptr(k_tail), _ptr(v_tail),
-                                           _ptr(out), _ptr(workspace), workspace.numel(),
+                                           _ptr(out), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
                                            _stream(q.device)), "lynx_attn_decode_tail")
         return out
     _check(lib().lynx_attn_decode(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr), _ptr(km),
                                   _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D, page, C, alpha,
-                                  mode, _ptr(out), _ptr(workspace), workspace.numel(),
+                                  mode, _ptr(out), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
                                   _stream(q.device)), "lynx_attn_decode")
     return out
 
@@ -571,6 +656,8 @@ def lynx_attn_decode_paged(q, k_pools, v_pools, block_table, L: int, page: int, 
     if q.dtype != torch.bfloat16 or q.dim() != 4:
         raise ValueError("lynx_attn_decode_paged: q must be a 4-D bfloat16 tensor")
     batch, T, H_q, D = q.shape
+    if ka.dim() != 4:
+        raise ValueError("lynx_attn_decode_paged: pools must be [num_blocks][H_kv][...]")
     num_blocks, H_kv = ka.shape[0], ka.shape[1]
     _check_table(block_table, batch, L // page)
     if out is None:
@@ -578,11 +665,18 @@ def lynx_attn_decode_paged(q, k_pools, v_pools, block_table, L: int, page: int, 
     need = lynx_attn_workspace_bytes(batch, T, H_q, L, H_kv, D, page)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check_attn_io("lynx_attn_decode_paged", q, k_pools, v_pools, L, page, C, mode, out,
+                   workspace, need, pools=True)
+    if k_tail is not None:
+        for t in (k_tail, v_tail):
+            _expect(t, (batch, T, H_kv, D), torch.bfloat16, q.device,
+                    "lynx_attn_decode_paged: tail")
     _check(lib().lynx_attn_decode_paged(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr), _ptr(km),
                                         _ptr(va), _ptr(vr), _ptr(vm), _ptr(block_table),
                                         num_blocks, L, H_kv, D, page, C, alpha, mode,
                                         _ptr(k_tail), _ptr(v_tail), _ptr(out), _ptr(workspace),
-                                        workspace.numel(), _stream(q.device)),
+                                        workspace.numel() * workspace.element_size(),
+                                        _stream(q.device)),
            "lynx_attn_decode_paged")
     return out
 
@@ -599,9 +693,13 @@ def lynx_attn_decode_noalloc(q, k_streams, v_streams, L: int, page: int, C: int,
     if q.dtype != torch.bfloat16 or q.dim() != 4:
         raise ValueError("lynx_attn_decode_noalloc: q must be a 4-D bfloat16 tensor")
     batch, T, H_q, D = q.shape
+    if ka.dim() != 5:
+        raise ValueError("lynx_attn_decode_noalloc: streams must be [batch][L/page][H_kv][...]")
     H_kv = ka.shape[2]
     if out is None:
         out = torch.empty((batch, T, H_q, D), dtype=torch.float32, device=q.device)
+    _check_attn_io("lynx_attn_decode_noalloc", q, k_streams, v_streams, L, page, C, mode, out,
+                   None, 0)
     _check(lib().lynx_attn_decode_noalloc(_ptr(q), batch, T, H_q, _ptr(ka), _ptr(kr), _ptr(km),
                                           _ptr(va), _ptr(vr), _ptr(vm), L, H_kv, D, page, C,
                                           alpha, mode, _ptr(out), _stream(q.device)),

@@ -46,6 +46,7 @@ OK = ctypes.c_void_p(0x10000)     # aligned, never dereferenced: every call belo
 @pytest.mark.parametrize("args,code", [
     (dict(D=64), -3),
     (dict(page=96), -3),
+    (dict(page=1024), -3),
     (dict(C=48), -2),
     (dict(C=8), -3),
     (dict(C=512, page=256), -3),
@@ -91,6 +92,7 @@ def test_attention_rejects(lynx_lib):
     assert call(mode=3) == -1
     assert call(ws=0) == -5
     assert call(L=100) == -2
+    assert call(page=512, L=1024) == -3       # attention is built for pages <= 256
     need = lynx_lib.lynx_attn_workspace_bytes(1, 1, 4, 256, 1, 128, 128)
     assert need > 0
     assert call(ws=need - 1) == -5
@@ -125,3 +127,44 @@ def test_binding_rejects_cpu_tensors(lynx_lib):
     kv = torch.zeros((1, 128, 1, 128), dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         lynx_lib.lynx_encode(kv, 128, 32, 255.0)
+
+
+def test_binding_rejects_mis_sized_buffers(lynx_lib):
+    """The C ABI sees pointers only, so the binding checks every caller
+    tensor against the sizes the call implies before anything is launched
+    (these checks run before any device work, so meta tensors suffice)."""
+    import torch
+
+    from split_stream_kv_gb300 import lynx
+    dev = torch.device("meta")
+
+    def streams(B, L, H, P=128, C=32):
+        a, r, m = lynx.stream_shapes(B, L, H, 128, P, C)
+        return (torch.empty(a, dtype=torch.uint8, device=dev),
+                torch.empty(r, dtype=torch.uint8, device=dev),
+                torch.empty(m, dtype=torch.float32, device=dev))
+
+    q = torch.empty((2, 1, 8, 128), dtype=torch.bfloat16, device=dev)
+    ks, vs = streams(2, 256, 2), streams(2, 256, 2)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    good_out = torch.empty((2, 1, 8, 128), dtype=torch.float32, device=dev)
+    check = lynx._check_attn_io
+    check("t", q, ks, vs, 256, 128, 32, lynx.LYNX_FULL, good_out, ws, 1024)
+    bad = [
+        dict(out=torch.empty((2, 1, 8, 64), dtype=torch.float32, device=dev)),
+        dict(out=torch.empty((2, 1, 8, 128), dtype=torch.bfloat16, device=dev)),
+        dict(L=512),                                   # streams hold 256 tokens
+        dict(vs=streams(2, 256, 4)),                   # V with other heads
+        dict(ks=(ks[0], None, ks[2])),                 # full mode without residuals
+        dict(ks=(ks[0], ks[1], torch.empty(1, device=dev))),
+        dict(need=1 << 21),                            # workspace too small
+    ]
+    for b in bad:
+        a = dict(q=q, ks=ks, vs=vs, L=256, out=good_out, need=1024)
+        a.update(b)
+        with pytest.raises(ValueError):
+            check("t", a["q"], a["ks"], a["vs"], a["L"], 128, 32, lynx.LYNX_FULL, a["out"], ws,
+                  a["need"])
+    with pytest.raises(ValueError):
+        lynx._expect(torch.empty((4,), device=dev), (4,), torch.float32,
+                     torch.device("cuda", 0), "device")

@@ -55,6 +55,12 @@ CASES = [
     (1, 768, 3, 256, 128),
     (5, 384, 1, 128, 16),
     (2, 320, 3, 64, 32),       # five pages of 64
+    # 512-token pages (the largest page of the pages' ablation grid): two
+    # TMA loads per tile, two decode units per page
+    (2, 1024, 3, 512, 16),
+    (1, 1536, 2, 512, 32),
+    (2, 1024, 1, 512, 64),
+    (1, 1024, 2, 512, 128),
 ]
 
 

@@ -84,7 +84,8 @@ def test_int_baseline_at_scale_on_samples(lynx_lib, oracle_mod, cuda_dev):
         del codes, meta
 
 
-CASES = [(2, 512, 2, 128, 32), (1, 512, 3, 256, 64), (3, 256, 1, 64, 16), (2, 384, 2, 128, 128)]
+CASES = [(2, 512, 2, 128, 32), (1, 512, 3, 256, 64), (3, 256, 1, 64, 16), (2, 384, 2, 128, 128),
+         (1, 1024, 2, 512, 32), (2, 1024, 1, 512, 16)]
 
 
 @pytest.mark.parametrize("k", [3, 4, 5, 6])
