@@ -37,6 +37,7 @@
 #include <stdio.h>
 
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -1111,24 +1112,57 @@ namespace lynx {
 constexpr size_t kNoAllocScratchBytes = (size_t)8 << 20;
 static __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
 
-// Device address of g_attn_scratch for the current device, looked up once
-// per device (cudaGetSymbolAddress with that device current) and cached.
+// Unique id of the calling thread's current CUDA context (cuCtxGetId ids are
+// never reused within a process), through the runtime's driver entry points
+// (the library does not link the driver library); 0 if unavailable.
+static unsigned long long current_context_id() {
+  using GetCurrentFn = CUresult (*)(CUcontext*);
+  using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static const auto fns = [] {
+    void* cur = nullptr;
+    void* id = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &cur, 12000, cudaEnableDefault,
+                                         &q1) != cudaSuccess || q1 != cudaDriverEntryPointSuccess)
+      cur = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &id, 12000, cudaEnableDefault, &q2) !=
+            cudaSuccess || q2 != cudaDriverEntryPointSuccess)
+      id = nullptr;
+    return std::make_pair(reinterpret_cast<GetCurrentFn>(cur), reinterpret_cast<GetIdFn>(id));
+  }();
+  if (!fns.first || !fns.second) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long v = 0;
+  if (fns.first(&ctx) != CUDA_SUCCESS || !ctx || fns.second(ctx, &v) != CUDA_SUCCESS) return 0;
+  return v;
+}
+
+// Device address of g_attn_scratch for the current device: looked up with
+// cudaGetSymbolAddress (that device current) on the first call and again
+// whenever the device's context has changed since (after cudaDeviceReset the
+// old address belongs to a destroyed context), else taken from the cache.
 static cudaError_t noalloc_scratch(void** ptr) {
   constexpr int kMaxDev = 64;
-  static void* addr[kMaxDev] = {};
+  struct Entry {
+    unsigned long long ctx;
+    void* addr;
+  };
+  static Entry cache[kMaxDev] = {};
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+  if (!cache[dev].addr || ctx == 0 || cache[dev].ctx != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_attn_scratch);
     if (e != cudaSuccess) return e;
-    addr[dev] = p;
+    // the lookup initialises the context if it was not yet: record its id
+    cache[dev] = Entry{ctx != 0 ? ctx : current_context_id(), p};
   }
-  *ptr = addr[dev];
+  *ptr = cache[dev].addr;
   return cudaSuccess;
 }
 
