@@ -951,7 +951,7 @@ def accuracy_table(K, V, q, P=128, C=32, alpha=255.0, sweep=True):
 
 # page sizes of the ablation sweep ([Review], Concrete Improvement
 # Suggestions, item 4)
-SWEEP_PAGES = (128, 256)
+SWEEP_PAGES = (128, 256, 512)
 
 
 def measure_variants(c, kv, anc, res, meta, dev, reps=5):

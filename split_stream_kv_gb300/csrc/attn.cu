@@ -158,9 +158,6 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
   return r;
 }
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-  asm volatile("prefetch.global.L2 [%0];" :: "l"(p));
-}
 // Table reads.  The table is written once before the first barrier and never
 // again, so these loads carry no ordering against other memory operations.
 __device__ __forceinline__ float2 lut_f2(uint32_t off) {
@@ -365,9 +362,9 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   const int64_t* seg_blk =
       reinterpret_cast<const int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo);
   // Paged streams: a two-entry cache of (table row -> page) per lane.  Chunks
-  // walk pages in order and the L2 prefetch two chunks ahead meets each new
-  // page first, so the loads that need a chunk's address rarely wait on the
-  // table.
+  // walk pages in order, so a table entry is read once per page.  (Prefetching
+  // the codes two chunks ahead into L2 was measured and dropped: verification
+  // ran 4 % faster dense and 8 % faster paged without it, the draft the same.)
   int64_t c_row0 = -1, c_pg0 = 0, c_row1 = -1, c_pg1 = 0;
   auto page_of = [&](int64_t row) -> int64_t {
     if (row == c_row1) return c_pg1;
@@ -474,22 +471,6 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       vA[ii].load(a.va + code_off + row * 64 + hb + VB * g);
       if constexpr (FULL) vR[ii].load(a.vr + code_off + row * 64 + hb + VB * g);
     }
-    // ---- warm L2 with the codes and constant rows two chunks ahead
-    if (left > 2 && qc + 2 < a.NCH) {
-      int tp2;
-      const int64_t blk2 = chunk_blk(sg, qc + 2, tp2);
-      const int64_t off2 = (blk2 * a.P + tp2) * (kD / 2) + lane * 64;
-      prefetch_l2(a.ka + off2);
-      prefetch_l2(a.va + off2);
-      if constexpr (FULL) {
-        prefetch_l2(a.kr + off2);
-        prefetch_l2(a.vr + off2);
-      }
-      const int cc = tp2 >> a.lgC, rsel = lane >> 3;  // mu, sigma rows of K and V
-      const float* mb = ((rsel & 2) ? a.vm : a.km) + blk2 * (int64_t)meta_rows * kD;
-      prefetch_l2(mb + (2 + ((rsel & 1) ? a.NC : 0) + cc) * kD + (lane & 7) * 16);
-    }
-
     // ---- scores: S^T for m-tiles j = 0, 1 (tokens 16j .. 16j+15)
     cp_wait<1>();  // constants of K for this chunk have landed
     __syncwarp();
@@ -975,19 +956,20 @@ attn_combine(const __grid_constant__ AttnParams a, int RP) {
 static int rows_per_pass(int R) { return R <= 8 ? 8 : 32; }
 static int row_groups(int R) { const int rp = rows_per_pass(R); return (R + rp - 1) / rp; }
 
-// CTAs of the attention grid.  Every shape runs two CTAs per SM, so the
-// 152 SMs of a GB300 hold 304 at once: one wave of equal shares of the
-// flattened (unit, chunk) space, with at least 2 chunks per work unit (8 of
-// them per CTA up to 8 query rows, 2 warp pairs above), and at least one CTA
-// per unit so that a share never exceeds one unit's chunks (several waves
-// when there are more units than that).  Device independent, so the
-// workspace size is a pure function of the shapes.
-constexpr int kGB300SMs = 152;
-static int ctas_for(int batch, int Hkv, int nrg, int64_t NCH, int R) {
+// CTAs of the attention grid.  Every shape runs two CTAs per SM, so `sms`
+// SMs hold 2 sms at once: one wave of equal shares of the flattened
+// (unit, chunk) space, with at least 2 chunks per work unit (8 of them per
+// CTA up to 8 query rows, 2 warp pairs above), and at least one CTA per unit
+// so that a share never exceeds one unit's chunks (several waves when there
+// are more units than that).  The launch takes the device's SM count, capped
+// at kMaxWaveSMs; the workspace is sized for that cap, so its size is a pure
+// function of the shapes and holds the partials on any device.
+constexpr int kMaxWaveSMs = 256;
+static int ctas_for(int batch, int Hkv, int nrg, int64_t NCH, int R, int sms) {
   const int64_t units = (int64_t)batch * Hkv * nrg;
   const int64_t n_chunks = units * NCH;
   const int64_t nu = R <= 8 ? 8 : 2;
-  int64_t n = (int64_t)kGB300SMs * 2;
+  int64_t n = (int64_t)(sms < kMaxWaveSMs ? sms : kMaxWaveSMs) * 2;
   if (n > n_chunks / (2 * nu)) n = n_chunks / (2 * nu);
   if (n < units) n = units;
   return (int)n;
@@ -995,11 +977,11 @@ static int ctas_for(int batch, int Hkv, int nrg, int64_t NCH, int R) {
 
 // Workspace: two partials per CTA (its segments) and one parked state per
 // CTA (a work unit's state for the first unit when its run crosses into the
-// second).
+// second), for the largest grid any device can launch.
 size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L) {
   const int R = (H_q / H_kv) * T;
   const int RP = rows_per_pass(R), nrg = row_groups(R);
-  const int n = ctas_for(batch, H_kv, nrg, L / 32, R);
+  const int n = ctas_for(batch, H_kv, nrg, L / 32, R, kMaxWaveSMs);
   return (size_t)3 * n * (2 * RP + RP * kD) * sizeof(float);
 }
 
@@ -1079,7 +1061,7 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
   prm.NB = x.s.NB();
   prm.NCH = x.s.L / 32;
   prm.n_chunks = (int64_t)x.batch * prm.Hkv * prm.nrg * prm.NCH;
-  prm.n_cta = ctas_for(x.batch, prm.Hkv, prm.nrg, prm.NCH, prm.R);
+  prm.n_cta = ctas_for(x.batch, prm.Hkv, prm.nrg, prm.NCH, prm.R, sm_count());
   prm.P = x.s.page;
   prm.C = x.s.C;
   prm.NC = x.s.NC();
