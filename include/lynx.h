@@ -352,7 +352,11 @@ int lynx_spec_verify(const float *p_target, const float *q_draft,
  * library in this process has reported: 1 = a bounded wait on an
  * asynchronous copy gave up (the kernel returned early, its outputs are
  * incomplete), 2 = a block-table entry was outside [0, num_blocks), 4 = a
- * draft token of lynx_spec_verify was outside [0, V). */
+ * draft token of lynx_spec_verify was outside [0, V), 8 = (checked build
+ * only, liblynx_checked.so, the same sources compiled with -DLYNX_CHECKED) an
+ * index that a kernel computed for a global access fell outside the extent the
+ * call's shapes give; the index was replaced by 0, so the outputs are wrong
+ * but nothing outside the buffers was touched. */
 int lynx_device_errors(unsigned int *bits);
 
 /* Host-only.  Device workspace (bytes) that lynx_attn_decode needs for these

@@ -1,5 +1,7 @@
 """Build liblynx.so in-tree: each csrc/*.cu compiled by nvcc for sm_103a in
-parallel, then linked into one shared library next to this file."""
+parallel, then linked into one shared library next to this file.  The same
+sources compiled with -DLYNX_CHECKED give liblynx_checked.so, the checked
+build whose kernels verify their index arithmetic (see common.cuh)."""
 from __future__ import annotations
 
 import glob
@@ -13,6 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_objs")
 LIB = os.path.join(HERE, "liblynx.so")
+OBJ_CHECKED = os.path.join(HERE, "_objs_checked")
+LIB_CHECKED = os.path.join(HERE, "liblynx_checked.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -49,43 +53,57 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link if anything changed; return the library path."""
-    os.makedirs(OBJ, exist_ok=True)
-    nvcc = _nvcc()
+def _build_one(lib: str, objdir: str, extra, force: bool, verbose: bool, pool) -> list:
+    """Compile jobs for one library (the stale objects) and the link step."""
+    os.makedirs(objdir, exist_ok=True)
     hdrs = _headers()
-    jobs = []
-    objs = []
+    objs, jobs = [], []
     for src in _sources():
-        obj = os.path.join(OBJ, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs):
-            jobs.append((src, obj))
+            jobs.append((src, obj, extra))
+    return objs, jobs
 
-    def compile_one(job):
-        src, obj = job
-        tmp = obj + f".tmp{os.getpid()}"
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", tmp]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
-        os.replace(tmp, obj)
-        return r.stderr
 
-    if jobs:
-        with ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
-            for log in ex.map(compile_one, jobs):
-                if verbose and log:
-                    sys.stderr.write(log)
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
+def _compile_one(job, verbose=False):
+    src, obj, extra = job
+    tmp = obj + f".tmp{os.getpid()}"
+    cmd = [_nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", tmp]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr}")
+    os.replace(tmp, obj)
+    return r.stderr
+
+
+def _link(lib: str, objs, force: bool, built: bool):
+    if force or built or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
+        cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose: bool = False, checked: bool = True) -> str:
+    """Compile and link if anything changed; return the library path.  With
+    `checked`, also the checked build (compiled in the same parallel pass)."""
+    targets = [(LIB, OBJ, [])]
+    if checked:
+        targets.append((LIB_CHECKED, OBJ_CHECKED, ["-DLYNX_CHECKED"]))
+    plans = [(lib, *_build_one(lib, od, extra, force, verbose, None)) for lib, od, extra in targets]
+    jobs = [j for _, _, js in plans for j in js]
+    if jobs:
+        with ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+            for log in ex.map(lambda j: _compile_one(j, verbose), jobs):
+                if verbose and log:
+                    sys.stderr.write(log)
+    for lib, objs, js in plans:
+        _link(lib, objs, force, bool(js))
     return LIB
 
 

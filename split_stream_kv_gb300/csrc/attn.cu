@@ -385,9 +385,11 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     const int p = t0 >> a.lgP;
     tp = t0 & (a.P - 1);
     if constexpr (PAGED) {  // the table names the physical page
-      return page_of(seg_blk[sg] + p) * a.Hkv + seg_blk[2 + sg];
+      return checked_index(page_of(seg_blk[sg] + p) * a.Hkv + seg_blk[2 + sg], a.nphys * a.Hkv,
+                           &g_attn_flags);
     } else {
-      return seg_blk[sg] + p * a.Hkv;
+      return checked_index(seg_blk[sg] + p * a.Hkv, (int64_t)a.batch * a.NB * a.Hkv,
+                           &g_attn_flags);
     }
   };
   // Asynchronous copies of the constant rows of chunk qc into the warp's
@@ -915,7 +917,8 @@ attn_combine(const __grid_constant__ AttnParams a, int RP) {
       const int k = kb + i;
       if (k <= k1) {
         const int64_t seg = z - (a.n_chunks * k / a.n_cta) / a.NCH;
-        const float* ps = a.part + (2 * k + seg) * part_floats;
+        const float* ps = a.part + checked_index(2 * k + seg, 2 * (int64_t)a.n_cta,
+                                                 &g_attn_flags) * part_floats;
         mv[i] = ps[r];
         lv[i] = ps[RP + r];
         ov[i] = *reinterpret_cast<const float4*>(ps + 2 * RP + r * kD + 4 * lane);

@@ -99,6 +99,29 @@ __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
 constexpr unsigned kFlagWaitTimeout = 1u;   // a bounded wait gave up
 constexpr unsigned kFlagBadBlock = 2u;      // a block-table entry was out of range
 constexpr unsigned kFlagBadToken = 4u;      // a draft token was outside the vocabulary
+constexpr unsigned kFlagIndexCheck = 8u;    // checked build: an index check failed
+
+// The checked build (compiled with -DLYNX_CHECKED) verifies the index
+// arithmetic of every kernel at the points where it addresses global memory
+// (TMA coordinates, bulk-copy offsets, block and row indices) against the
+// extents that the call's shapes give.  An index outside [0, n) is recorded in
+// *flag (bit kFlagIndexCheck, read through lynx_device_errors) and replaced by
+// 0, so a bad index gives wrong numbers, never a stray access.  In the
+// regular build the check compiles to nothing.
+#ifdef LYNX_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+__device__ __forceinline__ int64_t checked_index(int64_t i, int64_t n, unsigned int* flag) {
+  if constexpr (kChecked) {
+    if (i < 0 || i >= n) {
+      atomicOr(flag, kFlagIndexCheck);
+      return 0;
+    }
+  }
+  return i;
+}
 
 // Physical page block of logical block blk = (b*NB + p)*H + h.  Without a
 // block table the streams are dense and the two coincide; with one, row

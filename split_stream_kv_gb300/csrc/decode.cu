@@ -147,7 +147,8 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
 
   auto issue = [&](int64_t un, int stage) {
     const int64_t part = un % parts;
-    const int64_t blk = phys_block(bt, nphys, un / parts, H, &g_dec_wait_timeout);
+    const int64_t blk = checked_index(phys_block(bt, nphys, un / parts, H, &g_dec_wait_timeout),
+                                      bt ? nphys * H : nblk, &g_dec_wait_timeout);
     uint8_t* st = stages + stage * stage_bytes;
     const int64_t code_off = (blk * parts + part) * code_bytes;
     mbar_expect_tx(&bars[stage], stage_bytes);
@@ -190,7 +191,9 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
     const int64_t blk = un / parts, part = un % parts;
     const int64_t h = blk % H, rest = blk / H;
     const int64_t p = rest % NB, b = rest / NB;
-    const int64_t orow0 = ((b * L + p * P + part * U + t0) * H + h) * kD + 8 * g;
+    const int64_t row0 = checked_index(b * L + p * P + part * U + t0, nblk / H * P - run + 1,
+                                       &g_dec_wait_timeout);
+    const int64_t orow0 = (row0 * H + h) * kD + 8 * g;
 
     if constexpr (FULL) {
       // pairs (k, k+1) in channel order

@@ -176,15 +176,18 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
   }
   __syncthreads();
 
+  const int64_t rows_total = nunit / G::kUnits / H * P;   // B * L rows of the BF16 view
   auto issue = [&](int64_t u, int stage) {
     const int64_t blk = u / G::kUnits, half = u % G::kUnits;
     const int64_t h = blk % H, rest = blk / H;
     const int64_t p = rest % NB, b = rest / NB;
+    const int64_t x = checked_index(h * kD + half * W, (int64_t)H * kD - W + 1, &g_wait_timeout);
+    const int64_t y = checked_index(b * L + p * P, rows_total - P + 1, &g_wait_timeout);
     mbar_expect_tx(&bars[stage], G::kTileBytes);
 #pragma unroll
     for (int r0 = 0; r0 < P; r0 += 256)   // a box is at most 256 rows
-      tma_load_2d(tiles + stage * G::kTileBytes + r0 * G::kRowBytes, &tmap,
-                  (int32_t)(h * kD + half * W), (int32_t)(b * L + p * P + r0), &bars[stage]);
+      tma_load_2d(tiles + stage * G::kTileBytes + r0 * G::kRowBytes, &tmap, (int32_t)x,
+                  (int32_t)(y + r0), &bars[stage]);
   };
   if (tid == 0)
     for (int i = 0; i < G::kStages; ++i) {
@@ -269,7 +272,8 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
       }
     }
 
-    const int64_t pb = phys_block(bt, nphys, blk, H, &g_wait_timeout);  // output block
+    const int64_t pb = checked_index(phys_block(bt, nphys, blk, H, &g_wait_timeout),
+                                     bt ? nphys * H : nunit / G::kUnits, &g_wait_timeout);
     float* mrow = meta + pb * (int64_t)(G::kMetaRows * kD) + 8 * wofs;
     uint32_t* arow = anchor + pb * (int64_t)(P * 16) + wofs;
     uint32_t* rrow = residual + pb * (int64_t)(P * 16) + wofs;

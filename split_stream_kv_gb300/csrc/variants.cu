@@ -327,6 +327,7 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
   const float* xl = xk + lane;
 
   auto issue = [&](int64_t un, int stage) {
+    un = checked_index(un, nunit, &g_variant_wait_timeout);
     const int64_t blk = un / parts, part = un % parts;
     uint8_t* st = stages + stage * stage_bytes;
     mbar_expect_tx(&bars[stage], stage_bytes);
@@ -375,7 +376,9 @@ decode_anchor_bits_kernel(const uint8_t* __restrict__ ak, const float* __restric
     const int64_t blk = un / parts, part = un % parts;
     const int64_t h = blk % H, rest = blk / H;
     const int64_t p = rest % NB, b = rest / NB;
-    const int64_t orow0 = ((b * L + p * P + part * U + t0) * H + h) * kD + 8 * G;
+    const int64_t row0 = checked_index(b * L + p * P + part * U + t0, nblk / H * P - run + 1,
+                                       &g_variant_wait_timeout);
+    const int64_t orow0 = (row0 * H + h) * kD + 8 * G;
 #pragma unroll 4
     for (int r = 0; r < run; ++r) {
       const uint32_t o = (uint32_t)((t0 + r) * 16 + G) * K;

@@ -12,7 +12,11 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "liblynx.so")
+# LYNX_LIBRARY=checked selects the checked build (liblynx_checked.so: kernels
+# that verify their index arithmetic and report a failed check through
+# lynx_device_errors); the default is the regular build.
+LIB_PATH = os.path.join(_HERE, "liblynx_checked.so" if os.environ.get("LYNX_LIBRARY") == "checked"
+                        else "liblynx.so")
 
 LYNX_OK, LYNX_EINVAL, LYNX_ESHAPE, LYNX_EUNSUPPORTED, LYNX_ECUDA, LYNX_EWORKSPACE = (
     0, -1, -2, -3, -4, -5)

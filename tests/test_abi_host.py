@@ -29,6 +29,17 @@ def test_library_exports_every_declared_symbol(lynx_lib):
         assert hasattr(lynx_lib, n), n
 
 
+def test_checked_build_exports_every_declared_symbol(lynx_lib):
+    """liblynx_checked.so (the same sources with in-kernel index checks) is
+    built beside the regular library and exports the same C ABI."""
+    import ctypes
+
+    from split_stream_kv_gb300 import _build
+    lib = ctypes.CDLL(_build.LIB_CHECKED)
+    for n in declared_symbols():
+        assert hasattr(lib, n), n
+
+
 def test_encoded_sizes(lynx_lib):
     # Llama-3-8B-shaped: 32 layers x K,V, L=16384, 8 heads, page 128, C 32
     a, r, m = lynx_lib.lynx_encoded_sizes(64, 16384, 8, 128, 128, 32)
