@@ -369,10 +369,15 @@ int lynx_attn_workspace_bytes(int batch, int T, int H_q, int64_t L, int H_kv,
  *   O = softmax(q K^T / sqrt(D)) V
  * for every sequence, query row and query head, grouped-query: query head hq
  * reads KV head hq / (H_q / H_kv).  K and V are reconstructed in registers
- * exactly as lynx_decode_anchor (mode LYNX_ANCHOR, the draft step of
- * [Review, Mechanism 2, Anchor Phase]) or lynx_decode_full (LYNX_FULL, the
- * T-token verification pass of [Review, Mechanism 3]) would with BF16 output;
- * every one of the T query rows attends to all L cached tokens.
+ * as lynx_decode_anchor (mode LYNX_ANCHOR, the draft step of [Review,
+ * Mechanism 2, Anchor Phase]) or lynx_decode_full (LYNX_FULL, the T-token
+ * verification pass of [Review, Mechanism 3]) would with BF16 output, the
+ * affine map applied as one fused multiply-add x = fma(v, A, B) with
+ * A = (sigma + eps)(gamma_scale + eps), B = fma(mu, gamma_scale + eps,
+ * gamma_min) per chunk and channel (the decoders use two; the BF16 operands
+ * then differ from the decoders' on about 2e-4 of the values, by one BF16 ulp
+ * or by 2^-22 of the channel's gamma_scale, far inside the attention
+ * tolerance); every one of the T query rows attends to all L cached tokens.
  *   q          [batch][T][H_q][D] BF16, device
  *   k_*, v_*   the encode outputs of the K and V tensors [batch][L][H_kv][D]
  *              (B = batch); k_residual / v_residual may be NULL in ANCHOR mode

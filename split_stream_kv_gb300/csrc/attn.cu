@@ -4,9 +4,15 @@
 // step over Anchor codes (Mechanism 2, Anchor Phase) and the T-token
 // verification pass over Anchor + Residual (Mechanism 3).
 //
-// K and V are reconstructed in registers exactly as the decoders do with BF16
-// output (same lookup values, same two fused multiply-adds, round to nearest
-// even), then fed to mma.sync m16n8k16 (bf16 x bf16 -> f32):
+// K and V are reconstructed in registers from the decoders' lookup values
+// with one fused multiply-add, x = fma(v, A, B), A = (sigma + eps)(gamma_scale
+// + eps) and B = fma(mu, gamma_scale + eps, gamma_min) built once per chunk and
+// channel, then rounded to nearest even BF16, and fed to mma.sync m16n8k16
+// (bf16 x bf16 -> f32).  The decoders apply the same affine map as two fused
+// multiply-adds; the two float32 results differ by at most 2^-22 of the
+// channel's gamma_scale + eps, so their BF16 roundings differ on about 2e-4 of
+// the values: by one BF16 ulp, or, for a value that nearly cancels to zero in
+// its channel, by that 2^-22 of the range.
 //   scores  S^T[token][row] = K^[token][:] . q[row][:]     (A = K^, B = Q^T)
 //   output  O^T[ch][row]   += V^[:][ch]^T . P^T[:][row]    (A = V^T, B = P^T)
 // A query "row" is one (query token, query head of the group).
@@ -69,11 +75,18 @@ struct Cfg {
   // C >= 32: two CTAs = 16 warps per SM), else 4 warps at up to 255.
   static constexpr int kWarps = (!FULL && !PAIR && ONE) ? 8 : 4;
   static constexpr int kNU = PAIR ? kWarps / 2 : kWarps;  // work units
-  // Constant rows per tensor: gamma_min, gamma_scale, then (mu, sigma) of
-  // the chunk of each 16-token half (one pair when C >= 32).
-  static constexpr int kRows = ONE ? 4 : 6;
+  // Constant rows per tensor in the table tails: the one-FMA decode constants
+  // (A, B) of the chunk of each 16-token half (one pair when C >= 32), in the
+  // (k, k+4) channel pairs of the nibble layout.
+  static constexpr int kRows = ONE ? 2 : 4;
   static constexpr int kTails = 2 * kRows * 4;  // per warp: K then V, 4 tails a row
-  static_assert(kWarps * kTails <= 256, "constant rows fit the table tails");
+  // Raw metadata rows per tensor, in channel order: gamma_min, gamma_scale,
+  // then (mu, sigma) of each 16-token half.  A warp pair stages them in the
+  // free tails (a row of its 64 channels is 2 tails), a single warp (128
+  // channels, 512-byte rows) in the extra region.
+  static constexpr int kRawRows = ONE ? 4 : 6;
+  static constexpr int kRawTails = PAIR ? 2 * kRawRows * 2 : 0;
+  static_assert(kWarps * (kTails + kRawTails) <= 256, "constant rows fit the table tails");
 };
 
 // Bytes after the table: during the chunk loop the staged Q fragments (one
@@ -87,8 +100,10 @@ struct ExtraLayout {
   static constexpr size_t kQ = (size_t)2 * kHalves * NKT * NT * 32 * 8;  // [seg][half][kt][nt][lane]
   static constexpr size_t kXchg = PAIR ? (size_t)CF::kWarps * 2 * 32 * 8 * NT * 4 : 0;
   static constexpr size_t kInfo = kQ + kXchg;  // int64 page-row base and head of segments 0, 1
-  static_assert(kLutBytes + kInfo + 32 + 1024 <= 116 * 1024, "two CTAs per SM");
-  static constexpr size_t kLoop = kInfo + 32;
+  static constexpr size_t kRaw = kInfo + 32;   // single warps: raw rows, [warp][K, V][row][512 B]
+  static constexpr size_t kRawBytes = PAIR ? 0 : (size_t)CF::kWarps * 2 * CF::kRawRows * 512;
+  static_assert(kLutBytes + kRaw + kRawBytes <= 113 * 1024, "two CTAs per SM");
+  static constexpr size_t kLoop = kRaw + kRawBytes;
   static constexpr size_t kMerge = (size_t)CF::kNU * 8 * NT * (2 + kD) * 4 + (size_t)CF::kNU * 8;
   static constexpr size_t kBytes = kLoop > kMerge ? kLoop : kMerge;
 };
@@ -174,6 +189,10 @@ static_assert(kSmemBase == 1024, "immediate offset of the table loads");
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
 }
+// 16-byte asynchronous copy global -> shared, cached in L2 only.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_wait() {
@@ -205,28 +224,23 @@ struct Bytes<4> {
   }
 };
 
-// Constants of two nibble positions (2hh, 2hh+1) of one channel group: the
-// pairs (k, k+4) for k = 2hh, 2hh+1, with epsilon added to both scales.
+// One-FMA decode constants of two nibble positions (2hh, 2hh+1) of one
+// channel group: the pairs (k, k+4) for k = 2hh, 2hh+1 of
+// A = (sigma + eps)(gamma_scale + eps) and B = fma(mu, gamma_scale + eps, gamma_min).
 struct Half {
-  f2 gm[2], gs[2], mu[2], sg[2];
+  f2 A[2], B[2];
 };
 // gb: byte offset of unit 0 of the group in row 0 (unit_off(tb, 0, grp, 0)).
+// Rows 2 jrow and 2 jrow + 1 hold A and B of the chunk of token half jrow.
 __device__ __forceinline__ void load_half(Half& k, const uint8_t* smem, uint32_t gb, int jrow,
                                           int hh) {
   const uint8_t* p = smem + gb + hh * 16;
-  const float4 g = *reinterpret_cast<const float4*>(p);
-  const float4 s = *reinterpret_cast<const float4*>(p + kRowStride);
-  const float4 m = *reinterpret_cast<const float4*>(p + (2 + 2 * jrow) * kRowStride);
-  const float4 a = *reinterpret_cast<const float4*>(p + (3 + 2 * jrow) * kRowStride);
-  const f2 e = make_float2(kEps, kEps);
-  k.gm[0] = make_float2(g.x, g.y);
-  k.gm[1] = make_float2(g.z, g.w);
-  k.gs[0] = add2(make_float2(s.x, s.y), e);
-  k.gs[1] = add2(make_float2(s.z, s.w), e);
-  k.mu[0] = make_float2(m.x, m.y);
-  k.mu[1] = make_float2(m.z, m.w);
-  k.sg[0] = add2(make_float2(a.x, a.y), e);
-  k.sg[1] = add2(make_float2(a.z, a.w), e);
+  const float4 a = *reinterpret_cast<const float4*>(p + (2 * jrow) * kRowStride);
+  const float4 b = *reinterpret_cast<const float4*>(p + (2 * jrow + 1) * kRowStride);
+  k.A[0] = make_float2(a.x, a.y);
+  k.A[1] = make_float2(a.z, a.w);
+  k.B[0] = make_float2(b.x, b.y);
+  k.B[1] = make_float2(b.z, b.w);
 }
 
 // Table offset of byte `pos` (0..3) of word w: [lane_off, w.b_pos, 0, 0].
@@ -256,7 +270,7 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t a, uint32_t r, uint32_
                                                  const Half& k) {
   constexpr int i = POS & 1;
   const f2 v = lookup_pair<FULL, POS>(a, r, lane_off);
-  const f2 x = fma2(fma2(v, k.sg[i], k.mu[i]), k.gs[i], k.gm[i]);
+  const f2 x = fma2(v, k.A[i], k.B[i]);
   return f2_to_bf2(x.x, x.y);
 }
 
@@ -358,6 +372,19 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   const int64_t ue = cta_b + (cta_e - cta_b) * (unit + 1) / NU;
   const int meta_rows = 2 + 2 * a.NC;
   const int tbK = w * CF::kTails, tbV = tbK + CF::kRows * 4;
+  // raw rows: piece q (16 bytes, channels 4q..4q+3 of the warp's range) of row
+  // r of tensor t; pieces are xor-swizzled by bit 3 so that the build's reads
+  // of groups g and g + 4 land in different banks
+  auto raw_off = [&](int t, int r, int q) -> uint32_t {
+    const int qs = q ^ ((q >> 3) & 1);
+    if constexpr (PAIR) {
+      const int tail = NW * CF::kTails + (w * 2 + t) * CF::kRawRows * 2 + r * 2 + (qs >> 3);
+      return (uint32_t)(tail * 256 + 128 + (qs & 7) * 16);
+    } else {
+      return (uint32_t)(kLutBytes + ExtraLayout<FULL, PAIR, ONE, NT>::kRaw +
+                        ((w * 2 + t) * CF::kRawRows + r) * 512 + qs * 16);
+    }
+  };
   // Packed block (sequence, page, KV head) of chunk qc of segment sg.
   const int64_t* seg_blk =
       reinterpret_cast<const int64_t*>(extra + ExtraLayout<FULL, PAIR, ONE, NT>::kInfo);
@@ -392,30 +419,54 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
                            &g_attn_flags);
     }
   };
-  // Asynchronous copies of the constant rows of chunk qc into the warp's
-  // rows of one tensor (gamma rows only with_gamma).  Each copy instruction
-  // fills one 128-byte tail (32 words, 32 banks): lane = slot * 8 + unit * 4
-  // + word, the slot holding group 4T + (slot ^ T) of tail T; the words are
-  // copied one by one so that the pairs (k, k+4) land side by side.
-  auto copy_consts = [&](const float* meta, int tb, int sg, int qc, bool with_gamma) {
+  // Asynchronous 16-byte copies of the raw metadata rows of chunk qc of one
+  // tensor (t: 0 = K, 1 = V) into the warp's staging rows (the gamma rows
+  // only with_gamma): a single warp copies one 512-byte row per instruction,
+  // a warp pair's warp two 256-byte rows.
+  auto copy_raw = [&](const float* meta, int t, int sg, int qc, bool with_gamma) {
     int tp;
     const int64_t blk = chunk_blk(sg, qc, tp);
     const int cc0 = tp >> a.lgC, cc1 = (tp + 16) >> a.lgC;
-    const float* mb = meta + blk * (int64_t)meta_rows * kD;
-    const int slot = lane >> 3, hu = (lane >> 2) & 1, pos = lane & 3;
-    const int ch_in = 2 * hu + (pos >> 1) + 4 * (pos & 1);  // channel within the group
+    const float* mb = meta + blk * (int64_t)meta_rows * kD + hb * 2;
+    constexpr int kPieces = KCH / 4;               // 16-byte pieces of a row
+    constexpr int kPerInst = 32 / kPieces;         // rows per copy instruction
+    const int q = lane % kPieces;
 #pragma unroll
-    for (int rr = 0; rr < CF::kRows; ++rr) {
+    for (int r0 = 0; r0 < CF::kRawRows; r0 += kPerInst) {
+      const int rr = r0 + lane / kPieces;
       if (rr < 2 && !with_gamma) continue;
       const int src = rr == 0 ? 0 : rr == 1 ? 1 : rr == 2 ? 2 + cc0 : rr == 3 ? 2 + a.NC + cc0
                     : rr == 4 ? 2 + cc1 : 2 + a.NC + cc1;
+      cp_async16(sbase + raw_off(t, rr, q), mb + src * kD + 4 * q);
+    }
+  };
+  // The (A, B) rows of one tensor from its raw rows (after they have landed):
+  // lane (group g, unit h) computes the channel pairs (2h, 2h+4) and
+  // (2h+1, 2h+5) of g, for each token half of the chunk.
+  auto build_ab = [&](int t, int tb) {
+    constexpr int kUnits = (KCH / 8) * 2;          // 32 (single warp) or 16 (pair)
+    constexpr int kJ = ONE ? 1 : 2;
+    const int u = lane % kUnits, jl = lane / kUnits;
+    const int gl = u >> 1, h = u & 1;
+    const int grp = hb / 4 + gl;
 #pragma unroll
-      for (int e = 0; e < GW / 4; ++e) {       // tails of the row this warp fills
-        const int T = hb / 16 + e;
-        const int grp = 4 * T + (slot ^ (T & 3));
-        cp_async4(sbase + (uint32_t)((tb + rr * 4 + T) * 256 + 128 + lane * 4),
-                  mb + src * kD + 8 * grp + ch_in);
-      }
+    for (int j0 = 0; j0 < kJ; j0 += 32 / kUnits) {
+      const int j = j0 + jl;
+      if (j >= kJ) continue;
+      auto rd = [&](int r, int q) -> f2 {
+        return *reinterpret_cast<const float2*>(smem + raw_off(t, r, q) + 8 * h);
+      };
+      const f2 e = make_float2(kEps, kEps);
+      const f2 gm_lo = rd(0, 2 * gl), gm_hi = rd(0, 2 * gl + 1);
+      const f2 gs_lo = add2(rd(1, 2 * gl), e), gs_hi = add2(rd(1, 2 * gl + 1), e);
+      const f2 mu_lo = rd(2 + 2 * j, 2 * gl), mu_hi = rd(2 + 2 * j, 2 * gl + 1);
+      const f2 sg_lo = add2(rd(3 + 2 * j, 2 * gl), e), sg_hi = add2(rd(3 + 2 * j, 2 * gl + 1), e);
+      const f2 A_lo = mul2(sg_lo, gs_lo), A_hi = mul2(sg_hi, gs_hi);
+      const f2 B_lo = fma2(mu_lo, gs_lo, gm_lo), B_hi = fma2(mu_hi, gs_hi, gm_hi);
+      const uint32_t ub = unit_off(tb, 2 * j, grp, h);
+      *reinterpret_cast<float4*>(smem + ub) = make_float4(A_lo.x, A_hi.x, A_lo.y, A_hi.y);
+      *reinterpret_cast<float4*>(smem + ub + kRowStride) =
+          make_float4(B_lo.x, B_hi.x, B_lo.y, B_hi.y);
     }
   };
 
@@ -446,9 +497,9 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   int sg = sg_start;
   int qc = (int)(ub - (u0 + sg) * a.NCH);
   if (ub < ue) {
-    copy_consts(a.km, tbK, sg, qc, true);
+    copy_raw(a.km, 0, sg, qc, true);
     cp_commit();
-    copy_consts(a.vm, tbV, sg, qc, true);
+    copy_raw(a.vm, 1, sg, qc, true);
     cp_commit();
     load_k(sg, qc);
   }
@@ -474,8 +525,12 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       if constexpr (FULL) vR[ii].load(a.vr + code_off + row * 64 + hb + VB * g);
     }
     // ---- scores: S^T for m-tiles j = 0, 1 (tokens 16j .. 16j+15)
-    cp_wait<1>();  // constants of K for this chunk have landed
+    cp_wait<1>();  // raw rows of K for this chunk have landed
     __syncwarp();
+    build_ab(0, tbK);
+    __syncwarp();  // (A, B) of K ready; its raw rows are free for the next chunk
+    if (has_next) copy_raw(a.km, 0, sg_n(), qc_n(), next_gamma());
+    cp_commit();
     float s[2][NT][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
@@ -520,11 +575,7 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       }
     }
     __syncwarp();  // every lane is done with this chunk's K constants and codes
-    if (has_next) {
-      load_k(sg_n(), qc_n());
-      copy_consts(a.km, tbK, sg_n(), qc_n(), next_gamma());
-    }
-    cp_commit();
+    if (has_next) load_k(sg_n(), qc_n());
 
     // ---- the warp's own n-tiles: all NT of them for a single warp; for a
     // warp pair, half of them each (tiles half*OWN .. +OWN-1), so that the
@@ -692,8 +743,12 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
     }
 
     // ---- output: O^T += V^T P^T over this warp's V m-tiles (byte VB*g + mt)
-    cp_wait<1>();  // constants of V for this chunk have landed
+    cp_wait<1>();  // raw rows of V for this chunk have landed
     __syncwarp();
+    build_ab(1, tbV);
+    __syncwarp();  // (A, B) of V ready; its raw rows are free for the next chunk
+    if (has_next) copy_raw(a.vm, 1, sg_n(), qc_n(), next_gamma());
+    cp_commit();
 #pragma unroll
     for (int gi = 0; gi < VB / 4; ++gi) {
       const int grp = (hb + VB * g) / 4 + gi;
@@ -733,8 +788,6 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       }
     }
     __syncwarp();  // every lane is done with this chunk's V constants
-    if (has_next) copy_consts(a.vm, tbV, sg_n(), qc_n(), next_gamma());
-    cp_commit();
 
     if (cross() && has_next) {
       // The run leaves unit u0 (only one work unit of a CTA can): park its
