@@ -186,9 +186,6 @@ __device__ __forceinline__ float lut_f1(uint32_t off) {
   return v;
 }
 static_assert(kSmemBase == 1024, "immediate offset of the table loads");
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(dst), "l"(src) : "memory");
-}
 // 16-byte asynchronous copy global -> shared, cached in L2 only.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst), "l"(src) : "memory");
@@ -285,7 +282,6 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
   constexpr int VB = KCH / 16;          // V bytes per token row per lane (g)
   constexpr int NU = CF::kNU;
   constexpr int RP = 8 * NT;            // query rows per pass
-  constexpr int GW = KCH / 8;           // channel groups per warp
 
   extern __shared__ __align__(16) uint8_t smem[];
   uint8_t* extra = smem + kLutBytes;
