@@ -2,21 +2,25 @@
 // for Disaggregated LLM Inference" (technical review, Mechanism 1, Stages 1-4)
 // as one persistent sm_103a kernel.
 //
-// Work unit: one page block = `page` tokens x 128 channels of one KV head.
-// A 2D TMA load stages the block's BF16 tile (page x 256 bytes, rows strided
-// by H*256 bytes in HBM) in shared memory; the next one or two tiles are in
+// Work unit: W channels of one page block (`page` tokens of one KV head; the
+// statistics are per channel, so a block splits into 128/W independent units).
+// A 2D TMA load stages the unit's BF16 tile (page x 2W bytes, rows strided by
+// H*256 bytes in HBM) in shared memory; the next one or two tiles are in
 // flight per CTA while the CTA computes on the current one.
 //
-// Thread layout for a block (2*page threads): every chunk of C tokens is
-// covered by C/16 warps, each owning a slice of 2048/C channels of all C
-// tokens, so a chunk's statistics never leave the warp.  In a warp, lane =
-// tl * CG + cg with TL = C/8 token lanes and CG = 256/C channel groups of 8
-// channels (16 bytes of a BF16 row, 4 bytes of each packed row); register m
-// holds chunk token i = TL*m + tl.  The chunk mean's pairwise-halving sum
-// (v[i] += v[i+h], h = C/2 .. 1) then reduces the register index first (the
-// top bits of i), then the token lanes by shuffles with h = TL/2 .. 1: exactly
-// the order the oracle uses.  Only the page minimum and maximum cross warps
-// (two block barriers per page block).
+// Thread layout: a warp owns a slice of a unit, one chunk of C tokens x
+// 2048/C channels, so a chunk's statistics never leave the warp.  In a warp,
+// lane = k * CG + cg with TL = C/8 token-lane slots k and CG = 256/C channel
+// groups of 8 channels (16 bytes of a BF16 row, 4 bytes of each packed row);
+// register m holds chunk token i = TL*m + tl(k).  The chunk mean's
+// pairwise-halving sum (v[i] += v[i+h], h = C/2 .. 1) then reduces the
+// register index first (the top bits of i), then the token lanes by shuffles
+// with h = TL/2 .. 1: exactly the order the oracle uses.  The token-lane
+// levels are a reduce-scatter: each level halves the channels a lane keeps,
+// so every lane finishes the statistics of 8/TL channels (one when TL >= 8)
+// and hands them to the other lanes through a small per-warp exchange in
+// shared memory.  The per-chunk minima and maxima reduce the same way.  Only
+// the page minimum and maximum cross warps (one block barrier per unit).
 //
 // Arithmetic, each step one IEEE binary32 rounding (no contraction):
 //   gmin = min x (a zero minimum as -0), gmax = max x, gs = gmax - gmin,
@@ -113,8 +117,17 @@ struct EncGeom {
   static constexpr int kRedFloats = kRedSets * 2 * kNC * kW;
   // page-statistic channels each token lane computes (of its group's 8)
   static constexpr int kCPL = kTL >= 8 ? 1 : 8 / kTL;
-  static constexpr size_t kSmem =
-      (size_t)kStages * kTileBytes + (size_t)kRedFloats * 4 + kStages * 8;
+  // reduce-scatter over the token lanes (the chunk sum's levels h = TL/2 .. 1):
+  // with 16 token lanes the first level is an all-reduce; every later level
+  // halves the channels a lane keeps (channel bit 2, then 1, then 0), so a
+  // lane ends with the kCPL channels whose statistics it finishes
+  static constexpr int kLevels = kTL == 2 ? 1 : kTL == 4 ? 2 : kTL == 8 ? 3 : 4;
+  static constexpr int kSplits = kLevels < 3 ? kLevels : 3;
+  static constexpr int kAllLevels = kLevels - kSplits;
+  // per-warp exchange of the finished statistics: [value][half][group][4]
+  static constexpr int kScrFloats = 32 * kCG;
+  static constexpr size_t kSmem = (size_t)kStages * kTileBytes + (size_t)kRedFloats * 4 +
+                                  (size_t)kWarps * kScrFloats * 4 + kStages * 8;
   static_assert(C >= 16 && C <= P, "chunk");
   static_assert(P >= 64 && P <= 512, "page");
   static_assert(kSlices % kWarps == 0 && kW * C % 2048 == 0, "slices");
@@ -146,6 +159,23 @@ __device__ __forceinline__ constexpr int enc_kxor(int hh) {
   return k;
 }
 
+// Lane-slot xor of level l of the token-lane reduction (token lanes tl and
+// tl ^ TL/2^(l+1)).
+template <int TL, int CG, bool SW>
+__device__ __forceinline__ constexpr int enc_level_xor(int l) {
+  return enc_kxor<TL, CG, SW>(TL >> (l + 1));
+}
+// First of the channels (of a group's 8) that lane slot k keeps after the
+// split levels: split s keeps the half whose channel bit 2 - s equals the
+// slot's bit at that level's xor.
+template <int TL, int CG, bool SW, int ALL, int SPLITS>
+__device__ __forceinline__ constexpr int enc_chan(int k) {
+  int base = 0;
+  for (int s = 0; s < SPLITS; ++s)
+    if (k & enc_level_xor<TL, CG, SW>(ALL + s)) base |= 4 >> s;
+  return base;
+}
+
 template <int P, int C>
 __global__ void __launch_bounds__(EncGeom<P, C>::kThreads, (EncGeom<P, C>::kThreads <= 256 ? 2 : 1))
 encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
@@ -158,11 +188,42 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* tiles = smem;
   float* red_mn = reinterpret_cast<float*>(smem + G::kStages * G::kTileBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(red_mn + G::kRedFloats);
+  float* scr_all = red_mn + G::kRedFloats;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scr_all + G::kWarps * G::kScrFloats);
 
   const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
   const int cg = lane % G::kCG, kl = lane / G::kCG;     // lane slot of the token lanes
   const int tl = enc_tl<G::kTL, G::kCG, G::kSwizzle>(kl);  // token offset in the chunk
+  constexpr int kAll = G::kAllLevels, kSp = G::kSplits, kCPL = G::kCPL;
+  // the kCPL channels of each group whose statistics this lane finishes
+  const int cbase = enc_chan<G::kTL, G::kCG, G::kSwizzle, kAll, kSp>(kl);
+  // one writer per channel (with an all-reduce level two lanes hold each)
+  const bool owner = kAll == 0 || (kl & enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(0)) == 0;
+  // which half a lane keeps at each split level
+  const bool kb0 = kSp >= 1 && (kl & enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll)) != 0;
+  const bool kb1 = kSp >= 2 && (kl & enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll + 1)) != 0;
+  const bool kb2 = kSp >= 3 && (kl & enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll + 2)) != 0;
+  // last split of the min / max words: keep {min, max} of channel bit kb2
+  const uint32_t sel_keep = kb2 ? 0x7632u : 0x5410u, sel_send = kb2 ? 0x5410u : 0x7632u;
+  // this warp's statistics exchange, [value][half][group][4]
+  float* scr = scr_all + w * G::kScrFloats;
+  auto scr_at = [&](int v, int j) { return scr + ((v * 2 + (j >> 2)) * G::kCG + cg) * 4 + (j & 3); };
+  // write this lane's kCPL values of statistic v, then (after a __syncwarp)
+  // read all 8 channels of the group as packed pairs
+  auto scr_put = [&](int v, const float* x) {
+    float* p = scr_at(v, cbase);
+    if constexpr (kCPL == 1) p[0] = x[0];
+    else if constexpr (kCPL == 2) *reinterpret_cast<float2*>(p) = make_float2(x[0], x[1]);
+    else *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+  };
+  auto scr_get = [&](int v, f2* out) {
+    const float4 a = *reinterpret_cast<const float4*>(scr_at(v, 0));
+    const float4 b = *reinterpret_cast<const float4*>(scr_at(v, 4));
+    out[0] = make_float2(a.x, a.y);
+    out[1] = make_float2(a.z, a.w);
+    out[2] = make_float2(b.x, b.y);
+    out[3] = make_float2(b.z, b.w);
+  };
 
   if (G::kSwizzle && (smem_u32(tiles) & 1023u) != 0u) {
     // the swizzled reads assume 1024-byte aligned tiles; the host checks the
@@ -232,24 +293,65 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
           mx[k] = m == 0 ? vv[k] : bf2_max(mx[k], vv[k]);
         }
       }
+      // across the token lanes: all-reduce levels, then split levels that
+      // leave each lane the extremes of its own kCPL channels
 #pragma unroll
-      for (int x = G::kCG; x < 32; x <<= 1)
+      for (int l = 0; l < kAll; ++l) {
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(l) * G::kCG;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           mn[k] = bf2_min(mn[k], __shfl_xor_sync(kFull, mn[k], x));
           mx[k] = bf2_max(mx[k], __shfl_xor_sync(kFull, mx[k], x));
         }
-      if (kl == 0) {
-        float4* pm = reinterpret_cast<float4*>(pmn + c * W + 8 * g);
-        float4* px = reinterpret_cast<float4*>(pmx + c * W + 8 * g);
-        const f2 a0 = bf2_to_f2(mn[0]), a1 = bf2_to_f2(mn[1]);
-        const f2 a2 = bf2_to_f2(mn[2]), a3 = bf2_to_f2(mn[3]);
-        pm[0] = make_float4(a0.x, a0.y, a1.x, a1.y);
-        pm[1] = make_float4(a2.x, a2.y, a3.x, a3.y);
-        const f2 b0 = bf2_to_f2(mx[0]), b1 = bf2_to_f2(mx[1]);
-        const f2 b2 = bf2_to_f2(mx[2]), b3 = bf2_to_f2(mx[3]);
-        px[0] = make_float4(b0.x, b0.y, b1.x, b1.y);
-        px[1] = make_float4(b2.x, b2.y, b3.x, b3.y);
+      }
+      if constexpr (kSp >= 1) {   // channel bit 2: words {0, 1} or {2, 3}
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll) * G::kCG;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint32_t smn = kb0 ? mn[j] : mn[j + 2], kmn = kb0 ? mn[j + 2] : mn[j];
+          const uint32_t smx = kb0 ? mx[j] : mx[j + 2], kmx = kb0 ? mx[j + 2] : mx[j];
+          mn[j] = bf2_min(kmn, __shfl_xor_sync(kFull, smn, x));
+          mx[j] = bf2_max(kmx, __shfl_xor_sync(kFull, smx, x));
+        }
+      }
+      if constexpr (kSp >= 2) {   // channel bit 1: word 0 or 1
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll + 1) * G::kCG;
+        const uint32_t smn = kb1 ? mn[0] : mn[1], kmn = kb1 ? mn[1] : mn[0];
+        const uint32_t smx = kb1 ? mx[0] : mx[1], kmx = kb1 ? mx[1] : mx[0];
+        mn[0] = bf2_min(kmn, __shfl_xor_sync(kFull, smn, x));
+        mx[0] = bf2_max(kmx, __shfl_xor_sync(kFull, smx, x));
+      }
+      float plo[kCPL], phi[kCPL];
+      if constexpr (kSp >= 3) {   // channel bit 0: one half of the min and max words
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll + 2) * G::kCG;
+        const uint32_t keep = prmt(mn[0], mx[0], sel_keep);   // {min, max} halves
+        const uint32_t r = __shfl_xor_sync(kFull, prmt(mn[0], mx[0], sel_send), x);
+        const uint32_t mm = prmt(bf2_min(keep, r), bf2_max(keep, r), 0x7610u);
+        plo[0] = __uint_as_float(mm << 16);
+        phi[0] = __uint_as_float(mm & 0xffff0000u);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kCPL / 2; ++j) {
+          const f2 a = bf2_to_f2(mn[j]), b = bf2_to_f2(mx[j]);
+          plo[2 * j] = a.x;
+          plo[2 * j + 1] = a.y;
+          phi[2 * j] = b.x;
+          phi[2 * j + 1] = b.y;
+        }
+      }
+      if (owner) {
+        float* pm = pmn + c * W + 8 * g + cbase;
+        float* px = pmx + c * W + 8 * g + cbase;
+        if constexpr (kCPL == 1) {
+          pm[0] = plo[0];
+          px[0] = phi[0];
+        } else if constexpr (kCPL == 2) {
+          *reinterpret_cast<float2*>(pm) = make_float2(plo[0], plo[1]);
+          *reinterpret_cast<float2*>(px) = make_float2(phi[0], phi[1]);
+        } else {
+          *reinterpret_cast<float4*>(pm) = make_float4(plo[0], plo[1], plo[2], plo[3]);
+          *reinterpret_cast<float4*>(px) = make_float4(phi[0], phi[1], phi[2], phi[3]);
+        }
       }
     }
     if (!__syncthreads_and(ok)) {
@@ -284,13 +386,13 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
       const int g = (slice % G::kSlicesPerChunk) * G::kCG + cg;
 
       // ---- Stage 1b: gamma_min, gamma_scale, reciprocal.  The token lanes
-      // that share a channel group split its 8 channels (kCPL each; with 16
-      // token lanes two lanes compute each channel) and exchange them by
-      // shuffles.
+      // that share a channel group split its 8 channels (kCPL each, the ones
+      // the reduce-scatter leaves them; with 16 token lanes two lanes compute
+      // each channel) and exchange them through the warp's exchange.
       float lo_q[G::kCPL], rg_q[G::kCPL];
 #pragma unroll
       for (int q = 0; q < G::kCPL; ++q) {
-        const int ch = 8 * g + ((kl * G::kCPL) & 7) + q;
+        const int ch = 8 * g + cbase + q;
         float lo = pmn[ch], hi = pmx[ch];
 #pragma unroll
         for (int cc = 1; cc < G::kNC; ++cc) {
@@ -304,21 +406,21 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
         const float gs = __fsub_rn(hi, lo);
         lo_q[q] = lo;
         rg_q[q] = __frcp_rn(__fadd_rn(gs, kEps));
-        if (c == 0 && kl * G::kCPL < 8) {   // one writer per channel
+        if (c == 0 && owner) {
           mrow[ch] = lo;
           mrow[kD + ch] = gs;
         }
       }
-      // ---- Stage 1c: n = (x - gmin) * rg for the thread's 8 tokens x 8 ch
-      f2 gm2[4], rg2[4];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {      // channel 8g + j comes from lane slot j / kCPL
-        const int src = (j / G::kCPL) * G::kCG + cg;
-        const float lo = __shfl_sync(kFull, lo_q[j % G::kCPL], src);
-        const float rg = __shfl_sync(kFull, rg_q[j % G::kCPL], src);
-        if (j & 1) { gm2[j >> 1].y = lo; rg2[j >> 1].y = rg; }
-        else       { gm2[j >> 1].x = lo; rg2[j >> 1].x = rg; }
+      // ---- Stage 1c: n = (x - gmin) * rg for the thread's 8 tokens x 8 ch,
+      // with every channel's gmin and rg from the warp's exchange
+      if (owner) {
+        scr_put(0, lo_q);
+        scr_put(1, rg_q);
       }
+      __syncwarp();
+      f2 gm2[4], rg2[4];
+      scr_get(0, gm2);
+      scr_get(1, rg2);
       f2 n[8][4];
 #pragma unroll
       for (int m = 0; m < 8; ++m) {
@@ -334,80 +436,84 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
         }
       }
 
-      // ---- Stage 2a: chunk mean, pairwise-halving order
-      f2 mu2[4];
+      // ---- Stage 2a: chunk mean, pairwise-halving order: the register
+      // index first, then the token lanes (all-reduce levels, then split
+      // levels that leave each lane the sums of its own kCPL channels)
+      f2 s[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         f2 t0 = add2(n[0][k], n[4][k]), t1 = add2(n[1][k], n[5][k]);
         f2 t2 = add2(n[2][k], n[6][k]), t3 = add2(n[3][k], n[7][k]);
         t0 = add2(t0, t2);
         t1 = add2(t1, t3);
-        f2 s = add2(t0, t1);
+        s[k] = add2(t0, t1);
+      }
+      auto shfl2 = [&](f2 v, int x) {
+        return make_float2(__shfl_xor_sync(kFull, v.x, x), __shfl_xor_sync(kFull, v.y, x));
+      };
 #pragma unroll
-        for (int hh = G::kTL / 2; hh >= 1; hh /= 2) {  // token lanes tl and tl ^ hh
-          const int x = enc_kxor<G::kTL, G::kCG, G::kSwizzle>(hh) * G::kCG;
-          f2 o;
-          o.x = __shfl_xor_sync(kFull, s.x, x);
-          o.y = __shfl_xor_sync(kFull, s.y, x);
-          s = add2(s, o);
+      for (int l = 0; l < kAll; ++l) {
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(l) * G::kCG;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s[k] = add2(s[k], shfl2(s[k], x));
+      }
+      if constexpr (kSp >= 1) {   // channel bit 2: pairs {0, 1} or {2, 3}
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll) * G::kCG;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const f2 snd = kb0 ? s[j] : s[j + 2], kp = kb0 ? s[j + 2] : s[j];
+          s[j] = add2(kp, shfl2(snd, x));
         }
-        mu2[k] = mul2(s, f2{inv_C, inv_C});
+      }
+      if constexpr (kSp >= 2) {   // channel bit 1: pair 0 or 1
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll + 1) * G::kCG;
+        const f2 snd = kb1 ? s[0] : s[1], kp = kb1 ? s[1] : s[0];
+        s[0] = add2(kp, shfl2(snd, x));
+      }
+      float mu_q[kCPL];
+      if constexpr (kSp >= 3) {   // channel bit 0: one of the pair
+        const int x = enc_level_xor<G::kTL, G::kCG, G::kSwizzle>(kAll + 2) * G::kCG;
+        const float snd = kb2 ? s[0].x : s[0].y, kp = kb2 ? s[0].y : s[0].x;
+        mu_q[0] = __fmul_rn(__fadd_rn(kp, __shfl_xor_sync(kFull, snd, x)), inv_C);
+      } else {
+#pragma unroll
+        for (int j = 0; j < kCPL / 2; ++j) {
+          mu_q[2 * j] = __fmul_rn(s[j].x, inv_C);
+          mu_q[2 * j + 1] = __fmul_rn(s[j].y, inv_C);
+        }
       }
 
       // ---- Stage 2b: d = n - mu; sigma = max |d| over the chunk.  Every
       // step x -> x - gmin -> * rg -> - mu rounds monotonically (rg > 0), so
       // the largest |d| is that of the chunk's largest or smallest x, which
-      // stage 1a left in the partials.
-      float sg[8];
-      {
-        const float4* pm = reinterpret_cast<const float4*>(pmn + c * W + 8 * g);
-        const float4* px = reinterpret_cast<const float4*>(pmx + c * W + 8 * g);
-        const float4 ma = pm[0], mb = pm[1], xa = px[0], xb = px[1];
-        const float lov[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
-        const float hiv[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+      // stage 1a left in the partials.  Each lane finishes sigma and
+      // rs = rn(1/(sigma + eps)) of its own channels; the warp's exchange
+      // hands mu and rs of all 8 channels of the group to every lane.
+      float rs_q[kCPL];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const f2 lo = sub2(make_float2(lov[2 * k], lov[2 * k + 1]), gm2[k]);
-          const f2 hi = sub2(make_float2(hiv[2 * k], hiv[2 * k + 1]), gm2[k]);
-          f2 nlo, nhi;
-          nlo.x = __fmul_rn(lo.x, rg2[k].x);
-          nlo.y = __fmul_rn(lo.y, rg2[k].y);
-          nhi.x = __fmul_rn(hi.x, rg2[k].x);
-          nhi.y = __fmul_rn(hi.y, rg2[k].y);
-          const f2 dlo = sub2(nlo, mu2[k]), dhi = sub2(nhi, mu2[k]);
-          sg[2 * k] = fmaxf(fabsf(dlo.x), fabsf(dhi.x));
-          sg[2 * k + 1] = fmaxf(fabsf(dlo.y), fabsf(dhi.y));
+      for (int q = 0; q < kCPL; ++q) {
+        const int ch = 8 * g + cbase + q;
+        const float nlo = __fmul_rn(__fsub_rn(pmn[c * W + ch], lo_q[q]), rg_q[q]);
+        const float nhi = __fmul_rn(__fsub_rn(pmx[c * W + ch], lo_q[q]), rg_q[q]);
+        const float sg = fmaxf(fabsf(__fsub_rn(nlo, mu_q[q])), fabsf(__fsub_rn(nhi, mu_q[q])));
+        rs_q[q] = __frcp_rn(__fadd_rn(sg, kEps));
+        if (owner) {
+          mrow[(2 + c) * kD + ch] = mu_q[q];
+          mrow[(2 + G::kNC + c) * kD + ch] = sg;
         }
       }
+      if (owner) {
+        scr_put(2, mu_q);
+        scr_put(3, rs_q);
+      }
+      __syncwarp();
+      f2 mu2[4], rs2[4];
+      scr_get(2, mu2);
+      scr_get(3, rs2);
 #pragma unroll
       for (int m = 0; m < 8; ++m)
 #pragma unroll
         for (int k = 0; k < 4; ++k) n[m][k] = sub2(n[m][k], mu2[k]);
-      if (kl == 0) {
-        float4* pmu = reinterpret_cast<float4*>(mrow + (2 + c) * kD + 8 * g);
-        float4* psg = reinterpret_cast<float4*>(mrow + (2 + G::kNC + c) * kD + 8 * g);
-        pmu[0] = make_float4(mu2[0].x, mu2[0].y, mu2[1].x, mu2[1].y);
-        pmu[1] = make_float4(mu2[2].x, mu2[2].y, mu2[3].x, mu2[3].y);
-        psg[0] = make_float4(sg[0], sg[1], sg[2], sg[3]);
-        psg[1] = make_float4(sg[4], sg[5], sg[6], sg[7]);
-      }
-      // rs = rn(1/(sigma + eps)): the token lanes of a channel group split
-      // the 8 channels as in stage 1b and exchange the reciprocals by shuffles.
-      float rs_q[G::kCPL];
-#pragma unroll
-      for (int q = 0; q < G::kCPL; ++q) {
-        const int j = ((kl * G::kCPL) & 7) + q;
-        float sj = sg[0];
-#pragma unroll
-        for (int i = 1; i < 8; ++i) sj = j == i ? sg[i] : sj;
-        rs_q[q] = __frcp_rn(__fadd_rn(sj, kEps));
-      }
-      f2 rs2[4];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float r = __shfl_sync(kFull, rs_q[j % G::kCPL], (j / G::kCPL) * G::kCG + cg);
-        if (j & 1) rs2[j >> 1].y = r; else rs2[j >> 1].x = r;
-      }
 
       // ---- Stages 3-4: codes, sign map, nibble split, store one row per m
 #pragma unroll
