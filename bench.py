@@ -119,8 +119,8 @@ ROW_SOURCES = {
     "encode": ["encode.cu", "common.cuh", "internal.h"],
     "decode_anchor": ["decode.cu", "common.cuh", "internal.h"],
     "decode_full": ["decode.cu", "common.cuh", "internal.h"],
-    "attn_draft": ["attn.cu", "common.cuh", "internal.h"],
-    "attn_verify": ["attn.cu", "common.cuh", "internal.h"],
+    "attn_draft": ["attn.cu", "attn_params.h", "common.cuh", "internal.h"],
+    "attn_verify": ["attn_tc.cu", "attn.cu", "attn_params.h", "common.cuh", "internal.h"],
 }
 TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 

@@ -46,6 +46,7 @@
 #include <utility>
 
 #include "common.cuh"
+#include "attn_params.h"
 #include "internal.h"
 #include "lynx.h"
 
@@ -63,11 +64,6 @@ namespace lynx {
 //  [64 KiB, ..) Q fragments, the partner-score exchange of the warp-pair
 //               shape, and at the end the merge buffers.
 constexpr int kLutBytes = 65536;
-// Shared-window address of the first byte of dynamic shared memory for a
-// kernel without static shared memory: the block's reserved shared memory
-// (1 KiB on sm_100-class GPUs) comes first.  The host checks the device
-// attribute before launching and the kernel checks the address itself.
-constexpr uint32_t kSmemBase = 1024;
 
 template <bool FULL, bool PAIR, bool ONE>
 struct Cfg {
@@ -130,25 +126,13 @@ constexpr int kRowStride = 4 * 256;  // bytes between constant rows
 __device__ unsigned int g_attn_flags = 0;
 
 cudaError_t read_attn_flags(unsigned int* flag) {
-  return cudaMemcpyFromSymbol(flag, g_attn_flags, sizeof(unsigned int));
+  unsigned int mine = 0, tc = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&mine, g_attn_flags, sizeof(unsigned int));
+  if (e == cudaSuccess) e = read_attn_tc_flags(&tc);
+  *flag = mine | tc;
+  return e;
 }
 
-struct AttnParams {
-  const uint16_t* q;
-  const uint8_t *ka, *kr, *va, *vr;
-  const float *km, *vm;
-  const uint16_t *kt, *vt;  // draft tokens' own keys / values, or null
-  const int32_t* bt;        // block table [batch][NB] of physical pages, or null (dense)
-  int64_t nphys;            // physical pages behind the table
-  float* part;
-  float* out;
-  int batch, T, Hq, Hkv, G, R, nrg;
-  int64_t L, NB, NCH;
-  int64_t n_chunks;  // units x NCH: the flattened (unit, chunk) space
-  int n_cta;         // CTAs of the attention grid
-  int P, C, NC, lgP, lgC;
-  float scale_log2;
-};
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -1063,9 +1047,13 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   fn<<<(unsigned)prm.n_cta, threads, smem, stream>>>(prm, tab);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  return launch_attn_combine(prm, 8 * NT, stream);
+}
+
+cudaError_t launch_attn_combine(const AttnParams& prm, int RP, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(prm.batch * prm.Hkv * prm.nrg),
-                     (unsigned)((8 * NT + kCombineWarps - 1) / kCombineWarps));
+                     (unsigned)((RP + kCombineWarps - 1) / kCombineWarps));
   cfg.blockDim = dim3(32 * kCombineWarps);
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
@@ -1073,7 +1061,7 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, attn_combine, prm, 8 * NT);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attn_combine, prm, RP);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1121,6 +1109,13 @@ cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t 
   prm.lgC = __builtin_ctz((unsigned)x.s.C);
   prm.scale_log2 = (float)(1.4426950408889634 / sqrt((double)kD));
   const bool small = prm.R <= 8;
+  if (x.full && !small && x.s.L % 128 == 0) {
+    // the verification pass: tensor-memory kernel over tiles of 128 tokens
+    prm.NCH = x.s.L / 128;
+    prm.n_chunks = (int64_t)x.batch * prm.Hkv * prm.nrg * prm.NCH;
+    prm.n_cta = attn_tc_ctas(x.batch, prm.Hkv, prm.nrg, prm.NCH, sm_count());
+    return launch_attn_tc(prm, tab, stream);
+  }
   if (x.full)
     return small ? run_attn_c<true, 1, false>(prm, tab, stream)
                  : run_attn_c<true, 4, true>(prm, tab, stream);
