@@ -12,11 +12,11 @@
 //    the chunk's one-FMA constants A = (sigma + eps)(gamma_scale + eps),
 //    B = fma(mu, gamma_scale + eps, gamma_min), rounded to nearest even BF16,
 //    goes to shared memory as 8 x 8 core matrices (two tile stages).
-//  * the tcgen05 MMAs, each issued by one thread: S^T = K^ Q^T (M = 128
-//    tokens, N = 32 rows, K = 128 channels) into tensor memory by producer
-//    thread 0 once the producers' barrier shows the tile complete, and
-//    O^T += V^T [P_hi | P_lo]^T (M = 128 channels, N = 64, K = 128 tokens)
-//    by softmax thread 0 once the softmax warps have written P, into an
+//  * the tcgen05 MMAs, issued by softmax thread 0: S^T = K^ Q^T (M = 128
+//    tokens, N = 32 rows, K = 128 channels) into tensor memory once the K
+//    producers have signalled the tile, and O^T += V^T [P_hi | P_lo]^T
+//    (M = 128 channels, N = 64, K = 128 tokens) once the softmax warps have
+//    written P and the V producers have signalled the tile, into an
 //    accumulator that stays in tensor memory for the whole unit.
 //  * 4 softmax warps, one thread per token (its tensor-memory lane), turn
 //    the token's 32 scores into weights p = 2^(s log2(e)/sqrt(d) - m_r)
@@ -64,7 +64,7 @@ constexpr int kSoftThreads = 32 * kSoftWarps;
 // kSmemBase; the host checks the block's reserved shared memory):
 //  [0, 64K)    table: 256 rows of 256 bytes, one per code byte; bytes 0..127 the
 //              32 lanes' copies of the value, bytes 128..255 the one-FMA
-//              constants of two tiles (16-byte pieces, see piece_off)
+//              constants of each producer warp's chunks (see piece_off)
 //  [64K,192K)  two stages of the K^ and V^ tiles (32 KiB each)
 //  [192K,208K) Q of the CTA's two units (K-major core matrices, 8 KiB each)
 //  [208K,224K) P^T: 64 columns (hi rows 0..31, lo rows 32..63) x 128 tokens;
@@ -80,7 +80,8 @@ constexpr uint32_t kP = kQ + 2 * kQBytes;
 constexpr uint32_t kPBytes = 0x4000;
 constexpr uint32_t kBar = kP + kPBytes;
 // mbarrier indices
-constexpr int kBKEmpty = 0, kBVEmpty = 2, kBVFull = 4, kBSReady = 6, kBSFree = 8, kBODone = 10;
+constexpr int kBKEmpty = 0, kBVEmpty = 2, kBKFull = 4, kBVFull = 6, kBSReady = 8, kBSFree = 10,
+              kBODone = 12;
 constexpr uint32_t kMisc = kBar + 8 * 16;     // [0] tmem address, [1] abort, [2..4] votes
 constexpr uint32_t kRed = kMisc + 64;         // [4 warps][32 rows], [32], [32] floats
 constexpr uint32_t kSmem = kRed + (kSoftWarps + 2) * kRows * 4;
@@ -176,12 +177,12 @@ __device__ __forceinline__ float lut(uint32_t w, uint32_t lane_off) {
 static_assert(kSmemBase == 1024, "immediate offset of the table loads");
 
 // Byte offset of 16-byte constant piece k (0, 1: A of channels 8G..8G+3,
-// 8G+4..8G+7; 2, 3: B) of channel group G, chunk ct of the tile, tensor t,
-// buffer bb, in the table's row tails.  Pieces of groups G and G + 8 sit in
-// consecutive rows, rotated by two slots, so that the four groups one load
+// 8G+4..8G+7; 2, 3: B) of channel group G, chunk ch (0, 1) of producer warp
+// w's 32 tokens, in the table's row tails.  Pieces of groups G and G + 8 sit
+// in consecutive rows, rotated by two slots, so that the four groups one load
 // instruction reads (G = gi, gi + 4, gi + 8, gi + 12) hit distinct banks.
-__device__ __forceinline__ uint32_t piece_off(int bb, int t, int ct, int k, int G) {
-  const uint32_t pi = (uint32_t)((((bb * 2 + t) * 8 + ct) * 64) + k * 16 + G);
+__device__ __forceinline__ uint32_t piece_off(int w, int ch, int k, int G) {
+  const uint32_t pi = (uint32_t)((w * 2 + ch) * 64 + k * 16 + G);
   const uint32_t row = pi >> 3, slot = (pi + ((pi >> 3) & 1u) * 2u) & 7u;
   return row * 256u + 128u + slot * 16u;
 }
@@ -281,6 +282,7 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kBKEmpty + i], 1);
       mbar_init(&bars[kBVEmpty + i], 1);
+      mbar_init(&bars[kBKFull + i], kProdThreads / 2);
       mbar_init(&bars[kBVFull + i], kProdThreads / 2);
       mbar_init(&bars[kBSReady + i], 1);
       mbar_init(&bars[kBSFree + i], kSoftThreads);
@@ -303,19 +305,20 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
   const uint32_t tm = misc[0];
 
   if (w < kProdWarps) {
-    // ================= producers: K^ (warps 0-3) and V^ (warps 4-7), two
-    // groups with their own barriers, so that the K group can run ahead: the
-    // scores of a tile start as soon as its K^ is complete
+    // ================= producers: K^ (warps 0-3) and V^ (warps 4-7).  No
+    // barrier joins them: each warp computes the one-FMA constants of its own
+    // chunk(s), and the tile's completion is signalled on an mbarrier per
+    // tensor (K^: the softmax's thread 0 then issues the scores; V^: it
+    // issues the output MMA).
     const int T = w >> 2, wr = w & 3;          // tensor, 32-token range of the tile
     const int gq = lane >> 3, t8 = lane & 7;   // channel groups 4gq..4gq+3, tokens t8 + 8j
-    const int ptid = tid & 127;                // thread of the group
-    constexpr int kGroup = kProdThreads / 2;
     const uint8_t* an = T ? a.va : a.ka;
     const uint8_t* re = T ? a.vr : a.kr;
     const uint32_t lane_off = (uint32_t)lane * 4u;
-    const int NCt = kTile >> a.lgC;            // chunks per tile
     const int meta_rows = 2 + 2 * a.NC;
-    constexpr int kItems = C16 ? 2 : 1;        // constant items per thread and tile
+    constexpr int kChunks = C16 ? 2 : 1;       // chunks of the warp's 32 tokens
+    // constant item of this lane: channels 8G + 4hh .. +3 of each chunk
+    const int it_hh = lane & 1, it_G = lane >> 1;
 
     // codes of tile i for this lane: anchor / residual bytes 16gq..16gq+15
     // of tokens 32wr + t8 + 8j
@@ -335,41 +338,22 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
                      : "=r"(R[j].x), "=r"(R[j].y), "=r"(R[j].z), "=r"(R[j].w) : "l"(re + off));
       }
     };
-    // raw metadata of the constant items of tile i: gamma_min, gamma_scale,
-    // mu, sigma of 4 channels each
-    float4 mr[kItems][4];
+    // raw metadata of the lane's constant items for tile i: gamma_min,
+    // gamma_scale, mu, sigma of 4 channels per chunk
+    float4 mr[kChunks][4];
     auto load_meta = [&](int i) {
       const int sg = seg_of(i);
-      const int64_t tok0 = tile_tok(i);
 #pragma unroll
-      for (int k = 0; k < kItems; ++k) {
-        const int it = ptid + kGroup * k;
-        if (it >= 32 * NCt) continue;
-        const int hh = it & 1, G = (it >> 1) & 15, ct = it >> 5, t = T;
-        const int64_t tok = tok0 + ct * a.C;
+      for (int k = 0; k < kChunks; ++k) {
+        const int64_t tok = tile_tok(i) + 32 * wr + 16 * k;   // a token of chunk k
         const int64_t blk = block_of(sg, tok);
         const int cc = (int)((tok & (a.P - 1)) >> a.lgC);
-        const float* mb = (t ? a.vm : a.km) + blk * (int64_t)meta_rows * kD + 8 * G + 4 * hh;
+        const float* mb = (T ? a.vm : a.km) + blk * (int64_t)meta_rows * kD + 8 * it_G + 4 * it_hh;
         mr[k][0] = __ldg(reinterpret_cast<const float4*>(mb));
         mr[k][1] = __ldg(reinterpret_cast<const float4*>(mb + kD));
         mr[k][2] = __ldg(reinterpret_cast<const float4*>(mb + (2 + cc) * kD));
         mr[k][3] = __ldg(reinterpret_cast<const float4*>(mb + (2 + a.NC + cc) * kD));
       }
-    };
-    // S^T of tile i (producer thread 0, after the producers' barrier that
-    // follows the tile's stores and their proxy fences)
-    auto issue_s = [&](int i) {
-      const int b = i & 1;
-      if (i >= 2) (void)wait_bar(&bars[kBSFree + b], (uint32_t)((i - 2) >> 1) & 1u, abort_w);
-      fence_after();
-      const uint32_t ka = smem_u32(smem + kStage + b * (2 * kTileBytes));  // K^ of stage b
-      const uint32_t qa = smem_u32(smem + kQ + seg_of(i) * kQBytes);
-#pragma unroll
-      for (int k = 0; k < kD / 16; ++k)
-        umma(tm + kColS + 32 * b, sdesc(ka + 256 * k, 128, 2048), sdesc(qa + 256 * k, 128, 2048),
-             kIdS, k > 0 ? 1u : 0u);
-      umma_commit(&bars[kBSReady + b]);
-      umma_commit(&bars[kBKEmpty + b]);
     };
     uint4 ca[4], cr[4];
     if (n > 0) {
@@ -378,12 +362,11 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
     }
     for (int i = 0; i < n; ++i) {
       const int b = i & 1;
-      // the one-FMA constants of tile i into buffer b
+      // the one-FMA constants of this warp's chunk(s) of tile i (the warp's
+      // last reads of the previous tile's constants precede this __syncwarp)
+      __syncwarp();
 #pragma unroll
-      for (int k = 0; k < kItems; ++k) {
-        const int it = ptid + kGroup * k;
-        if (it >= 32 * NCt) continue;
-        const int hh = it & 1, G = (it >> 1) & 15, ct = it >> 5, t = T;
+      for (int k = 0; k < kChunks; ++k) {
         const f2 e = make_float2(kEps, kEps);
         const f2 gm0 = make_float2(mr[k][0].x, mr[k][0].y), gm1 = make_float2(mr[k][0].z, mr[k][0].w);
         const f2 gs0 = add2(make_float2(mr[k][1].x, mr[k][1].y), e);
@@ -393,37 +376,32 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
         const f2 sg1 = add2(make_float2(mr[k][3].z, mr[k][3].w), e);
         const f2 A0 = mul2(sg0, gs0), A1 = mul2(sg1, gs1);
         const f2 B0 = fma2(mu0, gs0, gm0), B1 = fma2(mu1, gs1, gm1);
-        *reinterpret_cast<float4*>(smem + piece_off(b, t, ct, hh, G)) =
+        *reinterpret_cast<float4*>(smem + piece_off(w, k, it_hh, it_G)) =
             make_float4(A0.x, A0.y, A1.x, A1.y);
-        *reinterpret_cast<float4*>(smem + piece_off(b, t, ct, 2 + hh, G)) =
+        *reinterpret_cast<float4*>(smem + piece_off(w, k, 2 + it_hh, it_G)) =
             make_float4(B0.x, B0.y, B1.x, B1.y);
       }
-      if (i + 1 < n) load_meta(i + 1);
+      __syncwarp();
       uint4 na[4], nr[4];
-      if (i + 1 < n) load_codes(i + 1, na, nr);
-      // constants visible to the group; the group is past tile i-1 (for K^,
-      // the tile is complete: its scores can start)
-      if (T == 0) {
-        asm volatile("barrier.sync 1, %0;" :: "n"(kGroup) : "memory");
-        if (ptid == 0 && i >= 1) issue_s(i - 1);
-        // K^ of stage b is free once the scores of tile i-2 are done
-        if (i >= 2) (void)wait_bar(&bars[kBKEmpty + b], (uint32_t)((i - 2) >> 1) & 1u, abort_w);
-      } else {
-        asm volatile("barrier.sync 3, %0;" :: "n"(kGroup) : "memory");
-        // V^ of stage b is free once the output of tile i-2 is accumulated
-        if (i >= 2) (void)wait_bar(&bars[kBVEmpty + b], (uint32_t)((i - 2) >> 1) & 1u, abort_w);
+      if (i + 1 < n) {
+        load_meta(i + 1);
+        load_codes(i + 1, na, nr);
       }
+      // this tensor's stage b is free once the scores (K^) or the output
+      // (V^) of tile i-2 are done
+      if (i >= 2)
+        (void)wait_bar(&bars[(T ? kBVEmpty : kBKEmpty) + b], (uint32_t)((i - 2) >> 1) & 1u, abort_w);
       uint8_t* tile = smem + kStage + b * (2 * kTileBytes) + T * kTileBytes;
 #pragma unroll
       for (int gi = 0; gi < 4; ++gi) {
         const int G = 4 * gq + gi;
 #pragma unroll
         for (int jc = 0; jc < 4; jc += (C16 ? 2 : 4)) {
-          const int ct = (32 * wr + t8 + 8 * jc) >> a.lgC;
-          const float4 A0 = *reinterpret_cast<const float4*>(smem + piece_off(b, T, ct, 0, G));
-          const float4 A1 = *reinterpret_cast<const float4*>(smem + piece_off(b, T, ct, 1, G));
-          const float4 B0 = *reinterpret_cast<const float4*>(smem + piece_off(b, T, ct, 2, G));
-          const float4 B1 = *reinterpret_cast<const float4*>(smem + piece_off(b, T, ct, 3, G));
+          const int k = C16 ? (jc >> 1) : 0;
+          const float4 A0 = *reinterpret_cast<const float4*>(smem + piece_off(w, k, 0, G));
+          const float4 A1 = *reinterpret_cast<const float4*>(smem + piece_off(w, k, 1, G));
+          const float4 B0 = *reinterpret_cast<const float4*>(smem + piece_off(w, k, 2, G));
+          const float4 B1 = *reinterpret_cast<const float4*>(smem + piece_off(w, k, 3, G));
 #pragma unroll
           for (int j = jc; j < jc + (C16 ? 2 : 4); ++j) {
             const uint32_t aw = gi == 0 ? ca[j].x : gi == 1 ? ca[j].y : gi == 2 ? ca[j].z : ca[j].w;
@@ -447,22 +425,13 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
         }
       }
       fence_proxy_async();  // the tile is read by the tensor core
-      if (T == 1) arrive(&bars[kBVFull + b]);
+      arrive(&bars[(T ? kBVFull : kBKFull) + b]);
       if (i + 1 < n) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           ca[j] = na[j];
           cr[j] = nr[j];
         }
-      }
-    }
-    if (T == 0) {
-      asm volatile("barrier.sync 1, %0;" :: "n"(kGroup) : "memory");
-      if (ptid == 0 && n > 0) {
-        issue_s(n - 1);
-        // every commit's arrival has landed before tear-down
-        for (int i = n - 2 < 0 ? 0 : n - 2; i < n; ++i)
-          (void)wait_bar(&bars[kBKEmpty + (i & 1)], (uint32_t)(i >> 1) & 1u, abort_w);
       }
     }
   } else {
@@ -479,8 +448,27 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
 #pragma unroll
     for (int r = 0; r < RP; ++r) ls[r] = 0.f;
     bool o_waited = true;   // odone of the previous tile already waited for
+    // S^T of tile i, issued by thread 0 once the tile's K^ is complete and
+    // the tile two back has released its score buffer
+    int s_next = 0;         // thread 0: the next tile whose scores are to be issued
+    auto issue_s = [&](int i) {
+      const int b = i & 1;
+      (void)wait_bar(&bars[kBKFull + b], (uint32_t)(i >> 1) & 1u, abort_w);
+      if (i >= 2) (void)wait_bar(&bars[kBSFree + b], (uint32_t)((i - 2) >> 1) & 1u, abort_w);
+      fence_after();
+      const uint32_t ka = smem_u32(smem + kStage + b * (2 * kTileBytes));  // K^ of stage b
+      const uint32_t qa = smem_u32(smem + kQ + seg_of(i) * kQBytes);
+#pragma unroll
+      for (int k = 0; k < kD / 16; ++k)
+        umma(tm + kColS + 32 * b, sdesc(ka + 256 * k, 128, 2048), sdesc(qa + 256 * k, 128, 2048),
+             kIdS, k > 0 ? 1u : 0u);
+      umma_commit(&bars[kBSReady + b]);
+      umma_commit(&bars[kBKEmpty + b]);
+      s_next = i + 1;
+    };
     for (int i = 0; i < n; ++i) {
       const int b = i & 1, sg = seg_of(i);
+      if (q == 0 && lane == 0 && s_next == i) issue_s(i);
       const bool first = i == 0 || ti0 + i == a.NCH;       // a unit's first tile here
       const bool last = i == n - 1 || ti0 + i + 1 == a.NCH;  // a unit's last tile here
       (void)wait_bar(&bars[kBSReady + b], (uint32_t)(i >> 1) & 1u, abort_w);
@@ -597,6 +585,9 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
                (k > 0 || !first) ? 1u : 0u);
         umma_commit(&bars[kBODone]);
         umma_commit(&bars[kBVEmpty + b]);
+        // the next tile's scores, if its K^ is already complete
+        if (i + 1 < n && mbar_try_wait(&bars[kBKFull + (b ^ 1)], (uint32_t)((i + 1) >> 1) & 1u))
+          issue_s(i + 1);
       }
       o_waited = false;
       if (last) {
@@ -637,8 +628,10 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
     if (q == 0 && lane == 0) {
       // every commit's arrival has landed before tear-down (the last tile's
       // O was waited for in its epilogue)
-      for (int i = n - 2 < 0 ? 0 : n - 2; i < n; ++i)
+      for (int i = n - 2 < 0 ? 0 : n - 2; i < n; ++i) {
         (void)wait_bar(&bars[kBVEmpty + (i & 1)], (uint32_t)(i >> 1) & 1u, abort_w);
+        (void)wait_bar(&bars[kBKEmpty + (i & 1)], (uint32_t)(i >> 1) & 1u, abort_w);
+      }
     }
   }
 
