@@ -368,8 +368,8 @@ int lynx_attn_workspace_bytes(int batch, int T, int H_q, int64_t L, int H_kv,
 /* Decode attention over packed KV [Review, Prerequisites Eq. 1]:
  *   O = softmax(q K^T / sqrt(D)) V
  * for every sequence, query row and query head, grouped-query: query head hq
- * reads KV head hq / (H_q / H_kv).  K and V are reconstructed in registers
- * as lynx_decode_anchor (mode LYNX_ANCHOR, the draft step of [Review,
+ * reads KV head hq / (H_q / H_kv).  K and V are reconstructed on the fly
+ * (never written to global memory) as lynx_decode_anchor (mode LYNX_ANCHOR, the draft step of [Review,
  * Mechanism 2, Anchor Phase]) or lynx_decode_full (LYNX_FULL, the T-token
  * verification pass of [Review, Mechanism 3]) would with BF16 output, the
  * affine map applied as one fused multiply-add x = fma(v, A, B) with
@@ -386,8 +386,11 @@ int lynx_attn_workspace_bytes(int batch, int T, int H_q, int64_t L, int H_kv,
  *              contents on entry do not matter and are clobbered
  * Limits: 1 <= T <= 64 (the pages' speculative cap), H_q % H_kv == 0,
  * (H_q / H_kv) * T <= 256, C >= 16, L >= 1.  Up to 8 query rows per KV head
- * take the single-warp shape, up to 32 the warp-pair shape; beyond 32 the
- * rows form groups of 32, each of which reads the packed K and V once. */
+ * take the single-warp shape (register-direct MMAs); more rows form groups of
+ * up to 32, each of which reads the packed K and V once: in LYNX_FULL mode
+ * with L a multiple of 128 on the tcgen05 path (tiles of 128 tokens rebuilt
+ * in shared memory, scores and output accumulated in tensor memory), else
+ * in the warp-pair shape. */
 int lynx_attn_decode(const void *q, int batch, int T, int H_q,
                      const void *k_anchor, const void *k_residual,
                      const float *k_meta, const void *v_anchor,
