@@ -101,6 +101,9 @@ def test_page_and_chunk_sizes(lynx_lib, oracle_mod, cuda_dev, P, C, L):
     (128, 16, 1024, 1, 3, 3, 3),     # 9 rows both modes
     (128, 32, 768, 1, 16, 2, 1),     # 16 query heads per KV head: anchor mode with 16 rows
     (128, 32, 1024, 2, 8, 16, 2),    # 64 rows: two row groups of 32
+    (128, 128, 1024, 2, 8, 8, 1),    # 32 rows, chunks of 128 (one per verification tile)
+    (64, 32, 1088, 1, 4, 8, 1),      # L not a multiple of 128: the register-direct pair shape
+    (128, 32, 128, 4, 16, 8, 1),     # one 128-token tile per (KV head, row group): one CTA each
 ])
 def test_row_counts_and_pairs(lynx_lib, oracle_mod, cuda_dev, P, C, L, H_kv, H_q, T, Ta):
     pairs = [(0, h) for h in range(H_kv)]
