@@ -531,12 +531,14 @@ encode_kernel(const __grid_constant__ CUtensorMap tmap, const int64_t nunit,
           compand_fast2(make_float2(a[2 * k], a[2 * k + 1]), alpha2, c16_2, bits[2 * k],
                         bits[2 * k + 1]);
         }
-        // smallest distance to a rounding boundary (low 16 bits) of the 8
-        // values, two at a time in 16-bit lanes
-        uint32_t dmin = __vminu2(prmt(bits[0], bits[1], 0x5410u), prmt(bits[2], bits[3], 0x5410u));
-        dmin = __vminu2(dmin, __vminu2(prmt(bits[4], bits[5], 0x5410u), prmt(bits[6], bits[7], 0x5410u)));
-        const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
-        if (__any_sync(kFull, amb)) {
+        // smallest distance to a rounding boundary (the low 16 bits) of the
+        // 8 values: a 16-bit-lane minimum over the words (their high halves
+        // are not looked at), then one test of the low half
+        const uint32_t d01 = __vminu2(bits[0], bits[1]), d23 = __vminu2(bits[2], bits[3]);
+        const uint32_t d45 = __vminu2(bits[4], bits[5]), d67 = __vminu2(bits[6], bits[7]);
+        const uint32_t dmin = __vminu2(__vminu2(d01, d23), __vminu2(d45, d67));
+        const bool amb = (dmin & 0xffffu) < 2u * kAmbiguityK;
+        if (amb) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             if (compand_ambiguous(bits[i]))

@@ -565,10 +565,11 @@ a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, 
       }
     }
     if constexpr (FAST) {
-      uint32_t dmin = __vminu2(a1_prmt(bits[0], bits[1], 0x5410u), a1_prmt(bits[2], bits[3], 0x5410u));
-      dmin = __vminu2(dmin, __vminu2(a1_prmt(bits[4], bits[5], 0x5410u), a1_prmt(bits[6], bits[7], 0x5410u)));
-      const bool amb = __vcmpltu2(dmin, 0x00010001u * (2u * kAmbiguityK)) != 0u;
-      if (__any_sync(kFull, amb)) {
+      // a 16-bit-lane minimum over the words, then one test of the low half
+      const uint32_t d01 = __vminu2(bits[0], bits[1]), d23 = __vminu2(bits[2], bits[3]);
+      const uint32_t d45 = __vminu2(bits[4], bits[5]), d67 = __vminu2(bits[6], bits[7]);
+      const uint32_t dmin = __vminu2(__vminu2(d01, d23), __vminu2(d45, d67));
+      if ((dmin & 0xffffu) < 2u * kAmbiguityK) {
 #pragma unroll
         for (int i = 0; i < 8; ++i)
           if ((bits[i] & 0xffffu) < 2u * kAmbiguityK) {
