@@ -110,6 +110,32 @@ def test_row_counts_and_pairs(lynx_lib, oracle_mod, cuda_dev, P, C, L, H_kv, H_q
     _run(lynx_lib, oracle_mod, cuda_dev, 1, L, H_kv, H_q, T, P, C, pairs, seed=L + T, T_anchor=Ta)
 
 
+def test_rising_maxima_rescale_every_tile(lynx_lib, oracle_mod, cuda_dev):
+    """Keys whose channel 0 grows by 1 per token and queries that weight it:
+    each 128-token tile raises every row's running maximum by about
+    16 (log2 units), more than the 2^8 a weight may reach before the maximum is
+    raised, so the verification pass rescales its accumulators on every tile
+    (and its split partials carry maxima far apart)."""
+    from split_stream_kv_gb300 import synth
+    batch, L, H_kv, H_q, T, P, C = 1, 1024, 1, 4, 8, 128, 32
+    kv = synth.kv_cache(2 * batch, L, H_kv, 128, seed=31, device=cuda_dev)
+    ramp = torch.arange(L, device=cuda_dev, dtype=torch.float32)
+    kv[0::2, :, :, 0] = (kv[0::2, :, :, 0].float() + ramp[None, :, None]).to(kv.dtype)
+    k = kv[0::2].contiguous()
+    v = kv[1::2].contiguous()
+    ks = lynx_lib.lynx_encode(k, P, C, ALPHA)
+    vs = lynx_lib.lynx_encode(v, P, C, ALPHA)
+    q = synth.queries(batch, T, H_q, 128, seed=32, device=cuda_dev)
+    q[..., 0] = 1.0
+    out = lynx_lib.lynx_attn_decode(q, ks, vs, L, P, C, ALPHA, lynx_lib.LYNX_FULL)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    assert lynx_lib.lynx_device_errors() == 0
+    k_np = tuple(t.cpu().numpy() for t in ks)
+    v_np = tuple(t.cpu().numpy() for t in vs)
+    _check(oracle_mod, q, k_np, v_np, out, L, P, C, True, [(0, 0)], H_q, H_kv, T)
+
+
 def test_decode_attention_full_size_sampled(lynx_lib, oracle_mod, cuda_dev):
     """8 sequences x 32768 tokens, 32 query heads over 8 KV heads: draft step
     (T=1, Anchor) and verification (T=8, Anchor+Residual); three sampled
