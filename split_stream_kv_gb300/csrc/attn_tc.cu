@@ -466,6 +466,12 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
       umma_commit(&bars[kBKEmpty + b]);
       s_next = i + 1;
     };
+    auto try_issue_s = [&](int j) {   // thread 0: without waiting for K^
+      if (s_next == j && j < n) {
+        const int bk = j & 1;
+        if (mbar_try_wait(&bars[kBKFull + bk], (uint32_t)(j >> 1) & 1u)) issue_s(j);
+      }
+    };
     for (int i = 0; i < n; ++i) {
       const int b = i & 1, sg = seg_of(i);
       if (q == 0 && lane == 0 && s_next == i) issue_s(i);
@@ -478,6 +484,9 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
       tmem_wait_ld();
       fence_before();
       arrive(&bars[kBSFree + b]);
+      // the next tile's scores go into the other buffer (released by the
+      // softmax of tile i - 1), so they can be issued now if its K^ is ready
+      if (q == 0 && lane == 0) try_issue_s(i + 1);
       float p[RP];
       float pm = 0.f;
 #pragma unroll
@@ -585,9 +594,8 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
                (k > 0 || !first) ? 1u : 0u);
         umma_commit(&bars[kBODone]);
         umma_commit(&bars[kBVEmpty + b]);
-        // the next tile's scores, if its K^ is already complete
-        if (i + 1 < n && mbar_try_wait(&bars[kBKFull + (b ^ 1)], (uint32_t)((i + 1) >> 1) & 1u))
-          issue_s(i + 1);
+        // the next tile's scores, if not yet issued and its K^ is complete
+        try_issue_s(i + 1);
       }
       o_waited = false;
       if (last) {
