@@ -322,10 +322,10 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
 
     // codes of tile i for this lane: anchor / residual bytes 16gq..16gq+15
     // of tokens 32wr + t8 + 8j
-    auto load_codes = [&](int i, uint4 (&A)[4], uint4 (&R)[4]) {
-      const int sg = seg_of(i);
+    // (blk: the packed block of the warp's 32 tokens of tile i, found a
+    // tile earlier; a page holds at least 64 tokens, so one block serves them)
+    auto load_codes = [&](int i, int64_t blk, uint4 (&A)[4], uint4 (&R)[4]) {
       const int64_t tok = tile_tok(i) + 32 * wr;
-      const int64_t blk = block_of(sg, tok);
       const int64_t row0 = blk * a.P + (tok & (a.P - 1));
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -341,12 +341,10 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
     // raw metadata of the lane's constant items for tile i: gamma_min,
     // gamma_scale, mu, sigma of 4 channels per chunk
     float4 mr[kChunks][4];
-    auto load_meta = [&](int i) {
-      const int sg = seg_of(i);
+    auto load_meta = [&](int i, int64_t blk) {
 #pragma unroll
       for (int k = 0; k < kChunks; ++k) {
         const int64_t tok = tile_tok(i) + 32 * wr + 16 * k;   // a token of chunk k
-        const int64_t blk = block_of(sg, tok);
         const int cc = (int)((tok & (a.P - 1)) >> a.lgC);
         const float* mb = (T ? a.vm : a.km) + blk * (int64_t)meta_rows * kD + 8 * it_G + 4 * it_hh;
         mr[k][0] = __ldg(reinterpret_cast<const float4*>(mb));
@@ -355,11 +353,17 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
         mr[k][3] = __ldg(reinterpret_cast<const float4*>(mb + (2 + a.NC + cc) * kD));
       }
     };
+    auto warp_block = [&](int i) { return block_of(seg_of(i), tile_tok(i) + 32 * wr); };
     uint4 ca[4], cr[4];
+    // paged: the block of tile i + 1, read from the block table a tile ahead
+    // so that the code loads need not wait for it (dense: arithmetic)
+    int64_t blk_next = 0;
     if (n > 0) {
-      load_codes(0, ca, cr);
-      load_meta(0);
+      const int64_t blk0 = warp_block(0);
+      load_codes(0, blk0, ca, cr);
+      load_meta(0, blk0);
     }
+    if (PAGED && n > 1) blk_next = warp_block(1);
     for (int i = 0; i < n; ++i) {
       const int b = i & 1;
       // the one-FMA constants of this warp's chunk(s) of tile i (the warp's
@@ -384,9 +388,11 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
       __syncwarp();
       uint4 na[4], nr[4];
       if (i + 1 < n) {
-        load_meta(i + 1);
-        load_codes(i + 1, na, nr);
+        const int64_t blk = PAGED ? blk_next : warp_block(i + 1);
+        load_meta(i + 1, blk);
+        load_codes(i + 1, blk, na, nr);
       }
+      if (PAGED && i + 2 < n) blk_next = warp_block(i + 2);
       // this tensor's stage b is free once the scores (K^) or the output
       // (V^) of tile i-2 are done
       if (i >= 2)
