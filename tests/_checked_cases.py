@@ -71,6 +71,18 @@ def run_cases():
     keep("attn_paged", lynx.lynx_attn_decode_paged(q8, tuple(pool(t) for t in ks),
                                                    tuple(pool(t) for t in vs), table, L, P, C,
                                                    ALPHA, lynx.LYNX_FULL))
+    # the same verification, dense and paged, over pages of 64 and chunks of 16
+    P, C = 64, 16
+    ks = lynx.lynx_encode(kvv[0::2].contiguous(), P, C, ALPHA)
+    vs = lynx.lynx_encode(kvv[1::2].contiguous(), P, C, ALPHA)
+    keep("attn_T8_c16", lynx.lynx_attn_decode(q8, ks, vs, L, P, C, ALPHA, lynx.LYNX_FULL))
+    NB = L // P
+    table = torch.randperm(batch * NB + 7, generator=g)[: batch * NB].view(batch, NB)
+    table = table.to(torch.int32).to(dev)
+    idx = table.view(-1).long()
+    keep("attn_paged_c16", lynx.lynx_attn_decode_paged(q8, tuple(pool(t) for t in ks),
+                                                       tuple(pool(t) for t in vs), table, L, P,
+                                                       C, ALPHA, lynx.LYNX_FULL))
     torch.cuda.synchronize()
     out["device_errors"] = __import__("numpy").array([lynx.lynx_device_errors()])
     out["library"] = __import__("numpy").frombuffer(

@@ -56,12 +56,15 @@ def test_paged_encode_decode_match_oracle(lynx_lib, oracle_mod, cuda_dev, B, L, 
     assert lynx_lib.lynx_device_errors() == 0
 
 
-@pytest.mark.parametrize("mode_name,T,H_q,tail", [("anchor", 1, 8, False), ("full", 8, 8, True),
-                                                  ("full", 2, 4, False)])
+@pytest.mark.parametrize("mode_name,T,H_q,tail,P,C", [
+    ("anchor", 1, 8, False, 128, 32), ("full", 8, 8, True, 128, 32), ("full", 2, 4, False, 128, 32),
+    # 16 rows per KV head over pages of 64 and chunks of 16 (two chunks per
+    # 32-token producer range on the tensor-memory path)
+    ("full", 4, 8, False, 64, 16)])
 def test_paged_attention_matches_oracle(lynx_lib, oracle_mod, cuda_dev, mode_name, T, H_q,
-                                        tail):
+                                        tail, P, C):
     from split_stream_kv_gb300 import synth
-    batch, L, H_kv, P, C = 2, 2048, 2, 128, 32
+    batch, L, H_kv = 2, 2048, 2
     NB = L // P
     kv = synth.kv_cache(2 * batch, L, H_kv, 128, seed=T + H_q, device=cuda_dev)
     k, v = kv[0::2].contiguous(), kv[1::2].contiguous()
