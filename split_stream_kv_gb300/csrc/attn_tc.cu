@@ -322,8 +322,8 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
 
     // codes of tile i for this lane: anchor / residual bytes 16gq..16gq+15
     // of tokens 32wr + t8 + 8j
-    // (blk: the packed block of the warp's 32 tokens of tile i, found a
-    // tile earlier; a page holds at least 64 tokens, so one block serves them)
+    // (blk: the packed block of the warp's 32 tokens of tile i; a page holds at
+    // least 64 tokens, so one block serves them)
     auto load_codes = [&](int i, int64_t blk, uint4 (&A)[4], uint4 (&R)[4]) {
       const int64_t tok = tile_tok(i) + 32 * wr;
       const int64_t row0 = blk * a.P + (tok & (a.P - 1));
