@@ -481,10 +481,16 @@ int lynx_compander_selfcheck(float alpha, uint64_t *counts, void *stream);
 int lynx_wait_timeouts(unsigned int *flag);
 
 /* Check of the bounded wait every asynchronous-copy wait in the library
- * uses: one CTA initialises an mbarrier, arrives on it (arrive != 0) or not,
- * and waits with a limit of limit_ns nanoseconds (0 < limit_ns <= 1e9) on
- * the global timer.  *status (device) = 1 if the barrier completed, 2 if the
- * wait gave up.  Nothing faults or hangs either way.  Enqueued on `stream`. */
+ * uses: one CTA initialises an mbarrier, arrives on it (arrive == 1) or not
+ * (arrive == 0), and waits with a limit of limit_ns nanoseconds
+ * (0 < limit_ns <= 1e9) on the global timer.  *status (device) = 1 if the
+ * barrier completed, 2 if the wait gave up.  arrive == 2 runs the
+ * verification pass's own wait (lynx_attn_decode on the tensor-memory path)
+ * twice on barriers nothing arrives on: the first, limited to limit_ns, must
+ * give up and raise the CTA's abort word; the second, started half a limit
+ * later with the kernel's full limit (2 s), must then return at once;
+ * *status = 3 if both held, 4 if not.  The library's error words are not
+ * touched.  Nothing faults or hangs either way.  Enqueued on `stream`. */
 int lynx_wait_selftest(uint64_t limit_ns, int arrive, unsigned int *status,
                        void *stream);
 

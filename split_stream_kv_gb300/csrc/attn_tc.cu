@@ -187,20 +187,27 @@ __device__ __forceinline__ uint32_t piece_off(int w, int ch, int k, int G) {
   return row * 256u + 128u + slot * 16u;
 }
 
-// Bounded wait; false once the CTA has aborted (see the file comment).
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t phase, volatile uint32_t* abort_w) {
+// Bounded wait; false once the CTA has aborted (see the file comment).  A
+// wait that runs out after limit_ns raises the CTA's abort word and records
+// kFlagWaitTimeout in *flags.
+__device__ __forceinline__ bool wait_bar_for(uint64_t* bar, uint32_t phase,
+                                             volatile uint32_t* abort_w, uint64_t limit_ns,
+                                             unsigned int* flags) {
   if (mbar_try_wait(bar, phase)) return true;
   if (*abort_w) return false;
   const uint64_t t0 = global_ns();
   for (;;) {
     if (mbar_try_wait(bar, phase)) return true;
     if (*abort_w) return false;
-    if (global_ns() - t0 > kWaitNs) {
+    if (global_ns() - t0 > limit_ns) {
       *abort_w = 1u;
-      atomicOr(&g_attn_tc_flags, kFlagWaitTimeout);
+      atomicOr(flags, kFlagWaitTimeout);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t phase, volatile uint32_t* abort_w) {
+  return wait_bar_for(bar, phase, abort_w, kWaitNs, &g_attn_tc_flags);
 }
 
 }  // namespace tc
@@ -659,6 +666,49 @@ attn_tc_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Exp
                  "r"(kTmemCols) : "memory");
   // the split combine may launch now; it waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ------------------------------------------------------------ wait self-test
+
+// This kernel's wait on mbarriers that nothing arrives on (the producer is
+// absent): warp 0 waits with limit_ns and must give up, raise the abort word
+// and record kFlagWaitTimeout; warp 1 starts half a limit later with the full
+// limit and must return unsatisfied once the abort word is up, well before
+// its own limit.  *status = 3 if both held, else 4.  The flag word is the
+// CTA's own, not the library's.
+__global__ void __launch_bounds__(64, 1)
+tc_wait_selftest_kernel(uint64_t limit_ns, unsigned int* status) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ uint32_t abort_w, good;
+  __shared__ unsigned int flags;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    abort_w = 0u;
+    flags = 0u;
+    good = 0u;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const uint64_t t0 = global_ns();
+  if (w == 0) {
+    const bool ok = tc::wait_bar_for(&bars[0], 0, &abort_w, limit_ns, &flags);
+    if (lane == 0 && !ok && abort_w) atomicAdd(&good, 1u);
+  } else {
+    while (global_ns() - t0 < limit_ns / 2) {
+    }
+    const uint64_t t1 = global_ns();
+    const bool ok = tc::wait_bar_for(&bars[1], 0, &abort_w, kWaitNs, &flags);
+    if (lane == 0 && !ok && global_ns() - t1 < 2 * limit_ns) atomicAdd(&good, 1u);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *status = (good == 2u && (flags & kFlagWaitTimeout)) ? 3u : 4u;
+}
+
+cudaError_t launch_tc_wait_selftest(uint64_t limit_ns, unsigned int* status, cudaStream_t stream) {
+  tc_wait_selftest_kernel<<<1, 64, 0, stream>>>(limit_ns, status);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ host

@@ -302,9 +302,10 @@ def lynx_spec_verify(p, q, draft_tokens, u, r, n_accepted=None, next_token=None)
     return n_accepted, next_token
 
 
-def lynx_wait_selftest(limit_ns: int, arrive: bool, device) -> int:
+def lynx_wait_selftest(limit_ns: int, arrive, device) -> int:
     """Run the bounded-wait check; returns 1 (barrier completed) or 2 (the
-    wait gave up after limit_ns)."""
+    wait gave up after limit_ns); with arrive == 2 the verification pass's
+    wait and abort word: 3 (both waits ended as they must) or 4."""
     st = torch.zeros(1, dtype=torch.int32, device=device)
     _check(lib().lynx_wait_selftest(limit_ns, int(arrive), _ptr(st), _stream(st.device)),
            "lynx_wait_selftest")

@@ -129,6 +129,12 @@ def test_bounded_wait_gives_up_and_reports(lynx_lib, cuda_dev, kv):
     # and the context must stay usable
     assert lynx_lib.lynx_wait_selftest(1_000_000, False, cuda_dev) == 2
     assert lynx_lib.lynx_wait_selftest(1_000_000, True, cuda_dev) == 1
+    # the verification pass's wait: the first gives up after 1 ms and raises
+    # the abort word, the second (2 s limit) then returns at once
+    assert lynx_lib.lynx_wait_selftest(1_000_000, 2, cuda_dev) == 3
+    # the self-test keeps its own flag word: the library's timeout bit stays clear
+    assert (lynx_lib.lynx_device_errors() & 1) == 0
+    assert lynx_lib.lynx_wait_timeouts() == 0
     anc, res, meta = lynx_lib.lynx_encode(kv, 128, 32, ALPHA)
     torch.cuda.synchronize()
     assert anc.numel() > 0
