@@ -155,6 +155,17 @@ def test_shares_straddling_units_all_heads(lynx_lib, oracle_mod, cuda_dev):
     print(r)
 
 
+def test_more_units_than_sms(lynx_lib, oracle_mod, cuda_dev):
+    """4 sequences x 8 KV heads x 8 row groups of 32 (T = 64, 4 query heads per
+    KV head) = 256 work units of two 128-token tiles: more units than a GB300
+    has SMs, so the verification pass runs one unit per CTA over more than one
+    wave and the combine maps every unit to its own CTA.  Four (sequence, KV
+    head) pairs checked on all 256 rows."""
+    pairs = [(0, 0), (1, 7), (2, 3), (3, 5)]
+    r = _run(lynx_lib, oracle_mod, cuda_dev, 4, 256, 8, 32, 64, 128, 32, pairs, seed=13)
+    print(r)
+
+
 def _run_tail(lynx_lib, oracle_mod, dev, batch, L, H_kv, H_q, T, P, C, pairs, mode, seed):
     """Attention with the draft tokens' own keys and values (causal tail)."""
     from split_stream_kv_gb300 import synth
