@@ -340,7 +340,7 @@ int lynx_a1_decode(const void* anchor, const void* residual, const float* meta, 
 
 static int check_attn_shape(int batch, int T, int H_q, int64_t L, int H_kv, int D, int page,
                             int C) {
-  int rc = check_codec_shape(batch, L, H_kv, D, page, C, 256);
+  int rc = check_codec_shape(batch, L, H_kv, D, page, C, 512);
   if (rc) return rc;
   if (batch < 1 || L < 1) return fail(LYNX_ESHAPE, "attention needs batch >= 1 and L >= 1");
   if (T < 1) return fail(LYNX_ESHAPE, "T = %d must be >= 1", T);

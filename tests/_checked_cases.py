@@ -83,6 +83,14 @@ def run_cases():
     keep("attn_paged_c16", lynx.lynx_attn_decode_paged(q8, tuple(pool(t) for t in ks),
                                                        tuple(pool(t) for t in vs), table, L, P,
                                                        C, ALPHA, lynx.LYNX_FULL))
+    # pages of 512: draft and verification
+    P, C = 512, 64
+    ks = lynx.lynx_encode(kvv[0::2].contiguous(), P, C, ALPHA)
+    vs = lynx.lynx_encode(kvv[1::2].contiguous(), P, C, ALPHA)
+    q1 = synth.queries(batch, 1, Hq, 128, seed=1, device=dev)
+    keep("attn_T1_p512", lynx.lynx_attn_decode(q1, (ks[0], None, ks[2]), (vs[0], None, vs[2]),
+                                               L, P, C, ALPHA, lynx.LYNX_ANCHOR))
+    keep("attn_T8_p512", lynx.lynx_attn_decode(q8, ks, vs, L, P, C, ALPHA, lynx.LYNX_FULL))
     torch.cuda.synchronize()
     out["device_errors"] = __import__("numpy").array([lynx.lynx_device_errors()])
     out["library"] = __import__("numpy").frombuffer(

@@ -103,7 +103,9 @@ def test_attention_rejects(lynx_lib):
     assert call(mode=3) == -1
     assert call(ws=0) == -5
     assert call(L=100) == -2
-    assert call(page=512, L=1024) == -3       # attention is built for pages <= 256
+    assert call(page=1024, L=2048) == -3      # pages up to 512, like the codec
+    assert call(page=96, L=192) == -3         # pages are powers of two from 64
+    assert lynx_lib.lynx_attn_workspace_bytes(1, 8, 4, 1024, 1, 128, 512) > 0
     need = lynx_lib.lynx_attn_workspace_bytes(1, 1, 4, 256, 1, 128, 128)
     assert need > 0
     assert call(ws=need - 1) == -5

@@ -104,6 +104,8 @@ def test_page_and_chunk_sizes(lynx_lib, oracle_mod, cuda_dev, P, C, L):
     (128, 128, 1024, 2, 8, 8, 1),    # 32 rows, chunks of 128 (one per verification tile)
     (64, 32, 1088, 1, 4, 8, 1),      # L not a multiple of 128: the register-direct pair shape
     (128, 32, 128, 4, 16, 8, 1),     # one 128-token tile per (KV head, row group): one CTA each
+    (512, 64, 2048, 2, 8, 8, 1),     # pages of 512 (the codec's largest): tensor-memory pass
+    (512, 16, 1536, 1, 4, 8, 2),     # pages of 512, chunks of 16 (32 chunks a page)
 ])
 def test_row_counts_and_pairs(lynx_lib, oracle_mod, cuda_dev, P, C, L, H_kv, H_q, T, Ta):
     pairs = [(0, h) for h in range(H_kv)]

@@ -60,7 +60,9 @@ def test_paged_encode_decode_match_oracle(lynx_lib, oracle_mod, cuda_dev, B, L, 
     ("anchor", 1, 8, False, 128, 32), ("full", 8, 8, True, 128, 32), ("full", 2, 4, False, 128, 32),
     # 16 rows per KV head over pages of 64 and chunks of 16 (two chunks per
     # 32-token producer range on the tensor-memory path)
-    ("full", 4, 8, False, 64, 16)])
+    ("full", 4, 8, False, 64, 16),
+    # pages of 512 (four per sequence) behind the table, draft and verification
+    ("anchor", 1, 8, False, 512, 64), ("full", 8, 8, False, 512, 32)])
 def test_paged_attention_matches_oracle(lynx_lib, oracle_mod, cuda_dev, mode_name, T, H_q,
                                         tail, P, C):
     from split_stream_kv_gb300 import synth
