@@ -39,7 +39,7 @@
  *   - Limits: D == 128; page in {64, 128, 256, 512} for the codec (encode,
  *     both decoders, the k-bit Anchor decode; the page sizes of the pages'
  *     ablation grid, [Review], "Concrete Improvement Suggestions", item 4)
- *     and for attention; page <= 256 for the Appendix A.1 variant; C in
+ *     and for attention and the Appendix A.1 variant; C in
  *     {16, 32, 64, 128}, C <= page; L % page == 0; B * L < 2^31; alpha
  *     finite and > 0; every pointer 16-byte aligned.
  */

@@ -310,7 +310,7 @@ int lynx_decode_anchor_bits(const void* anchor_k, const float* meta, int64_t B, 
 
 int lynx_a1_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int page, float alpha,
                    void* anchor, void* residual, float* meta, void* stream) {
-  int rc = check_codec_shape(B, L, H_kv, D, page, 16, 256);
+  int rc = check_codec_shape(B, L, H_kv, D, page, 16, 512);
   if (rc) return rc;
   if ((rc = check_alpha(alpha))) return rc;
   if (B * L == 0) return LYNX_OK;
@@ -324,7 +324,7 @@ int lynx_a1_encode(const void* kv, int64_t B, int64_t L, int H_kv, int D, int pa
 int lynx_a1_decode(const void* anchor, const void* residual, const float* meta, int64_t B,
                    int64_t L, int H_kv, int D, int page, float alpha, void* out, int out_dtype,
                    void* stream) {
-  int rc = check_codec_shape(B, L, H_kv, D, page, 16, 256);
+  int rc = check_codec_shape(B, L, H_kv, D, page, 16, 512);
   if (rc) return rc;
   if ((rc = check_alpha(alpha))) return rc;
   if (out_dtype != LYNX_OUT_BF16 && out_dtype != LYNX_OUT_FP32)

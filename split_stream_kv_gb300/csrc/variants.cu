@@ -475,12 +475,12 @@ __device__ __forceinline__ int a1_round(float a, float alpha, float c16, const f
 }
 
 template <bool FAST>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(512)
 a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, const int64_t L,
                  const int P, uint32_t* __restrict__ anchor, uint32_t* __restrict__ residual,
                  float* __restrict__ meta, const __grid_constant__ CompanderTable tab) {
   __shared__ float thr[128];
-  __shared__ uint4 pmx[16][16];                  // [chunk][group]: bf16x2 maxima of |x|
+  __shared__ uint4 pmx[32][16];                  // [chunk][group]: bf16x2 maxima of |x|
   const int tid = threadIdx.x, G = tid & 15, k = tid >> 4;
   const int64_t blk = blockIdx.x;
   const int64_t h = blk % H, p = (blk / H) % NB, b = blk / (H * NB);
@@ -594,8 +594,8 @@ a1_encode_kernel(const uint8_t* __restrict__ kv, const int64_t NB, const int H, 
 // Decode of the A.1 variant, persistent, like the 4+4 decoders: a block's
 // Anchor and Residual codes and its metadata rows (m, then m_i per 16-token
 // chunk) arrive in shared memory by bulk asynchronous copies, one stage
-// ahead; thread (slot, G) of 256 decodes a run of page/16 tokens (inside one
-// chunk) of channels 8G..8G+7.  The 8-bit code of a channel, Anchor nibble
+// ahead; thread (slot, G) of 256 decodes a run of page/16 tokens (one chunk
+// or part of one, two chunks at page 512) of channels 8G..8G+7.  The 8-bit code of a channel, Anchor nibble
 // above Residual nibble (Residual 7 in Anchor-only mode), read as an int8 is
 // Q; a lane-replicated table over that byte gives sgn(Q) X(min(|Q|, 127)).
 constexpr int kA1Stages = 2;
@@ -675,8 +675,19 @@ a1_decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__
     const int64_t h = blk % H, rest = blk / H;
     const int64_t p = rest % NB, b = rest / NB;
     const int64_t orow0 = ((b * L + p * P + t0) * H + h) * kD + 8 * G;
+    // a run lies in one chunk up to pages of 256 and spans two at 512: the
+    // chunk factors are reloaded at each 16-token boundary
+    for (int r0 = 0; r0 < run; r0 += kA1Chunk) {
+      if (r0 > 0) {
+        const float* crow = mrow + (1 + (t0 + r0) / kA1Chunk) * kD;
+        const float4 v0 = reinterpret_cast<const float4*>(crow)[0];
+        const float4 v1 = reinterpret_cast<const float4*>(crow)[1];
+        mi2[0] = make_float2(v0.x, v0.y); mi2[1] = make_float2(v0.z, v0.w);
+        mi2[2] = make_float2(v1.x, v1.y); mi2[3] = make_float2(v1.z, v1.w);
+      }
+      const int r1 = run < r0 + kA1Chunk ? run : r0 + kA1Chunk;
 #pragma unroll 4
-    for (int r = 0; r < run; ++r) {
+    for (int r = r0; r < r1; ++r) {
       const uint32_t a = aw[r * 16], rr = FULL ? rw[r * 16] : 0x77777777u;
       const uint32_t E = ((a << 4) & 0xf0f0f0f0u) | (rr & 0x0f0f0f0fu);  // codes of ch 0-3
       const uint32_t O = (a & 0xf0f0f0f0u) | ((rr >> 4) & 0x0f0f0f0fu);  // codes of ch 4-7
@@ -696,6 +707,7 @@ a1_decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__
         stg_stream(ob + oe * 4 + 16, make_uint4(__float_as_uint(y[2].x), __float_as_uint(y[2].y),
                                                 __float_as_uint(y[3].x), __float_as_uint(y[3].y)));
       }
+    }
     }
 
     if (!__syncthreads_and(ok)) {
@@ -801,7 +813,7 @@ static cudaError_t run_a1_decode(const uint8_t* a, const uint8_t* r, const float
   const size_t stage = (size_t)s.page * (kD / 2) * (FULL ? 2 : 1) +
                        (size_t)(1 + s.page / kA1Chunk) * kD * 4;
   const size_t smem = kA1Table + kA1Stages * stage + kA1Stages * 8;
-  constexpr size_t kMaxSmem = kA1Table + kA1Stages * (256 * 64 * 2 + 17 * kD * 4) + 64;
+  constexpr size_t kMaxSmem = kA1Table + kA1Stages * (512 * 64 * 2 + 33 * kD * 4) + 64;
   static thread_local int configured_dev = -1;
   static thread_local size_t last_smem = 0;
   static thread_local int per_sm = 1;

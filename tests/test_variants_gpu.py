@@ -185,7 +185,7 @@ def test_vnmse_harness_matches_the_oracle(lynx_lib, oracle_mod, cuda_dev):
     print({n: f"{v:.3g}" for n, v in want.items()})
 
 
-A1_CASES = [(2, 512, 2, 128), (1, 512, 3, 256), (3, 256, 1, 64)]
+A1_CASES = [(2, 512, 2, 128), (1, 512, 3, 256), (3, 256, 1, 64), (2, 1024, 2, 512)]
 
 
 @pytest.mark.parametrize("B,L,H,P", A1_CASES)
