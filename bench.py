@@ -718,12 +718,46 @@ def median_ms(fn, dev, reps, flush=None, warm=3):
     return statistics.median(ts)
 
 
+def graph_us(fns, dev, reps=200):
+    """Device latency of `fns` run in order, captured once as a CUDA graph and
+    replayed `reps` times back to back between two events (so the host's
+    per-call work is out of the measurement): microseconds per replay."""
+    import torch
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for f in fns:
+            f()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for f in fns:
+            f()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    del g
+    return round(us, 2)
+
+
 def measure_configs(dev, reps=20):
     """The codec rows on every other configuration (median of `reps` CUDA-event
     timings after 3 warm-ups, L2 flushed between repetitions), with each row's
     roofline fraction.  The tiny configuration sits in L2 and is bound by
     launch latency, so it reports microseconds (no flush), for its attention
-    rows too."""
+    rows too: "us" for one call through the binding (the host's work
+    included), "graph_us" per replay of the row captured as a CUDA graph, and
+    "step_graph_us" for the whole tiny step (encode, both decodes, draft and
+    verification) as one graph."""
     import torch
     peak, _ = load_peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -743,13 +777,24 @@ def measure_configs(dev, reps=20):
                 rows[r] = {"ms": round(ms, 4), "algorithmic_bytes": int(alg[r]),
                            "achieved_GBps": round(ach, 1), "roofline_frac": round(ach / peak, 4),
                            "bf16_equiv_GBps": round(2 * codec_elems(c) / (ms / 1e3) / 1e9, 1)}
+        step_graph = None
         if name == "tiny":
             ta = attn_setup(TINY_ATTN, dev)
             for r in ATTN_ROWS:
                 ms = median_ms(lambda: attn_row(r, TINY_ATTN, ta), dev, 100)
                 rows[r] = {"us": round(ms * 1e3, 2)}
+            try:
+                fns = {r: (lambda r=r: codec_row(r, c, tc)) for r in CODEC_ROWS}
+                fns.update({r: (lambda r=r: attn_row(r, TINY_ATTN, ta)) for r in ATTN_ROWS})
+                for r, f in fns.items():
+                    rows[r]["graph_us"] = graph_us([f], dev)
+                step_graph = graph_us(list(fns.values()), dev)
+            except Exception as ex:   # a capture the runtime refuses: say so
+                step_graph = f"not captured: {type(ex).__name__}: {ex}"[:200]
             del ta
         out[name] = {"workload": codec_desc(name, c), "rows": rows}
+        if step_graph is not None:
+            out[name]["step_graph_us"] = step_graph
         del tc
         torch.cuda.empty_cache()
     return out
