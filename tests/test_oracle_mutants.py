@@ -135,6 +135,14 @@ MUTANTS = [
      "float rmi = mi > 0.0f ? 1.0f / mi : 0.0f;", "float rmi = 1.0f / (mi + 1e-6f);"),
     ("A.1 page maximum + 1e-6 instead of the zero rule",
      "float rm = m > 0.0f ? 1.0f / m : 0.0f;", "float rm = 1.0f / (m + 1e-6f);"),
+    ("literal Stage 4 biased by 8", "int I_bias = I + 7;", "int I_bias = I + 8;"),
+    ("literal Stage 4 residual sign flipped", "int V_res = V_recon - I;", "int V_res = I - V_recon;"),
+    ("expansion without the division by alpha",
+     "return (float)((pow(1.0 + al, (double)I / 127.0) - 1.0) / al);",
+     "return (float)(pow(1.0 + al, (double)I / 127.0) - 1.0);"),
+    ("compander normalised by log(alpha), not log1p(alpha)",
+     "return 127.0 * log1p(al * (double)a) / log1p(al);",
+     "return 127.0 * log1p(al * (double)a) / log(al);"),
     ("spec integer weights at 2^32", "(uint64_t)(w * 1099511627776.0f)",
      "(uint64_t)(w * 4294967296.0f)"),
 ]
