@@ -255,7 +255,9 @@ __device__ __forceinline__ uint32_t dequant_pair(uint32_t a, uint32_t r, uint32_
   return f2_to_bf2(x.x, x.y);
 }
 
-template <bool FULL, int NT, bool PAIR, bool ONE, bool PAGED>
+// DIRECT: every work unit lies in one CTA's share and there is no draft-token
+// tail, so the CTA writes the unit's output rows itself (no split combine).
+template <bool FULL, int NT, bool PAIR, bool ONE, bool PAGED, bool DIRECT>
 __global__ void __launch_bounds__(Cfg<FULL, PAIR, ONE>::kWarps * 32, 2)
 attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ ExpandTable tab) {
   using CF = Cfg<FULL, PAIR, ONE>;
@@ -888,11 +890,21 @@ attn_kernel(const __grid_constant__ AttnParams a, const __grid_constant__ Expand
       acc += f * sm_o[(u * RP + r) * kD + d];
       den += f * sm_l[u * RP + r];
     }
-    float* ps = part + sgm * part_floats;
-    ps[2 * RP + r * kD + d] = acc;
-    if (d == 0) {
-      ps[r] = M;
-      ps[RP + r] = den;
+    if constexpr (DIRECT) {
+      // the unit's whole softmax: out = o / l (what the combine computes
+      // from a single partial).  One unit per CTA: it is u0, segment 0.
+      const int row = rg0 * RP + r;
+      if (row < a.R) {
+        const int tq = row / a.G, gq = row % a.G;
+        a.out[((int64_t)(b0 * a.T + tq) * a.Hq + h0 * a.G + gq) * kD + d] = acc / den;
+      }
+    } else {
+      float* ps = part + sgm * part_floats;
+      ps[2 * RP + r * kD + d] = acc;
+      if (d == 0) {
+        ps[r] = M;
+        ps[RP + r] = den;
+      }
     }
   }
   // the split combine may launch now; it waits for this grid before reading
@@ -1021,9 +1033,9 @@ size_t attn_workspace_bytes(int batch, int T, int H_q, int H_kv, int64_t L) {
   return (size_t)3 * n * (2 * RP + RP * kD) * sizeof(float);
 }
 
-template <bool FULL, int NT, bool PAIR, bool ONE, bool PAGED>
+template <bool FULL, int NT, bool PAIR, bool ONE, bool PAGED, bool DIRECT>
 static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
-  auto fn = attn_kernel<FULL, NT, PAIR, ONE, PAGED>;
+  auto fn = attn_kernel<FULL, NT, PAIR, ONE, PAGED, DIRECT>;
   constexpr size_t smem = attn_smem_bytes<FULL, PAIR, ONE, NT>();
   constexpr int threads = Cfg<FULL, PAIR, ONE>::kWarps * 32;
   static thread_local int configured_dev = -1;
@@ -1047,6 +1059,7 @@ static cudaError_t run_attn(const AttnParams& prm, const ExpandTable& tab, cudaS
   fn<<<(unsigned)prm.n_cta, threads, smem, stream>>>(prm, tab);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if constexpr (DIRECT) return cudaSuccess;   // the kernel wrote the output rows
   return launch_attn_combine(prm, 8 * NT, stream);
 }
 
@@ -1066,13 +1079,24 @@ cudaError_t launch_attn_combine(const AttnParams& prm, int RP, cudaStream_t stre
   return cudaGetLastError();
 }
 
+template <bool FULL, int NT, bool PAIR, bool DIRECT>
+static cudaError_t run_attn_d(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
+  if (prm.bt)
+    return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true, true, DIRECT>(prm, tab, stream)
+                       : run_attn<FULL, NT, PAIR, false, true, DIRECT>(prm, tab, stream);
+  return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true, false, DIRECT>(prm, tab, stream)
+                     : run_attn<FULL, NT, PAIR, false, false, DIRECT>(prm, tab, stream);
+}
+
+// One CTA per work unit (short sequences) and no draft-token tail: the single
+// shape writes its output rows itself and no combine is launched.
 template <bool FULL, int NT, bool PAIR>
 static cudaError_t run_attn_c(const AttnParams& prm, const ExpandTable& tab, cudaStream_t stream) {
-  if (prm.bt)
-    return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true, true>(prm, tab, stream)
-                       : run_attn<FULL, NT, PAIR, false, true>(prm, tab, stream);
-  return prm.C >= 32 ? run_attn<FULL, NT, PAIR, true, false>(prm, tab, stream)
-                     : run_attn<FULL, NT, PAIR, false, false>(prm, tab, stream);
+  if constexpr (!PAIR) {
+    if (prm.n_cta * prm.NCH == prm.n_chunks && prm.kt == nullptr)
+      return run_attn_d<FULL, NT, PAIR, true>(prm, tab, stream);
+  }
+  return run_attn_d<FULL, NT, PAIR, false>(prm, tab, stream);
 }
 
 cudaError_t launch_attn(const AttnArgs& x, const ExpandTable& tab, cudaStream_t stream) {
