@@ -18,12 +18,13 @@
 // Full: Q8 = Anchor<<4 | Residual, S = sign(Q8), I = S>0 ? Q8 : -Q8-1.
 // Anchor-only: a = signed Anchor, S = sign(a), V = S>0 ? a : -a-1, I = 16V+7.
 //
-// Lookup tables live in shared memory: 256 rows of 256 bytes, one per byte
-// value, whose first 128 bytes are replicated so that every lane reads its
-// own bank (full mode: 32 lanes x float per 8-bit code; anchor mode: 16 lane
-// slots x float2 per anchor byte, both channels of the byte in one load).
-// A lookup address is one byte permute, (byte << 8) | lane offset, and the
-// load adds the fixed shared-window base as its immediate offset.
+// Lookup tables live in shared memory, one row per byte value, replicated so
+// that every lane reads its own bank: full mode 256 rows of 256 bytes (32
+// lanes x float per 8-bit code), anchor mode 256 rows of 128 bytes (16 lane
+// slots x float2 per anchor byte, both channels of the byte in one load).  A lookup
+// address is one byte permute, (byte << 8) | lane offset (halved in anchor
+// mode), and the load adds the fixed shared-window base as its immediate
+// offset.
 #include "common.cuh"
 #include "internal.h"
 
@@ -32,7 +33,9 @@ namespace lynx {
 constexpr int kDecThreads = 256;
 constexpr int kDecUnit = 256;   // most tokens of a decode unit
 constexpr int kDecStages = 2;
-constexpr int kDecLut = 65536;
+constexpr int kDecLut = 65536;   // full mode: 256 rows of 256 bytes
+constexpr int kDecLutAnchor = 32768;   // anchor mode: 256 rows of 128 bytes
+template <bool FULL> constexpr int dec_lut_bytes() { return FULL ? kDecLut : kDecLutAnchor; }
 // Shared-window address of the first byte of dynamic shared memory for a
 // kernel without static shared memory (the block's reserved shared memory
 // comes first); checked by the host before launch and by the kernel.
@@ -105,7 +108,7 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
   const uint32_t code_bytes = (uint32_t)U * (kD / 2);          // one stream of a unit
   const uint32_t meta_bytes = (uint32_t)(2 + 2 * NC) * kD * 4;
   const uint32_t stage_bytes = code_bytes * (FULL ? 2 : 1) + meta_bytes;
-  uint8_t* stages = smem + kDecLut;
+  uint8_t* stages = smem + dec_lut_bytes<FULL>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(stages + kDecStages * stage_bytes);
   const int run = U >> 4;                 // tokens per thread per unit (4, 8 or 16)
   const int t0 = slot * run;
@@ -133,7 +136,7 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
       reinterpret_cast<float*>(smem + row * 256)[l] = row < 128 ? tab.x[row] : -tab.x[255 - row];
     } else if (l < 16) {
       const int a0 = row & 15, a1 = row >> 4;
-      reinterpret_cast<float2*>(smem + row * 256)[l] =
+      reinterpret_cast<float2*>(smem + row * 128)[l] =
           make_float2(a0 < 8 ? tab.x[16 * a0 + 7] : -tab.x[16 * (15 - a0) + 7],
                       a1 < 8 ? tab.x[16 * a1 + 7] : -tab.x[16 * (15 - a1) + 7]);
     }
@@ -143,7 +146,8 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
     fence_barrier_init();
   }
   __syncthreads();
-  const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 8u;
+  // anchor mode: the permute gives (byte << 8) | 16 slot, halved at the load
+  const uint32_t lane_off = FULL ? (uint32_t)lane * 4u : (uint32_t)(lane & 15) * 16u;
 
   auto issue = [&](int64_t un, int stage) {
     const int64_t part = un % parts;
@@ -241,10 +245,10 @@ decode_kernel(const uint8_t* __restrict__ anchor, const uint8_t* __restrict__ re
         const uint32_t a = aw[r * 16];
         float v[8];  // channel order 0..7 of the group
         {
-          const float2 p0 = dec_lut_f2(dec_lut_off<0>(a, lane_off));
-          const float2 p1 = dec_lut_f2(dec_lut_off<1>(a, lane_off));
-          const float2 p2 = dec_lut_f2(dec_lut_off<2>(a, lane_off));
-          const float2 p3 = dec_lut_f2(dec_lut_off<3>(a, lane_off));
+          const float2 p0 = dec_lut_f2(dec_lut_off<0>(a, lane_off) >> 1);
+          const float2 p1 = dec_lut_f2(dec_lut_off<1>(a, lane_off) >> 1);
+          const float2 p2 = dec_lut_f2(dec_lut_off<2>(a, lane_off) >> 1);
+          const float2 p3 = dec_lut_f2(dec_lut_off<3>(a, lane_off) >> 1);
           v[0] = p0.x; v[4] = p0.y; v[1] = p1.x; v[5] = p1.y;
           v[2] = p2.x; v[6] = p2.y; v[3] = p3.x; v[7] = p3.y;
         }
@@ -282,7 +286,7 @@ static cudaError_t run_decode(const void* anchor, const void* residual, const fl
   auto fn = decode_kernel<FULL, BF16OUT>;
   const int U = s.page < kDecUnit ? s.page : kDecUnit;
   const size_t stage = (size_t)U * (kD / 2) * (FULL ? 2 : 1) + (size_t)(2 + 2 * (U / s.C)) * kD * 4;
-  const size_t smem = kDecLut + kDecStages * stage + kDecStages * 8;
+  const size_t smem = dec_lut_bytes<FULL>() + kDecStages * stage + kDecStages * 8;
   constexpr size_t kMaxSmem = kDecLut + kDecStages * (256 * 64 * 2 + 34 * kD * 4) + 64;
   static thread_local int configured_dev = -1;
   int dev = 0;
